@@ -1,0 +1,386 @@
+"""Pins for the fp64 oracle, checked against things other than the oracle itself:
+library routines (PyTorch CPU scaled-dot-product attention in float64), closed
+forms, the pages' teaching example, brute force on tiny inputs, and invariants
+the pages fix (Orthros, Sec. 2.3-2.5 of the close-reading notes: Eqs. (4)-(5),
+dependency isolation, original-position masks, the four modes).
+
+Each pin is chosen so that a plausible slip in the oracle (window off by one,
+a dropped beta, alpha applied to the key, the wrong GQA head, values and keys
+swapped, a missing max-subtraction or normalisation, the copy masked by its
+physical slot, attend-before-append in decode) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from synthetic import bf16_bits, bf16_to_f32, normal_bf16, scale_offset
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_inputs(seed, B, T, Hq, Hkv, d):
+    q = normal_bf16(seed, "q_raw", (B, T, Hq, d))
+    k = normal_bf16(seed, "k", (B, T, Hkv, d))
+    v = normal_bf16(seed, "v", (B, T, Hkv, d))
+    a, b = scale_offset(seed, Hq, d)
+    return q, k, v, a, b
+
+
+def _sdpa(q64, k64, v64, mask, scale):
+    """Library reference: torch SDPA in float64 on the CPU.  q64 [B,T,Hq,d];
+    k64/v64 [B,S,Hkv,d]; GQA by repeat_interleave (head h -> kv head h // group)."""
+    Hq, Hkv = q64.shape[2], k64.shape[2]
+    kq = torch.from_numpy(k64).repeat_interleave(Hq // Hkv, dim=2)
+    vq = torch.from_numpy(v64).repeat_interleave(Hq // Hkv, dim=2)
+    out = F.scaled_dot_product_attention(
+        torch.from_numpy(q64).transpose(1, 2), kq.transpose(1, 2), vq.transpose(1, 2),
+        attn_mask=None if mask is None else torch.from_numpy(mask), scale=scale)
+    return out.transpose(1, 2).numpy()
+
+
+def _w(x):
+    return bf16_to_f32(x).astype(np.float64)
+
+
+def _band(T, w):
+    t = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    return (j <= t) & (j > t - w)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,w", [
+    (1, 1, 1, 1, 8, 1), (1, 37, 2, 1, 16, 5), (2, 130, 4, 2, 32, 128),
+    (1, 300, 8, 2, 64, 128), (2, 200, 4, 4, 16, 64), (1, 257, 6, 3, 8, 300)])
+def test_swa_equals_sdpa_with_band_mask(B, T, Hq, Hkv, d, w):
+    """Eq. (4) with scale-offset == library SDPA over the band mask W_t (GQA expanded)."""
+    q, k, v, a, b = _rand_inputs(100 + T, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    o = oracle.swa(q, k, v, a, b, w, s)
+    q64 = _w(q) * a.astype(np.float64) + b.astype(np.float64)
+    ref = _sdpa(q64, _w(k), _w(v), _band(T, w), s)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def test_swa_window_ge_T_is_full_causal():
+    """With w >= T the sliding window covers all of 1..t: plain causal attention."""
+    B, T, Hq, Hkv, d = 2, 96, 4, 1, 32
+    q, k, v, a, b = _rand_inputs(7, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    o = oracle.swa(q, k, v, np.ones_like(a), np.zeros_like(b), 128, s)
+    kq = torch.from_numpy(_w(k)).repeat_interleave(Hq, dim=2)
+    vq = torch.from_numpy(_w(v)).repeat_interleave(Hq, dim=2)
+    ref = F.scaled_dot_product_attention(torch.from_numpy(_w(q)).transpose(1, 2),
+                                         kq.transpose(1, 2), vq.transpose(1, 2),
+                                         is_causal=True).transpose(1, 2).numpy()
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def test_rows_before_window_fills_equal_causal_rows():
+    """Rows t < w see all of 0..t, so they equal the full-causal rows; later rows differ."""
+    B, T, Hq, Hkv, d, w = 1, 80, 2, 1, 16, 32
+    q, k, v, a, b = _rand_inputs(8, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    o_w = oracle.swa(q, k, v, a, b, w, s)
+    o_full = oracle.swa(q, k, v, a, b, T, s)
+    np.testing.assert_array_equal(o_w[:, :w], o_full[:, :w])
+    assert np.abs(o_w[:, w:] - o_full[:, w:]).max() > 1e-3
+
+
+@pytest.mark.parametrize("T,w,d", [(300, 128, 64), (50, 7, 8), (5, 128, 4)])
+def test_zero_keys_reveal_the_exact_window(T, w, d):
+    """K == 0 makes every weight equal: o_t is the mean of v over W_t.  With
+    v_j = (j mod 128, j div 128, 1, 0, ...) (exact in bf16), 128*o[1] + o[0] is the
+    mean of the window's indices, (lo + t) / 2 with lo = max(0, t-w+1), and o[2]
+    is exactly 1."""
+    B, Hq, Hkv = 1, 2, 1
+    q = normal_bf16(3, "q_raw", (B, T, Hq, d))
+    k = np.zeros((B, T, Hkv, d), np.uint16)
+    vf = np.zeros((B, T, Hkv, d), np.float32)
+    vf[0, :, 0, 0] = np.arange(T) % 128
+    vf[0, :, 0, 1] = np.arange(T) // 128
+    vf[0, :, 0, 2] = 1
+    v = bf16_bits(vf)
+    assert np.array_equal(bf16_to_f32(v), vf)
+    a, b = scale_offset(3, Hq, d)
+    o = oracle.swa(q, k, v, a, b, w, 0.5)
+    t = np.arange(T)
+    lo = np.maximum(0, t - w + 1)
+    for h in range(Hq):
+        np.testing.assert_allclose(128 * o[0, :, h, 1] + o[0, :, h, 0], (lo + t) / 2,
+                                   rtol=0, atol=1e-11)
+        np.testing.assert_allclose(o[0, :, h, 2], 1.0, rtol=0, atol=1e-14)
+        np.testing.assert_array_equal(o[0, :, h, 3:], 0.0)
+
+
+def test_window_one_is_identity_on_values():
+    """w = 1: each position attends only to itself, o_t = v_t exactly."""
+    B, T, Hq, Hkv, d = 2, 40, 4, 2, 16
+    q, k, v, a, b = _rand_inputs(9, B, T, Hq, Hkv, d)
+    o = oracle.swa(q, k, v, a, b, 1, 0.25)
+    vq = np.repeat(_w(v), Hq // Hkv, axis=2)
+    np.testing.assert_array_equal(o, vq)
+
+
+def test_constant_values_give_that_constant():
+    """Weights sum to one: if every v_j = c then o_t = c, for any keys and queries."""
+    B, T, Hq, Hkv, d = 1, 70, 2, 1, 8
+    q, k, _, a, b = _rand_inputs(10, B, T, Hq, Hkv, d)
+    c = np.linspace(-2, 2, d).astype(np.float32)
+    v = bf16_bits(np.broadcast_to(c, (B, T, Hkv, d)))
+    o = oracle.swa(q, k, v, a, b, 16, 0.3)
+    np.testing.assert_allclose(o, np.broadcast_to(_w(v)[0, 0, 0], o.shape), rtol=0, atol=1e-14)
+
+
+def test_scale_offset_alpha_zero_leaves_only_beta():
+    """alpha = 0: q = beta for every row, whatever Q_raw holds.  Pins that beta is
+    added to the query (not the key) and that alpha multiplies Q_raw."""
+    B, T, Hq, Hkv, d = 1, 60, 2, 1, 16
+    q, k, v, _, b = _rand_inputs(11, B, T, Hq, Hkv, d)
+    s = 0.25
+    o1 = oracle.swa(q, k, v, np.zeros((Hq, d), np.float32), b, 8, s)
+    q2 = normal_bf16(12, "q_raw", (B, T, Hq, d))
+    o2 = oracle.swa(q2, k, v, np.zeros((Hq, d), np.float32), b, 8, s)
+    np.testing.assert_array_equal(o1, o2)
+    qb = np.broadcast_to(b.astype(np.float64), (B, T, Hq, d)).copy()
+    ref = _sdpa(qb, _w(k), _w(v), _band(T, 8), s)
+    np.testing.assert_allclose(o1, ref, rtol=0, atol=1e-12)
+
+
+def test_scale_offset_is_per_head():
+    """alpha/beta are [Hq, d]: head h uses row h (checked with rows that differ)."""
+    B, T, Hq, Hkv, d = 1, 33, 4, 2, 8
+    q, k, v, a, b = _rand_inputs(13, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    o = oracle.swa(q, k, v, a, b, 10, s)
+    for h in range(Hq):
+        q64 = _w(q[:, :, h:h + 1]) * a[h].astype(np.float64) + b[h].astype(np.float64)
+        ref = _sdpa(q64, _w(k[:, :, h // 2:h // 2 + 1]), _w(v[:, :, h // 2:h // 2 + 1]),
+                    _band(T, 10), s)
+        np.testing.assert_allclose(o[:, :, h:h + 1], ref, rtol=0, atol=1e-12)
+
+
+def test_brute_force_triple_loop_tiny():
+    """Brute force in pure Python on a tiny case (explicit sums, no vector ops)."""
+    B, T, Hq, Hkv, d, w = 1, 9, 2, 1, 3, 4
+    q, k, v, a, b = _rand_inputs(14, B, T, Hq, Hkv, d)
+    s = 0.7
+    o = oracle.swa(q, k, v, a, b, w, s)
+    qf, kf, vf = _w(q), _w(k), _w(v)
+    for t in range(T):
+        for h in range(Hq):
+            qq = [qf[0, t, h, e] * float(a[h, e]) + float(b[h, e]) for e in range(d)]
+            js = list(range(max(0, t - w + 1), t + 1))
+            lg = [s * sum(qq[e] * kf[0, j, 0, e] for e in range(d)) for j in js]
+            m = max(lg)
+            ws = [math.exp(x - m) for x in lg]
+            z = sum(ws)
+            for e in range(d):
+                ref = sum(ws[i] * vf[0, j, 0, e] for i, j in enumerate(js)) / z
+                assert abs(o[0, t, h, e] - ref) < 1e-13
+
+
+def test_large_logits_do_not_overflow():
+    """Softmax is shift-invariant; logits near 700 must not overflow (max subtraction)."""
+    B, T, Hq, Hkv, d = 1, 20, 1, 1, 4
+    qf = np.zeros((B, T, Hq, d), np.float32)
+    qf[..., 0] = 32.0
+    kf = np.zeros((B, T, Hkv, d), np.float32)
+    kf[0, :, 0, 0] = 32.0 + np.arange(T) % 3
+    v = normal_bf16(15, "v", (B, T, Hkv, d))
+    o = oracle.swa(bf16_bits(qf), bf16_bits(kf), v, np.ones((Hq, d), np.float32),
+                   np.zeros((Hq, d), np.float32), 8, 0.7)
+    assert np.isfinite(o).all()
+    ref = _sdpa(_w(bf16_bits(qf)), _w(bf16_bits(kf)), _w(v), _band(T, 8), 0.7)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-10)
+
+
+# ----------------------------------------------------------------- copies (Eq. 5)
+
+def test_copy_equals_causal_row_when_streams_coincide():
+    """With alpha'=alpha, beta'=beta and x'=x, the copy at t equals row t of
+    standard causal attention (Eq. 5 reads all j <= t)."""
+    B, T, Hq, Hkv, d = 2, 150, 4, 2, 32
+    q, k, v, a, b = _rand_inputs(20, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    pos = np.array([[149, 0, 77, 128], [5, 149, 149, 60]], np.int32)
+    qc = np.stack([q[bb, pos[bb]] for bb in range(B)])
+    oc = oracle.xattn(qc, pos, k, v, a, b, s)
+    q64 = _w(q) * a.astype(np.float64) + b.astype(np.float64)
+    full = _sdpa(q64, _w(k), _w(v), _band(T, T + 1), s)
+    for bb in range(B):
+        np.testing.assert_allclose(oc[bb], full[bb, pos[bb]], rtol=0, atol=1e-12)
+    # and it is the w >= T base stream at that row
+    o_full = oracle.swa(q, k, v, a, b, T, s)
+    for bb in range(B):
+        np.testing.assert_allclose(oc[bb], o_full[bb, pos[bb]], rtol=0, atol=1e-13)
+
+
+def test_copy_mask_uses_original_position_not_slot():
+    """Algorithm 2 appends copies at the tensor tail; the mask must follow the
+    original position.  Permuting the physical order (with pos) permutes the
+    outputs and changes nothing else, bit for bit."""
+    B, T, Hq, Hkv, d, n = 2, 120, 4, 1, 16, 11
+    _, k, v, _, _ = _rand_inputs(21, B, T, Hq, Hkv, d)
+    qc = normal_bf16(21, "qc_raw", (B, n, Hq, d))
+    ac, bc = scale_offset(21, Hq, d, prefix="_c")
+    g = np.random.default_rng(5)
+    pos = np.stack([g.choice(T, n, replace=False) for _ in range(B)]).astype(np.int32)
+    oc = oracle.xattn(qc, pos, k, v, ac, bc, 0.25)
+    perm = g.permutation(n)
+    oc_p = oracle.xattn(qc[:, perm], pos[:, perm], k, v, ac, bc, 0.25)
+    np.testing.assert_array_equal(oc_p, oc[:, perm])
+    # a copy whose query is placed in slot 0 but whose position is 50 reads keys 0..50
+    kz = np.zeros_like(k)
+    vf = np.zeros((B, T, Hkv, d), np.float32)
+    vf[:, :, 0, 0] = np.arange(T)
+    one = oracle.xattn(qc[:, :1], np.array([[50], [3]], np.int32), kz, bf16_bits(vf), ac, bc, 0.25)
+    np.testing.assert_allclose(one[0, 0, :, 0], 25.0, atol=1e-12)
+    np.testing.assert_allclose(one[1, 0, :, 0], 1.5, atol=1e-12)
+
+
+def test_copies_allow_duplicates_and_position_zero():
+    B, T, Hq, Hkv, d = 1, 64, 2, 1, 8
+    _, k, v, _, _ = _rand_inputs(22, B, T, Hq, Hkv, d)
+    qc = normal_bf16(22, "qc_raw", (B, 3, Hq, d))
+    qc[:, 1] = qc[:, 0]
+    ac, bc = scale_offset(22, Hq, d, prefix="_c")
+    oc = oracle.xattn(qc, np.array([[9, 9, 0]], np.int32), k, v, ac, bc, 0.3)
+    np.testing.assert_array_equal(oc[:, 0], oc[:, 1])
+    np.testing.assert_array_equal(oc[0, 2], np.repeat(_w(v)[0, 0], Hq, axis=0))
+
+
+def test_copy_rejects_out_of_range_positions():
+    B, T, Hq, Hkv, d = 1, 16, 2, 1, 8
+    _, k, v, _, _ = _rand_inputs(23, B, T, Hq, Hkv, d)
+    qc = normal_bf16(23, "qc_raw", (B, 1, Hq, d))
+    ac, bc = scale_offset(23, Hq, d, prefix="_c")
+    for bad in (-1, T):
+        with pytest.raises(ValueError):
+            oracle.xattn(qc, np.array([[bad]], np.int32), k, v, ac, bc, 0.3)
+
+
+# ----------------------------------------------------------------- decode (Sec. 3.2)
+
+def _decode_run(T0, steps, B=2, Hq=4, Hkv=2, d=16, w=8, seed=30):
+    L = T0 + steps
+    T = L
+    q, k, v, a, b = _rand_inputs(seed, B, T, Hq, Hkv, d)
+    qc = normal_bf16(seed, "qc_raw", (B, T, Hq, d))
+    ac, bc = scale_offset(seed, Hq, d, prefix="_c")
+    kc = np.full((B, L, Hkv, d), 0x7FC0, np.uint16)
+    vc = np.full((B, L, Hkv, d), 0x7FC0, np.uint16)
+    kc[:, :T0], vc[:, :T0] = k[:, :T0], v[:, :T0]
+    cl = np.full((B,), T0, np.int32)
+    outs = []
+    for i in range(steps):
+        p = T0 + i
+        o, oc = oracle.decode_step(q[:, p], qc[:, p], k[:, p], v[:, p], kc, vc, cl,
+                                   a, b, ac, bc, w, 1 / math.sqrt(d))
+        outs.append((o, oc))
+    return (q, k, v, a, b, qc, ac, bc), kc, vc, cl, outs
+
+
+def test_decode_equals_prefill_at_appended_positions():
+    """Decoding token by token gives the prefill result at each appended position,
+    for the base output (Eq. 4) and for the copy (Eq. 5) (the [A,B,C] -> D, D' example)."""
+    T0, steps, w, d = 20, 12, 8, 16
+    (q, k, v, a, b, qc, ac, bc), kc, vc, cl, outs = _decode_run(T0, steps, w=w, d=d)
+    s = 1 / math.sqrt(d)
+    o_pre = oracle.swa(q, k, v, a, b, w, s)
+    B = q.shape[0]
+    pos = np.tile(np.arange(T0, T0 + steps, dtype=np.int32), (B, 1))
+    oc_pre = oracle.xattn(np.stack([qc[bb, pos[bb]] for bb in range(B)]), pos, k, v, ac, bc, s)
+    for i, (o, oc) in enumerate(outs):
+        np.testing.assert_allclose(o, o_pre[:, T0 + i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(oc, oc_pre[:, i], rtol=0, atol=1e-13)
+    # cache after n steps = initial cache + appended rows, bit for bit
+    np.testing.assert_array_equal(kc, k)
+    np.testing.assert_array_equal(vc, v)
+    np.testing.assert_array_equal(cl, T0 + steps)
+
+
+def test_decode_copy_never_writes_cache_and_is_isolated():
+    """Perturbing the copy's query or alpha'/beta' leaves o, the cache and cache_len
+    bit-identical (output copies never write K/V, Sec. 2.4)."""
+    B, Hq, Hkv, d, L, T0 = 1, 4, 1, 16, 40, 30
+    k = normal_bf16(31, "k", (B, L, Hkv, d))
+    v = normal_bf16(31, "v", (B, L, Hkv, d))
+    a, b = scale_offset(31, Hq, d)
+    ac, bc = scale_offset(31, Hq, d, prefix="_c")
+    qn = normal_bf16(31, "q_new", (B, Hq, d))
+    kn = normal_bf16(31, "k_new", (B, Hkv, d))
+    vn = normal_bf16(31, "v_new", (B, Hkv, d))
+    res = []
+    for qc_seed, acs in ((1, 1.0), (2, 3.0)):
+        kc, vc = k.copy(), v.copy()
+        kc[:, T0:] = 0x7FC0
+        vc[:, T0:] = 0x7FC0
+        cl = np.full((B,), T0, np.int32)
+        qcn = normal_bf16(qc_seed, "qc_new", (B, Hq, d))
+        o, oc = oracle.decode_step(qn, qcn, kn, vn, kc, vc, cl, a, b, ac * acs, bc * acs, 16, 0.25)
+        res.append((o, oc, kc, vc, cl))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    for i in (2, 3, 4):
+        np.testing.assert_array_equal(res[0][i], res[1][i])
+    assert np.abs(res[0][1] - res[1][1]).max() > 1e-3
+
+
+def test_decode_reads_only_rows_below_cache_len():
+    """Unused cache rows hold bf16 NaN; a correct step never touches them."""
+    (_, _, _, _, _, _, _, _), kc, vc, cl, outs = _decode_run(10, 3)
+    for o, oc in outs:
+        assert np.isfinite(o).all() and np.isfinite(oc).all()
+
+
+# ----------------------------------------------------------------- the pages' example
+
+def _frac(rows):
+    return np.array([n / dd for n, dd in rows], np.float64)
+
+
+def test_golden_abc_teaching_example():
+    """Sec. 2.4: prompt [A,B,C]; C' reads K_A, K_B, K_C; then D, D' in decode."""
+    g = json.load(open(os.path.join(GOLDEN, "abc_teaching_example.json")))
+    d, w = g["d"], g["window"]
+    T = 3
+    vals = np.array(g["prompt_values"], np.float32).reshape(1, T, 1, d)
+    k = np.zeros((1, T, 1, d), np.uint16)
+    v = bf16_bits(vals)
+    q = normal_bf16(40, "q_raw", (1, T, 1, d))
+    a, b = scale_offset(40, 1, d)
+    ac, bc = scale_offset(40, 1, d, prefix="_c")
+    s = 1 / math.sqrt(d)
+    o = oracle.swa(q, k, v, a, b, w, s)
+    ex = g["expected"]
+    for t, name in enumerate(("base_A", "base_B", "base_C")):
+        np.testing.assert_allclose(o[0, t, 0], _frac(ex[name]), rtol=0, atol=1e-15)
+    qc = normal_bf16(40, "qc_raw", (1, 1, 1, d))
+    oc = oracle.xattn(qc, np.array([[2]], np.int32), k, v, ac, bc, s)
+    np.testing.assert_allclose(oc[0, 0, 0], _frac(ex["copy_C"]), rtol=0, atol=1e-15)
+    # decode D: append, then D reads its window {C, D}, D' reads {A, B, C, D}
+    L = 4
+    kc = np.zeros((1, L, 1, d), np.uint16)
+    vc = np.full((1, L, 1, d), 0x7FC0, np.uint16)
+    vc[:, :T] = v
+    cl = np.array([T], np.int32)
+    vD = bf16_bits(np.array(g["decode_value"], np.float32).reshape(1, 1, d))
+    o_d, oc_d = oracle.decode_step(q[:, 0], qc[:, 0], np.zeros((1, 1, d), np.uint16), vD,
+                                   kc, vc, cl, a, b, ac, bc, w, s)
+    np.testing.assert_allclose(o_d[0, 0], _frac(ex["decode_base_D"]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oc_d[0, 0], _frac(ex["decode_copy_D"]), rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(vc[0, 3], vD[0])
+    assert cl[0] == 4
+    # weighted variant: logits 0, 1, 2 exactly
+    kf = np.zeros((1, T, 1, d), np.float32)
+    kf[0, :, 0, 0] = [0, 1, 2]
+    qcw = bf16_bits(np.array([1, 0, 0, 0], np.float32).reshape(1, 1, 1, d))
+    oc_w = oracle.xattn(qcw, np.array([[2]], np.int32), bf16_bits(kf), v,
+                        np.array([[2, 1, 1, 1]], np.float32), np.zeros((1, d), np.float32), s)
+    e = np.exp(np.array(g["weighted"]["copy_logits"], np.float64))
+    np.testing.assert_allclose(oc_w[0, 0, 0, :3], e / e.sum(), rtol=0, atol=1e-15)
