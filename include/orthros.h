@@ -1,0 +1,169 @@
+/*
+ * orthros.h -- C ABI of the Orthros per-layer attention operator on one GB300
+ * (sm_103a).
+ *
+ * The operator (Orthros: Phase-Aware Heterogeneous Attention, arXiv 2610.13735;
+ * close-reading notes Sec. 2.1-2.5 with Fig. 1, Eqs. (4)-(5), Algorithms 1-2):
+ *
+ *   base stream   q_t  = Q_raw[t]  * alpha  + beta        (scale-offset, Sec. 3.1)
+ *                 o_t  = softmax_{j in W_t}(scale * q_t . k_j) v_j,
+ *                 W_t  = {max(0, t-w+1) .. t}              (Eq. 4, 0-based)
+ *   output copy   q'_i = Q'_raw[i] * alpha' + beta'
+ *                 o'_i = softmax_{j <= pos_i}(scale * q'_i . k_j) v_j   (Eq. 5)
+ *
+ * K and V are produced by the base stream only; copies never write K/V
+ * (dependency isolation, Sec. 2.4).  pos_i is the copy's ORIGINAL position,
+ * whatever slot the copy occupies in memory (Algorithm 2 appends copies at the
+ * tensor tail).  Query head h reads KV head h / (Hq / Hkv).
+ *
+ * Conventions shared by every entry point
+ *  - bf16 tensors are passed as pointers to raw bf16 bits (orthros_bf16) in
+ *    device memory, token-major [B, T, H, d] with d contiguous.  Each tensor
+ *    takes a batch stride in ELEMENTS (0 = dense, i.e. T*H*d); within a batch
+ *    the layout is dense.  A non-zero batch stride lets Q_raw and Q'_raw live in
+ *    one [B, T+T_out, Hq, d] buffer (copies appended after the base tokens).
+ *    Base addresses must be 16-byte aligned and batch strides multiples of 8.
+ *  - alpha, beta, alpha', beta' are fp32 [Hq, d] device arrays (one 1 x d
+ *    vector per query head).
+ *  - scale multiplies the logit q . k (pass 1/sqrt(d) for the standard
+ *    scaling); it is applied after the scale-offset.
+ *  - Supported: d in {64, 128}; Hq % Hkv == 0 with Hq / Hkv <= 16; window >= 1.
+ *  - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream; the returned status reports host-side
+ *    argument checks and launch errors only.
+ *  - Ownership: the caller owns every buffer (inputs, outputs, KV cache,
+ *    workspace).  The library keeps no per-call state and never allocates
+ *    device memory.  Outputs must not alias inputs.
+ *  - dev_err (optional, may be NULL) is an int32 in device memory.  A kernel
+ *    that meets bad data it cannot reject on the host (a copy position outside
+ *    [0, T_kv), a full KV cache) ORs an ORTHROS_DEVERR_* bit into it, writes
+ *    zeros for the affected outputs and carries on; nothing traps.
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef ORTHROS_H
+#define ORTHROS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t orthros_bf16; /* raw bf16 bits */
+
+typedef enum {
+    ORTHROS_OK = 0,
+    ORTHROS_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer or stride */
+    ORTHROS_ERR_UNSUPPORTED = 2, /* d, head grouping or device not supported */
+    ORTHROS_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query asks */
+    ORTHROS_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} orthros_status;
+
+/* bits ORed into *dev_err by kernels */
+#define ORTHROS_DEVERR_POSITION 1   /* a copy position outside [0, T_kv) */
+#define ORTHROS_DEVERR_CACHE_FULL 2 /* decode: cache_len[b] + 1 > L_max */
+#define ORTHROS_DEVERR_TIMEOUT 4    /* an internal pipeline wait gave up after ~2 s (a bug) */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *orthros_status_string(orthros_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int orthros_version(void);
+
+/*
+ * Base-stream causal sliding-window attention, Eq. (4), with the base
+ * scale-offset fused into the query load (Sec. 3.1).
+ *
+ *   q_raw  [B, T, Hq, d]  bf16  (batch stride q_bstride elements, 0 = T*Hq*d)
+ *   k, v   [B, T, Hkv, d] bf16  (batch stride kv_bstride, 0 = T*Hkv*d)
+ *   alpha, beta [Hq, d] fp32
+ *   o      [B, T, Hq, d]  bf16  output (batch stride o_bstride, 0 = T*Hq*d)
+ *
+ * Every row t of every sequence attends to keys max(0, t-window+1) .. t of its
+ * own sequence.  window >= T gives plain causal attention.  Accumulation and
+ * softmax are fp32; the scaled query and the softmax weights are rounded to
+ * bf16 as tensor-core operands; o is rounded to bf16 (nearest even).
+ */
+orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                               const orthros_bf16 *v, const float *alpha, const float *beta,
+                               orthros_bf16 *o, int B, int T, int Hq, int Hkv, int d,
+                               int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                               int64_t o_bstride, int32_t *dev_err, void *stream);
+
+/*
+ * Bytes of device workspace orthros_xattn_fwd needs for these sizes
+ * (split-KV partial results).  Returns 0 for invalid sizes.
+ */
+size_t orthros_xattn_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d);
+
+/*
+ * Output-copy full causal cross-attention, Eq. (5), with the copy
+ * scale-offset fused into the query load.
+ *
+ *   qc_raw [B, T_out, Hq, d] bf16 (batch stride qc_bstride, 0 = T_out*Hq*d)
+ *   pos    [B, T_out] int32 device, the copies' ORIGINAL positions, any order,
+ *          duplicates allowed, each in [0, T_kv)
+ *   k, v   [B, T_kv, Hkv, d] bf16 base-stream K/V (batch stride kv_bstride)
+ *   alpha_c, beta_c [Hq, d] fp32
+ *   oc     [B, T_out, Hq, d] bf16 output (batch stride oc_bstride)
+ *   workspace: device buffer of at least orthros_xattn_workspace_size(...)
+ *          bytes, 256-byte aligned, contents need not be initialised.
+ *
+ * Split-KV: the key range of each KV head is cut into chunks streamed by
+ * separate CTAs (query heads of one KV head share each K/V load); partial
+ * (max, sum, unnormalised output) triples are merged by a log-sum-exp
+ * combine kernel.  Two kernel launches.  A copy whose position is out of
+ * range gets a zero output and sets ORTHROS_DEVERR_POSITION.  T_out == 0 is a
+ * no-op.
+ */
+orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
+                                 const orthros_bf16 *k, const orthros_bf16 *v,
+                                 const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
+                                 int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
+                                 int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride,
+                                 void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                 void *stream);
+
+/*
+ * Bytes of device workspace orthros_decode_step needs.  The workspace must be
+ * zero-filled once before its first use (e.g. cudaMemset); every step leaves
+ * its counters at zero again, so it can be reused step after step (but not by
+ * two steps in flight at once).  Returns 0 for invalid sizes.
+ */
+size_t orthros_decode_workspace_size(int B, int L_max, int Hq, int Hkv, int d);
+
+/*
+ * One decode step (Sec. 3.2, decode mode: T_in = 0, T_out = 1 per step): a new
+ * base token and its output copy at the same original position p = cache_len[b].
+ * In one kernel launch, for every sequence b:
+ *   1. k_new[b], v_new[b] are written to cache row p (KV-cache append);
+ *   2. o[b]  = Eq. (4) for q_new[b]  over cache rows max(0, p-window+1) .. p;
+ *   3. oc[b] = Eq. (5) for qc_new[b] over cache rows 0 .. p (the whole cache,
+ *      including the new token);
+ *   4. cache_len[b] = p + 1.
+ * The copy never writes the cache.  Rows at or beyond the old cache_len are
+ * never read from memory (the new row is taken from k_new / v_new).
+ *
+ *   q_new, qc_new [B, Hq, d] bf16; k_new, v_new [B, Hkv, d] bf16
+ *   k_cache, v_cache [B, L_max, Hkv, d] bf16 (updated in place)
+ *   cache_len [B] int32 device (updated in place); each must be < L_max
+ *   o, oc [B, Hq, d] bf16 outputs
+ *   workspace: orthros_decode_workspace_size(...) bytes, zeroed before first use.
+ * A sequence whose cache is full gets zero outputs, no append, no increment,
+ * and sets ORTHROS_DEVERR_CACHE_FULL.
+ */
+orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16 *qc_new,
+                                   const orthros_bf16 *k_new, const orthros_bf16 *v_new,
+                                   orthros_bf16 *k_cache, orthros_bf16 *v_cache,
+                                   int32_t *cache_len, int L_max, const float *alpha,
+                                   const float *beta, const float *alpha_c, const float *beta_c,
+                                   orthros_bf16 *o, orthros_bf16 *oc, int B, int Hq, int Hkv,
+                                   int d, int window, float scale, void *workspace,
+                                   size_t ws_bytes, int32_t *dev_err, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ORTHROS_H */

@@ -1,0 +1,25 @@
+"""Orthros per-layer attention operator on one GB300 (sm_103a).
+
+A thin binding over the C ABI in ``include/orthros.h`` (``liborthros.so``):
+argument marshalling only -- every step of the operator runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.
+
+* :func:`swa_fwd`      -- base-stream sliding-window attention, Eq. (4)
+* :func:`xattn_fwd`    -- output-copy full causal cross-attention, Eq. (5)
+* :func:`decode_step`  -- one fused decode step with KV-cache append
+
+If the library is missing these functions raise; there is no fallback.
+"""
+from ._binding import (  # noqa: F401
+    DEVERR_CACHE_FULL,
+    DEVERR_POSITION,
+    DEVERR_TIMEOUT,
+    OrthrosError,
+    decode_step,
+    decode_workspace_size,
+    lib,
+    library_path,
+    swa_fwd,
+    xattn_fwd,
+    xattn_workspace_size,
+)

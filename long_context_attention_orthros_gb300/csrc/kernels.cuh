@@ -1,0 +1,64 @@
+// kernels.cuh -- launch parameters and host launchers of the Orthros kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/orthros.h"
+
+namespace orthros {
+
+struct SwaParams {
+    const float *alpha;
+    const float *beta;
+    int32_t *dev_err;
+    int T, Hkv, window;
+    float qscale;          // softmax scale * log2(e), folded into the query
+    int tiles_per_stream;  // ceil(T / TOK), set by the launcher
+    long long total_tiles; // B * Hkv on input; B * Hkv * tiles_per_stream after launch set-up
+    int reuse;             // 1: keep K/V blocks resident across consecutive tiles (set by launcher)
+};
+
+struct XattnParams {
+    const orthros_bf16 *qc;
+    const int32_t *pos;
+    const float *alpha_c;
+    const float *beta_c;
+    float *part_o;     // [n_part][B*Hkv][R][D]
+    float2 *part_ml;   // [n_part][B*Hkv][R]  (max in log2 units, sum)
+    orthros_bf16 *oc;
+    int32_t *dev_err;
+    long long qc_bstride, oc_bstride;
+    int B, T_out, T_kv, Hq, Hkv, G, R, row_tiles, splits, chunk, n_part, direct;
+    float qscale;
+};
+
+struct DecodeParams {
+    const orthros_bf16 *q_new, *qc_new, *k_new, *v_new;
+    orthros_bf16 *k_cache, *v_cache;
+    int32_t *cache_len;
+    const float *alpha, *beta, *alpha_c, *beta_c;
+    orthros_bf16 *o, *oc;
+    float *part_o;    // [B*Hkv][n_part][G][D]
+    float2 *part_ml;  // [B*Hkv][n_part][G]
+    int *cnt_bh;      // [B*Hkv]
+    int *cnt_b;       // [B]
+    int32_t *dev_err;
+    int B, Hq, Hkv, L_max, window, nsplit, n_part;
+    float qscale;
+};
+
+cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                       const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);
+
+size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D);
+cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p, void *workspace,
+                         cudaStream_t stream);
+
+size_t decode_workspace_bytes(int B, int L_max, int Hq, int Hkv, int D);
+cudaError_t launch_decode(int D, const CUtensorMap &k, const CUtensorMap &v, DecodeParams p, void *workspace,
+                          cudaStream_t stream);
+
+}  // namespace orthros

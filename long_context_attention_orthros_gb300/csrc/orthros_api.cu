@@ -1,0 +1,255 @@
+// orthros_api.cu -- the C ABI (include/orthros.h): host-side argument checks,
+// TMA descriptor set-up and kernel dispatch.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace {
+
+using orthros::DecodeParams;
+using orthros::SwaParams;
+using orthros::XattnParams;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 4-D bf16 view {d, H, T, B} of a token-major tensor, 128-byte swizzled boxes of
+// {64, box_h, box_t, 1}.  Out-of-range boxes read zeros.
+bool make_map(CUtensorMap *m, const void *base, int d, int H, long long T, int B, long long bstride_elems,
+              int box_h, int box_t)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                             static_cast<cuuint64_t>(bstride_elems) * 2};
+    cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_h), static_cast<cuuint32_t>(box_t), 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool heads_ok(int Hq, int Hkv)
+{
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return false;
+    const int G = Hq / Hkv;
+    return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+}
+
+// A batch stride: 0 selects the dense value; otherwise at least dense and a multiple of 8.
+bool resolve_bstride(long long &s, long long dense)
+{
+    if (s == 0) {
+        s = dense;
+        return true;
+    }
+    return s >= dense && s % 8 == 0;
+}
+
+const float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+const char *orthros_status_string(orthros_status s)
+{
+    switch (s) {
+    case ORTHROS_OK:
+        return "ok";
+    case ORTHROS_ERR_INVALID_ARG:
+        return "invalid argument";
+    case ORTHROS_ERR_UNSUPPORTED:
+        return "unsupported configuration";
+    case ORTHROS_ERR_WORKSPACE:
+        return "workspace missing or too small";
+    case ORTHROS_ERR_CUDA:
+        return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int orthros_version(void) { return 100; }
+
+orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                               const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
+                               int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                               int64_t o_bstride, int32_t *dev_err, void *stream)
+{
+    if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
+        !aligned16(o) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return ORTHROS_ERR_UNSUPPORTED;
+    long long qs = q_bstride, ks = kv_bstride, os = o_bstride;
+    if (!resolve_bstride(qs, static_cast<long long>(T) * Hq * d) ||
+        !resolve_bstride(ks, static_cast<long long>(T) * Hkv * d) ||
+        !resolve_bstride(os, static_cast<long long>(T) * Hq * d))
+        return ORTHROS_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    const int TOK = 128 / G;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, q_raw, d, Hq, T, B, qs, G, TOK) || !make_map(&mk, k, d, Hkv, T, B, ks, 1, 32) ||
+        !make_map(&mv, v, d, Hkv, T, B, ks, 1, 32) || !make_map(&mo, o, d, Hq, T, B, os, G, TOK))
+        return ORTHROS_ERR_CUDA;
+    const int sms = num_sms();
+    if (sms <= 0)
+        return ORTHROS_ERR_CUDA;
+    SwaParams p{};
+    p.alpha = alpha;
+    p.beta = beta;
+    p.dev_err = dev_err;
+    p.T = T;
+    p.Hkv = Hkv;
+    p.window = window;
+    p.qscale = scale * kLog2e;
+    p.total_tiles = static_cast<long long>(B) * Hkv;
+    const cudaError_t e = orthros::launch_swa(d, G, mq, mk, mv, mo, p, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+size_t orthros_xattn_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T_out < 0 || T_kv < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    if (T_out == 0)
+        return 256;
+    return orthros::xattn_workspace_bytes(B, T_out, T_kv, Hq, Hkv, d);
+}
+
+orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
+                                 const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
+                                 orthros_bf16 *oc, int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
+                                 int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride, void *workspace,
+                                 size_t ws_bytes, int32_t *dev_err, void *stream)
+{
+    if (B < 1 || T_out < 0 || T_kv < 1 || !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return ORTHROS_ERR_UNSUPPORTED;
+    if (T_out == 0)
+        return ORTHROS_OK;
+    if (!aligned16(qc_raw) || !pos || !aligned16(k) || !aligned16(v) || !aligned16(alpha_c) ||
+        !aligned16(beta_c) || !aligned16(oc))
+        return ORTHROS_ERR_INVALID_ARG;
+    long long qs = qc_bstride, ks = kv_bstride, os = oc_bstride;
+    if (!resolve_bstride(qs, static_cast<long long>(T_out) * Hq * d) ||
+        !resolve_bstride(ks, static_cast<long long>(T_kv) * Hkv * d) ||
+        !resolve_bstride(os, static_cast<long long>(T_out) * Hq * d))
+        return ORTHROS_ERR_INVALID_ARG;
+    const size_t need = orthros::xattn_workspace_bytes(B, T_out, T_kv, Hq, Hkv, d);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ORTHROS_ERR_WORKSPACE;
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 64) || !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 64))
+        return ORTHROS_ERR_CUDA;
+    XattnParams p{};
+    p.qc = qc_raw;
+    p.pos = pos;
+    p.alpha_c = alpha_c;
+    p.beta_c = beta_c;
+    p.oc = oc;
+    p.dev_err = dev_err;
+    p.qc_bstride = qs;
+    p.oc_bstride = os;
+    p.B = B;
+    p.T_out = T_out;
+    p.T_kv = T_kv;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.qscale = scale * kLog2e;
+    const cudaError_t e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+size_t orthros_decode_workspace_size(int B, int L_max, int Hq, int Hkv, int d)
+{
+    if (B < 1 || L_max < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    return orthros::decode_workspace_bytes(B, L_max, Hq, Hkv, d);
+}
+
+orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16 *qc_new,
+                                   const orthros_bf16 *k_new, const orthros_bf16 *v_new, orthros_bf16 *k_cache,
+                                   orthros_bf16 *v_cache, int32_t *cache_len, int L_max, const float *alpha,
+                                   const float *beta, const float *alpha_c, const float *beta_c, orthros_bf16 *o,
+                                   orthros_bf16 *oc, int B, int Hq, int Hkv, int d, int window, float scale,
+                                   void *workspace, size_t ws_bytes, int32_t *dev_err, void *stream)
+{
+    if (!aligned16(q_new) || !aligned16(qc_new) || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned16(k_cache) || !aligned16(v_cache) || !cache_len || !aligned16(alpha) || !aligned16(beta) ||
+        !aligned16(alpha_c) || !aligned16(beta_c) || !aligned16(o) || !aligned16(oc) || B < 1 || L_max < 1 ||
+        window < 1 || !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return ORTHROS_ERR_UNSUPPORTED;
+    const size_t need = orthros::decode_workspace_bytes(B, L_max, Hq, Hkv, d);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ORTHROS_ERR_WORKSPACE;
+    CUtensorMap mk, mv;
+    const long long cs = static_cast<long long>(L_max) * Hkv * d;
+    if (!make_map(&mk, k_cache, d, Hkv, L_max, B, cs, 1, 64) || !make_map(&mv, v_cache, d, Hkv, L_max, B, cs, 1, 64))
+        return ORTHROS_ERR_CUDA;
+    DecodeParams p{};
+    p.q_new = q_new;
+    p.qc_new = qc_new;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.cache_len = cache_len;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.alpha_c = alpha_c;
+    p.beta_c = beta_c;
+    p.o = o;
+    p.oc = oc;
+    p.dev_err = dev_err;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.L_max = L_max;
+    p.window = window;
+    p.qscale = scale * kLog2e;
+    const cudaError_t e = orthros::launch_decode(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+}  // extern "C"

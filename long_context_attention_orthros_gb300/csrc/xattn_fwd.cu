@@ -1,0 +1,362 @@
+// xattn_fwd.cu -- output-copy full causal cross-attention, Eq. (5) of
+// "Orthros: Phase-Aware Heterogeneous Attention" (Sec. 2.3 / 2.4 of the
+// close-reading notes), with the copy scale-offset q' = Q'_raw * alpha' + beta'
+// fused into the query load.
+//
+// A copy i at original position pos_i attends over base keys 0 .. pos_i of its
+// own sequence; the mask uses pos_i, never the copy's slot in memory (copies may
+// be appended after the base tokens, Algorithm 2).  Query rows of one KV head are
+// grouped: row r of a (batch, KV head) pair is (copy r / G, head r % G), so each
+// K/V byte staged in shared memory serves every query head that reads it (GQA).
+//
+// Split-KV: grid (split, row tile, batch * KV head).  A CTA streams the keys
+// [split * chunk, min((split + 1) * chunk, kmax + 1)) of its KV head through a
+// 3-stage TMA ring (64-key blocks, 128-byte swizzle) filled by one producer
+// warp; kmax is the largest position among its rows.  Four consumer warps run
+// the online softmax with warp MMAs:
+//   * few rows (T_out * G <= 16): all four warps share the same 16 rows and
+//     take every fourth 16-key chunk of a block (4 partial results per CTA);
+//   * many rows: each warp owns 16 rows and walks every chunk.
+// Each warp writes an unnormalised partial (max, sum, o[d]) per row; a second
+// kernel merges the partials of a row with a warp-shuffle log-sum-exp reduction.
+// When a row has a single partial the first kernel writes the output directly.
+#include "kernels.cuh"
+#include "xattn.cuh"
+
+namespace orthros {
+
+template <int D>
+struct XCfg {
+    static constexpr int KB = 64;
+    static constexpr int SLAB = KB * 128;
+    static constexpr int KV_BYTES = KB * D * 2;
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+    static constexpr int STAGES = 3;
+    static constexpr int CWARPS = 4;
+    static constexpr int THREADS = (CWARPS + 1) * 32;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int MISC_OFF = BAR_OFF + 2 * STAGES * 8;
+    static constexpr int SMEM = MISC_OFF + 64 * 4 + 1024;
+};
+
+template <int D, int WK>
+__global__ void __launch_bounds__(XCfg<D>::THREADS)
+    xattn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const XattnParams p)
+{
+    using C = XCfg<D>;
+    constexpr int RPC = 16 * (C::CWARPS / WK);  // query rows per CTA
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_s + pad;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    int *s_pos = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [RPC], -1 = masked row
+
+    const int split = blockIdx.x, rt = blockIdx.y, bh = blockIdx.z;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+    const int row0 = rt * RPC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x < RPC) {
+        const int r = row0 + threadIdx.x;
+        int ps = -1;
+        if (r < p.R) {
+            ps = p.pos[static_cast<long long>(b) * p.T_out + r / p.G];
+            if (ps < 0 || ps >= p.T_kv) {
+                if (split == 0 && r % p.G == 0)
+                    record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
+                ps = -1;
+            }
+        }
+        s_pos[threadIdx.x] = ps;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    int kmax = -1;
+    for (int i = 0; i < RPC; ++i)
+        kmax = max(kmax, s_pos[i]);
+    const int js = split * p.chunk;
+    const int je = min(js + p.chunk, kmax + 1);
+    const int nblk = je > js ? (je - js + C::KB - 1) / C::KB : 0;
+
+    if (warp == C::CWARPS) {
+        if (lane != 0)
+            return;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        for (int i = 0; i < nblk; ++i) {
+            const int s = i % C::STAGES;
+            if (i >= C::STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / C::STAGES) - 1) & 1))) {
+                record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+                return;
+            }
+            uint8_t *dst = smem + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl) {
+                tma_load_4d(dst + sl * C::SLAB, &kmap, &full[s], sl * 64, g, js + i * C::KB, b);
+                tma_load_4d(dst + C::KV_BYTES + sl * C::SLAB, &vmap, &full[s], sl * 64, g,
+                            js + i * C::KB, b);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int rg = warp / WK, kl = warp % WK;
+    const int gr = lane >> 2, qd = (lane & 3) * 2;
+    const int rA = rg * 16 + gr, rB = rA + 8;
+    // padding rows (beyond R) borrow kmax so they never force the masked path;
+    // their results are never written.  Rows with a bad position keep -1.
+    auto lim_of = [&](int r) { return (row0 + r < p.R) ? s_pos[r] : kmax; };
+    const int limA = lim_of(rA), limB = lim_of(rB);
+    int pmin = 0x7fffffff, pmax = -1;
+    for (int i = 0; i < 16; ++i) {
+        const int l = lim_of(rg * 16 + i);
+        pmin = min(pmin, l);
+        pmax = max(pmax, l);
+    }
+
+    WarpRows16<D> st;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = (r & 1) ? rB : rA;
+            const int grow = row0 + row;
+            const int dcol = kt * 16 + qd + ((r & 2) ? 8 : 0);
+            uint32_t v = 0;
+            if (grow < p.R && s_pos[row] >= 0) {
+                const int h = g * p.G + grow % p.G;
+                const orthros_bf16 *qrow =
+                    p.qc + b * p.qc_bstride + (static_cast<long long>(grow / p.G) * p.Hq + h) * D;
+                v = load_q_pair(qrow, p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale);
+            }
+            st.qa[kt][r] = v;
+        }
+    st.reset();
+
+    bool ok = true;
+    for (int i = 0; i < nblk && ok; ++i) {
+        const int s = i % C::STAGES;
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((i / C::STAGES) & 1))) {
+            ok = false;
+            break;
+        }
+        const uint32_t kbase = sbase + s * C::STAGE_BYTES;
+#pragma unroll
+        for (int c = kl; c < 4; c += WK) {
+            const int j0 = js + i * C::KB + c * 16;
+            if (j0 > pmax)
+                continue;
+            st.step(kbase, kbase + C::KV_BYTES, C::SLAB, c * 16, j0, limA, limB, j0 + 15 <= pmin);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+
+    st.finish_sums();
+    const int BH = p.B * p.Hkv;
+    const int part = split * WK + kl;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int row = half ? rB : rA;
+        const int grow = row0 + row;
+        if (grow >= p.R)
+            continue;
+        const float m = half ? st.mB : st.mA;
+        const float l = half ? st.lB : st.lA;
+        if (p.direct) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int h = g * p.G + grow % p.G;
+            orthros_bf16 *orow =
+                p.oc + b * p.oc_bstride + (static_cast<long long>(grow / p.G) * p.Hq + h) * D;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+                *reinterpret_cast<uint32_t *>(orow + i * 8 + qd) =
+                    pack_bf16x2(st.o[i][half * 2] * inv, st.o[i][half * 2 + 1] * inv);
+        } else {
+            const long long slot = (static_cast<long long>(part) * BH + bh) * p.R + grow;
+            float *po = p.part_o + slot * D;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+                *reinterpret_cast<float2 *>(po + i * 8 + qd) =
+                    make_float2(st.o[i][half * 2], st.o[i][half * 2 + 1]);
+            if ((lane & 3) == 0)
+                p.part_ml[slot] = make_float2(m, l);
+        }
+    }
+}
+
+// One warp per output row: merge the row's partial (max, sum, o) triples.
+template <int D>
+__global__ void __launch_bounds__(256) xattn_combine_kernel(const XattnParams p)
+{
+    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long nrows = static_cast<long long>(p.B) * p.T_out * p.Hq;
+    if (wid >= nrows)
+        return;
+    const int b = static_cast<int>(wid / (static_cast<long long>(p.T_out) * p.Hq));
+    const int rem = static_cast<int>(wid % (static_cast<long long>(p.T_out) * p.Hq));
+    const int i = rem / p.Hq, h = rem % p.Hq;
+    const int g = h / p.G;
+    const int bh = b * p.Hkv + g;
+    const int r = i * p.G + h % p.G;
+    const int BH = p.B * p.Hkv;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    float M = NEG_INF;
+    for (int q = lane; q < p.n_part; q += 32) {
+        const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(q) * BH + bh) * p.R + r]);
+        if (ml.y > 0.f)
+            M = fmaxf(M, ml.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int q = lane; q < p.n_part; q += 32) {
+        const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(q) * BH + bh) * p.R + r]);
+        if (ml.y > 0.f)
+            L += ml.y * fast_exp2(ml.x - M);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        L += __shfl_xor_sync(0xffffffffu, L, off);
+
+    constexpr int E = D / 32;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        acc[e] = 0.f;
+    for (int q = 0; q < p.n_part; ++q) {
+        const long long slot = (static_cast<long long>(q) * BH + bh) * p.R + r;
+        const float2 ml = __ldcg(&p.part_ml[slot]);
+        if (!(ml.y > 0.f))
+            continue;
+        const float w = fast_exp2(ml.x - M);
+        const float *po = p.part_o + slot * D + lane * E;
+        if constexpr (E == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+            acc[2] += w * v.z;
+            acc[3] += w * v.w;
+        } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    orthros_bf16 *orow = p.oc + b * p.oc_bstride + (static_cast<long long>(i) * p.Hq + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t *>(orow + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+}
+
+// ------------------------------------------------------------------ host side
+
+struct XattnPlan {
+    int WK, RPC, row_tiles, splits, chunk, n_part, direct;
+};
+
+// Deterministic split plan (also used by the workspace-size query): aim for about
+// two co-resident CTAs per SM of a 152-SM part in a single wave.
+XattnPlan xattn_plan(int B, int T_out, int T_kv, int Hq, int Hkv)
+{
+    XattnPlan pl{};
+    const int G = Hq / Hkv;
+    const long long R = static_cast<long long>(T_out) * G;
+    pl.WK = R <= 16 ? 4 : 1;
+    pl.RPC = 16 * (4 / pl.WK);
+    pl.row_tiles = static_cast<int>((R + pl.RPC - 1) / pl.RPC);
+    const long long target = 304;
+    const long long base = static_cast<long long>(B) * Hkv * pl.row_tiles;
+    long long splits = (target + base - 1) / base;
+    const long long max_splits = (T_kv + 255) / 256;  // at least 256 keys per split
+    if (splits > max_splits)
+        splits = max_splits;
+    if (splits < 1)
+        splits = 1;
+    long long chunk = (T_kv + splits - 1) / splits;
+    chunk = (chunk + 63) / 64 * 64;
+    splits = (T_kv + chunk - 1) / chunk;
+    pl.splits = static_cast<int>(splits);
+    pl.chunk = static_cast<int>(chunk);
+    pl.n_part = pl.splits * pl.WK;
+    pl.direct = pl.n_part == 1 ? 1 : 0;
+    return pl;
+}
+
+size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D)
+{
+    const XattnPlan pl = xattn_plan(B, T_out, T_kv, Hq, Hkv);
+    if (pl.direct)
+        return 256;
+    const size_t rows = static_cast<size_t>(pl.n_part) * B * Hkv * T_out * (Hq / Hkv);
+    const size_t o_bytes = (rows * D * sizeof(float) + 255) / 256 * 256;
+    return o_bytes + (rows * sizeof(float2) + 255) / 256 * 256;
+}
+
+template <int D, int WK>
+static cudaError_t launch_partial(const CUtensorMap &k, const CUtensorMap &v, const XattnParams &p,
+                                  cudaStream_t stream)
+{
+    auto kern = xattn_partial_kernel<D, WK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<D>::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid(p.splits, p.row_tiles, p.B * p.Hkv);
+    kern<<<grid, XCfg<D>::THREADS, XCfg<D>::SMEM, stream>>>(k, v, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p,
+                         void *workspace, cudaStream_t stream)
+{
+    const XattnPlan pl = xattn_plan(p.B, p.T_out, p.T_kv, p.Hq, p.Hkv);
+    p.G = p.Hq / p.Hkv;
+    p.R = p.T_out * p.G;
+    p.row_tiles = pl.row_tiles;
+    p.splits = pl.splits;
+    p.chunk = pl.chunk;
+    p.n_part = pl.n_part;
+    p.direct = pl.direct;
+    if (!pl.direct) {
+        const size_t rows = static_cast<size_t>(pl.n_part) * p.B * p.Hkv * p.R;
+        const size_t o_bytes = (rows * D * sizeof(float) + 255) / 256 * 256;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
+    }
+    cudaError_t e;
+    if (D == 128)
+        e = pl.WK == 4 ? launch_partial<128, 4>(k, v, p, stream) : launch_partial<128, 1>(k, v, p, stream);
+    else
+        e = pl.WK == 4 ? launch_partial<64, 4>(k, v, p, stream) : launch_partial<64, 1>(k, v, p, stream);
+    if (e != cudaSuccess || pl.direct)
+        return e;
+    const long long warps = static_cast<long long>(p.B) * p.T_out * p.Hq;
+    const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+    if (D == 128)
+        xattn_combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
+    else
+        xattn_combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace orthros

@@ -1,0 +1,104 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+function include/orthros.h declares, and its host-side argument checks and
+workspace-size queries behave as documented (none of these calls touches a GPU).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "orthros.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from long_context_attention_orthros_gb300 import build
+    build.build()
+    import long_context_attention_orthros_gb300 as orth
+    return orth.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(orthros_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_operator_entry_points():
+    names = _declared()
+    for n in ("orthros_swa_fwd", "orthros_xattn_fwd", "orthros_decode_step",
+              "orthros_xattn_workspace_size", "orthros_decode_workspace_size",
+              "orthros_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert L.orthros_status_string(0) == b"ok"
+    assert L.orthros_status_string(3).startswith(b"workspace")
+    assert L.orthros_status_string(99) == b"unknown status"
+    assert L.orthros_version() >= 100
+
+
+def _aligned_dummy():
+    # an aligned host address that is never dereferenced: every call below fails a
+    # host-side check before any pointer is used or any CUDA call is made
+    buf = (ctypes.c_uint8 * 64)()
+    return ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15), buf
+
+
+def test_swa_rejects_bad_arguments_on_the_host(L):
+    p, _keep = _aligned_dummy()
+    args = dict(B=1, T=16, Hq=4, Hkv=2, d=128, w=8)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return L.orthros_swa_fwd(kw.get("q", p), p, p, p, p, p, a["B"], a["T"], a["Hq"], a["Hkv"],
+                                 a["d"], a["w"], ctypes.c_float(0.1), 0, 0, 0, None, None)
+    assert call(q=None) == 1
+    assert call(q=ctypes.c_void_p(p.value + 2)) == 1  # misaligned
+    assert call(B=0) == 1
+    assert call(T=0) == 1
+    assert call(w=0) == 1
+    assert call(d=96) == 2
+    assert call(Hq=6, Hkv=4) == 2
+    assert call(Hq=96, Hkv=3) == 2  # 32 heads per KV head: unsupported grouping
+    assert L.orthros_swa_fwd(p, p, p, p, p, p, 1, 16, 4, 2, 128, 8, ctypes.c_float(0.1), 3, 0, 0,
+                             None, None) == 1  # batch stride below dense
+    assert L.orthros_swa_fwd(p, p, p, p, p, p, 1, 16, 4, 2, 128, 8, ctypes.c_float(float("nan")), 0,
+                             0, 0, None, None) == 1
+
+
+def test_xattn_workspace_size_and_checks(L):
+    p, _keep = _aligned_dummy()
+    assert L.orthros_xattn_workspace_size(1, 1, 0, 4, 2, 128) == 0
+    assert L.orthros_xattn_workspace_size(1, 1, 100, 4, 2, 100) == 0
+    small = L.orthros_xattn_workspace_size(2, 1, 131072, 32, 8, 128)
+    assert small > 0
+    # more copies need more partial-result space
+    assert L.orthros_xattn_workspace_size(4, 2048, 16384, 32, 8, 128) > 0
+    # T_out == 0 is a no-op that never touches memory
+    assert L.orthros_xattn_fwd(None, None, None, None, None, None, None, 1, 0, 10, 4, 2, 128,
+                               ctypes.c_float(0.1), 0, 0, 0, None, 0, None, None) == 0
+    # workspace too small
+    assert L.orthros_xattn_fwd(p, p, p, p, p, p, p, 2, 1, 131072, 32, 8, 128, ctypes.c_float(0.1),
+                               0, 0, 0, p, 16, None, None) == 3
+    assert L.orthros_xattn_fwd(p, p, p, p, p, p, p, 2, 1, 131072, 32, 8, 128, ctypes.c_float(0.1),
+                               0, 0, 0, None, small, None, None) == 3
+
+
+def test_decode_workspace_size_and_checks(L):
+    p, _keep = _aligned_dummy()
+    n = L.orthros_decode_workspace_size(2, 131200, 32, 8, 128)
+    assert n > 0
+    assert L.orthros_decode_workspace_size(2, 0, 32, 8, 128) == 0
+    assert L.orthros_decode_step(p, p, p, p, p, p, p, 131200, p, p, p, p, p, p, 2, 32, 8, 128, 128,
+                                 ctypes.c_float(0.1), p, 8, None, None) == 3
+    assert L.orthros_decode_step(p, p, p, p, p, p, None, 131200, p, p, p, p, p, p, 2, 32, 8, 128,
+                                 128, ctypes.c_float(0.1), p, n, None, None) == 1

@@ -1,0 +1,114 @@
+"""GPU parity of the fused decode step (append + base SWA + full-cache copy query)
+against the fp64 oracle; the KV cache and cache_len must match bit for bit."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_attention_orthros_gb300 as orth
+import oracle
+from synthetic import CONFIGS, DecodeConfig, make_decode, reduced
+from tests.gpu_util import assert_parity, bf, bits, dev, f32, i32, val
+
+pytestmark = pytest.mark.gpu
+
+
+class GpuDecode:
+    def __init__(self, inp):
+        c = inp.cfg
+        self.inp = inp
+        self.kc, self.vc = bf(inp.k_cache), bf(inp.v_cache)
+        self.cl = i32(inp.cache_len)
+        self.a, self.b, self.ac, self.bc = (f32(x) for x in (inp.alpha, inp.beta, inp.alpha_c, inp.beta_c))
+        self.ws = orth._binding.decode_workspace(c.B, c.L_max, c.Hq, c.Hkv, c.d, dev())
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev())
+
+    def step(self, i, qc_override=None):
+        inp, c = self.inp, self.inp.cfg
+        qc = inp.qc_new[i] if qc_override is None else qc_override
+        return orth.decode_step(bf(inp.q_new[i]), bf(qc), bf(inp.k_new[i]), bf(inp.v_new[i]),
+                                self.kc, self.vc, self.cl, self.a, self.b, self.ac, self.bc,
+                                window=c.window, scale=c.scale, workspace=self.ws, dev_err=self.err)
+
+
+def _oracle_steps(inp, steps):
+    c = inp.cfg
+    kc, vc, cl = inp.k_cache.copy(), inp.v_cache.copy(), inp.cache_len.copy()
+    outs = []
+    for i in steps:
+        o, oc = oracle.decode_step(inp.q_new[i], inp.qc_new[i], inp.k_new[i], inp.v_new[i], kc, vc,
+                                   cl, inp.alpha, inp.beta, inp.alpha_c, inp.beta_c, c.window, c.scale)
+        outs.append((o, oc))
+    return outs, kc, vc, cl
+
+
+@pytest.mark.parametrize("B,T0,steps,Hq,Hkv,d,w", [
+    (2, 1000, 6, 32, 8, 128, 128),   # 8B-class heads; crosses a 64-key block boundary
+    (1, 63, 3, 8, 2, 128, 128),      # cache shorter than one block
+    (2, 130, 4, 4, 4, 64, 128),      # G=1, d=64
+    (1, 2000, 3, 16, 1, 128, 7),     # G=16, narrow window
+    (1, 1, 2, 8, 2, 128, 128),       # almost empty cache
+    (1, 0, 2, 8, 2, 128, 128),       # empty cache: the first token attends to itself only
+])
+def test_decode_steps_match_oracle(B, T0, steps, Hq, Hkv, d, w):
+    cfg = DecodeConfig("case", B=B, T0=T0, steps=steps, Hq=Hq, Hkv=Hkv, d=d, window=w)
+    inp = make_decode(cfg, 300 + T0)
+    g = GpuDecode(inp)
+    ref, kc, vc, cl = _oracle_steps(inp, range(steps))
+    for i in range(steps):
+        o, oc = g.step(i)
+        assert_parity(val(o), ref[i][0], f"step {i} base")
+        assert_parity(val(oc), ref[i][1], f"step {i} copy")
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    np.testing.assert_array_equal(bits(g.kc), kc)
+    np.testing.assert_array_equal(bits(g.vc), vc)
+    np.testing.assert_array_equal(g.cl.cpu().numpy(), cl)
+
+
+def test_decode_copy_is_isolated_from_cache_and_base():
+    """Changing the copy's query changes only oc: o, the cache and cache_len are
+    bit-identical (copies never write K/V)."""
+    cfg = DecodeConfig("iso", B=2, T0=700, steps=1, Hq=32, Hkv=8, d=128)
+    inp = make_decode(cfg, 11)
+    res = []
+    for qc in (inp.qc_new[0], inp.qc_new[0] ^ np.uint16(0x0001)):
+        g = GpuDecode(inp)
+        o, oc = g.step(0, qc_override=qc)
+        res.append((bits(o), bits(oc), bits(g.kc), bits(g.vc), g.cl.cpu().numpy()))
+    for i in (0, 2, 3, 4):
+        np.testing.assert_array_equal(res[0][i], res[1][i])
+
+
+def test_decode_equals_prefill_at_appended_position():
+    """Decode of token p after a prefix equals the prefill kernels' result at p."""
+    B, T, Hq, Hkv, d, w = 1, 800, 8, 2, 128, 128
+    cfg = DecodeConfig("dp", B=B, T0=T - 1, steps=1, Hq=Hq, Hkv=Hkv, d=d, window=w)
+    inp = make_decode(cfg, 12)
+    g = GpuDecode(inp)
+    o, oc = g.step(0)
+    k_full = bits(g.kc)[:, :T]
+    v_full = bits(g.vc)[:, :T]
+    q = np.zeros((B, T, Hq, d), np.uint16)
+    q[:, T - 1] = inp.q_new[0]
+    o_pre = orth.swa_fwd(bf(q), bf(k_full), bf(v_full), g.a, g.b, window=w)
+    oc_pre = orth.xattn_fwd(bf(inp.qc_new[0][:, None]), i32(np.full((B, 1), T - 1, np.int32)),
+                            bf(k_full), bf(v_full), g.ac, g.bc)
+    assert np.abs(val(o) - val(o_pre)[:, T - 1]).max() <= 1e-2
+    assert np.abs(val(oc) - val(oc_pre)[:, 0]).max() <= 1e-2
+
+
+def test_decode_full_cache_sets_error_and_leaves_cache():
+    cfg = DecodeConfig("fullc", B=2, T0=10, steps=1, Hq=8, Hkv=2, d=128)
+    inp = make_decode(cfg, 13)
+    inp.cache_len[1] = cfg.L_max  # sequence 1 is full
+    g = GpuDecode(inp)
+    before = bits(g.kc).copy()
+    o, oc = g.step(0)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) & orth.DEVERR_CACHE_FULL
+    assert (val(o)[1] == 0).all() and (val(oc)[1] == 0).all()
+    after = bits(g.kc)
+    np.testing.assert_array_equal(after[1], before[1])
+    assert g.cl.cpu().numpy().tolist() == [11, cfg.L_max]
