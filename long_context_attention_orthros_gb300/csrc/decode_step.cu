@@ -211,13 +211,14 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
             for (int r = 0; r < 4; ++r) {
                 const int row = gr + ((r & 1) ? 8 : 0);
                 const int dcol = kt * 16 + qd + ((r & 2) ? 8 : 0);
-                uint32_t v = 0;
+                uint32_t hi = 0, lo = 0;
                 if (row < G && !cache_full) {
                     const int h = g * G + row;
-                    v = load_q_pair(p.qc_new + (static_cast<long long>(b) * p.Hq + h) * D,
-                                    p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale);
+                    load_q_pair(p.qc_new + (static_cast<long long>(b) * p.Hq + h) * D, p.alpha_c + h * D,
+                                p.beta_c + h * D, dcol, p.qscale, hi, lo);
                 }
-                st.qa[kt][r] = v;
+                st.qa[kt][r] = hi;
+                st.ql[kt][r] = lo;
             }
         st.reset();
         bool ok = true;

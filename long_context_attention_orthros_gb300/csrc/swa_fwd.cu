@@ -25,6 +25,7 @@
 //   blocks are streamed once per tile instead (same code, no reuse).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "xattn.cuh"
 
 namespace orthros {
 
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
                 ok = false;
                 break;
             }
-            uint32_t qa[D / 16][4];
+            uint32_t qa[D / 16][4], ql[D / 16][4];  // scaled query: bf16 high part and residual
             const uint32_t qbase = sbase + C::Q_OFF + qs * C::Q_BYTES;
 #pragma unroll
             for (int kt = 0; kt < D / 16; ++kt) {
@@ -223,8 +224,8 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
                     const float2 al = __ldg(reinterpret_cast<const float2 *>(p.alpha + h * D + dd));
                     const float2 be = __ldg(reinterpret_cast<const float2 *>(p.beta + h * D + dd));
                     const float2 x = unpack_bf16x2(qa[kt][r]);
-                    qa[kt][r] = pack_bf16x2(fmaf(x.x, al.x, be.x) * p.qscale,
-                                            fmaf(x.y, al.y, be.y) * p.qscale);
+                    split_q_pair(fmaf(x.x, al.x, be.x) * p.qscale, fmaf(x.y, al.y, be.y) * p.qscale,
+                                 qa[kt][r], ql[kt][r]);
                 }
             }
 
@@ -264,6 +265,8 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
                         ldsm_x4(a, b0, b1, b2, b3);
                         mma_16816(sacc[0], qa[kt], b0, b1);
                         mma_16816(sacc[1], qa[kt], b2, b3);
+                        mma_16816(sacc[0], ql[kt], b0, b1);
+                        mma_16816(sacc[1], ql[kt], b2, b3);
                     }
                     const bool full_chunk = (j0 >= 0) && (j0 + 15 <= tmin) && (j0 > tmax - p.window);
                     if (!full_chunk) {

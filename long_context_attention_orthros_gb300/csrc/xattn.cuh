@@ -10,7 +10,8 @@ namespace orthros {
 // Per-warp flash state for 16 query rows (fragment rows gr and gr + 8 of this lane).
 template <int D>
 struct WarpRows16 {
-    uint32_t qa[D / 16][4];  // bf16 query fragments (already scale-offset and scaled)
+    uint32_t qa[D / 16][4];  // bf16 query fragments (already scale-offset and scaled): high part
+    uint32_t ql[D / 16][4];  // bf16 residual q - high part: QK runs twice, hi and lo, into one sum
     float o[D / 8][4];       // unnormalised output accumulator
     float mA, mB;            // running max (log2 domain) of rows gr, gr + 8
     float lA, lB;            // running sum (this lane's partial; quad-reduced at the end)
@@ -51,6 +52,8 @@ struct WarpRows16 {
                     b0, b1, b2, b3);
             mma_16816(s[0], qa[kt], b0, b1);
             mma_16816(s[1], qa[kt], b2, b3);
+            mma_16816(s[0], ql[kt], b0, b1);
+            mma_16816(s[1], ql[kt], b2, b3);
         }
         if (!full) {
 #pragma unroll
@@ -118,16 +121,26 @@ struct WarpRows16 {
     }
 };
 
-// Load a query fragment element pair from global bf16 memory and apply the
-// stream's scale-offset: q = (x * alpha + beta) * qscale, rounded to bf16.
-__device__ __forceinline__ uint32_t load_q_pair(const orthros_bf16 *row, const float *alpha,
-                                                const float *beta, int dcol, float qscale)
+// Split a pair of fp32 query values into bf16 high parts and bf16 residuals, so
+// that q . k = hi . k + lo . k keeps ~16 significant bits of the scaled query
+// (one bf16 rounding of q alone is amplified by large keys).
+__device__ __forceinline__ void split_q_pair(float a, float b, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf16x2(a, b);
+    const float2 h = unpack_bf16x2(hi);
+    lo = pack_bf16x2(a - h.x, b - h.y);
+}
+
+// Load a query element pair from global bf16 memory, apply the stream's
+// scale-offset q = (x * alpha + beta) * qscale, and split it into hi / lo bf16.
+__device__ __forceinline__ void load_q_pair(const orthros_bf16 *row, const float *alpha, const float *beta,
+                                            int dcol, float qscale, uint32_t &hi, uint32_t &lo)
 {
     const uint32_t raw = __ldg(reinterpret_cast<const unsigned int *>(row + dcol));
     const float2 x = unpack_bf16x2(raw);
     const float2 al = __ldg(reinterpret_cast<const float2 *>(alpha + dcol));
     const float2 be = __ldg(reinterpret_cast<const float2 *>(beta + dcol));
-    return pack_bf16x2(fmaf(x.x, al.x, be.x) * qscale, fmaf(x.y, al.y, be.y) * qscale);
+    split_q_pair(fmaf(x.x, al.x, be.x) * qscale, fmaf(x.y, al.y, be.y) * qscale, hi, lo);
 }
 
 }  // namespace orthros

@@ -135,14 +135,15 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
             const int row = (r & 1) ? rB : rA;
             const int grow = row0 + row;
             const int dcol = kt * 16 + qd + ((r & 2) ? 8 : 0);
-            uint32_t v = 0;
+            uint32_t hi = 0, lo = 0;
             if (grow < p.R && s_pos[row] >= 0) {
                 const int h = g * p.G + grow % p.G;
                 const orthros_bf16 *qrow =
                     p.qc + b * p.qc_bstride + (static_cast<long long>(grow / p.G) * p.Hq + h) * D;
-                v = load_q_pair(qrow, p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale);
+                load_q_pair(qrow, p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale, hi, lo);
             }
-            st.qa[kt][r] = v;
+            st.qa[kt][r] = hi;
+            st.ql[kt][r] = lo;
         }
     st.reset();
 

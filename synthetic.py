@@ -142,9 +142,12 @@ CONFIGS = {
                              appended=True, positions="shuffled"),
     "prefill_1m": PrefillConfig("prefill_1m", B=1, T=1048576, Hq=32, Hkv=8, d=128,
                                 needle_frac=0.001),
+    # a profiling-sized prefill with the same layer shape (inputs still larger than L2)
+    "prefill_16k": PrefillConfig("prefill_16k", B=1, T=16384, Hq=32, Hkv=8, d=128),
 }
 
-SEEDS = {"tiny_prefill": 1, "prefill_128k": 2, "decode_128k": 3, "sft_16k": 4, "prefill_1m": 5}
+SEEDS = {"tiny_prefill": 1, "prefill_128k": 2, "decode_128k": 3, "sft_16k": 4, "prefill_1m": 5,
+         "prefill_16k": 6}
 
 
 @dataclass
