@@ -33,7 +33,9 @@
  *    argument checks and launch errors only.
  *  - Ownership: the caller owns every buffer (inputs, outputs, KV cache,
  *    workspace).  The library keeps no per-call state and never allocates
- *    device memory.  Outputs must not alias inputs.
+ *    device memory at run time (the one fixed array behind
+ *    orthros_xattn_fwd_noalloc is part of the loaded module).  Outputs must not
+ *    alias inputs.
  *  - dev_err (optional, may be NULL) is an int32 in device memory.  A kernel
  *    that meets bad data it cannot reject on the host (a copy position outside
  *    [0, T_kv), a full KV cache) ORs an ORTHROS_DEVERR_* bit into it, writes
@@ -82,8 +84,9 @@ int orthros_version(void);
  *
  * Every row t of every sequence attends to keys max(0, t-window+1) .. t of its
  * own sequence.  window >= T gives plain causal attention.  Accumulation and
- * softmax are fp32; the scaled query and the softmax weights are rounded to
- * bf16 as tensor-core operands; o is rounded to bf16 (nearest even).
+ * softmax are fp32; the scaled query enters the tensor cores as a bf16 high
+ * part plus a bf16 residual (two products summed into one fp32 logit), the
+ * softmax weights as bf16; o is rounded to bf16 (nearest even).
  */
 orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                const orthros_bf16 *v, const float *alpha, const float *beta,
@@ -124,6 +127,33 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride,
                                  void *workspace, size_t ws_bytes, int32_t *dev_err,
                                  void *stream);
+
+/*
+ * orthros_xattn_fwd without a workspace argument, for callers that cannot
+ * allocate device memory (the paper has no counterpart; this is a deployment
+ * convenience).  Such callers include plug-ins whose host runtime owns all
+ * device memory and forbids allocation on the hot path, and latency-bound loops
+ * that must never call cudaMalloc, which can block on the device and fail once
+ * memory is fragmented or capped.
+ *
+ * Same arguments, layouts and results as orthros_xattn_fwd.  The split-KV
+ * partials live in a fixed file-scope device array of
+ * ORTHROS_XATTN_NOALLOC_MAX_BYTES that every GPU loading this library holds
+ * until the process exits; nothing is allocated per call.  Sizes for which
+ * orthros_xattn_workspace_size(...) exceeds that maximum are rejected with
+ * ORTHROS_ERR_WORKSPACE before anything runs.  All calls share the array, so
+ * calls that overlap on the GPU race on it; order them (one stream, or events).
+ * The array's device address is looked up on the first call made on each
+ * device; make that first call before any stream capture begins.
+ */
+#define ORTHROS_XATTN_NOALLOC_MAX_BYTES (8u << 20)
+orthros_status orthros_xattn_fwd_noalloc(const orthros_bf16 *qc_raw, const int32_t *pos,
+                                         const orthros_bf16 *k, const orthros_bf16 *v,
+                                         const float *alpha_c, const float *beta_c,
+                                         orthros_bf16 *oc, int B, int T_out, int T_kv, int Hq,
+                                         int Hkv, int d, float scale, int64_t qc_bstride,
+                                         int64_t kv_bstride, int64_t oc_bstride, int32_t *dev_err,
+                                         void *stream);
 
 /*
  * Bytes of device workspace orthros_decode_step needs.  The workspace must be
