@@ -276,7 +276,7 @@ def run_gpu(args):
     value = tokens * world / (ms / 1e3)
     swa_bytes = B * T * (2 * Hq + 2 * Hkv) * d * 2  # Q + O (Hq heads) + K + V, once each
     swa_gbs = swa_bytes / (swa_ms / 1e3) / 1e9
-    swa_hash = kernel_hash("swa_fwd.cu", "common.cuh", "kernels.cuh")
+    swa_hash = kernel_hash("swa_fwd.cu", "swa_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh")
     traffic = _profile_traffic(f"swa_fwd_{cfg.name}", swa_hash)
 
     # ---- end to end: pinned host inputs -> device -> kernels -> host outputs

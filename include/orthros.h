@@ -66,6 +66,7 @@ typedef enum {
 #define ORTHROS_DEVERR_POSITION 1   /* a copy position outside [0, T_kv) */
 #define ORTHROS_DEVERR_CACHE_FULL 2 /* decode: cache_len[b] + 1 > L_max */
 #define ORTHROS_DEVERR_TIMEOUT 4    /* an internal pipeline wait gave up after ~2 s (a bug) */
+#define ORTHROS_DEVERR_RANGE 8      /* swa: a key or scaled query outside the fp16 range of QK^T */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *orthros_status_string(orthros_status s);
@@ -84,9 +85,12 @@ int orthros_version(void);
  *
  * Every row t of every sequence attends to keys max(0, t-window+1) .. t of its
  * own sequence.  window >= T gives plain causal attention.  Accumulation and
- * softmax are fp32; the scaled query enters the tensor cores as a bf16 high
- * part plus a bf16 residual (two products summed into one fp32 logit), the
- * softmax weights as bf16; o is rounded to bf16 (nearest even).
+ * softmax are fp32.  q . k is taken with at least 11 significant bits of the
+ * scaled query: in fp16 on the tensor-memory path (q rounded once to fp16, K
+ * converted exactly from bf16; |k| >= 65520 or a scaled |q| >= 65504 sets
+ * ORTHROS_DEVERR_RANGE), or as a bf16 high part plus residual on the path used
+ * for windows too wide for tensor memory.  The softmax weights enter P V as
+ * bf16; o is rounded to bf16 (nearest even).
  */
 orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                const orthros_bf16 *v, const float *alpha, const float *beta,

@@ -13,6 +13,7 @@ If the library is missing these functions raise; there is no fallback.
 from ._binding import (  # noqa: F401
     DEVERR_CACHE_FULL,
     DEVERR_POSITION,
+    DEVERR_RANGE,
     DEVERR_TIMEOUT,
     OrthrosError,
     decode_step,

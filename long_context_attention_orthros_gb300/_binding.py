@@ -19,6 +19,7 @@ library_path = os.path.join(_HERE, "_lib", "liborthros.so")
 DEVERR_POSITION = 1
 DEVERR_CACHE_FULL = 2
 DEVERR_TIMEOUT = 4
+DEVERR_RANGE = 8
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace missing or too small", 4: "CUDA error"}

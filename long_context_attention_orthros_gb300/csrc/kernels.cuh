@@ -52,6 +52,9 @@ struct DecodeParams {
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);
+bool swa_tc_supported(int D, int G, int window);
+cudaError_t launch_swa_tc(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                          const CUtensorMap &o, const SwaParams &p, int num_sms, cudaStream_t stream);
 
 size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D);
 cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p, void *workspace,

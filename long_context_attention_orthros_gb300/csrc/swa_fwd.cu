@@ -420,6 +420,9 @@ cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k,
     const long long band = (static_cast<long long>(p.window) - 1 + TOK + KB - 1) / KB + 1;
     p.reuse = band <= STAGES ? 1 : 0;
     p.total_tiles *= p.tiles_per_stream;
+    // tensor-memory kernel whenever a tile's whole band fits its ring and tensor memory
+    if (swa_tc_supported(D, G, p.window))
+        return launch_swa_tc(D, G, q, k, v, o, p, num_sms, stream);
 #define ORTHROS_SWA_CASE(DD, GG) \
     if (D == DD && G == GG)      \
         return launch_swa_t<DD, GG>(q, k, v, o, p, num_sms, stream);
