@@ -63,6 +63,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` (it resumes
+// as soon as the phase completes), so waiting warps do not take issue slots from
+// working warps on the same scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false after the time limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
@@ -70,9 +86,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
         return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
+            return true;
         if (global_timer_ns() - t0 > kWaitLimitNs)
             return false;
     }

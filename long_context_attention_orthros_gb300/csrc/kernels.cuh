@@ -13,6 +13,9 @@ namespace orthros {
 struct SwaParams {
     const float *alpha;
     const float *beta;
+    orthros_bf16 *o;       // output (the tensor-memory kernel stores rows directly)
+    long long o_bstride;   // elements between batches of o
+    int Hq;
     int32_t *dev_err;
     int T, Hkv, window;
     float qscale;          // softmax scale * log2(e), folded into the query

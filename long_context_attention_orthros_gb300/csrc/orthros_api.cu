@@ -135,6 +135,9 @@ orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     SwaParams p{};
     p.alpha = alpha;
     p.beta = beta;
+    p.o = o;
+    p.o_bstride = os;
+    p.Hq = Hq;
     p.dev_err = dev_err;
     p.T = T;
     p.Hkv = Hkv;

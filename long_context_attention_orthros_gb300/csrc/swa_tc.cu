@@ -8,9 +8,9 @@
 // persistent CTA walks consecutive tiles of a (batch, KV head) stream and keeps
 // each 32-key K/V block resident in a ring for every tile of its band, so K and
 // V leave HBM once.  The band of a tile (at most NB blocks) is one MMA of
-// N = 32 * blocks: the K ring carries NB - 1 mirror slots after its last slot
-// (the producer writes blocks of the first NB - 1 slots twice), so a band that
-// starts anywhere in the ring is contiguous.
+// N = 32 * blocks per k-step: the K ring carries NB - 1 mirror slots after its
+// last slot (the producer writes blocks of the first NB - 1 slots twice), so a
+// band that starts anywhere in the ring is contiguous.
 //
 // Arithmetic:
 //   S = q K^T in fp16 (q rounded once to fp16 after scale-offset, softmax scale
@@ -20,14 +20,17 @@
 //       memory, so there is no online rescaling), stored as bf16 over S;
 //   O = P V in bf16 with fp32 accumulation; o = O / rowsum rounded to bf16.
 //
-// Roles (384 threads, one CTA per SM):
-//   warp 0      TMA producer (raw Q tile, K/V blocks + K mirror copies)
-//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2-3   convert each landed K block to fp16 in place
-//   warps 4-7   softmax (one thread per tile row = tensor-memory lane)
-//   warps 8-11  query preparation and the epilogue (O / l -> bf16 -> TMA store)
-// Tensor memory: q [0, D/2), S/P double buffer [S0, S0 + 2 * 32 * NB), O after.
-// QK of tile n+1 runs while the softmax of tile n does, PV of tile n after it.
+// Roles (512 threads, one CTA per SM):
+//   warp 0        TMA producer: raw Q tiles (double buffered), K/V blocks
+//   warp 1        allocates tensor memory; lane 0 issues every tcgen05.mma
+//   warps 2-3     convert each landed K block to fp16 in place
+//   warps 4-7     softmax + epilogue of even tiles (S buffer 0), one thread per
+//                 row / tensor-memory lane; the epilogue stores O / l as bf16
+//                 straight from registers to global memory
+//   warps 8-11    the same for odd tiles (S buffer 1)
+//   warps 12-15   query preparation in place in shared memory (bf16 -> scaled fp16)
+// S = q K^T reads q and K from shared memory; O = P V reads P from tensor
+// memory.  Tensor memory: S/P buffers [0, 2 * 32 * NB), O at column 384.
 // Every mbarrier wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and
 // all roles drain to the common exit, where tensor memory is released.
 #include <cuda_fp16.h>
@@ -46,7 +49,7 @@ struct TcCfg {
     static constexpr int NB = D == 128 ? 5 : 6;  // most blocks a tile's band may span
     static constexpr int STAGES = 8;
     static constexpr int MIRROR = NB - 1;
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 512;
     static constexpr int SLOT = KB * 128;                   // one slot of one slab array
     static constexpr int K_SLAB = (STAGES + MIRROR) * SLOT;  // one K slab array (with mirrors)
     static constexpr int V_SLAB = STAGES * SLOT;
@@ -54,24 +57,18 @@ struct TcCfg {
     static constexpr int V_OFF = K_OFF + SLABS * K_SLAB;
     static constexpr int Q_OFF = V_OFF + SLABS * V_SLAB;
     static constexpr int Q_SLAB = ROWS * 128;
-    static constexpr int Q_BYTES = SLABS * Q_SLAB;
-    static constexpr int O_OFF = Q_OFF + Q_BYTES;
-    static constexpr int BAR_OFF = O_OFF + Q_BYTES;
-    static constexpr int NBARS = 3 * STAGES + 12;
-    static constexpr int LINV_OFF = BAR_OFF + NBARS * 8;     // float [2][128] row scales
-    static constexpr int HOLD_OFF = LINV_OFF + 2 * ROWS * 4;  // tensor-memory base address
+    static constexpr int Q_BYTES = SLABS * Q_SLAB;  // one of two query buffers
+    static constexpr int BAR_OFF = Q_OFF + 2 * Q_BYTES;
+    static constexpr int NBARS = 3 * STAGES + 11;
+    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;      // tensor-memory base address
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;         // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_Q = 0;
-    static constexpr uint32_t TM_S0 = (D / 2 + 31) / 32 * 32;
     static constexpr uint32_t TM_SSTRIDE = 32 * NB;
-    static constexpr uint32_t TM_O = TM_S0 + 2 * TM_SSTRIDE;
+    static constexpr uint32_t TM_O = 384;
     static constexpr uint32_t TM_COLS = 512;
-    static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
-};
-
-struct TcTile {
-    int b, g, n;
+    static_assert(2 * TM_SSTRIDE <= TM_O && TM_O + D <= TM_COLS, "tensor memory budget");
+    static constexpr int CPR = D / 8;      // 16-byte chunks per query row
+    static constexpr int RPP = 128 / CPR;  // rows one pass of 128 threads covers
 };
 
 __device__ __forceinline__ int tc_kb_lo(int n, int TOK, int window)
@@ -89,10 +86,9 @@ __device__ __forceinline__ int tc_kb_hi(int n, int TOK, int T)
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     swa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                  const SwaParams p)
+                  const __grid_constant__ CUtensorMap vmap, const SwaParams p)
 {
     using C = TcCfg<D>;
     constexpr int TOK = 128 / G;
@@ -102,18 +98,15 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw_s + pad;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *full = bars;                      // [STAGES] block landed (TMA)
-    uint64_t *kconv = bars + C::STAGES;         // [STAGES] K block converted to fp16
-    uint64_t *empty = bars + 2 * C::STAGES;     // [STAGES] block released (MMA commit)
-    uint64_t *qfull = bars + 3 * C::STAGES;     // raw Q tile landed
-    uint64_t *qempty = qfull + 1;               // raw Q tile consumed
-    uint64_t *qt_full = qfull + 2;              // q written to tensor memory
-    uint64_t *s_full = qfull + 3;               // [2] S = q K^T complete
-    uint64_t *p_full = qfull + 5;               // [2] P written over S
-    uint64_t *o_full = qfull + 7;               // O = P V complete
-    uint64_t *o_free = qfull + 8;               // O read out of tensor memory
-    uint64_t *osync = qfull + 9;                // epilogue warps' rendezvous
-    float *linv = reinterpret_cast<float *>(smem + C::LINV_OFF);
+    uint64_t *full = bars;                   // [STAGES] block landed (TMA)
+    uint64_t *kconv = bars + C::STAGES;      // [STAGES] K block converted to fp16
+    uint64_t *empty = bars + 2 * C::STAGES;  // [STAGES] block released (MMA commit)
+    uint64_t *qfull = bars + 3 * C::STAGES;  // [2] raw Q tile landed
+    uint64_t *qt_full = qfull + 2;           // [2] q prepared in place
+    uint64_t *s_full = qfull + 4;            // [2] S = q K^T complete
+    uint64_t *p_full = qfull + 6;            // [2] P written over S
+    uint64_t *o_full = qfull + 8;            // [2] O = P V complete (by the parity of the tile)
+    uint64_t *o_free = qfull + 10;           // O read out of tensor memory
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,16 +116,15 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&kconv[s], 2);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(qfull, 1);
-        mbar_init(qempty, 4);
-        mbar_init(qt_full, 4);
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(&p_full[0], 4);
-        mbar_init(&p_full[1], 4);
-        mbar_init(o_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qt_full[i], 4);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+        }
+        mbar_init(&o_full[0], 1);
+        mbar_init(&o_full[1], 1);
         mbar_init(o_free, 4);
-        mbar_init(osync, 4);
         fence_barrier_init();
     }
     if (warp == 1)
@@ -166,14 +158,17 @@ __global__ void __launch_bounds__(384, 1)
                 const int b = stream / p.Hkv, g = stream % p.Hkv;
                 int next_kb = tc_kb_lo(n0, TOK, p.window);
                 for (int n = n0; n < n1 && ok; ++n, ++it) {
-                    if (it > 0 && !mbar_wait(qempty, static_cast<uint32_t>((it - 1) & 1))) {
+                    const int qb = it & 1;
+                    // query buffer qb is free once QK of tile it-2 has read it
+                    if (it >= 2 && !mbar_wait(&s_full[qb], static_cast<uint32_t>(((it - 2) >> 1) & 1))) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(qfull, C::Q_BYTES);
+                    mbar_arrive_expect_tx(&qfull[qb], C::Q_BYTES);
 #pragma unroll
                     for (int sl = 0; sl < C::SLABS; ++sl)
-                        tma_load_4d(smem + C::Q_OFF + sl * C::Q_SLAB, &qmap, qfull, sl * 64, g * G, n * TOK, b);
+                        tma_load_4d(smem + C::Q_OFF + qb * C::Q_BYTES + sl * C::Q_SLAB, &qmap, &qfull[qb], sl * 64,
+                                    g * G, n * TOK, b);
                     const int hi = tc_kb_hi(n, TOK, p.T);
                     for (; next_kb <= hi && ok; ++next_kb, ++load_idx) {
                         const int s = static_cast<int>(load_idx % C::STAGES);
@@ -209,24 +204,25 @@ __global__ void __launch_bounds__(384, 1)
             int it = 0;
             // the previous tile, whose PV is issued after this tile's QK
             bool have_prev = false;
-            int p_buf = 0, p_nb = 0, p_klo = 0, p_seg = -1;
+            int p_nb = 0, p_klo = 0, p_seg = -1;
             long long p_idx0 = 0;
             int seg = 0;
             constexpr uint32_t IDESC_PV = umma_idesc(128, D, true, true);
             auto issue_pv = [&](int pit, int rel) -> bool {
-                if (!mbar_wait(&p_full[p_buf], static_cast<uint32_t>((pit >> 1) & 1)))
+                const int pbuf = pit & 1;
+                if (!mbar_wait(&p_full[pbuf], static_cast<uint32_t>((pit >> 1) & 1)))
                     return false;
                 if (pit >= 1 && !mbar_wait(o_free, static_cast<uint32_t>((pit - 1) & 1)))
                     return false;
                 tc_fence_after();
-                const uint32_t s_col = tbase + C::TM_S0 + p_buf * C::TM_SSTRIDE;
+                const uint32_t s_col = tbase + pbuf * C::TM_SSTRIDE;
                 for (int j = 0; j < p_nb; ++j) {
                     const uint32_t vslot = sbase + C::V_OFF + static_cast<uint32_t>((p_idx0 + j) % C::STAGES) * C::SLOT;
                     const uint64_t vdesc = umma_desc_sw128(vslot, C::V_SLAB, 1024);
                     umma_ts(tbase + C::TM_O, s_col + 16 * j, vdesc, IDESC_PV, j != 0);
                     umma_ts(tbase + C::TM_O, s_col + 16 * j + 8, vdesc + (2048 >> 4), IDESC_PV, 1);
                 }
-                umma_commit(o_full);
+                umma_commit(&o_full[pbuf]);
                 for (int r = 0; r < rel; ++r)
                     umma_commit(&empty[(p_idx0 + r) % C::STAGES]);
                 return true;
@@ -242,9 +238,9 @@ __global__ void __launch_bounds__(384, 1)
                     const long long idx0 = seg_base + (klo - seg_kb0);
                     const int buf = it & 1;
                     // ---- S[buf] = q K^T for tile `it`
-                    ok = mbar_wait(qt_full, static_cast<uint32_t>(it & 1));
-                    if (ok && it >= 2)
-                        ok = mbar_wait(o_full, static_cast<uint32_t>((it - 2) & 1));  // PV(it-2) read S[buf]
+                    ok = mbar_wait(&qt_full[buf], static_cast<uint32_t>((it >> 1) & 1));
+                    if (ok && it >= 2)  // PV(it-2) has read P from S[buf]
+                        ok = mbar_wait(&o_full[buf], static_cast<uint32_t>(((it - 2) >> 1) & 1));
                     for (int j = 0; j < nb && ok; ++j) {
                         const long long idx = idx0 + j;
                         if (idx > waited) {
@@ -259,13 +255,14 @@ __global__ void __launch_bounds__(384, 1)
                     {
                         const uint32_t slot0 = static_cast<uint32_t>(idx0 % C::STAGES);
                         const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot0 * C::SLOT, 16, 1024);
+                        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + buf * C::Q_BYTES, 16, 1024);
                         const uint32_t idesc = umma_idesc(128, 32 * nb, false, false);
-                        const uint32_t s_col = tbase + C::TM_S0 + buf * C::TM_SSTRIDE;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            umma_ts(s_col, tbase + C::TM_Q + 8 * kk,
-                                    kdesc + (static_cast<uint32_t>((kk >> 2) * C::K_SLAB + (kk & 3) * 32) >> 4),
-                                    idesc, kk != 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::K_SLAB + (kk & 3) * 32) >> 4;
+                            const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+                            umma_ss(tbase + buf * C::TM_SSTRIDE, qdesc + qoff, kdesc + koff, idesc, kk != 0);
+                        }
                         umma_commit(&s_full[buf]);
                     }
                     // ---- O = P V for the previous tile
@@ -277,7 +274,6 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                     have_prev = true;
-                    p_buf = buf;
                     p_nb = nb;
                     p_klo = klo;
                     p_seg = seg;
@@ -319,7 +315,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float2 f = unpack_bf16x2(w[e]);
-                                bad |= !(fabsf(f.x) < 65520.f) || !(fabsf(f.y) < 65520.f);
+                                bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
                                 __half2 hv = __floats2half2_rn(f.x, f.y);
                                 w[e] = *reinterpret_cast<uint32_t *>(&hv);
                             }
@@ -337,138 +333,42 @@ __global__ void __launch_bounds__(384, 1)
             record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         if (!ok && lane == 0)
             record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
-    } else if (warp < 8) {
-        // ------------------------------------------------------------------ softmax
-        const int rw = warp - 4;
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ softmax (two warpgroups)
+        const int wg = (warp - 4) >> 2;  // 0: even tiles / S buffer 0, 1: odd tiles / S buffer 1
+        const int rw = warp & 3;
         const int r = rw * 32 + lane;
         const int ti = r / G;
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        const int wti_min = (rw * 32) / G, wti_max = (rw * 32 + 31) / G;
+        const uint32_t s_col = tbase + (static_cast<uint32_t>(rw * 32) << 16) + wg * C::TM_SSTRIDE;
+        const uint32_t o_lane = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_O;
         const float NEG_INF = -__int_as_float(0x7f800000);
         bool ok = true;
         int it = 0;
-        for (long long gt = gt_begin; gt < gt_end && ok;) {
-            const int n0 = static_cast<int>(gt % tps);
-            const int n1 = seg_end(gt, n0);
-            for (int n = n0; n < n1; ++n, ++it) {
-                const int buf = it & 1;
-                const int klo = tc_kb_lo(n, TOK, p.window), khi = tc_kb_hi(n, TOK, p.T);
-                const int nb = khi - klo + 1;
-                const int bs = klo * 32;
-                const int t0 = n * TOK, t = t0 + ti;
-                const int lo_key = max(0, t - p.window + 1), hi_key = min(t, p.T - 1);
-                const int wk_lo = t0 + wti_min - p.window + 1, wk_hi = t0 + wti_max;
-                const uint32_t s_col = tl + C::TM_S0 + buf * C::TM_SSTRIDE;
-                if (!mbar_wait(&s_full[buf], static_cast<uint32_t>((it >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float m0 = NEG_INF, m1 = NEG_INF;
-                for (int q = 0; q < nb; ++q) {
-                    const int key0 = bs + 32 * q;
-                    if (key0 > wk_hi || key0 + 31 < wk_lo)
-                        continue;  // masked for every row of this warp
-                    uint32_t v[32];
-                    tmem_ld32(s_col + 32 * q, v);
-                    tmem_wait_ld();
-                    if (key0 >= lo_key && key0 + 31 <= hi_key) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            m0 = fmaxf(m0, __uint_as_float(v[e]));
-                            m1 = fmaxf(m1, __uint_as_float(v[e + 1]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int key = key0 + e;
-                            if (key >= lo_key && key <= hi_key)
-                                m0 = fmaxf(m0, __uint_as_float(v[e]));
-                        }
-                    }
-                }
-                const float m = fmaxf(m0, m1);
-                const float mu = (m == NEG_INF) ? 0.f : m;
-                float l0 = 0.f, l1 = 0.f;
-                for (int q = 0; q < nb; ++q) {
-                    const int key0 = bs + 32 * q;
-                    uint32_t pw[16];
-                    if (key0 > wk_hi || key0 + 31 < wk_lo) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pw[e] = 0u;
-                    } else {
-                        uint32_t v[32];
-                        tmem_ld32(s_col + 32 * q, v);
-                        tmem_wait_ld();
-                        if (key0 >= lo_key && key0 + 31 <= hi_key) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float a = fast_exp2(__uint_as_float(v[2 * e]) - mu);
-                                const float c = fast_exp2(__uint_as_float(v[2 * e + 1]) - mu);
-                                l0 += a;
-                                l1 += c;
-                                pw[e] = pack_bf16x2(a, c);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int k0 = key0 + 2 * e;
-                                const float s0 = (k0 >= lo_key && k0 <= hi_key) ? __uint_as_float(v[2 * e]) : NEG_INF;
-                                const float s1 =
-                                    (k0 + 1 >= lo_key && k0 + 1 <= hi_key) ? __uint_as_float(v[2 * e + 1]) : NEG_INF;
-                                const float a = fast_exp2(s0 - mu), c = fast_exp2(s1 - mu);
-                                l0 += a;
-                                l1 += c;
-                                pw[e] = pack_bf16x2(a, c);
-                            }
-                        }
-                    }
-                    tmem_st16(s_col + 16 * q, pw);
-                }
-                const float l = l0 + l1;
-                linv[buf * 128 + r] = l > 0.f ? 1.f / l : 0.f;
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&p_full[buf]);
-            }
-            gt += n1 - n0;
-        }
-        if (!ok && lane == 0)
-            record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
-    } else {
-        // ------------------------------------------------------------------ query preparation + epilogue
-        const int rw = warp - 8;
-        const int r = rw * 32 + lane;
-        const int hl = r % G;
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        bool ok = true, bad = false;
-        uint32_t osync_phase = 0;
-        auto rendezvous = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(osync);
-            const bool r_ok = mbar_wait(osync, osync_phase & 1u);
-            ++osync_phase;
-            return r_ok;
-        };
-        auto epilogue = [&](int eit, const TcTile &et) -> bool {
-            const int buf = eit & 1;
-            if (!mbar_wait(o_full, static_cast<uint32_t>(eit & 1)) ||
-                !mbar_wait(&p_full[buf], static_cast<uint32_t>((eit >> 1) & 1)))
+        // this warpgroup's epilogue for its tile `eit`: O / l -> bf16 -> global memory
+        auto epilogue = [&](int eit, int eb, int eg, int en, float inv_l) -> bool {
+            if (!mbar_wait(&o_full[wg], static_cast<uint32_t>((eit >> 1) & 1)))
                 return false;
             tc_fence_after();
-            const float inv_l = linv[buf * 128 + r];
-            if (r == 0)
-                bulk_wait_read_all();  // the previous store has finished reading the stage
-            if (!rendezvous())
-                return false;
+            const int token = en * TOK + ti;
+            const bool valid = token < p.T;
+            orthros_bf16 *orow =
+                p.o + eb * p.o_bstride + (static_cast<long long>(token) * p.Hq + eg * G + r % G) * D;
+            uint32_t v[2][32];
+            tmem_ld32(o_lane, v[0]);
+            tmem_wait_ld();
 #pragma unroll
             for (int cq = 0; cq < D / 32; ++cq) {
-                uint32_t v[32];
-                tmem_ld32(tl + C::TM_O + 32 * cq, v);
+                if (cq + 1 < D / 32)
+                    tmem_ld32(o_lane + 32 * (cq + 1), v[(cq + 1) & 1]);
+                uint4 w[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t *x = &v[cq & 1][8 * c4];
+                    w[c4].x = pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
+                    w[c4].y = pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+                    w[c4].z = pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
+                    w[c4].w = pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
+                }
                 tmem_wait_ld();
                 if (cq == D / 32 - 1) {
                     tc_fence_before();
@@ -476,94 +376,175 @@ __global__ void __launch_bounds__(384, 1)
                     if (lane == 0)
                         mbar_arrive(o_free);
                 }
+                if (valid) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(v[8 * c4 + 0]) * inv_l, __uint_as_float(v[8 * c4 + 1]) * inv_l);
-                    w.y = pack_bf16x2(__uint_as_float(v[8 * c4 + 2]) * inv_l, __uint_as_float(v[8 * c4 + 3]) * inv_l);
-                    w.z = pack_bf16x2(__uint_as_float(v[8 * c4 + 4]) * inv_l, __uint_as_float(v[8 * c4 + 5]) * inv_l);
-                    w.w = pack_bf16x2(__uint_as_float(v[8 * c4 + 6]) * inv_l, __uint_as_float(v[8 * c4 + 7]) * inv_l);
-                    const int dcol = 32 * cq + 8 * c4;
-                    *reinterpret_cast<uint4 *>(smem + C::O_OFF + (dcol / 64) * C::Q_SLAB +
-                                               sw128_offset(r, (dcol % 64) / 8)) = w;
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        *reinterpret_cast<uint4 *>(orow + 32 * cq + 8 * c4) = w[c4];
                 }
-            }
-            fence_proxy_async_smem();
-            if (!rendezvous())
-                return false;
-            if (r == 0) {
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl)
-                    tma_store_4d(&omap, smem + C::O_OFF + sl * C::Q_SLAB, sl * 64, et.g * G, et.n * TOK, et.b);
-                bulk_commit();
             }
             return true;
         };
-        int it = 0;
-        TcTile prev{0, 0, 0};
         for (long long gt = gt_begin; gt < gt_end && ok;) {
-            const int stream = static_cast<int>(gt / tps), n0 = static_cast<int>(gt % tps);
+            const int n0 = static_cast<int>(gt % tps);
             const int n1 = seg_end(gt, n0);
-            const int b = stream / p.Hkv, g = stream % p.Hkv;
-            const float *al = p.alpha + (g * G + hl) * D;
-            const float *be = p.beta + (g * G + hl) * D;
-            for (int n = n0; n < n1 && ok; ++n, ++it) {
-                // q of tile `it` may overwrite tensor memory once QK(it-1) is done
-                if (it >= 1 && !mbar_wait(&s_full[(it - 1) & 1], static_cast<uint32_t>(((it - 1) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(qfull, static_cast<uint32_t>(it & 1))) {
+            const int stream_b = static_cast<int>(gt / tps) / p.Hkv, stream_g = static_cast<int>(gt / tps) % p.Hkv;
+            for (int n = n0; n < n1; ++n, ++it) {
+                if ((it & 1) != wg)
+                    continue;
+                const int klo = tc_kb_lo(n, TOK, p.window), khi = tc_kb_hi(n, TOK, p.T);
+                const int nb = khi - klo + 1;
+                const int bs = klo * 32;
+                const int t = n * TOK + ti;
+                const int lo_key = max(0, t - p.window + 1), hi_key = min(t, p.T - 1);
+                if (!mbar_wait(&s_full[wg], static_cast<uint32_t>((it >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // pass 1: row max (loads of chunk q+1 overlap the work on chunk q)
+                uint32_t v[2][32];
+                float m0 = NEG_INF, m1 = NEG_INF;
+                tmem_ld32(s_col, v[0]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    uint32_t w[32];
+                for (int q = 0; q < C::NB; ++q) {
+                    if (q >= nb)
+                        break;
+                    if (q + 1 < nb)
+                        tmem_ld32(s_col + 32 * (q + 1), v[(q + 1) & 1]);
+                    const int key0 = bs + 32 * q;
+                    if (key0 >= lo_key && key0 + 31 <= hi_key) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 raw =
-                            *reinterpret_cast<const uint4 *>(smem + C::Q_OFF + sl * C::Q_SLAB + sw128_offset(r, c));
-                        const int d0 = 64 * sl + 8 * c;
-                        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(al + d0));
-                        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(al + d0 + 4));
-                        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(be + d0));
-                        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(be + d0 + 4));
-                        const float2 x0 = unpack_bf16x2(raw.x), x1 = unpack_bf16x2(raw.y);
-                        const float2 x2 = unpack_bf16x2(raw.z), x3 = unpack_bf16x2(raw.w);
-                        const float qv[8] = {fmaf(x0.x, a0.x, b0.x) * p.qscale, fmaf(x0.y, a0.y, b0.y) * p.qscale,
-                                             fmaf(x1.x, a0.z, b0.z) * p.qscale, fmaf(x1.y, a0.w, b0.w) * p.qscale,
-                                             fmaf(x2.x, a1.x, b1.x) * p.qscale, fmaf(x2.y, a1.y, b1.y) * p.qscale,
-                                             fmaf(x3.x, a1.z, b1.z) * p.qscale, fmaf(x3.y, a1.w, b1.w) * p.qscale};
+                        for (int e = 0; e < 32; e += 2) {
+                            m0 = fmaxf(m0, __uint_as_float(v[q & 1][e]));
+                            m1 = fmaxf(m1, __uint_as_float(v[q & 1][e + 1]));
+                        }
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            bad |= !(fabsf(qv[2 * e]) < 65504.f) || !(fabsf(qv[2 * e + 1]) < 65504.f);
-                            __half2 hv = __floats2half2_rn(qv[2 * e], qv[2 * e + 1]);
-                            w[4 * c + e] = *reinterpret_cast<uint32_t *>(&hv);
+                        for (int e = 0; e < 32; ++e) {
+                            const int key = key0 + e;
+                            if (key >= lo_key && key <= hi_key)
+                                m0 = fmaxf(m0, __uint_as_float(v[q & 1][e]));
                         }
                     }
-                    tmem_st32(tl + C::TM_Q + 32 * sl, w);
+                    tmem_wait_ld();
                 }
+                const float m = fmaxf(m0, m1);
+                const float mu = (m == NEG_INF) ? 0.f : m;
+                // pass 2: P = exp2(S - max) as bf16 over S, row sum
+                float l0 = 0.f, l1 = 0.f;
+                tmem_ld32(s_col, v[0]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < C::NB; ++q) {
+                    if (q >= nb)
+                        break;
+                    if (q + 1 < nb)
+                        tmem_ld32(s_col + 32 * (q + 1), v[(q + 1) & 1]);
+                    const int key0 = bs + 32 * q;
+                    uint32_t pw[16];
+                    if (key0 >= lo_key && key0 + 31 <= hi_key) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float a = fast_exp2(__uint_as_float(v[q & 1][2 * e]) - mu);
+                            const float c = fast_exp2(__uint_as_float(v[q & 1][2 * e + 1]) - mu);
+                            l0 += a;
+                            l1 += c;
+                            pw[e] = pack_bf16x2(a, c);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int k0 = key0 + 2 * e;
+                            const float s0 =
+                                (k0 >= lo_key && k0 <= hi_key) ? __uint_as_float(v[q & 1][2 * e]) : NEG_INF;
+                            const float s1 =
+                                (k0 + 1 >= lo_key && k0 + 1 <= hi_key) ? __uint_as_float(v[q & 1][2 * e + 1]) : NEG_INF;
+                            const float a = fast_exp2(s0 - mu), c = fast_exp2(s1 - mu);
+                            l0 += a;
+                            l1 += c;
+                            pw[e] = pack_bf16x2(a, c);
+                        }
+                    }
+                    // P columns 16q.. overwrite S columns already read (chunk q/2 <= q)
+                    tmem_st16(s_col + 16 * q, pw);
+                    tmem_wait_ld();
+                }
+                const float l = l0 + l1;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(qt_full);
-                    mbar_arrive(qempty);
-                }
-                if (it >= 1 && !epilogue(it - 1, prev)) {
+                if (lane == 0)
+                    mbar_arrive(&p_full[wg]);
+                // this warpgroup also writes its tile's output once O = P V is done
+                if (!epilogue(it, stream_b, stream_g, n, l > 0.f ? 1.f / l : 0.f)) {
                     ok = false;
                     break;
                 }
-                prev = TcTile{b, g, n};
             }
             gt += n1 - n0;
         }
-        if (ok && it >= 1 && !epilogue(it - 1, prev))
-            ok = false;
-        if (r == 0)
-            bulk_wait_all();
+        if (!ok && lane == 0)
+            record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    } else {
+        // ------------------------------------------------------------------ query preparation + epilogue
+        const int tid = threadIdx.x - 384;  // 0..127
+        const int cr = tid % C::CPR;        // this thread's 16-byte chunk within a query row
+        const int row0 = tid / C::CPR;      // first row it prepares; then every RPP-th row
+        const int sl = cr / 8, c8 = cr % 8;
+        bool ok = true, bad = false;
+        int it = 0;
+        for (long long gt = gt_begin; gt < gt_end && ok;) {
+            const int stream = static_cast<int>(gt / tps), n0 = static_cast<int>(gt % tps);
+            const int n1 = seg_end(gt, n0);
+            const int g = stream % p.Hkv;
+            // alpha * scale and beta * scale for this thread's columns; its rows alternate
+            // between at most two heads (G divides 2 * RPP)
+            float as[2][8], bsv[2][8];
+#pragma unroll
+            for (int hsel = 0; hsel < 2; ++hsel) {
+                const int h = g * G + (row0 + hsel * C::RPP) % G;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    as[hsel][e] = __ldg(p.alpha + h * D + 8 * cr + e) * p.qscale;
+                    bsv[hsel][e] = __ldg(p.beta + h * D + 8 * cr + e) * p.qscale;
+                }
+            }
+            for (int n = n0; n < n1 && ok; ++n, ++it) {
+                const int buf = it & 1;
+                if (!mbar_wait(&qfull[buf], static_cast<uint32_t>((it >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *qb = smem + C::Q_OFF + buf * C::Q_BYTES + sl * C::Q_SLAB;
+                float amax = 0.f;
+#pragma unroll 4
+                for (int j = 0; j < C::CPR; ++j) {
+                    const int row = row0 + j * C::RPP;
+                    const int hs = ((j * C::RPP) % G == 0) ? 0 : 1;  // which of the two heads
+                    uint4 *ptr = reinterpret_cast<uint4 *>(qb + sw128_offset(row, c8));
+                    const uint4 raw = *ptr;
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = unpack_bf16x2(w[e]);
+                        const float q0 = fmaf(x.x, as[hs][2 * e], bsv[hs][2 * e]);
+                        const float q1 = fmaf(x.y, as[hs][2 * e + 1], bsv[hs][2 * e + 1]);
+                        amax = fmaxf(amax, fmaxf(fabsf(q0), fabsf(q1)));
+                        __half2 hv = __floats2half2_rn(q0, q1);
+                        o4[e] = *reinterpret_cast<uint32_t *>(&hv);
+                    }
+                    *ptr = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                }
+                bad |= !(amax < 65504.f);
+                fence_proxy_async_smem();  // the MMA reads q through the async proxy
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&qt_full[buf]);
+            }
+            gt += n1 - n0;
+        }
         if (bad)
             record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         if (!ok && lane == 0)
@@ -581,7 +562,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, int G>
 static cudaError_t launch_swa_tc_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                   const CUtensorMap &o, const SwaParams &p, int num_sms, cudaStream_t stream)
+                                   const SwaParams &p, int num_sms, cudaStream_t stream)
 {
     using C = TcCfg<D>;
     auto kern = swa_tc_kernel<D, G>;
@@ -591,7 +572,7 @@ static cudaError_t launch_swa_tc_t(const CUtensorMap &q, const CUtensorMap &k, c
     long long grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
     if (grid < 1)
         grid = 1;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(q, k, v, o, p);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -619,9 +600,10 @@ bool swa_tc_supported(int D, int G, int window)
 cudaError_t launch_swa_tc(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                           const CUtensorMap &o, const SwaParams &p, int num_sms, cudaStream_t stream)
 {
+    (void)o;  // rows are stored straight from registers (p.o)
 #define ORTHROS_TC_CASE(DD, GG) \
     if (D == DD && G == GG)     \
-        return launch_swa_tc_t<DD, GG>(q, k, v, o, p, num_sms, stream);
+        return launch_swa_tc_t<DD, GG>(q, k, v, p, num_sms, stream);
     ORTHROS_TC_CASE(128, 2)
     ORTHROS_TC_CASE(128, 4)
     ORTHROS_TC_CASE(128, 8)
