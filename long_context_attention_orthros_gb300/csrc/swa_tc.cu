@@ -401,75 +401,76 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 }
                 tc_fence_after();
-                // pass 1: row max (loads of chunk q+1 overlap the work on chunk q)
-                uint32_t v[2][32];
-                float m0 = NEG_INF, m1 = NEG_INF;
-                tmem_ld32(s_col, v[0]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < C::NB; ++q) {
-                    if (q >= nb)
-                        break;
-                    if (q + 1 < nb)
-                        tmem_ld32(s_col + 32 * (q + 1), v[(q + 1) & 1]);
-                    const int key0 = bs + 32 * q;
-                    if (key0 >= lo_key && key0 + 31 <= hi_key) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            m0 = fmaxf(m0, __uint_as_float(v[q & 1][e]));
-                            m1 = fmaxf(m1, __uint_as_float(v[q & 1][e + 1]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int key = key0 + e;
-                            if (key >= lo_key && key <= hi_key)
-                                m0 = fmaxf(m0, __uint_as_float(v[q & 1][e]));
-                        }
-                    }
-                    tmem_wait_ld();
+                // keys of this row: lo_key .. hi_key; a key is valid iff 0 <= key - lo_key <= span
+                int lo = lo_key, span = hi_key - lo_key;
+                if (span < 0) {
+                    lo = -(1 << 29);  // empty row: every key fails the test below
+                    span = 0;
                 }
-                const float m = fmaxf(m0, m1);
+                const unsigned uspan = static_cast<unsigned>(span);
+                uint32_t va[32], vb[32];
+                // pass 1: row max over the band, two 32-column chunks per round
+                float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll 1
+                for (int q = 0; q < nb; q += 2) {
+                    const bool two = q + 1 < nb;
+                    tmem_ld32(s_col + 32 * q, va);
+                    if (two)
+                        tmem_ld32(s_col + 32 * (q + 1), vb);
+                    tmem_wait_ld();
+                    const int k0 = bs + 32 * q - lo;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        m4[e & 3] = fmaxf(m4[e & 3], static_cast<unsigned>(k0 + e) <= uspan ? __uint_as_float(va[e])
+                                                                                               : NEG_INF);
+                    if (two) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            m4[e & 3] = fmaxf(m4[e & 3], static_cast<unsigned>(k0 + 32 + e) <= uspan
+                                                              ? __uint_as_float(vb[e])
+                                                              : NEG_INF);
+                    }
+                }
+                const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float mu = (m == NEG_INF) ? 0.f : m;
-                // pass 2: P = exp2(S - max) as bf16 over S, row sum
-                float l0 = 0.f, l1 = 0.f;
-                tmem_ld32(s_col, v[0]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < C::NB; ++q) {
-                    if (q >= nb)
-                        break;
-                    if (q + 1 < nb)
-                        tmem_ld32(s_col + 32 * (q + 1), v[(q + 1) & 1]);
-                    const int key0 = bs + 32 * q;
-                    uint32_t pw[16];
-                    if (key0 >= lo_key && key0 + 31 <= hi_key) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float a = fast_exp2(__uint_as_float(v[q & 1][2 * e]) - mu);
-                            const float c = fast_exp2(__uint_as_float(v[q & 1][2 * e + 1]) - mu);
-                            l0 += a;
-                            l1 += c;
-                            pw[e] = pack_bf16x2(a, c);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int k0 = key0 + 2 * e;
-                            const float s0 =
-                                (k0 >= lo_key && k0 <= hi_key) ? __uint_as_float(v[q & 1][2 * e]) : NEG_INF;
-                            const float s1 =
-                                (k0 + 1 >= lo_key && k0 + 1 <= hi_key) ? __uint_as_float(v[q & 1][2 * e + 1]) : NEG_INF;
-                            const float a = fast_exp2(s0 - mu), c = fast_exp2(s1 - mu);
-                            l0 += a;
-                            l1 += c;
-                            pw[e] = pack_bf16x2(a, c);
-                        }
-                    }
-                    // P columns 16q.. overwrite S columns already read (chunk q/2 <= q)
-                    tmem_st16(s_col + 16 * q, pw);
+                // pass 2: P = exp2(S - max) as bf16 over S (P columns 16q.. overwrite S
+                // columns of chunks already read), row sum
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int q = 0; q < nb; q += 2) {
+                    const bool two = q + 1 < nb;
+                    tmem_ld32(s_col + 32 * q, va);
+                    if (two)
+                        tmem_ld32(s_col + 32 * (q + 1), vb);
                     tmem_wait_ld();
+                    const int k0 = bs + 32 * q - lo;
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float s0 = static_cast<unsigned>(k0 + 2 * e) <= uspan ? __uint_as_float(va[2 * e]) : NEG_INF;
+                        const float s1 =
+                            static_cast<unsigned>(k0 + 2 * e + 1) <= uspan ? __uint_as_float(va[2 * e + 1]) : NEG_INF;
+                        const float p0 = fast_exp2(s0 - mu), p1 = fast_exp2(s1 - mu);
+                        l4[e & 3] += p0 + p1;
+                        pw[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_col + 16 * q, pw);
+                    if (two) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float s0 =
+                                static_cast<unsigned>(k0 + 32 + 2 * e) <= uspan ? __uint_as_float(vb[2 * e]) : NEG_INF;
+                            const float s1 = static_cast<unsigned>(k0 + 33 + 2 * e) <= uspan
+                                                 ? __uint_as_float(vb[2 * e + 1])
+                                                 : NEG_INF;
+                            const float p0 = fast_exp2(s0 - mu), p1 = fast_exp2(s1 - mu);
+                            l4[e & 3] += p0 + p1;
+                            pw[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_col + 16 * (q + 1), pw);
+                    }
                 }
+                const float l0 = l4[0] + l4[1], l1 = l4[2] + l4[3];
                 const float l = l0 + l1;
                 tmem_wait_st();
                 tc_fence_before();
