@@ -361,13 +361,17 @@ __global__ void __launch_bounds__(512, 1)
                 if (cq + 1 < D / 32)
                     tmem_ld32(o_lane + 32 * (cq + 1), v[(cq + 1) & 1]);
                 uint4 w[4];
+                const float2 il = make_float2(inv_l, inv_l);
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const uint32_t *x = &v[cq & 1][8 * c4];
-                    w[c4].x = pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
-                    w[c4].y = pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
-                    w[c4].z = pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
-                    w[c4].w = pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 y = fmul2(make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), il);
+                        pk[e] = pack_bf16x2(y.x, y.y);
+                    }
+                    w[c4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 tmem_wait_ld();
                 if (cq == D / 32 - 1) {
@@ -409,6 +413,48 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 const unsigned uspan = static_cast<unsigned>(span);
                 uint32_t va[32], vb[32];
+                // chunks whose keys are inside the window of every row of this warp need no mask
+                unsigned inner = 0;
+                for (int q = 0; q < nb; ++q) {
+                    const int key0 = bs + 32 * q;
+                    if (__all_sync(0xffffffffu, key0 >= lo_key && key0 + 31 <= hi_key))
+                        inner |= 1u << q;
+                }
+                // row max of one 32-column chunk (masked or not) into m4
+                auto chunk_max = [&](const uint32_t (&v)[32], int q, float (&m4)[4]) {
+                    if (inner >> q & 1u) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2)
+                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                    } else {
+                        const int k0 = bs + 32 * q - lo;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float s0 = static_cast<unsigned>(k0 + e) <= uspan ? __uint_as_float(v[e]) : NEG_INF;
+                            const float s1 =
+                                static_cast<unsigned>(k0 + e + 1) <= uspan ? __uint_as_float(v[e + 1]) : NEG_INF;
+                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s0, s1);
+                        }
+                    }
+                };
+                // P = exp2(S - mu) of one chunk as bf16 pairs; row sums into l2
+                auto chunk_exp = [&](const uint32_t (&v)[32], int q, float mu, float2 (&l2)[2], uint32_t (&pw)[16]) {
+                    const float2 nmu = make_float2(-mu, -mu);
+                    const bool in = inner >> q & 1u;
+                    const int k0 = bs + 32 * q - lo;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float s0 = __uint_as_float(v[2 * e]), s1 = __uint_as_float(v[2 * e + 1]);
+                        if (!in) {
+                            s0 = static_cast<unsigned>(k0 + 2 * e) <= uspan ? s0 : NEG_INF;
+                            s1 = static_cast<unsigned>(k0 + 2 * e + 1) <= uspan ? s1 : NEG_INF;
+                        }
+                        const float2 d = fadd2(make_float2(s0, s1), nmu);
+                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        l2[e & 1] = fadd2(l2[e & 1], pp);
+                        pw[e] = pack_bf16x2(pp.x, pp.y);
+                    }
+                };
                 // pass 1: row max over the band, two 32-column chunks per round
                 float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll 1
@@ -418,24 +464,15 @@ __global__ void __launch_bounds__(512, 1)
                     if (two)
                         tmem_ld32(s_col + 32 * (q + 1), vb);
                     tmem_wait_ld();
-                    const int k0 = bs + 32 * q - lo;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        m4[e & 3] = fmaxf(m4[e & 3], static_cast<unsigned>(k0 + e) <= uspan ? __uint_as_float(va[e])
-                                                                                               : NEG_INF);
-                    if (two) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            m4[e & 3] = fmaxf(m4[e & 3], static_cast<unsigned>(k0 + 32 + e) <= uspan
-                                                              ? __uint_as_float(vb[e])
-                                                              : NEG_INF);
-                    }
+                    chunk_max(va, q, m4);
+                    if (two)
+                        chunk_max(vb, q + 1, m4);
                 }
                 const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float mu = (m == NEG_INF) ? 0.f : m;
                 // pass 2: P = exp2(S - max) as bf16 over S (P columns 16q.. overwrite S
                 // columns of chunks already read), row sum
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 1
                 for (int q = 0; q < nb; q += 2) {
                     const bool two = q + 1 < nb;
@@ -443,33 +480,15 @@ __global__ void __launch_bounds__(512, 1)
                     if (two)
                         tmem_ld32(s_col + 32 * (q + 1), vb);
                     tmem_wait_ld();
-                    const int k0 = bs + 32 * q - lo;
                     uint32_t pw[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float s0 = static_cast<unsigned>(k0 + 2 * e) <= uspan ? __uint_as_float(va[2 * e]) : NEG_INF;
-                        const float s1 =
-                            static_cast<unsigned>(k0 + 2 * e + 1) <= uspan ? __uint_as_float(va[2 * e + 1]) : NEG_INF;
-                        const float p0 = fast_exp2(s0 - mu), p1 = fast_exp2(s1 - mu);
-                        l4[e & 3] += p0 + p1;
-                        pw[e] = pack_bf16x2(p0, p1);
-                    }
+                    chunk_exp(va, q, mu, l2, pw);
                     tmem_st16(s_col + 16 * q, pw);
                     if (two) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float s0 =
-                                static_cast<unsigned>(k0 + 32 + 2 * e) <= uspan ? __uint_as_float(vb[2 * e]) : NEG_INF;
-                            const float s1 = static_cast<unsigned>(k0 + 33 + 2 * e) <= uspan
-                                                 ? __uint_as_float(vb[2 * e + 1])
-                                                 : NEG_INF;
-                            const float p0 = fast_exp2(s0 - mu), p1 = fast_exp2(s1 - mu);
-                            l4[e & 3] += p0 + p1;
-                            pw[e] = pack_bf16x2(p0, p1);
-                        }
+                        chunk_exp(vb, q + 1, mu, l2, pw);
                         tmem_st16(s_col + 16 * (q + 1), pw);
                     }
                 }
+                const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
                 const float l0 = l4[0] + l4[1], l1 = l4[2] + l4[3];
                 const float l = l0 + l1;
                 tmem_wait_st();
@@ -529,11 +548,10 @@ __global__ void __launch_bounds__(512, 1)
                     uint32_t o4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 x = unpack_bf16x2(w[e]);
-                        const float q0 = fmaf(x.x, as[hs][2 * e], bsv[hs][2 * e]);
-                        const float q1 = fmaf(x.y, as[hs][2 * e + 1], bsv[hs][2 * e + 1]);
-                        amax = fmaxf(amax, fmaxf(fabsf(q0), fabsf(q1)));
-                        __half2 hv = __floats2half2_rn(q0, q1);
+                        const float2 qq = ffma2(unpack_bf16x2(w[e]), make_float2(as[hs][2 * e], as[hs][2 * e + 1]),
+                                                make_float2(bsv[hs][2 * e], bsv[hs][2 * e + 1]));
+                        amax = fmax3(amax, fabsf(qq.x), fabsf(qq.y));
+                        __half2 hv = __floats2half2_rn(qq.x, qq.y);
                         o4[e] = *reinterpret_cast<uint32_t *>(&hv);
                     }
                     *ptr = make_uint4(o4[0], o4[1], o4[2], o4[3]);
