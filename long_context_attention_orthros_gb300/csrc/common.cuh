@@ -79,11 +79,9 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// The waiting loop of mbar_wait, out of line so that every call site stays small.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u))
@@ -91,6 +89,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
         if (global_timer_ns() - t0 > kWaitLimitNs)
             return false;
     }
+}
+
+// Wait for the phase with the given parity to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -174,6 +178,14 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 32-byte global store (one full sector per thread; the address must be 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void *ptr, uint4 a, uint4 b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
 }
 
 // max of three floats in one instruction (sm_100 and later)

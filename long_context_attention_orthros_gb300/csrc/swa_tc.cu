@@ -200,90 +200,87 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = true;
-            long long load_idx = 0, waited = -1;
-            int it = 0;
+            constexpr uint32_t IDESC_PV = umma_idesc(128, D, true, true);
+            // ring position (count of K/V blocks loaded before) of the current stream segment's first block
+            int seg_base = 0, seg_kb0 = 0, seg = -1, last_khi = -1, waited = -1;
             // the previous tile, whose PV is issued after this tile's QK
             bool have_prev = false;
-            int p_nb = 0, p_klo = 0, p_seg = -1;
-            long long p_idx0 = 0;
-            int seg = 0;
-            constexpr uint32_t IDESC_PV = umma_idesc(128, D, true, true);
-            auto issue_pv = [&](int pit, int rel) -> bool {
-                const int pbuf = pit & 1;
-                if (!mbar_wait(&p_full[pbuf], static_cast<uint32_t>((pit >> 1) & 1)))
-                    return false;
-                if (pit >= 1 && !mbar_wait(o_free, static_cast<uint32_t>((pit - 1) & 1)))
-                    return false;
-                tc_fence_after();
-                const uint32_t s_col = tbase + pbuf * C::TM_SSTRIDE;
-                for (int j = 0; j < p_nb; ++j) {
-                    const uint32_t vslot = sbase + C::V_OFF + static_cast<uint32_t>((p_idx0 + j) % C::STAGES) * C::SLOT;
-                    const uint64_t vdesc = umma_desc_sw128(vslot, C::V_SLAB, 1024);
-                    umma_ts(tbase + C::TM_O, s_col + 16 * j, vdesc, IDESC_PV, j != 0);
-                    umma_ts(tbase + C::TM_O, s_col + 16 * j + 8, vdesc + (2048 >> 4), IDESC_PV, 1);
-                }
-                umma_commit(&o_full[pbuf]);
-                for (int r = 0; r < rel; ++r)
-                    umma_commit(&empty[(p_idx0 + r) % C::STAGES]);
-                return true;
-            };
-            for (long long gt = gt_begin; gt < gt_end && ok; ++seg) {
-                const int n0 = static_cast<int>(gt % tps);
-                const int n1 = seg_end(gt, n0);
-                const long long seg_base = load_idx;
-                const int seg_kb0 = tc_kb_lo(n0, TOK, p.window);
-                for (int n = n0; n < n1 && ok; ++n, ++it) {
-                    const int klo = tc_kb_lo(n, TOK, p.window), khi = tc_kb_hi(n, TOK, p.T);
-                    const int nb = khi - klo + 1;
-                    const long long idx0 = seg_base + (klo - seg_kb0);
-                    const int buf = it & 1;
+            int p_nb = 0, p_klo = 0, p_seg = -1, p_idx0 = 0;
+            int n = static_cast<int>(gt_begin % tps) - 1;
+            // one pass per tile, plus a last pass for the PV of the last tile
+            for (long long gt = gt_begin, it = 0; ok; ++gt, ++it) {
+                const bool have = gt < gt_end;
+                int klo = 0, nb = 0, idx0 = 0;
+                if (have) {
+                    if (++n == tps || gt == gt_begin) {  // a new stream segment
+                        if (n == tps)
+                            n = 0;
+                        if (seg >= 0)
+                            seg_base += last_khi - seg_kb0 + 1;
+                        ++seg;
+                        seg_kb0 = tc_kb_lo(n, TOK, p.window);
+                    }
+                    klo = tc_kb_lo(n, TOK, p.window);
+                    last_khi = tc_kb_hi(n, TOK, p.T);
+                    nb = last_khi - klo + 1;
+                    idx0 = seg_base + (klo - seg_kb0);
+                    const int buf = static_cast<int>(it & 1);
                     // ---- S[buf] = q K^T for tile `it`
                     ok = mbar_wait(&qt_full[buf], static_cast<uint32_t>((it >> 1) & 1));
                     if (ok && it >= 2)  // PV(it-2) has read P from S[buf]
                         ok = mbar_wait(&o_full[buf], static_cast<uint32_t>(((it - 2) >> 1) & 1));
-                    for (int j = 0; j < nb && ok; ++j) {
-                        const long long idx = idx0 + j;
-                        if (idx > waited) {
-                            const uint32_t ph = static_cast<uint32_t>((idx / C::STAGES) & 1);
-                            ok = mbar_wait(&full[idx % C::STAGES], ph) && mbar_wait(&kconv[idx % C::STAGES], ph);
-                            waited = idx;
-                        }
+#pragma unroll 1
+                    for (int idx = max(waited + 1, idx0); idx < idx0 + nb && ok; ++idx) {
+                        const uint32_t ph = static_cast<uint32_t>((idx / C::STAGES) & 1);
+                        ok = mbar_wait(&full[idx % C::STAGES], ph) && mbar_wait(&kconv[idx % C::STAGES], ph);
+                        waited = idx;
                     }
                     if (!ok)
                         break;
                     tc_fence_after();
-                    {
-                        const uint32_t slot0 = static_cast<uint32_t>(idx0 % C::STAGES);
-                        const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot0 * C::SLOT, 16, 1024);
-                        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + buf * C::Q_BYTES, 16, 1024);
-                        const uint32_t idesc = umma_idesc(128, 32 * nb, false, false);
+                    const uint32_t slot0 = static_cast<uint32_t>(idx0 % C::STAGES);
+                    const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot0 * C::SLOT, 16, 1024);
+                    const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + buf * C::Q_BYTES, 16, 1024);
+                    const uint32_t idesc = umma_idesc(128, 32 * nb, false, false);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::K_SLAB + (kk & 3) * 32) >> 4;
-                            const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
-                            umma_ss(tbase + buf * C::TM_SSTRIDE, qdesc + qoff, kdesc + koff, idesc, kk != 0);
-                        }
-                        umma_commit(&s_full[buf]);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::K_SLAB + (kk & 3) * 32) >> 4;
+                        const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+                        umma_ss(tbase + buf * C::TM_SSTRIDE, qdesc + qoff, kdesc + koff, idesc, kk != 0);
                     }
-                    // ---- O = P V for the previous tile
-                    if (have_prev) {
-                        const int rel = (p_seg == seg) ? klo - p_klo : p_nb;
-                        if (!issue_pv(it - 1, rel)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    have_prev = true;
-                    p_nb = nb;
-                    p_klo = klo;
-                    p_seg = seg;
-                    p_idx0 = idx0;
+                    umma_commit(&s_full[buf]);
                 }
-                load_idx = seg_base + (tc_kb_hi(n1 - 1, TOK, p.T) - seg_kb0 + 1);
-                gt += n1 - n0;
+                // ---- O = P V for the previous tile; blocks no later tile of its segment uses go back to the ring
+                if (have_prev) {
+                    const int pit = static_cast<int>(it - 1), pbuf = pit & 1;
+                    const int rel = (have && p_seg == seg) ? klo - p_klo : p_nb;
+                    ok = mbar_wait(&p_full[pbuf], static_cast<uint32_t>((pit >> 1) & 1)) &&
+                         (pit < 1 || mbar_wait(o_free, static_cast<uint32_t>((pit - 1) & 1)));
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t s_col = tbase + pbuf * C::TM_SSTRIDE;
+#pragma unroll 1
+                    for (int j = 0; j < p_nb; ++j) {
+                        const uint32_t vslot =
+                            sbase + C::V_OFF + static_cast<uint32_t>((p_idx0 + j) % C::STAGES) * C::SLOT;
+                        const uint64_t vdesc = umma_desc_sw128(vslot, C::V_SLAB, 1024);
+                        umma_ts(tbase + C::TM_O, s_col + 16 * j, vdesc, IDESC_PV, j != 0);
+                        umma_ts(tbase + C::TM_O, s_col + 16 * j + 8, vdesc + (2048 >> 4), IDESC_PV, 1);
+                    }
+                    umma_commit(&o_full[pbuf]);
+#pragma unroll 1
+                    for (int r = 0; r < rel; ++r)
+                        umma_commit(&empty[(p_idx0 + r) % C::STAGES]);
+                }
+                if (!have)
+                    break;
+                have_prev = true;
+                p_nb = nb;
+                p_klo = klo;
+                p_seg = seg;
+                p_idx0 = idx0;
             }
-            if (ok && have_prev)
-                ok = issue_pv(it - 1, p_nb);
             if (!ok)
                 record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
         }
@@ -342,6 +339,8 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t s_col = tbase + (static_cast<uint32_t>(rw * 32) << 16) + wg * C::TM_SSTRIDE;
         const uint32_t o_lane = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_O;
         const float NEG_INF = -__int_as_float(0x7f800000);
+        // rows can be written as whole 32-byte sectors when the output is 32-byte aligned
+        const bool o32 = ((reinterpret_cast<uintptr_t>(p.o) | static_cast<uintptr_t>(p.o_bstride * 2)) & 31u) == 0;
         bool ok = true;
         int it = 0;
         // this warpgroup's epilogue for its tile `eit`: O / l -> bf16 -> global memory
@@ -381,9 +380,14 @@ __global__ void __launch_bounds__(512, 1)
                         mbar_arrive(o_free);
                 }
                 if (valid) {
+                    if (o32) {
+                        st_global_v8(orow + 32 * cq, w[0], w[1]);
+                        st_global_v8(orow + 32 * cq + 16, w[2], w[3]);
+                    } else {
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        *reinterpret_cast<uint4 *>(orow + 32 * cq + 8 * c4) = w[c4];
+                        for (int c4 = 0; c4 < 4; ++c4)
+                            *reinterpret_cast<uint4 *>(orow + 32 * cq + 8 * c4) = w[c4];
+                    }
                 }
             }
             return true;
@@ -420,36 +424,26 @@ __global__ void __launch_bounds__(512, 1)
                     if (__all_sync(0xffffffffu, key0 >= lo_key && key0 + 31 <= hi_key))
                         inner |= 1u << q;
                 }
-                // row max of one 32-column chunk (masked or not) into m4
-                auto chunk_max = [&](const uint32_t (&v)[32], int q, float (&m4)[4]) {
-                    if (inner >> q & 1u) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2)
-                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-                    } else {
+                // row max of one 32-column chunk into m4; a chunk that needs the mask is
+                // masked here and written back, so the exponent pass needs no mask
+                auto chunk_max = [&](uint32_t (&v)[32], int q, float (&m4)[4]) {
+                    if (!(inner >> q & 1u)) {
                         const int k0 = bs + 32 * q - lo;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float s0 = static_cast<unsigned>(k0 + e) <= uspan ? __uint_as_float(v[e]) : NEG_INF;
-                            const float s1 =
-                                static_cast<unsigned>(k0 + e + 1) <= uspan ? __uint_as_float(v[e + 1]) : NEG_INF;
-                            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], s0, s1);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            if (static_cast<unsigned>(k0 + e) > uspan)
+                                v[e] = __float_as_uint(NEG_INF);
+                        tmem_st32(s_col + 32 * q, v);
                     }
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2)
+                        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
                 };
                 // P = exp2(S - mu) of one chunk as bf16 pairs; row sums into l2
-                auto chunk_exp = [&](const uint32_t (&v)[32], int q, float mu, float2 (&l2)[2], uint32_t (&pw)[16]) {
-                    const float2 nmu = make_float2(-mu, -mu);
-                    const bool in = inner >> q & 1u;
-                    const int k0 = bs + 32 * q - lo;
+                auto chunk_exp = [&](const uint32_t (&v)[32], float2 nmu, float2 (&l2)[2], uint32_t (&pw)[16]) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        float s0 = __uint_as_float(v[2 * e]), s1 = __uint_as_float(v[2 * e + 1]);
-                        if (!in) {
-                            s0 = static_cast<unsigned>(k0 + 2 * e) <= uspan ? s0 : NEG_INF;
-                            s1 = static_cast<unsigned>(k0 + 2 * e + 1) <= uspan ? s1 : NEG_INF;
-                        }
-                        const float2 d = fadd2(make_float2(s0, s1), nmu);
+                        const float2 d = fadd2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), nmu);
                         const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
                         l2[e & 1] = fadd2(l2[e & 1], pp);
                         pw[e] = pack_bf16x2(pp.x, pp.y);
@@ -468,8 +462,10 @@ __global__ void __launch_bounds__(512, 1)
                     if (two)
                         chunk_max(vb, q + 1, m4);
                 }
+                tmem_wait_st();
                 const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float mu = (m == NEG_INF) ? 0.f : m;
+                const float2 nmu = make_float2(-mu, -mu);
                 // pass 2: P = exp2(S - max) as bf16 over S (P columns 16q.. overwrite S
                 // columns of chunks already read), row sum
                 float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -481,10 +477,10 @@ __global__ void __launch_bounds__(512, 1)
                         tmem_ld32(s_col + 32 * (q + 1), vb);
                     tmem_wait_ld();
                     uint32_t pw[16];
-                    chunk_exp(va, q, mu, l2, pw);
+                    chunk_exp(va, nmu, l2, pw);
                     tmem_st16(s_col + 16 * q, pw);
                     if (two) {
-                        chunk_exp(vb, q + 1, mu, l2, pw);
+                        chunk_exp(vb, nmu, l2, pw);
                         tmem_st16(s_col + 16 * (q + 1), pw);
                     }
                 }
