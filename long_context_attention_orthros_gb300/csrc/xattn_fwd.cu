@@ -204,70 +204,96 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
 
 // One warp per output row: merge the row's partial (max, sum, o) triples.
 template <int D>
-__global__ void __launch_bounds__(256) xattn_combine_kernel(const XattnParams p)
+__global__ void __launch_bounds__(128) xattn_combine_kernel(const XattnParams p)
 {
-    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const long long nrows = static_cast<long long>(p.B) * p.T_out * p.Hq;
-    if (wid >= nrows)
-        return;
-    const int b = static_cast<int>(wid / (static_cast<long long>(p.T_out) * p.Hq));
-    const int rem = static_cast<int>(wid % (static_cast<long long>(p.T_out) * p.Hq));
+    // one block per output row (b, copy i, head h); its four warps split the partials
+    const long long row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = static_cast<int>(row / (static_cast<long long>(p.T_out) * p.Hq));
+    const int rem = static_cast<int>(row % (static_cast<long long>(p.T_out) * p.Hq));
     const int i = rem / p.Hq, h = rem % p.Hq;
     const int g = h / p.G;
     const int bh = b * p.Hkv + g;
     const int r = i * p.G + h % p.G;
     const int BH = p.B * p.Hkv;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    __shared__ float red_ml[4];
+    __shared__ float red_o[4][D];
+    auto ml_at = [&](int q) { return __ldcg(&p.part_ml[(static_cast<long long>(q) * BH + bh) * p.R + r]); };
 
+    // the row's overall max M (log2 units) and sum L over the non-empty partials
     float M = NEG_INF;
-    for (int q = lane; q < p.n_part; q += 32) {
-        const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(q) * BH + bh) * p.R + r]);
+    for (int q = threadIdx.x; q < p.n_part; q += 128) {
+        const float2 ml = ml_at(q);
         if (ml.y > 0.f)
             M = fmaxf(M, ml.x);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0)
+        red_ml[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red_ml[0], red_ml[1]), fmaxf(red_ml[2], red_ml[3]));
+    __syncthreads();
     float L = 0.f;
-    for (int q = lane; q < p.n_part; q += 32) {
-        const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(q) * BH + bh) * p.R + r]);
+    for (int q = threadIdx.x; q < p.n_part; q += 128) {
+        const float2 ml = ml_at(q);
         if (ml.y > 0.f)
             L += ml.y * fast_exp2(ml.x - M);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0)
+        red_ml[warp] = L;
+    __syncthreads();
+    L = (red_ml[0] + red_ml[1]) + (red_ml[2] + red_ml[3]);
 
+    // sum of exp2(m_q - M) * o_q: warp w takes partials w, w + 4, ...; independent loads
     constexpr int E = D / 32;
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e)
         acc[e] = 0.f;
-    for (int q = 0; q < p.n_part; ++q) {
+#pragma unroll 4
+    for (int q = warp; q < p.n_part; q += 4) {
         const long long slot = (static_cast<long long>(q) * BH + bh) * p.R + r;
         const float2 ml = __ldcg(&p.part_ml[slot]);
-        if (!(ml.y > 0.f))
-            continue;
-        const float w = fast_exp2(ml.x - M);
+        const float w = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
         const float *po = p.part_o + slot * D + lane * E;
         if constexpr (E == 4) {
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
+            // an empty partial may hold anything; its weight must not meet a NaN
+            if (ml.y > 0.f) {
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+                acc[2] += w * v.z;
+                acc[3] += w * v.w;
+            }
         } else {
             const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
+            if (ml.y > 0.f) {
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+            }
         }
     }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        red_o[warp][lane * E + e] = acc[e];
+    __syncthreads();
+    if (warp != 0)
+        return;
     const float inv = L > 0.f ? 1.f / L : 0.f;
     orthros_bf16 *orow = p.oc + b * p.oc_bstride + (static_cast<long long>(i) * p.Hq + h) * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<uint32_t *>(orow + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < E; e += 2) {
+        const int c = lane * E + e;
+        const float x0 = (red_o[0][c] + red_o[1][c]) + (red_o[2][c] + red_o[3][c]);
+        const float x1 = (red_o[0][c + 1] + red_o[1][c + 1]) + (red_o[2][c + 1] + red_o[3][c + 1]);
+        *reinterpret_cast<uint32_t *>(orow + e) = pack_bf16x2(x0 * inv, x1 * inv);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -351,12 +377,11 @@ cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, Xatt
         e = pl.WK == 4 ? launch_partial<64, 4>(k, v, p, stream) : launch_partial<64, 1>(k, v, p, stream);
     if (e != cudaSuccess || pl.direct)
         return e;
-    const long long warps = static_cast<long long>(p.B) * p.T_out * p.Hq;
-    const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+    const unsigned blocks = static_cast<unsigned>(static_cast<long long>(p.B) * p.T_out * p.Hq);
     if (D == 128)
-        xattn_combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
+        xattn_combine_kernel<128><<<blocks, 128, 0, stream>>>(p);
     else
-        xattn_combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
+        xattn_combine_kernel<64><<<blocks, 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

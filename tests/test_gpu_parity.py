@@ -161,3 +161,25 @@ def test_copy_equals_base_causal_row_when_streams_coincide():
     oc = val(orth.xattn_fwd(bf(np.ascontiguousarray(q[:, pos[0]])), i32(pos), bf(k), bf(v),
                             f32(a), f32(b)))
     assert np.abs(oc[0] - full[0, pos[0]]).max() <= 2e-2
+
+
+def test_output_alignment_paths_agree():
+    """Output rows go out as whole 32-byte sectors when the output is 32-byte aligned and
+    as 16-byte pieces otherwise; both paths hold the same bits and meet the oracle."""
+    cfg = PrefillConfig("case", B=2, T=700, Hq=32, Hkv=8, d=128, window=128)
+    inp = make_prefill(cfg, 4242)
+    q, k, v = bf(inp.q_raw), bf(inp.k), bf(inp.v)
+    a, b = f32(inp.alpha), f32(inp.beta)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    o_aligned = orth.swa_fwd(q, k, v, a, b, window=cfg.window, scale=cfg.scale, dev_err=err)
+    n = cfg.B * cfg.T * cfg.Hq * cfg.d
+    buf = torch.zeros(n + 8, dtype=torch.bfloat16, device=dev())
+    o_off = buf[8:].view(cfg.B, cfg.T, cfg.Hq, cfg.d)  # 16 bytes past a 32-byte boundary
+    orth.swa_fwd(q, k, v, a, b, window=cfg.window, scale=cfg.scale, out=o_off, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert o_off.data_ptr() % 32 == 16
+    assert torch.equal(o_off.view(torch.int16), o_aligned.view(torch.int16))
+    ref = oracle.swa(np.ascontiguousarray(inp.q_base), inp.k, inp.v, inp.alpha, inp.beta, cfg.window,
+                     cfg.scale)
+    assert_parity(val(o_off), ref, "base O, 16-byte stores")
