@@ -133,6 +133,40 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  void *stream);
 
 /*
+ * Bytes of device workspace orthros_prefill_fwd needs for these sizes (that of
+ * the copies' cross-attention).  Returns 0 for invalid sizes.
+ */
+size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, int d);
+
+/*
+ * One prefill layer in one call (the paper has no counterpart; a convenience):
+ * Eq. (4) for the base stream, then Eq. (5) for T_out output copies over the
+ * base K/V up to their original positions (Sec. 3.2, prefill mode).  Exactly
+ * orthros_swa_fwd followed by orthros_xattn_fwd with T_kv = T on the same
+ * stream, with the same results and error behaviour (three kernel launches; the
+ * copies' kernel reads K/V a second time).  A variant that attended the copies
+ * inside the SWA pass, reading K/V once, measured no faster on GB300: the extra
+ * work in the SWA kernel cost as much time as the second read saves.
+ *
+ *   q_raw, k, v, alpha, beta, o, window, q_bstride, kv_bstride, o_bstride:
+ *          as orthros_swa_fwd
+ *   qc_raw, pos, alpha_c, beta_c, oc, qc_bstride, oc_bstride: as
+ *          orthros_xattn_fwd with T_kv = T (qc_raw may point into the q_raw
+ *          buffer, after the base tokens)
+ *   workspace: orthros_prefill_workspace_size(...) bytes, 256-byte aligned,
+ *          contents need not be initialised (unused when T_out == 0).
+ */
+orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                                   const orthros_bf16 *v, const float *alpha, const float *beta,
+                                   orthros_bf16 *o, const orthros_bf16 *qc_raw,
+                                   const int32_t *pos, const float *alpha_c, const float *beta_c,
+                                   orthros_bf16 *oc, int B, int T, int T_out, int Hq, int Hkv,
+                                   int d, int window, float scale, int64_t q_bstride,
+                                   int64_t kv_bstride, int64_t o_bstride, int64_t qc_bstride,
+                                   int64_t oc_bstride, void *workspace, size_t ws_bytes,
+                                   int32_t *dev_err, void *stream);
+
+/*
  * orthros_xattn_fwd without a workspace argument, for callers that cannot
  * allocate device memory (the paper has no counterpart; this is a deployment
  * convenience).  Such callers include plug-ins whose host runtime owns all

@@ -6,6 +6,7 @@ CUDA kernels.  PyTorch provides device memory and the current stream.
 
 * :func:`swa_fwd`      -- base-stream sliding-window attention, Eq. (4)
 * :func:`xattn_fwd`    -- output-copy full causal cross-attention, Eq. (5)
+* :func:`prefill_fwd`  -- both of them for one prefill layer in one call
 * :func:`decode_step`  -- one fused decode step with KV-cache append
 
 If the library is missing these functions raise; there is no fallback.
@@ -20,6 +21,8 @@ from ._binding import (  # noqa: F401
     decode_workspace_size,
     lib,
     library_path,
+    prefill_fwd,
+    prefill_workspace_size,
     swa_fwd,
     xattn_fwd,
     xattn_workspace_size,

@@ -55,6 +55,11 @@ def lib() -> ctypes.CDLL:
             L.orthros_xattn_fwd.restype = I
             L.orthros_xattn_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64,
                                             P, SZ, P, P]
+            L.orthros_prefill_workspace_size.restype = SZ
+            L.orthros_prefill_workspace_size.argtypes = [I, I, I, I, I, I]
+            L.orthros_prefill_fwd.restype = I
+            L.orthros_prefill_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
+                                              L64, L64, L64, L64, L64, P, SZ, P, P]
             L.orthros_decode_workspace_size.restype = SZ
             L.orthros_decode_workspace_size.argtypes = [I, I, I, I, I]
             L.orthros_decode_step.restype = I
@@ -159,6 +164,49 @@ def xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, scale=None, out=None, workspac
                                      _stream(k.device))
     _check(st, "orthros_xattn_fwd")
     return out
+
+
+def prefill_workspace_size(B, T, T_out, Hq, Hkv, d) -> int:
+    return int(lib().orthros_prefill_workspace_size(B, T, T_out, Hq, Hkv, d))
+
+
+def prefill_fwd(q_raw, k, v, alpha, beta, qc_raw, pos, alpha_c, beta_c, window: int = 128, scale=None,
+                out=None, out_c=None, workspace=None, dev_err=None):
+    """One prefill layer in one call: swa_fwd for the base stream, then xattn_fwd (T_kv = T)
+    for the output copies.  Returns (o, oc)."""
+    B, T, Hkv, d = k.shape
+    Hq = q_raw.shape[2]
+    T_out = qc_raw.shape[1]
+    qs = _bf16_rows(q_raw, "q_raw")
+    qcs = _bf16_rows(qc_raw, "qc_raw")
+    ks = _bf16_rows(k, "k")
+    if _bf16_rows(v, "v") != ks or v.shape != k.shape:
+        raise OrthrosError("k and v must have the same shape and strides")
+    if q_raw.shape[0] != B or q_raw.shape[1] < T or q_raw.shape[3] != d:
+        raise OrthrosError("q_raw shape does not match k")
+    if qc_raw.shape[0] != B or qc_raw.shape[2] != Hq or qc_raw.shape[3] != d:
+        raise OrthrosError("qc_raw shape does not match q_raw")
+    if pos.dtype != torch.int32 or tuple(pos.shape) != (B, T_out) or not pos.is_contiguous():
+        raise OrthrosError("pos must be a contiguous int32 tensor [B, T_out]")
+    for t, nm in ((alpha, "alpha"), (beta, "beta"), (alpha_c, "alpha_c"), (beta_c, "beta_c")):
+        _vec(t, nm, Hq, d)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=k.device)
+    if out_c is None:
+        out_c = torch.empty((B, T_out, Hq, d), dtype=torch.bfloat16, device=k.device)
+    os_ = _bf16_rows(out, "out")
+    ocs = _bf16_rows(out_c, "out_c")
+    if workspace is None:
+        workspace = torch.empty(max(prefill_workspace_size(B, T, T_out, Hq, Hkv, d), 256),
+                                dtype=torch.uint8, device=k.device)
+    with torch.cuda.device(k.device):
+        st = lib().orthros_prefill_fwd(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(out),
+                                       _ptr(qc_raw), _ptr(pos), _ptr(alpha_c), _ptr(beta_c), _ptr(out_c),
+                                       B, T, T_out, Hq, Hkv, d, int(window), _scale(scale, d), qs, ks, os_,
+                                       qcs, ocs, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _ptr(dev_err), _stream(k.device))
+    _check(st, "orthros_prefill_fwd")
+    return out, out_c
 
 
 def decode_workspace(B, L_max, Hq, Hkv, d, device) -> torch.Tensor:

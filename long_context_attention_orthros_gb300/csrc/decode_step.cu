@@ -203,24 +203,32 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
 
     if (x < p.nsplit) {
         // ------------------------------------------------ split CTA: copy rows
-        const int gr = lane >> 2, qd = (lane & 3) * 2;
-        WarpRows16<D> st;
+        // the G copy rows of this KV head on the MMA's N side (keys on M): q^T fragments
+        // hold row 8 nt + lane / 4; the lane keeps rows 8 nt + 2 (lane % 4) + {0, 1}
+        constexpr int NT = (G + 7) / 8;
+        WarpKeys16<D, NT, false> st;
 #pragma unroll
-        for (int kt = 0; kt < D / 16; ++kt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int row = gr + ((r & 1) ? 8 : 0);
-                const int dcol = kt * 16 + qd + ((r & 2) ? 8 : 0);
-                uint32_t hi = 0, lo = 0;
-                if (row < G && !cache_full) {
-                    const int h = g * G + row;
-                    load_q_pair(p.qc_new + (static_cast<long long>(b) * p.Hq + h) * D, p.alpha_c + h * D,
-                                p.beta_c + h * D, dcol, p.qscale, hi, lo);
+            for (int kt = 0; kt < D / 16; ++kt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = 8 * nt + (lane >> 2);
+                    const int dcol = kt * 16 + 2 * (lane & 3) + 8 * hf;
+                    uint32_t hi = 0, lo = 0;
+                    if (row < G && !cache_full) {
+                        const int h = g * G + row;
+                        load_q_pair(p.qc_new + (static_cast<long long>(b) * p.Hq + h) * D, p.alpha_c + h * D,
+                                    p.beta_c + h * D, dcol, p.qscale, hi, lo);
+                    }
+                    st.qb[nt][kt][hf] = hi;
+                    st.ql[nt][kt][hf] = lo;
                 }
-                st.qa[kt][r] = hi;
-                st.ql[kt][r] = lo;
-            }
         st.reset();
+        int lim[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            lim[nt][0] = lim[nt][1] = 0x7fffffff;
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
             const int s = i % C::STAGES;
@@ -230,8 +238,7 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
             }
             const uint32_t kbase = sbase + s * C::STAGE_BYTES;
             // every key of a whole block is below p: no mask (padding rows are never written)
-            st.step(kbase, kbase + C::KV_BYTES, C::SLAB, warp * 16, js + i * C::KB + warp * 16, 0x7fffffff,
-                    0x7fffffff, true);
+            st.step(kbase, C::SLAB, kbase + C::KV_BYTES, C::SLAB, warp * 16, js + i * C::KB + warp * 16, lim, true);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[s]);
@@ -241,19 +248,21 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
         st.finish_sums();
         const int part = x * C::CWARPS + warp;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int row = gr + half * 8;
-            if (row >= G)
-                continue;
-            float *po = part_o + (static_cast<long long>(part) * G + row) * D;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i)
-                *reinterpret_cast<float2 *>(po + i * 8 + qd) =
-                    make_float2(st.o[i][half * 2], st.o[i][half * 2 + 1]);
-            if ((lane & 3) == 0)
-                part_ml[static_cast<long long>(part) * G + row] =
-                    make_float2(half ? st.mB : st.mA, half ? st.lB : st.lA);
-        }
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int row = 8 * nt + 2 * (lane & 3) + r2;
+                if (row >= G)
+                    continue;
+                float *po = part_o + (static_cast<long long>(part) * G + row) * D + (lane >> 2);
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    po[16 * mt] = st.o[nt][mt][r2];
+                    po[16 * mt + 8] = st.o[nt][mt][2 + r2];
+                }
+                if ((lane >> 2) == 0)
+                    part_ml[static_cast<long long>(part) * G + row] = make_float2(st.m[nt][r2], st.l[nt][r2]);
+            }
     } else {
         // ------------------------------------------------ tail CTA
         float *q_s = reinterpret_cast<float *>(smem);          // [G][D]

@@ -62,6 +62,8 @@ cudaError_t launch_swa_tc(int D, int G, const CUtensorMap &q, const CUtensorMap 
 size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D);
 cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p, void *workspace,
                          cudaStream_t stream);
+// merge split partials [n_part][B*Hkv][R][D] into the copy outputs
+cudaError_t launch_xattn_combine(int D, const XattnParams &p, cudaStream_t stream);
 
 size_t decode_workspace_bytes(int B, int L_max, int Hq, int Hkv, int D);
 cudaError_t launch_decode(int D, const CUtensorMap &k, const CUtensorMap &v, DecodeParams p, void *workspace,

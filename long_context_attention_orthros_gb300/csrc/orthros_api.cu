@@ -202,6 +202,33 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
+size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T < 1 || T_out < 0 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    return T_out == 0 ? 256 : orthros::xattn_workspace_bytes(B, T_out, T, Hq, Hkv, d);
+}
+
+orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                                   const float *alpha, const float *beta, orthros_bf16 *o, const orthros_bf16 *qc_raw,
+                                   const int32_t *pos, const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
+                                   int B, int T, int T_out, int Hq, int Hkv, int d, int window, float scale,
+                                   int64_t q_bstride, int64_t kv_bstride, int64_t o_bstride, int64_t qc_bstride,
+                                   int64_t oc_bstride, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                   void *stream)
+{
+    if (T_out < 0)
+        return ORTHROS_ERR_INVALID_ARG;
+    if (T_out > 0 && (!workspace || ws_bytes < orthros_prefill_workspace_size(B, T, T_out, Hq, Hkv, d)))
+        return ORTHROS_ERR_WORKSPACE;
+    const orthros_status st = orthros_swa_fwd(q_raw, k, v, alpha, beta, o, B, T, Hq, Hkv, d, window, scale,
+                                              q_bstride, kv_bstride, o_bstride, dev_err, stream);
+    if (st != ORTHROS_OK || T_out == 0)
+        return st;
+    return orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T, Hq, Hkv, d, scale, qc_bstride,
+                             kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, stream);
+}
+
 size_t orthros_decode_workspace_size(int B, int L_max, int Hq, int Hkv, int d)
 {
     if (B < 1 || L_max < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))

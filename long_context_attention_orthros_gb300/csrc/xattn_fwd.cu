@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
             const int j0 = js + i * C::KB + c * 16;
             if (j0 > pmax)
                 continue;
-            st.step(kbase, kbase + C::KV_BYTES, C::SLAB, c * 16, j0, limA, limB, j0 + 15 <= pmin);
+            st.step(kbase, C::SLAB, kbase + C::KV_BYTES, C::SLAB, c * 16, j0, limA, limB, j0 + 15 <= pmin);
         }
         __syncwarp();
         if (lane == 0)
@@ -377,7 +377,14 @@ cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, Xatt
         e = pl.WK == 4 ? launch_partial<64, 4>(k, v, p, stream) : launch_partial<64, 1>(k, v, p, stream);
     if (e != cudaSuccess || pl.direct)
         return e;
+    return launch_xattn_combine(D, p, stream);
+}
+
+cudaError_t launch_xattn_combine(int D, const XattnParams &p, cudaStream_t stream)
+{
     const unsigned blocks = static_cast<unsigned>(static_cast<long long>(p.B) * p.T_out * p.Hq);
+    if (blocks == 0)
+        return cudaSuccess;
     if (D == 128)
         xattn_combine_kernel<128><<<blocks, 128, 0, stream>>>(p);
     else

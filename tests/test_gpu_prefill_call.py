@@ -1,0 +1,95 @@
+"""GPU parity of the one-call prefill layer (orthros_prefill_fwd) against the fp64
+oracle: the base stream (Eq. 4) and the output copies (Eq. 5) of one call.  The
+base output must also equal a separate orthros_swa_fwd bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_attention_orthros_gb300 as orth
+import oracle
+from synthetic import PrefillConfig, make_prefill
+from tests.gpu_util import assert_parity, bf, dev, f32, i32, val
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(inp, window=None):
+    cfg = inp.cfg
+    w = cfg.window if window is None else window
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    q_all = bf(inp.q_raw)
+    k, v = bf(inp.k), bf(inp.v)
+    qc = q_all[:, cfg.T:] if cfg.appended else bf(inp.qc_raw)
+    o, oc = orth.prefill_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), qc, i32(inp.pos), f32(inp.alpha_c),
+                             f32(inp.beta_c), window=w, scale=cfg.scale, dev_err=err)
+    o_swa = orth.swa_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), window=w, scale=cfg.scale, dev_err=err)
+    torch.cuda.synchronize()
+    return o, oc, o_swa, int(err.item())
+
+
+def _check(inp, window=None):
+    cfg = inp.cfg
+    w = cfg.window if window is None else window
+    o, oc, o_swa, err = _run(inp, window)
+    assert err == 0
+    assert torch.equal(o.view(torch.int16), o_swa.view(torch.int16)), "base output differs from swa_fwd"
+    ref_o = oracle.swa(np.ascontiguousarray(inp.q_base), inp.k, inp.v, inp.alpha, inp.beta, w, cfg.scale)
+    ref_oc = oracle.xattn(np.ascontiguousarray(inp.qc_raw), inp.pos, inp.k, inp.v, inp.alpha_c, inp.beta_c,
+                          cfg.scale)
+    assert_parity(val(o), ref_o, "base O")
+    assert_parity(val(oc), ref_oc, "copy O'")
+
+
+def _positions(cfg, seed):
+    """Seeded original positions: block edges, the ends, duplicates and random rows."""
+    g = np.random.default_rng(seed)
+    edges = np.array([0, 31, 32, 63, 64, cfg.T - 1, cfg.T - 1, cfg.T // 2], np.int64)
+    pos = np.empty((cfg.B, cfg.T_out), np.int32)
+    for b in range(cfg.B):
+        cand = np.concatenate([edges[edges < cfg.T], g.integers(0, cfg.T, size=cfg.T_out)])
+        pos[b] = g.permutation(cand)[:cfg.T_out]
+    return pos
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,T_out", [
+    (2, 1000, 32, 8, 128, 1),   # 8B-class heads, one copy (the prefill workload's shape)
+    (2, 1000, 32, 8, 128, 4),   # 16 copy rows per KV head
+    (1, 777, 8, 4, 64, 3),      # G=2, d=64
+    (1, 257, 16, 2, 128, 2),    # G=8
+    (1, 200, 16, 1, 64, 1),     # G=16
+    (3, 5000, 8, 2, 128, 2),    # each stream spread over many CTAs
+    (1, 5, 4, 1, 128, 2),       # fewer tiles than SMs
+    (2, 1000, 32, 8, 128, 8),   # 32 copy rows per KV head
+])
+def test_prefill_call_parity(B, T, Hq, Hkv, d, T_out):
+    cfg = PrefillConfig("call", B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, T_out=T_out)
+    inp = make_prefill(cfg, 2000 + T + T_out)
+    inp.pos[:] = _positions(cfg, T + 7 * T_out)
+    _check(inp)
+
+
+def test_prefill_call_last_position_appended():
+    """Algorithm 2's layout: the copy of the last position stored after the base tokens."""
+    cfg = PrefillConfig("call_app", B=2, T=2048, Hq=32, Hkv=8, d=128, T_out=1, appended=True)
+    _check(make_prefill(cfg, 31))
+
+
+def test_prefill_call_wide_window():
+    """A band wider than tensor memory holds (the streaming SWA kernel)."""
+    cfg = PrefillConfig("call_wide", B=1, T=700, Hq=8, Hkv=2, d=128, window=600, T_out=2)
+    inp = make_prefill(cfg, 44)
+    _check(inp, window=600)
+
+
+def test_prefill_call_bad_position():
+    cfg = PrefillConfig("call_bad", B=1, T=600, Hq=8, Hkv=2, d=128, T_out=3)
+    inp = make_prefill(cfg, 45)
+    inp.pos[0] = [100, 600, -1]
+    o, oc, o_swa, err = _run(inp)
+    assert err & orth.DEVERR_POSITION
+    got = val(oc)
+    assert (got[0, 1] == 0).all() and (got[0, 2] == 0).all()
+    ref = oracle.xattn(np.ascontiguousarray(inp.qc_raw[:, :1]), inp.pos[:, :1], inp.k, inp.v, inp.alpha_c,
+                       inp.beta_c, cfg.scale)
+    assert_parity(got[:, :1], ref, "valid copy next to bad ones")
+    assert torch.equal(o.view(torch.int16), o_swa.view(torch.int16))
