@@ -399,7 +399,12 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
 int decode_nsplit(int B, int L_max, int Hkv)
 {
     const long long BH = static_cast<long long>(B) * Hkv;
-    long long ns = (304 + BH - 1) / BH;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 148;
+    // two CTAs fit an SM (shared memory): the split and tail CTAs of every (b, KV head) in one wave
+    long long ns = 2LL * sms / BH - 1;
     const long long by_len = (static_cast<long long>(L_max) + 1023) / 1024;
     if (ns > by_len)
         ns = by_len;
