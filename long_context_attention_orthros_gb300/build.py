@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "liborthros.so")
-SOURCES = ["swa_fwd.cu", "swa_tc.cu", "xattn_fwd.cu", "decode_step.cu", "orthros_api.cu", "xattn_noalloc.cu"]
+SOURCES = ["swa_fwd.cu", "swa_tc.cu", "xattn_fwd.cu", "xattn_tc.cu", "decode_step.cu", "orthros_api.cu",
+           "xattn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

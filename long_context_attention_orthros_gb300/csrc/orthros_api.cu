@@ -180,9 +180,6 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     const size_t need = orthros::xattn_workspace_bytes(B, T_out, T_kv, Hq, Hkv, d);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return ORTHROS_ERR_WORKSPACE;
-    CUtensorMap mk, mv;
-    if (!make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 64) || !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 64))
-        return ORTHROS_ERR_CUDA;
     XattnParams p{};
     p.qc = qc_raw;
     p.pos = pos;
@@ -198,7 +195,22 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.qscale = scale * kLog2e;
-    const cudaError_t e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
+    const int G = Hq / Hkv;
+    CUtensorMap mq, mk, mv;
+    cudaError_t e;
+    if (orthros::xattn_tc_supported(d, G, T_out)) {
+        // many copies: tensor-memory flash kernel, 128-key K/V blocks, 128-row query tiles
+        p.G = G;
+        p.R = T_out * G;
+        if (!make_map(&mq, qc_raw, d, Hq, T_out, B, qs, G, 128 / G) || !make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 128) ||
+            !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 128))
+            return ORTHROS_ERR_CUDA;
+        e = orthros::launch_xattn_tc(d, G, mq, mk, mv, p, static_cast<cudaStream_t>(stream));
+    } else {
+        if (!make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 64) || !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 64))
+            return ORTHROS_ERR_CUDA;
+        e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
