@@ -64,7 +64,9 @@ cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, Xatt
                          cudaStream_t stream);
 // merge split partials [n_part][B*Hkv][R][D] into the copy outputs
 cudaError_t launch_xattn_combine(int D, const XattnParams &p, cudaStream_t stream);
-// many copies per (batch, KV head) (T_out * G >= 256): tcgen05 flash kernel over key blocks of 128
+// many copies per (batch, KV head) (T_out * G >= 256): tcgen05 flash kernel over key blocks of
+// XATTN_TC_KEYS (the K/V tensor maps' box height)
+constexpr int XATTN_TC_KEYS = 64;
 bool xattn_tc_supported(int D, int G, int T_out);
 cudaError_t launch_xattn_tc(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                             const XattnParams &p, cudaStream_t stream);

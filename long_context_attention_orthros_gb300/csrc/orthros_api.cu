@@ -199,11 +199,12 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     CUtensorMap mq, mk, mv;
     cudaError_t e;
     if (orthros::xattn_tc_supported(d, G, T_out)) {
-        // many copies: tensor-memory flash kernel, 128-key K/V blocks, 128-row query tiles
+        // many copies: tensor-memory flash kernel, 128-row query tiles, K/V blocks of XATTN_TC_KEYS
         p.G = G;
         p.R = T_out * G;
-        if (!make_map(&mq, qc_raw, d, Hq, T_out, B, qs, G, 128 / G) || !make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 128) ||
-            !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 128))
+        constexpr int KB = orthros::XATTN_TC_KEYS;
+        if (!make_map(&mq, qc_raw, d, Hq, T_out, B, qs, G, 128 / G) || !make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, KB) ||
+            !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, KB))
             return ORTHROS_ERR_CUDA;
         e = orthros::launch_xattn_tc(d, G, mq, mk, mv, p, static_cast<cudaStream_t>(stream));
     } else {

@@ -7,7 +7,7 @@
 // A CTA owns 256 copy rows of one (batch, KV head): tiles A and B of 128 rows =
 // 128 / G copies x the G query heads of the KV head, in the order a 4-D TMA box
 // lands them (row = copy * G + head).  It streams the keys 0 .. max(pos) of its
-// rows in blocks of 128 through a two-stage ring, each block serving both tiles:
+// rows in blocks of 64 through a four-stage ring, each block serving both tiles:
 //   S_t = q_t K^T   (fp16: q rounded once after scale-offset, softmax scale and
 //                    log2(e); K converted from bf16 in shared memory, exact for
 //                    |k| < 65520, otherwise ORTHROS_DEVERR_RANGE), fp32 in TMEM;
@@ -15,7 +15,9 @@
 //   bf16 over S; the running max is raised only when it grows by more than 8 (in
 //   log2 units), so the rescale of O is rare and P stays <= 256 (exact scaling);
 //   O_t += P V      (bf16, fp32 accumulation in TMEM);
-// and finally o' = O / l rounded to bf16.  Rows whose position is outside
+// and finally o' = O / l rounded to bf16.  Each tile has two S buffers, so the
+// MMA issuer computes S of block j + 1 while the softmax works on block j, and
+// O += P V of block j runs while the softmax moves on to block j + 1.  Rows whose position is outside
 // [0, T_kv) get zeros and ORTHROS_DEVERR_POSITION.
 //
 // Roles (512 threads, one CTA per SM):
@@ -25,7 +27,7 @@
 //   warps 4-7     softmax and epilogue of tile A (TMEM lanes = rows)
 //   warps 8-11    the same for tile B
 //   warps 12-15   query preparation of both tiles, then K conversion
-// Tensor memory: S_A [0, 128), S_B [128, 256), O_A [256, 256 + D), O_B after it.
+// Tensor memory: S of tile t, buffer u at 128 t + 64 u; O_A at 256, O_B at 256 + D.
 // Every mbarrier wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and
 // all roles drain to the common exit, where tensor memory is released.
 #include <cuda_fp16.h>
@@ -39,9 +41,9 @@ namespace orthros {
 template <int D>
 struct XtCfg {
     static constexpr int ROWS = 128;           // rows of one tile
-    static constexpr int KB = 128;             // keys per block
+    static constexpr int KB = XATTN_TC_KEYS;   // keys per block (= the K/V boxes' height)
     static constexpr int SLABS = D / 64;
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = 4;
     static constexpr int KSLOT = KB * 128;     // one 64-wide slab of one block
     static constexpr int STAGE_SLABS = STAGES * SLABS;
     static constexpr int K_OFF = 0;
@@ -52,11 +54,11 @@ struct XtCfg {
     static constexpr int POS_OFF = Q_OFF + 2 * Q_BYTES;   // int [256]: row limits
     static constexpr int RED_OFF = POS_OFF + 256 * 4;     // int [16]: per-warp maxima
     static constexpr int BAR_OFF = RED_OFF + 16 * 4;
-    static constexpr int NBARS = 3 * STAGES + 10;
+    static constexpr int NBARS = 3 * STAGES + 16;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0;        // + 128 * tile
+    static constexpr uint32_t TM_S = 0;        // + 128 * tile + 64 * buffer
     static constexpr uint32_t TM_O = 256;      // + D * tile
     static constexpr int CPR = D / 8;          // 16-byte chunks per query row
     static constexpr int RPP = 128 / CPR;      // rows one pass of 128 threads covers
@@ -80,9 +82,10 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *empty = bars + 2 * C::STAGES;  // [STAGES] block released (MMA commit)
     uint64_t *qfull = bars + 3 * C::STAGES;  // [2] raw query tile landed
     uint64_t *qt_full = qfull + 2;           // [2] query tile prepared
-    uint64_t *s_full = qfull + 4;            // [2] S_t of the current block complete
-    uint64_t *p_full = qfull + 6;            // [2] P_t written (and O_t rescaled if needed)
-    uint64_t *o_done = qfull + 8;            // [2] O_t += P V of the current block complete
+    uint64_t *s_full = qfull + 4;            // [tile][buffer] S of a block complete
+    uint64_t *p_full = qfull + 8;            // [tile][buffer] P written (and O rescaled if needed)
+    uint64_t *o_done = qfull + 12;           // [tile] O += P V of a block complete (one phase per block)
+    uint64_t *o_final = qfull + 14;          // [tile] O += P V of the last block complete
     int *s_pos = reinterpret_cast<int *>(smem + C::POS_OFF);
     int *s_red = reinterpret_cast<int *>(smem + C::RED_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
@@ -118,9 +121,12 @@ __global__ void __launch_bounds__(512, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(&qfull[t], 1);
             mbar_init(&qt_full[t], 4);
-            mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 4);
             mbar_init(&o_done[t], 1);
+            mbar_init(&o_final[t], 1);
+            for (int u = 0; u < 2; ++u) {
+                mbar_init(&s_full[2 * t + u], 1);
+                mbar_init(&p_full[2 * t + u], 4);
+            }
         }
         fence_barrier_init();
     }
@@ -171,40 +177,48 @@ __global__ void __launch_bounds__(512, 1)
             constexpr uint32_t IDESC_QK = umma_idesc(128, C::KB, false, false);
             constexpr uint32_t IDESC_PV = umma_idesc(128, D, true, true);
             bool ok = mbar_wait(&qt_full[0], 0) && mbar_wait(&qt_full[1], 0);
-            for (int j = 0; j < nkb && ok; ++j) {
-                const int s = j % C::STAGES;
-                const uint32_t ph = static_cast<uint32_t>((j / C::STAGES) & 1);
-                ok = mbar_wait(&full[s], ph) && mbar_wait(&kconv[s], ph);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + s * C::SLABS * C::KSLOT, 16, 1024);
-                const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + s * C::SLABS * C::KSLOT, C::KSLOT, 1024);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    // S_t is free once O_t += P V of the previous block has read P from it
-                    if (j >= 1 && !(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1))))
+            // pass j: S of block j (both tiles), then O += P V of block j - 1
+            for (int j = 0; j <= nkb && ok; ++j) {
+                if (j < nkb) {
+                    const int s = j % C::STAGES;
+                    const uint32_t ph = static_cast<uint32_t>((j / C::STAGES) & 1);
+                    if (!(ok = mbar_wait(&full[s], ph) && mbar_wait(&kconv[s], ph)))
                         break;
-                    tc_fence_after();
-                    const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
+                    const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + s * C::SLABS * C::KSLOT, 16, 1024);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        // S buffer j & 1 is free once O += P V of block j - 2 has read it
+                        if (j >= 2 && !(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 2) & 1))))
+                            break;
+                        tc_fence_after();
+                        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
+                        const uint32_t s_tm = tbase + C::TM_S + 128 * t + 64 * (j & 1);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::KSLOT + (kk & 3) * 32) >> 4;
-                        const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
-                        umma_ss(tbase + C::TM_S + 128 * t, qdesc + qoff, kdesc + koff, IDESC_QK, kk != 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::KSLOT + (kk & 3) * 32) >> 4;
+                            const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+                            umma_ss(s_tm, qdesc + qoff, kdesc + koff, IDESC_QK, kk != 0);
+                        }
+                        umma_commit(&s_full[2 * t + (j & 1)]);
                     }
-                    umma_commit(&s_full[t]);
                 }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!(ok = mbar_wait(&p_full[t], static_cast<uint32_t>(j & 1))))
-                        break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int kk = 0; kk < C::KB / 16; ++kk)
-                        umma_ts(tbase + C::TM_O + D * t, tbase + C::TM_S + 128 * t + 8 * kk,
-                                vdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&o_done[t]);
+                if (j >= 1 && ok) {
+                    const int jp = j - 1, sp = jp % C::STAGES;
+                    const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + sp * C::SLABS * C::KSLOT, C::KSLOT, 1024);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!(ok = mbar_wait(&p_full[2 * t + (jp & 1)], static_cast<uint32_t>((jp >> 1) & 1))))
+                            break;
+                        tc_fence_after();
+                        const uint32_t p_tm = tbase + C::TM_S + 128 * t + 64 * (jp & 1);
+#pragma unroll
+                        for (int kk = 0; kk < C::KB / 16; ++kk)
+                            umma_ts(tbase + C::TM_O + D * t, p_tm + 8 * kk,
+                                    vdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(&o_done[t]);
+                        if (jp == nkb - 1)
+                            umma_commit(&o_final[t]);  // the epilogue's own barrier (o_done may run ahead of it)
+                    }
+                    umma_commit(&empty[sp]);
                 }
-                umma_commit(&empty[s]);
             }
             if (!ok)
                 record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
@@ -292,40 +306,38 @@ __global__ void __launch_bounds__(512, 1)
         const int r = rw * 32 + lane;   // row of the tile = tensor-memory lane
         const int row = row_base + t * 128 + r;
         const int pr = s_pos[t * 128 + r];
-        const uint32_t s_col = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_S + 128 * t;
+        const uint32_t s_lane = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_S + 128 * t;
         const uint32_t o_col = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_O + D * t;
         const float NEG_INF = -__int_as_float(0x7f800000);
         float m = NEG_INF, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkb && ok; ++j) {
-            if (!(ok = mbar_wait(&s_full[t], static_cast<uint32_t>(j & 1))))
+            const int u = j & 1;
+            if (!(ok = mbar_wait(&s_full[2 * t + u], static_cast<uint32_t>((j >> 1) & 1))))
                 break;
             tc_fence_after();
+            const uint32_t s_col = s_lane + 64 * u;
             const int k0 = j * C::KB;
             const bool whole = __all_sync(0xffffffffu, k0 + C::KB - 1 <= pr);
             const int nvalid = pr - k0;  // column c is a valid key iff c <= nvalid
             uint32_t va[32], vb[32];
-            // pass 1: this block's row max
+            tmem_ld32(s_col, va);
+            tmem_ld32(s_col + 32, vb);
+            tmem_wait_ld();
+            if (!whole) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    if (e > nvalid)
+                        va[e] = __float_as_uint(NEG_INF);
+                    if (32 + e > nvalid)
+                        vb[e] = __float_as_uint(NEG_INF);
+                }
+            }
             float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll 1
-            for (int q = 0; q < C::KB / 32; q += 2) {
-                tmem_ld32(s_col + 32 * q, va);
-                tmem_ld32(s_col + 32 * (q + 1), vb);
-                tmem_wait_ld();
-                if (!whole) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        if (32 * q + e > nvalid)
-                            va[e] = __float_as_uint(NEG_INF);
-                        if (32 * (q + 1) + e > nvalid)
-                            vb[e] = __float_as_uint(NEG_INF);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(va[e]), __uint_as_float(va[e + 1]));
-                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(vb[e]), __uint_as_float(vb[e + 1]));
-                }
+            for (int e = 0; e < 32; e += 2) {
+                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(va[e]), __uint_as_float(va[e + 1]));
+                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(vb[e]), __uint_as_float(vb[e + 1]));
             }
             const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             // raise the running max only when it grows by more than 2^8 (P stays <= 256)
@@ -333,15 +345,19 @@ __global__ void __launch_bounds__(512, 1)
             if (__any_sync(0xffffffffu, raise)) {
                 const float f = raise ? fast_exp2(m - mb) : 1.f;  // m = -inf on the first block: f = 0
                 if (j > 0) {
-                    // O_t holds the previous blocks (complete: QK of this block waited for them)
+                    // O holds blocks up to j - 1 once their O += P V is complete
+                    if (!(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1))))
+                        break;
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < D; c += 32) {
-                        tmem_ld32(o_col + c, va);
+                        uint32_t w[32];
+                        tmem_ld32(o_col + c, w);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            va[e] = __float_as_uint(__uint_as_float(va[e]) * f);
-                        tmem_st32(o_col + c, va);
+                            w[e] = __float_as_uint(__uint_as_float(w[e]) * f);
+                        tmem_st32(o_col + c, w);
                     }
                 }
                 if (raise) {
@@ -349,42 +365,29 @@ __global__ void __launch_bounds__(512, 1)
                     m = mb;
                 }
             }
-            const float u = (m == NEG_INF) ? 0.f : m;
-            const float2 nu = make_float2(-u, -u);
-            // pass 2: P = exp2(S - m) as bf16 over S (P columns 16q.. overwrite S
-            // columns of chunks already read), row sum
+            const float uo = (m == NEG_INF) ? 0.f : m;
+            const float2 nu = make_float2(-uo, -uo);
+            // P = exp2(S - m) as bf16 over the first 32 columns of this S buffer, row sum
             float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
-            for (int q = 0; q < C::KB / 32; q += 2) {
-                tmem_ld32(s_col + 32 * q, va);
-                tmem_ld32(s_col + 32 * (q + 1), vb);
-                tmem_wait_ld();
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                const uint32_t *v = hq ? vb : va;
                 uint32_t pw[16];
 #pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t *v = hq ? vb : va;
-                    const int cb = 32 * (q + hq);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float s0 = __uint_as_float(v[2 * e]), s1 = __uint_as_float(v[2 * e + 1]);
-                        if (!whole) {
-                            s0 = cb + 2 * e > nvalid ? NEG_INF : s0;
-                            s1 = cb + 2 * e + 1 > nvalid ? NEG_INF : s1;
-                        }
-                        const float2 d = fadd2(make_float2(s0, s1), nu);
-                        const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                        l2[e & 1] = fadd2(l2[e & 1], pp);
-                        pw[e] = pack_bf16x2(pp.x, pp.y);
-                    }
-                    tmem_st16(s_col + 16 * (q + hq), pw);
+                for (int e = 0; e < 16; ++e) {
+                    const float2 d = fadd2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), nu);
+                    const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                    l2[e & 1] = fadd2(l2[e & 1], pp);
+                    pw[e] = pack_bf16x2(pp.x, pp.y);
                 }
+                tmem_st16(s_col + 16 * hq, pw);
             }
             l += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[t]);
+                mbar_arrive(&p_full[2 * t + u]);
         }
         // ---- epilogue: O / l -> bf16 -> the copy's output row
         const bool store = row < R;
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(512, 1)
                              (static_cast<long long>(row / G) * p.Hq + g * G + row % G) * D;
         const bool o32 = ((reinterpret_cast<uintptr_t>(p.oc) | static_cast<uintptr_t>(p.oc_bstride * 2)) & 31u) == 0;
         if (ok && nkb > 0) {
-            if (!(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((nkb - 1) & 1)))) {
+            if (!(ok = mbar_wait(&o_final[t], 0))) {
                 record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
             } else {
                 tc_fence_after();
