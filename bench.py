@@ -283,13 +283,55 @@ def run_gpu(args):
     h2d = sum(h[k_].numel() * h[k_].element_size() for k_ in h)
     d2h = ho.numel() * 2 + hoc.numel() * 2
 
-    def e2e_step():
-        for key in h:
-            dst = g[key].view(torch.int16) if key in ("q", "k", "v", "qc") else g[key]
+    # pipelined by 16K-row chunks on three streams: the upload of chunk c+1, the SWA of chunk c
+    # (orthros_swa_fwd_rows; its key halo is in chunk c-1) and the download of chunk c-1 overlap;
+    # the copies' cross-attention runs once the last K/V chunk is on the device
+    chunk = 16384
+    cuts = list(range(0, T, chunk)) + [T]
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def up(key, r0=None, r1=None):
+        dst = g[key].view(torch.int16) if key in ("q", "k", "v", "qc") else g[key]
+        if r0 is None:
             dst.copy_(h[key], non_blocking=True)
-        step()
-        ho.copy_(o.view(torch.int16), non_blocking=True)
-        hoc.copy_(oc.view(torch.int16), non_blocking=True)
+        else:
+            for bb in range(B):
+                dst[bb, r0:r1].copy_(h[key][bb, r0:r1], non_blocking=True)
+
+    def e2e_step():
+        start = torch.cuda.Event()
+        start.record(stream)
+        for st_ in (s_in, s_comp, s_out):
+            st_.wait_event(start)
+        with torch.cuda.stream(s_in):
+            for key in ("a", "b", "ac", "bc", "qc", "pos"):
+                up(key)
+        for c0, c1 in zip(cuts[:-1], cuts[1:]):
+            with torch.cuda.stream(s_in):
+                for key in ("q", "k", "v"):
+                    up(key, c0, c1)
+                landed = torch.cuda.Event()
+                landed.record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(landed)
+                orth.swa_fwd_rows(g["q"], g["k"], g["v"], g["a"], g["b"], c0, c1, window=cfg.window,
+                                  scale=cfg.scale, out=o, dev_err=err)
+                done = torch.cuda.Event()
+                done.record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                for bb in range(B):
+                    ho[bb, c0:c1].copy_(o.view(torch.int16)[bb, c0:c1], non_blocking=True)
+        with torch.cuda.stream(s_comp):
+            orth.xattn_fwd(g["qc"], g["pos"], g["k"], g["v"], g["ac"], g["bc"], scale=cfg.scale, out=oc,
+                           workspace=ws, dev_err=err)
+            done = torch.cuda.Event()
+            done.record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            hoc.copy_(oc.view(torch.int16), non_blocking=True)
+        for st_ in (s_in, s_comp, s_out):
+            stream.wait_stream(st_)
 
     e2e_steps = max(3, min(args.steps, 10))
     for _ in range(2):

@@ -99,6 +99,23 @@ orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                int64_t o_bstride, int32_t *dev_err, void *stream);
 
 /*
+ * orthros_swa_fwd for output rows row_begin .. row_end-1 of every sequence only
+ * (chunked prefill; the paper has no counterpart): those rows of o get exactly
+ * what orthros_swa_fwd writes there, and no other row of o is written.  Rows
+ * read their keys from row max(0, t-window+1), so a chunk needs the K/V rows
+ * max(0, row_begin-window+1) .. row_end-1 and the q_raw rows of the chunk in
+ * place; the rest of the buffers is not read.  row_begin must be a multiple of
+ * 128 and row_end a multiple of 128 or T; 0 <= row_begin <= row_end <= T
+ * (row_begin == row_end is a no-op).  Other arguments as orthros_swa_fwd.
+ */
+orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                                    const orthros_bf16 *v, const float *alpha, const float *beta,
+                                    orthros_bf16 *o, int B, int T, int Hq, int Hkv, int d,
+                                    int window, float scale, int64_t q_bstride,
+                                    int64_t kv_bstride, int64_t o_bstride, int row_begin,
+                                    int row_end, int32_t *dev_err, void *stream);
+
+/*
  * Bytes of device workspace orthros_xattn_fwd needs for these sizes
  * (split-KV partial results).  Returns 0 for invalid sizes.
  */

@@ -5,6 +5,7 @@ argument marshalling only -- every step of the operator runs in the library's
 CUDA kernels.  PyTorch provides device memory and the current stream.
 
 * :func:`swa_fwd`      -- base-stream sliding-window attention, Eq. (4)
+* :func:`swa_fwd_rows` -- the same for a range of output rows (chunked prefill)
 * :func:`xattn_fwd`    -- output-copy full causal cross-attention, Eq. (5)
 * :func:`prefill_fwd`  -- both of them for one prefill layer in one call
 * :func:`decode_step`  -- one fused decode step with KV-cache append
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     prefill_fwd,
     prefill_workspace_size,
     swa_fwd,
+    swa_fwd_rows,
     xattn_fwd,
     xattn_workspace_size,
 )

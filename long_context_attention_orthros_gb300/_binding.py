@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
             L.orthros_version.restype = I
             L.orthros_swa_fwd.restype = I
             L.orthros_swa_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64, P, P]
+            L.orthros_swa_fwd_rows.restype = I
+            L.orthros_swa_fwd_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64, I, I, P, P]
             L.orthros_xattn_workspace_size.restype = SZ
             L.orthros_xattn_workspace_size.argtypes = [I, I, I, I, I, I]
             L.orthros_xattn_fwd.restype = I
@@ -125,6 +127,32 @@ def swa_fwd(q_raw, k, v, alpha, beta, window: int = 128, scale=None, out=None, d
                                    B, T, Hq, Hkv, d, int(window), _scale(scale, d), qs, ks, os_,
                                    _ptr(dev_err), _stream(k.device))
     _check(st, "orthros_swa_fwd")
+    return out
+
+
+def swa_fwd_rows(q_raw, k, v, alpha, beta, row_begin: int, row_end: int, window: int = 128, scale=None,
+                 out=None, dev_err=None):
+    """swa_fwd for output rows row_begin..row_end-1 of every sequence only (chunked prefill);
+    other rows of `out` are left as they are.  row_begin a multiple of 128, row_end a multiple
+    of 128 or T.  Keys are read from row max(0, row_begin - window + 1)."""
+    B, T, Hkv, d = k.shape
+    Hq = q_raw.shape[2]
+    qs = _bf16_rows(q_raw, "q_raw")
+    ks = _bf16_rows(k, "k")
+    if _bf16_rows(v, "v") != ks or v.shape != k.shape:
+        raise OrthrosError("k and v must have the same shape and strides")
+    if q_raw.shape[0] != B or q_raw.shape[1] < T or q_raw.shape[3] != d:
+        raise OrthrosError("q_raw shape does not match k")
+    _vec(alpha, "alpha", Hq, d)
+    _vec(beta, "beta", Hq, d)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=k.device)
+    os_ = _bf16_rows(out, "out")
+    with torch.cuda.device(k.device):
+        st = lib().orthros_swa_fwd_rows(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(out),
+                                        B, T, Hq, Hkv, d, int(window), _scale(scale, d), qs, ks, os_,
+                                        int(row_begin), int(row_end), _ptr(dev_err), _stream(k.device))
+    _check(st, "orthros_swa_fwd_rows")
     return out
 
 

@@ -19,7 +19,9 @@ struct SwaParams {
     int32_t *dev_err;
     int T, Hkv, window;
     float qscale;          // softmax scale * log2(e), folded into the query
-    int tiles_per_stream;  // ceil(T / TOK), set by the launcher
+    int tiles_per_stream;  // tiles of the launched row range, set by the launcher
+    int n_base;            // index of the range's first tile (rows n_base * TOK ..), set by the launcher
+    int row_begin, row_end;  // output rows of each sequence to compute (row_begin a multiple of 128)
     long long total_tiles; // B * Hkv on input; B * Hkv * tiles_per_stream after launch set-up
     int reuse;             // 1: keep K/V blocks resident across consecutive tiles (set by launcher)
 };

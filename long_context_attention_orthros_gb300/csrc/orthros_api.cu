@@ -108,16 +108,21 @@ const char *orthros_status_string(orthros_status s)
 
 int orthros_version(void) { return 100; }
 
-orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
-                               const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
-                               int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
-                               int64_t o_bstride, int32_t *dev_err, void *stream)
+orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                                    const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
+                                    int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                                    int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
 {
     if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(o) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
         return ORTHROS_ERR_INVALID_ARG;
+    if (row_begin < 0 || row_end > T || row_begin > row_end || row_begin % 128 != 0 ||
+        (row_end % 128 != 0 && row_end != T))
+        return ORTHROS_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return ORTHROS_ERR_UNSUPPORTED;
+    if (row_begin == row_end)
+        return ORTHROS_OK;
     long long qs = q_bstride, ks = kv_bstride, os = o_bstride;
     if (!resolve_bstride(qs, static_cast<long long>(T) * Hq * d) ||
         !resolve_bstride(ks, static_cast<long long>(T) * Hkv * d) ||
@@ -144,8 +149,19 @@ orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.qscale = scale * kLog2e;
     p.total_tiles = static_cast<long long>(B) * Hkv;
+    p.row_begin = row_begin;
+    p.row_end = row_end;
     const cudaError_t e = orthros::launch_swa(d, G, mq, mk, mv, mo, p, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                               const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
+                               int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                               int64_t o_bstride, int32_t *dev_err, void *stream)
+{
+    return orthros_swa_fwd_rows(q_raw, k, v, alpha, beta, o, B, T, Hq, Hkv, d, window, scale, q_bstride, kv_bstride,
+                                o_bstride, 0, T < 1 ? 0 : T, dev_err, stream);
 }
 
 size_t orthros_xattn_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d)

@@ -143,8 +143,10 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
         };
         for (long long gt = gt_begin; gt < gt_end && ok;) {
             const int stream = static_cast<int>(gt / tps);
-            const int n0 = static_cast<int>(gt % tps);
-            const int n1 = static_cast<int>((tps < n0 + (gt_end - gt) ? (long long)tps : n0 + (gt_end - gt)));
+            // absolute tile indices: the launched row range starts at tile p.n_base
+            const int n0r = static_cast<int>(gt % tps);
+            const int n0 = p.n_base + n0r;
+            const int n1 = p.n_base + static_cast<int>((tps < n0r + (gt_end - gt) ? (long long)tps : n0r + (gt_end - gt)));
             const int b = stream / p.Hkv, g = stream % p.Hkv;
             int next_kb = swa_kb_lo(n0, C::TOK, p.window, C::KB);
             for (int n = n0; n < n1 && ok; ++n) {
@@ -189,8 +191,9 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
     };
     for (long long gt = gt_begin; gt < gt_end && ok;) {
         const int stream = static_cast<int>(gt / tps);
-        const int n0 = static_cast<int>(gt % tps);
-        const int n1 = static_cast<int>((tps < n0 + (gt_end - gt) ? (long long)tps : n0 + (gt_end - gt)));
+        const int n0r = static_cast<int>(gt % tps);
+        const int n0 = p.n_base + n0r;
+        const int n1 = p.n_base + static_cast<int>((tps < n0r + (gt_end - gt) ? (long long)tps : n0r + (gt_end - gt)));
         const int b = stream / p.Hkv, g = stream % p.Hkv;
         const int hA = g * G + (gr % G), hB = g * G + ((gr + 8) % G);
         const long long seg_base = load_idx;  // ring index of block kb_lo(n0) in reuse mode
@@ -415,7 +418,9 @@ cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k,
                        cudaStream_t stream)
 {
     const int TOK = 128 / G, KB = 32, STAGES = 8;
-    p.tiles_per_stream = (p.T + TOK - 1) / TOK;
+    // the row range [row_begin, row_end) as whole tiles (row_begin is a multiple of 128)
+    p.n_base = p.row_begin / TOK;
+    p.tiles_per_stream = (p.row_end + TOK - 1) / TOK - p.n_base;
     // widest band of key blocks any tile can need (worst-case alignment)
     const long long band = (static_cast<long long>(p.window) - 1 + TOK + KB - 1) / KB + 1;
     p.reuse = band <= STAGES ? 1 : 0;

@@ -85,7 +85,8 @@ __device__ __forceinline__ int tc_kb_hi(int n, int TOK, int T)
     return t / 32;
 }
 
-template <int D, int G>
+// RANGE: the launch covers a row range that may start mid-sequence (tile base n_base > 0)
+template <int D, int G, bool RANGE>
 __global__ void __launch_bounds__(512, 1)
     swa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const SwaParams p)
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(&o_full[0], 1);
         mbar_init(&o_full[1], 1);
         mbar_init(o_free, 4);
+        tmem_holder[1] = static_cast<uint32_t>(p.n_base);
         fence_barrier_init();
     }
     if (warp == 1)
@@ -137,10 +139,16 @@ __global__ void __launch_bounds__(512, 1)
     const long long gt_begin = p.total_tiles * blockIdx.x / gridDim.x;
     const long long gt_end = p.total_tiles * (blockIdx.x + 1) / gridDim.x;
     const int tps = p.tiles_per_stream;
-    // the tile sequence of this CTA, in segments of consecutive tiles of one stream
+    // the tile sequence of this CTA, in segments of consecutive tiles of one stream; tile
+    // indices are absolute (the launched row range starts at tile n_base).  n_base is read
+    // from shared memory where a segment starts, so no role keeps it in a register.
+    const volatile int *n_base_s = reinterpret_cast<const volatile int *>(tmem_holder + 1);
+    auto n_base = [&]() { return RANGE ? *n_base_s : 0; };
+    auto seg_begin = [&](long long gt) { return n_base() + static_cast<int>(gt % tps); };
     auto seg_end = [&](long long gt, int n0) {
         const long long lim = n0 + (gt_end - gt);
-        return static_cast<int>(lim < tps ? lim : tps);
+        const int end = n_base() + tps;
+        return static_cast<int>(lim < end ? lim : end);
     };
 
     if (warp == 0) {
@@ -153,7 +161,7 @@ __global__ void __launch_bounds__(512, 1)
             long long load_idx = 0;
             int it = 0;
             for (long long gt = gt_begin; gt < gt_end && ok;) {
-                const int stream = static_cast<int>(gt / tps), n0 = static_cast<int>(gt % tps);
+                const int stream = static_cast<int>(gt / tps), n0 = seg_begin(gt);
                 const int n1 = seg_end(gt, n0);
                 const int b = stream / p.Hkv, g = stream % p.Hkv;
                 int next_kb = tc_kb_lo(n0, TOK, p.window);
@@ -206,7 +214,29 @@ __global__ void __launch_bounds__(512, 1)
             // the previous tile, whose PV is issued after this tile's QK
             bool have_prev = false;
             int p_nb = 0, p_klo = 0, p_seg = -1, p_idx0 = 0;
-            int n = static_cast<int>(gt_begin % tps) - 1;
+            int n = static_cast<int>(gt_begin % tps) - 1;  // relative to the range; na = n + p.n_base
+            // O = P V for tile pit; the first `rel` blocks of its band go back to the ring
+            auto issue_pv = [&](int pit, int rel) -> bool {
+                const int pbuf = pit & 1;
+                ok = mbar_wait(&p_full[pbuf], static_cast<uint32_t>((pit >> 1) & 1)) &&
+                     (pit < 1 || mbar_wait(o_free, static_cast<uint32_t>((pit - 1) & 1)));
+                if (!ok)
+                    return false;
+                tc_fence_after();
+                const uint32_t s_col = tbase + pbuf * C::TM_SSTRIDE;
+#pragma unroll 1
+                for (int j = 0; j < p_nb; ++j) {
+                    const uint32_t vslot = sbase + C::V_OFF + static_cast<uint32_t>((p_idx0 + j) % C::STAGES) * C::SLOT;
+                    const uint64_t vdesc = umma_desc_sw128(vslot, C::V_SLAB, 1024);
+                    umma_ts(tbase + C::TM_O, s_col + 16 * j, vdesc, IDESC_PV, j != 0);
+                    umma_ts(tbase + C::TM_O, s_col + 16 * j + 8, vdesc + (2048 >> 4), IDESC_PV, 1);
+                }
+                umma_commit(&o_full[pbuf]);
+#pragma unroll 1
+                for (int r = 0; r < rel; ++r)
+                    umma_commit(&empty[(p_idx0 + r) % C::STAGES]);
+                return true;
+            };
             // one pass per tile, plus a last pass for the PV of the last tile
             for (long long gt = gt_begin, it = 0; ok; ++gt, ++it) {
                 const bool have = gt < gt_end;
@@ -218,12 +248,20 @@ __global__ void __launch_bounds__(512, 1)
                         if (seg >= 0)
                             seg_base += last_khi - seg_kb0 + 1;
                         ++seg;
-                        seg_kb0 = tc_kb_lo(n, TOK, p.window);
+                        seg_kb0 = tc_kb_lo(n + n_base(), TOK, p.window);
                     }
-                    klo = tc_kb_lo(n, TOK, p.window);
-                    last_khi = tc_kb_hi(n, TOK, p.T);
+                    const int na = n + n_base();  // absolute tile index
+                    klo = tc_kb_lo(na, TOK, p.window);
+                    last_khi = tc_kb_hi(na, TOK, p.T);
                     nb = last_khi - klo + 1;
                     idx0 = seg_base + (klo - seg_kb0);
+                    // a new segment's first band (a row range that starts mid-sequence) may not fit
+                    // the ring next to the previous segment's last band: release that tile first
+                    if (have_prev && p_seg != seg && p_nb + nb > C::STAGES) {
+                        if (!issue_pv(static_cast<int>(it - 1), p_nb))
+                            break;
+                        have_prev = false;
+                    }
                     const int buf = static_cast<int>(it & 1);
                     // ---- S[buf] = q K^T for tile `it`
                     ok = mbar_wait(&qt_full[buf], static_cast<uint32_t>((it >> 1) & 1));
@@ -250,29 +288,10 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     umma_commit(&s_full[buf]);
                 }
-                // ---- O = P V for the previous tile; blocks no later tile of its segment uses go back to the ring
-                if (have_prev) {
-                    const int pit = static_cast<int>(it - 1), pbuf = pit & 1;
-                    const int rel = (have && p_seg == seg) ? klo - p_klo : p_nb;
-                    ok = mbar_wait(&p_full[pbuf], static_cast<uint32_t>((pit >> 1) & 1)) &&
-                         (pit < 1 || mbar_wait(o_free, static_cast<uint32_t>((pit - 1) & 1)));
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t s_col = tbase + pbuf * C::TM_SSTRIDE;
-#pragma unroll 1
-                    for (int j = 0; j < p_nb; ++j) {
-                        const uint32_t vslot =
-                            sbase + C::V_OFF + static_cast<uint32_t>((p_idx0 + j) % C::STAGES) * C::SLOT;
-                        const uint64_t vdesc = umma_desc_sw128(vslot, C::V_SLAB, 1024);
-                        umma_ts(tbase + C::TM_O, s_col + 16 * j, vdesc, IDESC_PV, j != 0);
-                        umma_ts(tbase + C::TM_O, s_col + 16 * j + 8, vdesc + (2048 >> 4), IDESC_PV, 1);
-                    }
-                    umma_commit(&o_full[pbuf]);
-#pragma unroll 1
-                    for (int r = 0; r < rel; ++r)
-                        umma_commit(&empty[(p_idx0 + r) % C::STAGES]);
-                }
+                // ---- O = P V for the previous tile: within a segment it keeps the blocks this tile
+                // still uses; at a segment change or after the last tile it releases its whole band
+                if (have_prev && !issue_pv(static_cast<int>(it - 1), (have && p_seg == seg) ? klo - p_klo : p_nb))
+                    break;
                 if (!have)
                     break;
                 have_prev = true;
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = true, bad = false;
         long long idx = 0;
         for (long long gt = gt_begin; gt < gt_end && ok;) {
-            const int n0 = static_cast<int>(gt % tps);
+            const int n0 = seg_begin(gt);
             const int n1 = seg_end(gt, n0);
             const int nload = tc_kb_hi(n1 - 1, TOK, p.T) - tc_kb_lo(n0, TOK, p.window) + 1;
             for (int i = 0; i < nload; ++i, ++idx) {
@@ -393,7 +412,7 @@ __global__ void __launch_bounds__(512, 1)
             return true;
         };
         for (long long gt = gt_begin; gt < gt_end && ok;) {
-            const int n0 = static_cast<int>(gt % tps);
+            const int n0 = seg_begin(gt);
             const int n1 = seg_end(gt, n0);
             const int stream_b = static_cast<int>(gt / tps) / p.Hkv, stream_g = static_cast<int>(gt / tps) % p.Hkv;
             for (int n = n0; n < n1; ++n, ++it) {
@@ -511,7 +530,7 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = true, bad = false;
         int it = 0;
         for (long long gt = gt_begin; gt < gt_end && ok;) {
-            const int stream = static_cast<int>(gt / tps), n0 = static_cast<int>(gt % tps);
+            const int stream = static_cast<int>(gt / tps), n0 = seg_begin(gt);
             const int n1 = seg_end(gt, n0);
             const int g = stream % p.Hkv;
             // alpha * scale and beta * scale for this thread's columns; its rows alternate
@@ -580,7 +599,7 @@ static cudaError_t launch_swa_tc_t(const CUtensorMap &q, const CUtensorMap &k, c
                                    const SwaParams &p, int num_sms, cudaStream_t stream)
 {
     using C = TcCfg<D>;
-    auto kern = swa_tc_kernel<D, G>;
+    auto kern = p.n_base > 0 ? swa_tc_kernel<D, G, true> : swa_tc_kernel<D, G, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
         return e;
