@@ -112,3 +112,61 @@ def test_decode_full_cache_sets_error_and_leaves_cache():
     after = bits(g.kc)
     np.testing.assert_array_equal(after[1], before[1])
     assert g.cl.cpu().numpy().tolist() == [11, cfg.L_max]
+
+
+def test_decode_steps_replay_as_one_cuda_graph():
+    """Multi-step decode captured once as a CUDA graph: the step allocates nothing, never
+    waits on the host and keeps cache_len on the device, so replaying the captured steps
+    gives the eager steps' outputs and cache bit for bit (and meets the oracle)."""
+    cfg = DecodeConfig("graph", B=2, T0=700, steps=8, Hq=32, Hkv=8, d=128)
+    inp = make_decode(cfg, 911)
+    qn, qcn, kn, vn = bf(inp.q_new), bf(inp.qc_new), bf(inp.k_new), bf(inp.v_new)
+
+    def run(graph):
+        g = GpuDecode(inp)
+        o = torch.empty((cfg.B, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=dev())
+        oc = torch.empty_like(o)
+        outs = [torch.empty_like(o) for _ in range(cfg.steps)], [torch.empty_like(o) for _ in range(cfg.steps)]
+
+        def steps():
+            for i in range(cfg.steps):
+                orth.decode_step(qn[i], qcn[i], kn[i], vn[i], g.kc, g.vc, g.cl, g.a, g.b, g.ac, g.bc,
+                                 window=cfg.window, scale=cfg.scale, o=o, oc=oc, workspace=g.ws, dev_err=g.err)
+                outs[0][i].copy_(o)
+                outs[1][i].copy_(oc)
+        if graph:
+            cl0 = g.cl.clone()
+            kc0, vc0 = g.kc.clone(), g.vc.clone()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                steps()  # warm-up on a side stream (sets kernel attributes)
+            torch.cuda.current_stream().wait_stream(s)
+            g.cl.copy_(cl0)
+            g.kc.copy_(kc0)
+            g.vc.copy_(vc0)
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cg):
+                steps()
+            g.cl.copy_(cl0)  # capture does not run the steps; start from the initial state
+            g.kc.copy_(kc0)
+            g.vc.copy_(vc0)
+            cg.replay()
+        else:
+            steps()
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == 0
+        return g, outs
+
+    ge, oe = run(False)
+    gg, og = run(True)
+    assert torch.equal(ge.cl, gg.cl)
+    assert torch.equal(ge.kc.view(torch.int16), gg.kc.view(torch.int16))
+    assert torch.equal(ge.vc.view(torch.int16), gg.vc.view(torch.int16))
+    for i in range(cfg.steps):
+        assert torch.equal(oe[0][i].view(torch.int16), og[0][i].view(torch.int16))
+        assert torch.equal(oe[1][i].view(torch.int16), og[1][i].view(torch.int16))
+    ref, _kc, _vc, _cl = _oracle_steps(inp, range(cfg.steps))
+    for i in (0, cfg.steps - 1):
+        assert_parity(val(og[0][i]), ref[i][0], f"graph step {i} base")
+        assert_parity(val(og[1][i]), ref[i][1], f"graph step {i} copy")
