@@ -283,10 +283,10 @@ def run_gpu(args):
     h2d = sum(h[k_].numel() * h[k_].element_size() for k_ in h)
     d2h = ho.numel() * 2 + hoc.numel() * 2
 
-    # pipelined by 16K-row chunks on three streams: the upload of chunk c+1, the SWA of chunk c
+    # pipelined by 8K-row chunks on three streams: the upload of chunk c+1, the SWA of chunk c
     # (orthros_swa_fwd_rows; its key halo is in chunk c-1) and the download of chunk c-1 overlap;
     # the copies' cross-attention runs once the last K/V chunk is on the device
-    chunk = 16384
+    chunk = 8192
     cuts = list(range(0, T, chunk)) + [T]
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
