@@ -50,9 +50,11 @@ def _load():
             lib.oracle_swa.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_swa_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D, P, P, I]
             lib.oracle_xattn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, D]
+            lib.oracle_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                                I, I, I, I, I, D]
-            for f in (lib.oracle_swa, lib.oracle_swa_rows, lib.oracle_xattn, lib.oracle_decode_step):
+            for f in (lib.oracle_swa, lib.oracle_swa_rows, lib.oracle_xattn, lib.oracle_decode_step,
+                      lib.oracle_swa_bwd):
                 f.restype = I
             _lib = lib
     return _lib
@@ -87,6 +89,25 @@ def swa(q_raw, k, v, alpha, beta, window: int, scale: float) -> np.ndarray:
                             B, T, Hq, Hkv, d, int(window), float(scale))
     _check(rc, "swa")
     return o
+
+
+def swa_bwd(q_raw, k, v, alpha, beta, dO, window: int, scale: float):
+    """Gradient of Eq. (4) with its scale-offset for an output gradient dO (bf16 bits
+    [B,T,Hq,d]): returns fp64 (dq_raw [B,T,Hq,d], dk, dv [B,T,Hkv,d], dalpha, dbeta [Hq,d])."""
+    B, T, Hq, d = q_raw.shape
+    Hkv = k.shape[2]
+    assert k.shape == v.shape == (B, T, Hkv, d) and dO.shape == q_raw.shape
+    q_raw, pq = _c(q_raw, np.uint16)
+    k, pk = _c(k, np.uint16)
+    v, pv = _c(v, np.uint16)
+    alpha, pa = _c(alpha, np.float32)
+    beta, pb = _c(beta, np.float32)
+    dO, pg = _c(dO, np.uint16)
+    out = [np.zeros(s, np.float64) for s in ((B, T, Hq, d), (B, T, Hkv, d), (B, T, Hkv, d), (Hq, d), (Hq, d))]
+    rc = _load().oracle_swa_bwd(pq, pk, pv, pa, pb, pg, *[o.ctypes.data_as(ctypes.c_void_p) for o in out],
+                                B, T, Hq, Hkv, d, int(window), float(scale))
+    _check(rc, "swa_bwd")
+    return tuple(out)
 
 
 def swa_rows(q_raw, k, v, alpha, beta, window: int, scale: float, b_idx, t_idx) -> np.ndarray:

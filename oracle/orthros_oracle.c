@@ -292,3 +292,110 @@ int oracle_decode_step(const uint16_t *q_new, const uint16_t *qc_new, const uint
         cache_len[b] += 1;
     return bad ? -2 : 0;
 }
+
+/*
+ * Gradient of the base stream, Eq. (4) with its scale-offset, for a loss L whose
+ * gradient with respect to the output o is dO (bf16 [B, T, Hq, d]).  Per row
+ * (b, t, h) with window keys j = lo..t:
+ *   p_j  = softmax_j(s_j),  s_j = scale * (q . k_j),  q = q_raw * alpha + beta
+ *   dp_j = dO . v_j,  D = sum_j p_j dp_j,  ds_j = p_j (dp_j - D)
+ *   dq   = scale * sum_j ds_j k_j,   dk_j += scale * ds_j q,   dv_j += p_j dO
+ * and through the scale-offset: dq_raw = dq * alpha, dalpha += q_raw * dq,
+ * dbeta += dq (summed over every row of the head).
+ * Outputs (fp64, overwritten): dq_raw [B, T, Hq, d]; dk, dv [B, T, Hkv, d];
+ * dalpha, dbeta [Hq, d].  Each KV head is one parallel job, so every output
+ * element has a single writer.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_swa_bwd(const uint16_t *q_raw, const uint16_t *k, const uint16_t *v,
+                   const float *alpha, const float *beta, const uint16_t *dO,
+                   double *dq_raw, double *dk, double *dv, double *dalpha, double *dbeta,
+                   int B, int T, int Hq, int Hkv, int d, int window, double scale)
+{
+    if (!shapes_ok(B, T, Hq, Hkv, d) || window < 1)
+        return -1;
+    const int group = Hq / Hkv;
+    const int64_t kv_row = (int64_t)Hkv * d;
+    memset(dq_raw, 0, sizeof(double) * (size_t)B * T * Hq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * T * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * T * Hkv * d);
+    memset(dalpha, 0, sizeof(double) * (size_t)Hq * d);
+    memset(dbeta, 0, sizeof(double) * (size_t)Hq * d);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dq = (double *)malloc(sizeof(double) * (size_t)d);
+        double *p = (double *)malloc(sizeof(double) * (size_t)window);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)window);
+        if (!q || !dq || !p || !dp) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int g = 0; g < Hkv; ++g)
+                for (int64_t b = 0; b < B; ++b)
+                    for (int64_t t = 0; t < T; ++t)
+                        for (int hh = 0; hh < group; ++hh) {
+                            const int h = g * group + hh;
+                            const int64_t lo = t - window + 1 > 0 ? t - window + 1 : 0;
+                            const int64_t n = t - lo + 1;
+                            const uint16_t *xr = q_raw + ((b * T + t) * Hq + h) * d;
+                            const uint16_t *gr = dO + ((b * T + t) * Hq + h) * d;
+                            const uint16_t *kb = k + (b * T * Hkv + g) * d;
+                            const uint16_t *vb = v + (b * T * Hkv + g) * d;
+                            scale_offset_row(xr, alpha + (int64_t)h * d, beta + (int64_t)h * d, d, q);
+                            /* forward probabilities over the window */
+                            double m = -INFINITY;
+                            for (int64_t j = 0; j < n; ++j) {
+                                const uint16_t *kj = kb + (lo + j) * kv_row;
+                                double s = 0.0;
+                                for (int e = 0; e < d; ++e)
+                                    s += q[e] * bf16_to_double(kj[e]);
+                                p[j] = s * scale;
+                                if (p[j] > m)
+                                    m = p[j];
+                            }
+                            double den = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                p[j] = exp(p[j] - m);
+                                den += p[j];
+                            }
+                            /* dp_j = dO . v_j and D = sum_j p_j dp_j */
+                            double D = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                p[j] /= den;
+                                const uint16_t *vj = vb + (lo + j) * kv_row;
+                                double acc = 0.0;
+                                for (int e = 0; e < d; ++e)
+                                    acc += bf16_to_double(gr[e]) * bf16_to_double(vj[e]);
+                                dp[j] = acc;
+                                D += p[j] * acc;
+                            }
+                            for (int e = 0; e < d; ++e)
+                                dq[e] = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                const double ds = p[j] * (dp[j] - D);
+                                const uint16_t *kj = kb + (lo + j) * kv_row;
+                                double *dkj = dk + ((b * T + lo + j) * Hkv + g) * d;
+                                double *dvj = dv + ((b * T + lo + j) * Hkv + g) * d;
+                                for (int e = 0; e < d; ++e) {
+                                    dq[e] += scale * ds * bf16_to_double(kj[e]);
+                                    dkj[e] += scale * ds * q[e];
+                                    dvj[e] += p[j] * bf16_to_double(gr[e]);
+                                }
+                            }
+                            double *dxr = dq_raw + ((b * T + t) * Hq + h) * d;
+                            for (int e = 0; e < d; ++e) {
+                                dxr[e] = dq[e] * (double)alpha[(int64_t)h * d + e];
+                                dalpha[(int64_t)h * d + e] += bf16_to_double(xr[e]) * dq[e];
+                                dbeta[(int64_t)h * d + e] += dq[e];
+                            }
+                        }
+        }
+        free(q);
+        free(dq);
+        free(p);
+        free(dp);
+    }
+    return bad ? -2 : 0;
+}

@@ -34,7 +34,7 @@ _TAGS = {
     "q_raw": 1, "k": 2, "v": 3, "qc_raw": 4, "alpha": 5, "beta": 6,
     "alpha_c": 7, "beta_c": 8, "pos": 9, "needle": 10,
     "q_new": 11, "qc_new": 12, "k_new": 13, "v_new": 14,
-    "k_cache": 15, "v_cache": 16,
+    "k_cache": 15, "v_cache": 16, "dO": 17, "dOc": 18,
 }
 
 _CHUNK = 1 << 22  # elements per independently keyed chunk

@@ -384,3 +384,66 @@ def test_golden_abc_teaching_example():
                         np.array([[2, 1, 1, 1]], np.float32), np.zeros((1, d), np.float32), s)
     e = np.exp(np.array(g["weighted"]["copy_logits"], np.float64))
     np.testing.assert_allclose(oc_w[0, 0, 0, :3], e / e.sum(), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- gradient of Eq. (4)
+
+def _autograd_swa_grads(q, k, v, a, b, dO, w, scale):
+    """Library reference: torch autograd through float64 SDPA with the band mask and the
+    scale-offset q = x * alpha + beta, for the loss sum(dO * o)."""
+    x = torch.from_numpy(_w(q)).requires_grad_(True)
+    kk = torch.from_numpy(_w(k)).requires_grad_(True)
+    vv = torch.from_numpy(_w(v)).requires_grad_(True)
+    al = torch.from_numpy(a.astype(np.float64)).requires_grad_(True)
+    be = torch.from_numpy(b.astype(np.float64)).requires_grad_(True)
+    Hq, Hkv = q.shape[2], k.shape[2]
+    qq = x * al + be
+    kq = kk.repeat_interleave(Hq // Hkv, dim=2)
+    vq = vv.repeat_interleave(Hq // Hkv, dim=2)
+    mask = torch.from_numpy(_band(q.shape[1], w))
+    o = F.scaled_dot_product_attention(qq.transpose(1, 2), kq.transpose(1, 2), vq.transpose(1, 2),
+                                       attn_mask=mask, scale=scale).transpose(1, 2)
+    (o * torch.from_numpy(_w(dO))).sum().backward()
+    return [t.grad.numpy() for t in (x, kk, vv, al, be)]
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,w", [
+    (1, 9, 1, 1, 8, 3), (1, 40, 4, 2, 16, 7), (2, 33, 4, 1, 8, 128), (1, 70, 8, 2, 32, 16),
+])
+def test_swa_gradient_equals_autograd(B, T, Hq, Hkv, d, w):
+    q, k, v, a, b = _rand_inputs(60 + T, B, T, Hq, Hkv, d)
+    dO = normal_bf16(60 + T, "dO", (B, T, Hq, d))
+    scale = 1.0 / math.sqrt(d)
+    got = oracle.swa_bwd(q, k, v, a, b, dO, w, scale)
+    ref = _autograd_swa_grads(q, k, v, a, b, dO, w, scale)
+    for name, g, r in zip(("dq_raw", "dk", "dv", "dalpha", "dbeta"), got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_swa_gradient_in_values_is_exact_finite_difference():
+    """o is linear in V, so a one-ulp bf16 step of one value element changes
+    L = sum(dO * o) by exactly dv times the step."""
+    B, T, Hq, Hkv, d, w = 1, 12, 2, 1, 8, 5
+    q, k, v, a, b = _rand_inputs(71, B, T, Hq, Hkv, d)
+    dO = normal_bf16(71, "dO", (B, T, Hq, d))
+    scale = 1.0 / math.sqrt(d)
+    dv = oracle.swa_bwd(q, k, v, a, b, dO, w, scale)[2]
+    L0 = (oracle.swa(q, k, v, a, b, w, scale) * _w(dO)).sum()
+    for (t, e) in [(0, 0), (5, 3), (11, 7)]:
+        v2 = v.copy()
+        v2[0, t, 0, e] = np.uint16(int(v2[0, t, 0, e]) + 1)  # next bf16 value
+        step = _w(v2)[0, t, 0, e] - _w(v)[0, t, 0, e]
+        L1 = (oracle.swa(q, k, v2, a, b, w, scale) * _w(dO)).sum()
+        assert abs((L1 - L0) / step - dv[0, t, 0, e]) <= 1e-9 * max(1.0, abs(dv[0, t, 0, e]))
+
+
+def test_swa_gradient_window_one():
+    """w = 1: o_t = v_t, so dv_t = the sum of dO_t over the query heads of the KV head
+    and there is no gradient in q, k, alpha or beta."""
+    q, k, v, a, b = _rand_inputs(72, 2, 10, 4, 2, 8)
+    dO = normal_bf16(72, "dO", (2, 10, 4, 8))
+    dq, dk, dv, da, db = oracle.swa_bwd(q, k, v, a, b, dO, 1, 0.3)
+    g = _w(dO).reshape(2, 10, 2, 2, 8).sum(axis=3)
+    np.testing.assert_array_equal(dv, g)
+    for z in (dq, dk, da, db):
+        assert not z.any()
