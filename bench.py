@@ -4,7 +4,8 @@ Default workload: 8B-class prefill, batch 2 x 131072 tokens, 32 query heads /
 8 KV heads, d=128, w=128, one output copy per sequence at its last position.
 One step = base SWA (Eq. 4) over every token + the copies' cross-attention
 (Eq. 5), i.e. the whole prefill hot path.  The line also reports decode steps/s
-(batch 2, 131072-token cache, 128 consecutive fused decode steps).
+(batch 2, 131072-token cache, 128 consecutive fused decode steps) and the time of
+the base stream's gradient (orthros_swa_bwd) on the prefill inputs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl orthros|reference]
 
@@ -352,6 +353,11 @@ def run_gpu(args):
     if not args.no_decode:
         dec = run_decode(args, dev, world, hbm_peak, peak_kind)
 
+    # ---- base-stream gradient on the same inputs (training modes)
+    bwd = None
+    if not args.no_bwd:
+        bwd = run_bwd(dev, world, g, o, cfg, _tf_peak, peak_kind)
+
     del g, o, oc, ws
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -368,6 +374,7 @@ def run_gpu(args):
         "gpu_launches": args.steps * launches_per_prefill_step(cfg),
         "clocks": clocks,
         "decode": dec,
+        "swa_bwd": bwd,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, threads, sample = oracle_prefill_rate(inp)
@@ -397,6 +404,49 @@ def launches_per_prefill_step(cfg) -> int:
     chunk = math.ceil(math.ceil(cfg.T / splits) / 64) * 64
     splits = math.ceil(cfg.T / chunk)
     return 2 + (0 if splits * wk == 1 else 1)
+
+
+def swa_pairs(B, T, Hq, w) -> int:
+    """(query row, key) pairs of Eq. (4): row t sees min(t + 1, w) keys."""
+    n = min(T, w)
+    return B * Hq * (n * (n + 1) // 2 + (T - n) * w)
+
+
+def run_bwd(dev, world, g, o, cfg, tf_peak, peak_kind, calls: int = 5):
+    """orthros_swa_bwd on the prefill inputs with a seeded N(0, 1) output gradient."""
+    import torch
+    import long_context_attention_orthros_gb300 as orth
+    B, T, Hq, Hkv, d = cfg.B, cfg.T, cfg.Hq, cfg.Hkv, cfg.d
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEEDS[cfg.name] + 17)
+    dO = torch.randn((B, T, Hq, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    ws = torch.empty(orth.swa_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        return orth.swa_bwd(g["q"], g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
+                            scale=cfg.scale, workspace=ws)
+
+    for _ in range(3):
+        grads = call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        grads = call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
+    assert all(bool(torch.isfinite(t).all()) for t in grads)
+    del grads, dO, ws
+    # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
+    flops = 10 * d * swa_pairs(B, T, Hq, cfg.window)
+    tfs = flops / (ms / 1e3) / 1e12
+    return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
+            "roofline": {"kernel": "swa_bwd (3 launches)", "bound": "tensor", "achieved": tfs,
+                         "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
+                         "peak_kind": peak_kind, "algorithmic_flops": flops},
+            "gpu_launches": 3 * calls}
 
 
 def run_decode(args, dev, world, hbm_peak, peak_kind):
@@ -481,6 +531,7 @@ def main(argv=None):
     ap.add_argument("--config", default="prefill_128k", choices=["prefill_128k", "prefill_1m", "sft_16k",
                                                                  "tiny_prefill", "prefill_16k"])
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.impl == "reference":

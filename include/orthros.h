@@ -247,6 +247,45 @@ orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16
                                    int d, int window, float scale, void *workspace,
                                    size_t ws_bytes, int32_t *dev_err, void *stream);
 
+/*
+ * Bytes of device workspace orthros_swa_bwd needs (two fp32 values per query
+ * row: the row's log-sum-exp and dO . o).  Returns 0 for invalid sizes.
+ */
+size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
+
+/*
+ * Gradient of the base stream (Eq. (4) with its scale-offset, Sec. 3.1), for
+ * the training modes of Sec. 3.2.  Given the forward inputs, the forward
+ * output o (as orthros_swa_fwd wrote it) and the output gradient dO, with
+ * p_tj the softmax weight of key j for row t and q_t = Q_raw[t]*alpha+beta:
+ *   dp_tj = dO_t . v_j,  D_t = dO_t . o_t,  ds_tj = p_tj (dp_tj - D_t)
+ *   dq_t  = scale * sum_j ds_tj k_j         dq_raw_t = dq_t * alpha
+ *   dk_j  = scale * sum_t ds_tj q_t         dv_j = sum_t p_tj dO_t
+ *   dalpha = sum_t Q_raw[t] * dq_t          dbeta = sum_t dq_t   (per head, over B and T)
+ * summed over every query head of a KV head for dk, dv.
+ *
+ *   q_raw, o, dO [B, T, Hq, d] bf16, dense; k, v [B, T, Hkv, d] bf16, dense
+ *   alpha, beta [Hq, d] fp32
+ *   dq_raw [B, T, Hq, d], dk, dv [B, T, Hkv, d], dalpha, dbeta [Hq, d]: fp32
+ *   outputs, every element written (dalpha and dbeta are zeroed first)
+ *   workspace: orthros_swa_bwd_workspace_size(...) bytes, 16-byte aligned.
+ * Products are bf16 x bf16 with fp32 accumulation: q . k as a bf16 high part
+ * plus residual of q (as the forward's wide-window path), P and dS rounded to
+ * bf16 before they multiply dO, K and q, q rounded once to bf16 in dK.  Three
+ * launches: D_t, then dq (rows on the MMA's M side, which also stores each
+ * row's log-sum-exp), then dk and dv (keys on the M side, no atomics).
+ * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; window >= 1
+ * with 4*d*(window + 15 + 64/G) + 8*G*d + 1024 <= 232448 (the dq kernel keeps
+ * the K/V band of its rows in shared memory; window <= 371 at d = 128, G = 1),
+ * else ORTHROS_ERR_UNSUPPORTED.  Outputs must not alias inputs.
+ */
+orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                               const orthros_bf16 *v, const float *alpha, const float *beta,
+                               const orthros_bf16 *o, const orthros_bf16 *dO, float *dq_raw,
+                               float *dk, float *dv, float *dalpha, float *dbeta, int B, int T,
+                               int Hq, int Hkv, int d, int window, float scale, void *workspace,
+                               size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

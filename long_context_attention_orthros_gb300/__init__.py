@@ -9,6 +9,7 @@ CUDA kernels.  PyTorch provides device memory and the current stream.
 * :func:`xattn_fwd`    -- output-copy full causal cross-attention, Eq. (5)
 * :func:`prefill_fwd`  -- both of them for one prefill layer in one call
 * :func:`decode_step`  -- one fused decode step with KV-cache append
+* :func:`swa_bwd`      -- gradient of the base stream (Eq. (4) and its scale-offset)
 
 If the library is missing these functions raise; there is no fallback.
 """
@@ -24,6 +25,8 @@ from ._binding import (  # noqa: F401
     library_path,
     prefill_fwd,
     prefill_workspace_size,
+    swa_bwd,
+    swa_bwd_workspace_size,
     swa_fwd,
     swa_fwd_rows,
     xattn_fwd,

@@ -67,6 +67,11 @@ def lib() -> ctypes.CDLL:
             L.orthros_decode_step.restype = I
             L.orthros_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, P, P, P, P, I, I, I, I,
                                               I, F, P, SZ, P, P]
+            L.orthros_swa_bwd_workspace_size.restype = SZ
+            L.orthros_swa_bwd_workspace_size.argtypes = [I, I, I, I, I]
+            L.orthros_swa_bwd.restype = I
+            L.orthros_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, SZ,
+                                          P]
             _lib = L
     return _lib
 
@@ -235,6 +240,40 @@ def prefill_fwd(q_raw, k, v, alpha, beta, qc_raw, pos, alpha_c, beta_c, window: 
                                        _ptr(dev_err), _stream(k.device))
     _check(st, "orthros_prefill_fwd")
     return out, out_c
+
+
+def swa_bwd_workspace_size(B, T, Hq, Hkv, d) -> int:
+    return int(lib().orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d))
+
+
+def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, workspace=None):
+    """Gradient of Eq. (4) with its scale-offset: returns fp32 (dq_raw, dk, dv, dalpha, dbeta) for
+    the output gradient dO, given the forward inputs and the forward output o.  q_raw, o, dO
+    [B, T, Hq, d] and k, v [B, T, Hkv, d], all dense bf16; alpha, beta [Hq, d] fp32."""
+    B, T, Hkv, d = k.shape
+    Hq = q_raw.shape[2]
+    for t, nm, shp in ((q_raw, "q_raw", (B, T, Hq, d)), (o, "o", (B, T, Hq, d)), (dO, "dO", (B, T, Hq, d)),
+                       (k, "k", (B, T, Hkv, d)), (v, "v", (B, T, Hkv, d))):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shp or not t.is_contiguous():
+            raise OrthrosError(f"{nm} must be a contiguous bf16 CUDA tensor {shp}")
+    _vec(alpha, "alpha", Hq, d)
+    _vec(beta, "beta", Hq, d)
+    f32 = dict(dtype=torch.float32, device=k.device)
+    dq = torch.empty((B, T, Hq, d), **f32)
+    dk = torch.empty((B, T, Hkv, d), **f32)
+    dv = torch.empty((B, T, Hkv, d), **f32)
+    dalpha = torch.empty((Hq, d), **f32)
+    dbeta = torch.empty((Hq, d), **f32)
+    if workspace is None:
+        workspace = torch.empty(max(swa_bwd_workspace_size(B, T, Hq, Hkv, d), 256), dtype=torch.uint8,
+                                device=k.device)
+    with torch.cuda.device(k.device):
+        st = lib().orthros_swa_bwd(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o), _ptr(dO),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta), B, T, Hq, Hkv, d,
+                                   int(window), _scale(scale, d), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(k.device))
+    _check(st, "orthros_swa_bwd")
+    return dq, dk, dv, dalpha, dbeta
 
 
 def decode_workspace(B, L_max, Hq, Hkv, d, device) -> torch.Tensor:

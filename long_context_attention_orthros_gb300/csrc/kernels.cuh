@@ -55,6 +55,23 @@ struct DecodeParams {
     float qscale;
 };
 
+// gradient of the base stream (Eq. 4 with its scale-offset); dense [B, T, H, d] rows
+struct SwaBwdParams {
+    const orthros_bf16 *q, *k, *v, *o, *dO;  // q raw, the forward output o, its gradient dO
+    const float *alpha, *beta;
+    float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta accumulated (zeroed first)
+    float *lse, *Drow;                       // workspace [B*T*Hq] each: log2-sum-exp, dO . o
+    long long q_bstride, kv_bstride, o_bstride;  // batch strides in elements (q/o/dO share o_bstride for dO)
+    int B, T, Hq, Hkv, window;
+    int band_max;                            // K/V rows the dQ kernel stages per CTA (swa_bwd_band_max)
+    float scale;
+};
+
+int swa_bwd_band_max(int G, int window);
+size_t swa_bwd_workspace_floats(int B, int T, int Hq);
+bool swa_bwd_supported(int D, int G, int window);
+cudaError_t launch_swa_bwd(int D, int G, const SwaBwdParams &p, cudaStream_t stream);
+
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);
 bool swa_tc_supported(int D, int G, int window);

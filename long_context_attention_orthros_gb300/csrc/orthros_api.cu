@@ -311,4 +311,55 @@ orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
+size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    return sizeof(float) * orthros::swa_bwd_workspace_floats(B, T, Hq);
+}
+
+orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                               const float *alpha, const float *beta, const orthros_bf16 *o, const orthros_bf16 *dO,
+                               float *dq_raw, float *dk, float *dv, float *dalpha, float *dbeta, int B, int T, int Hq,
+                               int Hkv, int d, int window, float scale, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(dO) || !aligned16(dq_raw) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(dalpha) || !aligned16(dbeta) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv) || !orthros::swa_bwd_supported(d, Hq / Hkv, window))
+        return ORTHROS_ERR_UNSUPPORTED;
+    const size_t need = orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d);
+    if (!aligned16(workspace) || ws_bytes < need)
+        return ORTHROS_ERR_WORKSPACE;
+    const int G = Hq / Hkv;
+    orthros::SwaBwdParams p{};
+    p.q = q_raw;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.dO = dO;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.dq = dq_raw;
+    p.dk = dk;
+    p.dv = dv;
+    p.dalpha = dalpha;
+    p.dbeta = dbeta;
+    p.lse = static_cast<float *>(workspace);
+    p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
+    p.q_bstride = static_cast<long long>(T) * Hq * d;
+    p.kv_bstride = static_cast<long long>(T) * Hkv * d;
+    p.o_bstride = p.q_bstride;
+    p.B = B;
+    p.T = T;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = window;
+    p.band_max = orthros::swa_bwd_band_max(G, window);
+    p.scale = scale;
+    const cudaError_t e = orthros::launch_swa_bwd(d, G, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -102,3 +102,21 @@ def test_decode_workspace_size_and_checks(L):
                                  ctypes.c_float(0.1), p, 8, None, None) == 3
     assert L.orthros_decode_step(p, p, p, p, p, p, None, 131200, p, p, p, p, p, p, 2, 32, 8, 128,
                                  128, ctypes.c_float(0.1), p, n, None, None) == 1
+
+
+def test_swa_bwd_workspace_size_and_checks(L):
+    p, _keep = _aligned_dummy()
+    n = L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 128)
+    assert n == 2 * 4 * 2 * 1000 * 32
+    assert L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 96) == 0
+    assert L.orthros_swa_bwd_workspace_size(0, 1000, 32, 8, 128) == 0
+
+    def call(w=128, ws=p, nbytes=n, q=p, d=128):
+        return L.orthros_swa_bwd(q, p, p, p, p, p, p, p, p, p, p, p, 2, 1000, 32, 8, d, w,
+                                 ctypes.c_float(0.1), ws, nbytes, None)
+    assert call(q=None) == 1
+    assert call(w=0) == 1
+    assert call(d=96) == 2
+    assert call(w=4096) == 2   # the K/V band of a dq tile no longer fits shared memory
+    assert call(ws=None) == 3
+    assert call(nbytes=n - 4) == 3
