@@ -51,10 +51,11 @@ def _load():
             lib.oracle_swa_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D, P, P, I]
             lib.oracle_xattn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
+            lib.oracle_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                                I, I, I, I, I, D]
             for f in (lib.oracle_swa, lib.oracle_swa_rows, lib.oracle_xattn, lib.oracle_decode_step,
-                      lib.oracle_swa_bwd):
+                      lib.oracle_swa_bwd, lib.oracle_xattn_bwd):
                 f.restype = I
             _lib = lib
     return _lib
@@ -107,6 +108,28 @@ def swa_bwd(q_raw, k, v, alpha, beta, dO, window: int, scale: float):
     rc = _load().oracle_swa_bwd(pq, pk, pv, pa, pb, pg, *[o.ctypes.data_as(ctypes.c_void_p) for o in out],
                                 B, T, Hq, Hkv, d, int(window), float(scale))
     _check(rc, "swa_bwd")
+    return tuple(out)
+
+
+def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, dOc, scale: float):
+    """Gradient of Eq. (5) with the copies' scale-offset for an output gradient dOc (bf16 bits
+    [B,T_out,Hq,d]): returns fp64 (dqc_raw [B,T_out,Hq,d], dk, dv [B,T_kv,Hkv,d] -- the copies'
+    share only --, dalpha_c, dbeta_c [Hq,d])."""
+    B, T_out, Hq, d = qc_raw.shape
+    T_kv, Hkv = k.shape[1], k.shape[2]
+    assert k.shape == v.shape == (B, T_kv, Hkv, d) and dOc.shape == qc_raw.shape
+    qc_raw, pq = _c(qc_raw, np.uint16)
+    pos, pp = _c(pos, np.int32)
+    k, pk = _c(k, np.uint16)
+    v, pv = _c(v, np.uint16)
+    alpha_c, pa = _c(alpha_c, np.float32)
+    beta_c, pb = _c(beta_c, np.float32)
+    dOc, pg = _c(dOc, np.uint16)
+    out = [np.zeros(s, np.float64) for s in ((B, T_out, Hq, d), (B, T_kv, Hkv, d), (B, T_kv, Hkv, d),
+                                             (Hq, d), (Hq, d))]
+    rc = _load().oracle_xattn_bwd(pq, pp, pk, pv, pa, pb, pg, *[o.ctypes.data_as(ctypes.c_void_p) for o in out],
+                                  B, T_out, T_kv, Hq, Hkv, d, float(scale))
+    _check(rc, "xattn_bwd")
     return tuple(out)
 
 

@@ -399,3 +399,113 @@ int oracle_swa_bwd(const uint16_t *q_raw, const uint16_t *k, const uint16_t *v,
     }
     return bad ? -2 : 0;
 }
+
+/*
+ * Gradient of the output copies, Eq. (5) with the copies' scale-offset, for a
+ * loss whose gradient with respect to the copy outputs oc is dOc (bf16
+ * [B, T_out, Hq, d]).  Copy i of sequence b sits at original position
+ * p = pos[b, i] and attends base keys j = 0..p; with q' = qc_raw * alpha_c + beta_c:
+ *   p_j = softmax_j(scale * q' . k_j),  dp_j = dOc . v_j,  D = sum_j p_j dp_j,
+ *   ds_j = p_j (dp_j - D),  dq' = scale * sum_j ds_j k_j,
+ *   dk_j += scale * ds_j q',  dv_j += p_j dOc,
+ *   dqc_raw = dq' * alpha_c,  dalpha_c += qc_raw * dq',  dbeta_c += dq'.
+ * The copies' gradient reaches only base K/V (copies own no K/V).  Outputs
+ * (fp64, overwritten): dqc_raw [B, T_out, Hq, d]; dk, dv [B, T_kv, Hkv, d] (the
+ * copies' share only: a training step adds it to the base stream's);
+ * dalpha_c, dbeta_c [Hq, d].  One parallel job per KV head.  Returns 0, or -1
+ * on a bad argument or position.
+ */
+int oracle_xattn_bwd(const uint16_t *qc_raw, const int32_t *pos, const uint16_t *k,
+                     const uint16_t *v, const float *alpha_c, const float *beta_c,
+                     const uint16_t *dOc, double *dqc_raw, double *dk, double *dv,
+                     double *dalpha_c, double *dbeta_c, int B, int T_out, int T_kv, int Hq,
+                     int Hkv, int d, double scale)
+{
+    if (!shapes_ok(B, T_kv, Hq, Hkv, d) || T_out < 0)
+        return -1;
+    for (int64_t i = 0; i < (int64_t)B * T_out; ++i)
+        if (pos[i] < 0 || pos[i] >= T_kv)
+            return -1;
+    const int group = Hq / Hkv;
+    const int64_t kv_row = (int64_t)Hkv * d;
+    memset(dqc_raw, 0, sizeof(double) * (size_t)B * T_out * Hq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * T_kv * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * T_kv * Hkv * d);
+    memset(dalpha_c, 0, sizeof(double) * (size_t)Hq * d);
+    memset(dbeta_c, 0, sizeof(double) * (size_t)Hq * d);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dq = (double *)malloc(sizeof(double) * (size_t)d);
+        double *p = (double *)malloc(sizeof(double) * (size_t)T_kv);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)T_kv);
+        if (!q || !dq || !p || !dp) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int g = 0; g < Hkv; ++g)
+                for (int64_t b = 0; b < B; ++b)
+                    for (int64_t i = 0; i < T_out; ++i)
+                        for (int hh = 0; hh < group; ++hh) {
+                            const int h = g * group + hh;
+                            const int64_t n = (int64_t)pos[b * T_out + i] + 1; /* keys 0..pos */
+                            const uint16_t *xr = qc_raw + ((b * T_out + i) * Hq + h) * d;
+                            const uint16_t *gr = dOc + ((b * T_out + i) * Hq + h) * d;
+                            const uint16_t *kb = k + (b * T_kv * Hkv + g) * d;
+                            const uint16_t *vb = v + (b * T_kv * Hkv + g) * d;
+                            scale_offset_row(xr, alpha_c + (int64_t)h * d, beta_c + (int64_t)h * d, d, q);
+                            double m = -INFINITY;
+                            for (int64_t j = 0; j < n; ++j) {
+                                const uint16_t *kj = kb + j * kv_row;
+                                double s = 0.0;
+                                for (int e = 0; e < d; ++e)
+                                    s += q[e] * bf16_to_double(kj[e]);
+                                p[j] = s * scale;
+                                if (p[j] > m)
+                                    m = p[j];
+                            }
+                            double den = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                p[j] = exp(p[j] - m);
+                                den += p[j];
+                            }
+                            double D = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                p[j] /= den;
+                                const uint16_t *vj = vb + j * kv_row;
+                                double acc = 0.0;
+                                for (int e = 0; e < d; ++e)
+                                    acc += bf16_to_double(gr[e]) * bf16_to_double(vj[e]);
+                                dp[j] = acc;
+                                D += p[j] * acc;
+                            }
+                            for (int e = 0; e < d; ++e)
+                                dq[e] = 0.0;
+                            for (int64_t j = 0; j < n; ++j) {
+                                const double ds = p[j] * (dp[j] - D);
+                                const uint16_t *kj = kb + j * kv_row;
+                                double *dkj = dk + ((b * T_kv + j) * Hkv + g) * d;
+                                double *dvj = dv + ((b * T_kv + j) * Hkv + g) * d;
+                                for (int e = 0; e < d; ++e) {
+                                    dq[e] += scale * ds * bf16_to_double(kj[e]);
+                                    dkj[e] += scale * ds * q[e];
+                                    dvj[e] += p[j] * bf16_to_double(gr[e]);
+                                }
+                            }
+                            double *dxr = dqc_raw + ((b * T_out + i) * Hq + h) * d;
+                            for (int e = 0; e < d; ++e) {
+                                dxr[e] = dq[e] * (double)alpha_c[(int64_t)h * d + e];
+                                dalpha_c[(int64_t)h * d + e] += bf16_to_double(xr[e]) * dq[e];
+                                dbeta_c[(int64_t)h * d + e] += dq[e];
+                            }
+                        }
+        }
+        free(q);
+        free(dq);
+        free(p);
+        free(dp);
+    }
+    return bad ? -2 : 0;
+}

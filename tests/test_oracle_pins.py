@@ -447,3 +447,95 @@ def test_swa_gradient_window_one():
     np.testing.assert_array_equal(dv, g)
     for z in (dq, dk, da, db):
         assert not z.any()
+
+
+# ---------------------------------------------------------------- gradient of Eq. (5)
+
+def _autograd_xattn_grads(qc, pos, k, v, a, b, dOc, scale):
+    """Library reference: torch autograd through float64 SDPA where copy i sees keys
+    0..pos[b, i], with the copies' scale-offset, for the loss sum(dOc * oc)."""
+    B, T_out, Hq, d = qc.shape
+    T_kv, Hkv = k.shape[1], k.shape[2]
+    x = torch.from_numpy(_w(qc)).requires_grad_(True)
+    kk = torch.from_numpy(_w(k)).requires_grad_(True)
+    vv = torch.from_numpy(_w(v)).requires_grad_(True)
+    al = torch.from_numpy(a.astype(np.float64)).requires_grad_(True)
+    be = torch.from_numpy(b.astype(np.float64)).requires_grad_(True)
+    qq = x * al + be
+    kq = kk.repeat_interleave(Hq // Hkv, dim=2)
+    vq = vv.repeat_interleave(Hq // Hkv, dim=2)
+    mask = torch.from_numpy(np.arange(T_kv)[None, None, :] <= pos[:, :, None])  # [B, T_out, T_kv]
+    o = F.scaled_dot_product_attention(qq.transpose(1, 2), kq.transpose(1, 2), vq.transpose(1, 2),
+                                       attn_mask=mask[:, None], scale=scale).transpose(1, 2)
+    (o * torch.from_numpy(_w(dOc))).sum().backward()
+    return [t.grad.numpy() for t in (x, kk, vv, al, be)]
+
+
+@pytest.mark.parametrize("B,T_kv,T_out,Hq,Hkv,d", [
+    (1, 9, 3, 1, 1, 8), (2, 40, 6, 4, 2, 16), (1, 70, 11, 8, 2, 32), (2, 25, 25, 4, 1, 8),
+])
+def test_xattn_gradient_equals_autograd(B, T_kv, T_out, Hq, Hkv, d):
+    """Shuffled positions with duplicates, position 0 and the last position included."""
+    _, k, v, _, _ = _rand_inputs(80 + T_kv, B, T_kv, Hq, Hkv, d)
+    qc = normal_bf16(80 + T_kv, "qc_raw", (B, T_out, Hq, d))
+    a, b = scale_offset(80 + T_kv, Hq, d, prefix="_c")
+    g = np.random.default_rng(T_kv)
+    pos = g.integers(0, T_kv, size=(B, T_out)).astype(np.int32)
+    pos[:, 0] = 0
+    pos[:, -1] = T_kv - 1
+    if T_out > 2:
+        pos[:, 1] = pos[:, 2]
+    dOc = normal_bf16(80 + T_kv, "dOc", (B, T_out, Hq, d))
+    scale = 1.0 / math.sqrt(d)
+    got = oracle.xattn_bwd(qc, pos, k, v, a, b, dOc, scale)
+    ref = _autograd_xattn_grads(qc, pos, k, v, a, b, dOc, scale)
+    for name, gg, r in zip(("dqc_raw", "dk", "dv", "dalpha_c", "dbeta_c"), got, ref):
+        np.testing.assert_allclose(gg, r, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_xattn_gradient_of_a_copy_at_every_position_is_the_causal_gradient():
+    """Copies of every row in order, with the base query, scale-offset and output gradient,
+    see exactly what base rows see when w >= T (Eq. (5) at pos = t is Eq. (4) with the
+    window open), so the two gradients coincide."""
+    B, T, Hq, Hkv, d = 2, 30, 4, 2, 16
+    q, k, v, a, b = _rand_inputs(90, B, T, Hq, Hkv, d)
+    dO = normal_bf16(90, "dO", (B, T, Hq, d))
+    pos = np.tile(np.arange(T, dtype=np.int32), (B, 1))
+    scale = 0.2
+    base = oracle.swa_bwd(q, k, v, a, b, dO, T, scale)
+    copy = oracle.xattn_bwd(q, pos, k, v, a, b, dO, scale)
+    for name, x, y in zip(("dq_raw", "dk", "dv", "dalpha", "dbeta"), copy, base):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-13, err_msg=name)
+
+
+def test_xattn_gradient_in_values_is_exact_finite_difference():
+    B, T_kv, T_out, Hq, Hkv, d = 1, 14, 4, 2, 1, 8
+    _, k, v, _, _ = _rand_inputs(91, B, T_kv, Hq, Hkv, d)
+    qc = normal_bf16(91, "qc_raw", (B, T_out, Hq, d))
+    a, b = scale_offset(91, Hq, d, prefix="_c")
+    pos = np.array([[13, 2, 7, 7]], np.int32)
+    dOc = normal_bf16(91, "dOc", (B, T_out, Hq, d))
+    scale = 1.0 / math.sqrt(d)
+    dv = oracle.xattn_bwd(qc, pos, k, v, a, b, dOc, scale)[2]
+    L0 = (oracle.xattn(qc, pos, k, v, a, b, scale) * _w(dOc)).sum()
+    for (j, e) in [(0, 0), (2, 5), (7, 1), (13, 7)]:
+        v2 = v.copy()
+        v2[0, j, 0, e] = np.uint16(int(v2[0, j, 0, e]) + 1)
+        step = _w(v2)[0, j, 0, e] - _w(v)[0, j, 0, e]
+        L1 = (oracle.xattn(qc, pos, k, v2, a, b, scale) * _w(dOc)).sum()
+        assert abs((L1 - L0) / step - dv[0, j, 0, e]) <= 1e-9 * max(1.0, abs(dv[0, j, 0, e]))
+
+
+def test_xattn_gradient_position_zero():
+    """A copy at position 0 sees only key 0: its output is v_0, so dv_0 gathers its dOc
+    and nothing flows to q', k, alpha' or beta'."""
+    _, k, v, _, _ = _rand_inputs(92, 1, 6, 4, 2, 8)
+    qc = normal_bf16(92, "qc_raw", (1, 3, 4, 8))
+    a, b = scale_offset(92, 4, 8, prefix="_c")
+    dOc = normal_bf16(92, "dOc", (1, 3, 4, 8))
+    pos = np.zeros((1, 3), np.int32)
+    dq, dk, dv, da, db = oracle.xattn_bwd(qc, pos, k, v, a, b, dOc, 0.3)
+    np.testing.assert_array_equal(dv[0, 0], _w(dOc)[0].reshape(3, 2, 2, 8).sum(axis=(0, 2)))
+    assert not dv[0, 1:].any()
+    for z in (dq, dk, da, db):
+        assert not z.any()
