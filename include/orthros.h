@@ -274,10 +274,8 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  * bf16 before they multiply dO, K and q, q rounded once to bf16 in dK.  Three
  * launches: D_t, then dq (rows on the MMA's M side, which also stores each
  * row's log-sum-exp), then dk and dv (keys on the M side, no atomics).
- * Supported: d in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8, 16}; window >= 1
- * with 4*d*(window + 15 + 64/G) + 8*G*d + 1024 <= 232448 (the dq kernel keeps
- * the K/V band of its rows in shared memory; window <= 371 at d = 128, G = 1),
- * else ORTHROS_ERR_UNSUPPORTED.  Outputs must not alias inputs.
+ * Supported: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}; any window >= 1.
+ * Outputs must not alias inputs.
  */
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                const orthros_bf16 *v, const float *alpha, const float *beta,
@@ -285,6 +283,43 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                float *dk, float *dv, float *dalpha, float *dbeta, int B, int T,
                                int Hq, int Hkv, int d, int window, float scale, void *workspace,
                                size_t ws_bytes, void *stream);
+
+/*
+ * Bytes of device workspace orthros_xattn_bwd needs (two fp32 values per copy
+ * row).  Returns 0 for invalid sizes.
+ */
+size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d);
+
+/*
+ * Gradient of the output copies (Eq. (5) with the copies' scale-offset), the
+ * second half of a training step's attention gradient.  With p_ij the weight of
+ * base key j (0 <= j <= pos_i) for copy row i and q'_i = Q'_raw[i]*alpha'+beta':
+ *   dp_ij = dOc_i . v_j,  D_i = dOc_i . oc_i,  ds_ij = p_ij (dp_ij - D_i)
+ *   dq'_i = scale * sum_j ds_ij k_j         dqc_raw_i = dq'_i * alpha'
+ *   dk_j  = scale * sum_i ds_ij q'_i        dv_j = sum_i p_ij dOc_i
+ *   dalpha' = sum_i Q'_raw[i] * dq'_i       dbeta' = sum_i dq'_i
+ * Copies own no K/V, so their gradient reaches the base K and V only: with
+ * accumulate != 0 the copies' share is ADDED to dk and dv (e.g. after
+ * orthros_swa_bwd filled them); with accumulate == 0 they are overwritten.
+ *
+ *   qc_raw, oc, dOc [B, T_out, Hq, d] bf16, dense; pos [B, T_out] int32
+ *   k, v [B, T_kv, Hkv, d] bf16, dense; alpha_c, beta_c [Hq, d] fp32
+ *   dqc_raw [B, T_out, Hq, d], dk, dv [B, T_kv, Hkv, d], dalpha_c, dbeta_c
+ *   [Hq, d]: fp32 outputs (dalpha_c and dbeta_c are zeroed first)
+ *   workspace: orthros_xattn_bwd_workspace_size(...) bytes, 16-byte aligned.
+ * A copy whose position is outside [0, T_kv) gets a zero row of dqc_raw,
+ * contributes nothing, and sets ORTHROS_DEVERR_POSITION in *dev_err.
+ * Arithmetic and launches as orthros_swa_bwd.  T_out == 0 leaves dk, dv as
+ * they are (accumulate) or zero.  Outputs must not alias inputs.
+ */
+orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
+                                 const orthros_bf16 *k, const orthros_bf16 *v,
+                                 const float *alpha_c, const float *beta_c,
+                                 const orthros_bf16 *oc, const orthros_bf16 *dOc,
+                                 float *dqc_raw, float *dk, float *dv, float *dalpha_c,
+                                 float *dbeta_c, int B, int T_out, int T_kv, int Hq, int Hkv,
+                                 int d, float scale, int accumulate, void *workspace,
+                                 size_t ws_bytes, int32_t *dev_err, void *stream);
 
 #ifdef __cplusplus
 }

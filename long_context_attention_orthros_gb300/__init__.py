@@ -10,6 +10,7 @@ CUDA kernels.  PyTorch provides device memory and the current stream.
 * :func:`prefill_fwd`  -- both of them for one prefill layer in one call
 * :func:`decode_step`  -- one fused decode step with KV-cache append
 * :func:`swa_bwd`      -- gradient of the base stream (Eq. (4) and its scale-offset)
+* :func:`xattn_bwd`    -- gradient of the output copies (Eq. (5)), added into dK / dV
 
 If the library is missing these functions raise; there is no fallback.
 """
@@ -29,6 +30,8 @@ from ._binding import (  # noqa: F401
     swa_bwd_workspace_size,
     swa_fwd,
     swa_fwd_rows,
+    xattn_bwd,
+    xattn_bwd_workspace_size,
     xattn_fwd,
     xattn_workspace_size,
 )

@@ -72,6 +72,11 @@ def lib() -> ctypes.CDLL:
             L.orthros_swa_bwd.restype = I
             L.orthros_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, SZ,
                                           P]
+            L.orthros_xattn_bwd_workspace_size.restype = SZ
+            L.orthros_xattn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+            L.orthros_xattn_bwd.restype = I
+            L.orthros_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I,
+                                            P, SZ, P, P]
             _lib = L
     return _lib
 
@@ -273,6 +278,53 @@ def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, work
                                    int(window), _scale(scale, d), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(k.device))
     _check(st, "orthros_swa_bwd")
+    return dq, dk, dv, dalpha, dbeta
+
+
+def xattn_bwd_workspace_size(B, T_out, T_kv, Hq, Hkv, d) -> int:
+    return int(lib().orthros_xattn_bwd_workspace_size(B, T_out, T_kv, Hq, Hkv, d))
+
+
+def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, dOc, scale=None, dk=None, dv=None, workspace=None,
+              dev_err=None):
+    """Gradient of Eq. (5) with the copies' scale-offset: returns fp32 (dqc_raw, dk, dv, dalpha_c,
+    dbeta_c).  Passing dk, dv (fp32 [B, T_kv, Hkv, d], e.g. from swa_bwd) adds the copies' share
+    to them in place; otherwise fresh tensors hold the copies' share alone.  qc_raw, oc, dOc
+    [B, T_out, Hq, d] and k, v [B, T_kv, Hkv, d] dense bf16; pos int32 [B, T_out]."""
+    B, T_kv, Hkv, d = k.shape
+    T_out, Hq = qc_raw.shape[1], qc_raw.shape[2]
+    for t, nm, shp in ((qc_raw, "qc_raw", (B, T_out, Hq, d)), (oc, "oc", (B, T_out, Hq, d)),
+                       (dOc, "dOc", (B, T_out, Hq, d)), (k, "k", (B, T_kv, Hkv, d)), (v, "v", (B, T_kv, Hkv, d))):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shp or not t.is_contiguous():
+            raise OrthrosError(f"{nm} must be a contiguous bf16 CUDA tensor {shp}")
+    if pos.dtype != torch.int32 or tuple(pos.shape) != (B, T_out) or not pos.is_contiguous():
+        raise OrthrosError("pos must be a contiguous int32 tensor [B, T_out]")
+    _vec(alpha_c, "alpha_c", Hq, d)
+    _vec(beta_c, "beta_c", Hq, d)
+    f32 = dict(dtype=torch.float32, device=k.device)
+    accumulate = dk is not None
+    if (dk is None) != (dv is None):
+        raise OrthrosError("pass both dk and dv, or neither")
+    for t, nm in ((dk, "dk"), (dv, "dv")):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (B, T_kv, Hkv, d)
+                              or not t.is_contiguous()):
+            raise OrthrosError(f"{nm} must be a contiguous fp32 tensor [B, T_kv, Hkv, d]")
+    if not accumulate:
+        dk = torch.empty((B, T_kv, Hkv, d), **f32)
+        dv = torch.empty((B, T_kv, Hkv, d), **f32)
+    dq = torch.empty((B, T_out, Hq, d), **f32)
+    dalpha = torch.empty((Hq, d), **f32)
+    dbeta = torch.empty((Hq, d), **f32)
+    if workspace is None:
+        workspace = torch.empty(max(xattn_bwd_workspace_size(B, T_out, T_kv, Hq, Hkv, d), 256), dtype=torch.uint8,
+                                device=k.device)
+    with torch.cuda.device(k.device):
+        st = lib().orthros_xattn_bwd(_ptr(qc_raw), _ptr(pos), _ptr(k), _ptr(v), _ptr(alpha_c), _ptr(beta_c),
+                                     _ptr(oc), _ptr(dOc), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta),
+                                     B, T_out, T_kv, Hq, Hkv, d, _scale(scale, d), int(accumulate),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _ptr(dev_err), _stream(k.device))
+    _check(st, "orthros_xattn_bwd")
     return dq, dk, dv, dalpha, dbeta
 
 

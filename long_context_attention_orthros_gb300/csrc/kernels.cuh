@@ -55,22 +55,24 @@ struct DecodeParams {
     float qscale;
 };
 
-// gradient of the base stream (Eq. 4 with its scale-offset); dense [B, T, H, d] rows
-struct SwaBwdParams {
+// gradient of the base stream (Eq. 4) or of the output copies (Eq. 5), each with its
+// scale-offset.  Query rows are "units" (base tokens, or copies) x heads, dense
+// [B, n_units, Hq, d]; K/V dense [B, T_kv, Hkv, d].  A unit's position is the token
+// itself (pos == nullptr) or pos[b * n_units + u]; it sees keys pos-window+1 .. pos.
+struct AttnBwdParams {
     const orthros_bf16 *q, *k, *v, *o, *dO;  // q raw, the forward output o, its gradient dO
     const float *alpha, *beta;
-    float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta accumulated (zeroed first)
-    float *lse, *Drow;                       // workspace [B*T*Hq] each: log2-sum-exp, dO . o
-    long long q_bstride, kv_bstride, o_bstride;  // batch strides in elements (q/o/dO share o_bstride for dO)
-    int B, T, Hq, Hkv, window;
-    int band_max;                            // K/V rows the dQ kernel stages per CTA (swa_bwd_band_max)
+    const int32_t *pos;                      // copies' original positions, or nullptr (base)
+    float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta zeroed first
+    float *lse, *Drow;                       // workspace [B*n_units*Hq] each: log2-sum-exp, dO . o
+    int32_t *dev_err;
+    int B, n_units, T_kv, Hq, Hkv, window;   // window = T_kv for the copies
+    int accumulate;                          // add to dk, dv instead of overwriting them
     float scale;
 };
 
-int swa_bwd_band_max(int G, int window);
-size_t swa_bwd_workspace_floats(int B, int T, int Hq);
-bool swa_bwd_supported(int D, int G, int window);
-cudaError_t launch_swa_bwd(int D, int G, const SwaBwdParams &p, cudaStream_t stream);
+size_t attn_bwd_workspace_floats(int B, int n_units, int Hq);
+cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);

@@ -315,7 +315,7 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
 {
     if (B < 1 || T < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return sizeof(float) * orthros::swa_bwd_workspace_floats(B, T, Hq);
+    return sizeof(float) * orthros::attn_bwd_workspace_floats(B, T, Hq);
 }
 
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
@@ -327,13 +327,12 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
         !aligned16(o) || !aligned16(dO) || !aligned16(dq_raw) || !aligned16(dk) || !aligned16(dv) ||
         !aligned16(dalpha) || !aligned16(dbeta) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
         return ORTHROS_ERR_INVALID_ARG;
-    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv) || !orthros::swa_bwd_supported(d, Hq / Hkv, window))
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return ORTHROS_ERR_UNSUPPORTED;
     const size_t need = orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d);
     if (!aligned16(workspace) || ws_bytes < need)
         return ORTHROS_ERR_WORKSPACE;
-    const int G = Hq / Hkv;
-    orthros::SwaBwdParams p{};
+    orthros::AttnBwdParams p{};
     p.q = q_raw;
     p.k = k;
     p.v = v;
@@ -341,6 +340,7 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.dO = dO;
     p.alpha = alpha;
     p.beta = beta;
+    p.pos = nullptr;
     p.dq = dq_raw;
     p.dk = dk;
     p.dv = dv;
@@ -348,17 +348,68 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.dbeta = dbeta;
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
-    p.q_bstride = static_cast<long long>(T) * Hq * d;
-    p.kv_bstride = static_cast<long long>(T) * Hkv * d;
-    p.o_bstride = p.q_bstride;
     p.B = B;
-    p.T = T;
+    p.n_units = T;
+    p.T_kv = T;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.window = window;
-    p.band_max = orthros::swa_bwd_band_max(G, window);
+    p.accumulate = 0;
     p.scale = scale;
-    const cudaError_t e = orthros::launch_swa_bwd(d, G, p, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T_out < 0 || T_kv < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    return T_out == 0 ? 256 : sizeof(float) * orthros::attn_bwd_workspace_floats(B, T_out, Hq);
+}
+
+orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
+                                 const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
+                                 const orthros_bf16 *oc, const orthros_bf16 *dOc, float *dqc_raw, float *dk, float *dv,
+                                 float *dalpha_c, float *dbeta_c, int B, int T_out, int T_kv, int Hq, int Hkv, int d,
+                                 float scale, int accumulate, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                 void *stream)
+{
+    if ((T_out > 0 && (!aligned16(qc_raw) || !pos || !aligned16(oc) || !aligned16(dOc) || !aligned16(dqc_raw))) ||
+        !aligned16(k) || !aligned16(v) || !aligned16(alpha_c) || !aligned16(beta_c) || !aligned16(dk) ||
+        !aligned16(dv) || !aligned16(dalpha_c) || !aligned16(dbeta_c) || B < 1 || T_out < 0 || T_kv < 1 ||
+        !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return ORTHROS_ERR_UNSUPPORTED;
+    const size_t need = orthros_xattn_bwd_workspace_size(B, T_out, T_kv, Hq, Hkv, d);
+    if (!aligned16(workspace) || ws_bytes < need)
+        return ORTHROS_ERR_WORKSPACE;
+    orthros::AttnBwdParams p{};
+    p.q = qc_raw;
+    p.k = k;
+    p.v = v;
+    p.o = oc;
+    p.dO = dOc;
+    p.alpha = alpha_c;
+    p.beta = beta_c;
+    p.pos = pos ? pos : reinterpret_cast<const int32_t *>(workspace);  // T_out == 0: never read
+    p.dq = dqc_raw;
+    p.dk = dk;
+    p.dv = dv;
+    p.dalpha = dalpha_c;
+    p.dbeta = dbeta_c;
+    p.lse = static_cast<float *>(workspace);
+    p.Drow = p.lse + static_cast<size_t>(B) * T_out * Hq;
+    p.dev_err = dev_err;
+    p.B = B;
+    p.n_units = T_out;
+    p.T_kv = T_kv;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = T_kv;
+    p.accumulate = accumulate ? 1 : 0;
+    p.scale = scale;
+    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 

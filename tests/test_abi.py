@@ -117,6 +117,23 @@ def test_swa_bwd_workspace_size_and_checks(L):
     assert call(q=None) == 1
     assert call(w=0) == 1
     assert call(d=96) == 2
-    assert call(w=4096) == 2   # the K/V band of a dq tile no longer fits shared memory
+    assert call(q=ctypes.c_void_p(p.value + 4)) == 1  # misaligned
+
+
+def test_xattn_bwd_workspace_size_and_checks(L):
+    p, _keep = _aligned_dummy()
+    n = L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 128)
+    assert n == 2 * 4 * 4 * 2048 * 32
+    assert L.orthros_xattn_bwd_workspace_size(4, 2048, 0, 32, 8, 128) == 0
+    assert L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 96) == 0
+
+    def call(ws=p, nbytes=n, pos=p, T_out=2048, Hkv=8):
+        return L.orthros_xattn_bwd(p, pos, p, p, p, p, p, p, p, p, p, p, p, 4, T_out, 16384, 32, Hkv, 128,
+                                   ctypes.c_float(0.1), 1, ws, nbytes, None, None)
+    assert call(pos=None) == 1
+    assert call(T_out=-1) == 1
+    assert call(Hkv=5) == 2
+    assert call(ws=None) == 3
+    assert call(nbytes=n - 4) == 3
     assert call(ws=None) == 3
     assert call(nbytes=n - 4) == 3
