@@ -356,7 +356,7 @@ def run_gpu(args):
     # ---- base-stream gradient on the same inputs (training modes)
     bwd = None
     if not args.no_bwd:
-        bwd = run_bwd(dev, world, g, o, cfg, _tf_peak, peak_kind)
+        bwd = run_bwd(dev, world, g, o, oc, cfg, _tf_peak, peak_kind)
 
     del g, o, oc, ws
     line = {
@@ -412,20 +412,28 @@ def swa_pairs(B, T, Hq, w) -> int:
     return B * Hq * (n * (n + 1) // 2 + (T - n) * w)
 
 
-def run_bwd(dev, world, g, o, cfg, tf_peak, peak_kind, calls: int = 5):
-    """orthros_swa_bwd on the prefill inputs with a seeded N(0, 1) output gradient."""
+def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
+    """The layer's attention gradient on the prefill inputs with seeded N(0, 1) output
+    gradients: orthros_swa_bwd (base stream), then orthros_xattn_bwd adding the copies'
+    share into the same dK / dV."""
     import torch
     import long_context_attention_orthros_gb300 as orth
-    B, T, Hq, Hkv, d = cfg.B, cfg.T, cfg.Hq, cfg.Hkv, cfg.d
+    B, T, Hq, Hkv, d, T_out = cfg.B, cfg.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.T_out
     gen = torch.Generator(device=dev)
     gen.manual_seed(SEEDS[cfg.name] + 17)
     dO = torch.randn((B, T, Hq, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dOc = torch.randn((B, T_out, Hq, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
     ws = torch.empty(orth.swa_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    wsc = torch.empty(orth.xattn_bwd_workspace_size(B, T_out, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    qc = g["qc"].contiguous()
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        return orth.swa_bwd(g["q"], g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
+        base = orth.swa_bwd(g["q"], g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
                             scale=cfg.scale, workspace=ws)
+        copy = orth.xattn_bwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], oc, dOc, scale=cfg.scale,
+                              dk=base[1], dv=base[2], workspace=wsc)
+        return base + copy
 
     for _ in range(3):
         grads = call()
@@ -438,15 +446,18 @@ def run_bwd(dev, world, g, o, cfg, tf_peak, peak_kind, calls: int = 5):
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
-    del grads, dO, ws
+    del grads, dO, dOc, ws, wsc
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
-    flops = 10 * d * swa_pairs(B, T, Hq, cfg.window)
+    pos = g["pos"].cpu().numpy().astype(np.int64)
+    pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
+    flops = 10 * d * pairs
     tfs = flops / (ms / 1e3) / 1e12
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
-            "roofline": {"kernel": "swa_bwd (3 launches)", "bound": "tensor", "achieved": tfs,
+            "what": "swa_bwd + xattn_bwd (copies' share added into dK/dV)",
+            "roofline": {"kernel": "attn_bwd (6 launches)", "bound": "tensor", "achieved": tfs,
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
                          "peak_kind": peak_kind, "algorithmic_flops": flops},
-            "gpu_launches": 3 * calls}
+            "gpu_launches": 6 * calls}
 
 
 def run_decode(args, dev, world, hbm_peak, peak_kind):
