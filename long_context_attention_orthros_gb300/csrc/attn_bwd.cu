@@ -25,6 +25,7 @@
 // products as bf16, and q enters dK as its bf16 high part.  Outputs are fp32.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc.cuh"
 #include "xattn.cuh"
 
 namespace orthros {
@@ -535,6 +536,786 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const AttnBwdParams p
     }
 }
 
+// ------------------------------------------------------------------ dK, dV on tcgen05
+
+// A CTA owns 128 keys of one (batch, KV head): the MMA's M side, K and V resident in
+// shared memory (one TMA load each).  The query rows that can see them stream through
+// a three-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
+// lands them): per round
+//   S^T  = K q^T          (q as bf16 high part + residual: two products into one fp32 sum)
+//   dP^T = V dO^T         fp32 in tensor memory (two buffers each)
+//   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), both
+//          written back over S^T / dP^T as bf16 by the softmax warps (lane = key)
+//   dV  += P^T dO,  dK += dS^T q_high      (A from tensor memory, B = the row tiles)
+// and dK, dV (fp32, tensor memory) leave once at the end.  The MMA issuer computes S^T,
+// dP^T of round i + 1 while the softmax works on round i.
+// Roles (256 threads, one CTA per SM):
+//   warp 0      TMA producer (K, V once; q raw and dO per round)
+//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
+//   warps 2-3   turn the raw query tile into q = x alpha + beta (bf16 high part in place,
+//               residual beside it) and stage each row's lse, D and position
+//   warps 4-7   P^T, dS^T (tensor-memory lane = key), then the dK / dV epilogue
+// Tensor memory: S^T at 64 u, dP^T at 128 + 64 u (buffer u), dK at 256, dV at 256 + D.
+// Every wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and every role drains
+// to the common exit, where tensor memory is released.
+template <int D>
+struct BtCfg {
+    static constexpr int KEYS = 128;          // keys of a CTA (the MMA's M)
+    static constexpr int RB = 64;             // query rows per round (N of S^T, dP^T)
+    static constexpr int SLABS = D / 64;
+    static constexpr int STG = 3;
+    static constexpr int KSLAB = KEYS * 128;  // one 64-wide slab of the K (or V) tile
+    static constexpr int RSLAB = RB * 128;    // one 64-wide slab of a row tile
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + SLABS * KSLAB;
+    static constexpr int ST_OFF = V_OFF + SLABS * KSLAB;
+    static constexpr int ST_QH = 0;                   // raw x, then q high part
+    static constexpr int ST_QL = SLABS * RSLAB;       // q residual
+    static constexpr int ST_DO = 2 * SLABS * RSLAB;   // dO
+    static constexpr int ST_BYTES = 3 * SLABS * RSLAB;
+    static constexpr int META_OFF = ST_OFF + STG * ST_BYTES;  // [STG][3][RB]: lse, D, position
+    static constexpr int BAR_OFF = META_OFF + STG * 3 * RB * 4;
+    static constexpr int NBARS = 1 + 3 * STG + 3 * 2 + 1;
+    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DK = 256, TM_DV = 256 + D;
+};
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// wait on an mbarrier as a whole warp (lane 0 polls); false after the time limit
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait(bar, parity);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// the next round (of `units` units) at or after r that holds a unit seeing keys >= kt0
+// (copies; base rounds are a contiguous range).  Called by whole warps.
+template <bool COPY>
+__device__ __forceinline__ int next_round(const AttnBwdParams &p, int b, int kt0, int r, int r_end, int units)
+{
+    if (!COPY)
+        return r;
+    const int lane = threadIdx.x & 31;
+    for (; r < r_end; ++r) {
+        bool hit = false;
+        for (int u = lane; u < units; u += 32)
+            hit |= unit_pos<COPY>(p, b, r * units + u) >= kt0;
+        if (__any_sync(0xffffffffu, hit))
+            return r;
+    }
+    return r_end;
+}
+
+template <int D, int G, bool COPY>
+__global__ void __launch_bounds__(256, 1)
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                           const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           const AttnBwdParams p)
+{
+    using C = BtCfg<D>;
+    constexpr int UNITS = C::RB / G;  // units per round
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *kv_full = bars;                     // K, V landed
+    uint64_t *st_full = bars + 1;                 // [STG] row tiles landed
+    uint64_t *qconv = bars + 1 + C::STG;          // [STG] q prepared, row metadata staged
+    uint64_t *st_empty = bars + 1 + 2 * C::STG;   // [STG] round's MMAs done with the stage
+    uint64_t *s_full = bars + 1 + 3 * C::STG;     // [2] S^T, dP^T of a round complete
+    uint64_t *p_full = s_full + 2;                // [2] P^T, dS^T written
+    uint64_t *pv_done = s_full + 4;               // [2] dV, dK of a round issued and complete
+    uint64_t *acc_final = s_full + 6;             // dV, dK of the last round complete
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
+    float *meta = reinterpret_cast<float *>(smem + C::META_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt0 = blockIdx.x * C::KEYS, bh = blockIdx.y;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+    // rounds r cover units r*UNITS .. r*UNITS+UNITS-1
+    const int r_begin = COPY ? 0 : kt0 / UNITS;
+    const int r_end = COPY ? (p.n_units + UNITS - 1) / UNITS
+                           : static_cast<int>((min(static_cast<long long>(p.n_units),
+                                                   static_cast<long long>(kt0) + C::KEYS - 1 + p.window) +
+                                               UNITS - 1) /
+                                              UNITS);
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < C::STG; ++s) {
+            mbar_init(&st_full[s], 1);
+            mbar_init(&qconv[s], 2);
+            mbar_init(&st_empty[s], 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&s_full[u], 1);
+            mbar_init(&p_full[u], 4);
+            mbar_init(&pv_done[u], 1);
+        }
+        mbar_init(acc_final, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1)
+        tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&omap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            mbar_arrive_expect_tx(kv_full, 2 * C::SLABS * C::KSLAB);
+#pragma unroll
+            for (int sl = 0; sl < C::SLABS; ++sl) {
+                tma_load_4d(smem + C::K_OFF + sl * C::KSLAB, &kmap, kv_full, sl * 64, g, kt0, b);
+                tma_load_4d(smem + C::V_OFF + sl * C::KSLAB, &vmap, kv_full, sl * 64, g, kt0, b);
+            }
+        }
+        int i = 0;
+        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
+             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+            const int s = i % C::STG;
+            if (i >= C::STG && !(ok = warp_wait(&st_empty[s], static_cast<uint32_t>(((i / C::STG) - 1) & 1))))
+                break;
+            if (lane == 0) {
+                uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
+                mbar_arrive_expect_tx(&st_full[s], 2 * C::SLABS * C::RSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(st + C::ST_QH + sl * C::RSLAB, &qmap, &st_full[s], sl * 64, g * G, r * UNITS, b);
+                    tma_load_4d(st + C::ST_DO + sl * C::RSLAB, &omap, &st_full[s], sl * 64, g * G, r * UNITS, b);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::RB, true, false);
+        constexpr uint32_t IDESC_ACC = umma_idesc(128, D, true, true);
+        const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF, 16, 1024);
+        const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF, 16, 1024);
+        // dV += P^T dO and dK += dS^T q_high of round j
+        auto accumulate = [&](int j) -> bool {
+            const int u = j & 1, s = j % C::STG;
+            if (!warp_wait(&p_full[u], static_cast<uint32_t>((j >> 1) & 1)))
+                return false;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
+                const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, C::RSLAB, 1024);
+                const uint64_t qdesc = umma_desc_sw128(st + C::ST_QH, C::RSLAB, 1024);
+#pragma unroll
+                for (int kk = 0; kk < C::RB / 16; ++kk) {
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    umma_ts(tbase + C::TM_DV, tbase + C::TM_S + 64 * u + 8 * kk,
+                            odesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_ACC, acc);
+                    umma_ts(tbase + C::TM_DK, tbase + C::TM_DP + 64 * u + 8 * kk,
+                            qdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_ACC, acc);
+                }
+                umma_commit(&pv_done[u]);
+                umma_commit(&st_empty[s]);
+            }
+            __syncwarp();
+            return true;
+        };
+        ok = warp_wait(kv_full, 0);
+        int i = 0;
+        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
+             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+            const int s = i % C::STG, u = i & 1;
+            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1)) &&
+                       warp_wait(&qconv[s], static_cast<uint32_t>((i / C::STG) & 1))))
+                break;
+            // S^T / dP^T buffer u is free once dV, dK of round i - 2 have read P^T, dS^T from it
+            if (i >= 2 && !(ok = warp_wait(&pv_done[u], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
+                break;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
+                const uint64_t qhdesc = umma_desc_sw128(st + C::ST_QH, 16, 1024);
+                const uint64_t qldesc = umma_desc_sw128(st + C::ST_QL, 16, 1024);
+                const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
+                    const uint32_t ro = static_cast<uint32_t>((kk >> 2) * C::RSLAB + (kk & 3) * 32) >> 4;
+                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qhdesc + ro, IDESC_S, kk != 0);
+                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qldesc + ro, IDESC_S, 1u);
+                    umma_ss(tbase + C::TM_DP + 64 * u, vdesc + ko, odesc + ro, IDESC_S, kk != 0);
+                }
+                umma_commit(&s_full[u]);
+            }
+            __syncwarp();
+            if (i >= 1 && !(ok = accumulate(i - 1)))
+                break;
+        }
+        if (ok && i >= 1) {
+            ok = accumulate(i - 1);
+            if (ok && lane == 0)
+                umma_commit(acc_final);
+            __syncwarp();
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ query preparation
+        const int ct = threadIdx.x - 64;  // 0..63
+        int i = 0;
+        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
+             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+            const int s = i % C::STG;
+            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
+                break;
+            uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
+#pragma unroll 2
+            for (int idx = ct; idx < C::RB * C::SLABS * 8; idx += 64) {
+                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
+                const int sl = rem / 8, c8 = rem % 8;
+                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
+                const uint32_t off = sl * C::RSLAB + sw128_offset(row, c8);
+                uint4 *qh = reinterpret_cast<uint4 *>(st + C::ST_QH + off);
+                const uint4 x4 = *qh;
+                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0));
+                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0 + 4));
+                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0));
+                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0 + 4));
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xv = unpack_bf16x2(xw[e]);
+                    split_q_pair(fmaf(xv.x, av[2 * e], bv[2 * e]), fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]), hw[e],
+                                 lw[e]);
+                }
+                *qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(st + C::ST_QL + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            {
+                const int row = ct;  // RB == 64 rows, one per thread
+                const int u = r * UNITS + row / G, h = g * G + row % G;
+                const int P = unit_pos<COPY>(p, b, u);
+                const long long ri = (static_cast<long long>(b) * p.n_units + u) * p.Hq + h;
+                float *m = meta + s * 3 * C::RB;
+                m[row] = P >= 0 ? p.lse[ri] : 0.f;
+                m[C::RB + row] = P >= 0 ? p.Drow[ri] : 0.f;
+                m[2 * C::RB + row] = __int_as_float(P);
+            }
+            fence_proxy_async_smem();  // the MMA reads q through the async proxy
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&qconv[s]);
+        }
+    } else {
+        // ------------------------------------------------------------------ P^T, dS^T + epilogue
+        const int rw = warp - 4;
+        const int key = kt0 + rw * 32 + lane;
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        const float c2 = p.scale * kLog2eF;
+        int i = 0;
+        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
+             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+            const int s = i % C::STG, u = i & 1;
+            if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((i >> 1) & 1)) &&
+                       warp_wait(&qconv[s], static_cast<uint32_t>((i / C::STG) & 1))))
+                break;
+            tc_fence_after();
+            const float *m = meta + s * 3 * C::RB;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
+                tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
+                tmem_wait_ld();
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int c = 32 * half + 2 * e + q;
+                        const int P = __float_as_int(m[2 * C::RB + c]);
+                        const bool valid = key <= P && key >= P - p.window + 1;  // P = -1: none
+                        pr[q] = valid ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - m[c]) : 0.f;
+                        ds[q] = pr[q] * (__uint_as_float(dv[2 * e + q]) - m[C::RB + c]);
+                    }
+                    pw[e] = pack_bf16x2(pr[0], pr[1]);
+                    dw[e] = pack_bf16x2(ds[0], ds[1]);
+                }
+                tmem_st16(tl + C::TM_S + 64 * u + 16 * half, pw);
+                tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&p_full[u]);
+        }
+        // ---- epilogue: dK (scaled), dV of this key -> global (written, or added)
+        const bool have = ok && i > 0;
+        if (have && !(ok = warp_wait(acc_final, 0))) {
+        } else {
+            if (have)
+                tc_fence_after();
+            const long long off =
+                (static_cast<long long>(b) * p.T_kv + key) * p.Hkv * D + static_cast<long long>(g) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t wk[32], wv[32];
+                if (have) {
+                    tmem_ld32(tl + C::TM_DK + c, wk);
+                    tmem_ld32(tl + C::TM_DV + c, wv);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        wk[e] = wv[e] = 0u;
+                }
+                if (key < p.T_kv) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 nk = make_float4(__uint_as_float(wk[e]) * p.scale, __uint_as_float(wk[e + 1]) * p.scale,
+                                                __uint_as_float(wk[e + 2]) * p.scale,
+                                                __uint_as_float(wk[e + 3]) * p.scale);
+                        float4 nv = make_float4(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1]),
+                                                __uint_as_float(wv[e + 2]), __uint_as_float(wv[e + 3]));
+                        float4 *pk = reinterpret_cast<float4 *>(p.dk + off + c + e);
+                        float4 *pv = reinterpret_cast<float4 *>(p.dv + off + c + e);
+                        if (p.accumulate) {
+                            const float4 ok4 = *pk, ov4 = *pv;
+                            nk.x += ok4.x;
+                            nk.y += ok4.y;
+                            nk.z += ok4.z;
+                            nk.w += ok4.w;
+                            nv.x += ov4.x;
+                            nv.y += ov4.y;
+                            nv.z += ov4.z;
+                            nv.w += ov4.w;
+                        }
+                        *pk = nk;
+                        *pv = nv;
+                    }
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// ------------------------------------------------------------------ dQ on tcgen05
+
+// A CTA owns 128 query rows (128/G units x G heads of one KV head): the MMA's M side,
+// q (bf16 high part + residual) and dO resident in shared memory.  The keys its rows see
+// stream through a three-stage TMA ring in blocks of 64, twice:
+//   pass 1  S = q K^T -> per-row running max / sum (lane = row) -> log2-sum-exp, stored
+//           for the dK/dV kernel;
+//   pass 2  S = q K^T, dP = dO V^T (fp32 in tensor memory, two buffers each);
+//           dS = P (dP - D) with P = exp2(S c - lse), written over dP as bf16;
+//           dQ += dS K  (A from tensor memory, B = the key block, MN-major)
+// then dq_raw = scale dQ * alpha, and dalpha / dbeta reduced across the warp's rows of
+// each head and added with global atomics.
+// Roles (256 threads, one CTA per SM): warp 0 TMA producer; warp 1 tensor-memory
+// allocation and MMA issue; warps 2-3 query preparation; warps 4-7 softmax and epilogue.
+// Tensor memory: S at 64 u, dP at 128 + 64 u (buffer u), dQ at 256.
+template <int D>
+struct BqCfg {
+    static constexpr int ROWS = 128;          // query rows of a CTA (the MMA's M)
+    static constexpr int KB = 64;             // keys per block (N of S, dP)
+    static constexpr int SLABS = D / 64;
+    static constexpr int STG = 3;
+    static constexpr int QSLAB = ROWS * 128;
+    static constexpr int KSLAB = KB * 128;
+    static constexpr int QH_OFF = 0;                          // raw x, then q high part
+    static constexpr int QL_OFF = QH_OFF + SLABS * QSLAB;     // q residual
+    static constexpr int DO_OFF = QL_OFF + SLABS * QSLAB;     // dO
+    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;      // [STG] K blocks
+    static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB; // [STG] V blocks
+    static constexpr int RANGE_OFF = V_OFF + STG * SLABS * KSLAB;
+    static constexpr int BAR_OFF = RANGE_OFF + 16;
+    static constexpr int NBARS = 2 + 2 * STG + 3 * 2 + 1;
+    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+};
+
+template <int D, int G, bool COPY>
+__global__ void __launch_bounds__(256, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                          const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const AttnBwdParams p)
+{
+    using C = BqCfg<D>;
+    constexpr int UNITS = C::ROWS / G;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *q_full = bars;                    // raw query and dO tiles landed
+    uint64_t *q_conv = bars + 1;                // q prepared
+    uint64_t *kv_full = bars + 2;               // [STG] key block landed
+    uint64_t *kv_empty = bars + 2 + C::STG;     // [STG] key block released
+    uint64_t *s_full = bars + 2 + 2 * C::STG;   // [2] S (and dP) of a block complete
+    uint64_t *buf_free = s_full + 2;            // [2] S / dP buffer may be overwritten
+    uint64_t *p_full = s_full + 4;              // [2] dS written (pass 2)
+    uint64_t *dq_final = s_full + 6;            // dQ complete
+    int *krange = reinterpret_cast<int *>(smem + C::RANGE_OFF);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u0 = blockIdx.x * UNITS, bh = blockIdx.y;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+
+    // ---- each row's position and the CTA's key range
+    if (threadIdx.x == 0) {
+        krange[0] = 0x7fffffff;
+        krange[1] = -1;
+    }
+    int Prow = -1;
+    if (threadIdx.x < C::ROWS)
+        Prow = unit_pos<COPY>(p, b, u0 + static_cast<int>(threadIdx.x) / G);
+    if (COPY && threadIdx.x < C::ROWS && Prow < 0 && u0 + static_cast<int>(threadIdx.x) / G < p.n_units &&
+        threadIdx.x % G == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
+    const int wlo = __reduce_min_sync(0xffffffffu, Prow >= 0 ? max(0, Prow - p.window + 1) : 0x7fffffff);
+    const int whi = __reduce_max_sync(0xffffffffu, Prow);
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_conv, 2);
+        for (int s = 0; s < C::STG; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&s_full[u], 1);
+            mbar_init(&buf_free[u], 4);
+            mbar_init(&p_full[u], 4);
+        }
+        mbar_init(dq_final, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1)
+        tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    if (lane == 0 && whi >= 0) {
+        atomicMin(&krange[0], wlo);
+        atomicMax(&krange[1], whi);
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_holder;
+    const int kb0 = krange[1] >= 0 ? krange[0] / C::KB : 0;
+    const int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks, each streamed twice
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0 && nb > 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&omap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
+#pragma unroll
+            for (int sl = 0; sl < C::SLABS; ++sl) {
+                tma_load_4d(smem + C::QH_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
+                tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
+            }
+        }
+        for (int n = 0; n < 2 * nb; ++n) {
+            const int slot = n % C::STG, kb = kb0 + n % nb;
+            const bool pass2 = n >= nb;
+            if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&kv_full[slot], (pass2 ? 2 : 1) * C::SLABS * C::KSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(smem + C::K_OFF + (slot * C::SLABS + sl) * C::KSLAB, &kmap, &kv_full[slot], sl * 64, g,
+                                kb * C::KB, b);
+                    if (pass2)
+                        tma_load_4d(smem + C::V_OFF + (slot * C::SLABS + sl) * C::KSLAB, &vmap, &kv_full[slot],
+                                    sl * 64, g, kb * C::KB, b);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, true, false);
+        constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
+        const uint64_t qhdesc = umma_desc_sw128(sbase + C::QH_OFF, 16, 1024);
+        const uint64_t qldesc = umma_desc_sw128(sbase + C::QL_OFF, 16, 1024);
+        const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
+        // dQ += dS K of pass-2 block n
+        auto issue_dq = [&](int n) -> bool {
+            const int u = n & 1, slot = n % C::STG;
+            if (!warp_wait(&p_full[u], static_cast<uint32_t>(((n - nb) >> 1) & 1)))
+                return false;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, C::KSLAB, 1024);
+#pragma unroll
+                for (int kk = 0; kk < C::KB / 16; ++kk)
+                    umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + 64 * u + 8 * kk,
+                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (n > nb || kk > 0) ? 1u : 0u);
+                // buf_free counts 4 arrivals (the four softmax warps in pass 1): here the
+                // commit completes the phase once the dQ MMAs are done, after 3 plain arrivals
+                umma_commit(&buf_free[u]);
+                mbar_arrive_cnt(&buf_free[u], 3);
+                umma_commit(&kv_empty[slot]);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (nb > 0)
+            ok = warp_wait(q_full, 0) && warp_wait(q_conv, 0);
+        for (int n = 0; ok && n < 2 * nb; ++n) {
+            const int slot = n % C::STG, u = n & 1;
+            const bool pass2 = n >= nb;
+            if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
+                break;
+            if (n >= 2 && !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - 2) >> 1) & 1))))
+                break;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
+                const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
+                    umma_ss(tbase + C::TM_S + 64 * u, qhdesc + qo, kdesc + ko, IDESC_S, kk != 0);
+                    umma_ss(tbase + C::TM_S + 64 * u, qldesc + qo, kdesc + ko, IDESC_S, 1u);
+                    if (pass2)
+                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_S, kk != 0);
+                }
+                umma_commit(&s_full[u]);
+                if (!pass2)
+                    umma_commit(&kv_empty[slot]);  // pass 1 reads K only through S
+            }
+            __syncwarp();
+            if (n > nb && !(ok = issue_dq(n - 1)))
+                break;
+        }
+        if (ok && nb > 0) {
+            ok = issue_dq(2 * nb - 1);
+            if (ok && lane == 0)
+                umma_commit(dq_final);
+            __syncwarp();
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ query preparation
+        const int ct = threadIdx.x - 64;  // 0..63
+        if (nb > 0 && (ok = warp_wait(q_full, 0))) {
+#pragma unroll 2
+            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
+                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
+                const int sl = rem / 8, c8 = rem % 8;
+                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
+                const uint32_t off = sl * C::QSLAB + sw128_offset(row, c8);
+                uint4 *qh = reinterpret_cast<uint4 *>(smem + C::QH_OFF + off);
+                const uint4 x4 = *qh;
+                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0));
+                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0 + 4));
+                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0));
+                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0 + 4));
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xv = unpack_bf16x2(xw[e]);
+                    split_q_pair(fmaf(xv.x, av[2 * e], bv[2 * e]), fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]), hw[e],
+                                 lw[e]);
+                }
+                *qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(smem + C::QL_OFF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(q_conv);
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax + epilogue
+        const int rw = warp - 4;
+        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
+        const int P = unit_pos<COPY>(p, b, u0 + r / G);
+        const int lo = P - p.window + 1;
+        const int uu = u0 + r / G, h = g * G + r % G;
+        const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
+        const float Drow = P >= 0 ? p.Drow[ri] : 0.f;
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        const float c2 = p.scale * kLog2eF;
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        float m = NEG_INF, l = 0.f, lse = 0.f;
+        for (int n = 0; ok && n < 2 * nb; ++n) {
+            const int u = n & 1;
+            const bool pass2 = n >= nb;
+            const int k0 = (kb0 + n % nb) * C::KB;
+            if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
+                break;
+            tc_fence_after();
+            if (!pass2) {
+                uint32_t sa[32], sb[32];
+                tmem_ld32(tl + C::TM_S + 64 * u, sa);
+                tmem_ld32(tl + C::TM_S + 64 * u + 32, sb);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&buf_free[u]);  // this warp has read its lanes of S (4 arrivals)
+                float mb = NEG_INF;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int ka = k0 + c, kb = k0 + 32 + c;
+                    const float va = (ka <= P && ka >= lo) ? __uint_as_float(sa[c]) * c2 : NEG_INF;
+                    const float vb = (kb <= P && kb >= lo) ? __uint_as_float(sb[c]) * c2 : NEG_INF;
+                    sa[c] = __float_as_uint(va);
+                    sb[c] = __float_as_uint(vb);
+                    mb = fmax3(mb, va, vb);
+                }
+                const float mn = fmaxf(m, mb);
+                const float z = mn == NEG_INF ? 0.f : mn;
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    acc += fast_exp2(__uint_as_float(sa[c]) - z) + fast_exp2(__uint_as_float(sb[c]) - z);
+                l = l * fast_exp2(m - z) + acc;
+                m = mn;
+                if (n == nb - 1) {
+                    lse = P >= 0 ? m + __log2f(l) : 0.f;  // every valid row holds its own key
+                    if (P >= 0)
+                        p.lse[ri] = lse;
+                }
+            } else {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
+                    tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
+                    tmem_wait_ld();
+                    uint32_t dw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float ds[2];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int key = k0 + 32 * half + 2 * e + q;
+                            const float pr = (key <= P && key >= lo)
+                                                 ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
+                                                 : 0.f;
+                            ds[q] = pr * (__uint_as_float(dv[2 * e + q]) - Drow);
+                        }
+                        dw[e] = pack_bf16x2(ds[0], ds[1]);
+                    }
+                    tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[u]);
+            }
+        }
+        // ---- epilogue: dq_raw = scale dQ alpha; dalpha, dbeta summed over the warp's rows per head
+        const bool have = ok && nb > 0;
+        const bool any_live = __any_sync(0xffffffffu, uu < p.n_units);
+        if (have && !(ok = warp_wait(dq_final, 0))) {
+        } else if (any_live) {
+            if (have)
+                tc_fence_after();
+            const long long off = ri * D;
+            const bool live = uu < p.n_units;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t w[32];
+                if (have) {
+                    tmem_ld32(tl + C::TM_DQ + c, w);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        w[e] = 0u;
+                }
+                float dqv[32], xv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    dqv[e] = __uint_as_float(w[e]) * p.scale;
+                if (live && P >= 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        const uint4 x4 = *reinterpret_cast<const uint4 *>(p.q + off + c + e);
+                        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = unpack_bf16x2(xw[q]);
+                            xv[e + 2 * q] = f.x;
+                            xv[e + 2 * q + 1] = f.y;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        xv[e] = 0.f;
+                }
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 al = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
+                        *reinterpret_cast<float4 *>(p.dq + off + c + e) =
+                            make_float4(dqv[e] * al.x, dqv[e + 1] * al.y, dqv[e + 2] * al.z, dqv[e + 3] * al.w);
+                    }
+                }
+                // rows of one head are the lanes congruent mod G: butterfly over the other bits
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float sa = xv[e] * dqv[e], sb = dqv[e];
+#pragma unroll
+                    for (int o = G; o < 32; o <<= 1) {
+                        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+                        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+                    }
+                    if (lane < G) {
+                        atomicAdd(p.dalpha + h * D + c + e, sa);
+                        atomicAdd(p.dbeta + h * D + c + e, sb);
+                    }
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 size_t attn_bwd_workspace_floats(int B, int n_units, int Hq)
@@ -553,7 +1334,7 @@ static size_t dkv_smem(int D)
 }
 
 template <int D, int G, bool COPY>
-static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, cudaStream_t stream)
+static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
 {
     const long long rows = static_cast<long long>(p.B) * p.n_units * p.Hq;
     cudaError_t e = cudaMemsetAsync(p.dalpha, 0, sizeof(float) * p.Hq * D, stream);
@@ -566,18 +1347,42 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, cudaStream_t stream
                                                                                                 rows);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
-        const size_t s1 = dq_smem(D, G);
-        auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
-        if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
-            cudaSuccess)
-            return e;
-        constexpr int UNITS = BWD_ROWS / G;
-        dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-        k1<<<g1, 128, s1, stream>>>(p);
+        // base rows see at most window + 128/G keys, too few blocks to fill the tensor-memory
+        // pipeline of one CTA per SM: the warp-MMA kernel is faster there (measured 1.05 vs
+        // 1.45 ms for a 16K-token, 32/8-head, w = 128 layer); copies see long key ranges
+        if (maps && COPY) {
+            const size_t s1 = BqCfg<D>::SMEM;
+            auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
+            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
+                cudaSuccess)
+                return e;
+            constexpr int UNITS = BqCfg<D>::ROWS / G;
+            dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
+            k1<<<g1, 256, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], p);
+        } else {
+            const size_t s1 = dq_smem(D, G);
+            auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
+            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
+                cudaSuccess)
+                return e;
+            constexpr int UNITS = BWD_ROWS / G;
+            dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
+            k1<<<g1, 128, s1, stream>>>(p);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
     // dk/dv also runs without query rows: it writes (or keeps) zeros
+    if (maps) {
+        const size_t s3 = BtCfg<D>::SMEM;
+        auto k3 = attn_bwd_dkv_tc_kernel<D, G, COPY>;
+        if ((e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3))) !=
+            cudaSuccess)
+            return e;
+        dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
+        k3<<<g3, 256, s3, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        return cudaGetLastError();
+    }
     const size_t s2 = dkv_smem(D);
     auto k2 = attn_bwd_dkv_kernel<D, G, COPY>;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2))) !=
@@ -589,11 +1394,12 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, cudaStream_t stream
 }
 
 template <bool COPY>
-static cudaError_t dispatch_attn_bwd(int D, int G, const AttnBwdParams &p, cudaStream_t stream)
+static cudaError_t dispatch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps,
+                                     cudaStream_t stream)
 {
 #define ORTHROS_BWD_CASE(DD, GG) \
     if (D == DD && G == GG)      \
-        return launch_attn_bwd_t<DD, GG, COPY>(p, stream);
+        return launch_attn_bwd_t<DD, GG, COPY>(p, maps, stream);
     ORTHROS_BWD_CASE(128, 1)
     ORTHROS_BWD_CASE(128, 2)
     ORTHROS_BWD_CASE(128, 4)
@@ -608,9 +1414,9 @@ static cudaError_t dispatch_attn_bwd(int D, int G, const AttnBwdParams &p, cudaS
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, cudaStream_t stream)
+cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
 {
-    return p.pos ? dispatch_attn_bwd<true>(D, G, p, stream) : dispatch_attn_bwd<false>(D, G, p, stream);
+    return p.pos ? dispatch_attn_bwd<true>(D, G, p, maps, stream) : dispatch_attn_bwd<false>(D, G, p, maps, stream);
 }
 
 }  // namespace orthros

@@ -72,7 +72,10 @@ struct AttnBwdParams {
 };
 
 size_t attn_bwd_workspace_floats(int B, int n_units, int Hq);
-cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, cudaStream_t stream);
+// maps (tensor-memory kernels), or nullptr for the warp-MMA ones: [0..3] {q raw, dO} with boxes of
+// 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
+// with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ)
+cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);

@@ -85,6 +85,21 @@ bool resolve_bstride(long long &s, long long dense)
 
 const float kLog2e = 1.4426950408889634f;
 
+// tensor maps of the gradient's kernels: for dK/dV, query rows and their output gradient
+// in rounds of 64 rows (64/G units x G heads) and K, V in blocks of 128 keys; for dQ, tiles
+// of 128 rows and K, V blocks of 64 keys
+bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, int d, int Hq, int Hkv,
+              int n_units, int T_kv, int B)
+{
+    const int G = Hq / Hkv;
+    const long long qs = static_cast<long long>(n_units) * Hq * d, ks = static_cast<long long>(T_kv) * Hkv * d;
+    return make_map(&m[0], q, d, Hq, n_units, B, qs, G, 64 / G) && make_map(&m[1], dO, d, Hq, n_units, B, qs, G, 64 / G) &&
+           make_map(&m[2], k, d, Hkv, T_kv, B, ks, 1, 128) && make_map(&m[3], v, d, Hkv, T_kv, B, ks, 1, 128) &&
+           make_map(&m[4], q, d, Hq, n_units, B, qs, G, 128 / G) &&
+           make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
+           make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64);
+}
+
 }  // namespace
 
 extern "C" {
@@ -356,7 +371,10 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.accumulate = 0;
     p.scale = scale;
-    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, static_cast<cudaStream_t>(stream));
+    CUtensorMap maps[8];
+    if (!bwd_maps(maps, q_raw, dO, k, v, d, Hq, Hkv, T, T, B))
+        return ORTHROS_ERR_CUDA;
+    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
@@ -409,7 +427,11 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.window = T_kv;
     p.accumulate = accumulate ? 1 : 0;
     p.scale = scale;
-    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, static_cast<cudaStream_t>(stream));
+    CUtensorMap maps[8];
+    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
+                  B))
+        return ORTHROS_ERR_CUDA;
+    const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
