@@ -248,8 +248,9 @@ orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16
                                    size_t ws_bytes, int32_t *dev_err, void *stream);
 
 /*
- * Bytes of device workspace orthros_swa_bwd needs (two fp32 values per query
- * row: the row's log-sum-exp and dO . o).  Returns 0 for invalid sizes.
+ * Bytes of device workspace orthros_swa_bwd needs: two fp32 values per query
+ * row (the row's log-sum-exp and dO . o) and an fp16 copy of K.  Returns 0 for
+ * invalid sizes.
  */
 size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
 
@@ -269,11 +270,14 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  *   dq_raw [B, T, Hq, d], dk, dv [B, T, Hkv, d], dalpha, dbeta [Hq, d]: fp32
  *   outputs, every element written (dalpha and dbeta are zeroed first)
  *   workspace: orthros_swa_bwd_workspace_size(...) bytes, 16-byte aligned.
- * Products are bf16 x bf16 with fp32 accumulation: q . k as a bf16 high part
- * plus residual of q (as the forward's wide-window path), P and dS rounded to
- * bf16 before they multiply dO, K and q, q rounded once to bf16 in dK.  Three
- * launches: D_t, then dq (rows on the MMA's M side, which also stores each
- * row's log-sum-exp), then dk and dv (keys on the M side, no atomics).
+ * Products take fp32 accumulation.  q . k: in the dk/dv kernel (tensor memory)
+ * fp16, K converted exactly from bf16 into the workspace and q rounded once to
+ * fp16, as the forward's tensor-memory path (|k| >= 65520 or |q| >= 65504 sets
+ * ORTHROS_DEVERR_RANGE); in the dq kernel a bf16 high part plus residual of q.
+ * P and dS are rounded to bf16 before they multiply dO, K and q; q enters dk
+ * rounded once to bf16.  Launches: the fp16 copy of K, D_t, dq (rows on the
+ * MMA's M side; it also stores each row's log-sum-exp), then dk and dv (keys
+ * on the M side, no atomics).  dev_err (optional) as elsewhere.
  * Supported: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}; any window >= 1.
  * Outputs must not alias inputs.
  */
@@ -282,11 +286,11 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                const orthros_bf16 *o, const orthros_bf16 *dO, float *dq_raw,
                                float *dk, float *dv, float *dalpha, float *dbeta, int B, int T,
                                int Hq, int Hkv, int d, int window, float scale, void *workspace,
-                               size_t ws_bytes, void *stream);
+                               size_t ws_bytes, int32_t *dev_err, void *stream);
 
 /*
  * Bytes of device workspace orthros_xattn_bwd needs (two fp32 values per copy
- * row).  Returns 0 for invalid sizes.
+ * row and an fp16 copy of K).  Returns 0 for invalid sizes.
  */
 size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d);
 
@@ -309,8 +313,10 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
  *   workspace: orthros_xattn_bwd_workspace_size(...) bytes, 16-byte aligned.
  * A copy whose position is outside [0, T_kv) gets a zero row of dqc_raw,
  * contributes nothing, and sets ORTHROS_DEVERR_POSITION in *dev_err.
- * Arithmetic and launches as orthros_swa_bwd.  T_out == 0 leaves dk, dv as
- * they are (accumulate) or zero.  Outputs must not alias inputs.
+ * Arithmetic and launches as orthros_swa_bwd, except that the dq kernel also
+ * runs on tensor memory here (fp16 q . k; copies see long key ranges).
+ * T_out == 0 leaves dk, dv as they are (accumulate) or zero.  Outputs must not
+ * alias inputs.
  */
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  const orthros_bf16 *k, const orthros_bf16 *v,

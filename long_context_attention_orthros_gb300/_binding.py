@@ -71,7 +71,7 @@ def lib() -> ctypes.CDLL:
             L.orthros_swa_bwd_workspace_size.argtypes = [I, I, I, I, I]
             L.orthros_swa_bwd.restype = I
             L.orthros_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, SZ,
-                                          P]
+                                          P, P]
             L.orthros_xattn_bwd_workspace_size.restype = SZ
             L.orthros_xattn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
             L.orthros_xattn_bwd.restype = I
@@ -251,7 +251,7 @@ def swa_bwd_workspace_size(B, T, Hq, Hkv, d) -> int:
     return int(lib().orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d))
 
 
-def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, workspace=None):
+def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, workspace=None, dev_err=None):
     """Gradient of Eq. (4) with its scale-offset: returns fp32 (dq_raw, dk, dv, dalpha, dbeta) for
     the output gradient dO, given the forward inputs and the forward output o.  q_raw, o, dO
     [B, T, Hq, d] and k, v [B, T, Hkv, d], all dense bf16; alpha, beta [Hq, d] fp32."""
@@ -276,7 +276,7 @@ def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, work
         st = lib().orthros_swa_bwd(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o), _ptr(dO),
                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta), B, T, Hq, Hkv, d,
                                    int(window), _scale(scale, d), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(k.device))
+                                   workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(k.device))
     _check(st, "orthros_swa_bwd")
     return dq, dk, dv, dalpha, dbeta
 

@@ -23,6 +23,8 @@
 //                        dV += P^T dO, dK += dS^T q) and writes them once.
 // q . k takes q as a bf16 high part plus residual; P and dS enter the second
 // products as bf16, and q enters dK as its bf16 high part.  Outputs are fp32.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -75,6 +77,31 @@ __device__ __forceinline__ int unit_pos(const AttnBwdParams &p, int b, int u)
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ fp16 copy of K
+
+// The tensor-memory kernels take q . k in fp16 (as the forward's tensor-memory path): K is
+// converted once per call, exactly (|k| < 65520, else ORTHROS_DEVERR_RANGE).
+__global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k, uint16_t *k16, long long n8,
+                                                           int32_t *dev_err)
+{
+    bool bad = false;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(k) + i);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
+            __half2 hv = __floats2half2_rn(f.x, f.y);
+            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+        }
+        reinterpret_cast<uint4 *>(k16)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (bad)
+        record_error(dev_err, ORTHROS_DEVERR_RANGE);
+}
 
 // ------------------------------------------------------------------ D = dO . o
 
@@ -542,18 +569,19 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const AttnBwdParams p
 // shared memory (one TMA load each).  The query rows that can see them stream through
 // a three-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
 // lands them): per round
-//   S^T  = K q^T          (q as bf16 high part + residual: two products into one fp32 sum)
-//   dP^T = V dO^T         fp32 in tensor memory (two buffers each)
+//   S^T  = K q^T          (fp16: K from the call's exact fp16 copy, q rounded once; a
+//                         query outside the fp16 range sets ORTHROS_DEVERR_RANGE)
+//   dP^T = V dO^T         (bf16) fp32 in tensor memory (two buffers each)
 //   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), both
 //          written back over S^T / dP^T as bf16 by the softmax warps (lane = key)
-//   dV  += P^T dO,  dK += dS^T q_high      (A from tensor memory, B = the row tiles)
+//   dV  += P^T dO,  dK += dS^T q           (A from tensor memory, B = the row tiles; q bf16)
 // and dK, dV (fp32, tensor memory) leave once at the end.  The MMA issuer computes S^T,
 // dP^T of round i + 1 while the softmax works on round i.
 // Roles (256 threads, one CTA per SM):
 //   warp 0      TMA producer (K, V once; q raw and dO per round)
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2-3   turn the raw query tile into q = x alpha + beta (bf16 high part in place,
-//               residual beside it) and stage each row's lse, D and position
+//   warps 2-3   per round turn the raw query tile into q = x alpha + beta (fp16 in place,
+//               bf16 beside it) and stage each row's lse, D and position
 //   warps 4-7   P^T, dS^T (tensor-memory lane = key), then the dK / dV epilogue
 // Tensor memory: S^T at 64 u, dP^T at 128 + 64 u (buffer u), dK at 256, dV at 256 + D.
 // Every wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and every role drains
@@ -569,8 +597,8 @@ struct BtCfg {
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + SLABS * KSLAB;
     static constexpr int ST_OFF = V_OFF + SLABS * KSLAB;
-    static constexpr int ST_QH = 0;                   // raw x, then q high part
-    static constexpr int ST_QL = SLABS * RSLAB;       // q residual
+    static constexpr int ST_Q16 = 0;                  // raw x, then q as fp16
+    static constexpr int ST_QB = SLABS * RSLAB;       // q as bf16
     static constexpr int ST_DO = 2 * SLABS * RSLAB;   // dO
     static constexpr int ST_BYTES = 3 * SLABS * RSLAB;
     static constexpr int META_OFF = ST_OFF + STG * ST_BYTES;  // [STG][3][RB]: lse, D, position
@@ -581,6 +609,31 @@ struct BtCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DK = 256, TM_DV = 256 + D;
 };
+
+// q = x alpha + beta for 8 elements of head h at column d0: fp16 and bf16 copies
+__device__ __forceinline__ void scale_offset8(uint4 x4, const float *alpha, const float *beta, int d0, uint4 &q16,
+                                              uint4 &qb, bool &bad)
+{
+    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + d0));
+    const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + d0 + 4));
+    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + d0));
+    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + d0 + 4));
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+    uint32_t hw[4], bw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 xv = unpack_bf16x2(xw[e]);
+        const float qa = fmaf(xv.x, av[2 * e], bv[2 * e]), qc = fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]);
+        bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
+        __half2 hv = __floats2half2_rn(qa, qc);
+        hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+        bw[e] = pack_bf16x2(qa, qc);
+    }
+    q16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    qb = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+}
 
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count)
 {
@@ -697,14 +750,15 @@ __global__ void __launch_bounds__(256, 1)
                 mbar_arrive_expect_tx(&st_full[s], 2 * C::SLABS * C::RSLAB);
 #pragma unroll
                 for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(st + C::ST_QH + sl * C::RSLAB, &qmap, &st_full[s], sl * 64, g * G, r * UNITS, b);
+                    tma_load_4d(st + C::ST_Q16 + sl * C::RSLAB, &qmap, &st_full[s], sl * 64, g * G, r * UNITS, b);
                     tma_load_4d(st + C::ST_DO + sl * C::RSLAB, &omap, &st_full[s], sl * 64, g * G, r * UNITS, b);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = umma_idesc(128, C::RB, true, false);
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::RB, false, false);   // fp16
+        constexpr uint32_t IDESC_DP = umma_idesc(128, C::RB, true, false);   // bf16
         constexpr uint32_t IDESC_ACC = umma_idesc(128, D, true, true);
         const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF, 16, 1024);
         const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF, 16, 1024);
@@ -717,7 +771,7 @@ __global__ void __launch_bounds__(256, 1)
                 tc_fence_after();
                 const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
                 const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, C::RSLAB, 1024);
-                const uint64_t qdesc = umma_desc_sw128(st + C::ST_QH, C::RSLAB, 1024);
+                const uint64_t qdesc = umma_desc_sw128(st + C::ST_QB, C::RSLAB, 1024);
 #pragma unroll
                 for (int kk = 0; kk < C::RB / 16; ++kk) {
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
@@ -746,16 +800,14 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) {
                 tc_fence_after();
                 const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
-                const uint64_t qhdesc = umma_desc_sw128(st + C::ST_QH, 16, 1024);
-                const uint64_t qldesc = umma_desc_sw128(st + C::ST_QL, 16, 1024);
+                const uint64_t qdesc = umma_desc_sw128(st + C::ST_Q16, 16, 1024);
                 const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
                     const uint32_t ro = static_cast<uint32_t>((kk >> 2) * C::RSLAB + (kk & 3) * 32) >> 4;
-                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qhdesc + ro, IDESC_S, kk != 0);
-                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qldesc + ro, IDESC_S, 1u);
-                    umma_ss(tbase + C::TM_DP + 64 * u, vdesc + ko, odesc + ro, IDESC_S, kk != 0);
+                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qdesc + ro, IDESC_S, kk != 0);
+                    umma_ss(tbase + C::TM_DP + 64 * u, vdesc + ko, odesc + ro, IDESC_DP, kk != 0);
                 }
                 umma_commit(&s_full[u]);
             }
@@ -772,8 +824,9 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp < 4) {
         // ------------------------------------------------------------------ query preparation
         const int ct = threadIdx.x - 64;  // 0..63
+        bool bad = false;
         int i = 0;
-        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
+        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
              r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
             const int s = i % C::STG;
             if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
@@ -785,24 +838,11 @@ __global__ void __launch_bounds__(256, 1)
                 const int sl = rem / 8, c8 = rem % 8;
                 const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
                 const uint32_t off = sl * C::RSLAB + sw128_offset(row, c8);
-                uint4 *qh = reinterpret_cast<uint4 *>(st + C::ST_QH + off);
-                const uint4 x4 = *qh;
-                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0));
-                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0 + 4));
-                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0));
-                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0 + 4));
-                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xv = unpack_bf16x2(xw[e]);
-                    split_q_pair(fmaf(xv.x, av[2 * e], bv[2 * e]), fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]), hw[e],
-                                 lw[e]);
-                }
-                *qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(st + C::ST_QL + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                uint4 *qp = reinterpret_cast<uint4 *>(st + C::ST_Q16 + off);
+                uint4 q16, qb;
+                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
+                *qp = q16;
+                *reinterpret_cast<uint4 *>(st + C::ST_QB + off) = qb;
             }
             {
                 const int row = ct;  // RB == 64 rows, one per thread
@@ -819,6 +859,8 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0)
                 mbar_arrive(&qconv[s]);
         }
+        if (bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
         // ------------------------------------------------------------------ P^T, dS^T + epilogue
         const int rw = warp - 4;
@@ -925,15 +967,16 @@ __global__ void __launch_bounds__(256, 1)
 // ------------------------------------------------------------------ dQ on tcgen05
 
 // A CTA owns 128 query rows (128/G units x G heads of one KV head): the MMA's M side,
-// q (bf16 high part + residual) and dO resident in shared memory.  The keys its rows see
-// stream through a three-stage TMA ring in blocks of 64, twice:
+// q (fp16, rounded once) and dO resident in shared memory.  The keys its rows see stream
+// through a three-stage TMA ring in blocks of 64 (K from the call's fp16 copy for S; in
+// pass 2 also K itself, bf16, for dQ, and V), twice:
 //   pass 1  S = q K^T -> per-row running max / sum (lane = row) -> log2-sum-exp, stored
 //           for the dK/dV kernel;
 //   pass 2  S = q K^T, dP = dO V^T (fp32 in tensor memory, two buffers each);
 //           dS = P (dP - D) with P = exp2(S c - lse), written over dP as bf16;
 //           dQ += dS K  (A from tensor memory, B = the key block, MN-major)
-// then dq_raw = scale dQ * alpha, and dalpha / dbeta reduced across the warp's rows of
-// each head and added with global atomics.
+// then dq_raw = scale dQ * alpha, and dalpha / dbeta reduced across the CTA's rows of
+// each head (shuffles, then shared memory) and added with global atomics.
 // Roles (256 threads, one CTA per SM): warp 0 TMA producer; warp 1 tensor-memory
 // allocation and MMA issue; warps 2-3 query preparation; warps 4-7 softmax and epilogue.
 // Tensor memory: S at 64 u, dP at 128 + 64 u (buffer u), dQ at 256.
@@ -945,12 +988,13 @@ struct BqCfg {
     static constexpr int STG = 3;
     static constexpr int QSLAB = ROWS * 128;
     static constexpr int KSLAB = KB * 128;
-    static constexpr int QH_OFF = 0;                          // raw x, then q high part
-    static constexpr int QL_OFF = QH_OFF + SLABS * QSLAB;     // q residual
-    static constexpr int DO_OFF = QL_OFF + SLABS * QSLAB;     // dO
-    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;      // [STG] K blocks
+    static constexpr int Q16_OFF = 0;                         // raw x, then q as fp16
+    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;    // dO
+    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;      // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB; // [STG] V blocks
-    static constexpr int RANGE_OFF = V_OFF + STG * SLABS * KSLAB;
+    static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;   // [STG] K blocks as fp16
+    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB; // [2][16][D] dalpha, dbeta partials
+    static constexpr int RANGE_OFF = RED_OFF + 2 * 16 * D * 4;
     static constexpr int BAR_OFF = RANGE_OFF + 16;
     static constexpr int NBARS = 2 + 2 * STG + 3 * 2 + 1;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
@@ -963,7 +1007,7 @@ template <int D, int G, bool COPY>
 __global__ void __launch_bounds__(256, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                           const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                          const AttnBwdParams p)
+                          const __grid_constant__ CUtensorMap k16map, const AttnBwdParams p)
 {
     using C = BqCfg<D>;
     constexpr int UNITS = C::ROWS / G;
@@ -979,6 +1023,7 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t *buf_free = s_full + 2;            // [2] S / dP buffer may be overwritten
     uint64_t *p_full = s_full + 4;              // [2] dS written (pass 2)
     uint64_t *dq_final = s_full + 6;            // dQ complete
+    float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
     int *krange = reinterpret_cast<int *>(smem + C::RANGE_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
@@ -1014,6 +1059,8 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(dq_final, 1);
         fence_barrier_init();
     }
+    for (int i = threadIdx.x; i < 2 * G * D; i += 256)
+        red[i] = 0.f;
     if (warp == 1)
         tmem_alloc(tmem_holder, 512);
     tc_fence_before();
@@ -1036,10 +1083,11 @@ __global__ void __launch_bounds__(256, 1)
             tma_prefetch_desc(&omap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&k16map);
             mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
 #pragma unroll
             for (int sl = 0; sl < C::SLABS; ++sl) {
-                tma_load_4d(smem + C::QH_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
+                tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
                 tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
             }
         }
@@ -1049,23 +1097,26 @@ __global__ void __launch_bounds__(256, 1)
             if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
                 break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&kv_full[slot], (pass2 ? 2 : 1) * C::SLABS * C::KSLAB);
+                mbar_arrive_expect_tx(&kv_full[slot], (pass2 ? 3 : 1) * C::SLABS * C::KSLAB);
 #pragma unroll
                 for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + C::K_OFF + (slot * C::SLABS + sl) * C::KSLAB, &kmap, &kv_full[slot], sl * 64, g,
-                                kb * C::KB, b);
-                    if (pass2)
+                    tma_load_4d(smem + C::K16_OFF + (slot * C::SLABS + sl) * C::KSLAB, &k16map, &kv_full[slot], sl * 64,
+                                g, kb * C::KB, b);
+                    if (pass2) {
+                        tma_load_4d(smem + C::K_OFF + (slot * C::SLABS + sl) * C::KSLAB, &kmap, &kv_full[slot], sl * 64,
+                                    g, kb * C::KB, b);
                         tma_load_4d(smem + C::V_OFF + (slot * C::SLABS + sl) * C::KSLAB, &vmap, &kv_full[slot],
                                     sl * 64, g, kb * C::KB, b);
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, true, false);
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, false, false);   // fp16
+        constexpr uint32_t IDESC_DP = umma_idesc(128, C::KB, true, false);   // bf16
         constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
-        const uint64_t qhdesc = umma_desc_sw128(sbase + C::QH_OFF, 16, 1024);
-        const uint64_t qldesc = umma_desc_sw128(sbase + C::QL_OFF, 16, 1024);
+        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q16_OFF, 16, 1024);
         const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
         // dQ += dS K of pass-2 block n
         auto issue_dq = [&](int n) -> bool {
@@ -1099,16 +1150,15 @@ __global__ void __launch_bounds__(256, 1)
                 break;
             if (lane == 0) {
                 tc_fence_after();
-                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
+                const uint64_t kdesc = umma_desc_sw128(sbase + C::K16_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
                 const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
                     const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
-                    umma_ss(tbase + C::TM_S + 64 * u, qhdesc + qo, kdesc + ko, IDESC_S, kk != 0);
-                    umma_ss(tbase + C::TM_S + 64 * u, qldesc + qo, kdesc + ko, IDESC_S, 1u);
+                    umma_ss(tbase + C::TM_S + 64 * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
                     if (pass2)
-                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_S, kk != 0);
+                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
                 }
                 umma_commit(&s_full[u]);
                 if (!pass2)
@@ -1127,37 +1177,25 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp < 4) {
         // ------------------------------------------------------------------ query preparation
         const int ct = threadIdx.x - 64;  // 0..63
+        bool bad = false;
         if (nb > 0 && (ok = warp_wait(q_full, 0))) {
 #pragma unroll 2
             for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
                 const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
                 const int sl = rem / 8, c8 = rem % 8;
                 const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
-                const uint32_t off = sl * C::QSLAB + sw128_offset(row, c8);
-                uint4 *qh = reinterpret_cast<uint4 *>(smem + C::QH_OFF + off);
-                const uint4 x4 = *qh;
-                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0));
-                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + d0 + 4));
-                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0));
-                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(p.beta + h * D + d0 + 4));
-                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xv = unpack_bf16x2(xw[e]);
-                    split_q_pair(fmaf(xv.x, av[2 * e], bv[2 * e]), fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]), hw[e],
-                                 lw[e]);
-                }
-                *qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(smem + C::QL_OFF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                uint4 *qp = reinterpret_cast<uint4 *>(smem + C::Q16_OFF + sl * C::QSLAB + sw128_offset(row, c8));
+                uint4 q16, qb;
+                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
+                *qp = q16;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(q_conv);
         }
+        if (bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
         // ------------------------------------------------------------------ softmax + epilogue
         const int rw = warp - 4;
@@ -1299,11 +1337,16 @@ __global__ void __launch_bounds__(256, 1)
                         sb += __shfl_xor_sync(0xffffffffu, sb, o);
                     }
                     if (lane < G) {
-                        atomicAdd(p.dalpha + h * D + c + e, sa);
-                        atomicAdd(p.dbeta + h * D + c + e, sb);
+                        atomicAdd(&red[lane * D + c + e], sa);
+                        atomicAdd(&red[G * D + lane * D + c + e], sb);
                     }
                 }
             }
+        }
+        named_barrier(1, 128);  // every softmax warp reaches this point (all waits are bounded)
+        for (int i = r; i < G * D; i += 128) {
+            atomicAdd(p.dalpha + g * G * D + i, red[i]);
+            atomicAdd(p.dbeta + g * G * D + i, red[G * D + i]);
         }
     }
     if (!ok && lane == 0)
@@ -1318,9 +1361,14 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------------------ host side
 
-size_t attn_bwd_workspace_floats(int B, int n_units, int Hq)
+size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
 {
-    return 2 * static_cast<size_t>(B) * n_units * Hq;
+    return attn_bwd_k16_offset(B, n_units, Hq) + 2 * static_cast<size_t>(B) * T_kv * Hkv * D;
+}
+
+size_t attn_bwd_k16_offset(int B, int n_units, int Hq)
+{
+    return (8 * static_cast<size_t>(B) * n_units * Hq + 255) & ~static_cast<size_t>(255);
 }
 
 static size_t dq_smem(int D, int G)
@@ -1342,6 +1390,13 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         e = cudaMemsetAsync(p.dbeta, 0, sizeof(float) * p.Hq * D, stream);
     if (e != cudaSuccess)
         return e;
+    if (maps) {
+        const long long n8 = static_cast<long long>(p.B) * p.T_kv * p.Hkv * D / 8;
+        attn_bwd_k16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(p.k, p.k16, n8,
+                                                                                                  p.dev_err);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
     if (rows > 0) {
         attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p.o, p.dO, p.Drow,
                                                                                                 rows);
@@ -1358,7 +1413,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                 return e;
             constexpr int UNITS = BqCfg<D>::ROWS / G;
             dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-            k1<<<g1, 256, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], p);
+            k1<<<g1, 256, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
@@ -1380,7 +1435,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             cudaSuccess)
             return e;
         dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-        k3<<<g3, 256, s3, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        k3<<<g3, 256, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
         return cudaGetLastError();
     }
     const size_t s2 = dkv_smem(D);

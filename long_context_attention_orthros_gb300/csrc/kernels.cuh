@@ -65,16 +65,20 @@ struct AttnBwdParams {
     const int32_t *pos;                      // copies' original positions, or nullptr (base)
     float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta zeroed first
     float *lse, *Drow;                       // workspace [B*n_units*Hq] each: log2-sum-exp, dO . o
+    uint16_t *k16;                           // workspace: K as fp16 [B, T_kv, Hkv, d]
     int32_t *dev_err;
     int B, n_units, T_kv, Hq, Hkv, window;   // window = T_kv for the copies
     int accumulate;                          // add to dk, dv instead of overwriting them
     float scale;
 };
 
-size_t attn_bwd_workspace_floats(int B, int n_units, int Hq);
+// workspace: lse, D (fp32 per query row), then at a 256-byte boundary the fp16 copy of K
+size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
+size_t attn_bwd_k16_offset(int B, int n_units, int Hq);
 // maps (tensor-memory kernels), or nullptr for the warp-MMA ones: [0..3] {q raw, dO} with boxes of
 // 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
-// with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ)
+// with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ); [8], [9] the fp16 copy
+// of K (p.k16) with boxes of 128 and of 64 keys
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -87,9 +87,9 @@ const float kLog2e = 1.4426950408889634f;
 
 // tensor maps of the gradient's kernels: for dK/dV, query rows and their output gradient
 // in rounds of 64 rows (64/G units x G heads) and K, V in blocks of 128 keys; for dQ, tiles
-// of 128 rows and K, V blocks of 64 keys
-bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, int d, int Hq, int Hkv,
-              int n_units, int T_kv, int B)
+// of 128 rows and K, V blocks of 64 keys; the fp16 copy of K in blocks of 128 and of 64
+bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16, int d,
+              int Hq, int Hkv, int n_units, int T_kv, int B)
 {
     const int G = Hq / Hkv;
     const long long qs = static_cast<long long>(n_units) * Hq * d, ks = static_cast<long long>(T_kv) * Hkv * d;
@@ -97,7 +97,8 @@ bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, cons
            make_map(&m[2], k, d, Hkv, T_kv, B, ks, 1, 128) && make_map(&m[3], v, d, Hkv, T_kv, B, ks, 1, 128) &&
            make_map(&m[4], q, d, Hq, n_units, B, qs, G, 128 / G) &&
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
-           make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64);
+           make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 128) &&
+           make_map(&m[9], k16, d, Hkv, T_kv, B, ks, 1, 64);
 }
 
 }  // namespace
@@ -330,13 +331,14 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
 {
     if (B < 1 || T < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return sizeof(float) * orthros::attn_bwd_workspace_floats(B, T, Hq);
+    return orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d);
 }
 
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
                                const float *alpha, const float *beta, const orthros_bf16 *o, const orthros_bf16 *dO,
                                float *dq_raw, float *dk, float *dv, float *dalpha, float *dbeta, int B, int T, int Hq,
-                               int Hkv, int d, int window, float scale, void *workspace, size_t ws_bytes, void *stream)
+                               int Hkv, int d, int window, float scale, void *workspace, size_t ws_bytes,
+                               int32_t *dev_err, void *stream)
 {
     if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(o) || !aligned16(dO) || !aligned16(dq_raw) || !aligned16(dk) || !aligned16(dv) ||
@@ -363,6 +365,8 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.dbeta = dbeta;
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
+    p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T, Hq));
+    p.dev_err = dev_err;
     p.B = B;
     p.n_units = T;
     p.T_kv = T;
@@ -371,8 +375,8 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.accumulate = 0;
     p.scale = scale;
-    CUtensorMap maps[8];
-    if (!bwd_maps(maps, q_raw, dO, k, v, d, Hq, Hkv, T, T, B))
+    CUtensorMap maps[10];
+    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, d, Hq, Hkv, T, T, B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
@@ -382,7 +386,7 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
 {
     if (B < 1 || T_out < 0 || T_kv < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return T_out == 0 ? 256 : sizeof(float) * orthros::attn_bwd_workspace_floats(B, T_out, Hq);
+    return orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d);
 }
 
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
@@ -418,6 +422,7 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.dbeta = dbeta_c;
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T_out * Hq;
+    p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T_out, Hq));
     p.dev_err = dev_err;
     p.B = B;
     p.n_units = T_out;
@@ -427,8 +432,8 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.window = T_kv;
     p.accumulate = accumulate ? 1 : 0;
     p.scale = scale;
-    CUtensorMap maps[8];
-    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
+    CUtensorMap maps[10];
+    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
                   B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));

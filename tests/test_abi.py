@@ -107,13 +107,13 @@ def test_decode_workspace_size_and_checks(L):
 def test_swa_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 128)
-    assert n == 2 * 4 * 2 * 1000 * 32
+    assert n == 2 * 4 * 2 * 1000 * 32 + 2 * 2 * 1000 * 8 * 128  # lse, D per row; fp16 K
     assert L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 96) == 0
     assert L.orthros_swa_bwd_workspace_size(0, 1000, 32, 8, 128) == 0
 
     def call(w=128, ws=p, nbytes=n, q=p, d=128):
         return L.orthros_swa_bwd(q, p, p, p, p, p, p, p, p, p, p, p, 2, 1000, 32, 8, d, w,
-                                 ctypes.c_float(0.1), ws, nbytes, None)
+                                 ctypes.c_float(0.1), ws, nbytes, None, None)
     assert call(q=None) == 1
     assert call(w=0) == 1
     assert call(d=96) == 2
@@ -123,7 +123,7 @@ def test_swa_bwd_workspace_size_and_checks(L):
 def test_xattn_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 128)
-    assert n == 2 * 4 * 4 * 2048 * 32
+    assert n == 2 * 4 * 4 * 2048 * 32 + 2 * 4 * 16384 * 8 * 128
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 0, 32, 8, 128) == 0
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 96) == 0
 
