@@ -577,11 +577,11 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const AttnBwdParams p
 //   dV  += P^T dO,  dK += dS^T q           (A from tensor memory, B = the row tiles; q bf16)
 // and dK, dV (fp32, tensor memory) leave once at the end.  The MMA issuer computes S^T,
 // dP^T of round i + 1 while the softmax works on round i.
-// Roles (256 threads, one CTA per SM):
+// Roles (384 threads, one CTA per SM):
 //   warp 0      TMA producer (K, V once; q raw and dO per round)
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2-3   per round turn the raw query tile into q = x alpha + beta (fp16 in place,
-//               bf16 beside it) and stage each row's lse, D and position
+//   warps 2-3, 8-11  per round turn the raw query tile into q = x alpha + beta (fp16 in
+//               place, bf16 beside it) and stage each row's lse, D and position
 //   warps 4-7   P^T, dS^T (tensor-memory lane = key), then the dK / dV epilogue
 // Tensor memory: S^T at 64 u, dP^T at 128 + 64 u (buffer u), dK at 256, dV at 256 + D.
 // Every wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and every role drains
@@ -668,8 +668,11 @@ __device__ __forceinline__ int next_round(const AttnBwdParams &p, int b, int kt0
     return r_end;
 }
 
+constexpr int DKV_TC_THREADS = 384;
+constexpr int DKV_TC_CONV = 192;  // preparation threads (warps 2-3 and 8-11)
+
 template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnBwdParams p)
@@ -706,7 +709,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(kv_full, 1);
         for (int s = 0; s < C::STG; ++s) {
             mbar_init(&st_full[s], 1);
-            mbar_init(&qconv[s], 2);
+            mbar_init(&qconv[s], DKV_TC_CONV / 32);
             mbar_init(&st_empty[s], 1);
         }
         for (int u = 0; u < 2; ++u) {
@@ -821,19 +824,31 @@ __global__ void __launch_bounds__(256, 1)
                 umma_commit(acc_final);
             __syncwarp();
         }
-    } else if (warp < 4) {
+    } else if (warp < 4 || warp >= 8) {
         // ------------------------------------------------------------------ query preparation
-        const int ct = threadIdx.x - 64;  // 0..63
+        const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 256 + 64;  // 0..191
         bool bad = false;
         int i = 0;
         for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
              r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
             const int s = i % C::STG;
+            // this round's row metadata, loaded before the wait so that its latency overlaps
+            float m_lse = 0.f, m_d = 0.f;
+            int m_pos = -1;
+            if (ct < C::RB) {
+                const int u = r * UNITS + ct / G, h = g * G + ct % G;
+                m_pos = unit_pos<COPY>(p, b, u);
+                if (m_pos >= 0) {
+                    const long long ri = (static_cast<long long>(b) * p.n_units + u) * p.Hq + h;
+                    m_lse = p.lse[ri];
+                    m_d = p.Drow[ri];
+                }
+            }
             if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
                 break;
             uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
 #pragma unroll 2
-            for (int idx = ct; idx < C::RB * C::SLABS * 8; idx += 64) {
+            for (int idx = ct; idx < C::RB * C::SLABS * 8; idx += DKV_TC_CONV) {
                 const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
                 const int sl = rem / 8, c8 = rem % 8;
                 const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
@@ -844,15 +859,11 @@ __global__ void __launch_bounds__(256, 1)
                 *qp = q16;
                 *reinterpret_cast<uint4 *>(st + C::ST_QB + off) = qb;
             }
-            {
-                const int row = ct;  // RB == 64 rows, one per thread
-                const int u = r * UNITS + row / G, h = g * G + row % G;
-                const int P = unit_pos<COPY>(p, b, u);
-                const long long ri = (static_cast<long long>(b) * p.n_units + u) * p.Hq + h;
+            if (ct < C::RB) {  // one row per thread
                 float *m = meta + s * 3 * C::RB;
-                m[row] = P >= 0 ? p.lse[ri] : 0.f;
-                m[C::RB + row] = P >= 0 ? p.Drow[ri] : 0.f;
-                m[2 * C::RB + row] = __int_as_float(P);
+                m[ct] = m_lse;
+                m[C::RB + ct] = m_d;
+                m[2 * C::RB + ct] = __int_as_float(m_pos);
             }
             fence_proxy_async_smem();  // the MMA reads q through the async proxy
             __syncwarp();
@@ -977,8 +988,9 @@ __global__ void __launch_bounds__(256, 1)
 //           dQ += dS K  (A from tensor memory, B = the key block, MN-major)
 // then dq_raw = scale dQ * alpha, and dalpha / dbeta reduced across the CTA's rows of
 // each head (shuffles, then shared memory) and added with global atomics.
-// Roles (256 threads, one CTA per SM): warp 0 TMA producer; warp 1 tensor-memory
-// allocation and MMA issue; warps 2-3 query preparation; warps 4-7 softmax and epilogue.
+// Roles (384 threads, one CTA per SM): warp 0 TMA producer; warp 1 tensor-memory
+// allocation and MMA issue; warps 2-3 and 8-11 query preparation; warps 4-7 softmax and
+// epilogue.
 // Tensor memory: S at 64 u, dP at 128 + 64 u (buffer u), dQ at 256.
 template <int D>
 struct BqCfg {
@@ -1004,7 +1016,7 @@ struct BqCfg {
 };
 
 template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                           const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const __grid_constant__ CUtensorMap k16map, const AttnBwdParams p)
@@ -1046,7 +1058,7 @@ __global__ void __launch_bounds__(256, 1)
     const int whi = __reduce_max_sync(0xffffffffu, Prow);
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_conv, 2);
+        mbar_init(q_conv, DKV_TC_CONV / 32);
         for (int s = 0; s < C::STG; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
@@ -1059,7 +1071,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(dq_final, 1);
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < 2 * G * D; i += 256)
+    for (int i = threadIdx.x; i < 2 * G * D; i += DKV_TC_THREADS)
         red[i] = 0.f;
     if (warp == 1)
         tmem_alloc(tmem_holder, 512);
@@ -1174,13 +1186,13 @@ __global__ void __launch_bounds__(256, 1)
                 umma_commit(dq_final);
             __syncwarp();
         }
-    } else if (warp < 4) {
+    } else if (warp < 4 || warp >= 8) {
         // ------------------------------------------------------------------ query preparation
-        const int ct = threadIdx.x - 64;  // 0..63
+        const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 256 + 64;  // 0..191
         bool bad = false;
         if (nb > 0 && (ok = warp_wait(q_full, 0))) {
 #pragma unroll 2
-            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
+            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += DKV_TC_CONV) {
                 const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
                 const int sl = rem / 8, c8 = rem % 8;
                 const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
@@ -1402,9 +1414,10 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                                                                                                 rows);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
-        // base rows see at most window + 128/G keys, too few blocks to fill the tensor-memory
-        // pipeline of one CTA per SM: the warp-MMA kernel is faster there (measured 1.05 vs
-        // 1.45 ms for a 16K-token, 32/8-head, w = 128 layer); copies see long key ranges
+        // base rows see at most window + 128/G keys: a tensor-memory CTA (one per SM) spends
+        // most of its time filling and draining its pipeline, and the warp-MMA kernel is a
+        // little faster there (measured 1.05 vs 1.10 ms for a 16K-token, 32/8-head, w = 128
+        // layer); copies see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
         if (maps && COPY) {
             const size_t s1 = BqCfg<D>::SMEM;
             auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
@@ -1413,7 +1426,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                 return e;
             constexpr int UNITS = BqCfg<D>::ROWS / G;
             dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-            k1<<<g1, 256, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
+            k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
@@ -1435,7 +1448,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             cudaSuccess)
             return e;
         dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-        k3<<<g3, 256, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
+        k3<<<g3, DKV_TC_THREADS, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
         return cudaGetLastError();
     }
     const size_t s2 = dkv_smem(D);
