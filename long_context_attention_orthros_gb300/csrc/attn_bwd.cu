@@ -10,19 +10,18 @@
 // A query row is a "unit" (a base token, or a copy) times a head; the unit sits at
 // position P (the token itself, or the copy's original position) and sees keys
 // P - window + 1 .. P (window = T_kv for the copies: keys 0 .. P).
-// Three launches (warp MMAs, bf16 operands, fp32 accumulation):
-//   attn_bwd_d_kernel    D = dO . o per row;
-//   attn_bwd_dq_kernel   rows on the MMA's M side: K/V stream through a two-stage
-//                        shared-memory ring of 64-key blocks (cp.async); pass 1 takes
-//                        each row's log2-sum-exp (kept for the next kernel), pass 2
-//                        dP = dO V^T, dS = P (dP - D), dQ += dS K; then dq_raw, and
-//                        dalpha / dbeta through shared, then global, atomics;
-//   attn_bwd_dkv_kernel  keys on the M side: a CTA owns 64 keys and stages, round by
-//                        round, the query rows that can see them; each warp keeps dK,
-//                        dV of its 16 keys in registers (S^T = K q^T, dP^T = V dO^T,
-//                        dV += P^T dO, dK += dS^T q) and writes them once.
-// q . k takes q as a bf16 high part plus residual; P and dS enter the second
-// products as bf16, and q enters dK as its bf16 high part.  Outputs are fp32.
+// Launches (bf16 / fp16 operands, fp32 accumulation, fp32 outputs):
+//   attn_bwd_k16_kernel     an exact fp16 copy of K (for q . k on tensor memory);
+//   attn_bwd_d_kernel       D = dO . o per row;
+//   attn_bwd_dq_kernel      (base stream) warp MMAs, rows on the MMA's M side: K/V stream
+//                           through a two-stage shared-memory ring of 64-key blocks
+//                           (cp.async); pass 1 takes each row's log2-sum-exp (kept for
+//                           the dK/dV kernel), pass 2 dP = dO V^T, dS = P (dP - D),
+//                           dQ += dS K (q as bf16 high part + residual); then dq_raw,
+//                           and dalpha / dbeta through shared, then global, atomics;
+//   attn_bwd_dq_tc_kernel   (copies) the same on tcgen05 (below);
+//   attn_bwd_dkv_tc_kernel  keys on tcgen05's M side, dK and dV in tensor memory (below).
+// P and dS enter the second products as bf16; q enters dK as bf16.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -35,8 +34,8 @@ namespace orthros {
 namespace {
 
 constexpr float kLog2eF = 1.4426950408889634f;
-constexpr int BWD_ROWS = 64;  // query rows of a dq CTA, and rows staged per dk/dv round
-constexpr int BWD_KEYS = 64;  // keys of a dk/dv CTA, and keys per streamed dq block
+constexpr int BWD_ROWS = 64;  // query rows of a warp-MMA dq CTA
+constexpr int BWD_KEYS = 64;  // keys per streamed block of the warp-MMA dq kernel
 
 // [rows][D] bf16 tile in shared memory as D/64 slabs of rows x 128 bytes, 128-byte swizzle
 __device__ __forceinline__ uint32_t tile_off(int row, int col, int slab_bytes)
@@ -374,192 +373,6 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
     for (int i = threadIdx.x; i < G * D; i += 128) {
         atomicAdd(p.dalpha + g * G * D + i, red[i]);
         atomicAdd(p.dbeta + g * G * D + i, red[G * D + i]);
-    }
-}
-
-// ------------------------------------------------------------------ dK, dV (keys on M)
-
-template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const AttnBwdParams p)
-{
-    constexpr int RB = BWD_ROWS;  // rows staged per round = RB / G units x G heads
-    constexpr int TOKR = RB / G;
-    constexpr int KSLAB = BWD_KEYS * 128, RSLAB = RB * 128;
-    const int kt0 = blockIdx.x * BWD_KEYS, bh = blockIdx.y;
-    const int b = bh / p.Hkv, g = bh % p.Hkv;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    uint8_t *kt = smem;                   // K of the CTA's keys
-    uint8_t *vt = kt + (D / 64) * KSLAB;  // V
-    uint8_t *qh = vt + (D / 64) * KSLAB;  // staged rows: q high part
-    uint8_t *ql = qh + (D / 64) * RSLAB;  // q residual
-    uint8_t *gt = ql + (D / 64) * RSLAB;  // dO
-    float *lse_s = reinterpret_cast<float *>(gt + (D / 64) * RSLAB);  // [RB]
-    float *D_s = lse_s + RB;                                          // [RB]
-    int *P_s = reinterpret_cast<int *>(D_s + RB);                     // [RB] position, -1: none
-    const long long kv_rs = static_cast<long long>(p.Hkv) * D;
-    const long long kv_b = static_cast<long long>(b) * p.T_kv * kv_rs + static_cast<long long>(g) * D;
-    for (int i = threadIdx.x; i < BWD_KEYS * (D / 8); i += 128) {
-        const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-        const int key = kt0 + r;
-        uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = kv4;
-        if (key < p.T_kv) {
-            kv4 = *reinterpret_cast<const uint4 *>(p.k + kv_b + key * kv_rs + c);
-            vv4 = *reinterpret_cast<const uint4 *>(p.v + kv_b + key * kv_rs + c);
-        }
-        *reinterpret_cast<uint4 *>(kt + tile_off(r, c, KSLAB)) = kv4;
-        *reinterpret_cast<uint4 *>(vt + tile_off(r, c, KSLAB)) = vv4;
-    }
-    const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-    const uint32_t qhb = smem_u32(qh), qlb = smem_u32(ql), gb = smem_u32(gt);
-
-    const int k_w0 = kt0 + 16 * warp;  // this warp's first key
-    const float c2 = p.scale * kLog2eF;
-    const long long q_bs = static_cast<long long>(p.n_units) * p.Hq * D;
-    float dk[D / 8][4], dv[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-        dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.f;
-    const int a_row = (lane & 7) + (((lane >> 3) & 1) << 3), a_hi = lane >> 4;  // A: K / V rows
-    const int b_row = (lane & 7) + ((lane >> 4) << 3), b_hi = (lane >> 3) & 1;  // B from row tiles
-    const int t_row = a_row, t_hi = a_hi;                                       // B from row tiles, transposed
-    const int gk = lane >> 2, gq = (lane & 3) * 2;  // C fragment: key rows gk, gk+8; row columns gq, gq+1
-
-    // units whose keys can include the CTA's: base tokens kt0 .. kt0+63+w-1; every copy
-    const int u_begin = COPY ? 0 : kt0;
-    const int u_end = COPY ? p.n_units
-                           : static_cast<int>(min(static_cast<long long>(p.n_units),
-                                                  static_cast<long long>(kt0) + BWD_KEYS - 1 + p.window));
-#pragma unroll 1
-    for (int tr0 = u_begin; tr0 < u_end; tr0 += TOKR) {
-        __syncthreads();  // the previous round's rows are consumed
-        if (COPY) {
-            int need = 0;
-            for (int r = threadIdx.x; r < TOKR; r += 128)
-                need |= unit_pos<COPY>(p, b, tr0 + r) >= kt0;
-            if (!__syncthreads_or(need))
-                continue;  // no copy of this round reaches the CTA's keys
-        }
-        for (int i = threadIdx.x; i < RB * (D / 8); i += 128) {
-            const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-            const int u = tr0 + r / G, h = g * G + r % G;
-            uint4 hi4 = make_uint4(0u, 0u, 0u, 0u), lo4 = hi4, g4 = hi4;
-            if (unit_pos<COPY>(p, b, u) >= 0) {
-                const long long off = b * q_bs + (static_cast<long long>(u) * p.Hq + h) * D + c;
-                const uint4 x4 = *reinterpret_cast<const uint4 *>(p.q + off);
-                g4 = *reinterpret_cast<const uint4 *>(p.dO + off);
-                const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xv = unpack_bf16x2(xw[e]);
-                    const float2 al = __ldg(reinterpret_cast<const float2 *>(p.alpha + h * D + c + 2 * e));
-                    const float2 be = __ldg(reinterpret_cast<const float2 *>(p.beta + h * D + c + 2 * e));
-                    split_q_pair(fmaf(xv.x, al.x, be.x), fmaf(xv.y, al.y, be.y), hw[e], lw[e]);
-                }
-                hi4 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                lo4 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-            const uint32_t o = tile_off(r, c, RSLAB);
-            *reinterpret_cast<uint4 *>(qh + o) = hi4;
-            *reinterpret_cast<uint4 *>(ql + o) = lo4;
-            *reinterpret_cast<uint4 *>(gt + o) = g4;
-        }
-        for (int r = threadIdx.x; r < RB; r += 128) {
-            const int u = tr0 + r / G, h = g * G + r % G;
-            const int P = unit_pos<COPY>(p, b, u);
-            const long long ri = (static_cast<long long>(b) * p.n_units + u) * p.Hq + h;
-            P_s[r] = P;
-            lse_s[r] = P >= 0 ? p.lse[ri] : 0.f;
-            D_s[r] = P >= 0 ? p.Drow[ri] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 1
-        for (int rc = 0; rc < RB; rc += 16) {
-            // skip chunks none of whose rows sees a key of this warp (warp-uniform)
-            const int Pl = P_s[rc + (lane & 15)];
-            const int lol = Pl >= 0 ? Pl - p.window + 1 : 0x7fffffff;
-            if (__reduce_max_sync(0xffffffffu, Pl) < k_w0 || __reduce_min_sync(0xffffffffu, lol) > k_w0 + 15)
-                continue;
-            float s[2][4], dpt[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                s[i][0] = s[i][1] = s[i][2] = s[i][3] = dpt[i][0] = dpt[i][1] = dpt[i][2] = dpt[i][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t a[4], av[4], bh0, bh1, bh2, bh3, bl0, bl1, bl2, bl3, g0, g1, g2, g3;
-                ldsm_x4(kbase + tile_off(16 * warp + a_row, kk * 16 + a_hi * 8, KSLAB), a[0], a[1], a[2], a[3]);
-                ldsm_x4(vbase + tile_off(16 * warp + a_row, kk * 16 + a_hi * 8, KSLAB), av[0], av[1], av[2], av[3]);
-                ldsm_x4(qhb + tile_off(rc + b_row, kk * 16 + b_hi * 8, RSLAB), bh0, bh1, bh2, bh3);
-                ldsm_x4(qlb + tile_off(rc + b_row, kk * 16 + b_hi * 8, RSLAB), bl0, bl1, bl2, bl3);
-                ldsm_x4(gb + tile_off(rc + b_row, kk * 16 + b_hi * 8, RSLAB), g0, g1, g2, g3);
-                mma_16816(s[0], a, bh0, bh1);
-                mma_16816(s[1], a, bh2, bh3);
-                mma_16816(s[0], a, bl0, bl1);
-                mma_16816(s[1], a, bl2, bl3);
-                mma_16816(dpt[0], av, g0, g1);
-                mma_16816(dpt[1], av, g2, g3);
-            }
-            // P^T, dS^T: element (key gk (+8), row column 8 i + gq (+1))
-            float pt[2][4], dst[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = k_w0 + gk + ((e & 2) ? 8 : 0);
-                    const int rr = rc + 8 * i + gq + (e & 1);
-                    const int P = P_s[rr];
-                    const bool valid = key <= P && key >= P - p.window + 1;  // P = -1: none
-                    const float pr = valid ? fast_exp2(s[i][e] * c2 - lse_s[rr]) : 0.f;
-                    pt[i][e] = pr;
-                    dst[i][e] = pr * (dpt[i][e] - D_s[rr]);
-                }
-            uint32_t pa[4], da[4];
-            pa[0] = pack_bf16x2(pt[0][0], pt[0][1]);
-            pa[1] = pack_bf16x2(pt[0][2], pt[0][3]);
-            pa[2] = pack_bf16x2(pt[1][0], pt[1][1]);
-            pa[3] = pack_bf16x2(pt[1][2], pt[1][3]);
-            da[0] = pack_bf16x2(dst[0][0], dst[0][1]);
-            da[1] = pack_bf16x2(dst[0][2], dst[0][3]);
-            da[2] = pack_bf16x2(dst[1][0], dst[1][1]);
-            da[3] = pack_bf16x2(dst[1][2], dst[1][3]);
-#pragma unroll
-            for (int dd = 0; dd < D / 16; ++dd) {
-                uint32_t g0, g1, g2, g3, q0, q1, q2, q3;
-                ldsm_x4_trans(gb + tile_off(rc + t_row, dd * 16 + t_hi * 8, RSLAB), g0, g1, g2, g3);
-                ldsm_x4_trans(qhb + tile_off(rc + t_row, dd * 16 + t_hi * 8, RSLAB), q0, q1, q2, q3);
-                mma_16816(dv[2 * dd], pa, g0, g1);
-                mma_16816(dv[2 * dd + 1], pa, g2, g3);
-                mma_16816(dk[2 * dd], da, q0, q1);
-                mma_16816(dk[2 * dd + 1], da, q2, q3);
-            }
-        }
-    }
-    // write (or add) dK (scaled) and dV of the warp's 16 keys
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int key = k_w0 + gk + half * 8;
-        if (key >= p.T_kv)
-            continue;
-        const long long off = (static_cast<long long>(b) * p.T_kv + key) * kv_rs + static_cast<long long>(g) * D;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            const int dcol = i * 8 + gq;
-            float2 nk = make_float2(dk[i][2 * half] * p.scale, dk[i][2 * half + 1] * p.scale);
-            float2 nv = make_float2(dv[i][2 * half], dv[i][2 * half + 1]);
-            float2 *pk = reinterpret_cast<float2 *>(p.dk + off + dcol);
-            float2 *pv = reinterpret_cast<float2 *>(p.dv + off + dcol);
-            if (p.accumulate) {
-                const float2 ok = *pk, ov = *pv;
-                nk.x += ok.x;
-                nk.y += ok.y;
-                nv.x += ov.x;
-                nv.y += ov.y;
-            }
-            *pk = nk;
-            *pv = nv;
-        }
     }
 }
 
@@ -1388,11 +1201,6 @@ static size_t dq_smem(int D, int G)
     return static_cast<size_t>(4) * (D / 64) * BWD_KEYS * 128 + 2 * G * D * 4 + 16 + 1024;
 }
 
-static size_t dkv_smem(int D)
-{
-    return static_cast<size_t>(D / 64) * (2 * BWD_KEYS * 128 + 3 * BWD_ROWS * 128) + 3 * BWD_ROWS * 4 + 1024;
-}
-
 template <int D, int G, bool COPY>
 static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
 {
@@ -1402,7 +1210,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         e = cudaMemsetAsync(p.dbeta, 0, sizeof(float) * p.Hq * D, stream);
     if (e != cudaSuccess)
         return e;
-    if (maps) {
+    {
         const long long n8 = static_cast<long long>(p.B) * p.T_kv * p.Hkv * D / 8;
         attn_bwd_k16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(p.k, p.k16, n8,
                                                                                                   p.dev_err);
@@ -1418,7 +1226,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         // most of its time filling and draining its pipeline, and the warp-MMA kernel is a
         // little faster there (measured 1.05 vs 1.10 ms for a 16K-token, 32/8-head, w = 128
         // layer); copies see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
-        if (maps && COPY) {
+        if (COPY) {
             const size_t s1 = BqCfg<D>::SMEM;
             auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
             if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
@@ -1441,23 +1249,13 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             return e;
     }
     // dk/dv also runs without query rows: it writes (or keeps) zeros
-    if (maps) {
-        const size_t s3 = BtCfg<D>::SMEM;
-        auto k3 = attn_bwd_dkv_tc_kernel<D, G, COPY>;
-        if ((e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3))) !=
-            cudaSuccess)
-            return e;
-        dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-        k3<<<g3, DKV_TC_THREADS, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
-        return cudaGetLastError();
-    }
-    const size_t s2 = dkv_smem(D);
-    auto k2 = attn_bwd_dkv_kernel<D, G, COPY>;
-    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2))) !=
+    const size_t s3 = BtCfg<D>::SMEM;
+    auto k3 = attn_bwd_dkv_tc_kernel<D, G, COPY>;
+    if ((e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3))) !=
         cudaSuccess)
         return e;
-    dim3 g2((p.T_kv + BWD_KEYS - 1) / BWD_KEYS, p.B * p.Hkv);
-    k2<<<g2, 128, s2, stream>>>(p);
+    dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
+    k3<<<g3, DKV_TC_THREADS, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
     return cudaGetLastError();
 }
 

@@ -75,7 +75,7 @@ struct AttnBwdParams {
 // workspace: lse, D (fp32 per query row), then at a 256-byte boundary the fp16 copy of K
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
 size_t attn_bwd_k16_offset(int B, int n_units, int Hq);
-// maps (tensor-memory kernels), or nullptr for the warp-MMA ones: [0..3] {q raw, dO} with boxes of
+// maps of the tensor-memory kernels: [0..3] {q raw, dO} with boxes of
 // 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
 // with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ); [8], [9] the fp16 copy
 // of K (p.k16) with boxes of 128 and of 64 keys
