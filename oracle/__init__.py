@@ -52,10 +52,11 @@ def _load():
             lib.oracle_xattn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
+            lib.oracle_swa_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                                I, I, I, I, I, D]
             for f in (lib.oracle_swa, lib.oracle_swa_rows, lib.oracle_xattn, lib.oracle_decode_step,
-                      lib.oracle_swa_bwd, lib.oracle_xattn_bwd):
+                      lib.oracle_swa_bwd, lib.oracle_xattn_bwd, lib.oracle_swa_lse):
                 f.restype = I
             _lib = lib
     return _lib
@@ -109,6 +110,21 @@ def swa_bwd(q_raw, k, v, alpha, beta, dO, window: int, scale: float):
                                 B, T, Hq, Hkv, d, int(window), float(scale))
     _check(rc, "swa_bwd")
     return tuple(out)
+
+
+def swa_lse(q_raw, k, alpha, beta, window: int, scale: float) -> np.ndarray:
+    """Each base row's log-sum-exp of Eq. (4)'s scaled logits (natural log), fp64 [B,T,Hq]."""
+    B, T, Hq, d = q_raw.shape
+    Hkv = k.shape[2]
+    q_raw, pq = _c(q_raw, np.uint16)
+    k, pk = _c(k, np.uint16)
+    alpha, pa = _c(alpha, np.float32)
+    beta, pb = _c(beta, np.float32)
+    out = np.zeros((B, T, Hq), np.float64)
+    rc = _load().oracle_swa_lse(pq, pk, pa, pb, out.ctypes.data_as(ctypes.c_void_p), B, T, Hq, Hkv, d,
+                                int(window), float(scale))
+    _check(rc, "swa_lse")
+    return out
 
 
 def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, dOc, scale: float):

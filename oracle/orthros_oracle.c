@@ -509,3 +509,53 @@ int oracle_xattn_bwd(const uint16_t *qc_raw, const int32_t *pos, const uint16_t 
     }
     return bad ? -2 : 0;
 }
+
+/*
+ * Each base row's log-sum-exp, Eq. (4): lse[b, t, h] = ln sum_{j in W_t} exp(scale * q_t . k_j)
+ * with q_t = q_raw * alpha + beta, the normaliser of the row's softmax (the quantity a
+ * training forward keeps for the gradient).  lse: fp64 [B, T, Hq].  Returns 0, or -1 on a
+ * bad argument.
+ */
+int oracle_swa_lse(const uint16_t *q_raw, const uint16_t *k, const float *alpha, const float *beta,
+                   double *lse, int B, int T, int Hq, int Hkv, int d, int window, double scale)
+{
+    if (!shapes_ok(B, T, Hq, Hkv, d) || window < 1)
+        return -1;
+    const int group = Hq / Hkv;
+    const int64_t kv_row = (int64_t)Hkv * d;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)window);
+        if (!q || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 64)
+            for (int64_t job = 0; job < (int64_t)B * T * Hq; ++job) {
+                const int64_t bt = job / Hq, t = bt % T, b = bt / T;
+                const int h = (int)(job % Hq);
+                const int64_t lo = t - window + 1 > 0 ? t - window + 1 : 0;
+                const uint16_t *kb = k + (b * T * Hkv + h / group) * d;
+                scale_offset_row(q_raw + job * d, alpha + (int64_t)h * d, beta + (int64_t)h * d, d, q);
+                double m = -INFINITY;
+                for (int64_t j = lo; j <= t; ++j) {
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        acc += q[e] * bf16_to_double(kb[j * kv_row + e]);
+                    s[j - lo] = acc * scale;
+                    if (s[j - lo] > m)
+                        m = s[j - lo];
+                }
+                double sum = 0.0;
+                for (int64_t j = lo; j <= t; ++j)
+                    sum += exp(s[j - lo] - m);
+                lse[job] = m + log(sum);
+            }
+        }
+        free(q);
+        free(s);
+    }
+    return bad ? -2 : 0;
+}

@@ -539,3 +539,28 @@ def test_xattn_gradient_position_zero():
     assert not dv[0, 1:].any()
     for z in (dq, dk, da, db):
         assert not z.any()
+
+
+# ---------------------------------------------------------------- row log-sum-exp of Eq. (4)
+
+def test_swa_lse_of_zero_keys_is_log_of_window_size():
+    """K = 0: every logit is 0, so lse_t = ln(min(t + 1, w)) exactly."""
+    q, k, _, a, b = _rand_inputs(93, 2, 40, 4, 2, 16)
+    k = np.zeros_like(k)
+    got = oracle.swa_lse(q, k, a, b, 7, 0.25)
+    n = np.minimum(np.arange(40) + 1, 7).astype(np.float64)
+    np.testing.assert_allclose(got, np.broadcast_to(np.log(n)[None, :, None], got.shape), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,d,w", [(30, 4, 2, 16, 5), (65, 8, 2, 32, 128), (50, 2, 2, 8, 1)])
+def test_swa_lse_equals_scipy_logsumexp(T, Hq, Hkv, d, w):
+    """Library reference: scipy's logsumexp over the band of float64 logits from einsum."""
+    from scipy.special import logsumexp
+    q, k, _, a, b = _rand_inputs(94 + T, 1, T, Hq, Hkv, d)
+    scale = 1.0 / math.sqrt(d)
+    qq = _w(q) * a.astype(np.float64) + b.astype(np.float64)
+    kq = np.repeat(_w(k), Hq // Hkv, axis=2)
+    logits = np.einsum("bthd,bshd->bhts", qq, kq) * scale
+    band = _band(T, w)  # True where key s is in row t's window
+    ref = logsumexp(np.where(band[None, None], logits, -np.inf), axis=-1).transpose(0, 2, 1)
+    np.testing.assert_allclose(oracle.swa_lse(q, k, a, b, w, scale), ref, rtol=1e-12, atol=1e-12)
