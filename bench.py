@@ -427,10 +427,12 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     wsc = torch.empty(orth.xattn_bwd_workspace_size(B, T_out, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
     qc = g["qc"].contiguous()
     stream = torch.cuda.current_stream(dev)
+    # a training forward keeps each row's log-sum-exp; the gradient takes it
+    _, lse = orth.swa_fwd_lse(g["q"], g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale)
 
     def call():
         base = orth.swa_bwd(g["q"], g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
-                            scale=cfg.scale, workspace=ws)
+                            scale=cfg.scale, workspace=ws, lse=lse)
         copy = orth.xattn_bwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], oc, dOc, scale=cfg.scale,
                               dk=base[1], dv=base[2], workspace=wsc)
         return base + copy
@@ -446,18 +448,18 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
-    del grads, dO, dOc, ws, wsc
+    del grads, dO, dOc, ws, wsc, lse
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
     flops = 10 * d * pairs
     tfs = flops / (ms / 1e3) / 1e12
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
-            "what": "swa_bwd + xattn_bwd (copies' share added into dK/dV)",
+            "what": "swa_bwd (with the forward's log-sum-exp) + xattn_bwd (copies' share added into dK/dV)",
             "roofline": {"kernel": "attn_bwd (6 launches)", "bound": "tensor", "achieved": tfs,
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
                          "peak_kind": peak_kind, "algorithmic_flops": flops},
-            "gpu_launches": 6 * calls}
+            "gpu_launches": 8 * calls}
 
 
 def run_decode(args, dev, world, hbm_peak, peak_kind):

@@ -116,6 +116,18 @@ orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf1
                                     int row_end, int32_t *dev_err, void *stream);
 
 /*
+ * orthros_swa_fwd that also writes, for training, each row's log-sum-exp:
+ *   lse[b, t, h] = ln sum_{j in W_t} exp(scale * q_t . k_j)      (fp32 [B, T, Hq], dense)
+ * the normaliser of the row's softmax, which orthros_swa_bwd can take instead of
+ * recomputing it.  lse must be 16-byte aligned; other arguments as orthros_swa_fwd.
+ */
+orthros_status orthros_swa_fwd_lse(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                                   const orthros_bf16 *v, const float *alpha, const float *beta,
+                                   orthros_bf16 *o, float *lse, int B, int T, int Hq, int Hkv, int d,
+                                   int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                                   int64_t o_bstride, int32_t *dev_err, void *stream);
+
+/*
  * Bytes of device workspace orthros_xattn_fwd needs for these sizes
  * (split-KV partial results).  Returns 0 for invalid sizes.
  */
@@ -267,6 +279,8 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  *
  *   q_raw, o, dO [B, T, Hq, d] bf16, dense; k, v [B, T, Hkv, d] bf16, dense
  *   alpha, beta [Hq, d] fp32
+ *   lse: NULL, or the forward's per-row log-sum-exp (orthros_swa_fwd_lse), which
+ *        saves the dq kernel its first pass over the keys
  *   dq_raw [B, T, Hq, d], dk, dv [B, T, Hkv, d], dalpha, dbeta [Hq, d]: fp32
  *   outputs, every element written (dalpha and dbeta are zeroed first)
  *   workspace: orthros_swa_bwd_workspace_size(...) bytes, 16-byte aligned.
@@ -283,8 +297,9 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  */
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
                                const orthros_bf16 *v, const float *alpha, const float *beta,
-                               const orthros_bf16 *o, const orthros_bf16 *dO, float *dq_raw,
-                               float *dk, float *dv, float *dalpha, float *dbeta, int B, int T,
+                               const orthros_bf16 *o, const orthros_bf16 *dO, const float *lse,
+                               float *dq_raw, float *dk, float *dv, float *dalpha, float *dbeta,
+                               int B, int T,
                                int Hq, int Hkv, int d, int window, float scale, void *workspace,
                                size_t ws_bytes, int32_t *dev_err, void *stream);
 

@@ -6,6 +6,7 @@ CUDA kernels.  PyTorch provides device memory and the current stream.
 
 * :func:`swa_fwd`      -- base-stream sliding-window attention, Eq. (4)
 * :func:`swa_fwd_rows` -- the same for a range of output rows (chunked prefill)
+* :func:`swa_fwd_lse`  -- the same with each row's log-sum-exp (for the gradient)
 * :func:`xattn_fwd`    -- output-copy full causal cross-attention, Eq. (5)
 * :func:`prefill_fwd`  -- both of them for one prefill layer in one call
 * :func:`decode_step`  -- one fused decode step with KV-cache append
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     swa_bwd,
     swa_bwd_workspace_size,
     swa_fwd,
+    swa_fwd_lse,
     swa_fwd_rows,
     xattn_bwd,
     xattn_bwd_workspace_size,

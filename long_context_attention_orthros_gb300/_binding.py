@@ -70,8 +70,10 @@ def lib() -> ctypes.CDLL:
             L.orthros_swa_bwd_workspace_size.restype = SZ
             L.orthros_swa_bwd_workspace_size.argtypes = [I, I, I, I, I]
             L.orthros_swa_bwd.restype = I
-            L.orthros_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, SZ,
-                                          P, P]
+            L.orthros_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P,
+                                          SZ, P, P]
+            L.orthros_swa_fwd_lse.restype = I
+            L.orthros_swa_fwd_lse.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64, P, P]
             L.orthros_xattn_bwd_workspace_size.restype = SZ
             L.orthros_xattn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
             L.orthros_xattn_bwd.restype = I
@@ -251,7 +253,36 @@ def swa_bwd_workspace_size(B, T, Hq, Hkv, d) -> int:
     return int(lib().orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d))
 
 
-def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, workspace=None, dev_err=None):
+def swa_fwd_lse(q_raw, k, v, alpha, beta, window: int = 128, scale=None, out=None, lse=None, dev_err=None):
+    """swa_fwd that also returns each row's log-sum-exp, fp32 [B, T, Hq] (natural log of the
+    softmax normaliser), for swa_bwd.  Returns (o, lse)."""
+    B, T, Hkv, d = k.shape
+    Hq = q_raw.shape[2]
+    qs = _bf16_rows(q_raw, "q_raw")
+    ks = _bf16_rows(k, "k")
+    if _bf16_rows(v, "v") != ks or v.shape != k.shape:
+        raise OrthrosError("k and v must have the same shape and strides")
+    if q_raw.shape[0] != B or q_raw.shape[1] < T or q_raw.shape[3] != d:
+        raise OrthrosError("q_raw shape does not match k")
+    _vec(alpha, "alpha", Hq, d)
+    _vec(beta, "beta", Hq, d)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=k.device)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=k.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, T, Hq) or not lse.is_contiguous():
+        raise OrthrosError("lse must be a contiguous fp32 tensor [B, T, Hq]")
+    os_ = _bf16_rows(out, "out")
+    with torch.cuda.device(k.device):
+        st = lib().orthros_swa_fwd_lse(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(out), _ptr(lse),
+                                       B, T, Hq, Hkv, d, int(window), _scale(scale, d), qs, ks, os_, _ptr(dev_err),
+                                       _stream(k.device))
+    _check(st, "orthros_swa_fwd_lse")
+    return out, lse
+
+
+def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, workspace=None, dev_err=None,
+            lse=None):
     """Gradient of Eq. (4) with its scale-offset: returns fp32 (dq_raw, dk, dv, dalpha, dbeta) for
     the output gradient dO, given the forward inputs and the forward output o.  q_raw, o, dO
     [B, T, Hq, d] and k, v [B, T, Hkv, d], all dense bf16; alpha, beta [Hq, d] fp32."""
@@ -263,6 +294,8 @@ def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, work
             raise OrthrosError(f"{nm} must be a contiguous bf16 CUDA tensor {shp}")
     _vec(alpha, "alpha", Hq, d)
     _vec(beta, "beta", Hq, d)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, T, Hq) or not lse.is_contiguous()):
+        raise OrthrosError("lse must be a contiguous fp32 tensor [B, T, Hq] (from swa_fwd_lse)")
     f32 = dict(dtype=torch.float32, device=k.device)
     dq = torch.empty((B, T, Hq, d), **f32)
     dk = torch.empty((B, T, Hkv, d), **f32)
@@ -274,7 +307,7 @@ def swa_bwd(q_raw, k, v, alpha, beta, o, dO, window: int = 128, scale=None, work
                                 device=k.device)
     with torch.cuda.device(k.device):
         st = lib().orthros_swa_bwd(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o), _ptr(dO),
-                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta), B, T, Hq, Hkv, d,
+                                   _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta), B, T, Hq, Hkv, d,
                                    int(window), _scale(scale, d), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(k.device))
     _check(st, "orthros_swa_bwd")

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k
 
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, const orthros_bf16 *dO, float *Dout,
-                                                         long long rows)
+                                                         const float *lse_in, float *lse_out, long long rows)
 {
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -122,8 +122,11 @@ __global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0)
+    if (lane == 0) {
         Dout[row] = acc;
+        if (lse_in != nullptr)  // the forward's log-sum-exp, to log2 units
+            lse_out[row] = lse_in[row] * kLog2eF;
+    }
 }
 
 // ------------------------------------------------------------------ dQ (rows on M)
@@ -252,21 +255,27 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
     float mA = NEG_INF, mB = NEG_INF, lA = 0.f, lB = 0.f, lseA = 0.f, lseB = 0.f, DA = 0.f, DB = 0.f;
     const long long rA = (static_cast<long long>(b) * p.n_units + uA) * p.Hq + hA;
     const long long rB = (static_cast<long long>(b) * p.n_units + uB) * p.Hq + hB;
+    // pass 1 (each row's log-sum-exp) is skipped when the forward's is given
 #pragma unroll 1
-    for (int pass = 1; pass <= 2; ++pass) {
+    for (int pass = p.lse_in != nullptr ? 2 : 1; pass <= 2; ++pass) {
         if (pass == 2) {
-            // log2-sum-exp of each row over its keys (every valid row holds at least its own key)
-            lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-            lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-            lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-            lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-            lseA = vA ? mA + __log2f(lA) : 0.f;
-            lseB = vB ? mB + __log2f(lB) : 0.f;
-            if ((lane & 3) == 0) {
-                if (vA)
-                    p.lse[rA] = lseA;
-                if (vB)
-                    p.lse[rB] = lseB;
+            if (p.lse_in != nullptr) {  // converted to log2 units by the D kernel
+                lseA = vA ? p.lse[rA] : 0.f;
+                lseB = vB ? p.lse[rB] : 0.f;
+            } else {
+                // log2-sum-exp of each row over its keys (every valid row holds at least its own key)
+                lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+                lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+                lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+                lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+                lseA = vA ? mA + __log2f(lA) : 0.f;
+                lseB = vB ? mB + __log2f(lB) : 0.f;
+                if ((lane & 3) == 0) {
+                    if (vA)
+                        p.lse[rA] = lseA;
+                    if (vB)
+                        p.lse[rB] = lseB;
+                }
             }
             DA = vA ? p.Drow[rA] : 0.f;
             DB = vB ? p.Drow[rB] : 0.f;
@@ -1218,8 +1227,8 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             return e;
     }
     if (rows > 0) {
-        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p.o, p.dO, p.Drow,
-                                                                                                rows);
+        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+            p.o, p.dO, p.Drow, p.lse_in, p.lse, rows);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
         // base rows see at most window + 128/G keys: a tensor-memory CTA (one per SM) spends

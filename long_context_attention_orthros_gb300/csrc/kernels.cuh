@@ -24,6 +24,7 @@ struct SwaParams {
     int row_begin, row_end;  // output rows of each sequence to compute (row_begin a multiple of 128)
     long long total_tiles; // B * Hkv on input; B * Hkv * tiles_per_stream after launch set-up
     int reuse;             // 1: keep K/V blocks resident across consecutive tiles (set by launcher)
+    float *lse;            // optional [B, T, Hq]: natural log of each row's sum of exp(scale q . k)
 };
 
 struct XattnParams {
@@ -63,6 +64,7 @@ struct AttnBwdParams {
     const orthros_bf16 *q, *k, *v, *o, *dO;  // q raw, the forward output o, its gradient dO
     const float *alpha, *beta;
     const int32_t *pos;                      // copies' original positions, or nullptr (base)
+    const float *lse_in;                     // optional [B*n_units*Hq] natural-log lse from the forward
     float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta zeroed first
     float *lse, *Drow;                       // workspace [B*n_units*Hq] each: log2-sum-exp, dO . o
     uint16_t *k16;                           // workspace: K as fp16 [B, T_kv, Hkv, d]

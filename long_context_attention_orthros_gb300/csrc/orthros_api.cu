@@ -124,10 +124,14 @@ const char *orthros_status_string(orthros_status s)
 
 int orthros_version(void) { return 100; }
 
-orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
-                                    const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
-                                    int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
-                                    int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
+}  // extern "C"
+
+namespace {
+
+orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                            const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T, int Hq,
+                            int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                            int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
 {
     if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(o) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
@@ -167,8 +171,33 @@ orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf1
     p.total_tiles = static_cast<long long>(B) * Hkv;
     p.row_begin = row_begin;
     p.row_end = row_end;
+    p.lse = lse;
     const cudaError_t e = orthros::launch_swa(d, G, mq, mk, mv, mo, p, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+orthros_status orthros_swa_fwd_rows(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                                    const float *alpha, const float *beta, orthros_bf16 *o, int B, int T, int Hq,
+                                    int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                                    int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
+{
+    return swa_fwd_impl(q_raw, k, v, alpha, beta, o, nullptr, B, T, Hq, Hkv, d, window, scale, q_bstride, kv_bstride,
+                        o_bstride, row_begin, row_end, dev_err, stream);
+}
+
+orthros_status orthros_swa_fwd_lse(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                                   const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T,
+                                   int Hq, int Hkv, int d, int window, float scale, int64_t q_bstride,
+                                   int64_t kv_bstride, int64_t o_bstride, int32_t *dev_err, void *stream)
+{
+    if (!aligned16(lse))
+        return ORTHROS_ERR_INVALID_ARG;
+    return swa_fwd_impl(q_raw, k, v, alpha, beta, o, lse, B, T, Hq, Hkv, d, window, scale, q_bstride, kv_bstride,
+                        o_bstride, 0, T, dev_err, stream);
 }
 
 orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
@@ -336,9 +365,9 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
 
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
                                const float *alpha, const float *beta, const orthros_bf16 *o, const orthros_bf16 *dO,
-                               float *dq_raw, float *dk, float *dv, float *dalpha, float *dbeta, int B, int T, int Hq,
-                               int Hkv, int d, int window, float scale, void *workspace, size_t ws_bytes,
-                               int32_t *dev_err, void *stream)
+                               const float *lse, float *dq_raw, float *dk, float *dv, float *dalpha, float *dbeta,
+                               int B, int T, int Hq, int Hkv, int d, int window, float scale, void *workspace,
+                               size_t ws_bytes, int32_t *dev_err, void *stream)
 {
     if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(o) || !aligned16(dO) || !aligned16(dq_raw) || !aligned16(dk) || !aligned16(dv) ||
@@ -358,6 +387,7 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.alpha = alpha;
     p.beta = beta;
     p.pos = nullptr;
+    p.lse_in = lse;
     p.dq = dq_raw;
     p.dk = dk;
     p.dv = dv;

@@ -356,6 +356,12 @@ __global__ void __launch_bounds__(SwaCfg<D, G>::THREADS, 1)
             lB += __shfl_xor_sync(0xffffffffu, lB, 2);
             const float iA = lA > 0.f ? 1.f / lA : 0.f;
             const float iB = lB > 0.f ? 1.f / lB : 0.f;
+            if (p.lse != nullptr && (lane & 3) == 0) {  // the rows' log-sum-exp, natural log
+                if (tA < p.T && lA > 0.f)
+                    p.lse[(static_cast<long long>(b) * p.T + tA) * p.Hq + hA] = (mA + __log2f(lA)) * 0.6931471805599453f;
+                if (tB < p.T && lB > 0.f)
+                    p.lse[(static_cast<long long>(b) * p.T + tB) * p.Hq + hB] = (mB + __log2f(lB)) * 0.6931471805599453f;
+            }
             if (threadIdx.x == 0)
                 bulk_wait_read_all();  // previous tile's store has finished reading the stage
             if (!consumer_sync()) {

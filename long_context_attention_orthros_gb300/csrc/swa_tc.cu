@@ -506,6 +506,9 @@ __global__ void __launch_bounds__(512, 1)
                 const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
                 const float l0 = l4[0] + l4[1], l1 = l4[2] + l4[3];
                 const float l = l0 + l1;
+                if (p.lse != nullptr && t < p.T && l > 0.f)  // the row's log-sum-exp, natural log
+                    p.lse[(static_cast<long long>(stream_b) * p.T + t) * p.Hq + stream_g * G + r % G] =
+                        (mu + __log2f(l)) * 0.6931471805599453f;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

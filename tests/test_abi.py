@@ -112,7 +112,7 @@ def test_swa_bwd_workspace_size_and_checks(L):
     assert L.orthros_swa_bwd_workspace_size(0, 1000, 32, 8, 128) == 0
 
     def call(w=128, ws=p, nbytes=n, q=p, d=128):
-        return L.orthros_swa_bwd(q, p, p, p, p, p, p, p, p, p, p, p, 2, 1000, 32, 8, d, w,
+        return L.orthros_swa_bwd(q, p, p, p, p, p, p, None, p, p, p, p, p, 2, 1000, 32, 8, d, w,
                                  ctypes.c_float(0.1), ws, nbytes, None, None)
     assert call(q=None) == 1
     assert call(w=0) == 1
