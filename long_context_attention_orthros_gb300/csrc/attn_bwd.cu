@@ -907,7 +907,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
     const int kb0 = krange[1] >= 0 ? krange[0] / C::KB : 0;
-    const int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks, each streamed twice
+    const int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks
+    // steps n = 0 .. n1 + nb - 1: pass 1 (log-sum-exp; skipped when the forward's is given)
+    // over the blocks, then pass 2 over them again
+    const int n1 = p.lse_in != nullptr ? 0 : nb;
     bool ok = true;
 
     if (warp == 0) {
@@ -925,9 +928,9 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
             }
         }
-        for (int n = 0; n < 2 * nb; ++n) {
-            const int slot = n % C::STG, kb = kb0 + n % nb;
-            const bool pass2 = n >= nb;
+        for (int n = 0; n < n1 + nb; ++n) {
+            const bool pass2 = n >= n1;
+            const int slot = n % C::STG, kb = kb0 + (pass2 ? n - n1 : n);
             if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
                 break;
             if (lane == 0) {
@@ -955,7 +958,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         // dQ += dS K of pass-2 block n
         auto issue_dq = [&](int n) -> bool {
             const int u = n & 1, slot = n % C::STG;
-            if (!warp_wait(&p_full[u], static_cast<uint32_t>(((n - nb) >> 1) & 1)))
+            if (!warp_wait(&p_full[u], static_cast<uint32_t>(((n - n1) >> 1) & 1)))
                 return false;
             if (lane == 0) {
                 tc_fence_after();
@@ -963,7 +966,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::KB / 16; ++kk)
                     umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + 64 * u + 8 * kk,
-                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (n > nb || kk > 0) ? 1u : 0u);
+                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (n > n1 || kk > 0) ? 1u : 0u);
                 // buf_free counts 4 arrivals (the four softmax warps in pass 1): here the
                 // commit completes the phase once the dQ MMAs are done, after 3 plain arrivals
                 umma_commit(&buf_free[u]);
@@ -975,9 +978,9 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         };
         if (nb > 0)
             ok = warp_wait(q_full, 0) && warp_wait(q_conv, 0);
-        for (int n = 0; ok && n < 2 * nb; ++n) {
+        for (int n = 0; ok && n < n1 + nb; ++n) {
             const int slot = n % C::STG, u = n & 1;
-            const bool pass2 = n >= nb;
+            const bool pass2 = n >= n1;
             if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
                 break;
             if (n >= 2 && !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - 2) >> 1) & 1))))
@@ -999,11 +1002,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     umma_commit(&kv_empty[slot]);  // pass 1 reads K only through S
             }
             __syncwarp();
-            if (n > nb && !(ok = issue_dq(n - 1)))
+            if (n > n1 && !(ok = issue_dq(n - 1)))
                 break;
         }
         if (ok && nb > 0) {
-            ok = issue_dq(2 * nb - 1);
+            ok = issue_dq(n1 + nb - 1);
             if (ok && lane == 0)
                 umma_commit(dq_final);
             __syncwarp();
@@ -1042,11 +1045,12 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
         const float c2 = p.scale * kLog2eF;
         const float NEG_INF = -__int_as_float(0x7f800000);
-        float m = NEG_INF, l = 0.f, lse = 0.f;
-        for (int n = 0; ok && n < 2 * nb; ++n) {
+        float m = NEG_INF, l = 0.f;
+        float lse = (p.lse_in != nullptr && P >= 0) ? p.lse[ri] : 0.f;  // given: log2 units (D kernel)
+        for (int n = 0; ok && n < n1 + nb; ++n) {
             const int u = n & 1;
-            const bool pass2 = n >= nb;
-            const int k0 = (kb0 + n % nb) * C::KB;
+            const bool pass2 = n >= n1;
+            const int k0 = (kb0 + (pass2 ? n - n1 : n)) * C::KB;
             if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
                 break;
             tc_fence_after();
@@ -1077,7 +1081,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     acc += fast_exp2(__uint_as_float(sa[c]) - z) + fast_exp2(__uint_as_float(sb[c]) - z);
                 l = l * fast_exp2(m - z) + acc;
                 m = mn;
-                if (n == nb - 1) {
+                if (n == n1 - 1) {
                     lse = P >= 0 ? m + __log2f(l) : 0.f;  // every valid row holds its own key
                     if (P >= 0)
                         p.lse[ri] = lse;
@@ -1232,9 +1236,10 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
         // base rows see at most window + 128/G keys: a tensor-memory CTA (one per SM) spends
-        // most of its time filling and draining its pipeline, and the warp-MMA kernel is a
-        // little faster there (measured 1.05 vs 1.10 ms for a 16K-token, 32/8-head, w = 128
-        // layer); copies see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
+        // most of its time filling and draining its pipeline, and the warp-MMA kernel is
+        // faster there (whole base gradient of a 2 x 128K-token, 32/8-head, w = 128 layer:
+        // 21.6 vs 23.5 ms with the forward's log-sum-exp, 23.4 vs 24.5 ms without); copies
+        // see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
         if (COPY) {
             const size_t s1 = BqCfg<D>::SMEM;
             auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
