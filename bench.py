@@ -542,7 +542,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="orthros", choices=["orthros", "reference"])
     ap.add_argument("--config", default="prefill_128k", choices=["prefill_128k", "prefill_1m", "sft_16k",
-                                                                 "tiny_prefill", "prefill_16k"])
+                                                                 "tiny_prefill", "prefill_16k", "sft_16k_1"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -144,10 +144,13 @@ CONFIGS = {
                                 needle_frac=0.001),
     # a profiling-sized prefill with the same layer shape (inputs still larger than L2)
     "prefill_16k": PrefillConfig("prefill_16k", B=1, T=16384, Hq=32, Hkv=8, d=128),
+    # one sequence of the SFT layer (profiling size)
+    "sft_16k_1": PrefillConfig("sft_16k_1", B=1, T=16384, Hq=32, Hkv=8, d=128, T_out=2048,
+                               appended=True, positions="shuffled"),
 }
 
 SEEDS = {"tiny_prefill": 1, "prefill_128k": 2, "decode_128k": 3, "sft_16k": 4, "prefill_1m": 5,
-         "prefill_16k": 6}
+         "prefill_16k": 6, "sft_16k_1": 7}
 
 
 @dataclass
