@@ -426,12 +426,13 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     ws = torch.empty(orth.swa_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
     wsc = torch.empty(orth.xattn_bwd_workspace_size(B, T_out, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
     qc = g["qc"].contiguous()
+    q = g["q"] if g["q"].shape[1] == T else g["q"][:, :T].contiguous()  # appended copies: base rows only
     stream = torch.cuda.current_stream(dev)
     # a training forward keeps each row's log-sum-exp; the gradient takes it
-    _, lse = orth.swa_fwd_lse(g["q"], g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale)
+    _, lse = orth.swa_fwd_lse(q, g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale)
 
     def call():
-        base = orth.swa_bwd(g["q"], g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
+        base = orth.swa_bwd(q, g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
                             scale=cfg.scale, workspace=ws, lse=lse)
         copy = orth.xattn_bwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], oc, dOc, scale=cfg.scale,
                               dk=base[1], dv=base[2], workspace=wsc)
@@ -448,7 +449,7 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
-    del grads, dO, dOc, ws, wsc, lse
+    del grads, dO, dOc, ws, wsc, lse, q
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())

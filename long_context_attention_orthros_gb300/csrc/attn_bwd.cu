@@ -906,11 +906,18 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
-    const int kb0 = krange[1] >= 0 ? krange[0] / C::KB : 0;
-    const int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks
-    // steps n = 0 .. n1 + nb - 1: pass 1 (log-sum-exp; skipped when the forward's is given)
-    // over the blocks, then pass 2 over them again
-    const int n1 = p.lse_in != nullptr ? 0 : nb;
+    int kb0 = krange[1] >= 0 ? krange[0] / C::KB : 0;
+    int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks
+    const int mode = p.split_mode;
+    if (mode != 0) {  // this CTA's share of the key blocks
+        const int chunk = (nb + p.splits - 1) / p.splits, z = static_cast<int>(blockIdx.z);
+        kb0 += z * chunk;
+        nb = max(0, min(chunk, nb - z * chunk));
+    }
+    // steps n = 0 .. nsteps - 1: pass 1 (log-sum-exp; skipped when it is known) over the
+    // blocks, then pass 2 over them again (none in mode 1)
+    const int n1 = (p.lse_in != nullptr || mode == 2) ? 0 : nb;
+    const int nsteps = mode == 1 ? nb : n1 + nb;
     bool ok = true;
 
     if (warp == 0) {
@@ -928,7 +935,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
             }
         }
-        for (int n = 0; n < n1 + nb; ++n) {
+        for (int n = 0; n < nsteps; ++n) {
             const bool pass2 = n >= n1;
             const int slot = n % C::STG, kb = kb0 + (pass2 ? n - n1 : n);
             if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
@@ -978,7 +985,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         };
         if (nb > 0)
             ok = warp_wait(q_full, 0) && warp_wait(q_conv, 0);
-        for (int n = 0; ok && n < n1 + nb; ++n) {
+        for (int n = 0; ok && n < nsteps; ++n) {
             const int slot = n % C::STG, u = n & 1;
             const bool pass2 = n >= n1;
             if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
@@ -1005,8 +1012,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             if (n > n1 && !(ok = issue_dq(n - 1)))
                 break;
         }
-        if (ok && nb > 0) {
-            ok = issue_dq(n1 + nb - 1);
+        if (ok && nsteps > n1) {  // there is a pass 2: the last block's dQ
+            ok = issue_dq(nsteps - 1);
             if (ok && lane == 0)
                 umma_commit(dq_final);
             __syncwarp();
@@ -1046,8 +1053,9 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         const float c2 = p.scale * kLog2eF;
         const float NEG_INF = -__int_as_float(0x7f800000);
         float m = NEG_INF, l = 0.f;
-        float lse = (p.lse_in != nullptr && P >= 0) ? p.lse[ri] : 0.f;  // given: log2 units (D kernel)
-        for (int n = 0; ok && n < n1 + nb; ++n) {
+        // known beforehand (log2 units): from the forward via the D kernel, or the split combine
+        float lse = ((p.lse_in != nullptr || mode == 2) && P >= 0) ? p.lse[ri] : 0.f;
+        for (int n = 0; ok && n < nsteps; ++n) {
             const int u = n & 1;
             const bool pass2 = n >= n1;
             const int k0 = (kb0 + (pass2 ? n - n1 : n)) * C::KB;
@@ -1081,7 +1089,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     acc += fast_exp2(__uint_as_float(sa[c]) - z) + fast_exp2(__uint_as_float(sb[c]) - z);
                 l = l * fast_exp2(m - z) + acc;
                 m = mn;
-                if (n == n1 - 1) {
+                if (n == n1 - 1 && mode == 0) {
                     lse = P >= 0 ? m + __log2f(l) : 0.f;  // every valid row holds its own key
                     if (P >= 0)
                         p.lse[ri] = lse;
@@ -1117,10 +1125,14 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             }
         }
         // ---- epilogue: dq_raw = scale dQ alpha; dalpha, dbeta summed over the warp's rows per head
-        const bool have = ok && nb > 0;
+        if (mode == 1 && ok)  // this split's (max, sum) of every row of the tile (log2 units)
+            p.part_ml[(static_cast<long long>(bh) * p.splits + blockIdx.z) * C::ROWS + r] = make_float2(m, l);
+        const bool have = ok && nsteps > n1;  // a pass 2 ran: dQ is in tensor memory
         const bool any_live = __any_sync(0xffffffffu, uu < p.n_units);
+        // mode 0 writes every live row (zeros without keys); mode 2 adds its split's share
+        const bool write = mode == 0 ? any_live : (mode == 2 && have && any_live);
         if (have && !(ok = warp_wait(dq_final, 0))) {
-        } else if (any_live) {
+        } else if (write) {
             if (have)
                 tc_fence_after();
             const long long off = ri * D;
@@ -1161,8 +1173,17 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
                         const float4 al = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
-                        *reinterpret_cast<float4 *>(p.dq + off + c + e) =
+                        const float4 y =
                             make_float4(dqv[e] * al.x, dqv[e + 1] * al.y, dqv[e + 2] * al.z, dqv[e + 3] * al.w);
+                        float *dst = p.dq + off + c + e;
+                        if (mode == 2) {  // dq_raw is linear in dQ: the splits add up (dq zeroed first)
+                            atomicAdd(dst, y.x);
+                            atomicAdd(dst + 1, y.y);
+                            atomicAdd(dst + 2, y.z);
+                            atomicAdd(dst + 3, y.w);
+                        } else {
+                            *reinterpret_cast<float4 *>(dst) = y;
+                        }
                     }
                 }
                 // rows of one head are the lanes congruent mod G: butterfly over the other bits
@@ -1197,11 +1218,42 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ split log-sum-exp
+
+// rows of the single row tile of each (batch, KV head): merge the splits' (max, sum) into
+// the row's log2-sum-exp
+template <int G>
+__global__ void __launch_bounds__(128) attn_bwd_lse_combine_kernel(const AttnBwdParams p)
+{
+    const int bh = blockIdx.x, r = threadIdx.x;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+    const int u = r / G, h = g * G + r % G;
+    if (unit_pos<true>(p, b, u) < 0)
+        return;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float2 *part = p.part_ml + static_cast<long long>(bh) * p.splits * 128 + r;
+    float M = NEG_INF;
+    for (int z = 0; z < p.splits; ++z)
+        M = fmaxf(M, part[z * 128].x);
+    float L = 0.f;
+    for (int z = 0; z < p.splits; ++z) {
+        const float2 ml = part[z * 128];
+        if (ml.x != NEG_INF)
+            L += ml.y * exp2f(ml.x - M);
+    }
+    p.lse[(static_cast<long long>(b) * p.n_units + u) * p.Hq + h] = M + __log2f(L);  // the row holds its own key
+}
+
 // ------------------------------------------------------------------ host side
 
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
 {
     return attn_bwd_k16_offset(B, n_units, Hq) + 2 * static_cast<size_t>(B) * T_kv * Hkv * D;
+}
+
+size_t attn_bwd_split_bytes(int B, int Hkv)
+{
+    return static_cast<size_t>(B) * Hkv * ATTN_BWD_MAX_SPLITS * 128 * sizeof(float2);
 }
 
 size_t attn_bwd_k16_offset(int B, int n_units, int Hq)
@@ -1248,7 +1300,35 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                 return e;
             constexpr int UNITS = BqCfg<D>::ROWS / G;
             dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-            k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
+            // few copies (one row tile per batch and KV head) over many keys: split the keys
+            // so that the grid fills the GPU (two CTAs' worth per SM)
+            int splits = 1;
+            if (p.n_units <= UNITS && p.lse_in == nullptr && p.part_ml != nullptr) {
+                int dev = 0, sms = 0;
+                if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+                    (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                    return e;
+                const int nbk = (p.T_kv + BqCfg<D>::KB - 1) / BqCfg<D>::KB;
+                splits = min(min(ATTN_BWD_MAX_SPLITS, 2 * sms / (p.B * p.Hkv)), nbk / 8);
+            }
+            if (splits >= 2) {
+                if ((e = cudaMemsetAsync(p.dq, 0, sizeof(float) * rows * D, stream)) != cudaSuccess)
+                    return e;
+                AttnBwdParams ps = p;
+                ps.splits = splits;
+                ps.split_mode = 1;
+                dim3 gs(1, p.B * p.Hkv, splits);
+                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], ps);
+                if ((e = cudaGetLastError()) != cudaSuccess)
+                    return e;
+                attn_bwd_lse_combine_kernel<G><<<p.B * p.Hkv, 128, 0, stream>>>(ps);
+                if ((e = cudaGetLastError()) != cudaSuccess)
+                    return e;
+                ps.split_mode = 2;
+                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], ps);
+            } else {
+                k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
+            }
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;

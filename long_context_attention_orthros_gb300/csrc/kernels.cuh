@@ -72,11 +72,19 @@ struct AttnBwdParams {
     int B, n_units, T_kv, Hq, Hkv, window;   // window = T_kv for the copies
     int accumulate;                          // add to dk, dv instead of overwriting them
     float scale;
+    // few copy rows over a long key range: the tensor-memory dq kernel splits the keys of its
+    // row tile over blockIdx.z (set by the launcher): mode 1 writes per-split (max, sum) of
+    // each row, a combine kernel makes the log-sum-exp, mode 2 adds each split's dq
+    int split_mode, splits;
+    float2 *part_ml;                         // workspace [B*Hkv][splits][128]
 };
 
 // workspace: lse, D (fp32 per query row), then at a 256-byte boundary the fp16 copy of K
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
 size_t attn_bwd_k16_offset(int B, int n_units, int Hq);
+// extra workspace of the copies' gradient: per-split row partials of the split dq path
+constexpr int ATTN_BWD_MAX_SPLITS = 64;
+size_t attn_bwd_split_bytes(int B, int Hkv);
 // maps of the tensor-memory kernels: [0..3] {q raw, dO} with boxes of
 // 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
 // with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ); [8], [9] the fp16 copy

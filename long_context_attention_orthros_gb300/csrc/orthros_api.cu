@@ -416,7 +416,7 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
 {
     if (B < 1 || T_out < 0 || T_kv < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d);
+    return orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d) + orthros::attn_bwd_split_bytes(B, Hkv);
 }
 
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
@@ -453,6 +453,8 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T_out * Hq;
     p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T_out, Hq));
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                           orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d));
     p.dev_err = dev_err;
     p.B = B;
     p.n_units = T_out;

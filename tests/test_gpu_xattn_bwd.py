@@ -144,3 +144,22 @@ def test_xattn_bwd_sft_sized_copies():
     ref = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)
     for name, gg, r in zip(NAMES, got, ref):
         _assert_grad(gg, r, name)
+
+
+@pytest.mark.parametrize("positions", [[16383, 5000, 0], [700, 20, 999]])
+def test_xattn_bwd_few_copies_over_long_keys(positions):
+    """A few copies over a 16K-token sequence (8B-class heads): their dq runs with the keys
+    split over many CTAs (per-split max and sum, a combine, then per-split dq added up).
+    The second case puts every copy early, so most splits see no key at all."""
+    B, T_kv, Hq, Hkv, d = 1, 16384, 32, 8, 128
+    T_out = len(positions)
+    seed = 6300 + positions[0]
+    _, k, v, _, _, _ = _inputs(seed, B, T_kv, Hq, Hkv, d)
+    qc, _, dOc, ac, bc = _copies(seed, B, T_kv, T_out, Hq, d, "random")
+    pos = np.array([positions], np.int32)
+    scale = 1.0 / math.sqrt(d)
+    got, err = _gpu_xattn_grads(qc, pos, k, v, ac, bc, dOc, scale)
+    assert err == 0
+    ref = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)
+    for name, g, r in zip(NAMES, got, ref):
+        _assert_grad(g, r, name)
