@@ -86,7 +86,9 @@ __device__ __forceinline__ int tc_kb_hi(int n, int TOK, int T)
 }
 
 // RANGE: the launch covers a row range that may start mid-sequence (tile base n_base > 0)
-template <int D, int G, bool RANGE>
+// LSE: also store each row's log-sum-exp (p.lse); a separate instance, so that the
+// inference path carries no trace of it
+template <int D, int G, bool RANGE, bool LSE>
 __global__ void __launch_bounds__(512, 1)
     swa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const SwaParams p)
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(512, 1)
                 const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
                 const float l0 = l4[0] + l4[1], l1 = l4[2] + l4[3];
                 const float l = l0 + l1;
-                if (p.lse != nullptr && t < p.T && l > 0.f)  // the row's log-sum-exp, natural log
+                if (LSE && t < p.T && l > 0.f)  // the row's log-sum-exp, natural log
                     p.lse[(static_cast<long long>(stream_b) * p.T + t) * p.Hq + stream_g * G + r % G] =
                         (mu + __log2f(l)) * 0.6931471805599453f;
                 tmem_wait_st();
@@ -602,7 +604,11 @@ static cudaError_t launch_swa_tc_t(const CUtensorMap &q, const CUtensorMap &k, c
                                    const SwaParams &p, int num_sms, cudaStream_t stream)
 {
     using C = TcCfg<D>;
-    auto kern = p.n_base > 0 ? swa_tc_kernel<D, G, true> : swa_tc_kernel<D, G, false>;
+    // the log-sum-exp is asked for on full calls only (row_begin = 0)
+    if (p.lse != nullptr && p.n_base > 0)
+        return cudaErrorInvalidValue;
+    auto kern = p.lse != nullptr ? swa_tc_kernel<D, G, false, true>
+                                 : (p.n_base > 0 ? swa_tc_kernel<D, G, true, false> : swa_tc_kernel<D, G, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
         return e;
