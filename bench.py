@@ -450,6 +450,12 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
     del grads, dO, dOc, ws, wsc, lse, q
+    # launches per call: fp16 K copy, D, dq, dk/dv for each stream; the copies' dq splits the
+    # keys when one row tile per (batch, KV head) holds all copies (mirror of attn_bwd.cu)
+    G = Hq // Hkv
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    split = T_out <= 128 // G and min(64, 2 * sms // (B * Hkv), -(-T // 64) // 8) >= 2
+    per_call = 8 + (2 if (split and T_out > 0) else 0)
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
@@ -457,10 +463,10 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     tfs = flops / (ms / 1e3) / 1e12
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
             "what": "swa_bwd (with the forward's log-sum-exp) + xattn_bwd (copies' share added into dK/dV)",
-            "roofline": {"kernel": "attn_bwd (6 launches)", "bound": "tensor", "achieved": tfs,
+            "roofline": {"kernel": f"attn_bwd ({per_call} launches)", "bound": "tensor", "achieved": tfs,
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
                          "peak_kind": peak_kind, "algorithmic_flops": flops},
-            "gpu_launches": 8 * calls}
+            "gpu_launches": per_call * calls}
 
 
 def run_decode(args, dev, world, hbm_peak, peak_kind):
