@@ -1218,6 +1218,398 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ base-stream dQ, persistent
+
+// The base stream's rows see at most w + 128/G keys (two to four 64-key blocks per tile of
+// 128 rows), so a CTA per tile would spend most of its time on set-up, loads and the
+// epilogue.  Here one CTA per SM walks a contiguous run of row tiles with the forward's
+// log-sum-exp given (pass 2 only), and overlaps them: two dQ accumulators in tensor memory
+// let the epilogue of tile i run while tile i + 1's MMAs do, and tile i + 1's q / dO load
+// starts once tile i's last S, dP products are done.  Per key block as in the dq kernel
+// above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as bf16, dQ += dS K.
+// Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
+// warps 2-3 query preparation; warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane =
+// row: the same tensor-memory lanes), so that one tile's epilogue runs beside the next
+// tile's dS.  dalpha / dbeta: per tile the epilogue warps add their rows (butterfly per
+// head) into shared memory and flush it with global atomics, handing over through
+// mbarriers (bounded waits), not a CTA barrier.
+// Tensor memory: S at 64 u, dP at 128 + 64 u (block buffer u), dQ at 256 + D t (tile buffer t).
+template <int D>
+struct BpCfg {
+    static constexpr int ROWS = 128;
+    static constexpr int KB = 64;
+    static constexpr int SLABS = D / 64;
+    static constexpr int STG = 3;
+    static constexpr int QSLAB = ROWS * 128;
+    static constexpr int KSLAB = KB * 128;
+    static constexpr int Q16_OFF = 0;                              // raw x, then q as fp16
+    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;         // dO
+    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;           // [STG] K blocks (bf16)
+    static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
+    static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
+    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D] dalpha, dbeta
+    static constexpr int BAR_OFF = RED_OFF + 2 * 16 * D * 4;
+    static constexpr int NBARS = 3 + 2 * STG + 3 * 2 + 2 * 2 + 2;
+    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
+    attn_bwd_dq_tc_base_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                               const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                               const __grid_constant__ CUtensorMap k16map, const AttnBwdParams p)
+{
+    using C = BpCfg<D>;
+    constexpr int UNITS = C::ROWS / G;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *q_full = bars;                     // the tile's raw query and dO landed
+    uint64_t *q_conv = bars + 1;                 // the tile's q prepared
+    uint64_t *q_free = bars + 2;                 // the tile's last S, dP done: q / dO may be reloaded
+    uint64_t *kv_full = bars + 3;                // [STG] key block landed
+    uint64_t *kv_empty = kv_full + C::STG;       // [STG] key block released
+    uint64_t *s_full = kv_empty + C::STG;        // [2] S, dP of a block complete
+    uint64_t *buf_free = s_full + 2;             // [2] S / dP buffer may be overwritten
+    uint64_t *p_full = s_full + 4;               // [2] dS written
+    uint64_t *dq_final = s_full + 6;             // [2] a tile's dQ complete
+    uint64_t *dq_free = s_full + 8;              // [2] a tile's dQ read by the epilogue
+    uint64_t *red_full = s_full + 10;            // every softmax warp added the tile's rows
+    uint64_t *red_empty = s_full + 11;           // the tile's sums flushed and zeroed
+    float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // this CTA's tiles: a contiguous run of (batch, KV head, 128-row tile) in that order
+    const int n_xt = (p.n_units + UNITS - 1) / UNITS;
+    const long long n_tiles = static_cast<long long>(p.B) * p.Hkv * n_xt;
+    const long long per = (n_tiles + gridDim.x - 1) / gridDim.x;
+    const long long t_begin = blockIdx.x * per, t_end = min(n_tiles, t_begin + per);
+    // tile tau: sequence b, KV head g, first unit u0, key blocks kb0 .. kb0 + nb - 1
+    auto tile = [&](long long tau, int &b, int &g, int &u0, int &kb0, int &nb) {
+        const int bh = static_cast<int>(tau / n_xt);
+        b = bh / p.Hkv;
+        g = bh % p.Hkv;
+        u0 = static_cast<int>(tau % n_xt) * UNITS;
+        const int klo = max(0, u0 - p.window + 1), khi = min(p.n_units, u0 + UNITS) - 1;
+        kb0 = klo / C::KB;
+        nb = khi / C::KB - kb0 + 1;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_conv, 2);
+        mbar_init(q_free, 1);
+        for (int s = 0; s < C::STG; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&s_full[u], 1);
+            mbar_init(&buf_free[u], 1);
+            mbar_init(&p_full[u], 4);
+            mbar_init(&dq_final[u], 1);
+            mbar_init(&dq_free[u], 4);
+        }
+        mbar_init(red_full, 4);
+        mbar_init(red_empty, 4);
+        fence_barrier_init();
+    }
+    for (int i = threadIdx.x; i < 2 * G * D; i += DKV_TC_THREADS)
+        red[i] = 0.f;
+    if (warp == 1)
+        tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&omap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&k16map);
+        }
+        long long n = 0;  // key blocks issued so far, over all tiles
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int b, g, u0, kb0, nb;
+            tile(tau, b, g, u0, kb0, nb);
+            if (i >= 1 && !(ok = warp_wait(q_free, static_cast<uint32_t>((i - 1) & 1))))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
+                    tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
+                }
+            }
+            for (int j = 0; j < nb; ++j, ++n) {
+                const int slot = static_cast<int>(n % C::STG);
+                if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
+                    break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&kv_full[slot], 3 * C::SLABS * C::KSLAB);
+                    const int key0 = (kb0 + j) * C::KB;
+#pragma unroll
+                    for (int sl = 0; sl < C::SLABS; ++sl) {
+                        const int o = (slot * C::SLABS + sl) * C::KSLAB;
+                        tma_load_4d(smem + C::K16_OFF + o, &k16map, &kv_full[slot], sl * 64, g, key0, b);
+                        tma_load_4d(smem + C::K_OFF + o, &kmap, &kv_full[slot], sl * 64, g, key0, b);
+                        tma_load_4d(smem + C::V_OFF + o, &vmap, &kv_full[slot], sl * 64, g, key0, b);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, false, false);  // fp16
+        constexpr uint32_t IDESC_DP = umma_idesc(128, C::KB, true, false);  // bf16
+        constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
+        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q16_OFF, 16, 1024);
+        const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
+        // dQ[t] (+)= dS K of block m
+        auto issue_dq = [&](long long m, bool first, int t) -> bool {
+            const int u = static_cast<int>(m & 1), slot = static_cast<int>(m % C::STG);
+            if (!warp_wait(&p_full[u], static_cast<uint32_t>((m >> 1) & 1)))
+                return false;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, C::KSLAB, 1024);
+#pragma unroll
+                for (int kk = 0; kk < C::KB / 16; ++kk)
+                    umma_ts(tbase + C::TM_DQ + D * t, tbase + C::TM_DP + 64 * u + 8 * kk,
+                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (!first || kk > 0) ? 1u : 0u);
+                umma_commit(&buf_free[u]);
+                umma_commit(&kv_empty[slot]);
+            }
+            __syncwarp();
+            return true;
+        };
+        long long n = 0;
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int b, g, u0, kb0, nb;
+            tile(tau, b, g, u0, kb0, nb);
+            const int t = static_cast<int>(i & 1);
+            if (!(ok = warp_wait(q_full, static_cast<uint32_t>(i & 1)) && warp_wait(q_conv, static_cast<uint32_t>(i & 1))))
+                break;
+            // dQ[t] is free once the epilogue of tile i - 2 has read it
+            if (i >= 2 && !(ok = warp_wait(&dq_free[t], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
+                break;
+            for (int j = 0; j < nb; ++j, ++n) {
+                const int slot = static_cast<int>(n % C::STG), u = static_cast<int>(n & 1);
+                if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
+                    break;
+                if (n >= 2 && !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - 2) >> 1) & 1))))
+                    break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t kdesc = umma_desc_sw128(sbase + C::K16_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
+                    const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
+                        umma_ss(tbase + C::TM_S + 64 * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
+                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
+                    }
+                    umma_commit(&s_full[u]);
+                    if (j == nb - 1)
+                        umma_commit(q_free);  // the tile's q and dO are no longer read
+                }
+                __syncwarp();
+                if (j >= 1 && !(ok = issue_dq(n - 1, j == 1, t)))
+                    break;
+            }
+            if (!ok)
+                break;
+            if (!(ok = issue_dq(n - 1, nb == 1, t)))
+                break;
+            if (lane == 0)
+                umma_commit(&dq_final[t]);
+            __syncwarp();
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ query preparation
+        const int ct = threadIdx.x - 64;  // 0..63
+        bool bad = false;
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int b, g, u0, kb0, nb;
+            tile(tau, b, g, u0, kb0, nb);
+            if (!(ok = warp_wait(q_full, static_cast<uint32_t>(i & 1))))
+                break;
+#pragma unroll 4
+            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
+                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
+                const int sl = rem / 8, c8 = rem % 8;
+                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
+                uint4 *qp = reinterpret_cast<uint4 *>(smem + C::Q16_OFF + sl * C::QSLAB + sw128_offset(row, c8));
+                uint4 q16, qb;
+                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
+                *qp = q16;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(q_conv);
+        }
+        if (bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------ dS (lane = row)
+        const int rw = warp - 4;
+        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        const float c2 = p.scale * kLog2eF;
+        long long n = 0;
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int b, g, u0, kb0, nb;
+            tile(tau, b, g, u0, kb0, nb);
+            const int uu = u0 + r / G, h = g * G + r % G;
+            const bool live = uu < p.n_units;
+            const int P = live ? uu : -1, lo = P - p.window + 1;
+            const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
+            const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the D kernel converted it)
+            const float Drow = live ? p.Drow[ri] : 0.f;
+            for (int j = 0; j < nb; ++j, ++n) {
+                const int u = static_cast<int>(n & 1);
+                if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
+                    break;
+                tc_fence_after();
+                const int k0 = (kb0 + j) * C::KB;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
+                    tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
+                    tmem_wait_ld();
+                    uint32_t dw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float ds[2];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int key = k0 + 32 * half + 2 * e + q;
+                            const float pr = (key <= P && key >= lo)
+                                                 ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
+                                                 : 0.f;
+                            ds[q] = pr * (__uint_as_float(dv[2 * e + q]) - Drow);
+                        }
+                        dw[e] = pack_bf16x2(ds[0], ds[1]);
+                    }
+                    tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[u]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue (warps 8-11)
+        // dq_raw = scale dQ alpha; dalpha, dbeta into shared memory, flushed per tile
+        const int rw = warp - 8;
+        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int b, g, u0, kb0, nb;
+            tile(tau, b, g, u0, kb0, nb);
+            const int t = static_cast<int>(i & 1);
+            const int uu = u0 + r / G, h = g * G + r % G;
+            const bool live = uu < p.n_units;
+            const long long off = ((static_cast<long long>(b) * p.n_units + uu) * p.Hq + h) * D;
+            // the row's raw query, loaded before dQ is ready
+            uint32_t xw[D / 2];
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e) {
+                uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
+                if (live)
+                    x4 = *reinterpret_cast<const uint4 *>(p.q + off + 8 * e);
+                xw[4 * e] = x4.x;
+                xw[4 * e + 1] = x4.y;
+                xw[4 * e + 2] = x4.z;
+                xw[4 * e + 3] = x4.w;
+            }
+            if (!(ok = warp_wait(&dq_final[t], static_cast<uint32_t>((i >> 1) & 1))))
+                break;
+            if (i >= 1 && !(ok = warp_wait(red_empty, static_cast<uint32_t>((i - 1) & 1))))
+                break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t w[32];
+                tmem_ld32(tl + C::TM_DQ + D * t + c, w);
+                tmem_wait_ld();
+                float dqv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    dqv[e] = __uint_as_float(w[e]) * p.scale;
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 al = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
+                        *reinterpret_cast<float4 *>(p.dq + off + c + e) =
+                            make_float4(dqv[e] * al.x, dqv[e + 1] * al.y, dqv[e + 2] * al.z, dqv[e + 3] * al.w);
+                    }
+                }
+                // rows of one head are the lanes congruent mod G: butterfly over the other bits
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 x = unpack_bf16x2(xw[(c + e) / 2]);
+                    float sa0 = x.x * dqv[e], sa1 = x.y * dqv[e + 1], sb0 = dqv[e], sb1 = dqv[e + 1];
+#pragma unroll
+                    for (int o = G; o < 32; o <<= 1) {
+                        sa0 += __shfl_xor_sync(0xffffffffu, sa0, o);
+                        sa1 += __shfl_xor_sync(0xffffffffu, sa1, o);
+                        sb0 += __shfl_xor_sync(0xffffffffu, sb0, o);
+                        sb1 += __shfl_xor_sync(0xffffffffu, sb1, o);
+                    }
+                    if (lane < G) {
+                        atomicAdd(&red[lane * D + c + e], sa0);
+                        atomicAdd(&red[lane * D + c + e + 1], sa1);
+                        atomicAdd(&red[G * D + lane * D + c + e], sb0);
+                        atomicAdd(&red[G * D + lane * D + c + e + 1], sb1);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&dq_free[t]);  // this warp's lanes of dQ[t] are read
+                mbar_arrive(red_full);     // and its rows added
+            }
+            // flush the tile's sums (each warp a quarter) and zero them for the next tile
+            if (!(ok = warp_wait(red_full, static_cast<uint32_t>(i & 1))))
+                break;
+            for (int k = r; k < 2 * G * D; k += 128) {
+                const float v = red[k];
+                red[k] = 0.f;
+                atomicAdd((k < G * D ? p.dalpha + k : p.dbeta + (k - G * D)) + g * G * D, v);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(red_empty);
+        }
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
 // ------------------------------------------------------------------ split log-sum-exp
 
 // rows of the single row tile of each (batch, KV head): merge the splits' (max, sum) into
@@ -1329,6 +1721,21 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             } else {
                 k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
             }
+        } else if (p.lse_in != nullptr) {
+            // base stream with the forward's log-sum-exp: the persistent tensor-memory kernel
+            const size_t s1 = BpCfg<D>::SMEM;
+            auto k1 = attn_bwd_dq_tc_base_kernel<D, G>;
+            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
+                cudaSuccess)
+                return e;
+            int dev = 0, sms = 0;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                return e;
+            constexpr int UNITS = BpCfg<D>::ROWS / G;
+            const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
+            k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
+                maps[4], maps[5], maps[6], maps[7], maps[9], p);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;

@@ -1,6 +1,6 @@
 """GPU parity of the forward's per-row log-sum-exp (orthros_swa_fwd_lse) against the fp64
-oracle, and of the gradient that takes it (orthros_swa_bwd with lse) against the oracle's
-gradient.
+oracle, and of the gradient that takes it (orthros_swa_bwd with lse: the persistent
+tensor-memory dq kernel) against the oracle's gradient.
 
 Bar for lse: 1e-2 absolute.  The kernels take q . k with q rounded once to fp16 (tensor-memory
 path) or as a bf16 high part plus residual (warp path), i.e. each logit within ~2^-11 of its
@@ -51,6 +51,8 @@ def test_forward_lse_matches_oracle(B, T, Hq, Hkv, d, w):
     (1, 300, 8, 2, 128, 128),
     (2, 257, 16, 2, 128, 128),
     (1, 640, 8, 2, 128, 600),
+    (2, 4000, 16, 4, 128, 128),  # 1000 row tiles: each persistent CTA walks several
+    (1, 3000, 32, 8, 64, 128),   # d=64, 752 row tiles, ragged last tile
 ])
 def test_gradient_with_forward_lse(B, T, Hq, Hkv, d, w):
     q, k, v, a, b, dO = _inputs(3000 + T, B, T, Hq, Hkv, d)
