@@ -1247,8 +1247,9 @@ struct BpCfg {
     static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;           // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
     static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
-    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D] dalpha, dbeta
-    static constexpr int BAR_OFF = RED_OFF + 2 * 16 * D * 4;
+    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D+1] dalpha, dbeta
+    static constexpr int RS = D + 1;                               // padded row: no bank conflicts
+    static constexpr int BAR_OFF = RED_OFF + 2 * 16 * RS * 4;
     static constexpr int NBARS = 3 + 2 * STG + 3 * 2 + 2 * 2 + 2;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
@@ -1319,7 +1320,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         mbar_init(red_empty, 4);
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < 2 * G * D; i += DKV_TC_THREADS)
+    for (int i = threadIdx.x; i < 2 * G * C::RS; i += DKV_TC_THREADS)
         red[i] = 0.f;
     if (warp == 1)
         tmem_alloc(tmem_holder, 512);
@@ -1553,12 +1554,16 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     dqv[e] = __uint_as_float(w[e]) * p.scale;
-                if (live) {
+                if (live) {  // whole 32-byte sectors per store
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 al = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
-                        *reinterpret_cast<float4 *>(p.dq + off + c + e) =
-                            make_float4(dqv[e] * al.x, dqv[e + 1] * al.y, dqv[e + 2] * al.z, dqv[e + 3] * al.w);
+                    for (int e = 0; e < 32; e += 8) {
+                        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
+                        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e + 4));
+                        st_global_v8(p.dq + off + c + e,
+                                     make_uint4(__float_as_uint(dqv[e] * a0.x), __float_as_uint(dqv[e + 1] * a0.y),
+                                                __float_as_uint(dqv[e + 2] * a0.z), __float_as_uint(dqv[e + 3] * a0.w)),
+                                     make_uint4(__float_as_uint(dqv[e + 4] * a1.x), __float_as_uint(dqv[e + 5] * a1.y),
+                                                __float_as_uint(dqv[e + 6] * a1.z), __float_as_uint(dqv[e + 7] * a1.w)));
                     }
                 }
                 // rows of one head are the lanes congruent mod G: butterfly over the other bits
@@ -1574,10 +1579,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         sb1 += __shfl_xor_sync(0xffffffffu, sb1, o);
                     }
                     if (lane < G) {
-                        atomicAdd(&red[lane * D + c + e], sa0);
-                        atomicAdd(&red[lane * D + c + e + 1], sa1);
-                        atomicAdd(&red[G * D + lane * D + c + e], sb0);
-                        atomicAdd(&red[G * D + lane * D + c + e + 1], sb1);
+                        atomicAdd(&red[lane * C::RS + c + e], sa0);
+                        atomicAdd(&red[lane * C::RS + c + e + 1], sa1);
+                        atomicAdd(&red[(G + lane) * C::RS + c + e], sb0);
+                        atomicAdd(&red[(G + lane) * C::RS + c + e + 1], sb1);
                     }
                 }
             }
@@ -1591,9 +1596,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             if (!(ok = warp_wait(red_full, static_cast<uint32_t>(i & 1))))
                 break;
             for (int k = r; k < 2 * G * D; k += 128) {
-                const float v = red[k];
-                red[k] = 0.f;
-                atomicAdd((k < G * D ? p.dalpha + k : p.dbeta + (k - G * D)) + g * G * D, v);
+                const int row = k / D, dd = k % D;  // row: dalpha heads 0..G-1, then dbeta heads
+                float *slot = &red[row * C::RS + dd];
+                const float v = *slot;
+                *slot = 0.f;
+                atomicAdd((row < G ? p.dalpha : p.dbeta) + (g * G + row % G) * D + dd, v);
             }
             __syncwarp();
             if (lane == 0)
