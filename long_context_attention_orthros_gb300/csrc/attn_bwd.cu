@@ -759,29 +759,32 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     for (int e = 0; e < 32; ++e)
                         wk[e] = wv[e] = 0u;
                 }
-                if (key < p.T_kv) {
+                if (key < p.T_kv) {  // whole 32-byte sectors per store (rows are 32-byte aligned)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        float4 nk = make_float4(__uint_as_float(wk[e]) * p.scale, __uint_as_float(wk[e + 1]) * p.scale,
-                                                __uint_as_float(wk[e + 2]) * p.scale,
-                                                __uint_as_float(wk[e + 3]) * p.scale);
-                        float4 nv = make_float4(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1]),
-                                                __uint_as_float(wv[e + 2]), __uint_as_float(wv[e + 3]));
-                        float4 *pk = reinterpret_cast<float4 *>(p.dk + off + c + e);
-                        float4 *pv = reinterpret_cast<float4 *>(p.dv + off + c + e);
-                        if (p.accumulate) {
-                            const float4 ok4 = *pk, ov4 = *pv;
-                            nk.x += ok4.x;
-                            nk.y += ok4.y;
-                            nk.z += ok4.z;
-                            nk.w += ok4.w;
-                            nv.x += ov4.x;
-                            nv.y += ov4.y;
-                            nv.z += ov4.z;
-                            nv.w += ov4.w;
+                    for (int e = 0; e < 32; ++e)
+                        wk[e] = __float_as_uint(__uint_as_float(wk[e]) * p.scale);
+                    float *pk = p.dk + off + c, *pv = p.dv + off + c;
+                    if (p.accumulate) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 ok4 = *reinterpret_cast<const float4 *>(pk + e);
+                            const float4 ov4 = *reinterpret_cast<const float4 *>(pv + e);
+                            wk[e] = __float_as_uint(__uint_as_float(wk[e]) + ok4.x);
+                            wk[e + 1] = __float_as_uint(__uint_as_float(wk[e + 1]) + ok4.y);
+                            wk[e + 2] = __float_as_uint(__uint_as_float(wk[e + 2]) + ok4.z);
+                            wk[e + 3] = __float_as_uint(__uint_as_float(wk[e + 3]) + ok4.w);
+                            wv[e] = __float_as_uint(__uint_as_float(wv[e]) + ov4.x);
+                            wv[e + 1] = __float_as_uint(__uint_as_float(wv[e + 1]) + ov4.y);
+                            wv[e + 2] = __float_as_uint(__uint_as_float(wv[e + 2]) + ov4.z);
+                            wv[e + 3] = __float_as_uint(__uint_as_float(wv[e + 3]) + ov4.w);
                         }
-                        *pk = nk;
-                        *pv = nv;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        st_global_v8(pk + e, make_uint4(wk[e], wk[e + 1], wk[e + 2], wk[e + 3]),
+                                     make_uint4(wk[e + 4], wk[e + 5], wk[e + 6], wk[e + 7]));
+                        st_global_v8(pv + e, make_uint4(wv[e], wv[e + 1], wv[e + 2], wv[e + 3]),
+                                     make_uint4(wv[e + 4], wv[e + 5], wv[e + 6], wv[e + 7]));
                     }
                 }
             }
@@ -827,8 +830,9 @@ struct BqCfg {
     static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;      // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB; // [STG] V blocks
     static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;   // [STG] K blocks as fp16
-    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB; // [2][16][D] dalpha, dbeta partials
-    static constexpr int RANGE_OFF = RED_OFF + 2 * 16 * D * 4;
+    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB; // [2][16][D+1] dalpha, dbeta partials
+    static constexpr int RS = D + 1;                              // padded row: no bank conflicts
+    static constexpr int RANGE_OFF = RED_OFF + 2 * 16 * RS * 4;
     static constexpr int BAR_OFF = RANGE_OFF + 16;
     static constexpr int NBARS = 2 + 2 * STG + 3 * 2 + 1;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
@@ -893,7 +897,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         mbar_init(dq_final, 1);
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < 2 * G * D; i += DKV_TC_THREADS)
+    for (int i = threadIdx.x; i < 2 * G * C::RS; i += DKV_TC_THREADS)
         red[i] = 0.f;
     if (warp == 1)
         tmem_alloc(tmem_holder, 512);
@@ -1196,16 +1200,17 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         sb += __shfl_xor_sync(0xffffffffu, sb, o);
                     }
                     if (lane < G) {
-                        atomicAdd(&red[lane * D + c + e], sa);
-                        atomicAdd(&red[G * D + lane * D + c + e], sb);
+                        atomicAdd(&red[lane * C::RS + c + e], sa);
+                        atomicAdd(&red[(G + lane) * C::RS + c + e], sb);
                     }
                 }
             }
         }
         named_barrier(1, 128);  // every softmax warp reaches this point (all waits are bounded)
         for (int i = r; i < G * D; i += 128) {
-            atomicAdd(p.dalpha + g * G * D + i, red[i]);
-            atomicAdd(p.dbeta + g * G * D + i, red[G * D + i]);
+            const int hh = i / D, dd = i % D;
+            atomicAdd(p.dalpha + g * G * D + i, red[hh * C::RS + dd]);
+            atomicAdd(p.dbeta + g * G * D + i, red[(G + hh) * C::RS + dd]);
         }
     }
     if (!ok && lane == 0)
