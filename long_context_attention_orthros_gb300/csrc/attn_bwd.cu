@@ -104,25 +104,29 @@ __global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k
 
 // ------------------------------------------------------------------ D = dO . o
 
+// D/8 lanes per row, 16-byte loads (two or four rows per warp in flight)
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, const orthros_bf16 *dO, float *Dout,
                                                          const float *lse_in, float *lse_out, long long rows)
 {
-    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (row >= rows)
-        return;
+    constexpr int LPR = D / 8;  // lanes per row
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / LPR;
+    const int sub = threadIdx.x % LPR;
     float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(o + row * D) + sub);
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + row * D) + sub);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int e = lane * 2; e < D; e += 64) {
-        const float2 a = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(o + row * D + e));
-        const float2 b = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(dO + row * D + e));
-        acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = unpack_bf16x2(aw[e]), y = unpack_bf16x2(bw[e]);
+            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
+    for (int off = LPR / 2; off > 0; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
+    if (row < rows && sub == 0) {
         Dout[row] = acc;
         if (lse_in != nullptr)  // the forward's log-sum-exp, to log2 units
             lse_out[row] = lse_in[row] * kLog2eF;
@@ -1230,36 +1234,39 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // epilogue.  Here one CTA per SM walks a contiguous run of row tiles with the forward's
 // log-sum-exp given (pass 2 only), and overlaps them: two dQ accumulators in tensor memory
 // let the epilogue of tile i run while tile i + 1's MMAs do, and tile i + 1's q / dO load
-// starts once tile i's last S, dP products are done.  Per key block as in the dq kernel
-// above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as bf16, dQ += dS K.
+// loads into the other of two query buffers while tile i computes.  Per key block (32 keys,
+// so that the two query buffers and a three-stage key ring fit in shared memory) as in the
+// dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as bf16,
+// dQ += dS K.
 // Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
 // warps 2-3 query preparation; warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane =
 // row: the same tensor-memory lanes), so that one tile's epilogue runs beside the next
 // tile's dS.  dalpha / dbeta: per tile the epilogue warps add their rows (butterfly per
 // head) into shared memory and flush it with global atomics, handing over through
 // mbarriers (bounded waits), not a CTA barrier.
-// Tensor memory: S at 64 u, dP at 128 + 64 u (block buffer u), dQ at 256 + D t (tile buffer t).
+// Tensor memory: S at 32 u, dP at 64 + 32 u (block buffer u), dQ at 128 + D t (tile buffer t).
 template <int D>
 struct BpCfg {
     static constexpr int ROWS = 128;
-    static constexpr int KB = 64;
+    static constexpr int KB = 32;
     static constexpr int SLABS = D / 64;
     static constexpr int STG = 3;
     static constexpr int QSLAB = ROWS * 128;
     static constexpr int KSLAB = KB * 128;
-    static constexpr int Q16_OFF = 0;                              // raw x, then q as fp16
-    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;         // dO
-    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;           // [STG] K blocks (bf16)
+    static constexpr int QBUF = 2 * SLABS * QSLAB;                 // one query buffer: q, dO
+    static constexpr int Q16_OFF = 0;                              // [2] raw x, then q as fp16
+    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;         // [2] dO (QBUF apart)
+    static constexpr int K_OFF = 2 * QBUF;                         // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
     static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
     static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D+1] dalpha, dbeta
     static constexpr int RS = D + 1;                               // padded row: no bank conflicts
     static constexpr int BAR_OFF = RED_OFF + 2 * 16 * RS * 4;
-    static constexpr int NBARS = 3 + 2 * STG + 3 * 2 + 2 * 2 + 2;
+    static constexpr int NBARS = 3 * 2 + 2 * STG + 3 * 2 + 2 * 2 + 2;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+    static constexpr uint32_t TM_S = 0, TM_DP = 2 * KB, TM_DQ = 4 * KB;
 };
 
 template <int D, int G>
@@ -1274,10 +1281,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *q_full = bars;                     // the tile's raw query and dO landed
-    uint64_t *q_conv = bars + 1;                 // the tile's q prepared
-    uint64_t *q_free = bars + 2;                 // the tile's last S, dP done: q / dO may be reloaded
-    uint64_t *kv_full = bars + 3;                // [STG] key block landed
+    uint64_t *q_full = bars;                     // [2] a tile's raw query and dO landed
+    uint64_t *q_conv = bars + 2;                 // [2] a tile's q prepared
+    uint64_t *q_free = bars + 4;                 // [2] a tile's last S, dP done: the buffer may be reloaded
+    uint64_t *kv_full = bars + 6;                // [STG] key block landed
     uint64_t *kv_empty = kv_full + C::STG;       // [STG] key block released
     uint64_t *s_full = kv_empty + C::STG;        // [2] S, dP of a block complete
     uint64_t *buf_free = s_full + 2;             // [2] S / dP buffer may be overwritten
@@ -1307,9 +1314,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_conv, 2);
-        mbar_init(q_free, 1);
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(&q_full[qb], 1);
+            mbar_init(&q_conv[qb], 2);
+            mbar_init(&q_free[qb], 1);
+        }
         for (int s = 0; s < C::STG; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
@@ -1348,14 +1357,18 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int b, g, u0, kb0, nb;
             tile(tau, b, g, u0, kb0, nb);
-            if (i >= 1 && !(ok = warp_wait(q_free, static_cast<uint32_t>((i - 1) & 1))))
+            const int qb = static_cast<int>(i & 1);
+            // query buffer qb is free once tile i - 2's last S, dP products are done
+            if (i >= 2 && !(ok = warp_wait(&q_free[qb], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
                 break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
+                mbar_arrive_expect_tx(&q_full[qb], 2 * C::SLABS * C::QSLAB);
 #pragma unroll
                 for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
-                    tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
+                    tma_load_4d(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB, &qmap, &q_full[qb], sl * 64, g * G,
+                                u0, b);
+                    tma_load_4d(smem + qb * C::QBUF + C::DO_OFF + sl * C::QSLAB, &omap, &q_full[qb], sl * 64, g * G,
+                                u0, b);
                 }
             }
             for (int j = 0; j < nb; ++j, ++n) {
@@ -1380,8 +1393,6 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, false, false);  // fp16
         constexpr uint32_t IDESC_DP = umma_idesc(128, C::KB, true, false);  // bf16
         constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
-        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q16_OFF, 16, 1024);
-        const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
         // dQ[t] (+)= dS K of block m
         auto issue_dq = [&](long long m, bool first, int t) -> bool {
             const int u = static_cast<int>(m & 1), slot = static_cast<int>(m % C::STG);
@@ -1392,7 +1403,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, C::KSLAB, 1024);
 #pragma unroll
                 for (int kk = 0; kk < C::KB / 16; ++kk)
-                    umma_ts(tbase + C::TM_DQ + D * t, tbase + C::TM_DP + 64 * u + 8 * kk,
+                    umma_ts(tbase + C::TM_DQ + D * t, tbase + C::TM_DP + C::KB * u + 8 * kk,
                             kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (!first || kk > 0) ? 1u : 0u);
                 umma_commit(&buf_free[u]);
                 umma_commit(&kv_empty[slot]);
@@ -1404,9 +1415,12 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int b, g, u0, kb0, nb;
             tile(tau, b, g, u0, kb0, nb);
-            const int t = static_cast<int>(i & 1);
-            if (!(ok = warp_wait(q_full, static_cast<uint32_t>(i & 1)) && warp_wait(q_conv, static_cast<uint32_t>(i & 1))))
+            const int t = static_cast<int>(i & 1), qb = t;
+            const uint32_t qph = static_cast<uint32_t>((i >> 1) & 1);
+            if (!(ok = warp_wait(&q_full[qb], qph) && warp_wait(&q_conv[qb], qph)))
                 break;
+            const uint64_t qdesc = umma_desc_sw128(sbase + qb * C::QBUF + C::Q16_OFF, 16, 1024);
+            const uint64_t odesc = umma_desc_sw128(sbase + qb * C::QBUF + C::DO_OFF, 16, 1024);
             // dQ[t] is free once the epilogue of tile i - 2 has read it
             if (i >= 2 && !(ok = warp_wait(&dq_free[t], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
                 break;
@@ -1424,12 +1438,12 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
                         const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
-                        umma_ss(tbase + C::TM_S + 64 * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
-                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
+                        umma_ss(tbase + C::TM_S + C::KB * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
+                        umma_ss(tbase + C::TM_DP + C::KB * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
                     }
                     umma_commit(&s_full[u]);
                     if (j == nb - 1)
-                        umma_commit(q_free);  // the tile's q and dO are no longer read
+                        umma_commit(&q_free[qb]);  // the tile's q and dO are no longer read
                 }
                 __syncwarp();
                 if (j >= 1 && !(ok = issue_dq(n - 1, j == 1, t)))
@@ -1450,22 +1464,24 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int b, g, u0, kb0, nb;
             tile(tau, b, g, u0, kb0, nb);
-            if (!(ok = warp_wait(q_full, static_cast<uint32_t>(i & 1))))
+            const int qb = static_cast<int>(i & 1);
+            if (!(ok = warp_wait(&q_full[qb], static_cast<uint32_t>((i >> 1) & 1))))
                 break;
 #pragma unroll 4
             for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
                 const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
                 const int sl = rem / 8, c8 = rem % 8;
                 const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
-                uint4 *qp = reinterpret_cast<uint4 *>(smem + C::Q16_OFF + sl * C::QSLAB + sw128_offset(row, c8));
-                uint4 q16, qb;
-                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
+                uint4 *qp = reinterpret_cast<uint4 *>(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB +
+                                                      sw128_offset(row, c8));
+                uint4 q16, qbf;
+                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qbf, bad);
                 *qp = q16;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(q_conv);
+                mbar_arrive(&q_conv[qb]);
         }
         if (bad)
             record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
@@ -1491,11 +1507,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     break;
                 tc_fence_after();
                 const int k0 = (kb0 + j) * C::KB;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                {
                     uint32_t sv[32], dv[32];
-                    tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
-                    tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
+                    tmem_ld32(tl + C::TM_S + C::KB * u, sv);
+                    tmem_ld32(tl + C::TM_DP + C::KB * u, dv);
                     tmem_wait_ld();
                     uint32_t dw[16];
 #pragma unroll
@@ -1503,7 +1518,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         float ds[2];
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
-                            const int key = k0 + 32 * half + 2 * e + q;
+                            const int key = k0 + 2 * e + q;
                             const float pr = (key <= P && key >= lo)
                                                  ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
                                                  : 0.f;
@@ -1511,7 +1526,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         }
                         dw[e] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
+                    tmem_st16(tl + C::TM_DP + C::KB * u, dw);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -1687,7 +1702,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             return e;
     }
     if (rows > 0) {
-        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
             p.o, p.dO, p.Drow, p.lse_in, p.lse, rows);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
@@ -1747,7 +1762,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             constexpr int UNITS = BpCfg<D>::ROWS / G;
             const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
             k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
-                maps[4], maps[5], maps[6], maps[7], maps[9], p);
+                maps[4], maps[5], maps[10], maps[11], maps[12], p);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;

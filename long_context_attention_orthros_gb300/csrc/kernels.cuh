@@ -88,7 +88,7 @@ size_t attn_bwd_split_bytes(int B, int Hkv);
 // maps of the tensor-memory kernels: [0..3] {q raw, dO} with boxes of
 // 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
 // with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ); [8], [9] the fp16 copy
-// of K (p.k16) with boxes of 128 and of 64 keys
+// of K (p.k16) with boxes of 128 and of 64 keys; [10..12] K, V, fp16 K with boxes of 32 keys
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

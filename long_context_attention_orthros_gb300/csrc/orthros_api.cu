@@ -87,7 +87,8 @@ const float kLog2e = 1.4426950408889634f;
 
 // tensor maps of the gradient's kernels: for dK/dV, query rows and their output gradient
 // in rounds of 64 rows (64/G units x G heads) and K, V in blocks of 128 keys; for dQ, tiles
-// of 128 rows and K, V blocks of 64 keys; the fp16 copy of K in blocks of 128 and of 64
+// of 128 rows and K, V blocks of 64 keys; the fp16 copy of K in blocks of 128 and of 64;
+// K, V and the fp16 K in blocks of 32 (the base stream's persistent dQ)
 bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16, int d,
               int Hq, int Hkv, int n_units, int T_kv, int B)
 {
@@ -98,7 +99,8 @@ bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, cons
            make_map(&m[4], q, d, Hq, n_units, B, qs, G, 128 / G) &&
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
            make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 128) &&
-           make_map(&m[9], k16, d, Hkv, T_kv, B, ks, 1, 64);
+           make_map(&m[9], k16, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[10], k, d, Hkv, T_kv, B, ks, 1, 32) &&
+           make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[12], k16, d, Hkv, T_kv, B, ks, 1, 32);
 }
 
 }  // namespace
@@ -405,7 +407,7 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.accumulate = 0;
     p.scale = scale;
-    CUtensorMap maps[10];
+    CUtensorMap maps[13];
     if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, d, Hq, Hkv, T, T, B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
@@ -464,7 +466,7 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.window = T_kv;
     p.accumulate = accumulate ? 1 : 0;
     p.scale = scale;
-    CUtensorMap maps[10];
+    CUtensorMap maps[13];
     if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
                   B))
         return ORTHROS_ERR_CUDA;
