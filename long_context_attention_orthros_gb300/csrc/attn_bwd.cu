@@ -1244,7 +1244,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // tile's dS.  dalpha / dbeta: per tile the epilogue warps add their rows (butterfly per
 // head) into shared memory and flush it with global atomics, handing over through
 // mbarriers (bounded waits), not a CTA barrier.
-// Tensor memory: S at 32 u, dP at 64 + 32 u (block buffer u), dQ at 128 + D t (tile buffer t).
+// Tensor memory: S at 32 u, dP at 128 + 32 u (block buffer u of 4, so that four key blocks
+// are in flight), dQ at 256 + D t (tile buffer t).
 template <int D>
 struct BpCfg {
     static constexpr int ROWS = 128;
@@ -1262,11 +1263,12 @@ struct BpCfg {
     static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D+1] dalpha, dbeta
     static constexpr int RS = D + 1;                               // padded row: no bank conflicts
     static constexpr int BAR_OFF = RED_OFF + 2 * 16 * RS * 4;
-    static constexpr int NBARS = 3 * 2 + 2 * STG + 3 * 2 + 2 * 2 + 2;
+    static constexpr int NBUF = 4;                                 // S / dP buffers
+    static constexpr int NBARS = 3 * 2 + 2 * STG + 3 * NBUF + 2 * 2 + 2;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0, TM_DP = 2 * KB, TM_DQ = 4 * KB;
+    static constexpr uint32_t TM_S = 0, TM_DP = NBUF * KB, TM_DQ = 2 * NBUF * KB;
 };
 
 template <int D, int G>
@@ -1286,13 +1288,13 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     uint64_t *q_free = bars + 4;                 // [2] a tile's last S, dP done: the buffer may be reloaded
     uint64_t *kv_full = bars + 6;                // [STG] key block landed
     uint64_t *kv_empty = kv_full + C::STG;       // [STG] key block released
-    uint64_t *s_full = kv_empty + C::STG;        // [2] S, dP of a block complete
-    uint64_t *buf_free = s_full + 2;             // [2] S / dP buffer may be overwritten
-    uint64_t *p_full = s_full + 4;               // [2] dS written
-    uint64_t *dq_final = s_full + 6;             // [2] a tile's dQ complete
-    uint64_t *dq_free = s_full + 8;              // [2] a tile's dQ read by the epilogue
-    uint64_t *red_full = s_full + 10;            // every softmax warp added the tile's rows
-    uint64_t *red_empty = s_full + 11;           // the tile's sums flushed and zeroed
+    uint64_t *s_full = kv_empty + C::STG;        // [NBUF] S, dP of a block complete
+    uint64_t *buf_free = s_full + C::NBUF;       // [NBUF] S / dP buffer may be overwritten
+    uint64_t *p_full = buf_free + C::NBUF;       // [NBUF] dS written
+    uint64_t *dq_final = p_full + C::NBUF;       // [2] a tile's dQ complete
+    uint64_t *dq_free = dq_final + 2;            // [2] a tile's dQ read by the epilogue
+    uint64_t *red_full = dq_free + 2;            // every epilogue warp added the tile's rows
+    uint64_t *red_empty = red_full + 1;          // the tile's sums flushed and zeroed
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
@@ -1323,12 +1325,14 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < C::NBUF; ++u) {
             mbar_init(&s_full[u], 1);
             mbar_init(&buf_free[u], 1);
             mbar_init(&p_full[u], 4);
-            mbar_init(&dq_final[u], 1);
-            mbar_init(&dq_free[u], 4);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&dq_final[t], 1);
+            mbar_init(&dq_free[t], 4);
         }
         mbar_init(red_full, 4);
         mbar_init(red_empty, 4);
@@ -1395,8 +1399,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
         // dQ[t] (+)= dS K of block m
         auto issue_dq = [&](long long m, bool first, int t) -> bool {
-            const int u = static_cast<int>(m & 1), slot = static_cast<int>(m % C::STG);
-            if (!warp_wait(&p_full[u], static_cast<uint32_t>((m >> 1) & 1)))
+            const int u = static_cast<int>(m % C::NBUF), slot = static_cast<int>(m % C::STG);
+            if (!warp_wait(&p_full[u], static_cast<uint32_t>((m / C::NBUF) & 1)))
                 return false;
             if (lane == 0) {
                 tc_fence_after();
@@ -1425,10 +1429,12 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             if (i >= 2 && !(ok = warp_wait(&dq_free[t], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
                 break;
             for (int j = 0; j < nb; ++j, ++n) {
-                const int slot = static_cast<int>(n % C::STG), u = static_cast<int>(n & 1);
+                const int slot = static_cast<int>(n % C::STG), u = static_cast<int>(n % C::NBUF);
                 if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
                     break;
-                if (n >= 2 && !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - 2) >> 1) & 1))))
+                // S / dP buffer u is free once the dQ product of block n - NBUF has read dS
+                if (n >= C::NBUF &&
+                    !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - C::NBUF) / C::NBUF) & 1))))
                     break;
                 if (lane == 0) {
                     tc_fence_after();
@@ -1502,8 +1508,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the D kernel converted it)
             const float Drow = live ? p.Drow[ri] : 0.f;
             for (int j = 0; j < nb; ++j, ++n) {
-                const int u = static_cast<int>(n & 1);
-                if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
+                const int u = static_cast<int>(n % C::NBUF);
+                if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n / C::NBUF) & 1))))
                     break;
                 tc_fence_after();
                 const int k0 = (kb0 + j) * C::KB;
