@@ -284,14 +284,17 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  *   dq_raw [B, T, Hq, d], dk, dv [B, T, Hkv, d], dalpha, dbeta [Hq, d]: fp32
  *   outputs, every element written (dalpha and dbeta are zeroed first)
  *   workspace: orthros_swa_bwd_workspace_size(...) bytes, 16-byte aligned.
- * Products take fp32 accumulation.  q . k: in the dk/dv kernel (tensor memory)
- * fp16, K converted exactly from bf16 into the workspace and q rounded once to
- * fp16, as the forward's tensor-memory path (|k| >= 65520 or |q| >= 65504 sets
- * ORTHROS_DEVERR_RANGE); in the dq kernel a bf16 high part plus residual of q.
- * P and dS are rounded to bf16 before they multiply dO, K and q; q enters dk
- * rounded once to bf16.  Launches: the fp16 copy of K, D_t, dq (rows on the
- * MMA's M side; it also stores each row's log-sum-exp), then dk and dv (keys
- * on the M side, no atomics).  dev_err (optional) as elsewhere.
+ * Products take fp32 accumulation.  q . k on tensor memory is fp16: K converted
+ * exactly from bf16 into the workspace and q rounded once to fp16, as the
+ * forward's tensor-memory path (|k| >= 65520 or |q| >= 65504 sets
+ * ORTHROS_DEVERR_RANGE); the dq kernel used without lse (warp MMAs) takes q as
+ * a bf16 high part plus residual.  P and dS are rounded to bf16 before they
+ * multiply dO, K and q; q enters dk rounded once to bf16.  Launches: the fp16
+ * copy of K, D_t (which also converts a given lse), dq (rows on the MMA's M
+ * side: with lse a persistent tensor-memory kernel, else a two-pass warp-MMA
+ * one that stores each row's log-sum-exp), then dk and dv (keys on the M side,
+ * tensor memory, no atomics).  dq, dk, dv have one writer per element;
+ * dalpha, dbeta are summed with atomics.  dev_err (optional) as elsewhere.
  * Supported: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}; any window >= 1.
  * Outputs must not alias inputs.
  */
@@ -328,8 +331,10 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
  *   workspace: orthros_xattn_bwd_workspace_size(...) bytes, 16-byte aligned.
  * A copy whose position is outside [0, T_kv) gets a zero row of dqc_raw,
  * contributes nothing, and sets ORTHROS_DEVERR_POSITION in *dev_err.
- * Arithmetic and launches as orthros_swa_bwd, except that the dq kernel also
- * runs on tensor memory here (fp16 q . k; copies see long key ranges).
+ * Arithmetic and launches as orthros_swa_bwd, with the dq kernel on tensor
+ * memory in two passes (the first finds each copy row's log-sum-exp); when one
+ * 128-row tile per (batch, KV head) holds every copy, its key range is split
+ * over many CTAs (per-split maxima and sums, a combine, per-split dq added up).
  * T_out == 0 leaves dk, dv as they are (accumulate) or zero.  Outputs must not
  * alias inputs.
  */
