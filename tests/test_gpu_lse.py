@@ -64,3 +64,51 @@ def test_gradient_with_forward_lse(B, T, Hq, Hkv, d, w):
     ref = oracle.swa_bwd(q, k, v, a, b, dO, w, scale)
     for name, g, r in zip(NAMES, got, ref):
         _assert_grad(g.cpu().numpy().astype(np.float64), r, name)
+
+
+def test_gradient_full_size_sampled():
+    """The bench's gradient at its full size (2 x 131072 tokens, 32/8 heads, d=128, w=128, one
+    copy per sequence at its last position), launched as bench.py launches it: forward with
+    the log-sum-exp, base-stream backward, then the copy's share added into the same dK / dV.
+    Sampled base rows and keys against the oracle on the slices they depend on (a base row
+    on the w tokens up to it, a key on the tokens j-w+1..j+w-1), the copy's share of those
+    keys from the oracle's copy gradient, every copy row in full, and dalpha / dbeta as the
+    sums they are over the GPU's own dq."""
+    from tests.test_gpu_swa_bwd import _slice_grads
+    from tests.gpu_util import i32
+    B, T, Hq, Hkv, d, w = 2, 131072, 32, 8, 128, 128
+    q, k, v, a, b, dO = _inputs(8800, B, T, Hq, Hkv, d)
+    qc = normal_bf16(8800, "qc_raw", (B, 1, Hq, d))
+    dOc = normal_bf16(8800, "dOc", (B, 1, Hq, d))
+    ac, bc = scale_offset(8800, Hq, d, prefix="_c")
+    pos = np.full((B, 1), T - 1, np.int32)
+    scale = 1.0 / math.sqrt(d)
+    qg, kg, vg, ag, bg = bf(q), bf(k), bf(v), f32(a), f32(b)
+    o, lse = orth.swa_fwd_lse(qg, kg, vg, ag, bg, window=w, scale=scale)
+    dq, dk, dv, da, db = orth.swa_bwd(qg, kg, vg, ag, bg, o, bf(dO), window=w, scale=scale, lse=lse)
+    qcg, pg = bf(qc), i32(pos)
+    oc = orth.xattn_fwd(qcg, pg, kg, vg, f32(ac), f32(bc), scale=scale)
+    dqc, _, _, dac, dbc = orth.xattn_bwd(qcg, pg, kg, vg, f32(ac), f32(bc), oc, bf(dOc), scale=scale, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    del o, oc, lse
+    rc = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)  # the copy's share, every key
+    for name, g, r in zip(("dqc_raw", "dalpha_c", "dbeta_c"), (dqc, dac, dbc), (rc[0], rc[3], rc[4])):
+        _assert_grad(g.cpu().numpy().astype(np.float64), r, name)
+    for bb in range(B):
+        for t in (0, 1, 127, 128, 65535, 65536, 99999, T - 2, T - 1):
+            lo = max(0, t - w + 1)
+            r = _slice_grads(q[bb:bb + 1], k[bb:bb + 1], v[bb:bb + 1], a, b, dO[bb:bb + 1], w, scale, lo, t + 1)
+            _assert_grad(dq[bb, t].cpu().numpy().astype(np.float64), r[0][0, t - lo], f"dq_raw b{bb} row {t}")
+        for j in (0, 63, 64, 777, 65536, 100000, T - 129, T - 65, T - 1):
+            lo, hi = max(0, j - w + 1), min(T, j + w)
+            r = _slice_grads(q[bb:bb + 1], k[bb:bb + 1], v[bb:bb + 1], a, b, dO[bb:bb + 1], w, scale, lo, hi)
+            _assert_grad(dk[bb, j].cpu().numpy().astype(np.float64), r[1][0, j - lo] + rc[1][bb, j],
+                         f"dk b{bb} key {j}")
+            _assert_grad(dv[bb, j].cpu().numpy().astype(np.float64), r[2][0, j - lo] + rc[2][bb, j],
+                         f"dv b{bb} key {j}")
+    # the sums in float64 on the device (host copies of these would take tens of GB)
+    dq_post = dq.double() / ag.double()  # dq = dq_raw / alpha
+    db_ref = dq_post.sum(dim=(0, 1)).cpu().numpy()
+    da_ref = (qg.double() * dq_post).sum(dim=(0, 1)).cpu().numpy()
+    _assert_grad(db.cpu().numpy().astype(np.float64), db_ref, "dbeta as the sum of dq")
+    _assert_grad(da.cpu().numpy().astype(np.float64), da_ref, "dalpha as the sum of x * dq")
