@@ -374,7 +374,7 @@ def run_gpu(args):
         "gpu_launches": args.steps * launches_per_prefill_step(cfg),
         "clocks": clocks,
         "decode": dec,
-        "swa_bwd": bwd,
+        "gradient": bwd,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, threads, sample = oracle_prefill_rate(inp)
