@@ -261,8 +261,8 @@ orthros_status orthros_decode_step(const orthros_bf16 *q_new, const orthros_bf16
 
 /*
  * Bytes of device workspace orthros_swa_bwd needs: two fp32 values per query
- * row (the row's log-sum-exp and dO . o) and an fp16 copy of K.  Returns 0 for
- * invalid sizes.
+ * row (the row's log-sum-exp and dO . o) and fp16 copies of K and of the
+ * scale-offset q.  Returns 0 for invalid sizes.
  */
 size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
 

@@ -102,6 +102,80 @@ __global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k
         record_error(dev_err, ORTHROS_DEVERR_RANGE);
 }
 
+// ------------------------------------------------------------------ fp16 q and the dalpha / dbeta sums
+
+// q = x alpha + beta of every base row as fp16 (workspace), for the persistent dq kernel;
+// |q| >= 65504 sets ORTHROS_DEVERR_RANGE
+__global__ void __launch_bounds__(256) attn_bwd_q16_kernel(const orthros_bf16 *x, const float *alpha,
+                                                           const float *beta, uint16_t *q16, long long n8, int hd8,
+                                                           int32_t *dev_err)
+{
+    bool bad = false;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int col = static_cast<int>(i % hd8) * 8;  // h * D + d of the first element
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + col));
+        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + col + 4));
+        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + col));
+        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + col + 4));
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            const float qa = fmaf(f.x, av[2 * e], bv[2 * e]), qc = fmaf(f.y, av[2 * e + 1], bv[2 * e + 1]);
+            bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
+            __half2 hv = __floats2half2_rn(qa, qc);
+            o[e] = *reinterpret_cast<uint32_t *>(&hv);
+        }
+        reinterpret_cast<uint4 *>(q16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (bad)
+        record_error(dev_err, ORTHROS_DEVERR_RANGE);
+}
+
+// dalpha[c] += sum_rows x * dq, dbeta[c] += sum_rows dq over the columns c = h * D + d, with
+// dq = dq_raw / alpha (both sums are linear in the rows: one pass after the dq kernel).
+// Each thread owns 4 columns over a run of rows; one atomic per column and CTA.
+__global__ void __launch_bounds__(256) attn_bwd_dab_kernel(const float *dq_raw, const orthros_bf16 *x,
+                                                           const float *alpha, float *dalpha, float *dbeta,
+                                                           long long rows, int cols, int rows_per_cta)
+{
+    const int c4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;  // first of this thread's columns
+    if (c4 >= cols)
+        return;
+    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_cta;
+    const long long r1 = min(rows, r0 + rows_per_cta);
+    const float4 al = __ldg(reinterpret_cast<const float4 *>(alpha + c4));
+    const float4 ia = make_float4(1.f / al.x, 1.f / al.y, 1.f / al.z, 1.f / al.w);
+    float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
+    for (long long r = r0; r < r1; ++r) {
+        const float4 g = __ldcs(reinterpret_cast<const float4 *>(dq_raw + r * cols + c4));
+        const uint2 xr = __ldcs(reinterpret_cast<const uint2 *>(x + r * cols + c4));
+        const float2 x0 = unpack_bf16x2(xr.x), x1 = unpack_bf16x2(xr.y);
+        const float4 dq = make_float4(g.x * ia.x, g.y * ia.y, g.z * ia.z, g.w * ia.w);
+        sb.x += dq.x;
+        sb.y += dq.y;
+        sb.z += dq.z;
+        sb.w += dq.w;
+        sa.x = fmaf(x0.x, dq.x, sa.x);
+        sa.y = fmaf(x0.y, dq.y, sa.y);
+        sa.z = fmaf(x1.x, dq.z, sa.z);
+        sa.w = fmaf(x1.y, dq.w, sa.w);
+    }
+    atomicAdd(dalpha + c4, sa.x);
+    atomicAdd(dalpha + c4 + 1, sa.y);
+    atomicAdd(dalpha + c4 + 2, sa.z);
+    atomicAdd(dalpha + c4 + 3, sa.w);
+    atomicAdd(dbeta + c4, sb.x);
+    atomicAdd(dbeta + c4 + 1, sb.y);
+    atomicAdd(dbeta + c4 + 2, sb.z);
+    atomicAdd(dbeta + c4 + 3, sb.w);
+}
+
 // ------------------------------------------------------------------ D = dO . o
 
 // D/8 lanes per row, 16-byte loads (two or four rows per warp in flight)
@@ -1238,12 +1312,13 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // so that the two query buffers and a three-stage key ring fit in shared memory) as in the
 // dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as bf16,
 // dQ += dS K.
+// The query tile arrives as fp16 q = x alpha + beta, made for the whole tensor beforehand
+// (attn_bwd_q16_kernel), and dalpha / dbeta are summed afterwards from dq_raw
+// (attn_bwd_dab_kernel): both were measured to pace this kernel when done per tile here
+// (q preparation 7.8 us and the per-head butterfly 14.6 us of a 21 us tile).
 // Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
-// warps 2-3 query preparation; warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane =
-// row: the same tensor-memory lanes), so that one tile's epilogue runs beside the next
-// tile's dS.  dalpha / dbeta: per tile the epilogue warps add their rows (butterfly per
-// head) into shared memory and flush it with global atomics, handing over through
-// mbarriers (bounded waits), not a CTA barrier.
+// warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane = row: the same tensor-memory
+// lanes), so that one tile's epilogue runs beside the next tile's dS; warps 2-3 idle.
 // Tensor memory: S at 32 u, dP at 128 + 32 u (block buffer u of 4, so that four key blocks
 // are in flight), dQ at 256 + D t (tile buffer t).
 template <int D>
@@ -1260,11 +1335,9 @@ struct BpCfg {
     static constexpr int K_OFF = 2 * QBUF;                         // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
     static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
-    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB;  // [2][16][D+1] dalpha, dbeta
-    static constexpr int RS = D + 1;                               // padded row: no bank conflicts
-    static constexpr int BAR_OFF = RED_OFF + 2 * 16 * RS * 4;
+    static constexpr int BAR_OFF = K16_OFF + STG * SLABS * KSLAB;
     static constexpr int NBUF = 4;                                 // S / dP buffers
-    static constexpr int NBARS = 3 * 2 + 2 * STG + 3 * NBUF + 2 * 2 + 2;
+    static constexpr int NBARS = 2 * 2 + 2 * STG + 3 * NBUF + 2 * 2;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -1283,19 +1356,15 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *q_full = bars;                     // [2] a tile's raw query and dO landed
-    uint64_t *q_conv = bars + 2;                 // [2] a tile's q prepared
-    uint64_t *q_free = bars + 4;                 // [2] a tile's last S, dP done: the buffer may be reloaded
-    uint64_t *kv_full = bars + 6;                // [STG] key block landed
+    uint64_t *q_full = bars;                     // [2] a tile's fp16 q and dO landed
+    uint64_t *q_free = bars + 2;                 // [2] a tile's last S, dP done: the buffer may be reloaded
+    uint64_t *kv_full = bars + 4;                // [STG] key block landed
     uint64_t *kv_empty = kv_full + C::STG;       // [STG] key block released
     uint64_t *s_full = kv_empty + C::STG;        // [NBUF] S, dP of a block complete
     uint64_t *buf_free = s_full + C::NBUF;       // [NBUF] S / dP buffer may be overwritten
     uint64_t *p_full = buf_free + C::NBUF;       // [NBUF] dS written
     uint64_t *dq_final = p_full + C::NBUF;       // [2] a tile's dQ complete
     uint64_t *dq_free = dq_final + 2;            // [2] a tile's dQ read by the epilogue
-    uint64_t *red_full = dq_free + 2;            // every epilogue warp added the tile's rows
-    uint64_t *red_empty = red_full + 1;          // the tile's sums flushed and zeroed
-    float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1318,7 +1387,6 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int qb = 0; qb < 2; ++qb) {
             mbar_init(&q_full[qb], 1);
-            mbar_init(&q_conv[qb], 2);
             mbar_init(&q_free[qb], 1);
         }
         for (int s = 0; s < C::STG; ++s) {
@@ -1334,12 +1402,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             mbar_init(&dq_final[t], 1);
             mbar_init(&dq_free[t], 4);
         }
-        mbar_init(red_full, 4);
-        mbar_init(red_empty, 4);
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < 2 * G * C::RS; i += DKV_TC_THREADS)
-        red[i] = 0.f;
     if (warp == 1)
         tmem_alloc(tmem_holder, 512);
     tc_fence_before();
@@ -1421,7 +1485,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             tile(tau, b, g, u0, kb0, nb);
             const int t = static_cast<int>(i & 1), qb = t;
             const uint32_t qph = static_cast<uint32_t>((i >> 1) & 1);
-            if (!(ok = warp_wait(&q_full[qb], qph) && warp_wait(&q_conv[qb], qph)))
+            if (!(ok = warp_wait(&q_full[qb], qph)))
                 break;
             const uint64_t qdesc = umma_desc_sw128(sbase + qb * C::QBUF + C::Q16_OFF, 16, 1024);
             const uint64_t odesc = umma_desc_sw128(sbase + qb * C::QBUF + C::DO_OFF, 16, 1024);
@@ -1464,33 +1528,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             __syncwarp();
         }
     } else if (warp < 4) {
-        // ------------------------------------------------------------------ query preparation
-        const int ct = threadIdx.x - 64;  // 0..63
-        bool bad = false;
-        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            int b, g, u0, kb0, nb;
-            tile(tau, b, g, u0, kb0, nb);
-            const int qb = static_cast<int>(i & 1);
-            if (!(ok = warp_wait(&q_full[qb], static_cast<uint32_t>((i >> 1) & 1))))
-                break;
-#pragma unroll 4
-            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += 64) {
-                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
-                const int sl = rem / 8, c8 = rem % 8;
-                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
-                uint4 *qp = reinterpret_cast<uint4 *>(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB +
-                                                      sw128_offset(row, c8));
-                uint4 q16, qbf;
-                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qbf, bad);
-                *qp = q16;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&q_conv[qb]);
-        }
-        if (bad)
-            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
+        // warps 2-3: no role (the query tile arrives prepared)
     } else if (warp < 8) {
         // ------------------------------------------------------------------ dS (lane = row)
         const int rw = warp - 4;
@@ -1543,7 +1581,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue (warps 8-11)
-        // dq_raw = scale dQ alpha; dalpha, dbeta into shared memory, flushed per tile
+        // dq_raw = scale dQ alpha (dalpha, dbeta follow from it in attn_bwd_dab_kernel)
         const int rw = warp - 8;
         const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
@@ -1554,21 +1592,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             const int uu = u0 + r / G, h = g * G + r % G;
             const bool live = uu < p.n_units;
             const long long off = ((static_cast<long long>(b) * p.n_units + uu) * p.Hq + h) * D;
-            // the row's raw query, loaded before dQ is ready
-            uint32_t xw[D / 2];
-#pragma unroll
-            for (int e = 0; e < D / 8; ++e) {
-                uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
-                if (live)
-                    x4 = *reinterpret_cast<const uint4 *>(p.q + off + 8 * e);
-                xw[4 * e] = x4.x;
-                xw[4 * e + 1] = x4.y;
-                xw[4 * e + 2] = x4.z;
-                xw[4 * e + 3] = x4.w;
-            }
             if (!(ok = warp_wait(&dq_final[t], static_cast<uint32_t>((i >> 1) & 1))))
-                break;
-            if (i >= 1 && !(ok = warp_wait(red_empty, static_cast<uint32_t>((i - 1) & 1))))
                 break;
             tc_fence_after();
 #pragma unroll
@@ -1576,61 +1600,28 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 uint32_t w[32];
                 tmem_ld32(tl + C::TM_DQ + D * t + c, w);
                 tmem_wait_ld();
-                float dqv[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    dqv[e] = __uint_as_float(w[e]) * p.scale;
-                if (live) {  // whole 32-byte sectors per store
+                if (live) {  // dq_raw = scale dQ alpha, whole 32-byte sectors per store
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
                         const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e + 4));
+                        const float sc = p.scale;
                         st_global_v8(p.dq + off + c + e,
-                                     make_uint4(__float_as_uint(dqv[e] * a0.x), __float_as_uint(dqv[e + 1] * a0.y),
-                                                __float_as_uint(dqv[e + 2] * a0.z), __float_as_uint(dqv[e + 3] * a0.w)),
-                                     make_uint4(__float_as_uint(dqv[e + 4] * a1.x), __float_as_uint(dqv[e + 5] * a1.y),
-                                                __float_as_uint(dqv[e + 6] * a1.z), __float_as_uint(dqv[e + 7] * a1.w)));
-                    }
-                }
-                // rows of one head are the lanes congruent mod G: butterfly over the other bits
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 x = unpack_bf16x2(xw[(c + e) / 2]);
-                    float sa0 = x.x * dqv[e], sa1 = x.y * dqv[e + 1], sb0 = dqv[e], sb1 = dqv[e + 1];
-#pragma unroll
-                    for (int o = G; o < 32; o <<= 1) {
-                        sa0 += __shfl_xor_sync(0xffffffffu, sa0, o);
-                        sa1 += __shfl_xor_sync(0xffffffffu, sa1, o);
-                        sb0 += __shfl_xor_sync(0xffffffffu, sb0, o);
-                        sb1 += __shfl_xor_sync(0xffffffffu, sb1, o);
-                    }
-                    if (lane < G) {
-                        atomicAdd(&red[lane * C::RS + c + e], sa0);
-                        atomicAdd(&red[lane * C::RS + c + e + 1], sa1);
-                        atomicAdd(&red[(G + lane) * C::RS + c + e], sb0);
-                        atomicAdd(&red[(G + lane) * C::RS + c + e + 1], sb1);
+                                     make_uint4(__float_as_uint(__uint_as_float(w[e]) * sc * a0.x),
+                                                __float_as_uint(__uint_as_float(w[e + 1]) * sc * a0.y),
+                                                __float_as_uint(__uint_as_float(w[e + 2]) * sc * a0.z),
+                                                __float_as_uint(__uint_as_float(w[e + 3]) * sc * a0.w)),
+                                     make_uint4(__float_as_uint(__uint_as_float(w[e + 4]) * sc * a1.x),
+                                                __float_as_uint(__uint_as_float(w[e + 5]) * sc * a1.y),
+                                                __float_as_uint(__uint_as_float(w[e + 6]) * sc * a1.z),
+                                                __float_as_uint(__uint_as_float(w[e + 7]) * sc * a1.w)));
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&dq_free[t]);  // this warp's lanes of dQ[t] are read
-                mbar_arrive(red_full);     // and its rows added
-            }
-            // flush the tile's sums (each warp a quarter) and zero them for the next tile
-            if (!(ok = warp_wait(red_full, static_cast<uint32_t>(i & 1))))
-                break;
-            for (int k = r; k < 2 * G * D; k += 128) {
-                const int row = k / D, dd = k % D;  // row: dalpha heads 0..G-1, then dbeta heads
-                float *slot = &red[row * C::RS + dd];
-                const float v = *slot;
-                *slot = 0.f;
-                atomicAdd((row < G ? p.dalpha : p.dbeta) + (g * G + row % G) * D + dd, v);
-            }
-            __syncwarp();
             if (lane == 0)
-                mbar_arrive(red_empty);
+                mbar_arrive(&dq_free[t]);  // this warp's lanes of dQ[t] are read
         }
     }
     if (!ok && lane == 0)
@@ -1707,6 +1698,14 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
+    const bool persistent = !COPY && p.lse_in != nullptr && p.q16 != nullptr;  // base dq on tensor memory
+    if (persistent && rows > 0) {
+        const long long n8 = rows * D / 8;
+        attn_bwd_q16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(
+            p.q, p.alpha, p.beta, p.q16, n8, p.Hq * D / 8, p.dev_err);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
     if (rows > 0) {
         attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
             p.o, p.dO, p.Drow, p.lse_in, p.lse, rows);
@@ -1754,7 +1753,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             } else {
                 k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
             }
-        } else if (p.lse_in != nullptr) {
+        } else if (persistent) {
             // base stream with the forward's log-sum-exp: the persistent tensor-memory kernel
             const size_t s1 = BpCfg<D>::SMEM;
             auto k1 = attn_bwd_dq_tc_base_kernel<D, G>;
@@ -1768,7 +1767,18 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             constexpr int UNITS = BpCfg<D>::ROWS / G;
             const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
             k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
-                maps[4], maps[5], maps[10], maps[11], maps[12], p);
+                maps[13], maps[5], maps[10], maps[11], maps[12], p);
+            if ((e = cudaGetLastError()) != cudaSuccess)
+                return e;
+            // dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]:
+            // 4 columns per thread, runs of token rows per CTA
+            const long long trows = static_cast<long long>(p.B) * p.n_units;
+            const int cols = p.Hq * D;
+            const unsigned gx = static_cast<unsigned>((cols / 4 + 255) / 256);
+            const long long gy_t = (2LL * sms * 4 + gx - 1) / gx, gy = trows < gy_t ? trows : gy_t;
+            const int per = static_cast<int>((trows + gy - 1) / gy);
+            attn_bwd_dab_kernel<<<dim3(gx, static_cast<unsigned>((trows + per - 1) / per)), 256, 0, stream>>>(
+                p.dq, p.q, p.alpha, p.dalpha, p.dbeta, trows, cols, per);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;

@@ -89,8 +89,8 @@ const float kLog2e = 1.4426950408889634f;
 // in rounds of 64 rows (64/G units x G heads) and K, V in blocks of 128 keys; for dQ, tiles
 // of 128 rows and K, V blocks of 64 keys; the fp16 copy of K in blocks of 128 and of 64;
 // K, V and the fp16 K in blocks of 32 (the base stream's persistent dQ)
-bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16, int d,
-              int Hq, int Hkv, int n_units, int T_kv, int B)
+bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16,
+              const void *q16, int d, int Hq, int Hkv, int n_units, int T_kv, int B)
 {
     const int G = Hq / Hkv;
     const long long qs = static_cast<long long>(n_units) * Hq * d, ks = static_cast<long long>(T_kv) * Hkv * d;
@@ -100,7 +100,8 @@ bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, cons
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
            make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 128) &&
            make_map(&m[9], k16, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[10], k, d, Hkv, T_kv, B, ks, 1, 32) &&
-           make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[12], k16, d, Hkv, T_kv, B, ks, 1, 32);
+           make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[12], k16, d, Hkv, T_kv, B, ks, 1, 32) &&
+           make_map(&m[13], q16, d, Hq, n_units, B, qs, G, 128 / G);
 }
 
 }  // namespace
@@ -362,7 +363,8 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
 {
     if (B < 1 || T < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d);
+    // + the fp16 q of the persistent dq kernel (used when the forward's lse is given)
+    return orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d) + 2 * static_cast<size_t>(B) * T * Hq * d;
 }
 
 orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
@@ -398,6 +400,8 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
     p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T, Hq));
+    p.q16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) +
+                                         orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d));
     p.dev_err = dev_err;
     p.B = B;
     p.n_units = T;
@@ -407,8 +411,8 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.accumulate = 0;
     p.scale = scale;
-    CUtensorMap maps[13];
-    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, d, Hq, Hkv, T, T, B))
+    CUtensorMap maps[14];
+    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
@@ -466,8 +470,8 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.window = T_kv;
     p.accumulate = accumulate ? 1 : 0;
     p.scale = scale;
-    CUtensorMap maps[13];
-    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
+    CUtensorMap maps[14];
+    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, p.k16, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
                   B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));

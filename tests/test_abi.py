@@ -107,7 +107,7 @@ def test_decode_workspace_size_and_checks(L):
 def test_swa_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 128)
-    assert n == 2 * 4 * 2 * 1000 * 32 + 2 * 2 * 1000 * 8 * 128  # lse, D per row; fp16 K
+    assert n == 2 * 4 * 2 * 1000 * 32 + 2 * 2 * 1000 * 8 * 128 + 2 * 2 * 1000 * 32 * 128  # lse, D; fp16 K, q
     assert L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 96) == 0
     assert L.orthros_swa_bwd_workspace_size(0, 1000, 32, 8, 128) == 0
 
