@@ -1324,9 +1324,9 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 template <int D>
 struct BpCfg {
     static constexpr int ROWS = 128;
-    static constexpr int KB = 32;
+    static constexpr int KB = 64;
     static constexpr int SLABS = D / 64;
-    static constexpr int STG = 3;
+    static constexpr int STG = 2;
     static constexpr int QSLAB = ROWS * 128;
     static constexpr int KSLAB = KB * 128;
     static constexpr int QBUF = 2 * SLABS * QSLAB;                 // one query buffer: q, dO
@@ -1336,7 +1336,7 @@ struct BpCfg {
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
     static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
     static constexpr int BAR_OFF = K16_OFF + STG * SLABS * KSLAB;
-    static constexpr int NBUF = 4;                                 // S / dP buffers
+    static constexpr int NBUF = 2;                                 // S / dP buffers
     static constexpr int NBARS = 2 * 2 + 2 * STG + 3 * NBUF + 2 * 2;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
@@ -1551,10 +1551,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     break;
                 tc_fence_after();
                 const int k0 = (kb0 + j) * C::KB;
-                {
+#pragma unroll
+                for (int half = 0; half < C::KB / 32; ++half) {
                     uint32_t sv[32], dv[32];
-                    tmem_ld32(tl + C::TM_S + C::KB * u, sv);
-                    tmem_ld32(tl + C::TM_DP + C::KB * u, dv);
+                    tmem_ld32(tl + C::TM_S + C::KB * u + 32 * half, sv);
+                    tmem_ld32(tl + C::TM_DP + C::KB * u + 32 * half, dv);
                     tmem_wait_ld();
                     uint32_t dw[16];
 #pragma unroll
@@ -1562,7 +1563,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         float ds[2];
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
-                            const int key = k0 + 2 * e + q;
+                            const int key = k0 + 32 * half + 2 * e + q;
                             const float pr = (key <= P && key >= lo)
                                                  ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
                                                  : 0.f;
@@ -1570,7 +1571,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         }
                         dw[e] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    tmem_st16(tl + C::TM_DP + C::KB * u, dw);
+                    tmem_st16(tl + C::TM_DP + C::KB * u + 16 * half, dw);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -1767,7 +1768,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             constexpr int UNITS = BpCfg<D>::ROWS / G;
             const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
             k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
-                maps[13], maps[5], maps[10], maps[11], maps[12], p);
+                maps[13], maps[5], maps[6], maps[7], maps[9], p);
             if ((e = cudaGetLastError()) != cudaSuccess)
                 return e;
             // dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]:
