@@ -450,12 +450,13 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
     del grads, dO, dOc, ws, wsc, lse, q
-    # launches per call: fp16 K copy, D, dq, dk/dv for each stream; the copies' dq splits the
-    # keys when one row tile per (batch, KV head) holds all copies (mirror of attn_bwd.cu)
+    # launches per call (mirror of attn_bwd.cu): base stream with the log-sum-exp: fp16 K, fp16 q,
+    # D, dq, the dalpha / dbeta sums, dk/dv; copies: fp16 K, D, dq, dk/dv, and two more (a second
+    # dq pass and the combine) when one row tile per (batch, KV head) holds all copies
     G = Hq // Hkv
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     split = T_out <= 128 // G and min(64, 2 * sms // (B * Hkv), -(-T // 64) // 8) >= 2
-    per_call = 8 + (2 if (split and T_out > 0) else 0)
+    per_call = 6 + 4 + (2 if (split and T_out > 0) else 0)
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
