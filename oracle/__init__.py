@@ -53,10 +53,11 @@ def _load():
             lib.oracle_swa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_swa_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, D]
+            lib.oracle_xattn_lse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                                I, I, I, I, I, D]
             for f in (lib.oracle_swa, lib.oracle_swa_rows, lib.oracle_xattn, lib.oracle_decode_step,
-                      lib.oracle_swa_bwd, lib.oracle_xattn_bwd, lib.oracle_swa_lse):
+                      lib.oracle_swa_bwd, lib.oracle_xattn_bwd, lib.oracle_swa_lse, lib.oracle_xattn_lse):
                 f.restype = I
             _lib = lib
     return _lib
@@ -124,6 +125,23 @@ def swa_lse(q_raw, k, alpha, beta, window: int, scale: float) -> np.ndarray:
     rc = _load().oracle_swa_lse(pq, pk, pa, pb, out.ctypes.data_as(ctypes.c_void_p), B, T, Hq, Hkv, d,
                                 int(window), float(scale))
     _check(rc, "swa_lse")
+    return out
+
+
+def xattn_lse(qc_raw, pos, k, alpha_c, beta_c, scale: float) -> np.ndarray:
+    """Each copy row's log-sum-exp of Eq. (5)'s scaled logits over keys 0..pos (natural log),
+    fp64 [B,T_out,Hq]."""
+    B, T_out, Hq, d = qc_raw.shape
+    T_kv, Hkv = k.shape[1], k.shape[2]
+    qc_raw, pq = _c(qc_raw, np.uint16)
+    pos, pp = _c(pos, np.int32)
+    k, pk = _c(k, np.uint16)
+    alpha_c, pa = _c(alpha_c, np.float32)
+    beta_c, pb = _c(beta_c, np.float32)
+    out = np.zeros((B, T_out, Hq), np.float64)
+    rc = _load().oracle_xattn_lse(pq, pp, pk, pa, pb, out.ctypes.data_as(ctypes.c_void_p), B, T_out, T_kv, Hq, Hkv,
+                                  d, float(scale))
+    _check(rc, "xattn_lse")
     return out
 
 

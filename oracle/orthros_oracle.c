@@ -559,3 +559,56 @@ int oracle_swa_lse(const uint16_t *q_raw, const uint16_t *k, const float *alpha,
     }
     return bad ? -2 : 0;
 }
+
+/*
+ * Each copy row's log-sum-exp, Eq. (5): lse[b, i, h] = ln sum_{0 <= j <= pos[b, i]}
+ * exp(scale * q'_i . k_j) with q'_i = qc_raw * alpha_c + beta_c, the normaliser of the
+ * copy's softmax over the base keys up to its original position.  lse: fp64 [B, T_out, Hq].
+ * Returns 0, or -1 on a bad argument (a position outside [0, T_kv)).
+ */
+int oracle_xattn_lse(const uint16_t *qc_raw, const int32_t *pos, const uint16_t *k, const float *alpha_c,
+                     const float *beta_c, double *lse, int B, int T_out, int T_kv, int Hq, int Hkv, int d,
+                     double scale)
+{
+    if (!shapes_ok(B, T_kv, Hq, Hkv, d) || T_out < 0)
+        return -1;
+    for (int64_t i = 0; i < (int64_t)B * T_out; ++i)
+        if (pos[i] < 0 || pos[i] >= T_kv)
+            return -1;
+    const int group = Hq / Hkv;
+    const int64_t kv_row = (int64_t)Hkv * d;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)T_kv);
+        if (!q || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t job = 0; job < (int64_t)B * T_out * Hq; ++job) {
+                const int64_t bi = job / Hq, b = bi / T_out;
+                const int h = (int)(job % Hq);
+                const uint16_t *kb = k + (b * T_kv * Hkv + h / group) * d;
+                scale_offset_row(qc_raw + job * d, alpha_c + (int64_t)h * d, beta_c + (int64_t)h * d, d, q);
+                double m = -INFINITY;
+                for (int64_t j = 0; j <= pos[bi]; ++j) {
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        acc += q[e] * bf16_to_double(kb[j * kv_row + e]);
+                    s[j] = acc * scale;
+                    if (s[j] > m)
+                        m = s[j];
+                }
+                double sum = 0.0;
+                for (int64_t j = 0; j <= pos[bi]; ++j)
+                    sum += exp(s[j] - m);
+                lse[job] = m + log(sum);
+            }
+        }
+        free(q);
+        free(s);
+    }
+    return bad ? -2 : 0;
+}

@@ -564,3 +564,43 @@ def test_swa_lse_equals_scipy_logsumexp(T, Hq, Hkv, d, w):
     band = _band(T, w)  # True where key s is in row t's window
     ref = logsumexp(np.where(band[None, None], logits, -np.inf), axis=-1).transpose(0, 2, 1)
     np.testing.assert_allclose(oracle.swa_lse(q, k, a, b, w, scale), ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- row log-sum-exp of Eq. (5)
+
+def test_xattn_lse_of_zero_keys_is_log_of_position_count():
+    """K = 0: every logit is 0, so a copy at position p has lse = ln(p + 1) exactly."""
+    _, k, _, _, _ = _rand_inputs(95, 2, 50, 4, 2, 16)
+    k = np.zeros_like(k)
+    qc = normal_bf16(95, "qc_raw", (2, 6, 4, 16))
+    a, b = scale_offset(95, 4, 16, prefix="_c")
+    pos = np.array([[0, 49, 7, 7, 20, 1], [3, 0, 48, 12, 49, 5]], np.int32)
+    got = oracle.xattn_lse(qc, pos, k, a, b, 0.3)
+    want = np.broadcast_to(np.log(pos.astype(np.float64) + 1.0)[:, :, None], got.shape)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("T_kv,T_out,Hq,Hkv,d", [(40, 9, 4, 2, 16), (70, 5, 8, 1, 32)])
+def test_xattn_lse_equals_scipy_logsumexp(T_kv, T_out, Hq, Hkv, d):
+    """Library reference: scipy's logsumexp over keys 0..pos of float64 logits from einsum."""
+    from scipy.special import logsumexp
+    _, k, _, _, _ = _rand_inputs(96 + T_kv, 1, T_kv, Hq, Hkv, d)
+    qc = normal_bf16(96 + T_kv, "qc_raw", (1, T_out, Hq, d))
+    a, b = scale_offset(96 + T_kv, Hq, d, prefix="_c")
+    pos = np.random.default_rng(T_kv).integers(0, T_kv, size=(1, T_out)).astype(np.int32)
+    scale = 1.0 / math.sqrt(d)
+    qq = _w(qc) * a.astype(np.float64) + b.astype(np.float64)
+    kq = np.repeat(_w(k), Hq // Hkv, axis=2)
+    logits = np.einsum("bihd,bshd->bhis", qq, kq) * scale
+    seen = np.arange(T_kv)[None, None, :] <= pos[:, :, None]  # [1, T_out, T_kv]
+    ref = logsumexp(np.where(seen[:, None], logits, -np.inf), axis=-1).transpose(0, 2, 1)
+    np.testing.assert_allclose(oracle.xattn_lse(qc, pos, k, a, b, scale), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_xattn_lse_of_copies_at_every_position_is_the_full_causal_lse():
+    """PT mode: copies of every base row, with the base rows' own q, see keys 0..t -- the
+    base stream's lse with a window covering the whole sequence."""
+    q, k, _, a, b = _rand_inputs(97, 2, 33, 4, 2, 16)
+    pos = np.tile(np.arange(33, dtype=np.int32), (2, 1))
+    np.testing.assert_allclose(oracle.xattn_lse(q, pos, k, a, b, 0.25), oracle.swa_lse(q, k, a, b, 33, 0.25),
+                               rtol=1e-13, atol=1e-13)
