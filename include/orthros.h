@@ -288,10 +288,12 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  * exactly from bf16 into the workspace and q rounded once to fp16, as the
  * forward's tensor-memory path (|k| >= 65520 or |q| >= 65504 sets
  * ORTHROS_DEVERR_RANGE); the dq kernel used without lse (warp MMAs) takes q as
- * a bf16 high part plus residual.  P and dS are rounded to bf16 before they
- * multiply dO, K and q; q enters dk rounded once to bf16.  Launches: the fp16
- * copy of K, D_t (which also converts a given lse), dq (rows on the MMA's M
- * side: with lse a persistent tensor-memory kernel, else a two-pass warp-MMA
+ * a bf16 high part plus residual.  P is rounded to bf16 before it multiplies
+ * dO; dS is rounded to bf16 before it multiplies K (dq) and to fp16 before it
+ * multiplies the fp16 q (dk; |dS| >= 65504 sets ORTHROS_DEVERR_RANGE).
+ * Launches: the fp16 copies of K and of q, D_t (which also converts a given
+ * lse), dq (rows on the MMA's M side: with lse a persistent tensor-memory
+ * kernel followed by a column sum for dalpha, dbeta; else a two-pass warp-MMA
  * one that stores each row's log-sum-exp), then dk and dv (keys on the M side,
  * tensor memory, no atomics).  dq, dk, dv have one writer per element;
  * dalpha, dbeta are summed with atomics.  dev_err (optional) as elsewhere.
@@ -308,7 +310,8 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
 
 /*
  * Bytes of device workspace orthros_xattn_bwd needs (two fp32 values per copy
- * row and an fp16 copy of K).  Returns 0 for invalid sizes.
+ * row, fp16 copies of K and of the copies' scale-offset q, and per-split row
+ * partials of the split dq path).  Returns 0 for invalid sizes.
  */
 size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d);
 

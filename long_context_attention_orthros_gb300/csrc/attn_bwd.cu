@@ -467,21 +467,21 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
 
 // A CTA owns 128 keys of one (batch, KV head): the MMA's M side, K and V resident in
 // shared memory (one TMA load each).  The query rows that can see them stream through
-// a three-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
-// lands them): per round
-//   S^T  = K q^T          (fp16: K from the call's exact fp16 copy, q rounded once; a
-//                         query outside the fp16 range sets ORTHROS_DEVERR_RANGE)
+// a four-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
+// lands them): q as fp16 (the scale-offset applied and rounded once by
+// attn_bwd_q16_kernel, which also flags a query outside the fp16 range) and dO.  Per round
+//   S^T  = K q^T          (fp16: K from the call's exact fp16 copy)
 //   dP^T = V dO^T         (bf16) fp32 in tensor memory (two buffers each)
-//   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), both
-//          written back over S^T / dP^T as bf16 by the softmax warps (lane = key)
-//   dV  += P^T dO,  dK += dS^T q           (A from tensor memory, B = the row tiles; q bf16)
+//   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), written
+//          back over S^T (P^T, bf16) and dP^T (dS^T, fp16; |dS| >= 65504 sets
+//          ORTHROS_DEVERR_RANGE) by the softmax warps (lane = key)
+//   dV  += P^T dO,  dK += dS^T q           (A from tensor memory, B = the row tiles)
 // and dK, dV (fp32, tensor memory) leave once at the end.  The MMA issuer computes S^T,
 // dP^T of round i + 1 while the softmax works on round i.
-// Roles (384 threads, one CTA per SM):
-//   warp 0      TMA producer (K, V once; q raw and dO per round)
+// Roles (256 threads, one CTA per SM):
+//   warp 0      TMA producer (K, V once; q and dO per round)
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2-3, 8-11  per round turn the raw query tile into q = x alpha + beta (fp16 in
-//               place, bf16 beside it) and stage each row's lse, D and position
+//   warps 2-3   stage each round's per-row lse, D and position (one row per thread)
 //   warps 4-7   P^T, dS^T (tensor-memory lane = key), then the dK / dV epilogue
 // Tensor memory: S^T at 64 u, dP^T at 128 + 64 u (buffer u), dK at 256, dV at 256 + D.
 // Every wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and every role drains
@@ -491,16 +491,15 @@ struct BtCfg {
     static constexpr int KEYS = 128;          // keys of a CTA (the MMA's M)
     static constexpr int RB = 64;             // query rows per round (N of S^T, dP^T)
     static constexpr int SLABS = D / 64;
-    static constexpr int STG = 3;
+    static constexpr int STG = 4;
     static constexpr int KSLAB = KEYS * 128;  // one 64-wide slab of the K (or V) tile
     static constexpr int RSLAB = RB * 128;    // one 64-wide slab of a row tile
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + SLABS * KSLAB;
     static constexpr int ST_OFF = V_OFF + SLABS * KSLAB;
-    static constexpr int ST_Q16 = 0;                  // raw x, then q as fp16
-    static constexpr int ST_QB = SLABS * RSLAB;       // q as bf16
-    static constexpr int ST_DO = 2 * SLABS * RSLAB;   // dO
-    static constexpr int ST_BYTES = 3 * SLABS * RSLAB;
+    static constexpr int ST_Q16 = 0;                  // scale-offset q as fp16 (from the workspace)
+    static constexpr int ST_DO = SLABS * RSLAB;       // dO
+    static constexpr int ST_BYTES = 2 * SLABS * RSLAB;
     static constexpr int META_OFF = ST_OFF + STG * ST_BYTES;  // [STG][3][RB]: lse, D, position
     static constexpr int BAR_OFF = META_OFF + STG * 3 * RB * 4;
     static constexpr int NBARS = 1 + 3 * STG + 3 * 2 + 1;
@@ -569,10 +568,11 @@ __device__ __forceinline__ int next_round(const AttnBwdParams &p, int b, int kt0
 }
 
 constexpr int DKV_TC_THREADS = 384;
-constexpr int DKV_TC_CONV = 192;  // preparation threads (warps 2-3 and 8-11)
+constexpr int DKV_TC_CONV = 192;  // preparation threads of the dQ kernel (warps 2-3 and 8-11)
+constexpr int DKV_THREADS = 256;  // the dK/dV kernel: producer, MMA, 2 metadata warps, 4 softmax warps
 
 template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnBwdParams p)
@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *kv_full = bars;                     // K, V landed
     uint64_t *st_full = bars + 1;                 // [STG] row tiles landed
-    uint64_t *qconv = bars + 1 + C::STG;          // [STG] q prepared, row metadata staged
+    uint64_t *qconv = bars + 1 + C::STG;          // [STG] row metadata staged
     uint64_t *st_empty = bars + 1 + 2 * C::STG;   // [STG] round's MMAs done with the stage
     uint64_t *s_full = bars + 1 + 3 * C::STG;     // [2] S^T, dP^T of a round complete
     uint64_t *p_full = s_full + 2;                // [2] P^T, dS^T written
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         mbar_init(kv_full, 1);
         for (int s = 0; s < C::STG; ++s) {
             mbar_init(&st_full[s], 1);
-            mbar_init(&qconv[s], DKV_TC_CONV / 32);
+            mbar_init(&qconv[s], 2);
             mbar_init(&st_empty[s], 1);
         }
         for (int u = 0; u < 2; ++u) {
@@ -662,10 +662,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         // ------------------------------------------------------------------ MMA issuer
         constexpr uint32_t IDESC_S = umma_idesc(128, C::RB, false, false);   // fp16
         constexpr uint32_t IDESC_DP = umma_idesc(128, C::RB, true, false);   // bf16
-        constexpr uint32_t IDESC_ACC = umma_idesc(128, D, true, true);
+        constexpr uint32_t IDESC_DV = umma_idesc(128, D, true, true);    // bf16 P^T, dO
+        constexpr uint32_t IDESC_DK = umma_idesc(128, D, false, true);   // fp16 dS^T, q
         const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF, 16, 1024);
         const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF, 16, 1024);
-        // dV += P^T dO and dK += dS^T q_high of round j
+        // dV += P^T dO and dK += dS^T q of round j
         auto accumulate = [&](int j) -> bool {
             const int u = j & 1, s = j % C::STG;
             if (!warp_wait(&p_full[u], static_cast<uint32_t>((j >> 1) & 1)))
@@ -674,14 +675,14 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 tc_fence_after();
                 const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
                 const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, C::RSLAB, 1024);
-                const uint64_t qdesc = umma_desc_sw128(st + C::ST_QB, C::RSLAB, 1024);
+                const uint64_t qdesc = umma_desc_sw128(st + C::ST_Q16, C::RSLAB, 1024);
 #pragma unroll
                 for (int kk = 0; kk < C::RB / 16; ++kk) {
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                     umma_ts(tbase + C::TM_DV, tbase + C::TM_S + 64 * u + 8 * kk,
-                            odesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_ACC, acc);
+                            odesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DV, acc);
                     umma_ts(tbase + C::TM_DK, tbase + C::TM_DP + 64 * u + 8 * kk,
-                            qdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_ACC, acc);
+                            qdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DK, acc);
                 }
                 umma_commit(&pv_done[u]);
                 umma_commit(&st_empty[s]);
@@ -694,8 +695,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
              r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
             const int s = i % C::STG, u = i & 1;
-            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1)) &&
-                       warp_wait(&qconv[s], static_cast<uint32_t>((i / C::STG) & 1))))
+            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
                 break;
             // S^T / dP^T buffer u is free once dV, dK of round i - 2 have read P^T, dS^T from it
             if (i >= 2 && !(ok = warp_wait(&pv_done[u], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
@@ -724,18 +724,17 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                 umma_commit(acc_final);
             __syncwarp();
         }
-    } else if (warp < 4 || warp >= 8) {
-        // ------------------------------------------------------------------ query preparation
-        const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 256 + 64;  // 0..191
-        bool bad = false;
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ row metadata
+        const int ct = threadIdx.x - 64;  // 0..63: one row of the round each
         int i = 0;
         for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
              r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
             const int s = i % C::STG;
-            // this round's row metadata, loaded before the wait so that its latency overlaps
+            // loaded before the wait so that the latency overlaps it
             float m_lse = 0.f, m_d = 0.f;
             int m_pos = -1;
-            if (ct < C::RB) {
+            {
                 const int u = r * UNITS + ct / G, h = g * G + ct % G;
                 m_pos = unit_pos<COPY>(p, b, u);
                 if (m_pos >= 0) {
@@ -744,40 +743,25 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     m_d = p.Drow[ri];
                 }
             }
+            // the slot is free once the stage of this round has landed: its producer waited
+            // for the MMAs of round i - STG, which waited for that round's softmax
             if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
                 break;
-            uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
-#pragma unroll 2
-            for (int idx = ct; idx < C::RB * C::SLABS * 8; idx += DKV_TC_CONV) {
-                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
-                const int sl = rem / 8, c8 = rem % 8;
-                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
-                const uint32_t off = sl * C::RSLAB + sw128_offset(row, c8);
-                uint4 *qp = reinterpret_cast<uint4 *>(st + C::ST_Q16 + off);
-                uint4 q16, qb;
-                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
-                *qp = q16;
-                *reinterpret_cast<uint4 *>(st + C::ST_QB + off) = qb;
-            }
-            if (ct < C::RB) {  // one row per thread
-                float *m = meta + s * 3 * C::RB;
-                m[ct] = m_lse;
-                m[C::RB + ct] = m_d;
-                m[2 * C::RB + ct] = __int_as_float(m_pos);
-            }
-            fence_proxy_async_smem();  // the MMA reads q through the async proxy
+            float *m = meta + s * 3 * C::RB;
+            m[ct] = m_lse;
+            m[C::RB + ct] = m_d;
+            m[2 * C::RB + ct] = __int_as_float(m_pos);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&qconv[s]);
         }
-        if (bad)
-            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
         // ------------------------------------------------------------------ P^T, dS^T + epilogue
         const int rw = warp - 4;
         const int key = kt0 + rw * 32 + lane;
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
         const float c2 = p.scale * kLog2eF;
+        float ds_max = 0.f;  // dS^T goes to fp16: |dS| < 65504 or the range error
         int i = 0;
         for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
              r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
@@ -805,8 +789,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         pr[q] = valid ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - m[c]) : 0.f;
                         ds[q] = pr[q] * (__uint_as_float(dv[2 * e + q]) - m[C::RB + c]);
                     }
+                    ds_max = fmaxf(ds_max, fmaxf(fabsf(ds[0]), fabsf(ds[1])));
                     pw[e] = pack_bf16x2(pr[0], pr[1]);
-                    dw[e] = pack_bf16x2(ds[0], ds[1]);
+                    __half2 hv = __floats2half2_rn(ds[0], ds[1]);
+                    dw[e] = *reinterpret_cast<uint32_t *>(&hv);
                 }
                 tmem_st16(tl + C::TM_S + 64 * u + 16 * half, pw);
                 tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
@@ -817,6 +803,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(&p_full[u]);
         }
+        if (!(ds_max < 65504.f))
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         // ---- epilogue: dK (scaled), dV of this key -> global (written, or added)
         const bool have = ok && i > 0;
         if (have && !(ok = warp_wait(acc_final, 0))) {
@@ -1699,8 +1687,9 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    const bool persistent = !COPY && p.lse_in != nullptr && p.q16 != nullptr;  // base dq on tensor memory
-    if (persistent && rows > 0) {
+    // the fp16 scale-offset q: read by the dK/dV kernel and the base stream's persistent dQ
+    const bool persistent = !COPY && p.lse_in != nullptr;  // base dq on tensor memory
+    if (rows > 0) {
         const long long n8 = rows * D / 8;
         attn_bwd_q16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(
             p.q, p.alpha, p.beta, p.q16, n8, p.Hq * D / 8, p.dev_err);
@@ -1743,16 +1732,16 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                 ps.splits = splits;
                 ps.split_mode = 1;
                 dim3 gs(1, p.B * p.Hkv, splits);
-                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], ps);
+                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
                 if ((e = cudaGetLastError()) != cudaSuccess)
                     return e;
                 attn_bwd_lse_combine_kernel<G><<<p.B * p.Hkv, 128, 0, stream>>>(ps);
                 if ((e = cudaGetLastError()) != cudaSuccess)
                     return e;
                 ps.split_mode = 2;
-                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], ps);
+                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
             } else {
-                k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[9], p);
+                k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], p);
             }
         } else if (persistent) {
             // base stream with the forward's log-sum-exp: the persistent tensor-memory kernel
@@ -1768,7 +1757,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             constexpr int UNITS = BpCfg<D>::ROWS / G;
             const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
             k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
-                maps[13], maps[5], maps[6], maps[7], maps[9], p);
+                maps[9], maps[5], maps[6], maps[7], maps[8], p);
             if ((e = cudaGetLastError()) != cudaSuccess)
                 return e;
             // dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]:
@@ -1800,7 +1789,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         cudaSuccess)
         return e;
     dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-    k3<<<g3, DKV_TC_THREADS, s3, stream>>>(maps[0], maps[1], maps[8], maps[3], p);
+    k3<<<g3, DKV_THREADS, s3, stream>>>(maps[0], maps[1], maps[3], maps[2], p);
     return cudaGetLastError();
 }
 

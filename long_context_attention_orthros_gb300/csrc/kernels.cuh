@@ -68,7 +68,7 @@ struct AttnBwdParams {
     float *dq, *dk, *dv, *dalpha, *dbeta;    // dq = gradient of q raw; dalpha / dbeta zeroed first
     float *lse, *Drow;                       // workspace [B*n_units*Hq] each: log2-sum-exp, dO . o
     uint16_t *k16;                           // workspace: K as fp16 [B, T_kv, Hkv, d]
-    uint16_t *q16;                           // workspace (base stream with lse): q as fp16 [B, n_units, Hq, d]
+    uint16_t *q16;                           // workspace: q = x alpha + beta as fp16 [B, n_units, Hq, d]
     int32_t *dev_err;
     int B, n_units, T_kv, Hq, Hkv, window;   // window = T_kv for the copies
     int accumulate;                          // add to dk, dv instead of overwriting them
@@ -86,11 +86,11 @@ size_t attn_bwd_k16_offset(int B, int n_units, int Hq);
 // extra workspace of the copies' gradient: per-split row partials of the split dq path
 constexpr int ATTN_BWD_MAX_SPLITS = 64;
 size_t attn_bwd_split_bytes(int B, int Hkv);
-// maps of the tensor-memory kernels: [0..3] {q raw, dO} with boxes of
-// 64 x G heads x 64/G units and {K, V} with boxes of 64 x 1 x 128 keys (dK/dV); [4..7] {q raw, dO}
-// with boxes of 64 x G x 128/G and {K, V} with boxes of 64 x 1 x 64 (dQ); [8], [9] the fp16 copy
-// of K (p.k16) with boxes of 128 and of 64 keys; [10..12] K, V, fp16 K with boxes of 32 keys;
-// [13] the fp16 q (p.q16) with boxes of 64 x G x 128/G
+// maps of the tensor-memory kernels: [0], [1] the fp16 q (p.q16) and dO with boxes of
+// 64 x G heads x 64/G units, [2], [3] V and the fp16 copy of K (p.k16) with boxes of
+// 64 x 1 x 128 keys (dK/dV); [4], [5] q raw and dO with boxes of 64 x G x 128/G, [6..8] K, V
+// and the fp16 K with boxes of 64 x 1 x 64 (dQ); [9] the fp16 q with boxes of 64 x G x 128/G
+constexpr int ATTN_BWD_MAPS = 10;
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -85,23 +85,22 @@ bool resolve_bstride(long long &s, long long dense)
 
 const float kLog2e = 1.4426950408889634f;
 
-// tensor maps of the gradient's kernels: for dK/dV, query rows and their output gradient
-// in rounds of 64 rows (64/G units x G heads) and K, V in blocks of 128 keys; for dQ, tiles
-// of 128 rows and K, V blocks of 64 keys; the fp16 copy of K in blocks of 128 and of 64;
-// K, V and the fp16 K in blocks of 32 (the base stream's persistent dQ)
+// tensor maps of the gradient's kernels: for dK/dV, the fp16 q and dO in rounds of 64 rows
+// (64/G units x G heads), V and the fp16 K in blocks of 128 keys; for dQ, raw q and dO in
+// tiles of 128 rows, K, V and the fp16 K in blocks of 64 keys, and the fp16 q in tiles of 128
+// rows (the base stream's persistent dQ)
 bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16,
               const void *q16, int d, int Hq, int Hkv, int n_units, int T_kv, int B)
 {
     const int G = Hq / Hkv;
     const long long qs = static_cast<long long>(n_units) * Hq * d, ks = static_cast<long long>(T_kv) * Hkv * d;
-    return make_map(&m[0], q, d, Hq, n_units, B, qs, G, 64 / G) && make_map(&m[1], dO, d, Hq, n_units, B, qs, G, 64 / G) &&
-           make_map(&m[2], k, d, Hkv, T_kv, B, ks, 1, 128) && make_map(&m[3], v, d, Hkv, T_kv, B, ks, 1, 128) &&
+    return make_map(&m[0], q16, d, Hq, n_units, B, qs, G, 64 / G) &&
+           make_map(&m[1], dO, d, Hq, n_units, B, qs, G, 64 / G) &&
+           make_map(&m[2], v, d, Hkv, T_kv, B, ks, 1, 128) && make_map(&m[3], k16, d, Hkv, T_kv, B, ks, 1, 128) &&
            make_map(&m[4], q, d, Hq, n_units, B, qs, G, 128 / G) &&
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
-           make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 128) &&
-           make_map(&m[9], k16, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[10], k, d, Hkv, T_kv, B, ks, 1, 32) &&
-           make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[12], k16, d, Hkv, T_kv, B, ks, 1, 32) &&
-           make_map(&m[13], q16, d, Hq, n_units, B, qs, G, 128 / G);
+           make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 64) &&
+           make_map(&m[9], q16, d, Hq, n_units, B, qs, G, 128 / G);
 }
 
 }  // namespace
@@ -411,7 +410,7 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.window = window;
     p.accumulate = 0;
     p.scale = scale;
-    CUtensorMap maps[14];
+    CUtensorMap maps[orthros::ATTN_BWD_MAPS];
     if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
@@ -422,7 +421,8 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
 {
     if (B < 1 || T_out < 0 || T_kv < 1 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return 0;
-    return orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d) + orthros::attn_bwd_split_bytes(B, Hkv);
+    return orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d) + orthros::attn_bwd_split_bytes(B, Hkv) +
+           2 * static_cast<size_t>(B) * T_out * Hq * d;  // the copies' fp16 q
 }
 
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
@@ -461,6 +461,7 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T_out, Hq));
     p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
                                            orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d));
+    p.q16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(p.part_ml) + orthros::attn_bwd_split_bytes(B, Hkv));
     p.dev_err = dev_err;
     p.B = B;
     p.n_units = T_out;
@@ -470,9 +471,9 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.window = T_kv;
     p.accumulate = accumulate ? 1 : 0;
     p.scale = scale;
-    CUtensorMap maps[14];
-    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, p.k16, d, Hq, Hkv, T_out > 0 ? T_out : 1, T_kv,
-                  B))
+    CUtensorMap maps[orthros::ATTN_BWD_MAPS];
+    if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, T_out > 0 ? p.q16 : p.k16, d, Hq, Hkv,
+                  T_out > 0 ? T_out : 1, T_kv, B))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;

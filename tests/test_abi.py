@@ -123,7 +123,8 @@ def test_swa_bwd_workspace_size_and_checks(L):
 def test_xattn_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 128)
-    assert n == 2 * 4 * 4 * 2048 * 32 + 2 * 4 * 16384 * 8 * 128 + 4 * 8 * 64 * 128 * 8  # + split partials
+    # row lse and D, fp16 K, split partials, the copies' fp16 q
+    assert n == 2 * 4 * 4 * 2048 * 32 + 2 * 4 * 16384 * 8 * 128 + 4 * 8 * 64 * 128 * 8 + 2 * 4 * 2048 * 32 * 128
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 0, 32, 8, 128) == 0
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 96) == 0
 
