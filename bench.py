@@ -428,14 +428,17 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     qc = g["qc"].contiguous()
     q = g["q"] if g["q"].shape[1] == T else g["q"][:, :T].contiguous()  # appended copies: base rows only
     stream = torch.cuda.current_stream(dev)
-    # a training forward keeps each row's log-sum-exp; the gradient takes it
+    # a training forward keeps each row's log-sum-exp (both streams); the gradient takes it
     _, lse = orth.swa_fwd_lse(q, g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale)
+    lsec = None
+    if T_out > 0:
+        _, lsec = orth.xattn_fwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], scale=cfg.scale, lse=True)
 
     def call():
         base = orth.swa_bwd(q, g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
                             scale=cfg.scale, workspace=ws, lse=lse)
         copy = orth.xattn_bwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], oc, dOc, scale=cfg.scale,
-                              dk=base[1], dv=base[2], workspace=wsc)
+                              dk=base[1], dv=base[2], workspace=wsc, lse=lsec)
         return base + copy
 
     for _ in range(3):
@@ -449,21 +452,18 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
-    del grads, dO, dOc, ws, wsc, lse, q
+    del grads, dO, dOc, ws, wsc, lse, lsec, q
     # launches per call (mirror of attn_bwd.cu): base stream with the log-sum-exp: fp16 K, fp16 q,
-    # D, dq, the dalpha / dbeta sums, dk/dv; copies: fp16 K, D, dq, dk/dv, and two more (a second
-    # dq pass and the combine) when one row tile per (batch, KV head) holds all copies
-    G = Hq // Hkv
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    split = T_out <= 128 // G and min(64, 2 * sms // (B * Hkv), -(-T // 64) // 8) >= 2
-    per_call = 6 + 4 + (2 if (split and T_out > 0) else 0)
+    # D, dq, the dalpha / dbeta sums, dk/dv; copies with theirs: fp16 K, fp16 q, D, dq (one pass,
+    # or split over the keys when one row tile per (batch, KV head) holds all copies), dk/dv
+    per_call = 6 + (5 if T_out > 0 else 2)
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
     flops = 10 * d * pairs
     tfs = flops / (ms / 1e3) / 1e12
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
-            "what": "swa_bwd (with the forward's log-sum-exp) + xattn_bwd (copies' share added into dK/dV)",
+            "what": "swa_bwd + xattn_bwd (copies' share added into dK/dV), each with its forward's log-sum-exp",
             "roofline": {"kernel": f"attn_bwd ({per_call} launches)", "bound": "tensor", "achieved": tfs,
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
                          "peak_kind": peak_kind, "algorithmic_flops": flops},

@@ -162,6 +162,22 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  void *stream);
 
 /*
+ * orthros_xattn_fwd that also writes, for training, each copy row's log-sum-exp:
+ *   lse[b, i, h] = ln sum_{0 <= j <= pos[b, i]} exp(scale * q'_i . k_j)
+ * (fp32 [B, T_out, Hq], dense; -inf for a copy whose position is out of range),
+ * the normaliser of the copy's softmax, which orthros_xattn_bwd can take instead
+ * of recomputing it.  lse must be 16-byte aligned; other arguments as
+ * orthros_xattn_fwd.
+ */
+orthros_status orthros_xattn_fwd_lse(const orthros_bf16 *qc_raw, const int32_t *pos,
+                                     const orthros_bf16 *k, const orthros_bf16 *v,
+                                     const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
+                                     float *lse, int B, int T_out, int T_kv, int Hq, int Hkv, int d,
+                                     float scale, int64_t qc_bstride, int64_t kv_bstride,
+                                     int64_t oc_bstride, void *workspace, size_t ws_bytes,
+                                     int32_t *dev_err, void *stream);
+
+/*
  * Bytes of device workspace orthros_prefill_fwd needs for these sizes (that of
  * the copies' cross-attention).  Returns 0 for invalid sizes.
  */
@@ -329,22 +345,25 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
  *
  *   qc_raw, oc, dOc [B, T_out, Hq, d] bf16, dense; pos [B, T_out] int32
  *   k, v [B, T_kv, Hkv, d] bf16, dense; alpha_c, beta_c [Hq, d] fp32
+ *   lse: NULL, or the forward's per-copy-row log-sum-exp (orthros_xattn_fwd_lse),
+ *        which saves the dq kernel its first pass over the keys
  *   dqc_raw [B, T_out, Hq, d], dk, dv [B, T_kv, Hkv, d], dalpha_c, dbeta_c
  *   [Hq, d]: fp32 outputs (dalpha_c and dbeta_c are zeroed first)
  *   workspace: orthros_xattn_bwd_workspace_size(...) bytes, 16-byte aligned.
  * A copy whose position is outside [0, T_kv) gets a zero row of dqc_raw,
  * contributes nothing, and sets ORTHROS_DEVERR_POSITION in *dev_err.
  * Arithmetic and launches as orthros_swa_bwd, with the dq kernel on tensor
- * memory in two passes (the first finds each copy row's log-sum-exp); when one
- * 128-row tile per (batch, KV head) holds every copy, its key range is split
- * over many CTAs (per-split maxima and sums, a combine, per-split dq added up).
+ * memory in two passes (the first finds each copy row's log-sum-exp; skipped
+ * when lse is given); when one 128-row tile per (batch, KV head) holds every
+ * copy, its key range is split over many CTAs (without lse: per-split maxima
+ * and sums and a combine first; then per-split dq added up).
  * T_out == 0 leaves dk, dv as they are (accumulate) or zero.  Outputs must not
  * alias inputs.
  */
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  const orthros_bf16 *k, const orthros_bf16 *v,
                                  const float *alpha_c, const float *beta_c,
-                                 const orthros_bf16 *oc, const orthros_bf16 *dOc,
+                                 const orthros_bf16 *oc, const orthros_bf16 *dOc, const float *lse,
                                  float *dqc_raw, float *dk, float *dv, float *dalpha_c,
                                  float *dbeta_c, int B, int T_out, int T_kv, int Hq, int Hkv,
                                  int d, float scale, int accumulate, void *workspace,

@@ -77,8 +77,11 @@ def lib() -> ctypes.CDLL:
             L.orthros_xattn_bwd_workspace_size.restype = SZ
             L.orthros_xattn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
             L.orthros_xattn_bwd.restype = I
-            L.orthros_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I,
-                                            P, SZ, P, P]
+            L.orthros_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F,
+                                            I, P, SZ, P, P]
+            L.orthros_xattn_fwd_lse.restype = I
+            L.orthros_xattn_fwd_lse.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64,
+                                                P, SZ, P, P]
             _lib = L
     return _lib
 
@@ -176,10 +179,13 @@ def decode_workspace_size(B, L_max, Hq, Hkv, d) -> int:
     return int(lib().orthros_decode_workspace_size(B, L_max, Hq, Hkv, d))
 
 
-def xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, scale=None, out=None, workspace=None, dev_err=None):
+def xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, scale=None, out=None, workspace=None, dev_err=None,
+              lse=None):
     """Eq. (5): copy i of sequence b at original position pos[b, i] attends over k/v rows
     0..pos[b, i].  qc_raw [B, T_out, Hq, d] (may be a view of an appended buffer);
-    pos int32 [B, T_out]; k, v [B, T_kv, Hkv, d]."""
+    pos int32 [B, T_out]; k, v [B, T_kv, Hkv, d].  With lse (fp32 [B, T_out, Hq], or True for
+    a fresh one) each copy row's log-sum-exp is written too, for xattn_bwd, and (out, lse)
+    is returned."""
     B, T_kv, Hkv, d = k.shape
     T_out, Hq = qc_raw.shape[1], qc_raw.shape[2]
     qs = _bf16_rows(qc_raw, "qc_raw")
@@ -196,14 +202,26 @@ def xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, scale=None, out=None, workspac
     need = xattn_workspace_size(B, T_out, T_kv, Hq, Hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=k.device)
+    if lse is True:
+        lse = torch.empty((B, T_out, Hq), dtype=torch.float32, device=k.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, T_out, Hq) or
+                            not lse.is_contiguous()):
+        raise OrthrosError("lse must be a contiguous fp32 tensor [B, T_out, Hq]")
     with torch.cuda.device(k.device):
-        st = lib().orthros_xattn_fwd(_ptr(qc_raw), _ptr(pos), _ptr(k), _ptr(v), _ptr(alpha_c),
-                                     _ptr(beta_c), _ptr(out), B, T_out, T_kv, Hq, Hkv, d,
-                                     _scale(scale, d), qs, ks, os_, _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(), _ptr(dev_err),
-                                     _stream(k.device))
+        if lse is None:
+            st = lib().orthros_xattn_fwd(_ptr(qc_raw), _ptr(pos), _ptr(k), _ptr(v), _ptr(alpha_c),
+                                         _ptr(beta_c), _ptr(out), B, T_out, T_kv, Hq, Hkv, d,
+                                         _scale(scale, d), qs, ks, os_, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                         _stream(k.device))
+        else:
+            st = lib().orthros_xattn_fwd_lse(_ptr(qc_raw), _ptr(pos), _ptr(k), _ptr(v), _ptr(alpha_c),
+                                             _ptr(beta_c), _ptr(out), _ptr(lse), B, T_out, T_kv, Hq, Hkv, d,
+                                             _scale(scale, d), qs, ks, os_, _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                             _stream(k.device))
     _check(st, "orthros_xattn_fwd")
-    return out
+    return out if lse is None else (out, lse)
 
 
 def prefill_workspace_size(B, T, T_out, Hq, Hkv, d) -> int:
@@ -319,11 +337,12 @@ def xattn_bwd_workspace_size(B, T_out, T_kv, Hq, Hkv, d) -> int:
 
 
 def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, dOc, scale=None, dk=None, dv=None, workspace=None,
-              dev_err=None):
+              dev_err=None, lse=None):
     """Gradient of Eq. (5) with the copies' scale-offset: returns fp32 (dqc_raw, dk, dv, dalpha_c,
     dbeta_c).  Passing dk, dv (fp32 [B, T_kv, Hkv, d], e.g. from swa_bwd) adds the copies' share
     to them in place; otherwise fresh tensors hold the copies' share alone.  qc_raw, oc, dOc
-    [B, T_out, Hq, d] and k, v [B, T_kv, Hkv, d] dense bf16; pos int32 [B, T_out]."""
+    [B, T_out, Hq, d] and k, v [B, T_kv, Hkv, d] dense bf16; pos int32 [B, T_out]; lse (optional)
+    the forward's fp32 [B, T_out, Hq] log-sum-exp (xattn_fwd with lse)."""
     B, T_kv, Hkv, d = k.shape
     T_out, Hq = qc_raw.shape[1], qc_raw.shape[2]
     for t, nm, shp in ((qc_raw, "qc_raw", (B, T_out, Hq, d)), (oc, "oc", (B, T_out, Hq, d)),
@@ -334,6 +353,9 @@ def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, dOc, scale=None, dk=None, 
         raise OrthrosError("pos must be a contiguous int32 tensor [B, T_out]")
     _vec(alpha_c, "alpha_c", Hq, d)
     _vec(beta_c, "beta_c", Hq, d)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, T_out, Hq) or
+                            not lse.is_contiguous()):
+        raise OrthrosError("lse must be a contiguous fp32 tensor [B, T_out, Hq]")
     f32 = dict(dtype=torch.float32, device=k.device)
     accumulate = dk is not None
     if (dk is None) != (dv is None):
@@ -353,7 +375,8 @@ def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, dOc, scale=None, dk=None, 
                                 device=k.device)
     with torch.cuda.device(k.device):
         st = lib().orthros_xattn_bwd(_ptr(qc_raw), _ptr(pos), _ptr(k), _ptr(v), _ptr(alpha_c), _ptr(beta_c),
-                                     _ptr(oc), _ptr(dOc), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(dbeta),
+                                     _ptr(oc), _ptr(dOc), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
+                                     _ptr(dbeta),
                                      B, T_out, T_kv, Hq, Hkv, d, _scale(scale, d), int(accumulate),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _ptr(dev_err), _stream(k.device))

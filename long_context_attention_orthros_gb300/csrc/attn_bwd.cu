@@ -1715,9 +1715,10 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
             constexpr int UNITS = BqCfg<D>::ROWS / G;
             dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
             // few copies (one row tile per batch and KV head) over many keys: split the keys
-            // so that the grid fills the GPU (two CTAs' worth per SM)
+            // so that the grid fills the GPU (two CTAs' worth per SM); with the forward's
+            // log-sum-exp only the second pass runs
             int splits = 1;
-            if (p.n_units <= UNITS && p.lse_in == nullptr && p.part_ml != nullptr) {
+            if (p.n_units <= UNITS && (p.lse_in != nullptr || p.part_ml != nullptr)) {
                 int dev = 0, sms = 0;
                 if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
                     (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -1730,14 +1731,16 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
                     return e;
                 AttnBwdParams ps = p;
                 ps.splits = splits;
-                ps.split_mode = 1;
                 dim3 gs(1, p.B * p.Hkv, splits);
-                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
-                if ((e = cudaGetLastError()) != cudaSuccess)
-                    return e;
-                attn_bwd_lse_combine_kernel<G><<<p.B * p.Hkv, 128, 0, stream>>>(ps);
-                if ((e = cudaGetLastError()) != cudaSuccess)
-                    return e;
+                if (p.lse_in == nullptr) {  // per-split (max, sum), merged into the log-sum-exp
+                    ps.split_mode = 1;
+                    k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
+                    if ((e = cudaGetLastError()) != cudaSuccess)
+                        return e;
+                    attn_bwd_lse_combine_kernel<G><<<p.B * p.Hkv, 128, 0, stream>>>(ps);
+                    if ((e = cudaGetLastError()) != cudaSuccess)
+                        return e;
+                }
                 ps.split_mode = 2;
                 k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
             } else {

@@ -13,6 +13,7 @@
 namespace orthros {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded spin: 2 s
+constexpr float kLn2F = 0.6931471805599453f;       // ln 2: log2 units to natural log
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

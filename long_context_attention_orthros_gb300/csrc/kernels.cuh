@@ -35,6 +35,7 @@ struct XattnParams {
     float *part_o;     // [n_part][B*Hkv][R][D]
     float2 *part_ml;   // [n_part][B*Hkv][R]  (max in log2 units, sum)
     orthros_bf16 *oc;
+    float *lse;        // optional: each copy row's log-sum-exp, natural log, [B, T_out, Hq] (-inf: no key)
     int32_t *dev_err;
     long long qc_bstride, oc_bstride;
     int B, T_out, T_kv, Hq, Hkv, G, R, row_tiles, splits, chunk, n_part, direct;

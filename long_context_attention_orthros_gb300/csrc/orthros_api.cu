@@ -220,11 +220,15 @@ size_t orthros_xattn_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv,
     return orthros::xattn_workspace_bytes(B, T_out, T_kv, Hq, Hkv, d);
 }
 
-orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
-                                 const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
-                                 orthros_bf16 *oc, int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
-                                 int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride, void *workspace,
-                                 size_t ws_bytes, int32_t *dev_err, void *stream)
+}  // extern "C"
+
+namespace {
+
+orthros_status xattn_fwd_impl(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
+                              const orthros_bf16 *v, const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
+                              float *lse, int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
+                              int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride, void *workspace,
+                              size_t ws_bytes, int32_t *dev_err, void *stream)
 {
     if (B < 1 || T_out < 0 || T_kv < 1 || !std::isfinite(scale))
         return ORTHROS_ERR_INVALID_ARG;
@@ -249,6 +253,7 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.alpha_c = alpha_c;
     p.beta_c = beta_c;
     p.oc = oc;
+    p.lse = lse;
     p.dev_err = dev_err;
     p.qc_bstride = qs;
     p.oc_bstride = os;
@@ -276,6 +281,32 @@ orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos,
         e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+orthros_status orthros_xattn_fwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
+                                 const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
+                                 orthros_bf16 *oc, int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
+                                 int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride, void *workspace,
+                                 size_t ws_bytes, int32_t *dev_err, void *stream)
+{
+    return xattn_fwd_impl(qc_raw, pos, k, v, alpha_c, beta_c, oc, nullptr, B, T_out, T_kv, Hq, Hkv, d, scale,
+                          qc_bstride, kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, stream);
+}
+
+orthros_status orthros_xattn_fwd_lse(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
+                                     const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
+                                     orthros_bf16 *oc, float *lse, int B, int T_out, int T_kv, int Hq, int Hkv, int d,
+                                     float scale, int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride,
+                                     void *workspace, size_t ws_bytes, int32_t *dev_err, void *stream)
+{
+    if (T_out > 0 && !aligned16(lse))
+        return ORTHROS_ERR_INVALID_ARG;
+    return xattn_fwd_impl(qc_raw, pos, k, v, alpha_c, beta_c, oc, lse, B, T_out, T_kv, Hq, Hkv, d, scale, qc_bstride,
+                          kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, stream);
 }
 
 size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, int d)
@@ -427,12 +458,14 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
 
 orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos, const orthros_bf16 *k,
                                  const orthros_bf16 *v, const float *alpha_c, const float *beta_c,
-                                 const orthros_bf16 *oc, const orthros_bf16 *dOc, float *dqc_raw, float *dk, float *dv,
+                                 const orthros_bf16 *oc, const orthros_bf16 *dOc, const float *lse, float *dqc_raw,
+                                 float *dk, float *dv,
                                  float *dalpha_c, float *dbeta_c, int B, int T_out, int T_kv, int Hq, int Hkv, int d,
                                  float scale, int accumulate, void *workspace, size_t ws_bytes, int32_t *dev_err,
                                  void *stream)
 {
-    if ((T_out > 0 && (!aligned16(qc_raw) || !pos || !aligned16(oc) || !aligned16(dOc) || !aligned16(dqc_raw))) ||
+    if ((T_out > 0 && (!aligned16(qc_raw) || !pos || !aligned16(oc) || !aligned16(dOc) || !aligned16(dqc_raw) ||
+                       (lse != nullptr && !aligned16(lse)))) ||
         !aligned16(k) || !aligned16(v) || !aligned16(alpha_c) || !aligned16(beta_c) || !aligned16(dk) ||
         !aligned16(dv) || !aligned16(dalpha_c) || !aligned16(dbeta_c) || B < 1 || T_out < 0 || T_kv < 1 ||
         !std::isfinite(scale))
@@ -451,6 +484,7 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.alpha = alpha_c;
     p.beta = beta_c;
     p.pos = pos ? pos : reinterpret_cast<const int32_t *>(workspace);  // T_out == 0: never read
+    p.lse_in = T_out > 0 ? lse : nullptr;
     p.dq = dqc_raw;
     p.dk = dk;
     p.dv = dv;

@@ -183,6 +183,9 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
         if (p.direct) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int h = g * p.G + grow % p.G;
+            if (p.lse != nullptr && (lane & 3) == 0)
+                p.lse[(static_cast<long long>(b) * p.T_out + grow / p.G) * p.Hq + h] =
+                    l > 0.f ? (m + __log2f(l)) * kLn2F : -__int_as_float(0x7f800000);
             orthros_bf16 *orow =
                 p.oc + b * p.oc_bstride + (static_cast<long long>(grow / p.G) * p.Hq + h) * D;
 #pragma unroll
@@ -286,6 +289,8 @@ __global__ void __launch_bounds__(128) xattn_combine_kernel(const XattnParams p)
     if (warp != 0)
         return;
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (p.lse != nullptr && lane == 0)
+        p.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2F : NEG_INF;
     orthros_bf16 *orow = p.oc + b * p.oc_bstride + (static_cast<long long>(i) * p.Hq + h) * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; e += 2) {

@@ -389,8 +389,11 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0)
                 mbar_arrive(&p_full[2 * t + u]);
         }
-        // ---- epilogue: O / l -> bf16 -> the copy's output row
+        // ---- epilogue: O / l -> bf16 -> the copy's output row (and its log-sum-exp)
         const bool store = row < R;
+        if (store && p.lse != nullptr && ok)
+            p.lse[(static_cast<long long>(b) * p.T_out + row / G) * p.Hq + g * G + row % G] =
+                l > 0.f ? (m + __log2f(l)) * kLn2F : -__int_as_float(0x7f800000);
         orthros_bf16 *orow = p.oc + b * p.oc_bstride +
                              (static_cast<long long>(row / G) * p.Hq + g * G + row % G) * D;
         const bool o32 = ((reinterpret_cast<uintptr_t>(p.oc) | static_cast<uintptr_t>(p.oc_bstride * 2)) & 31u) == 0;

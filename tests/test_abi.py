@@ -91,6 +91,11 @@ def test_xattn_workspace_size_and_checks(L):
                                0, 0, 0, p, 16, None, None) == 3
     assert L.orthros_xattn_fwd(p, p, p, p, p, p, p, 2, 1, 131072, 32, 8, 128, ctypes.c_float(0.1),
                                0, 0, 0, None, small, None, None) == 3
+    # the log-sum-exp variant: a misaligned lse is rejected before anything runs
+    assert L.orthros_xattn_fwd_lse(p, p, p, p, p, p, p, ctypes.c_void_p(p.value + 4), 2, 1, 131072, 32, 8, 128,
+                                   ctypes.c_float(0.1), 0, 0, 0, p, small, None, None) == 1
+    assert L.orthros_xattn_fwd_lse(p, p, p, p, p, p, p, p, 2, 1, 131072, 32, 8, 128, ctypes.c_float(0.1),
+                                   0, 0, 0, p, 16, None, None) == 3
 
 
 def test_decode_workspace_size_and_checks(L):
@@ -128,10 +133,11 @@ def test_xattn_bwd_workspace_size_and_checks(L):
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 0, 32, 8, 128) == 0
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 96) == 0
 
-    def call(ws=p, nbytes=n, pos=p, T_out=2048, Hkv=8):
-        return L.orthros_xattn_bwd(p, pos, p, p, p, p, p, p, p, p, p, p, p, 4, T_out, 16384, 32, Hkv, 128,
+    def call(ws=p, nbytes=n, pos=p, T_out=2048, Hkv=8, lse=None):
+        return L.orthros_xattn_bwd(p, pos, p, p, p, p, p, p, lse, p, p, p, p, p, 4, T_out, 16384, 32, Hkv, 128,
                                    ctypes.c_float(0.1), 1, ws, nbytes, None, None)
     assert call(pos=None) == 1
+    assert call(lse=ctypes.c_void_p(p.value + 4)) == 1  # misaligned log-sum-exp
     assert call(T_out=-1) == 1
     assert call(Hkv=5) == 2
     assert call(ws=None) == 3

@@ -1,6 +1,7 @@
-"""GPU parity of the forward's per-row log-sum-exp (orthros_swa_fwd_lse) against the fp64
-oracle, and of the gradient that takes it (orthros_swa_bwd with lse: the persistent
-tensor-memory dq kernel) against the oracle's gradient.
+"""GPU parity of the forward's per-row log-sum-exp (orthros_swa_fwd_lse for the base stream,
+orthros_xattn_fwd_lse for the output copies) against the fp64 oracle, and of the gradients that
+take it (orthros_swa_bwd with lse: the persistent tensor-memory dq kernel; orthros_xattn_bwd
+with lse: the copies' dq in one pass) against the oracle's gradients.
 
 Bar for lse: 1e-2 absolute.  The kernels take q . k with q rounded once to fp16 (tensor-memory
 path) or as a bf16 high part plus residual (warp path), i.e. each logit within ~2^-11 of its
@@ -68,8 +69,8 @@ def test_gradient_with_forward_lse(B, T, Hq, Hkv, d, w):
 
 def test_gradient_full_size_sampled():
     """The bench's gradient at its full size (2 x 131072 tokens, 32/8 heads, d=128, w=128, one
-    copy per sequence at its last position), launched as bench.py launches it: forward with
-    the log-sum-exp, base-stream backward, then the copy's share added into the same dK / dV.
+    copy per sequence at its last position), launched as bench.py launches it: forwards with
+    their log-sum-exp, base-stream backward, then the copy's share added into the same dK / dV.
     Sampled base rows and keys against the oracle on the slices they depend on (a base row
     on the w tokens up to it, a key on the tokens j-w+1..j+w-1), the copy's share of those
     keys from the oracle's copy gradient, every copy row in full, and dalpha / dbeta as the
@@ -87,10 +88,11 @@ def test_gradient_full_size_sampled():
     o, lse = orth.swa_fwd_lse(qg, kg, vg, ag, bg, window=w, scale=scale)
     dq, dk, dv, da, db = orth.swa_bwd(qg, kg, vg, ag, bg, o, bf(dO), window=w, scale=scale, lse=lse)
     qcg, pg = bf(qc), i32(pos)
-    oc = orth.xattn_fwd(qcg, pg, kg, vg, f32(ac), f32(bc), scale=scale)
-    dqc, _, _, dac, dbc = orth.xattn_bwd(qcg, pg, kg, vg, f32(ac), f32(bc), oc, bf(dOc), scale=scale, dk=dk, dv=dv)
+    oc, lsec = orth.xattn_fwd(qcg, pg, kg, vg, f32(ac), f32(bc), scale=scale, lse=True)
+    dqc, _, _, dac, dbc = orth.xattn_bwd(qcg, pg, kg, vg, f32(ac), f32(bc), oc, bf(dOc), scale=scale, dk=dk, dv=dv,
+                                         lse=lsec)
     torch.cuda.synchronize()
-    del o, oc, lse
+    del o, oc, lse, lsec
     rc = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)  # the copy's share, every key
     for name, g, r in zip(("dqc_raw", "dalpha_c", "dbeta_c"), (dqc, dac, dbc), (rc[0], rc[3], rc[4])):
         _assert_grad(g.cpu().numpy().astype(np.float64), r, name)
@@ -112,3 +114,71 @@ def test_gradient_full_size_sampled():
     da_ref = (qg.double() * dq_post).sum(dim=(0, 1)).cpu().numpy()
     _assert_grad(db.cpu().numpy().astype(np.float64), db_ref, "dbeta as the sum of dq")
     _assert_grad(da.cpu().numpy().astype(np.float64), da_ref, "dalpha as the sum of x * dq")
+
+
+def _copy_inputs(seed, B, T_kv, T_out, Hq, Hkv, d, positions):
+    from tests.test_gpu_xattn_bwd import _copies
+    _, k, v, _, _, _ = _inputs(seed, B, T_kv, Hq, Hkv, d)
+    qc, pos, dOc, ac, bc = _copies(seed, B, T_kv, T_out, Hq, d, positions)
+    return qc, pos, k, v, ac, bc, dOc
+
+
+# (B, T_kv, T_out, Hq, Hkv, d, positions): which forward path writes the lse
+XATTN_LSE_CASES = [
+    (1, 2000, 256, 32, 8, 128, "tail_shuffled"),  # T_out * G >= 256: tensor-memory kernel
+    (2, 300, 20, 8, 2, 128, "random"),           # split-KV partials and the combine
+    (1, 200, 40, 8, 2, 64, "random"),            # one partial per row: written directly, d=64
+    (2, 5000, 1, 32, 8, 128, "tail_shuffled"),   # one copy per sequence (the inference layout)
+]
+
+
+@pytest.mark.parametrize("B,T_kv,T_out,Hq,Hkv,d,positions", XATTN_LSE_CASES)
+def test_copy_forward_lse_matches_oracle(B, T_kv, T_out, Hq, Hkv, d, positions):
+    from tests.gpu_util import i32
+    qc, pos, k, v, ac, bc, _ = _copy_inputs(7100 + T_kv + T_out, B, T_kv, T_out, Hq, Hkv, d, positions)
+    scale = 1.0 / math.sqrt(d)
+    args = (bf(qc), i32(pos), bf(k), bf(v), f32(ac), f32(bc))
+    oc, lse = orth.xattn_fwd(*args, scale=scale, lse=True)
+    oc_plain = orth.xattn_fwd(*args, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(oc, oc_plain)  # asking for lse changes nothing else
+    got = lse.cpu().numpy().astype(np.float64)
+    ref = oracle.xattn_lse(qc, pos, k, ac, bc, scale)
+    err = float(np.abs(got - ref).max())
+    assert err <= LSE_ABS, f"lse max |err| {err:.3e}"
+
+
+def test_copy_forward_lse_of_a_bad_position_is_minus_infinity():
+    from tests.gpu_util import i32
+    B, T_kv, T_out, Hq, Hkv, d = 1, 300, 20, 8, 2, 128
+    qc, pos, k, v, ac, bc, _ = _copy_inputs(7200, B, T_kv, T_out, Hq, Hkv, d, "random")
+    bad = pos.copy()
+    bad[0, 5] = T_kv
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    scale = 1.0 / math.sqrt(d)
+    _, lse = orth.xattn_fwd(bf(qc), i32(bad), bf(k), bf(v), f32(ac), f32(bc), scale=scale, lse=True, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & orth.DEVERR_POSITION
+    got = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isneginf(got[0, 5]))
+    keep = [i for i in range(T_out) if i != 5]
+    ref = oracle.xattn_lse(np.ascontiguousarray(qc[:, keep]), np.ascontiguousarray(pos[:, keep]), k, ac, bc, scale)
+    assert float(np.abs(got[:, keep] - ref).max()) <= LSE_ABS
+
+
+@pytest.mark.parametrize("B,T_kv,T_out,Hq,Hkv,d,positions", XATTN_LSE_CASES + [
+    (1, 16384, 3, 32, 8, 128, "random"),  # few copies over long keys: the split dq, second pass only
+])
+def test_copy_gradient_with_forward_lse(B, T_kv, T_out, Hq, Hkv, d, positions):
+    from tests.gpu_util import i32
+    qc, pos, k, v, ac, bc, dOc = _copy_inputs(7300 + T_kv + T_out, B, T_kv, T_out, Hq, Hkv, d, positions)
+    scale = 1.0 / math.sqrt(d)
+    args = (bf(qc), i32(pos), bf(k), bf(v), f32(ac), f32(bc))
+    oc, lse = orth.xattn_fwd(*args, scale=scale, lse=True)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = orth.xattn_bwd(*args, oc, bf(dOc), scale=scale, lse=lse, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)
+    for name, g, r in zip(NAMES, got, ref):
+        _assert_grad(g.cpu().numpy().astype(np.float64), r, name)
