@@ -414,8 +414,8 @@ def swa_pairs(B, T, Hq, w) -> int:
 
 def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     """The layer's attention gradient on the prefill inputs with seeded N(0, 1) output
-    gradients: orthros_swa_bwd (base stream), then orthros_xattn_bwd adding the copies'
-    share into the same dK / dV."""
+    gradients: orthros_attn_bwd, both streams in one call (each with its forward's
+    log-sum-exp, computed untimed beforehand)."""
     import torch
     import long_context_attention_orthros_gb300 as orth
     B, T, Hq, Hkv, d, T_out = cfg.B, cfg.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.T_out
@@ -423,8 +423,7 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     gen.manual_seed(SEEDS[cfg.name] + 17)
     dO = torch.randn((B, T, Hq, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
     dOc = torch.randn((B, T_out, Hq, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    ws = torch.empty(orth.swa_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
-    wsc = torch.empty(orth.xattn_bwd_workspace_size(B, T_out, T, Hq, Hkv, d), dtype=torch.uint8, device=dev)
+    ws = torch.empty(orth.attn_bwd_workspace_size(B, T, T_out, Hq, Hkv, d), dtype=torch.uint8, device=dev)
     qc = g["qc"].contiguous()
     q = g["q"] if g["q"].shape[1] == T else g["q"][:, :T].contiguous()  # appended copies: base rows only
     stream = torch.cuda.current_stream(dev)
@@ -435,11 +434,8 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
         _, lsec = orth.xattn_fwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], scale=cfg.scale, lse=True)
 
     def call():
-        base = orth.swa_bwd(q, g["k"], g["v"], g["a"], g["b"], o, dO, window=cfg.window,
-                            scale=cfg.scale, workspace=ws, lse=lse)
-        copy = orth.xattn_bwd(qc, g["pos"], g["k"], g["v"], g["ac"], g["bc"], oc, dOc, scale=cfg.scale,
-                              dk=base[1], dv=base[2], workspace=wsc, lse=lsec)
-        return base + copy
+        return orth.attn_bwd(q, g["k"], g["v"], g["a"], g["b"], o, dO, qc, g["pos"], g["ac"], g["bc"], oc, dOc,
+                             window=cfg.window, scale=cfg.scale, lse=lse, lsec=lsec, workspace=ws)
 
     for _ in range(3):
         grads = call()
@@ -452,18 +448,19 @@ def run_bwd(dev, world, g, o, oc, cfg, tf_peak, peak_kind, calls: int = 5):
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
-    del grads, dO, dOc, ws, wsc, lse, lsec, q
-    # launches per call (mirror of attn_bwd.cu): base stream with the log-sum-exp: fp16 K, fp16 q,
-    # D, dq, the dalpha / dbeta sums, dk/dv; copies with theirs: fp16 K, fp16 q, D, dq (one pass,
-    # or split over the keys when one row tile per (batch, KV head) holds all copies), dk/dv
-    per_call = 6 + (5 if T_out > 0 else 2)
+    del grads, dO, dOc, ws, lse, lsec, q
+    # launches per call (mirror of attn_bwd.cu): fp16 K; base stream with its log-sum-exp: fp16 q,
+    # D, dq, the dalpha / dbeta sums; copies with theirs: fp16 q, D, dq (one pass, or split over
+    # the keys when one row tile per (batch, KV head) holds all copies); one dk/dv for both
+    per_call = 1 + 4 + (3 if T_out > 0 else 0) + 1
     # the five contractions of the gradient (S, dP, dV, dK, dQ), 2 d flops each per pair
     pos = g["pos"].cpu().numpy().astype(np.int64)
     pairs = swa_pairs(B, T, Hq, cfg.window) + Hq * int((pos + 1).sum())
     flops = 10 * d * pairs
     tfs = flops / (ms / 1e3) / 1e12
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
-            "what": "swa_bwd + xattn_bwd (copies' share added into dK/dV), each with its forward's log-sum-exp",
+            "what": "attn_bwd: both streams' gradient in one call (dK/dV written once), each stream with its "
+                    "forward's log-sum-exp",
             "roofline": {"kernel": f"attn_bwd ({per_call} launches)", "bound": "tensor", "achieved": tfs,
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": tfs / tf_peak, "traffic": None,
                          "peak_kind": peak_kind, "algorithmic_flops": flops},

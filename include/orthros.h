@@ -369,6 +369,39 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
                                  int d, float scale, int accumulate, void *workspace,
                                  size_t ws_bytes, int32_t *dev_err, void *stream);
 
+/*
+ * Bytes of device workspace orthros_attn_bwd needs: the regions of
+ * orthros_swa_bwd and orthros_xattn_bwd, with one fp16 copy of K for both.
+ * Returns 0 for invalid sizes.
+ */
+size_t orthros_attn_bwd_workspace_size(int B, int T, int T_out, int Hq, int Hkv, int d);
+
+/*
+ * A layer's whole attention gradient in one call: orthros_swa_bwd of the base
+ * stream and orthros_xattn_bwd of the output copies (over the same K, V;
+ * T_kv = T), with the same arguments, meanings and arithmetic, except that
+ *   dk, dv  get the sum of both streams' shares, written once (not added to
+ *           what the buffers held);
+ *   lse, lsec  are each stream's forward log-sum-exp (orthros_swa_fwd_lse,
+ *           orthros_xattn_fwd_lse) or NULL;
+ *   one fp16 copy of K serves both streams, and one dk/dv launch takes, for
+ *   each block of 128 keys, the base rows and then the copy rows that see it.
+ * T_out == 0 is allowed (qc_raw, pos, oc, dOc, lsec and dqc_raw are then not
+ * read; dalpha_c and dbeta_c are zeroed).  workspace:
+ * orthros_attn_bwd_workspace_size(...) bytes, 16-byte aligned.  Outputs must
+ * not alias inputs.
+ */
+orthros_status orthros_attn_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
+                                const orthros_bf16 *v, const float *alpha, const float *beta,
+                                const orthros_bf16 *o, const orthros_bf16 *dO, const float *lse,
+                                const orthros_bf16 *qc_raw, const int32_t *pos,
+                                const float *alpha_c, const float *beta_c, const orthros_bf16 *oc,
+                                const orthros_bf16 *dOc, const float *lsec, float *dq_raw,
+                                float *dk, float *dv, float *dalpha, float *dbeta, float *dqc_raw,
+                                float *dalpha_c, float *dbeta_c, int B, int T, int T_out, int Hq,
+                                int Hkv, int d, int window, float scale, void *workspace,
+                                size_t ws_bytes, int32_t *dev_err, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
             L.orthros_xattn_bwd.restype = I
             L.orthros_xattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F,
                                             I, P, SZ, P, P]
+            L.orthros_attn_bwd_workspace_size.restype = SZ
+            L.orthros_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+            L.orthros_attn_bwd.restype = I
+            L.orthros_attn_bwd.argtypes = [P] * 23 + [I, I, I, I, I, I, I, F, P, SZ, P, P]
             L.orthros_xattn_fwd_lse.restype = I
             L.orthros_xattn_fwd_lse.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, L64, L64, L64,
                                                 P, SZ, P, P]
@@ -382,6 +386,46 @@ def xattn_bwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, dOc, scale=None, dk=None, 
                                      _ptr(dev_err), _stream(k.device))
     _check(st, "orthros_xattn_bwd")
     return dq, dk, dv, dalpha, dbeta
+
+
+def attn_bwd_workspace_size(B, T, T_out, Hq, Hkv, d) -> int:
+    return int(lib().orthros_attn_bwd_workspace_size(B, T, T_out, Hq, Hkv, d))
+
+
+def attn_bwd(q_raw, k, v, alpha, beta, o, dO, qc_raw, pos, alpha_c, beta_c, oc, dOc, window: int = 128,
+             scale=None, lse=None, lsec=None, workspace=None, dev_err=None):
+    """A layer's attention gradient, both streams in one call: returns fp32 (dq_raw, dk, dv, dalpha,
+    dbeta, dqc_raw, dalpha_c, dbeta_c), dk and dv holding both streams' shares.  Base tensors as
+    swa_bwd, copy tensors as xattn_bwd (T_kv = T); lse / lsec the forwards' log-sum-exp or None."""
+    B, T, Hkv, d = k.shape
+    Hq, T_out = q_raw.shape[2], qc_raw.shape[1]
+    for t, nm, shp in ((q_raw, "q_raw", (B, T, Hq, d)), (o, "o", (B, T, Hq, d)), (dO, "dO", (B, T, Hq, d)),
+                       (qc_raw, "qc_raw", (B, T_out, Hq, d)), (oc, "oc", (B, T_out, Hq, d)),
+                       (dOc, "dOc", (B, T_out, Hq, d)), (k, "k", (B, T, Hkv, d)), (v, "v", (B, T, Hkv, d))):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or tuple(t.shape) != shp or not t.is_contiguous():
+            raise OrthrosError(f"{nm} must be a contiguous bf16 CUDA tensor {shp}")
+    if pos.dtype != torch.int32 or tuple(pos.shape) != (B, T_out) or not pos.is_contiguous():
+        raise OrthrosError("pos must be a contiguous int32 tensor [B, T_out]")
+    for t, nm in ((alpha, "alpha"), (beta, "beta"), (alpha_c, "alpha_c"), (beta_c, "beta_c")):
+        _vec(t, nm, Hq, d)
+    for t, nm, shp in ((lse, "lse", (B, T, Hq)), (lsec, "lsec", (B, T_out, Hq))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp or not t.is_contiguous()):
+            raise OrthrosError(f"{nm} must be a contiguous fp32 tensor {shp}")
+    f32 = dict(dtype=torch.float32, device=k.device)
+    out = [torch.empty(shp, **f32) for shp in ((B, T, Hq, d), (B, T, Hkv, d), (B, T, Hkv, d), (Hq, d), (Hq, d),
+                                                (B, T_out, Hq, d), (Hq, d), (Hq, d))]
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(B, T, T_out, Hq, Hkv, d), dtype=torch.uint8,
+                                device=k.device)
+    with torch.cuda.device(k.device):
+        st = lib().orthros_attn_bwd(_ptr(q_raw), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(o), _ptr(dO),
+                                    _ptr(lse), _ptr(qc_raw), _ptr(pos), _ptr(alpha_c), _ptr(beta_c), _ptr(oc),
+                                    _ptr(dOc), _ptr(lsec), *[_ptr(t) for t in out], B, T, T_out, Hq, Hkv, d,
+                                    int(window), _scale(scale, d), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                    _stream(k.device))
+    _check(st, "orthros_attn_bwd")
+    return tuple(out)
 
 
 def decode_workspace(B, L_max, Hq, Hkv, d, device) -> torch.Tensor:

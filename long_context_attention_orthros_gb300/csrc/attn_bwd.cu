@@ -571,11 +571,57 @@ constexpr int DKV_TC_THREADS = 384;
 constexpr int DKV_TC_CONV = 192;  // preparation threads of the dQ kernel (warps 2-3 and 8-11)
 constexpr int DKV_THREADS = 256;  // the dK/dV kernel: producer, MMA, 2 metadata warps, 4 softmax warps
 
-template <int D, int G, bool COPY>
+// The rounds of query rows a dK/dV CTA takes, in order: phase 0 is the stream of p (base
+// rows: rounds kt0/UNITS .. while a row can see the block; copies: the rounds holding a copy at
+// a position >= kt0), phase 1 (STREAMS == 2) the copies of pc.  seek moves (ph, r) to the first
+// round at or after it and returns false once none is left.  Called by whole warps.
+template <int STREAMS>
+struct DkvRounds {
+    const AttnBwdParams &p, &pc;
+    int b, kt0, units, base_end;
+    __device__ __forceinline__ bool seek(int &ph, int &r) const
+    {
+        if (ph == 0) {
+            if (STREAMS == 1) {
+                const int e = (p.n_units + units - 1) / units;
+                r = next_round<true>(p, b, kt0, r, e, units);
+                return r < e;
+            }
+            if (r < base_end)
+                return true;
+            if (STREAMS == 0)
+                return false;
+            ph = 1;
+            r = 0;
+        }
+        const int e = (pc.n_units + units - 1) / units;
+        r = next_round<true>(pc, b, kt0, r, e, units);
+        return r < e;
+    }
+};
+
+// position of unit u of the round's stream (copies: pos, -1 when out of range or past the end)
+__device__ __forceinline__ int round_unit_pos(const AttnBwdParams &p, const AttnBwdParams &pc, bool from_pc,
+                                              bool copy, int b, int u)
+{
+    const int n = from_pc ? pc.n_units : p.n_units;
+    if (u >= n)
+        return -1;
+    if (!copy)
+        return u;
+    const int32_t *pos = from_pc ? pc.pos : p.pos;
+    const int P = __ldg(pos + static_cast<long long>(b) * n + u);
+    return (P >= 0 && P < p.T_kv) ? P : -1;
+}
+
+// STREAMS: 0 the base stream (p), 1 copies (p), 2 the base stream (p) and then the copies (pc,
+// with its own row maps qcmap / ocmap) into the same dK / dV, written once.
+template <int D, int G, int STREAMS>
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                           const __grid_constant__ CUtensorMap qcmap, const __grid_constant__ CUtensorMap ocmap,
                            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                           const AttnBwdParams p)
+                           const AttnBwdParams p, const AttnBwdParams pc)
 {
     using C = BtCfg<D>;
     constexpr int UNITS = C::RB / G;  // units per round
@@ -597,13 +643,13 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kt0 = blockIdx.x * C::KEYS, bh = blockIdx.y;
     const int b = bh / p.Hkv, g = bh % p.Hkv;
-    // rounds r cover units r*UNITS .. r*UNITS+UNITS-1
-    const int r_begin = COPY ? 0 : kt0 / UNITS;
-    const int r_end = COPY ? (p.n_units + UNITS - 1) / UNITS
-                           : static_cast<int>((min(static_cast<long long>(p.n_units),
-                                                   static_cast<long long>(kt0) + C::KEYS - 1 + p.window) +
-                                               UNITS - 1) /
-                                              UNITS);
+    // rounds r cover units r*UNITS .. r*UNITS+UNITS-1 of their stream
+    const int r_begin = STREAMS == 1 ? 0 : kt0 / UNITS;
+    const int base_end = static_cast<int>((min(static_cast<long long>(p.n_units),
+                                                static_cast<long long>(kt0) + C::KEYS - 1 + p.window) +
+                                            UNITS - 1) /
+                                           UNITS);
+    const DkvRounds<STREAMS> rounds{p, pc, b, kt0, UNITS, base_end};
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -633,6 +679,10 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         if (lane == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&omap);
+            if (STREAMS == 2) {
+                tma_prefetch_desc(&qcmap);
+                tma_prefetch_desc(&ocmap);
+            }
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
             mbar_arrive_expect_tx(kv_full, 2 * C::SLABS * C::KSLAB);
@@ -642,19 +692,20 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
                 tma_load_4d(smem + C::V_OFF + sl * C::KSLAB, &vmap, kv_full, sl * 64, g, kt0, b);
             }
         }
-        int i = 0;
-        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
-             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+        int i = 0, ph = 0, r = r_begin;
+        for (bool more = rounds.seek(ph, r); more; ++r, more = rounds.seek(ph, r), ++i) {
             const int s = i % C::STG;
             if (i >= C::STG && !(ok = warp_wait(&st_empty[s], static_cast<uint32_t>(((i / C::STG) - 1) & 1))))
                 break;
             if (lane == 0) {
                 uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
+                const CUtensorMap *qm = (STREAMS == 2 && ph == 1) ? &qcmap : &qmap;
+                const CUtensorMap *om = (STREAMS == 2 && ph == 1) ? &ocmap : &omap;
                 mbar_arrive_expect_tx(&st_full[s], 2 * C::SLABS * C::RSLAB);
 #pragma unroll
                 for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(st + C::ST_Q16 + sl * C::RSLAB, &qmap, &st_full[s], sl * 64, g * G, r * UNITS, b);
-                    tma_load_4d(st + C::ST_DO + sl * C::RSLAB, &omap, &st_full[s], sl * 64, g * G, r * UNITS, b);
+                    tma_load_4d(st + C::ST_Q16 + sl * C::RSLAB, qm, &st_full[s], sl * 64, g * G, r * UNITS, b);
+                    tma_load_4d(st + C::ST_DO + sl * C::RSLAB, om, &st_full[s], sl * 64, g * G, r * UNITS, b);
                 }
             }
         }
@@ -691,9 +742,8 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
             return true;
         };
         ok = warp_wait(kv_full, 0);
-        int i = 0;
-        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
-             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+        int i = 0, ph = 0, r = r_begin;
+        for (bool more = rounds.seek(ph, r); ok && more; ++r, more = rounds.seek(ph, r), ++i) {
             const int s = i % C::STG, u = i & 1;
             if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
                 break;
@@ -727,20 +777,21 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     } else if (warp < 4) {
         // ------------------------------------------------------------------ row metadata
         const int ct = threadIdx.x - 64;  // 0..63: one row of the round each
-        int i = 0;
-        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); ok && r < r_end;
-             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+        int i = 0, ph = 0, r = r_begin;
+        for (bool more = rounds.seek(ph, r); ok && more; ++r, more = rounds.seek(ph, r), ++i) {
             const int s = i % C::STG;
+            const bool from_pc = STREAMS == 2 && ph == 1;
             // loaded before the wait so that the latency overlaps it
             float m_lse = 0.f, m_d = 0.f;
             int m_pos = -1;
             {
                 const int u = r * UNITS + ct / G, h = g * G + ct % G;
-                m_pos = unit_pos<COPY>(p, b, u);
+                m_pos = round_unit_pos(p, pc, from_pc, STREAMS != 0 && (STREAMS == 1 || ph == 1), b, u);
                 if (m_pos >= 0) {
-                    const long long ri = (static_cast<long long>(b) * p.n_units + u) * p.Hq + h;
-                    m_lse = p.lse[ri];
-                    m_d = p.Drow[ri];
+                    const long long ri =
+                        (static_cast<long long>(b) * (from_pc ? pc.n_units : p.n_units) + u) * p.Hq + h;
+                    m_lse = (from_pc ? pc.lse : p.lse)[ri];
+                    m_d = (from_pc ? pc.Drow : p.Drow)[ri];
                 }
             }
             // the slot is free once the stage of this round has landed: its producer waited
@@ -762,10 +813,10 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
         const float c2 = p.scale * kLog2eF;
         float ds_max = 0.f;  // dS^T goes to fp16: |dS| < 65504 or the range error
-        int i = 0;
-        for (int r = next_round<COPY>(p, b, kt0, r_begin, r_end, UNITS); r < r_end;
-             r = next_round<COPY>(p, b, kt0, r + 1, r_end, UNITS), ++i) {
+        int i = 0, ph = 0, r = r_begin;
+        for (bool more = rounds.seek(ph, r); more; ++r, more = rounds.seek(ph, r), ++i) {
             const int s = i % C::STG, u = i & 1;
+            const int window = (STREAMS == 2 && ph == 1) ? pc.window : p.window;
             if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((i >> 1) & 1)) &&
                        warp_wait(&qconv[s], static_cast<uint32_t>((i / C::STG) & 1))))
                 break;
@@ -785,7 +836,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
                     for (int q = 0; q < 2; ++q) {
                         const int c = 32 * half + 2 * e + q;
                         const int P = __float_as_int(m[2 * C::RB + c]);
-                        const bool valid = key <= P && key >= P - p.window + 1;  // P = -1: none
+                        const bool valid = key <= P && key >= P - window + 1;  // P = -1: none
                         pr[q] = valid ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - m[c]) : 0.f;
                         ds[q] = pr[q] * (__uint_as_float(dv[2 * e + q]) - m[C::RB + c]);
                     }
@@ -1671,8 +1722,11 @@ static size_t dq_smem(int D, int G)
     return static_cast<size_t>(4) * (D / 64) * BWD_KEYS * 128 + 2 * G * D * 4 + 16 + 1024;
 }
 
+// One stream's launches before dK/dV: zeroed dalpha / dbeta, the fp16 copy of K (unless another
+// stream's call already made it), the fp16 scale-offset q, D (and the forward's log-sum-exp in
+// log2 units), then dq (and, after the persistent base kernel, the dalpha / dbeta sums).
 template <int D, int G, bool COPY>
-static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
+static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps, bool make_k16, cudaStream_t stream)
 {
     const long long rows = static_cast<long long>(p.B) * p.n_units * p.Hq;
     cudaError_t e = cudaMemsetAsync(p.dalpha, 0, sizeof(float) * p.Hq * D, stream);
@@ -1680,7 +1734,7 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         e = cudaMemsetAsync(p.dbeta, 0, sizeof(float) * p.Hq * D, stream);
     if (e != cudaSuccess)
         return e;
-    {
+    if (make_k16) {
         const long long n8 = static_cast<long long>(p.B) * p.T_kv * p.Hkv * D / 8;
         attn_bwd_k16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(p.k, p.k16, n8,
                                                                                                   p.dev_err);
@@ -1785,15 +1839,47 @@ static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    // dk/dv also runs without query rows: it writes (or keeps) zeros
+    return cudaSuccess;
+}
+
+// dK / dV of the rows of p (STREAMS 0: base, 1: copies) or of both streams (STREAMS 2: p base,
+// pc copies).  Also runs without query rows: it writes (or keeps) zeros.
+template <int D, int G, int STREAMS>
+static cudaError_t launch_dkv_t(const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
+                                const CUtensorMap *mapsc, cudaStream_t stream)
+{
     const size_t s3 = BtCfg<D>::SMEM;
-    auto k3 = attn_bwd_dkv_tc_kernel<D, G, COPY>;
-    if ((e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3))) !=
-        cudaSuccess)
+    auto k3 = attn_bwd_dkv_tc_kernel<D, G, STREAMS>;
+    cudaError_t e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3));
+    if (e != cudaSuccess)
         return e;
     dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-    k3<<<g3, DKV_THREADS, s3, stream>>>(maps[0], maps[1], maps[3], maps[2], p);
+    k3<<<g3, DKV_THREADS, s3, stream>>>(maps[0], maps[1], mapsc[0], mapsc[1], maps[3], maps[2], p, pc);
     return cudaGetLastError();
+}
+
+template <int D, int G, bool COPY>
+static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
+{
+    const cudaError_t e = launch_rows_t<D, G, COPY>(p, maps, true, stream);
+    if (e != cudaSuccess)
+        return e;
+    return launch_dkv_t<D, G, COPY ? 1 : 0>(p, p, maps, maps, stream);
+}
+
+// both streams of a layer: the copies reuse the base stream's fp16 K, and one dK/dV launch
+// takes the base rows and then the copies' rows of each key block
+template <int D, int G>
+static cudaError_t launch_layer_bwd_t(const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
+                                      const CUtensorMap *mapsc, cudaStream_t stream)
+{
+    cudaError_t e = launch_rows_t<D, G, false>(p, maps, true, stream);
+    if (e == cudaSuccess)
+        e = launch_rows_t<D, G, true>(pc, mapsc, false, stream);
+    if (e != cudaSuccess)
+        return e;
+    return pc.n_units > 0 ? launch_dkv_t<D, G, 2>(p, pc, maps, mapsc, stream)
+                          : launch_dkv_t<D, G, 0>(p, p, maps, maps, stream);
 }
 
 template <bool COPY>
@@ -1820,6 +1906,26 @@ static cudaError_t dispatch_attn_bwd(int D, int G, const AttnBwdParams &p, const
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
 {
     return p.pos ? dispatch_attn_bwd<true>(D, G, p, maps, stream) : dispatch_attn_bwd<false>(D, G, p, maps, stream);
+}
+
+cudaError_t launch_attn_bwd_layer(int D, int G, const AttnBwdParams &p, const AttnBwdParams &pc,
+                                  const CUtensorMap *maps, const CUtensorMap *mapsc, cudaStream_t stream)
+{
+#define ORTHROS_BWD_CASE(DD, GG) \
+    if (D == DD && G == GG)      \
+        return launch_layer_bwd_t<DD, GG>(p, pc, maps, mapsc, stream);
+    ORTHROS_BWD_CASE(128, 1)
+    ORTHROS_BWD_CASE(128, 2)
+    ORTHROS_BWD_CASE(128, 4)
+    ORTHROS_BWD_CASE(128, 8)
+    ORTHROS_BWD_CASE(128, 16)
+    ORTHROS_BWD_CASE(64, 1)
+    ORTHROS_BWD_CASE(64, 2)
+    ORTHROS_BWD_CASE(64, 4)
+    ORTHROS_BWD_CASE(64, 8)
+    ORTHROS_BWD_CASE(64, 16)
+#undef ORTHROS_BWD_CASE
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace orthros

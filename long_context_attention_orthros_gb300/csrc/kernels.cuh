@@ -93,6 +93,10 @@ size_t attn_bwd_split_bytes(int B, int Hkv);
 // and the fp16 K with boxes of 64 x 1 x 64 (dQ); [9] the fp16 q with boxes of 64 x G x 128/G
 constexpr int ATTN_BWD_MAPS = 10;
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
+// a layer's gradient, both streams: p the base stream, pc the copies (pc.k16 = p.k16; maps and
+// mapsc as above for each stream, mapsc's fp16-K maps over p.k16); dK / dV written once
+cudaError_t launch_attn_bwd_layer(int D, int G, const AttnBwdParams &p, const AttnBwdParams &pc,
+                                  const CUtensorMap *maps, const CUtensorMap *mapsc, cudaStream_t stream);
 
 cudaError_t launch_swa(int D, int G, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, SwaParams p, int num_sms, cudaStream_t stream);

@@ -513,4 +513,95 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
+size_t orthros_attn_bwd_workspace_size(int B, int T, int T_out, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T < 1 || T_out < 0 || (d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return 0;
+    // the base stream's region (rows, fp16 K, fp16 q), then the copies' (rows, split partials, fp16 q)
+    const size_t base = (orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d) + 255) & ~static_cast<size_t>(255);
+    return base + orthros::attn_bwd_k16_offset(B, T_out, Hq) + orthros::attn_bwd_split_bytes(B, Hkv) +
+           2 * static_cast<size_t>(B) * T_out * Hq * d;
+}
+
+orthros_status orthros_attn_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                                const float *alpha, const float *beta, const orthros_bf16 *o, const orthros_bf16 *dO,
+                                const float *lse, const orthros_bf16 *qc_raw, const int32_t *pos,
+                                const float *alpha_c, const float *beta_c, const orthros_bf16 *oc,
+                                const orthros_bf16 *dOc, const float *lsec, float *dq_raw, float *dk, float *dv,
+                                float *dalpha, float *dbeta, float *dqc_raw, float *dalpha_c, float *dbeta_c, int B,
+                                int T, int T_out, int Hq, int Hkv, int d, int window, float scale, void *workspace,
+                                size_t ws_bytes, int32_t *dev_err, void *stream)
+{
+    if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(dO) || !aligned16(dq_raw) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(dalpha) || !aligned16(dbeta) || (lse != nullptr && !aligned16(lse)) || !aligned16(alpha_c) ||
+        !aligned16(beta_c) || !aligned16(dalpha_c) || !aligned16(dbeta_c) || B < 1 || T < 1 || T_out < 0 ||
+        window < 1 || !std::isfinite(scale))
+        return ORTHROS_ERR_INVALID_ARG;
+    if (T_out > 0 && (!aligned16(qc_raw) || !pos || !aligned16(oc) || !aligned16(dOc) || !aligned16(dqc_raw) ||
+                      (lsec != nullptr && !aligned16(lsec))))
+        return ORTHROS_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
+        return ORTHROS_ERR_UNSUPPORTED;
+    const size_t need = orthros_attn_bwd_workspace_size(B, T, T_out, Hq, Hkv, d);
+    if (!aligned16(workspace) || ws_bytes < need)
+        return ORTHROS_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    orthros::AttnBwdParams p{};
+    p.q = q_raw;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.dO = dO;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.pos = nullptr;
+    p.lse_in = lse;
+    p.dq = dq_raw;
+    p.dk = dk;
+    p.dv = dv;
+    p.dalpha = dalpha;
+    p.dbeta = dbeta;
+    p.lse = reinterpret_cast<float *>(ws);
+    p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
+    p.k16 = reinterpret_cast<uint16_t *>(ws + orthros::attn_bwd_k16_offset(B, T, Hq));
+    p.q16 = reinterpret_cast<uint16_t *>(ws + orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d));
+    p.dev_err = dev_err;
+    p.B = B;
+    p.n_units = T;
+    p.T_kv = T;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.window = window;
+    p.accumulate = 0;
+    p.scale = scale;
+
+    char *wc = ws + ((orthros_swa_bwd_workspace_size(B, T, Hq, Hkv, d) + 255) & ~static_cast<size_t>(255));
+    orthros::AttnBwdParams pc = p;
+    pc.q = qc_raw;
+    pc.o = oc;
+    pc.dO = dOc;
+    pc.alpha = alpha_c;
+    pc.beta = beta_c;
+    pc.pos = T_out > 0 ? pos : reinterpret_cast<const int32_t *>(ws);  // T_out == 0: never read
+    pc.lse_in = T_out > 0 ? lsec : nullptr;
+    pc.dq = dqc_raw;
+    pc.dalpha = dalpha_c;
+    pc.dbeta = dbeta_c;
+    pc.lse = reinterpret_cast<float *>(wc);
+    pc.Drow = pc.lse + static_cast<size_t>(B) * T_out * Hq;
+    pc.part_ml = reinterpret_cast<float2 *>(wc + orthros::attn_bwd_k16_offset(B, T_out, Hq));
+    pc.q16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(pc.part_ml) + orthros::attn_bwd_split_bytes(B, Hkv));
+    pc.n_units = T_out;
+    pc.window = T;  // a copy at position P sees keys 0..P
+    CUtensorMap maps[orthros::ATTN_BWD_MAPS], mapsc[orthros::ATTN_BWD_MAPS];
+    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B) ||
+        !bwd_maps(mapsc, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, T_out > 0 ? pc.q16 : p.k16, d, Hq,
+                  Hkv, T_out > 0 ? T_out : 1, T, B))
+        return ORTHROS_ERR_CUDA;
+    const cudaError_t e =
+        orthros::launch_attn_bwd_layer(d, Hq / Hkv, p, pc, maps, mapsc, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -144,3 +144,28 @@ def test_xattn_bwd_workspace_size_and_checks(L):
     assert call(nbytes=n - 4) == 3
     assert call(ws=None) == 3
     assert call(nbytes=n - 4) == 3
+
+
+def test_attn_bwd_workspace_size_and_checks(L):
+    p, _keep = _aligned_dummy()
+    n = L.orthros_attn_bwd_workspace_size(2, 1000, 64, 32, 8, 128)
+    base = L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 128)
+    # the base stream's region (256-aligned), then the copies' rows, split partials and fp16 q
+    copies = ((8 * 2 * 64 * 32 + 255) // 256 * 256) + 2 * 8 * 64 * 128 * 8 + 2 * 2 * 64 * 32 * 128
+    assert n == (base + 255) // 256 * 256 + copies
+    assert L.orthros_attn_bwd_workspace_size(2, 1000, 0, 32, 8, 128) > base
+    assert L.orthros_attn_bwd_workspace_size(2, 0, 64, 32, 8, 128) == 0
+    assert L.orthros_attn_bwd_workspace_size(2, 1000, -1, 32, 8, 128) == 0
+    assert L.orthros_attn_bwd_workspace_size(2, 1000, 64, 32, 5, 128) == 0
+
+    def call(ws=p, nbytes=n, pos=p, T_out=64, Hkv=8, window=128, lsec=None):
+        args = [p] * 9 + [pos] + [p] * 4 + [lsec] + [p] * 8
+        return L.orthros_attn_bwd(*args, 2, 1000, T_out, 32, Hkv, 128, window, ctypes.c_float(0.1), ws, nbytes,
+                                  None, None)
+    assert call(pos=None) == 1
+    assert call(window=0) == 1
+    assert call(T_out=-1) == 1
+    assert call(lsec=ctypes.c_void_p(p.value + 4)) == 1
+    assert call(Hkv=5) == 2
+    assert call(ws=None) == 3
+    assert call(nbytes=n - 4) == 3

@@ -70,7 +70,7 @@ def test_gradient_with_forward_lse(B, T, Hq, Hkv, d, w):
 def test_gradient_full_size_sampled():
     """The bench's gradient at its full size (2 x 131072 tokens, 32/8 heads, d=128, w=128, one
     copy per sequence at its last position), launched as bench.py launches it: forwards with
-    their log-sum-exp, base-stream backward, then the copy's share added into the same dK / dV.
+    their log-sum-exp, then both streams' gradient in one call (orthros_attn_bwd).
     Sampled base rows and keys against the oracle on the slices they depend on (a base row
     on the w tokens up to it, a key on the tokens j-w+1..j+w-1), the copy's share of those
     keys from the oracle's copy gradient, every copy row in full, and dalpha / dbeta as the
@@ -86,11 +86,10 @@ def test_gradient_full_size_sampled():
     scale = 1.0 / math.sqrt(d)
     qg, kg, vg, ag, bg = bf(q), bf(k), bf(v), f32(a), f32(b)
     o, lse = orth.swa_fwd_lse(qg, kg, vg, ag, bg, window=w, scale=scale)
-    dq, dk, dv, da, db = orth.swa_bwd(qg, kg, vg, ag, bg, o, bf(dO), window=w, scale=scale, lse=lse)
     qcg, pg = bf(qc), i32(pos)
     oc, lsec = orth.xattn_fwd(qcg, pg, kg, vg, f32(ac), f32(bc), scale=scale, lse=True)
-    dqc, _, _, dac, dbc = orth.xattn_bwd(qcg, pg, kg, vg, f32(ac), f32(bc), oc, bf(dOc), scale=scale, dk=dk, dv=dv,
-                                         lse=lsec)
+    dq, dk, dv, da, db, dqc, dac, dbc = orth.attn_bwd(qg, kg, vg, ag, bg, o, bf(dO), qcg, pg, f32(ac), f32(bc), oc,
+                                                      bf(dOc), window=w, scale=scale, lse=lse, lsec=lsec)
     torch.cuda.synchronize()
     del o, oc, lse, lsec
     rc = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)  # the copy's share, every key
