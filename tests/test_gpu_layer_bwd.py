@@ -54,6 +54,7 @@ def _reference(inp, w):
     (2, 400, 48, 16, 4, 128, 128, "tail_shuffled", True),   # SFT layout at reduced size
     (2, 400, 48, 16, 4, 128, 128, "tail_shuffled", False),  # without the forwards' log-sum-exp
     (2, 3000, 1, 32, 8, 128, 128, "tail_shuffled", True),   # one copy per sequence: the split copy dq
+    (1, 3000, 3, 32, 8, 128, 128, "random", False),         # few copies, no lse: split dq, both passes
     (1, 130, 130, 8, 1, 64, 128, "every", True),            # PT mode: a copy at every position, G=8
     (1, 300, 20, 8, 2, 128, 33, "random", True),            # duplicates, positions 0 and T-1, narrow window
     (1, 700, 300, 32, 8, 128, 128, "random", True),         # many copies (tensor-memory forward), ragged tails
