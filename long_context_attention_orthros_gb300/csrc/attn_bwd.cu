@@ -12,16 +12,22 @@
 // P - window + 1 .. P (window = T_kv for the copies: keys 0 .. P).
 // Launches (bf16 / fp16 operands, fp32 accumulation, fp32 outputs):
 //   attn_bwd_k16_kernel     an exact fp16 copy of K (for q . k on tensor memory);
-//   attn_bwd_d_kernel       D = dO . o per row;
-//   attn_bwd_dq_kernel      (base stream) warp MMAs, rows on the MMA's M side: K/V stream
-//                           through a two-stage shared-memory ring of 64-key blocks
-//                           (cp.async); pass 1 takes each row's log2-sum-exp (kept for
-//                           the dK/dV kernel), pass 2 dP = dO V^T, dS = P (dP - D),
-//                           dQ += dS K (q as bf16 high part + residual); then dq_raw,
-//                           and dalpha / dbeta through shared, then global, atomics;
-//   attn_bwd_dq_tc_kernel   (copies) the same on tcgen05 (below);
-//   attn_bwd_dkv_tc_kernel  keys on tcgen05's M side, dK and dV in tensor memory (below).
-// P and dS enter the second products as bf16; q enters dK as bf16.
+//   attn_bwd_q16_kernel     the scale-offset q of the stream's rows as fp16;
+//   attn_bwd_d_kernel       D = dO . o per row (and a given forward log-sum-exp in log2 units);
+//   attn_bwd_dq_kernel      (base stream without the forward's log-sum-exp) warp MMAs, rows
+//                           on the MMA's M side: K/V stream through a two-stage shared-memory
+//                           ring of 64-key blocks (cp.async); pass 1 takes each row's
+//                           log2-sum-exp (kept for the dK/dV kernel), pass 2 dP = dO V^T,
+//                           dS = P (dP - D), dQ += dS K (q as bf16 high part + residual);
+//                           then dq_raw, and dalpha / dbeta through shared, then global,
+//                           atomics;
+//   attn_bwd_dq_tc_base_kernel + attn_bwd_dab_kernel  (base stream with it) the same on
+//                           tcgen05, persistent, then the dalpha / dbeta column sums;
+//   attn_bwd_dq_tc_kernel   (copies) the same on tcgen05, one or two passes, optionally
+//                           split over the keys (below);
+//   attn_bwd_dkv_tc_kernel  keys on tcgen05's M side, dK and dV in tensor memory (below),
+//                           for one stream or for both of a layer.
+// P enters dV as bf16; dS enters dQ as bf16 and dK as fp16 (beside the fp16 q).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -1347,10 +1353,10 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // epilogue.  Here one CTA per SM walks a contiguous run of row tiles with the forward's
 // log-sum-exp given (pass 2 only), and overlaps them: two dQ accumulators in tensor memory
 // let the epilogue of tile i run while tile i + 1's MMAs do, and tile i + 1's q / dO load
-// loads into the other of two query buffers while tile i computes.  Per key block (32 keys,
-// so that the two query buffers and a three-stage key ring fit in shared memory) as in the
-// dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as bf16,
-// dQ += dS K.
+// lands in the other of two query buffers while tile i computes.  Per key block (64 keys,
+// through a two-stage ring, so that the two query buffers fit in shared memory beside it)
+// as in the dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as
+// bf16, dQ += dS K.
 // The query tile arrives as fp16 q = x alpha + beta, made for the whole tensor beforehand
 // (attn_bwd_q16_kernel), and dalpha / dbeta are summed afterwards from dq_raw
 // (attn_bwd_dab_kernel): both were measured to pace this kernel when done per tile here
@@ -1358,8 +1364,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
 // warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane = row: the same tensor-memory
 // lanes), so that one tile's epilogue runs beside the next tile's dS; warps 2-3 idle.
-// Tensor memory: S at 32 u, dP at 128 + 32 u (block buffer u of 4, so that four key blocks
-// are in flight), dQ at 256 + D t (tile buffer t).
+// Tensor memory: S at 64 u, dP at 128 + 64 u (block buffer u of 2), dQ at 256 + D t (tile
+// buffer t).
 template <int D>
 struct BpCfg {
     static constexpr int ROWS = 128;
@@ -1369,7 +1375,7 @@ struct BpCfg {
     static constexpr int QSLAB = ROWS * 128;
     static constexpr int KSLAB = KB * 128;
     static constexpr int QBUF = 2 * SLABS * QSLAB;                 // one query buffer: q, dO
-    static constexpr int Q16_OFF = 0;                              // [2] raw x, then q as fp16
+    static constexpr int Q16_OFF = 0;                              // [2] q as fp16
     static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;         // [2] dO (QBUF apart)
     static constexpr int K_OFF = 2 * QBUF;                         // [STG] K blocks (bf16)
     static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
