@@ -87,22 +87,36 @@ __device__ __forceinline__ int unit_pos(const AttnBwdParams &p, int b, int u)
 
 // The tensor-memory kernels take q . k in fp16 (as the forward's tensor-memory path): K is
 // converted once per call, exactly (|k| < 65520, else ORTHROS_DEVERR_RANGE).
+__device__ __forceinline__ uint4 bf16x8_to_fp16(uint4 u, bool &bad)
+{
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
+        __half2 hv = __floats2half2_rn(f.x, f.y);
+        w[e] = *reinterpret_cast<uint32_t *>(&hv);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// two 16-byte chunks per thread and step, both loads in flight
 __global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k, uint16_t *k16, long long n8,
                                                            int32_t *dev_err)
 {
     bool bad = false;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(k) + i);
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16x2(w[e]);
-            bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
-            __half2 hv = __floats2half2_rn(f.x, f.y);
-            w[e] = *reinterpret_cast<uint32_t *>(&hv);
-        }
-        reinterpret_cast<uint4 *>(k16)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(k);
+    uint4 *o4 = reinterpret_cast<uint4 *>(k16);
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += 2 * stride) {
+        const long long i2 = i + stride;
+        const uint4 u0 = __ldg(k4 + i);
+        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
+        if (i2 < n8)
+            u1 = __ldg(k4 + i2);
+        o4[i] = bf16x8_to_fp16(u0, bad);
+        if (i2 < n8)
+            o4[i2] = bf16x8_to_fp16(u1, bad);
     }
     if (bad)
         record_error(dev_err, ORTHROS_DEVERR_RANGE);
@@ -110,34 +124,56 @@ __global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k
 
 // ------------------------------------------------------------------ fp16 q and the dalpha / dbeta sums
 
-// q = x alpha + beta of every base row as fp16 (workspace), for the persistent dq kernel;
-// |q| >= 65504 sets ORTHROS_DEVERR_RANGE
+// q = x alpha + beta of every row of the stream as fp16 (workspace), for the dK/dV kernel
+// and the persistent dq kernel; |q| >= 65504 sets ORTHROS_DEVERR_RANGE.  A thread takes two
+// 16-byte chunks per step (both loads in flight) and keeps its chunks' column in the row
+// [0, hd8) by adding the grid stride modulo hd8.
+__device__ __forceinline__ uint4 scale_offset_fp16(uint4 u, const float *alpha, const float *beta, int col,
+                                                   bool &bad)
+{
+    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + col));
+    const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + col + 4));
+    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + col));
+    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + col + 4));
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        const float qa = fmaf(f.x, av[2 * e], bv[2 * e]), qc = fmaf(f.y, av[2 * e + 1], bv[2 * e + 1]);
+        bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
+        __half2 hv = __floats2half2_rn(qa, qc);
+        o[e] = *reinterpret_cast<uint32_t *>(&hv);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256) attn_bwd_q16_kernel(const orthros_bf16 *x, const float *alpha,
                                                            const float *beta, uint16_t *q16, long long n8, int hd8,
                                                            int32_t *dev_err)
 {
     bool bad = false;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int col = static_cast<int>(i % hd8) * 8;  // h * D + d of the first element
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + col));
-        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + col + 4));
-        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + col));
-        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + col + 4));
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16x2(w[e]);
-            const float qa = fmaf(f.x, av[2 * e], bv[2 * e]), qc = fmaf(f.y, av[2 * e + 1], bv[2 * e + 1]);
-            bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
-            __half2 hv = __floats2half2_rn(qa, qc);
-            o[e] = *reinterpret_cast<uint32_t *>(&hv);
-        }
-        reinterpret_cast<uint4 *>(q16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const int step = static_cast<int>(stride % hd8);
+    long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    int c = static_cast<int>(i % hd8);  // column chunk of chunk i
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
+    uint4 *q4 = reinterpret_cast<uint4 *>(q16);
+    for (; i < n8; i += 2 * stride) {
+        const long long i2 = i + stride;
+        int c2 = c + step;
+        c2 -= c2 >= hd8 ? hd8 : 0;
+        const uint4 u0 = __ldg(x4 + i);
+        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
+        if (i2 < n8)
+            u1 = __ldg(x4 + i2);
+        q4[i] = scale_offset_fp16(u0, alpha, beta, c * 8, bad);
+        if (i2 < n8)
+            q4[i2] = scale_offset_fp16(u1, alpha, beta, c2 * 8, bad);
+        c = c2 + step;
+        c -= c >= hd8 ? hd8 : 0;
     }
     if (bad)
         record_error(dev_err, ORTHROS_DEVERR_RANGE);
