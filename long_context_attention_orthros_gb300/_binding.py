@@ -96,7 +96,14 @@ def _check(status: int, what: str) -> None:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a tensor argument.  Every pointer the library takes is a device
+    pointer of the call's GPU (the current device inside the calls below): a host tensor or
+    one on another GPU is refused here rather than handed to a kernel."""
+    if t is None:
+        return None
+    if not t.is_cuda or t.device.index != torch.cuda.current_device():
+        raise OrthrosError(f"tensor arguments must be CUDA tensors on the call's device (got {t.device})")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(device) -> ctypes.c_void_p:
