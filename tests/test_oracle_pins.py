@@ -67,6 +67,21 @@ def test_swa_equals_sdpa_with_band_mask(B, T, Hq, Hkv, d, w):
     np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
 
 
+def test_swa_rows_equal_sdpa_at_the_sampled_rows():
+    """The sampled-row form (the reference of the full-size GPU tests) == library SDPA over the
+    band mask at those rows: both batch entries, the first and last rows, rows at the window
+    edge, a repeated row, in arbitrary order."""
+    B, T, Hq, Hkv, d, w = 2, 70, 4, 2, 16, 9
+    q, k, v, a, b = _rand_inputs(111, B, T, Hq, Hkv, d)
+    s = 1 / math.sqrt(d)
+    bi = np.array([0, 1, 1, 0, 1, 0, 1], np.int64)
+    ti = np.array([0, T - 1, 8, 9, 9, T - 1, 0], np.int64)
+    got = oracle.swa_rows(q, k, v, a, b, w, s, bi, ti)
+    q64 = _w(q) * a.astype(np.float64) + b.astype(np.float64)
+    ref = _sdpa(q64, _w(k), _w(v), _band(T, w), s)
+    np.testing.assert_allclose(got, ref[bi, ti], rtol=0, atol=1e-12)
+
+
 def test_swa_window_ge_T_is_full_causal():
     """With w >= T the sliding window covers all of 1..t: plain causal attention."""
     B, T, Hq, Hkv, d = 2, 96, 4, 1, 32
