@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "liborthros.so")
 SOURCES = ["swa_fwd.cu", "swa_tc.cu", "xattn_fwd.cu", "xattn_tc.cu", "decode_step.cu", "orthros_api.cu",
-           "xattn_noalloc.cu", "attn_bwd.cu"]
+           "xattn_noalloc.cu", "attn_bwd.cu", "attn_bwd_d128.cu", "attn_bwd_d64.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

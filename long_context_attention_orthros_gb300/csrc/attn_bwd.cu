@@ -1,1748 +1,18 @@
-// attn_bwd.cu -- gradients of "Orthros: Phase-Aware Heterogeneous Attention" for
-// the training modes (Sec. 3.2: SFT / PT compute every base position and T_out
-// copies): the base stream, Eq. (4), and the output copies, Eq. (5), each with its
-// scale-offset q = Q_raw * alpha + beta (Sec. 3.1).  For an output gradient dO and,
-// per query row with the keys j it attends,
-//   p_j = softmax_j(s_j), s_j = scale * (q . k_j);  dp_j = dO . v_j
-//   D = dO . o = sum_j p_j dp_j;  ds_j = p_j (dp_j - D)
-//   dq = scale * sum_j ds_j k_j;  dk_j += scale * ds_j q;  dv_j += p_j dO
-//   dq_raw = dq * alpha;  dalpha += q_raw * dq;  dbeta += dq
-// A query row is a "unit" (a base token, or a copy) times a head; the unit sits at
-// position P (the token itself, or the copy's original position) and sees keys
-// P - window + 1 .. P (window = T_kv for the copies: keys 0 .. P).
-// Launches (bf16 / fp16 operands, fp32 accumulation, fp32 outputs):
-//   attn_bwd_k16_kernel     an exact fp16 copy of K (for q . k on tensor memory);
-//   attn_bwd_q16_kernel     the scale-offset q of the stream's rows as fp16;
-//   attn_bwd_d_kernel       D = dO . o per row (and a given forward log-sum-exp in log2 units);
-//   attn_bwd_dq_kernel      (base stream without the forward's log-sum-exp) warp MMAs, rows
-//                           on the MMA's M side: K/V stream through a two-stage shared-memory
-//                           ring of 64-key blocks (cp.async); pass 1 takes each row's
-//                           log2-sum-exp (kept for the dK/dV kernel), pass 2 dP = dO V^T,
-//                           dS = P (dP - D), dQ += dS K (q as bf16 high part + residual);
-//                           then dq_raw, and dalpha / dbeta through shared, then global,
-//                           atomics;
-//   attn_bwd_dq_tc_base_kernel + attn_bwd_dab_kernel  (base stream with it) the same on
-//                           tcgen05, persistent, then the dalpha / dbeta column sums;
-//   attn_bwd_dq_tc_kernel   (copies) the same on tcgen05, one or two passes, optionally
-//                           split over the keys (below);
-//   attn_bwd_dkv_tc_kernel  keys on tcgen05's M side, dK and dV in tensor memory (below),
-//                           for one stream or for both of a layer.
-// P enters dV as bf16; dS enters dQ as bf16 and dK as fp16 (beside the fp16 q).
-#include <cuda_fp16.h>
-
-#include "common.cuh"
+// attn_bwd.cu -- host side of the gradients of "Orthros: Phase-Aware Heterogeneous Attention"
+// (the base stream, Eq. (4), and the output copies, Eq. (5), each with its scale-offset):
+// the workspace layout and the dispatch on the head dimension.  The kernels and their launch
+// order are in attn_bwd.cuh, instantiated per head dimension in attn_bwd_d128.cu and
+// attn_bwd_d64.cu.
 #include "kernels.cuh"
-#include "tc.cuh"
-#include "xattn.cuh"
 
 namespace orthros {
 
-namespace {
-
-constexpr float kLog2eF = 1.4426950408889634f;
-constexpr int BWD_ROWS = 64;  // query rows of a warp-MMA dq CTA
-constexpr int BWD_KEYS = 64;  // keys per streamed block of the warp-MMA dq kernel
-
-// [rows][D] bf16 tile in shared memory as D/64 slabs of rows x 128 bytes, 128-byte swizzle
-__device__ __forceinline__ uint32_t tile_off(int row, int col, int slab_bytes)
-{
-    return static_cast<uint32_t>((col / 64) * slab_bytes) + sw128_offset(row, (col % 64) / 8);
-}
-
-// 16-byte asynchronous copy global -> shared; valid = false writes zeros (nothing is read)
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
-{
-    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
-
-// position of unit u of sequence b, or -1 when it has none in [0, T_kv)
-template <bool COPY>
-__device__ __forceinline__ int unit_pos(const AttnBwdParams &p, int b, int u)
-{
-    if (u >= p.n_units)
-        return -1;
-    if (!COPY)
-        return u;
-    const int P = __ldg(p.pos + static_cast<long long>(b) * p.n_units + u);
-    return (P >= 0 && P < p.T_kv) ? P : -1;
-}
-
-}  // namespace
-
-// ------------------------------------------------------------------ fp16 copy of K
-
-// The tensor-memory kernels take q . k in fp16 (as the forward's tensor-memory path): K is
-// converted once per call, exactly (|k| < 65520, else ORTHROS_DEVERR_RANGE).
-__device__ __forceinline__ uint4 bf16x8_to_fp16(uint4 u, bool &bad)
-{
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(w[e]);
-        bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
-        __half2 hv = __floats2half2_rn(f.x, f.y);
-        w[e] = *reinterpret_cast<uint32_t *>(&hv);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// two 16-byte chunks per thread and step, both loads in flight
-__global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k, uint16_t *k16, long long n8,
-                                                           int32_t *dev_err)
-{
-    bool bad = false;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const uint4 *k4 = reinterpret_cast<const uint4 *>(k);
-    uint4 *o4 = reinterpret_cast<uint4 *>(k16);
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += 2 * stride) {
-        const long long i2 = i + stride;
-        const uint4 u0 = __ldg(k4 + i);
-        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-        if (i2 < n8)
-            u1 = __ldg(k4 + i2);
-        o4[i] = bf16x8_to_fp16(u0, bad);
-        if (i2 < n8)
-            o4[i2] = bf16x8_to_fp16(u1, bad);
-    }
-    if (bad)
-        record_error(dev_err, ORTHROS_DEVERR_RANGE);
-}
-
-// ------------------------------------------------------------------ fp16 q and the dalpha / dbeta sums
-
-// q = x alpha + beta of every row of the stream as fp16 (workspace), for the dK/dV kernel
-// and the persistent dq kernel; |q| >= 65504 sets ORTHROS_DEVERR_RANGE.  A thread takes two
-// 16-byte chunks per step (both loads in flight) and keeps its chunks' column in the row
-// [0, hd8) by adding the grid stride modulo hd8.
-__device__ __forceinline__ uint4 scale_offset_fp16(uint4 u, const float *alpha, const float *beta, int col,
-                                                   bool &bad)
-{
-    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + col));
-    const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + col + 4));
-    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + col));
-    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + col + 4));
-    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(w[e]);
-        const float qa = fmaf(f.x, av[2 * e], bv[2 * e]), qc = fmaf(f.y, av[2 * e + 1], bv[2 * e + 1]);
-        bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
-        __half2 hv = __floats2half2_rn(qa, qc);
-        o[e] = *reinterpret_cast<uint32_t *>(&hv);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__global__ void __launch_bounds__(256) attn_bwd_q16_kernel(const orthros_bf16 *x, const float *alpha,
-                                                           const float *beta, uint16_t *q16, long long n8, int hd8,
-                                                           int32_t *dev_err)
-{
-    bool bad = false;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const int step = static_cast<int>(stride % hd8);
-    long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    int c = static_cast<int>(i % hd8);  // column chunk of chunk i
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
-    uint4 *q4 = reinterpret_cast<uint4 *>(q16);
-    for (; i < n8; i += 2 * stride) {
-        const long long i2 = i + stride;
-        int c2 = c + step;
-        c2 -= c2 >= hd8 ? hd8 : 0;
-        const uint4 u0 = __ldg(x4 + i);
-        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-        if (i2 < n8)
-            u1 = __ldg(x4 + i2);
-        q4[i] = scale_offset_fp16(u0, alpha, beta, c * 8, bad);
-        if (i2 < n8)
-            q4[i2] = scale_offset_fp16(u1, alpha, beta, c2 * 8, bad);
-        c = c2 + step;
-        c -= c >= hd8 ? hd8 : 0;
-    }
-    if (bad)
-        record_error(dev_err, ORTHROS_DEVERR_RANGE);
-}
-
-// dalpha[c] += sum_rows x * dq, dbeta[c] += sum_rows dq over the columns c = h * D + d, with
-// dq = dq_raw / alpha (both sums are linear in the rows: one pass after the dq kernel).
-// Each thread owns 4 columns over a run of rows; one atomic per column and CTA.
-__global__ void __launch_bounds__(256) attn_bwd_dab_kernel(const float *dq_raw, const orthros_bf16 *x,
-                                                           const float *alpha, float *dalpha, float *dbeta,
-                                                           long long rows, int cols, int rows_per_cta)
-{
-    const int c4 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;  // first of this thread's columns
-    if (c4 >= cols)
-        return;
-    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_cta;
-    const long long r1 = min(rows, r0 + rows_per_cta);
-    const float4 al = __ldg(reinterpret_cast<const float4 *>(alpha + c4));
-    const float4 ia = make_float4(1.f / al.x, 1.f / al.y, 1.f / al.z, 1.f / al.w);
-    float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
-    for (long long r = r0; r < r1; ++r) {
-        const float4 g = __ldcs(reinterpret_cast<const float4 *>(dq_raw + r * cols + c4));
-        const uint2 xr = __ldcs(reinterpret_cast<const uint2 *>(x + r * cols + c4));
-        const float2 x0 = unpack_bf16x2(xr.x), x1 = unpack_bf16x2(xr.y);
-        const float4 dq = make_float4(g.x * ia.x, g.y * ia.y, g.z * ia.z, g.w * ia.w);
-        sb.x += dq.x;
-        sb.y += dq.y;
-        sb.z += dq.z;
-        sb.w += dq.w;
-        sa.x = fmaf(x0.x, dq.x, sa.x);
-        sa.y = fmaf(x0.y, dq.y, sa.y);
-        sa.z = fmaf(x1.x, dq.z, sa.z);
-        sa.w = fmaf(x1.y, dq.w, sa.w);
-    }
-    atomicAdd(dalpha + c4, sa.x);
-    atomicAdd(dalpha + c4 + 1, sa.y);
-    atomicAdd(dalpha + c4 + 2, sa.z);
-    atomicAdd(dalpha + c4 + 3, sa.w);
-    atomicAdd(dbeta + c4, sb.x);
-    atomicAdd(dbeta + c4 + 1, sb.y);
-    atomicAdd(dbeta + c4 + 2, sb.z);
-    atomicAdd(dbeta + c4 + 3, sb.w);
-}
-
-// ------------------------------------------------------------------ D = dO . o
-
-// D/8 lanes per row, 16-byte loads (two or four rows per warp in flight)
-template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, const orthros_bf16 *dO, float *Dout,
-                                                         const float *lse_in, float *lse_out, long long rows)
-{
-    constexpr int LPR = D / 8;  // lanes per row
-    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / LPR;
-    const int sub = threadIdx.x % LPR;
-    float acc = 0.f;
-    if (row < rows) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(o + row * D) + sub);
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + row * D) + sub);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 x = unpack_bf16x2(aw[e]), y = unpack_bf16x2(bw[e]);
-            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-        }
-    }
-#pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && sub == 0) {
-        Dout[row] = acc;
-        if (lse_in != nullptr)  // the forward's log-sum-exp, to log2 units
-            lse_out[row] = lse_in[row] * kLog2eF;
-    }
-}
-
-// ------------------------------------------------------------------ dQ (rows on M)
-
-template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
-{
-    constexpr int UNITS = BWD_ROWS / G;
-    constexpr int SLAB = BWD_KEYS * 128;  // one 64-column slab of a 64-key block
-    constexpr int BLK = (D / 64) * SLAB;  // one K (or V) block
-    const int u0 = blockIdx.x * UNITS, bh = blockIdx.y;
-    const int b = bh / p.Hkv, g = bh % p.Hkv;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    float *red = reinterpret_cast<float *>(smem + 4 * BLK);  // [2][G][D]: dalpha, dbeta
-    int *krange = reinterpret_cast<int *>(red + 2 * G * D);  // the CTA's lowest and highest key
-    const uint32_t sbase = smem_u32(smem);
-
-    // this warp's 16 rows: r = 16 warp + 0..15 -> unit u0 + r / G, head g G + r % G
-    const int gr = lane >> 2, qd = (lane & 3) * 2;
-    const int rowA = 16 * warp + gr, rowB = rowA + 8;
-    const int uA = u0 + rowA / G, uB = u0 + rowB / G;
-    const int hA = g * G + rowA % G, hB = g * G + rowB % G;
-    const int PA = unit_pos<COPY>(p, b, uA), PB = unit_pos<COPY>(p, b, uB);
-    const bool vA = PA >= 0, vB = PB >= 0;
-    if (COPY && (lane & 3) == 0 && ((uA < p.n_units && !vA) || (uB < p.n_units && !vB)))
-        record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
-    const int loA = PA - p.window + 1, loB = PB - p.window + 1;
-    int wlo = 0x7fffffff, whi = -1;  // the warp's key range
-    if (vA) {
-        wlo = max(0, loA);
-        whi = PA;
-    }
-    if (vB) {
-        wlo = min(wlo, max(0, loB));
-        whi = max(whi, PB);
-    }
-    wlo = __reduce_min_sync(0xffffffffu, wlo);
-    whi = __reduce_max_sync(0xffffffffu, whi);
-    if (threadIdx.x == 0) {
-        krange[0] = 0x7fffffff;
-        krange[1] = -1;
-    }
-    for (int i = threadIdx.x; i < 2 * G * D; i += 128)
-        red[i] = 0.f;
-    __syncthreads();
-    if (lane == 0 && whi >= 0) {
-        atomicMin(&krange[0], wlo);
-        atomicMax(&krange[1], whi);
-    }
-    __syncthreads();
-    const int cb0 = krange[1] >= 0 ? krange[0] / BWD_KEYS : 0;
-    const int cb1 = krange[1] >= 0 ? krange[1] / BWD_KEYS + 1 : 0;  // key blocks [cb0, cb1)
-
-    const long long q_bs = static_cast<long long>(p.n_units) * p.Hq * D;
-    const float c2 = p.scale * kLog2eF;  // logits in log2 units
-    WarpRows16<D> st;                    // q fragments (unscaled q = x alpha + beta) + dQ accumulators
-    uint32_t ga[D / 16][4];              // dO fragments (A operand)
-#pragma unroll
-    for (int kt2 = 0; kt2 < D / 16; ++kt2)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const bool isB = r & 1;
-            const int u = isB ? uB : uA, h = isB ? hB : hA;
-            const int dcol = kt2 * 16 + qd + ((r & 2) ? 8 : 0);
-            uint32_t hi = 0, lo = 0, gw = 0;
-            if (isB ? vB : vA) {
-                const long long off = b * q_bs + (static_cast<long long>(u) * p.Hq + h) * D;
-                load_q_pair(p.q + off, p.alpha + h * D, p.beta + h * D, dcol, 1.f, hi, lo);
-                gw = *reinterpret_cast<const uint32_t *>(p.dO + off + dcol);
-            }
-            st.qa[kt2][r] = hi;
-            st.ql[kt2][r] = lo;
-            ga[kt2][r] = gw;
-        }
-    st.reset();
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    const int kld_row = (lane & 7) + ((lane >> 4) << 3), kld_hi = (lane >> 3) & 1;
-    const int vld_row = (lane & 7) + (((lane >> 3) & 1) << 3), vld_hi = lane >> 4;
-
-    // stream key block blk into ring slot buf: K, and V when withV
-    const long long kv_rs = static_cast<long long>(p.Hkv) * D;
-    const orthros_bf16 *kb = p.k + static_cast<long long>(b) * p.T_kv * kv_rs + static_cast<long long>(g) * D;
-    const orthros_bf16 *vb = p.v + static_cast<long long>(b) * p.T_kv * kv_rs + static_cast<long long>(g) * D;
-    auto stage = [&](int blk, int buf, bool withV) {
-        const int key0 = blk * BWD_KEYS;
-        for (int i = threadIdx.x; i < BWD_KEYS * (D / 8); i += 128) {
-            const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-            const int key = key0 + r;
-            const bool ok = key < p.T_kv;
-            const long long off = static_cast<long long>(ok ? key : 0) * kv_rs + c;
-            const uint32_t o = sbase + buf * 2 * BLK + tile_off(r, c, SLAB);
-            cp_async16(o, kb + off, ok);
-            if (withV)
-                cp_async16(o + BLK, vb + off, ok);
-        }
-        cp_async_commit();
-    };
-
-    // S chunk (16 rows x keys kc .. kc+15 at block row jc) in log2 units, masked
-    auto s_chunk = [&](uint32_t kbase, int jc, int kc, float (&s)[2][4]) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-        for (int kt2 = 0; kt2 < D / 16; ++kt2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + tile_off(jc + kld_row, kt2 * 16 + kld_hi * 8, SLAB), b0, b1, b2, b3);
-            mma_16816(s[0], st.qa[kt2], b0, b1);
-            mma_16816(s[1], st.qa[kt2], b2, b3);
-            mma_16816(s[0], st.ql[kt2], b0, b1);
-            mma_16816(s[1], st.ql[kt2], b2, b3);
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = kc + i * 8 + qd + (e & 1);
-                const bool isB = e & 2;
-                const int P = isB ? PB : PA, lo = isB ? loB : loA;
-                s[i][e] = (key <= P && key >= lo) ? s[i][e] * c2 : NEG_INF;  // P = -1: no key
-            }
-    };
-
-    float mA = NEG_INF, mB = NEG_INF, lA = 0.f, lB = 0.f, lseA = 0.f, lseB = 0.f, DA = 0.f, DB = 0.f;
-    const long long rA = (static_cast<long long>(b) * p.n_units + uA) * p.Hq + hA;
-    const long long rB = (static_cast<long long>(b) * p.n_units + uB) * p.Hq + hB;
-    // pass 1 (each row's log-sum-exp) is skipped when the forward's is given
-#pragma unroll 1
-    for (int pass = p.lse_in != nullptr ? 2 : 1; pass <= 2; ++pass) {
-        if (pass == 2) {
-            if (p.lse_in != nullptr) {  // converted to log2 units by the D kernel
-                lseA = vA ? p.lse[rA] : 0.f;
-                lseB = vB ? p.lse[rB] : 0.f;
-            } else {
-                // log2-sum-exp of each row over its keys (every valid row holds at least its own key)
-                lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-                lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-                lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-                lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-                lseA = vA ? mA + __log2f(lA) : 0.f;
-                lseB = vB ? mB + __log2f(lB) : 0.f;
-                if ((lane & 3) == 0) {
-                    if (vA)
-                        p.lse[rA] = lseA;
-                    if (vB)
-                        p.lse[rB] = lseB;
-                }
-            }
-            DA = vA ? p.Drow[rA] : 0.f;
-            DB = vB ? p.Drow[rB] : 0.f;
-        }
-        if (cb0 < cb1)
-            stage(cb0, 0, pass == 2);
-#pragma unroll 1
-        for (int blk = cb0; blk < cb1; ++blk) {
-            const int buf = (blk - cb0) & 1;
-            if (blk + 1 < cb1) {
-                stage(blk + 1, buf ^ 1, pass == 2);
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
-            __syncthreads();
-            const uint32_t kbase = sbase + buf * 2 * BLK, vbase = kbase + BLK;
-#pragma unroll 1
-            for (int jc = 0; jc < BWD_KEYS; jc += 16) {
-                const int kc = blk * BWD_KEYS + jc;
-                if (kc + 15 < wlo || kc > whi)
-                    continue;  // warp-uniform: no key of this chunk is seen by the warp's rows
-                float s[2][4];
-                s_chunk(kbase, jc, kc, s);
-                if (pass == 1) {
-                    float cA = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-                    float cB = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-                    cA = fmaxf(cA, __shfl_xor_sync(0xffffffffu, cA, 1));
-                    cA = fmaxf(cA, __shfl_xor_sync(0xffffffffu, cA, 2));
-                    cB = fmaxf(cB, __shfl_xor_sync(0xffffffffu, cB, 1));
-                    cB = fmaxf(cB, __shfl_xor_sync(0xffffffffu, cB, 2));
-                    const float nA = fmaxf(mA, cA), nB = fmaxf(mB, cB);
-                    const float zA = nA == NEG_INF ? 0.f : nA, zB = nB == NEG_INF ? 0.f : nB;
-                    lA = lA * fast_exp2(mA - zA) + fast_exp2(s[0][0] - zA) + fast_exp2(s[0][1] - zA) +
-                         fast_exp2(s[1][0] - zA) + fast_exp2(s[1][1] - zA);
-                    lB = lB * fast_exp2(mB - zB) + fast_exp2(s[0][2] - zB) + fast_exp2(s[0][3] - zB) +
-                         fast_exp2(s[1][2] - zB) + fast_exp2(s[1][3] - zB);
-                    mA = nA;
-                    mB = nB;
-                } else {
-                    float dp[2][4];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        dp[i][0] = dp[i][1] = dp[i][2] = dp[i][3] = 0.f;
-#pragma unroll
-                    for (int kt2 = 0; kt2 < D / 16; ++kt2) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(vbase + tile_off(jc + kld_row, kt2 * 16 + kld_hi * 8, SLAB), b0, b1, b2, b3);
-                        mma_16816(dp[0], ga[kt2], b0, b1);
-                        mma_16816(dp[1], ga[kt2], b2, b3);
-                    }
-                    uint32_t da[4];
-                    float ds[2][4];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const bool isB = e & 2;
-                            ds[i][e] = fast_exp2(s[i][e] - (isB ? lseB : lseA)) * (dp[i][e] - (isB ? DB : DA));
-                        }
-                    da[0] = pack_bf16x2(ds[0][0], ds[0][1]);
-                    da[1] = pack_bf16x2(ds[0][2], ds[0][3]);
-                    da[2] = pack_bf16x2(ds[1][0], ds[1][1]);
-                    da[3] = pack_bf16x2(ds[1][2], ds[1][3]);
-#pragma unroll
-                    for (int dp2 = 0; dp2 < D / 16; ++dp2) {
-                        uint32_t v0, v1, v2, v3;
-                        ldsm_x4_trans(kbase + tile_off(jc + vld_row, dp2 * 16 + vld_hi * 8, SLAB), v0, v1, v2, v3);
-                        mma_16816(st.o[2 * dp2], da, v0, v1);
-                        mma_16816(st.o[2 * dp2 + 1], da, v2, v3);
-                    }
-                }
-            }
-            __syncthreads();  // slot buf is refilled by the next iteration's prefetch
-        }
-    }
-    // epilogue: dq = scale * dQ; dq_raw = dq * alpha; dalpha += x * dq, dbeta += dq
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const bool live = half ? vB : vA;
-        const int u = half ? uB : uA, h = half ? hB : hA, hh = h - g * G;
-        const long long off = b * q_bs + (static_cast<long long>(u) * p.Hq + h) * D;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            const int dcol = i * 8 + qd;
-            if (!live)
-                continue;
-            const float dq0 = st.o[i][2 * half] * p.scale, dq1 = st.o[i][2 * half + 1] * p.scale;
-            const float2 al = __ldg(reinterpret_cast<const float2 *>(p.alpha + h * D + dcol));
-            *reinterpret_cast<float2 *>(p.dq + off + dcol) = make_float2(dq0 * al.x, dq1 * al.y);
-            const float2 x = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(p.q + off + dcol));
-            atomicAdd(&red[hh * D + dcol], x.x * dq0);
-            atomicAdd(&red[hh * D + dcol + 1], x.y * dq1);
-            atomicAdd(&red[G * D + hh * D + dcol], dq0);
-            atomicAdd(&red[G * D + hh * D + dcol + 1], dq1);
-        }
-        if (!live && u < p.n_units) {  // a copy without a valid position: zero gradient row
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i)
-                *reinterpret_cast<float2 *>(p.dq + off + i * 8 + qd) = make_float2(0.f, 0.f);
-        }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += 128) {
-        atomicAdd(p.dalpha + g * G * D + i, red[i]);
-        atomicAdd(p.dbeta + g * G * D + i, red[G * D + i]);
-    }
-}
-
-// ------------------------------------------------------------------ dK, dV on tcgen05
-
-// A CTA owns 128 keys of one (batch, KV head): the MMA's M side, K and V resident in
-// shared memory (one TMA load each).  The query rows that can see them stream through
-// a four-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
-// lands them): q as fp16 (the scale-offset applied and rounded once by
-// attn_bwd_q16_kernel, which also flags a query outside the fp16 range) and dO.  Per round
-//   S^T  = K q^T          (fp16: K from the call's exact fp16 copy)
-//   dP^T = V dO^T         (bf16) fp32 in tensor memory (two buffers each)
-//   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), written
-//          back over S^T (P^T, bf16) and dP^T (dS^T, fp16; |dS| >= 65504 sets
-//          ORTHROS_DEVERR_RANGE) by the softmax warps (lane = key)
-//   dV  += P^T dO,  dK += dS^T q           (A from tensor memory, B = the row tiles)
-// and dK, dV (fp32, tensor memory) leave once at the end.  The MMA issuer computes S^T,
-// dP^T of round i + 1 while the softmax works on round i.
-// Roles (256 threads, one CTA per SM):
-//   warp 0      TMA producer (K, V once; q and dO per round)
-//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2-3   stage each round's per-row lse, D and position (one row per thread)
-//   warps 4-7   P^T, dS^T (tensor-memory lane = key), then the dK / dV epilogue
-// Tensor memory: S^T at 64 u, dP^T at 128 + 64 u (buffer u), dK at 256, dV at 256 + D.
-// Every wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and every role drains
-// to the common exit, where tensor memory is released.
-template <int D>
-struct BtCfg {
-    static constexpr int KEYS = 128;          // keys of a CTA (the MMA's M)
-    static constexpr int RB = 64;             // query rows per round (N of S^T, dP^T)
-    static constexpr int SLABS = D / 64;
-    static constexpr int STG = 4;
-    static constexpr int KSLAB = KEYS * 128;  // one 64-wide slab of the K (or V) tile
-    static constexpr int RSLAB = RB * 128;    // one 64-wide slab of a row tile
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + SLABS * KSLAB;
-    static constexpr int ST_OFF = V_OFF + SLABS * KSLAB;
-    static constexpr int ST_Q16 = 0;                  // scale-offset q as fp16 (from the workspace)
-    static constexpr int ST_DO = SLABS * RSLAB;       // dO
-    static constexpr int ST_BYTES = 2 * SLABS * RSLAB;
-    static constexpr int META_OFF = ST_OFF + STG * ST_BYTES;  // [STG][3][RB]: lse, D, position
-    static constexpr int BAR_OFF = META_OFF + STG * 3 * RB * 4;
-    static constexpr int NBARS = 1 + 3 * STG + 3 * 2 + 1;
-    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
-    static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DK = 256, TM_DV = 256 + D;
-};
-
-// q = x alpha + beta for 8 elements of head h at column d0: fp16 and bf16 copies
-__device__ __forceinline__ void scale_offset8(uint4 x4, const float *alpha, const float *beta, int d0, uint4 &q16,
-                                              uint4 &qb, bool &bad)
-{
-    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(alpha + d0));
-    const float4 a1 = __ldg(reinterpret_cast<const float4 *>(alpha + d0 + 4));
-    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(beta + d0));
-    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(beta + d0 + 4));
-    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
-    uint32_t hw[4], bw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 xv = unpack_bf16x2(xw[e]);
-        const float qa = fmaf(xv.x, av[2 * e], bv[2 * e]), qc = fmaf(xv.y, av[2 * e + 1], bv[2 * e + 1]);
-        bad |= !(fmaxf(fabsf(qa), fabsf(qc)) < 65504.f);
-        __half2 hv = __floats2half2_rn(qa, qc);
-        hw[e] = *reinterpret_cast<uint32_t *>(&hv);
-        bw[e] = pack_bf16x2(qa, qc);
-    }
-    q16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    qb = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-}
-
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-// wait on an mbarrier as a whole warp (lane 0 polls); false after the time limit
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait(bar, parity);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
-// the next round (of `units` units) at or after r that holds a unit seeing keys >= kt0
-// (copies; base rounds are a contiguous range).  Called by whole warps.
-template <bool COPY>
-__device__ __forceinline__ int next_round(const AttnBwdParams &p, int b, int kt0, int r, int r_end, int units)
-{
-    if (!COPY)
-        return r;
-    const int lane = threadIdx.x & 31;
-    for (; r < r_end; ++r) {
-        bool hit = false;
-        for (int u = lane; u < units; u += 32)
-            hit |= unit_pos<COPY>(p, b, r * units + u) >= kt0;
-        if (__any_sync(0xffffffffu, hit))
-            return r;
-    }
-    return r_end;
-}
-
-constexpr int DKV_TC_THREADS = 384;
-constexpr int DKV_TC_CONV = 192;  // preparation threads of the dQ kernel (warps 2-3 and 8-11)
-constexpr int DKV_THREADS = 256;  // the dK/dV kernel: producer, MMA, 2 metadata warps, 4 softmax warps
-
-// The rounds of query rows a dK/dV CTA takes, in order: phase 0 is the stream of p (base
-// rows: rounds kt0/UNITS .. while a row can see the block; copies: the rounds holding a copy at
-// a position >= kt0), phase 1 (STREAMS == 2) the copies of pc.  seek moves (ph, r) to the first
-// round at or after it and returns false once none is left.  Called by whole warps.
-template <int STREAMS>
-struct DkvRounds {
-    const AttnBwdParams &p, &pc;
-    int b, kt0, units, base_end;
-    __device__ __forceinline__ bool seek(int &ph, int &r) const
-    {
-        if (ph == 0) {
-            if (STREAMS == 1) {
-                const int e = (p.n_units + units - 1) / units;
-                r = next_round<true>(p, b, kt0, r, e, units);
-                return r < e;
-            }
-            if (r < base_end)
-                return true;
-            if (STREAMS == 0)
-                return false;
-            ph = 1;
-            r = 0;
-        }
-        const int e = (pc.n_units + units - 1) / units;
-        r = next_round<true>(pc, b, kt0, r, e, units);
-        return r < e;
-    }
-};
-
-// position of unit u of the round's stream (copies: pos, -1 when out of range or past the end)
-__device__ __forceinline__ int round_unit_pos(const AttnBwdParams &p, const AttnBwdParams &pc, bool from_pc,
-                                              bool copy, int b, int u)
-{
-    const int n = from_pc ? pc.n_units : p.n_units;
-    if (u >= n)
-        return -1;
-    if (!copy)
-        return u;
-    const int32_t *pos = from_pc ? pc.pos : p.pos;
-    const int P = __ldg(pos + static_cast<long long>(b) * n + u);
-    return (P >= 0 && P < p.T_kv) ? P : -1;
-}
-
-// STREAMS: 0 the base stream (p), 1 copies (p), 2 the base stream (p) and then the copies (pc,
-// with its own row maps qcmap / ocmap) into the same dK / dV, written once.
-template <int D, int G, int STREAMS>
-__global__ void __launch_bounds__(DKV_THREADS, 1)
-    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                           const __grid_constant__ CUtensorMap qcmap, const __grid_constant__ CUtensorMap ocmap,
-                           const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                           const AttnBwdParams p, const AttnBwdParams pc)
-{
-    using C = BtCfg<D>;
-    constexpr int UNITS = C::RB / G;  // units per round
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *kv_full = bars;                     // K, V landed
-    uint64_t *st_full = bars + 1;                 // [STG] row tiles landed
-    uint64_t *qconv = bars + 1 + C::STG;          // [STG] row metadata staged
-    uint64_t *st_empty = bars + 1 + 2 * C::STG;   // [STG] round's MMAs done with the stage
-    uint64_t *s_full = bars + 1 + 3 * C::STG;     // [2] S^T, dP^T of a round complete
-    uint64_t *p_full = s_full + 2;                // [2] P^T, dS^T written
-    uint64_t *pv_done = s_full + 4;               // [2] dV, dK of a round issued and complete
-    uint64_t *acc_final = s_full + 6;             // dV, dK of the last round complete
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
-    float *meta = reinterpret_cast<float *>(smem + C::META_OFF);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt0 = blockIdx.x * C::KEYS, bh = blockIdx.y;
-    const int b = bh / p.Hkv, g = bh % p.Hkv;
-    // rounds r cover units r*UNITS .. r*UNITS+UNITS-1 of their stream
-    const int r_begin = STREAMS == 1 ? 0 : kt0 / UNITS;
-    const int base_end = static_cast<int>((min(static_cast<long long>(p.n_units),
-                                                static_cast<long long>(kt0) + C::KEYS - 1 + p.window) +
-                                            UNITS - 1) /
-                                           UNITS);
-    const DkvRounds<STREAMS> rounds{p, pc, b, kt0, UNITS, base_end};
-
-    if (threadIdx.x == 0) {
-        mbar_init(kv_full, 1);
-        for (int s = 0; s < C::STG; ++s) {
-            mbar_init(&st_full[s], 1);
-            mbar_init(&qconv[s], 2);
-            mbar_init(&st_empty[s], 1);
-        }
-        for (int u = 0; u < 2; ++u) {
-            mbar_init(&s_full[u], 1);
-            mbar_init(&p_full[u], 4);
-            mbar_init(&pv_done[u], 1);
-        }
-        mbar_init(acc_final, 1);
-        fence_barrier_init();
-    }
-    if (warp == 1)
-        tmem_alloc(tmem_holder, 512);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_holder;
-    bool ok = true;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&omap);
-            if (STREAMS == 2) {
-                tma_prefetch_desc(&qcmap);
-                tma_prefetch_desc(&ocmap);
-            }
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            mbar_arrive_expect_tx(kv_full, 2 * C::SLABS * C::KSLAB);
-#pragma unroll
-            for (int sl = 0; sl < C::SLABS; ++sl) {
-                tma_load_4d(smem + C::K_OFF + sl * C::KSLAB, &kmap, kv_full, sl * 64, g, kt0, b);
-                tma_load_4d(smem + C::V_OFF + sl * C::KSLAB, &vmap, kv_full, sl * 64, g, kt0, b);
-            }
-        }
-        int i = 0, ph = 0, r = r_begin;
-        for (bool more = rounds.seek(ph, r); more; ++r, more = rounds.seek(ph, r), ++i) {
-            const int s = i % C::STG;
-            if (i >= C::STG && !(ok = warp_wait(&st_empty[s], static_cast<uint32_t>(((i / C::STG) - 1) & 1))))
-                break;
-            if (lane == 0) {
-                uint8_t *st = smem + C::ST_OFF + s * C::ST_BYTES;
-                const CUtensorMap *qm = (STREAMS == 2 && ph == 1) ? &qcmap : &qmap;
-                const CUtensorMap *om = (STREAMS == 2 && ph == 1) ? &ocmap : &omap;
-                mbar_arrive_expect_tx(&st_full[s], 2 * C::SLABS * C::RSLAB);
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(st + C::ST_Q16 + sl * C::RSLAB, qm, &st_full[s], sl * 64, g * G, r * UNITS, b);
-                    tma_load_4d(st + C::ST_DO + sl * C::RSLAB, om, &st_full[s], sl * 64, g * G, r * UNITS, b);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = umma_idesc(128, C::RB, false, false);   // fp16
-        constexpr uint32_t IDESC_DP = umma_idesc(128, C::RB, true, false);   // bf16
-        constexpr uint32_t IDESC_DV = umma_idesc(128, D, true, true);    // bf16 P^T, dO
-        constexpr uint32_t IDESC_DK = umma_idesc(128, D, false, true);   // fp16 dS^T, q
-        const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF, 16, 1024);
-        const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF, 16, 1024);
-        // dV += P^T dO and dK += dS^T q of round j
-        auto accumulate = [&](int j) -> bool {
-            const int u = j & 1, s = j % C::STG;
-            if (!warp_wait(&p_full[u], static_cast<uint32_t>((j >> 1) & 1)))
-                return false;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
-                const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, C::RSLAB, 1024);
-                const uint64_t qdesc = umma_desc_sw128(st + C::ST_Q16, C::RSLAB, 1024);
-#pragma unroll
-                for (int kk = 0; kk < C::RB / 16; ++kk) {
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    umma_ts(tbase + C::TM_DV, tbase + C::TM_S + 64 * u + 8 * kk,
-                            odesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DV, acc);
-                    umma_ts(tbase + C::TM_DK, tbase + C::TM_DP + 64 * u + 8 * kk,
-                            qdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DK, acc);
-                }
-                umma_commit(&pv_done[u]);
-                umma_commit(&st_empty[s]);
-            }
-            __syncwarp();
-            return true;
-        };
-        ok = warp_wait(kv_full, 0);
-        int i = 0, ph = 0, r = r_begin;
-        for (bool more = rounds.seek(ph, r); ok && more; ++r, more = rounds.seek(ph, r), ++i) {
-            const int s = i % C::STG, u = i & 1;
-            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
-                break;
-            // S^T / dP^T buffer u is free once dV, dK of round i - 2 have read P^T, dS^T from it
-            if (i >= 2 && !(ok = warp_wait(&pv_done[u], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
-                break;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t st = sbase + C::ST_OFF + s * C::ST_BYTES;
-                const uint64_t qdesc = umma_desc_sw128(st + C::ST_Q16, 16, 1024);
-                const uint64_t odesc = umma_desc_sw128(st + C::ST_DO, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
-                    const uint32_t ro = static_cast<uint32_t>((kk >> 2) * C::RSLAB + (kk & 3) * 32) >> 4;
-                    umma_ss(tbase + C::TM_S + 64 * u, kdesc + ko, qdesc + ro, IDESC_S, kk != 0);
-                    umma_ss(tbase + C::TM_DP + 64 * u, vdesc + ko, odesc + ro, IDESC_DP, kk != 0);
-                }
-                umma_commit(&s_full[u]);
-            }
-            __syncwarp();
-            if (i >= 1 && !(ok = accumulate(i - 1)))
-                break;
-        }
-        if (ok && i >= 1) {
-            ok = accumulate(i - 1);
-            if (ok && lane == 0)
-                umma_commit(acc_final);
-            __syncwarp();
-        }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------------ row metadata
-        const int ct = threadIdx.x - 64;  // 0..63: one row of the round each
-        int i = 0, ph = 0, r = r_begin;
-        for (bool more = rounds.seek(ph, r); ok && more; ++r, more = rounds.seek(ph, r), ++i) {
-            const int s = i % C::STG;
-            const bool from_pc = STREAMS == 2 && ph == 1;
-            // loaded before the wait so that the latency overlaps it
-            float m_lse = 0.f, m_d = 0.f;
-            int m_pos = -1;
-            {
-                const int u = r * UNITS + ct / G, h = g * G + ct % G;
-                m_pos = round_unit_pos(p, pc, from_pc, STREAMS != 0 && (STREAMS == 1 || ph == 1), b, u);
-                if (m_pos >= 0) {
-                    const long long ri =
-                        (static_cast<long long>(b) * (from_pc ? pc.n_units : p.n_units) + u) * p.Hq + h;
-                    m_lse = (from_pc ? pc.lse : p.lse)[ri];
-                    m_d = (from_pc ? pc.Drow : p.Drow)[ri];
-                }
-            }
-            // the slot is free once the stage of this round has landed: its producer waited
-            // for the MMAs of round i - STG, which waited for that round's softmax
-            if (!(ok = warp_wait(&st_full[s], static_cast<uint32_t>((i / C::STG) & 1))))
-                break;
-            float *m = meta + s * 3 * C::RB;
-            m[ct] = m_lse;
-            m[C::RB + ct] = m_d;
-            m[2 * C::RB + ct] = __int_as_float(m_pos);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&qconv[s]);
-        }
-    } else {
-        // ------------------------------------------------------------------ P^T, dS^T + epilogue
-        const int rw = warp - 4;
-        const int key = kt0 + rw * 32 + lane;
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        const float c2 = p.scale * kLog2eF;
-        float ds_max = 0.f;  // dS^T goes to fp16: |dS| < 65504 or the range error
-        int i = 0, ph = 0, r = r_begin;
-        for (bool more = rounds.seek(ph, r); more; ++r, more = rounds.seek(ph, r), ++i) {
-            const int s = i % C::STG, u = i & 1;
-            const int window = (STREAMS == 2 && ph == 1) ? pc.window : p.window;
-            if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((i >> 1) & 1)) &&
-                       warp_wait(&qconv[s], static_cast<uint32_t>((i / C::STG) & 1))))
-                break;
-            tc_fence_after();
-            const float *m = meta + s * 3 * C::RB;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[32], dv[32];
-                tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
-                tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
-                tmem_wait_ld();
-                uint32_t pw[16], dw[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pr[2], ds[2];
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int c = 32 * half + 2 * e + q;
-                        const int P = __float_as_int(m[2 * C::RB + c]);
-                        const bool valid = key <= P && key >= P - window + 1;  // P = -1: none
-                        pr[q] = valid ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - m[c]) : 0.f;
-                        ds[q] = pr[q] * (__uint_as_float(dv[2 * e + q]) - m[C::RB + c]);
-                    }
-                    ds_max = fmaxf(ds_max, fmaxf(fabsf(ds[0]), fabsf(ds[1])));
-                    pw[e] = pack_bf16x2(pr[0], pr[1]);
-                    __half2 hv = __floats2half2_rn(ds[0], ds[1]);
-                    dw[e] = *reinterpret_cast<uint32_t *>(&hv);
-                }
-                tmem_st16(tl + C::TM_S + 64 * u + 16 * half, pw);
-                tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&p_full[u]);
-        }
-        if (!(ds_max < 65504.f))
-            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
-        // ---- epilogue: dK (scaled), dV of this key -> global (written, or added)
-        const bool have = ok && i > 0;
-        if (have && !(ok = warp_wait(acc_final, 0))) {
-        } else {
-            if (have)
-                tc_fence_after();
-            const long long off =
-                (static_cast<long long>(b) * p.T_kv + key) * p.Hkv * D + static_cast<long long>(g) * D;
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t wk[32], wv[32];
-                if (have) {
-                    tmem_ld32(tl + C::TM_DK + c, wk);
-                    tmem_ld32(tl + C::TM_DV + c, wv);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        wk[e] = wv[e] = 0u;
-                }
-                if (key < p.T_kv) {  // whole 32-byte sectors per store (rows are 32-byte aligned)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        wk[e] = __float_as_uint(__uint_as_float(wk[e]) * p.scale);
-                    float *pk = p.dk + off + c, *pv = p.dv + off + c;
-                    if (p.accumulate) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const float4 ok4 = *reinterpret_cast<const float4 *>(pk + e);
-                            const float4 ov4 = *reinterpret_cast<const float4 *>(pv + e);
-                            wk[e] = __float_as_uint(__uint_as_float(wk[e]) + ok4.x);
-                            wk[e + 1] = __float_as_uint(__uint_as_float(wk[e + 1]) + ok4.y);
-                            wk[e + 2] = __float_as_uint(__uint_as_float(wk[e + 2]) + ok4.z);
-                            wk[e + 3] = __float_as_uint(__uint_as_float(wk[e + 3]) + ok4.w);
-                            wv[e] = __float_as_uint(__uint_as_float(wv[e]) + ov4.x);
-                            wv[e + 1] = __float_as_uint(__uint_as_float(wv[e + 1]) + ov4.y);
-                            wv[e + 2] = __float_as_uint(__uint_as_float(wv[e + 2]) + ov4.z);
-                            wv[e + 3] = __float_as_uint(__uint_as_float(wv[e + 3]) + ov4.w);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        st_global_v8(pk + e, make_uint4(wk[e], wk[e + 1], wk[e + 2], wk[e + 3]),
-                                     make_uint4(wk[e + 4], wk[e + 5], wk[e + 6], wk[e + 7]));
-                        st_global_v8(pv + e, make_uint4(wv[e], wv[e + 1], wv[e + 2], wv[e + 3]),
-                                     make_uint4(wv[e + 4], wv[e + 5], wv[e + 6], wv[e + 7]));
-                    }
-                }
-            }
-        }
-    }
-    if (!ok && lane == 0)
-        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tbase, 512);
-    }
-}
-
-// ------------------------------------------------------------------ dQ on tcgen05
-
-// A CTA owns 128 query rows (128/G units x G heads of one KV head): the MMA's M side,
-// q (fp16, rounded once) and dO resident in shared memory.  The keys its rows see stream
-// through a three-stage TMA ring in blocks of 64 (K from the call's fp16 copy for S; in
-// pass 2 also K itself, bf16, for dQ, and V), twice:
-//   pass 1  S = q K^T -> per-row running max / sum (lane = row) -> log2-sum-exp, stored
-//           for the dK/dV kernel;
-//   pass 2  S = q K^T, dP = dO V^T (fp32 in tensor memory, two buffers each);
-//           dS = P (dP - D) with P = exp2(S c - lse), written over dP as bf16;
-//           dQ += dS K  (A from tensor memory, B = the key block, MN-major)
-// then dq_raw = scale dQ * alpha, and dalpha / dbeta reduced across the CTA's rows of
-// each head (shuffles, then shared memory) and added with global atomics.
-// Roles (384 threads, one CTA per SM): warp 0 TMA producer; warp 1 tensor-memory
-// allocation and MMA issue; warps 2-3 and 8-11 query preparation; warps 4-7 softmax and
-// epilogue.
-// Tensor memory: S at 64 u, dP at 128 + 64 u (buffer u), dQ at 256.
-template <int D>
-struct BqCfg {
-    static constexpr int ROWS = 128;          // query rows of a CTA (the MMA's M)
-    static constexpr int KB = 64;             // keys per block (N of S, dP)
-    static constexpr int SLABS = D / 64;
-    static constexpr int STG = 3;
-    static constexpr int QSLAB = ROWS * 128;
-    static constexpr int KSLAB = KB * 128;
-    static constexpr int Q16_OFF = 0;                         // raw x, then q as fp16
-    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;    // dO
-    static constexpr int K_OFF = DO_OFF + SLABS * QSLAB;      // [STG] K blocks (bf16)
-    static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB; // [STG] V blocks
-    static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;   // [STG] K blocks as fp16
-    static constexpr int RED_OFF = K16_OFF + STG * SLABS * KSLAB; // [2][16][D+1] dalpha, dbeta partials
-    static constexpr int RS = D + 1;                              // padded row: no bank conflicts
-    static constexpr int RANGE_OFF = RED_OFF + 2 * 16 * RS * 4;
-    static constexpr int BAR_OFF = RANGE_OFF + 16;
-    static constexpr int NBARS = 2 + 2 * STG + 3 * 2 + 1;
-    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
-    static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
-};
-
-template <int D, int G, bool COPY>
-__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                          const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                          const __grid_constant__ CUtensorMap k16map, const AttnBwdParams p)
-{
-    using C = BqCfg<D>;
-    constexpr int UNITS = C::ROWS / G;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *q_full = bars;                    // raw query and dO tiles landed
-    uint64_t *q_conv = bars + 1;                // q prepared
-    uint64_t *kv_full = bars + 2;               // [STG] key block landed
-    uint64_t *kv_empty = bars + 2 + C::STG;     // [STG] key block released
-    uint64_t *s_full = bars + 2 + 2 * C::STG;   // [2] S (and dP) of a block complete
-    uint64_t *buf_free = s_full + 2;            // [2] S / dP buffer may be overwritten
-    uint64_t *p_full = s_full + 4;              // [2] dS written (pass 2)
-    uint64_t *dq_final = s_full + 6;            // dQ complete
-    float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
-    int *krange = reinterpret_cast<int *>(smem + C::RANGE_OFF);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int u0 = blockIdx.x * UNITS, bh = blockIdx.y;
-    const int b = bh / p.Hkv, g = bh % p.Hkv;
-
-    // ---- each row's position and the CTA's key range
-    if (threadIdx.x == 0) {
-        krange[0] = 0x7fffffff;
-        krange[1] = -1;
-    }
-    int Prow = -1;
-    if (threadIdx.x < C::ROWS)
-        Prow = unit_pos<COPY>(p, b, u0 + static_cast<int>(threadIdx.x) / G);
-    if (COPY && threadIdx.x < C::ROWS && Prow < 0 && u0 + static_cast<int>(threadIdx.x) / G < p.n_units &&
-        threadIdx.x % G == 0)
-        record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
-    const int wlo = __reduce_min_sync(0xffffffffu, Prow >= 0 ? max(0, Prow - p.window + 1) : 0x7fffffff);
-    const int whi = __reduce_max_sync(0xffffffffu, Prow);
-    if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_conv, DKV_TC_CONV / 32);
-        for (int s = 0; s < C::STG; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-        }
-        for (int u = 0; u < 2; ++u) {
-            mbar_init(&s_full[u], 1);
-            mbar_init(&buf_free[u], 4);
-            mbar_init(&p_full[u], 4);
-        }
-        mbar_init(dq_final, 1);
-        fence_barrier_init();
-    }
-    for (int i = threadIdx.x; i < 2 * G * C::RS; i += DKV_TC_THREADS)
-        red[i] = 0.f;
-    if (warp == 1)
-        tmem_alloc(tmem_holder, 512);
-    tc_fence_before();
-    __syncthreads();
-    if (lane == 0 && whi >= 0) {
-        atomicMin(&krange[0], wlo);
-        atomicMax(&krange[1], whi);
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_holder;
-    int kb0 = krange[1] >= 0 ? krange[0] / C::KB : 0;
-    int nb = krange[1] >= 0 ? krange[1] / C::KB - kb0 + 1 : 0;  // key blocks
-    const int mode = p.split_mode;
-    if (mode != 0) {  // this CTA's share of the key blocks
-        const int chunk = (nb + p.splits - 1) / p.splits, z = static_cast<int>(blockIdx.z);
-        kb0 += z * chunk;
-        nb = max(0, min(chunk, nb - z * chunk));
-    }
-    // steps n = 0 .. nsteps - 1: pass 1 (log-sum-exp; skipped when it is known) over the
-    // blocks, then pass 2 over them again (none in mode 1)
-    const int n1 = (p.lse_in != nullptr || mode == 2) ? 0 : nb;
-    const int nsteps = mode == 1 ? nb : n1 + nb;
-    bool ok = true;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------ producer
-        if (lane == 0 && nb > 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&omap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            tma_prefetch_desc(&k16map);
-            mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
-#pragma unroll
-            for (int sl = 0; sl < C::SLABS; ++sl) {
-                tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
-                tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
-            }
-        }
-        for (int n = 0; n < nsteps; ++n) {
-            const bool pass2 = n >= n1;
-            const int slot = n % C::STG, kb = kb0 + (pass2 ? n - n1 : n);
-            if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
-                break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&kv_full[slot], (pass2 ? 3 : 1) * C::SLABS * C::KSLAB);
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + C::K16_OFF + (slot * C::SLABS + sl) * C::KSLAB, &k16map, &kv_full[slot], sl * 64,
-                                g, kb * C::KB, b);
-                    if (pass2) {
-                        tma_load_4d(smem + C::K_OFF + (slot * C::SLABS + sl) * C::KSLAB, &kmap, &kv_full[slot], sl * 64,
-                                    g, kb * C::KB, b);
-                        tma_load_4d(smem + C::V_OFF + (slot * C::SLABS + sl) * C::KSLAB, &vmap, &kv_full[slot],
-                                    sl * 64, g, kb * C::KB, b);
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, false, false);   // fp16
-        constexpr uint32_t IDESC_DP = umma_idesc(128, C::KB, true, false);   // bf16
-        constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
-        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q16_OFF, 16, 1024);
-        const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
-        // dQ += dS K of pass-2 block n
-        auto issue_dq = [&](int n) -> bool {
-            const int u = n & 1, slot = n % C::STG;
-            if (!warp_wait(&p_full[u], static_cast<uint32_t>(((n - n1) >> 1) & 1)))
-                return false;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, C::KSLAB, 1024);
-#pragma unroll
-                for (int kk = 0; kk < C::KB / 16; ++kk)
-                    umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + 64 * u + 8 * kk,
-                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (n > n1 || kk > 0) ? 1u : 0u);
-                // buf_free counts 4 arrivals (the four softmax warps in pass 1): here the
-                // commit completes the phase once the dQ MMAs are done, after 3 plain arrivals
-                umma_commit(&buf_free[u]);
-                mbar_arrive_cnt(&buf_free[u], 3);
-                umma_commit(&kv_empty[slot]);
-            }
-            __syncwarp();
-            return true;
-        };
-        if (nb > 0)
-            ok = warp_wait(q_full, 0) && warp_wait(q_conv, 0);
-        for (int n = 0; ok && n < nsteps; ++n) {
-            const int slot = n % C::STG, u = n & 1;
-            const bool pass2 = n >= n1;
-            if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
-                break;
-            if (n >= 2 && !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - 2) >> 1) & 1))))
-                break;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint64_t kdesc = umma_desc_sw128(sbase + C::K16_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
-                const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
-                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
-                    umma_ss(tbase + C::TM_S + 64 * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
-                    if (pass2)
-                        umma_ss(tbase + C::TM_DP + 64 * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
-                }
-                umma_commit(&s_full[u]);
-                if (!pass2)
-                    umma_commit(&kv_empty[slot]);  // pass 1 reads K only through S
-            }
-            __syncwarp();
-            if (n > n1 && !(ok = issue_dq(n - 1)))
-                break;
-        }
-        if (ok && nsteps > n1) {  // there is a pass 2: the last block's dQ
-            ok = issue_dq(nsteps - 1);
-            if (ok && lane == 0)
-                umma_commit(dq_final);
-            __syncwarp();
-        }
-    } else if (warp < 4 || warp >= 8) {
-        // ------------------------------------------------------------------ query preparation
-        const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 256 + 64;  // 0..191
-        bool bad = false;
-        if (nb > 0 && (ok = warp_wait(q_full, 0))) {
-#pragma unroll 2
-            for (int idx = ct; idx < C::ROWS * C::SLABS * 8; idx += DKV_TC_CONV) {
-                const int row = idx / (C::SLABS * 8), rem = idx % (C::SLABS * 8);
-                const int sl = rem / 8, c8 = rem % 8;
-                const int h = g * G + row % G, d0 = sl * 64 + c8 * 8;
-                uint4 *qp = reinterpret_cast<uint4 *>(smem + C::Q16_OFF + sl * C::QSLAB + sw128_offset(row, c8));
-                uint4 q16, qb;
-                scale_offset8(*qp, p.alpha + h * D, p.beta + h * D, d0, q16, qb, bad);
-                *qp = q16;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(q_conv);
-        }
-        if (bad)
-            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
-    } else {
-        // ------------------------------------------------------------------ softmax + epilogue
-        const int rw = warp - 4;
-        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
-        const int P = unit_pos<COPY>(p, b, u0 + r / G);
-        const int lo = P - p.window + 1;
-        const int uu = u0 + r / G, h = g * G + r % G;
-        const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
-        const float Drow = P >= 0 ? p.Drow[ri] : 0.f;
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        const float c2 = p.scale * kLog2eF;
-        const float NEG_INF = -__int_as_float(0x7f800000);
-        float m = NEG_INF, l = 0.f;
-        // known beforehand (log2 units): from the forward via the D kernel, or the split combine
-        float lse = ((p.lse_in != nullptr || mode == 2) && P >= 0) ? p.lse[ri] : 0.f;
-        for (int n = 0; ok && n < nsteps; ++n) {
-            const int u = n & 1;
-            const bool pass2 = n >= n1;
-            const int k0 = (kb0 + (pass2 ? n - n1 : n)) * C::KB;
-            if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
-                break;
-            tc_fence_after();
-            if (!pass2) {
-                uint32_t sa[32], sb[32];
-                tmem_ld32(tl + C::TM_S + 64 * u, sa);
-                tmem_ld32(tl + C::TM_S + 64 * u + 32, sb);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&buf_free[u]);  // this warp has read its lanes of S (4 arrivals)
-                float mb = NEG_INF;
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int ka = k0 + c, kb = k0 + 32 + c;
-                    const float va = (ka <= P && ka >= lo) ? __uint_as_float(sa[c]) * c2 : NEG_INF;
-                    const float vb = (kb <= P && kb >= lo) ? __uint_as_float(sb[c]) * c2 : NEG_INF;
-                    sa[c] = __float_as_uint(va);
-                    sb[c] = __float_as_uint(vb);
-                    mb = fmax3(mb, va, vb);
-                }
-                const float mn = fmaxf(m, mb);
-                const float z = mn == NEG_INF ? 0.f : mn;
-                float acc = 0.f;
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    acc += fast_exp2(__uint_as_float(sa[c]) - z) + fast_exp2(__uint_as_float(sb[c]) - z);
-                l = l * fast_exp2(m - z) + acc;
-                m = mn;
-                if (n == n1 - 1 && mode == 0) {
-                    lse = P >= 0 ? m + __log2f(l) : 0.f;  // every valid row holds its own key
-                    if (P >= 0)
-                        p.lse[ri] = lse;
-                }
-            } else {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32(tl + C::TM_S + 64 * u + 32 * half, sv);
-                    tmem_ld32(tl + C::TM_DP + 64 * u + 32 * half, dv);
-                    tmem_wait_ld();
-                    uint32_t dw[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float ds[2];
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int key = k0 + 32 * half + 2 * e + q;
-                            const float pr = (key <= P && key >= lo)
-                                                 ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
-                                                 : 0.f;
-                            ds[q] = pr * (__uint_as_float(dv[2 * e + q]) - Drow);
-                        }
-                        dw[e] = pack_bf16x2(ds[0], ds[1]);
-                    }
-                    tmem_st16(tl + C::TM_DP + 64 * u + 16 * half, dw);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&p_full[u]);
-            }
-        }
-        // ---- epilogue: dq_raw = scale dQ alpha; dalpha, dbeta summed over the warp's rows per head
-        if (mode == 1 && ok)  // this split's (max, sum) of every row of the tile (log2 units)
-            p.part_ml[(static_cast<long long>(bh) * p.splits + blockIdx.z) * C::ROWS + r] = make_float2(m, l);
-        const bool have = ok && nsteps > n1;  // a pass 2 ran: dQ is in tensor memory
-        const bool any_live = __any_sync(0xffffffffu, uu < p.n_units);
-        // mode 0 writes every live row (zeros without keys); mode 2 adds its split's share
-        const bool write = mode == 0 ? any_live : (mode == 2 && have && any_live);
-        if (have && !(ok = warp_wait(dq_final, 0))) {
-        } else if (write) {
-            if (have)
-                tc_fence_after();
-            const long long off = ri * D;
-            const bool live = uu < p.n_units;
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t w[32];
-                if (have) {
-                    tmem_ld32(tl + C::TM_DQ + c, w);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        w[e] = 0u;
-                }
-                float dqv[32], xv[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    dqv[e] = __uint_as_float(w[e]) * p.scale;
-                if (live && P >= 0) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        const uint4 x4 = *reinterpret_cast<const uint4 *>(p.q + off + c + e);
-                        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 f = unpack_bf16x2(xw[q]);
-                            xv[e + 2 * q] = f.x;
-                            xv[e + 2 * q + 1] = f.y;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        xv[e] = 0.f;
-                }
-                if (live) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 al = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
-                        const float4 y =
-                            make_float4(dqv[e] * al.x, dqv[e + 1] * al.y, dqv[e + 2] * al.z, dqv[e + 3] * al.w);
-                        float *dst = p.dq + off + c + e;
-                        if (mode == 2) {  // dq_raw is linear in dQ: the splits add up (dq zeroed first)
-                            atomicAdd(dst, y.x);
-                            atomicAdd(dst + 1, y.y);
-                            atomicAdd(dst + 2, y.z);
-                            atomicAdd(dst + 3, y.w);
-                        } else {
-                            *reinterpret_cast<float4 *>(dst) = y;
-                        }
-                    }
-                }
-                // rows of one head are the lanes congruent mod G: butterfly over the other bits
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float sa = xv[e] * dqv[e], sb = dqv[e];
-#pragma unroll
-                    for (int o = G; o < 32; o <<= 1) {
-                        sa += __shfl_xor_sync(0xffffffffu, sa, o);
-                        sb += __shfl_xor_sync(0xffffffffu, sb, o);
-                    }
-                    if (lane < G) {
-                        atomicAdd(&red[lane * C::RS + c + e], sa);
-                        atomicAdd(&red[(G + lane) * C::RS + c + e], sb);
-                    }
-                }
-            }
-        }
-        named_barrier(1, 128);  // every softmax warp reaches this point (all waits are bounded)
-        for (int i = r; i < G * D; i += 128) {
-            const int hh = i / D, dd = i % D;
-            atomicAdd(p.dalpha + g * G * D + i, red[hh * C::RS + dd]);
-            atomicAdd(p.dbeta + g * G * D + i, red[(G + hh) * C::RS + dd]);
-        }
-    }
-    if (!ok && lane == 0)
-        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tbase, 512);
-    }
-}
-
-// ------------------------------------------------------------------ base-stream dQ, persistent
-
-// The base stream's rows see at most w + 128/G keys (two to four 64-key blocks per tile of
-// 128 rows), so a CTA per tile would spend most of its time on set-up, loads and the
-// epilogue.  Here one CTA per SM walks a contiguous run of row tiles with the forward's
-// log-sum-exp given (pass 2 only), and overlaps them: two dQ accumulators in tensor memory
-// let the epilogue of tile i run while tile i + 1's MMAs do, and tile i + 1's q / dO load
-// lands in the other of two query buffers while tile i computes.  Per key block (64 keys,
-// through a two-stage ring, so that the two query buffers fit in shared memory beside it)
-// as in the dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as
-// bf16, dQ += dS K.
-// The query tile arrives as fp16 q = x alpha + beta, made for the whole tensor beforehand
-// (attn_bwd_q16_kernel), and dalpha / dbeta are summed afterwards from dq_raw
-// (attn_bwd_dab_kernel): both were measured to pace this kernel when done per tile here
-// (q preparation 7.8 us and the per-head butterfly 14.6 us of a 21 us tile).
-// Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
-// warps 4-7 dS (lane = row); warps 8-11 the epilogue (lane = row: the same tensor-memory
-// lanes), so that one tile's epilogue runs beside the next tile's dS; warps 2-3 idle.
-// Tensor memory: S at 64 u, dP at 128 + 64 u (block buffer u of 2), dQ at 256 + D t (tile
-// buffer t).
-template <int D>
-struct BpCfg {
-    static constexpr int ROWS = 128;
-    static constexpr int KB = 64;
-    static constexpr int SLABS = D / 64;
-    static constexpr int STG = 2;
-    static constexpr int QSLAB = ROWS * 128;
-    static constexpr int KSLAB = KB * 128;
-    static constexpr int QBUF = 2 * SLABS * QSLAB;                 // one query buffer: q, dO
-    static constexpr int Q16_OFF = 0;                              // [2] q as fp16
-    static constexpr int DO_OFF = Q16_OFF + SLABS * QSLAB;         // [2] dO (QBUF apart)
-    static constexpr int K_OFF = 2 * QBUF;                         // [STG] K blocks (bf16)
-    static constexpr int V_OFF = K_OFF + STG * SLABS * KSLAB;      // [STG] V blocks
-    static constexpr int K16_OFF = V_OFF + STG * SLABS * KSLAB;    // [STG] K blocks as fp16
-    static constexpr int BAR_OFF = K16_OFF + STG * SLABS * KSLAB;
-    static constexpr int NBUF = 2;                                 // S / dP buffers
-    static constexpr int NBARS = 2 * 2 + 2 * STG + 3 * NBUF + 2 * 2;
-    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
-    static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0, TM_DP = NBUF * KB, TM_DQ = 2 * NBUF * KB;
-};
-
-template <int D, int G>
-__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
-    attn_bwd_dq_tc_base_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                               const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                               const __grid_constant__ CUtensorMap k16map, const AttnBwdParams p)
-{
-    using C = BpCfg<D>;
-    constexpr int UNITS = C::ROWS / G;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *q_full = bars;                     // [2] a tile's fp16 q and dO landed
-    uint64_t *q_free = bars + 2;                 // [2] a tile's last S, dP done: the buffer may be reloaded
-    uint64_t *kv_full = bars + 4;                // [STG] key block landed
-    uint64_t *kv_empty = kv_full + C::STG;       // [STG] key block released
-    uint64_t *s_full = kv_empty + C::STG;        // [NBUF] S, dP of a block complete
-    uint64_t *buf_free = s_full + C::NBUF;       // [NBUF] S / dP buffer may be overwritten
-    uint64_t *p_full = buf_free + C::NBUF;       // [NBUF] dS written
-    uint64_t *dq_final = p_full + C::NBUF;       // [2] a tile's dQ complete
-    uint64_t *dq_free = dq_final + 2;            // [2] a tile's dQ read by the epilogue
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // this CTA's tiles: a contiguous run of (batch, KV head, 128-row tile) in that order
-    const int n_xt = (p.n_units + UNITS - 1) / UNITS;
-    const long long n_tiles = static_cast<long long>(p.B) * p.Hkv * n_xt;
-    const long long per = (n_tiles + gridDim.x - 1) / gridDim.x;
-    const long long t_begin = blockIdx.x * per, t_end = min(n_tiles, t_begin + per);
-    // tile tau: sequence b, KV head g, first unit u0, key blocks kb0 .. kb0 + nb - 1
-    auto tile = [&](long long tau, int &b, int &g, int &u0, int &kb0, int &nb) {
-        const int bh = static_cast<int>(tau / n_xt);
-        b = bh / p.Hkv;
-        g = bh % p.Hkv;
-        u0 = static_cast<int>(tau % n_xt) * UNITS;
-        const int klo = max(0, u0 - p.window + 1), khi = min(p.n_units, u0 + UNITS) - 1;
-        kb0 = klo / C::KB;
-        nb = khi / C::KB - kb0 + 1;
-    };
-
-    if (threadIdx.x == 0) {
-        for (int qb = 0; qb < 2; ++qb) {
-            mbar_init(&q_full[qb], 1);
-            mbar_init(&q_free[qb], 1);
-        }
-        for (int s = 0; s < C::STG; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-        }
-        for (int u = 0; u < C::NBUF; ++u) {
-            mbar_init(&s_full[u], 1);
-            mbar_init(&buf_free[u], 1);
-            mbar_init(&p_full[u], 4);
-        }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&dq_final[t], 1);
-            mbar_init(&dq_free[t], 4);
-        }
-        fence_barrier_init();
-    }
-    if (warp == 1)
-        tmem_alloc(tmem_holder, 512);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_holder;
-    bool ok = true;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&omap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            tma_prefetch_desc(&k16map);
-        }
-        long long n = 0;  // key blocks issued so far, over all tiles
-        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            int b, g, u0, kb0, nb;
-            tile(tau, b, g, u0, kb0, nb);
-            const int qb = static_cast<int>(i & 1);
-            // query buffer qb is free once tile i - 2's last S, dP products are done
-            if (i >= 2 && !(ok = warp_wait(&q_free[qb], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
-                break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&q_full[qb], 2 * C::SLABS * C::QSLAB);
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB, &qmap, &q_full[qb], sl * 64, g * G,
-                                u0, b);
-                    tma_load_4d(smem + qb * C::QBUF + C::DO_OFF + sl * C::QSLAB, &omap, &q_full[qb], sl * 64, g * G,
-                                u0, b);
-                }
-            }
-            for (int j = 0; j < nb; ++j, ++n) {
-                const int slot = static_cast<int>(n % C::STG);
-                if (n >= C::STG && !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::STG) - 1) & 1))))
-                    break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&kv_full[slot], 3 * C::SLABS * C::KSLAB);
-                    const int key0 = (kb0 + j) * C::KB;
-#pragma unroll
-                    for (int sl = 0; sl < C::SLABS; ++sl) {
-                        const int o = (slot * C::SLABS + sl) * C::KSLAB;
-                        tma_load_4d(smem + C::K16_OFF + o, &k16map, &kv_full[slot], sl * 64, g, key0, b);
-                        tma_load_4d(smem + C::K_OFF + o, &kmap, &kv_full[slot], sl * 64, g, key0, b);
-                        tma_load_4d(smem + C::V_OFF + o, &vmap, &kv_full[slot], sl * 64, g, key0, b);
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = umma_idesc(128, C::KB, false, false);  // fp16
-        constexpr uint32_t IDESC_DP = umma_idesc(128, C::KB, true, false);  // bf16
-        constexpr uint32_t IDESC_DQ = umma_idesc(128, D, true, true);
-        // dQ[t] (+)= dS K of block m
-        auto issue_dq = [&](long long m, bool first, int t) -> bool {
-            const int u = static_cast<int>(m % C::NBUF), slot = static_cast<int>(m % C::STG);
-            if (!warp_wait(&p_full[u], static_cast<uint32_t>((m / C::NBUF) & 1)))
-                return false;
-            if (lane == 0) {
-                tc_fence_after();
-                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + slot * C::SLABS * C::KSLAB, C::KSLAB, 1024);
-#pragma unroll
-                for (int kk = 0; kk < C::KB / 16; ++kk)
-                    umma_ts(tbase + C::TM_DQ + D * t, tbase + C::TM_DP + C::KB * u + 8 * kk,
-                            kdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_DQ, (!first || kk > 0) ? 1u : 0u);
-                umma_commit(&buf_free[u]);
-                umma_commit(&kv_empty[slot]);
-            }
-            __syncwarp();
-            return true;
-        };
-        long long n = 0;
-        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            int b, g, u0, kb0, nb;
-            tile(tau, b, g, u0, kb0, nb);
-            const int t = static_cast<int>(i & 1), qb = t;
-            const uint32_t qph = static_cast<uint32_t>((i >> 1) & 1);
-            if (!(ok = warp_wait(&q_full[qb], qph)))
-                break;
-            const uint64_t qdesc = umma_desc_sw128(sbase + qb * C::QBUF + C::Q16_OFF, 16, 1024);
-            const uint64_t odesc = umma_desc_sw128(sbase + qb * C::QBUF + C::DO_OFF, 16, 1024);
-            // dQ[t] is free once the epilogue of tile i - 2 has read it
-            if (i >= 2 && !(ok = warp_wait(&dq_free[t], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
-                break;
-            for (int j = 0; j < nb; ++j, ++n) {
-                const int slot = static_cast<int>(n % C::STG), u = static_cast<int>(n % C::NBUF);
-                if (!(ok = warp_wait(&kv_full[slot], static_cast<uint32_t>((n / C::STG) & 1))))
-                    break;
-                // S / dP buffer u is free once the dQ product of block n - NBUF has read dS
-                if (n >= C::NBUF &&
-                    !(ok = warp_wait(&buf_free[u], static_cast<uint32_t>(((n - C::NBUF) / C::NBUF) & 1))))
-                    break;
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint64_t kdesc = umma_desc_sw128(sbase + C::K16_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
-                    const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + slot * C::SLABS * C::KSLAB, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
-                        const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::KSLAB + (kk & 3) * 32) >> 4;
-                        umma_ss(tbase + C::TM_S + C::KB * u, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
-                        umma_ss(tbase + C::TM_DP + C::KB * u, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
-                    }
-                    umma_commit(&s_full[u]);
-                    if (j == nb - 1)
-                        umma_commit(&q_free[qb]);  // the tile's q and dO are no longer read
-                }
-                __syncwarp();
-                if (j >= 1 && !(ok = issue_dq(n - 1, j == 1, t)))
-                    break;
-            }
-            if (!ok)
-                break;
-            if (!(ok = issue_dq(n - 1, nb == 1, t)))
-                break;
-            if (lane == 0)
-                umma_commit(&dq_final[t]);
-            __syncwarp();
-        }
-    } else if (warp < 4) {
-        // warps 2-3: no role (the query tile arrives prepared)
-    } else if (warp < 8) {
-        // ------------------------------------------------------------------ dS (lane = row)
-        const int rw = warp - 4;
-        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        const float c2 = p.scale * kLog2eF;
-        long long n = 0;
-        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            int b, g, u0, kb0, nb;
-            tile(tau, b, g, u0, kb0, nb);
-            const int uu = u0 + r / G, h = g * G + r % G;
-            const bool live = uu < p.n_units;
-            const int P = live ? uu : -1, lo = P - p.window + 1;
-            const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
-            const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the D kernel converted it)
-            const float Drow = live ? p.Drow[ri] : 0.f;
-            for (int j = 0; j < nb; ++j, ++n) {
-                const int u = static_cast<int>(n % C::NBUF);
-                if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n / C::NBUF) & 1))))
-                    break;
-                tc_fence_after();
-                const int k0 = (kb0 + j) * C::KB;
-#pragma unroll
-                for (int half = 0; half < C::KB / 32; ++half) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32(tl + C::TM_S + C::KB * u + 32 * half, sv);
-                    tmem_ld32(tl + C::TM_DP + C::KB * u + 32 * half, dv);
-                    tmem_wait_ld();
-                    uint32_t dw[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float ds[2];
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int key = k0 + 32 * half + 2 * e + q;
-                            const float pr = (key <= P && key >= lo)
-                                                 ? fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse)
-                                                 : 0.f;
-                            ds[q] = pr * (__uint_as_float(dv[2 * e + q]) - Drow);
-                        }
-                        dw[e] = pack_bf16x2(ds[0], ds[1]);
-                    }
-                    tmem_st16(tl + C::TM_DP + C::KB * u + 16 * half, dw);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&p_full[u]);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------------ epilogue (warps 8-11)
-        // dq_raw = scale dQ alpha (dalpha, dbeta follow from it in attn_bwd_dab_kernel)
-        const int rw = warp - 8;
-        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
-        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            int b, g, u0, kb0, nb;
-            tile(tau, b, g, u0, kb0, nb);
-            const int t = static_cast<int>(i & 1);
-            const int uu = u0 + r / G, h = g * G + r % G;
-            const bool live = uu < p.n_units;
-            const long long off = ((static_cast<long long>(b) * p.n_units + uu) * p.Hq + h) * D;
-            if (!(ok = warp_wait(&dq_final[t], static_cast<uint32_t>((i >> 1) & 1))))
-                break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t w[32];
-                tmem_ld32(tl + C::TM_DQ + D * t + c, w);
-                tmem_wait_ld();
-                if (live) {  // dq_raw = scale dQ alpha, whole 32-byte sectors per store
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
-                        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e + 4));
-                        const float sc = p.scale;
-                        st_global_v8(p.dq + off + c + e,
-                                     make_uint4(__float_as_uint(__uint_as_float(w[e]) * sc * a0.x),
-                                                __float_as_uint(__uint_as_float(w[e + 1]) * sc * a0.y),
-                                                __float_as_uint(__uint_as_float(w[e + 2]) * sc * a0.z),
-                                                __float_as_uint(__uint_as_float(w[e + 3]) * sc * a0.w)),
-                                     make_uint4(__float_as_uint(__uint_as_float(w[e + 4]) * sc * a1.x),
-                                                __float_as_uint(__uint_as_float(w[e + 5]) * sc * a1.y),
-                                                __float_as_uint(__uint_as_float(w[e + 6]) * sc * a1.z),
-                                                __float_as_uint(__uint_as_float(w[e + 7]) * sc * a1.w)));
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&dq_free[t]);  // this warp's lanes of dQ[t] are read
-        }
-    }
-    if (!ok && lane == 0)
-        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tbase, 512);
-    }
-}
-
-// ------------------------------------------------------------------ split log-sum-exp
-
-// rows of the single row tile of each (batch, KV head): merge the splits' (max, sum) into
-// the row's log2-sum-exp
-template <int G>
-__global__ void __launch_bounds__(128) attn_bwd_lse_combine_kernel(const AttnBwdParams p)
-{
-    const int bh = blockIdx.x, r = threadIdx.x;
-    const int b = bh / p.Hkv, g = bh % p.Hkv;
-    const int u = r / G, h = g * G + r % G;
-    if (unit_pos<true>(p, b, u) < 0)
-        return;
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    const float2 *part = p.part_ml + static_cast<long long>(bh) * p.splits * 128 + r;
-    float M = NEG_INF;
-    for (int z = 0; z < p.splits; ++z)
-        M = fmaxf(M, part[z * 128].x);
-    float L = 0.f;
-    for (int z = 0; z < p.splits; ++z) {
-        const float2 ml = part[z * 128];
-        if (ml.x != NEG_INF)
-            L += ml.y * exp2f(ml.x - M);
-    }
-    p.lse[(static_cast<long long>(b) * p.n_units + u) * p.Hq + h] = M + __log2f(L);  // the row holds its own key
-}
-
-// ------------------------------------------------------------------ host side
+cudaError_t attn_bwd_launch_d128(int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
+cudaError_t attn_bwd_launch_d64(int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
+cudaError_t attn_bwd_layer_d128(int G, const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
+                               const CUtensorMap *mapsc, cudaStream_t stream);
+cudaError_t attn_bwd_layer_d64(int G, const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
+                              const CUtensorMap *mapsc, cudaStream_t stream);
 
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
 {
@@ -1759,214 +29,22 @@ size_t attn_bwd_k16_offset(int B, int n_units, int Hq)
     return (8 * static_cast<size_t>(B) * n_units * Hq + 255) & ~static_cast<size_t>(255);
 }
 
-static size_t dq_smem(int D, int G)
-{
-    return static_cast<size_t>(4) * (D / 64) * BWD_KEYS * 128 + 2 * G * D * 4 + 16 + 1024;
-}
-
-// One stream's launches before dK/dV: zeroed dalpha / dbeta, the fp16 copy of K (unless another
-// stream's call already made it), the fp16 scale-offset q, D (and the forward's log-sum-exp in
-// log2 units), then dq (and, after the persistent base kernel, the dalpha / dbeta sums).
-template <int D, int G, bool COPY>
-static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps, bool make_k16, cudaStream_t stream)
-{
-    const long long rows = static_cast<long long>(p.B) * p.n_units * p.Hq;
-    cudaError_t e = cudaMemsetAsync(p.dalpha, 0, sizeof(float) * p.Hq * D, stream);
-    if (e == cudaSuccess)
-        e = cudaMemsetAsync(p.dbeta, 0, sizeof(float) * p.Hq * D, stream);
-    if (e != cudaSuccess)
-        return e;
-    if (make_k16) {
-        const long long n8 = static_cast<long long>(p.B) * p.T_kv * p.Hkv * D / 8;
-        attn_bwd_k16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(p.k, p.k16, n8,
-                                                                                                  p.dev_err);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-    }
-    // the fp16 scale-offset q: read by the dK/dV kernel and the base stream's persistent dQ
-    const bool persistent = !COPY && p.lse_in != nullptr;  // base dq on tensor memory
-    if (rows > 0) {
-        const long long n8 = rows * D / 8;
-        attn_bwd_q16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(
-            p.q, p.alpha, p.beta, p.q16, n8, p.Hq * D / 8, p.dev_err);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-    }
-    if (rows > 0) {
-        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
-            p.o, p.dO, p.Drow, p.lse_in, p.lse, rows);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-        // base rows see at most window + 128/G keys: a tensor-memory CTA (one per SM) spends
-        // most of its time filling and draining its pipeline, and the warp-MMA kernel is
-        // faster there (whole base gradient of a 2 x 128K-token, 32/8-head, w = 128 layer:
-        // 21.6 vs 23.5 ms with the forward's log-sum-exp, 23.4 vs 24.5 ms without); copies
-        // see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
-        if (COPY) {
-            const size_t s1 = BqCfg<D>::SMEM;
-            auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
-            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
-                cudaSuccess)
-                return e;
-            constexpr int UNITS = BqCfg<D>::ROWS / G;
-            dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-            // few copies (one row tile per batch and KV head) over many keys: split the keys
-            // so that the grid fills the GPU (two CTAs' worth per SM); with the forward's
-            // log-sum-exp only the second pass runs
-            int splits = 1;
-            if (p.n_units <= UNITS && (p.lse_in != nullptr || p.part_ml != nullptr)) {
-                int dev = 0, sms = 0;
-                if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-                    (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-                    return e;
-                const int nbk = (p.T_kv + BqCfg<D>::KB - 1) / BqCfg<D>::KB;
-                splits = min(min(ATTN_BWD_MAX_SPLITS, 2 * sms / (p.B * p.Hkv)), nbk / 8);
-            }
-            if (splits >= 2) {
-                if ((e = cudaMemsetAsync(p.dq, 0, sizeof(float) * rows * D, stream)) != cudaSuccess)
-                    return e;
-                AttnBwdParams ps = p;
-                ps.splits = splits;
-                dim3 gs(1, p.B * p.Hkv, splits);
-                if (p.lse_in == nullptr) {  // per-split (max, sum), merged into the log-sum-exp
-                    ps.split_mode = 1;
-                    k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
-                    if ((e = cudaGetLastError()) != cudaSuccess)
-                        return e;
-                    attn_bwd_lse_combine_kernel<G><<<p.B * p.Hkv, 128, 0, stream>>>(ps);
-                    if ((e = cudaGetLastError()) != cudaSuccess)
-                        return e;
-                }
-                ps.split_mode = 2;
-                k1<<<gs, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], ps);
-            } else {
-                k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], p);
-            }
-        } else if (persistent) {
-            // base stream with the forward's log-sum-exp: the persistent tensor-memory kernel
-            const size_t s1 = BpCfg<D>::SMEM;
-            auto k1 = attn_bwd_dq_tc_base_kernel<D, G>;
-            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
-                cudaSuccess)
-                return e;
-            int dev = 0, sms = 0;
-            if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-                return e;
-            constexpr int UNITS = BpCfg<D>::ROWS / G;
-            const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
-            k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
-                maps[9], maps[5], maps[6], maps[7], maps[8], p);
-            if ((e = cudaGetLastError()) != cudaSuccess)
-                return e;
-            // dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]:
-            // 4 columns per thread, runs of token rows per CTA
-            const long long trows = static_cast<long long>(p.B) * p.n_units;
-            const int cols = p.Hq * D;
-            const unsigned gx = static_cast<unsigned>((cols / 4 + 255) / 256);
-            const long long gy_t = (2LL * sms * 4 + gx - 1) / gx, gy = trows < gy_t ? trows : gy_t;
-            const int per = static_cast<int>((trows + gy - 1) / gy);
-            attn_bwd_dab_kernel<<<dim3(gx, static_cast<unsigned>((trows + per - 1) / per)), 256, 0, stream>>>(
-                p.dq, p.q, p.alpha, p.dalpha, p.dbeta, trows, cols, per);
-        } else {
-            const size_t s1 = dq_smem(D, G);
-            auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
-            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=
-                cudaSuccess)
-                return e;
-            constexpr int UNITS = BWD_ROWS / G;
-            dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
-            k1<<<g1, 128, s1, stream>>>(p);
-        }
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-    }
-    return cudaSuccess;
-}
-
-// dK / dV of the rows of p (STREAMS 0: base, 1: copies) or of both streams (STREAMS 2: p base,
-// pc copies).  Also runs without query rows: it writes (or keeps) zeros.
-template <int D, int G, int STREAMS>
-static cudaError_t launch_dkv_t(const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
-                                const CUtensorMap *mapsc, cudaStream_t stream)
-{
-    const size_t s3 = BtCfg<D>::SMEM;
-    auto k3 = attn_bwd_dkv_tc_kernel<D, G, STREAMS>;
-    cudaError_t e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s3));
-    if (e != cudaSuccess)
-        return e;
-    dim3 g3((p.T_kv + BtCfg<D>::KEYS - 1) / BtCfg<D>::KEYS, p.B * p.Hkv);
-    k3<<<g3, DKV_THREADS, s3, stream>>>(maps[0], maps[1], mapsc[0], mapsc[1], maps[3], maps[2], p, pc);
-    return cudaGetLastError();
-}
-
-template <int D, int G, bool COPY>
-static cudaError_t launch_attn_bwd_t(const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
-{
-    const cudaError_t e = launch_rows_t<D, G, COPY>(p, maps, true, stream);
-    if (e != cudaSuccess)
-        return e;
-    return launch_dkv_t<D, G, COPY ? 1 : 0>(p, p, maps, maps, stream);
-}
-
-// both streams of a layer: the copies reuse the base stream's fp16 K, and one dK/dV launch
-// takes the base rows and then the copies' rows of each key block
-template <int D, int G>
-static cudaError_t launch_layer_bwd_t(const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
-                                      const CUtensorMap *mapsc, cudaStream_t stream)
-{
-    cudaError_t e = launch_rows_t<D, G, false>(p, maps, true, stream);
-    if (e == cudaSuccess)
-        e = launch_rows_t<D, G, true>(pc, mapsc, false, stream);
-    if (e != cudaSuccess)
-        return e;
-    return pc.n_units > 0 ? launch_dkv_t<D, G, 2>(p, pc, maps, mapsc, stream)
-                          : launch_dkv_t<D, G, 0>(p, p, maps, maps, stream);
-}
-
-template <bool COPY>
-static cudaError_t dispatch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps,
-                                     cudaStream_t stream)
-{
-#define ORTHROS_BWD_CASE(DD, GG) \
-    if (D == DD && G == GG)      \
-        return launch_attn_bwd_t<DD, GG, COPY>(p, maps, stream);
-    ORTHROS_BWD_CASE(128, 1)
-    ORTHROS_BWD_CASE(128, 2)
-    ORTHROS_BWD_CASE(128, 4)
-    ORTHROS_BWD_CASE(128, 8)
-    ORTHROS_BWD_CASE(128, 16)
-    ORTHROS_BWD_CASE(64, 1)
-    ORTHROS_BWD_CASE(64, 2)
-    ORTHROS_BWD_CASE(64, 4)
-    ORTHROS_BWD_CASE(64, 8)
-    ORTHROS_BWD_CASE(64, 16)
-#undef ORTHROS_BWD_CASE
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream)
 {
-    return p.pos ? dispatch_attn_bwd<true>(D, G, p, maps, stream) : dispatch_attn_bwd<false>(D, G, p, maps, stream);
+    if (D == 128)
+        return attn_bwd_launch_d128(G, p, maps, stream);
+    if (D == 64)
+        return attn_bwd_launch_d64(G, p, maps, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_bwd_layer(int D, int G, const AttnBwdParams &p, const AttnBwdParams &pc,
                                   const CUtensorMap *maps, const CUtensorMap *mapsc, cudaStream_t stream)
 {
-#define ORTHROS_BWD_CASE(DD, GG) \
-    if (D == DD && G == GG)      \
-        return launch_layer_bwd_t<DD, GG>(p, pc, maps, mapsc, stream);
-    ORTHROS_BWD_CASE(128, 1)
-    ORTHROS_BWD_CASE(128, 2)
-    ORTHROS_BWD_CASE(128, 4)
-    ORTHROS_BWD_CASE(128, 8)
-    ORTHROS_BWD_CASE(128, 16)
-    ORTHROS_BWD_CASE(64, 1)
-    ORTHROS_BWD_CASE(64, 2)
-    ORTHROS_BWD_CASE(64, 4)
-    ORTHROS_BWD_CASE(64, 8)
-    ORTHROS_BWD_CASE(64, 16)
-#undef ORTHROS_BWD_CASE
+    if (D == 128)
+        return attn_bwd_layer_d128(G, p, pc, maps, mapsc, stream);
+    if (D == 64)
+        return attn_bwd_layer_d64(G, p, pc, maps, mapsc, stream);
     return cudaErrorInvalidValue;
 }
 
