@@ -169,3 +169,41 @@ def test_attn_bwd_workspace_size_and_checks(L):
     assert call(Hkv=5) == 2
     assert call(ws=None) == 3
     assert call(nbytes=n - 4) == 3
+
+
+def test_a_c99_program_links_and_calls_the_library(tmp_path):
+    """The boundary as a C caller sees it: the header compiles as strict C99, a program links
+    against the shared library and calls its host-only entry points (version, status strings,
+    workspace sizes), whose values agree with those seen through the binding."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    import long_context_attention_orthros_gb300 as orth
+    libpath = orth.library_path
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "orthros.h"
+int main(void)
+{
+    printf("%d\n", orthros_version());
+    printf("%s\n", orthros_status_string(ORTHROS_ERR_WORKSPACE));
+    printf("%zu\n", orthros_attn_bwd_workspace_size(2, 1000, 64, 32, 8, 128));
+    printf("%zu\n", orthros_xattn_workspace_size(2, 1, 131072, 32, 8, 128));
+    printf("%zu\n", orthros_decode_workspace_size(2, 131200, 32, 8, 128));
+    return orthros_swa_bwd_workspace_size(0, 1, 1, 1, 64) == 0 ? 0 : 1;
+}
+""")
+    exe = tmp_path / "caller"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    libdir = os.path.dirname(libpath)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", f"-I{inc}", str(src), "-o", str(exe),
+                    f"-L{libdir}", "-l:" + os.path.basename(libpath), f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    assert int(out[0]) > 0
+    assert out[1] == "workspace missing or too small"
+    assert int(out[2]) == orth.attn_bwd_workspace_size(2, 1000, 64, 32, 8, 128)
+    assert int(out[3]) == orth.xattn_workspace_size(2, 1, 131072, 32, 8, 128)
+    assert int(out[4]) == orth.decode_workspace_size(2, 131200, 32, 8, 128)
