@@ -129,7 +129,10 @@ orthros_status orthros_swa_fwd_lse(const orthros_bf16 *q_raw, const orthros_bf16
 
 /*
  * Bytes of device workspace orthros_xattn_fwd needs for these sizes
- * (split-KV partial results).  Returns 0 for invalid sizes.
+ * (split-KV partial results).  Many copies per KV head (T_out * Hq/Hkv >= 256)
+ * run on a kernel that keeps no partials, and few copies whose rows all fit one
+ * partial need none: both get the 256-byte minimum.  Returns 0 for invalid
+ * sizes.
  */
 size_t orthros_xattn_workspace_size(int B, int T_out, int T_kv, int Hq, int Hkv, int d);
 
@@ -219,7 +222,8 @@ orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16
  * that must never call cudaMalloc, which can block on the device and fail once
  * memory is fragmented or capped.
  *
- * Same arguments, layouts and results as orthros_xattn_fwd.  The split-KV
+ * Same arguments, layouts, results and status codes as orthros_xattn_fwd
+ * (bits identical for the same inputs: the same kernels run).  The split-KV
  * partials live in a fixed file-scope device array of
  * ORTHROS_XATTN_NOALLOC_MAX_BYTES that every GPU loading this library holds
  * until the process exits; nothing is allocated per call.  Sizes for which

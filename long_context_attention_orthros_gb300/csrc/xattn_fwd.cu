@@ -337,6 +337,9 @@ XattnPlan xattn_plan(int B, int T_out, int T_kv, int Hq, int Hkv)
 
 size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D)
 {
+    // many copies run on the tensor-memory kernel, which keeps no partials
+    if (xattn_tc_supported(D, Hq / Hkv, T_out))
+        return 256;
     const XattnPlan pl = xattn_plan(B, T_out, T_kv, Hq, Hkv);
     if (pl.direct)
         return 256;

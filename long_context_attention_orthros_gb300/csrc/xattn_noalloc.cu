@@ -60,8 +60,9 @@ extern "C" orthros_status orthros_xattn_fwd_noalloc(const orthros_bf16 *qc_raw, 
                                                     int64_t oc_bstride, int32_t *dev_err, void *stream)
 {
     const size_t need = orthros_xattn_workspace_size(B, T_out, T_kv, Hq, Hkv, d);
-    if (need == 0)
-        return ORTHROS_ERR_INVALID_ARG;
+    if (need == 0)  // sizes, head dimension or grouping refused: the same status orthros_xattn_fwd gives
+        return orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T_kv, Hq, Hkv, d, scale,
+                                 qc_bstride, kv_bstride, oc_bstride, nullptr, 0, dev_err, stream);
     if (need > ORTHROS_XATTN_NOALLOC_MAX_BYTES)
         return ORTHROS_ERR_WORKSPACE;  // these sizes need more scratch than the fixed array holds
     void *scratch = scratch_on_current_device();

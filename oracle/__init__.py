@@ -47,6 +47,8 @@ def _load():
             I = ctypes.c_int
             D = ctypes.c_double
             lib.oracle_num_threads.restype = I
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_set_num_threads.restype = None
             lib.oracle_swa.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D]
             lib.oracle_swa_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D, P, P, I]
             lib.oracle_xattn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, D]
@@ -65,6 +67,12 @@ def _load():
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls from this thread (timing only; the values do not depend
+    on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _c(a, dtype):

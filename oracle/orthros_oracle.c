@@ -58,6 +58,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads of the calling thread's later parallel regions (timing only; no effect on values). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* q[e] = bf16(q_raw[e]) * alpha[e] + beta[e]  (the stream's scale-offset) */
 static void scale_offset_row(const uint16_t *q_raw, const float *alpha, const float *beta,
                              int d, double *q)

@@ -138,6 +138,8 @@ CONFIGS = {
     "tiny_prefill": PrefillConfig("tiny_prefill", B=1, T=512, Hq=2, Hkv=1, d=64),
     "prefill_128k": PrefillConfig("prefill_128k", B=2, T=131072, Hq=32, Hkv=8, d=128),
     "decode_128k": DecodeConfig("decode_128k", B=2, T0=131072, steps=128, Hq=32, Hkv=8, d=128),
+    # the same layer and cache length at batch 8 (decode's batch dependence)
+    "decode_128k_b8": DecodeConfig("decode_128k_b8", B=8, T0=131072, steps=32, Hq=32, Hkv=8, d=128),
     "sft_16k": PrefillConfig("sft_16k", B=4, T=16384, Hq=32, Hkv=8, d=128, T_out=2048,
                              appended=True, positions="shuffled"),
     "prefill_1m": PrefillConfig("prefill_1m", B=1, T=1048576, Hq=32, Hkv=8, d=128,
@@ -150,7 +152,7 @@ CONFIGS = {
 }
 
 SEEDS = {"tiny_prefill": 1, "prefill_128k": 2, "decode_128k": 3, "sft_16k": 4, "prefill_1m": 5,
-         "prefill_16k": 6, "sft_16k_1": 7}
+         "prefill_16k": 6, "sft_16k_1": 7, "decode_128k_b8": 8}
 
 
 @dataclass

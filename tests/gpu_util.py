@@ -52,3 +52,29 @@ def assert_parity(got: np.ndarray, ref: np.ndarray, what: str = "") -> None:
     mx, mn = float(d.max()), float(d.mean())
     assert excess <= MAX_ABS and mn <= MEAN_ABS, (
         f"{what}: max|err| {mx:.3e} (beyond bf16 output rounding {excess:.3e}) mean|err| {mn:.3e}")
+
+
+class ParityAccumulator:
+    """assert_parity over an output compared in chunks: the max bar on the largest excess over
+    all chunks, the mean bar on the mean over every element."""
+
+    def __init__(self, what: str = ""):
+        self.what, self.excess, self.mx, self.total, self.n = what, -np.inf, 0.0, 0.0, 0
+
+    def add(self, got: np.ndarray, ref: np.ndarray) -> None:
+        assert got.shape == ref.shape, (got.shape, ref.shape)
+        assert np.isfinite(got).all(), f"{self.what}: non-finite output"
+        if got.size == 0:
+            return
+        d = np.abs(got - ref)
+        self.excess = max(self.excess, float((d - BF16_HALF_ULP_REL * np.abs(ref)).max()))
+        self.mx = max(self.mx, float(d.max()))
+        self.total += float(d.sum())
+        self.n += d.size
+
+    def check(self) -> None:
+        assert self.n > 0, f"{self.what}: nothing compared"
+        mn = self.total / self.n
+        assert self.excess <= MAX_ABS and mn <= MEAN_ABS, (
+            f"{self.what}: max|err| {self.mx:.3e} (beyond bf16 output rounding {self.excess:.3e}) "
+            f"mean|err| {mn:.3e} over {self.n} values")

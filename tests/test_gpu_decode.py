@@ -8,7 +8,7 @@ import torch
 
 import long_context_attention_orthros_gb300 as orth
 import oracle
-from synthetic import CONFIGS, DecodeConfig, make_decode, reduced
+from synthetic import CONFIGS, DecodeConfig, bf16_bits, make_decode, reduced
 from tests.gpu_util import assert_parity, bf, bits, dev, f32, i32, val
 
 pytestmark = pytest.mark.gpu
@@ -79,6 +79,74 @@ def test_decode_copy_is_isolated_from_cache_and_base():
         res.append((bits(o), bits(oc), bits(g.kc), bits(g.vc), g.cl.cpu().numpy()))
     for i in (0, 2, 3, 4):
         np.testing.assert_array_equal(res[0][i], res[1][i])
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,d,w,steps", [
+    ((0, 1, 63, 127, 128, 1000, 4097, 9000), 32, 8, 128, 128, 3),  # B=8, 8B-class heads, ragged
+    ((5000, 64, 130, 2), 8, 2, 64, 100, 2),                          # d=64, one sequence far longer
+])
+def test_decode_ragged_batch_matches_oracle(lens, Hq, Hkv, d, w, steps):
+    """Sequences of different cache lengths in one launch: each reads its own cache_len[b]; rows at
+    or beyond it hold bf16 NaN, so a read past a sequence's end shows as a non-finite output."""
+    B = len(lens)
+    cfg = DecodeConfig("ragged", B=B, T0=max(lens), steps=steps, Hq=Hq, Hkv=Hkv, d=d, window=w)
+    inp = make_decode(cfg, 4242 + B)
+    for b, n in enumerate(lens):
+        inp.k_cache[b, n:] = cfg.fill_unused
+        inp.v_cache[b, n:] = cfg.fill_unused
+    inp.cache_len[:] = np.asarray(lens, np.int32)
+    g = GpuDecode(inp)
+    ref, kc, vc, cl = _oracle_steps(inp, range(steps))
+    for i in range(steps):
+        o, oc = g.step(i)
+        assert_parity(val(o), ref[i][0], f"ragged step {i} base")
+        assert_parity(val(oc), ref[i][1], f"ragged step {i} copy")
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    np.testing.assert_array_equal(bits(g.kc), kc)
+    np.testing.assert_array_equal(bits(g.vc), vc)
+    np.testing.assert_array_equal(g.cl.cpu().numpy(), np.asarray(lens, np.int32) + steps)
+
+
+def test_decode_equals_prefill_exactly_on_one_hot_values():
+    """With K = 0 every logit is 0, so each softmax weight is exactly 1 and o = (sum of the attended
+    V rows) / (their count).  With V row j = e_(j mod d) the output is count_c / n per column, a
+    value each kernel reaches exactly up to its final bf16 rounding, and one key row too many or
+    too few moves a column by 1/n, far beyond that rounding.  Decode at position p and the
+    prefill kernels at p must both give the closed form: the decode-equals-prefill invariant
+    with the mask checked row for row."""
+    B, Hq, Hkv, d, w = 2, 8, 2, 128, 128
+    for p in (0, 5, 127, 128, 129, 1000, 4000):
+        T = p + 1
+        cfg = DecodeConfig("onehot", B=B, T0=p, steps=1, Hq=Hq, Hkv=Hkv, d=d, window=w)
+        inp = make_decode(cfg, 77)
+        onehot = np.zeros((T, d), np.float32)
+        onehot[np.arange(T), np.arange(T) % d] = 1.0
+        vrows = np.broadcast_to(bf16_bits(onehot)[None, :, None, :], (B, T, Hkv, d))
+        inp.k_cache[:, :p] = 0
+        inp.v_cache[:, :p] = vrows[:, :p]
+        inp.k_new[0] = 0
+        inp.v_new[0] = vrows[:, p]
+        g = GpuDecode(inp)
+        o, oc = g.step(0)
+        torch.cuda.synchronize()
+        assert int(g.err.item()) == 0
+
+        def closed_form(lo):
+            cnt = np.zeros(d)
+            np.add.at(cnt, np.arange(lo, T) % d, 1.0)
+            return np.broadcast_to(cnt / (T - lo), (B, Hq, d))
+        want_o, want_oc = closed_form(max(0, p - w + 1)), closed_form(0)
+        k_full = bits(g.kc)[:, :T]
+        v_full = bits(g.vc)[:, :T]
+        q = np.zeros((B, T, Hq, d), np.uint16)
+        q[:, p] = inp.q_new[0]
+        o_pre = val(orth.swa_fwd(bf(q), bf(k_full), bf(v_full), g.a, g.b, window=w))[:, p]
+        oc_pre = val(orth.xattn_fwd(bf(inp.qc_new[0][:, None]), i32(np.full((B, 1), p, np.int32)),
+                                    bf(k_full), bf(v_full), g.ac, g.bc))[:, 0]
+        for got, want, what in ((val(o), want_o, "decode base"), (o_pre, want_o, "prefill base"),
+                                (val(oc), want_oc, "decode copy"), (oc_pre, want_oc, "prefill copy")):
+            assert np.abs(got - want).max() <= 2.0 ** -8 * np.abs(want).max() + 1e-7, (p, what)
 
 
 def test_decode_equals_prefill_at_appended_position():

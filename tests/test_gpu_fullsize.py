@@ -1,32 +1,29 @@
 """GPU parity at the workloads' full sizes, in the launch configuration bench.py
-times, against the fp64 oracle on sampled outputs the oracle computes one by one:
-the 8B-class 128K prefill (B=2), the 1M-token prefill with scaled key rows, the
-SFT layer with 2048 appended shuffled copies per sequence, and 128 decode steps
-after a 131072-token cache."""
+times, against the fp64 oracle:
+
+* the 8B-class 128K prefill (B=2): every base output row and both copies;
+* the 1M-token prefill with scaled key rows: 16384 seeded random base rows, the
+  first window and the tail, the rows around every scaled key row, and the copy;
+* the SFT layer (B=4, 2048 appended shuffled copies per sequence): every base row
+  and every copy;
+* 128 decode steps after a 131072-token cache: sampled steps, and the cache bit
+  for bit after all of them.
+"""
 import numpy as np
 import pytest
 import torch
 
 import long_context_attention_orthros_gb300 as orth
 import oracle
-from synthetic import CONFIGS, SEEDS, make_decode, make_prefill
-from tests.gpu_util import assert_parity, bf, bits, dev, f32, i32, val
+from synthetic import CONFIGS, SEEDS, bf16_to_f32, make_decode, make_prefill
+from tests.gpu_util import ParityAccumulator, assert_parity, bf, bits, dev, f32, i32, val
 
 pytestmark = pytest.mark.gpu
 
-
-def _sample_rows(cfg, n, seed):
-    """Seeded (b, t) rows: the first window, the tail, and random rows in between."""
-    g = np.random.default_rng(seed)
-    t = np.concatenate([np.arange(0, 160, 7), np.arange(cfg.T - 40, cfg.T),
-                        g.integers(0, cfg.T, size=n)])
-    b = g.integers(0, cfg.B, size=t.size)
-    return b.astype(np.int32), t.astype(np.int32)
+CHUNK_ROWS = 8192  # oracle rows per call when every row is compared
 
 
-def _prefill_full(name, n_rows, copies=None):
-    cfg = CONFIGS[name]
-    inp = make_prefill(cfg, SEEDS[cfg.name])
+def _run_prefill(cfg, inp):
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     q_all = bf(inp.q_raw)
     k, v = bf(inp.k), bf(inp.v)
@@ -37,36 +34,85 @@ def _prefill_full(name, n_rows, copies=None):
                         dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    bi, ti = _sample_rows(cfg, n_rows, 7)
-    got = val(o[torch.from_numpy(bi).long().to(dev()), torch.from_numpy(ti).long().to(dev())])
-    ref = oracle.swa_rows(inp.q_base, inp.k, inp.v, inp.alpha, inp.beta, cfg.window, cfg.scale, bi, ti)
-    assert_parity(got, ref, f"{name} base rows")
-    sel = np.arange(cfg.T_out) if copies is None else copies
-    ref_c = oracle.xattn(np.ascontiguousarray(inp.qc_raw[:, sel]), np.ascontiguousarray(inp.pos[:, sel]),
-                         inp.k, inp.v, inp.alpha_c, inp.beta_c, cfg.scale)
-    assert_parity(val(oc)[:, sel], ref_c, f"{name} copies")
-    return inp, o
+    del q_all, k, v, qc
+    return o, oc
 
 
-def test_prefill_128k_full_size():
-    _prefill_full("prefill_128k", 2048)
-
-
-def test_prefill_1m_needles_full_size():
-    inp, o = _prefill_full("prefill_1m", 1024)
-    # rows whose window holds a scaled key row
+def _compare_rows(inp, o_bits, bi, ti, acc):
+    """Oracle rows (b, t) against the GPU's output bits o_bits [B, T, Hq, d], in chunks."""
     cfg = inp.cfg
-    nd = inp.needles[(inp.needles > 200) & (inp.needles < cfg.T - 200)][:16]
-    ti = (nd[:, None] + np.array([0, 5, 63, 127])[None, :]).reshape(-1).astype(np.int32)
+    q = np.ascontiguousarray(inp.q_base)  # once: the SFT layout keeps copies after the base rows
+    for c0 in range(0, bi.size, CHUNK_ROWS):
+        b, t = bi[c0:c0 + CHUNK_ROWS], ti[c0:c0 + CHUNK_ROWS]
+        ref = oracle.swa_rows(q, inp.k, inp.v, inp.alpha, inp.beta, cfg.window, cfg.scale, b, t)
+        acc.add(bf16_to_f32(o_bits[b, t]).astype(np.float64), ref)
+
+
+def _compare_copies(inp, oc_bits, sel, acc, per_call=256):
+    cfg = inp.cfg
+    for c0 in range(0, sel.size, per_call):
+        s = sel[c0:c0 + per_call]
+        ref = oracle.xattn(np.ascontiguousarray(inp.qc_raw[:, s]), np.ascontiguousarray(inp.pos[:, s]),
+                           inp.k, inp.v, inp.alpha_c, inp.beta_c, cfg.scale)
+        acc.add(bf16_to_f32(oc_bits[:, s]).astype(np.float64), ref)
+
+
+def _every_row(cfg):
+    t = np.tile(np.arange(cfg.T, dtype=np.int32), cfg.B)
+    b = np.repeat(np.arange(cfg.B, dtype=np.int32), cfg.T)
+    return b, t
+
+
+def test_prefill_128k_every_row():
+    cfg = CONFIGS["prefill_128k"]
+    inp = make_prefill(cfg, SEEDS[cfg.name])
+    o, oc = _run_prefill(cfg, inp)
+    o_bits, oc_bits = bits(o), bits(oc)
+    del o, oc
+    acc = ParityAccumulator("prefill_128k every base row")
+    _compare_rows(inp, o_bits, *_every_row(cfg), acc)
+    acc.check()
+    accc = ParityAccumulator("prefill_128k copies")
+    _compare_copies(inp, oc_bits, np.arange(cfg.T_out), accc)
+    accc.check()
+
+
+def test_prefill_1m_sampled_rows_and_every_scaled_key():
+    cfg = CONFIGS["prefill_1m"]
+    inp = make_prefill(cfg, SEEDS[cfg.name])
+    o, oc = _run_prefill(cfg, inp)
+    o_bits, oc_bits = bits(o), bits(oc)
+    del o, oc
+    g = np.random.default_rng(1)
+    rand = g.integers(0, cfg.T, size=16384)
+    edges = np.concatenate([np.arange(0, 200), np.arange(cfg.T - 64, cfg.T)])
+    # rows whose window holds a scaled key row: the needle's own row, the next, the middle of
+    # its window and the last row that still sees it
+    near = (inp.needles[:, None] + np.array([0, 1, 64, cfg.window - 1])[None, :]).reshape(-1)
+    near = near[near < cfg.T]
+    ti = np.concatenate([rand, edges, near]).astype(np.int32)
     bi = np.zeros_like(ti)
-    got = val(o[torch.from_numpy(bi).long().to(dev()), torch.from_numpy(ti).long().to(dev())])
-    ref = oracle.swa_rows(inp.q_base, inp.k, inp.v, inp.alpha, inp.beta, cfg.window, cfg.scale, bi, ti)
-    assert_parity(got, ref, "1M rows next to scaled keys")
+    acc = ParityAccumulator("prefill_1m base rows")
+    _compare_rows(inp, o_bits, bi, ti, acc)
+    acc.check()
+    assert acc.n >= (16384 + 4 * len(inp.needles) - 8) * cfg.Hq * cfg.d
+    accc = ParityAccumulator("prefill_1m copy")
+    _compare_copies(inp, oc_bits, np.arange(cfg.T_out), accc)
+    accc.check()
 
 
-def test_sft_16k_full_size():
-    g = np.random.default_rng(11)
-    _prefill_full("sft_16k", 1024, copies=np.sort(g.choice(2048, size=24, replace=False)))
+def test_sft_16k_every_row_and_copy():
+    cfg = CONFIGS["sft_16k"]
+    inp = make_prefill(cfg, SEEDS[cfg.name])
+    o, oc = _run_prefill(cfg, inp)
+    o_bits, oc_bits = bits(o), bits(oc)
+    del o, oc
+    acc = ParityAccumulator("sft_16k every base row")
+    _compare_rows(inp, o_bits, *_every_row(cfg), acc)
+    acc.check()
+    accc = ParityAccumulator("sft_16k every copy")
+    _compare_copies(inp, oc_bits, np.arange(cfg.T_out), accc)
+    accc.check()
 
 
 def test_decode_128k_full_size_sampled_steps():
