@@ -14,9 +14,25 @@ cudaError_t attn_bwd_layer_d128(int G, const AttnBwdParams &p, const AttnBwdPara
 cudaError_t attn_bwd_layer_d64(int G, const AttnBwdParams &p, const AttnBwdParams &pc, const CUtensorMap *maps,
                               const CUtensorMap *mapsc, cudaStream_t stream);
 
+static size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+int attn_bwd_key_blocks(int T_kv) { return (T_kv + 63) / 64; }
+
+size_t attn_bwd_kexp_offset(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
+{
+    return attn_bwd_k16_offset(B, n_units, Hq) + round256(2 * static_cast<size_t>(B) * T_kv * Hkv * D);
+}
+
+size_t attn_bwd_kflag_offset(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
+{
+    return attn_bwd_kexp_offset(B, n_units, T_kv, Hkv, Hq, D) +
+           round256(static_cast<size_t>(B) * Hkv * attn_bwd_key_blocks(T_kv) * 64);
+}
+
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D)
 {
-    return attn_bwd_k16_offset(B, n_units, Hq) + 2 * static_cast<size_t>(B) * T_kv * Hkv * D;
+    return attn_bwd_kflag_offset(B, n_units, T_kv, Hkv, Hq, D) +
+           round256(static_cast<size_t>(B) * Hkv * attn_bwd_key_blocks(T_kv));
 }
 
 size_t attn_bwd_split_bytes(int B, int Hkv)

@@ -87,38 +87,43 @@ __device__ __forceinline__ int unit_pos(const AttnBwdParams &p, int b, int u)
 // ------------------------------------------------------------------ fp16 copy of K
 
 // The tensor-memory kernels take q . k in fp16 (as the forward's tensor-memory path): K is
-// converted once per call, exactly (|k| < 65520, else ORTHROS_DEVERR_RANGE).
-__device__ __forceinline__ uint4 bf16x8_to_fp16(uint4 u, bool &bad)
+// converted once per call.  A key row whose largest |k| reaches 65520 (beyond fp16) is stored
+// as k * 2^-e with its largest element in [2^14, 2^15); the row's e goes to kexp and its
+// 64-key block's flag to kflag, so that the kernels reading S multiply its logits back by 2^e.
+// One CTA per 64-key block of one (batch, KV head); D / 8 lanes per key row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k, uint16_t *k16, int8_t *kexp,
+                                                           uint8_t *kflag, int T, int Hkv, int nkb, int32_t *dev_err)
 {
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    constexpr int CPR = D / 8;      // 16-byte chunks per key row
+    constexpr int RPI = 256 / CPR;  // rows per pass of the CTA
+    const int kb = static_cast<int>(blockIdx.x % nkb);
+    const int bh = static_cast<int>(blockIdx.x / nkb);
+    const int b = bh / Hkv, g = bh % Hkv;
+    const int c = threadIdx.x % CPR, rr = threadIdx.x / CPR;
+    bool shifted = false, bad = false;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(w[e]);
-        bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
-        __half2 hv = __floats2half2_rn(f.x, f.y);
-        w[e] = *reinterpret_cast<uint32_t *>(&hv);
+    for (int r0 = 0; r0 < 64; r0 += RPI) {
+        const int key = kb * 64 + r0 + rr;
+        const bool valid = key < T;
+        const long long off = ((static_cast<long long>(b) * T + key) * Hkv + g) * D + c * 8;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (valid)
+            u = __ldg(reinterpret_cast<const uint4 *>(k + off));
+        float am = bf16x8_absmax(u);
+#pragma unroll
+        for (int o = 1; o < CPR; o <<= 1)
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const int ex = fp16_key_shift(am, bad);
+        shifted |= ex != 0;
+        if (valid)
+            *reinterpret_cast<uint4 *>(k16 + off) = ex != 0 ? k_to_fp16_scaled(u, exp2i(-ex)) : k_to_fp16(u);
+        if (c == 0)
+            kexp[static_cast<long long>(bh) * nkb * 64 + kb * 64 + r0 + rr] = static_cast<int8_t>(ex);
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// two 16-byte chunks per thread and step, both loads in flight
-__global__ void __launch_bounds__(256) attn_bwd_k16_kernel(const orthros_bf16 *k, uint16_t *k16, long long n8,
-                                                           int32_t *dev_err)
-{
-    bool bad = false;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const uint4 *k4 = reinterpret_cast<const uint4 *>(k);
-    uint4 *o4 = reinterpret_cast<uint4 *>(k16);
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += 2 * stride) {
-        const long long i2 = i + stride;
-        const uint4 u0 = __ldg(k4 + i);
-        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-        if (i2 < n8)
-            u1 = __ldg(k4 + i2);
-        o4[i] = bf16x8_to_fp16(u0, bad);
-        if (i2 < n8)
-            o4[i2] = bf16x8_to_fp16(u1, bad);
-    }
+    shifted = __syncthreads_or(shifted ? 1 : 0) != 0;
+    if (threadIdx.x == 0)
+        kflag[static_cast<long long>(bh) * nkb + kb] = shifted ? 1 : 0;
     if (bad)
         record_error(dev_err, ORTHROS_DEVERR_RANGE);
 }
@@ -854,7 +859,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         const int rw = warp - 4;
         const int key = kt0 + rw * 32 + lane;
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        const float c2 = p.scale * kLog2eF;
+        // logit scale of this key's row of S^T (its fp16 copy is k * 2^-e: the logits are times 2^e)
+        const float c2 = p.scale * kLog2eF *
+                         exp2i(key < p.T_kv ? p.kexp[static_cast<long long>(bh) * p.nkb * 64 + key] : 0);
         float ds_max = 0.f;  // dS^T goes to fp16: |dS| < 65504 or the range error
         int i = 0, ph = 0, r = r_begin;
         for (bool more = rounds.seek(ph, r); more; ++r, more = rounds.seek(ph, r), ++i) {
@@ -1219,13 +1226,19 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         float m = NEG_INF, l = 0.f;
         // known beforehand (log2 units): from the forward via the D kernel, or the split combine
         float lse = ((p.lse_in != nullptr || mode == 2) && P >= 0) ? p.lse[ri] : 0.f;
+        bool kshift_bad = false;
         for (int n = 0; ok && n < nsteps; ++n) {
             const int u = n & 1;
             const bool pass2 = n >= n1;
             const int k0 = (kb0 + (pass2 ? n - n1 : n)) * C::KB;
+            const bool kshift = p.kflag[static_cast<long long>(bh) * p.nkb + k0 / 64] != 0;  // rare
             if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n >> 1) & 1))))
                 break;
             tc_fence_after();
+            if (kshift)  // logits of shifted key rows times 2^e_j, in tensor memory
+                for (int half = 0; half < 2; ++half)
+                    unshift_chunk32(tl + C::TM_S + 64 * u + 32 * half, p.kexp + static_cast<long long>(bh) * p.nkb * 64 + k0,
+                                    32 * half, 1u, 1, 1, kshift_bad);
             if (!pass2) {
                 uint32_t sa[32], sb[32];
                 tmem_ld32(tl + C::TM_S + 64 * u, sa);
@@ -1288,6 +1301,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     mbar_arrive(&p_full[u]);
             }
         }
+        if (kshift_bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         // ---- epilogue: dq_raw = scale dQ alpha; dalpha, dbeta summed over the warp's rows per head
         if (mode == 1 && ok)  // this split's (max, sum) of every row of the tile (log2 units)
             p.part_ml[(static_cast<long long>(bh) * p.splits + blockIdx.z) * C::ROWS + r] = make_float2(m, l);
@@ -1617,6 +1632,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
         const float c2 = p.scale * kLog2eF;
+        bool kshift_bad = false;
         long long n = 0;
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int b, g, u0, kb0, nb;
@@ -1629,10 +1645,16 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             const float Drow = live ? p.Drow[ri] : 0.f;
             for (int j = 0; j < nb; ++j, ++n) {
                 const int u = static_cast<int>(n % C::NBUF);
+                const int k0 = (kb0 + j) * C::KB;
+                const long long bh = static_cast<long long>(b) * p.Hkv + g;
+                const bool kshift = p.kflag[bh * p.nkb + k0 / 64] != 0;  // rare
                 if (!(ok = warp_wait(&s_full[u], static_cast<uint32_t>((n / C::NBUF) & 1))))
                     break;
                 tc_fence_after();
-                const int k0 = (kb0 + j) * C::KB;
+                if (kshift)  // logits of shifted key rows times 2^e_j, in tensor memory
+                    for (int half = 0; half < C::KB / 32; ++half)
+                        unshift_chunk32(tl + C::TM_S + C::KB * u + 32 * half, p.kexp + bh * p.nkb * 64 + k0, 32 * half,
+                                        1u, 1, 1, kshift_bad);
 #pragma unroll
                 for (int half = 0; half < C::KB / 32; ++half) {
                     uint32_t sv[32], dv[32];
@@ -1662,6 +1684,8 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     mbar_arrive(&p_full[u]);
             }
         }
+        if (kshift_bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
         // ------------------------------------------------------------------ epilogue (warps 8-11)
         // dq_raw = scale dQ alpha (dalpha, dbeta follow from it in attn_bwd_dab_kernel)
@@ -1763,9 +1787,8 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
     if (e != cudaSuccess)
         return e;
     if (make_k16) {
-        const long long n8 = static_cast<long long>(p.B) * p.T_kv * p.Hkv * D / 8;
-        attn_bwd_k16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(p.k, p.k16, n8,
-                                                                                                  p.dev_err);
+        attn_bwd_k16_kernel<D><<<static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.nkb), 256, 0, stream>>>(
+            p.k, p.k16, p.kexp, p.kflag, p.T_kv, p.Hkv, p.nkb, p.dev_err);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }

@@ -14,9 +14,12 @@
 //     rows 64 * floor(p / 64) .. p-1 plus the new row (taken from k_new / v_new,
 //     never read back from the cache) for the copy, the base token's window,
 //     and the append itself;
-//   * the last CTA of each (b, KV head) to finish merges the partials (an atomic
-//     arrival counter, no spin-wait) and the last group of each sequence bumps
-//     cache_len.  Counters are left at zero for the next step.
+//   * each split CTA merges its four warps' partial results in shared memory and
+//     writes one partial; the last CTA of each (b, KV head) to finish merges the
+//     partials (an atomic arrival counter, no spin-wait), loading all of their
+//     weights first so that the partial outputs stream in with several loads in
+//     flight, and the last group of each sequence bumps cache_len.  Counters are
+//     left at zero for the next step.
 // Rows at or beyond the old cache_len are never read from memory.
 #include "kernels.cuh"
 #include "xattn.cuh"
@@ -246,7 +249,24 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
         if (!ok && lane == 0)
             record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
         st.finish_sums();
-        const int part = x * C::CWARPS + warp;
+        // one partial per CTA: the four warps' results merged in shared memory (the ring is free:
+        // every block has been consumed)
+        float *ms = reinterpret_cast<float *>(smem);  // [CWARPS][G] max
+        float *ls = ms + C::CWARPS * G;               // [CWARPS][G] sum
+        float *os = ls + C::CWARPS * G;               // [CWARPS][G][D] output, scaled to the CTA's max
+        named_barrier(3, C::CTHREADS);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int row = 8 * nt + 2 * (lane & 3) + r2;
+                if (row < G && (lane >> 2) == 0) {
+                    ms[warp * G + row] = st.m[nt][r2];
+                    ls[warp * G + row] = st.l[nt][r2];
+                }
+            }
+        named_barrier(3, C::CTHREADS);
+        const float NEG_INF = -__int_as_float(0x7f800000);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -254,15 +274,38 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
                 const int row = 8 * nt + 2 * (lane & 3) + r2;
                 if (row >= G)
                     continue;
-                float *po = part_o + (static_cast<long long>(part) * G + row) * D + (lane >> 2);
+                float M = NEG_INF;
+#pragma unroll
+                for (int w = 0; w < C::CWARPS; ++w)
+                    M = fmaxf(M, ms[w * G + row]);
+                const float f = (M == NEG_INF || st.m[nt][r2] == NEG_INF) ? 0.f : fast_exp2(st.m[nt][r2] - M);
+                float *po = os + (warp * G + row) * D + (lane >> 2);
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    po[16 * mt] = st.o[nt][mt][r2];
-                    po[16 * mt + 8] = st.o[nt][mt][2 + r2];
+                    po[16 * mt] = st.o[nt][mt][r2] * f;
+                    po[16 * mt + 8] = st.o[nt][mt][2 + r2] * f;
                 }
-                if ((lane >> 2) == 0)
-                    part_ml[static_cast<long long>(part) * G + row] = make_float2(st.m[nt][r2], st.l[nt][r2]);
             }
+        named_barrier(3, C::CTHREADS);
+        for (int i = threadIdx.x; i < G * D; i += C::CTHREADS) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::CWARPS; ++w)
+                a += os[w * G * D + i];
+            part_o[static_cast<long long>(x) * G * D + i] = a;
+        }
+        if (threadIdx.x < G) {
+            const int row = threadIdx.x;
+            float M = NEG_INF, L = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::CWARPS; ++w)
+                M = fmaxf(M, ms[w * G + row]);
+#pragma unroll
+            for (int w = 0; w < C::CWARPS; ++w)
+                if (ms[w * G + row] != NEG_INF)
+                    L += ls[w * G + row] * fast_exp2(ms[w * G + row] - M);
+            part_ml[static_cast<long long>(x) * G + row] = make_float2(M, L);
+        }
     } else {
         // ------------------------------------------------ tail CTA
         float *q_s = reinterpret_cast<float *>(smem);          // [G][D]
@@ -290,7 +333,7 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
                 q_s[i] = fmaf(x0, p.alpha_c[h * D + e], p.beta_c[h * D + e]) * p.qscale;
             }
             tail_attend<D, G>(q_s, logit_s, m_s, l_s, corr_s, kc, vc, row_stride, knew, vnew, nfull, pcur, acc);
-            const int part = p.nsplit * C::CWARPS;
+            const int part = p.nsplit;
             if (t < D) {
 #pragma unroll
                 for (int r = 0; r < G; ++r)
@@ -336,6 +379,7 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
         return;
     __threadfence();
     const float NEG_INF = -__int_as_float(0x7f800000);
+    float *w_s = reinterpret_cast<float *>(smem);  // [G][n_part] partial weights (this CTA's work is done)
     for (int r = warp; r < G; r += C::CWARPS) {
         const int h = g * G + r;
         orthros_bf16 *orow = p.oc + (static_cast<long long>(b) * p.Hq + h) * D;
@@ -344,6 +388,7 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
                 orow[e] = 0;
             continue;
         }
+        // the partials' weights exp2(m - M), all loaded at once (lane q, q + 32, ...)
         float M = NEG_INF;
         for (int q = lane; q < p.n_part; q += 32) {
             const float2 ml = __ldcg(&part_ml[static_cast<long long>(q) * G + r]);
@@ -356,22 +401,23 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
         float L = 0.f;
         for (int q = lane; q < p.n_part; q += 32) {
             const float2 ml = __ldcg(&part_ml[static_cast<long long>(q) * G + r]);
-            if (ml.y > 0.f)
-                L += ml.y * fast_exp2(ml.x - M);
+            const float w = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+            w_s[r * p.n_part + q] = w;
+            L += ml.y > 0.f ? ml.y * w : 0.f;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             L += __shfl_xor_sync(0xffffffffu, L, off);
+        __syncwarp();
+        // the weighted sum of the partial outputs: independent loads, several in flight
         constexpr int E = D / 32;
         float a[E];
 #pragma unroll
         for (int e = 0; e < E; ++e)
             a[e] = 0.f;
+#pragma unroll 8
         for (int q = 0; q < p.n_part; ++q) {
-            const float2 ml = __ldcg(&part_ml[static_cast<long long>(q) * G + r]);
-            if (!(ml.y > 0.f))
-                continue;
-            const float w = fast_exp2(ml.x - M);
+            const float w = w_s[r * p.n_part + q];
             const float *po = part_o + (static_cast<long long>(q) * G + r) * D + lane * E;
 #pragma unroll
             for (int e = 0; e < E; ++e)
@@ -417,7 +463,7 @@ size_t decode_workspace_bytes(int B, int L_max, int Hq, int Hkv, int D)
 {
     const int G = Hq / Hkv;
     const int ns = decode_nsplit(B, L_max, Hkv);
-    const size_t n_part = static_cast<size_t>(ns) * 4 + 1;
+    const size_t n_part = static_cast<size_t>(ns) + 1;
     const size_t BH = static_cast<size_t>(B) * Hkv;
     const size_t o_bytes = (BH * n_part * G * D * sizeof(float) + 255) / 256 * 256;
     const size_t ml_bytes = (BH * n_part * G * sizeof(float2) + 255) / 256 * 256;
@@ -443,7 +489,7 @@ cudaError_t launch_decode(int D, const CUtensorMap &k, const CUtensorMap &v, Dec
 {
     const int G = p.Hq / p.Hkv;
     p.nsplit = decode_nsplit(p.B, p.L_max, p.Hkv);
-    p.n_part = p.nsplit * 4 + 1;
+    p.n_part = p.nsplit + 1;  // one per split CTA and the tail
     const size_t BH = static_cast<size_t>(p.B) * p.Hkv;
     const size_t o_bytes = (BH * p.n_part * G * D * sizeof(float) + 255) / 256 * 256;
     const size_t ml_bytes = (BH * p.n_part * G * sizeof(float2) + 255) / 256 * 256;

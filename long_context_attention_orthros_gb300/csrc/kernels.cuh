@@ -25,6 +25,7 @@ struct SwaParams {
     long long total_tiles; // B * Hkv on input; B * Hkv * tiles_per_stream after launch set-up
     int reuse;             // 1: keep K/V blocks resident across consecutive tiles (set by launcher)
     float *lse;            // optional [B, T, Hq]: natural log of each row's sum of exp(scale q . k)
+    int B;
 };
 
 struct XattnParams {
@@ -70,6 +71,12 @@ struct AttnBwdParams {
     float *lse, *Drow;                       // workspace [B*n_units*Hq] each: log2-sum-exp, dO . o
     uint16_t *k16;                           // workspace: K as fp16 [B, T_kv, Hkv, d]
     uint16_t *q16;                           // workspace: q = x alpha + beta as fp16 [B, n_units, Hq, d]
+    // workspace, written with k16: each key row's shift e (k16 holds k * 2^-e; e != 0 only for a
+    // row whose largest |k| reaches 65520) as int8 [B*Hkv][nkb * 64], and per 64-key block
+    // whether any row of it is shifted, uint8 [B*Hkv][nkb]
+    int8_t *kexp;
+    uint8_t *kflag;
+    int nkb;                                 // 64-key blocks of T_kv
     int32_t *dev_err;
     int B, n_units, T_kv, Hq, Hkv, window;   // window = T_kv for the copies
     int accumulate;                          // add to dk, dv instead of overwriting them
@@ -81,8 +88,12 @@ struct AttnBwdParams {
     float2 *part_ml;                         // workspace [B*Hkv][splits][128]
 };
 
-// workspace: lse, D (fp32 per query row), then at a 256-byte boundary the fp16 copy of K
+// workspace: lse, D (fp32 per query row), then at 256-byte boundaries the fp16 copy of K, the
+// key rows' shifts and the 64-key blocks' shift flags
 size_t attn_bwd_workspace_bytes(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
+size_t attn_bwd_kexp_offset(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
+size_t attn_bwd_kflag_offset(int B, int n_units, int T_kv, int Hkv, int Hq, int D);
+int attn_bwd_key_blocks(int T_kv);
 size_t attn_bwd_k16_offset(int B, int n_units, int Hq);
 // extra workspace of the copies' gradient: per-split row partials of the split dq path
 constexpr int ATTN_BWD_MAX_SPLITS = 64;

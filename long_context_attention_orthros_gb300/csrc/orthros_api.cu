@@ -130,11 +130,15 @@ int orthros_version(void) { return 100; }
 
 namespace {
 
-orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
-                            const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T, int Hq,
-                            int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
-                            int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
+// Checks the arguments of a base-stream call and fills its tensor maps and parameters.  Returns
+// ORTHROS_OK with *empty set when there is no row to compute.
+orthros_status swa_setup(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                         const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T, int Hq,
+                         int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                         int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, CUtensorMap *maps,
+                         SwaParams &p, bool *empty)
 {
+    *empty = false;
     if (!aligned16(q_raw) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(o) || B < 1 || T < 1 || window < 1 || !std::isfinite(scale))
         return ORTHROS_ERR_INVALID_ARG;
@@ -143,8 +147,10 @@ orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, co
         return ORTHROS_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || !heads_ok(Hq, Hkv))
         return ORTHROS_ERR_UNSUPPORTED;
-    if (row_begin == row_end)
+    if (row_begin == row_end) {
+        *empty = true;
         return ORTHROS_OK;
+    }
     long long qs = q_bstride, ks = kv_bstride, os = o_bstride;
     if (!resolve_bstride(qs, static_cast<long long>(T) * Hq * d) ||
         !resolve_bstride(ks, static_cast<long long>(T) * Hkv * d) ||
@@ -152,14 +158,10 @@ orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, co
         return ORTHROS_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
     const int TOK = 128 / G;
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, q_raw, d, Hq, T, B, qs, G, TOK) || !make_map(&mk, k, d, Hkv, T, B, ks, 1, 32) ||
-        !make_map(&mv, v, d, Hkv, T, B, ks, 1, 32) || !make_map(&mo, o, d, Hq, T, B, os, G, TOK))
+    if (!make_map(&maps[0], q_raw, d, Hq, T, B, qs, G, TOK) || !make_map(&maps[1], k, d, Hkv, T, B, ks, 1, 32) ||
+        !make_map(&maps[2], v, d, Hkv, T, B, ks, 1, 32) || !make_map(&maps[3], o, d, Hq, T, B, os, G, TOK))
         return ORTHROS_ERR_CUDA;
-    const int sms = num_sms();
-    if (sms <= 0)
-        return ORTHROS_ERR_CUDA;
-    SwaParams p{};
+    p = SwaParams{};
     p.alpha = alpha;
     p.beta = beta;
     p.o = o;
@@ -174,7 +176,27 @@ orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, co
     p.row_begin = row_begin;
     p.row_end = row_end;
     p.lse = lse;
-    const cudaError_t e = orthros::launch_swa(d, G, mq, mk, mv, mo, p, sms, static_cast<cudaStream_t>(stream));
+    p.B = B;
+    return ORTHROS_OK;
+}
+
+orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
+                            const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T, int Hq,
+                            int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
+                            int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
+{
+    CUtensorMap maps[4];
+    SwaParams p;
+    bool empty = false;
+    const orthros_status st = swa_setup(q_raw, k, v, alpha, beta, o, lse, B, T, Hq, Hkv, d, window, scale, q_bstride,
+                                        kv_bstride, o_bstride, row_begin, row_end, dev_err, maps, p, &empty);
+    if (st != ORTHROS_OK || empty)
+        return st;
+    const int sms = num_sms();
+    if (sms <= 0)
+        return ORTHROS_ERR_CUDA;
+    const cudaError_t e =
+        orthros::launch_swa(d, Hq / Hkv, maps[0], maps[1], maps[2], maps[3], p, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
 
@@ -430,6 +452,10 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
     p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T, Hq));
+    p.kexp = reinterpret_cast<int8_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_kexp_offset(B, T, T, Hkv, Hq, d));
+    p.kflag = reinterpret_cast<uint8_t *>(static_cast<char *>(workspace) +
+                                          orthros::attn_bwd_kflag_offset(B, T, T, Hkv, Hq, d));
+    p.nkb = orthros::attn_bwd_key_blocks(T);
     p.q16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) +
                                          orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d));
     p.dev_err = dev_err;
@@ -493,6 +519,11 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.lse = static_cast<float *>(workspace);
     p.Drow = p.lse + static_cast<size_t>(B) * T_out * Hq;
     p.k16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + orthros::attn_bwd_k16_offset(B, T_out, Hq));
+    p.kexp = reinterpret_cast<int8_t *>(static_cast<char *>(workspace) +
+                                        orthros::attn_bwd_kexp_offset(B, T_out, T_kv, Hkv, Hq, d));
+    p.kflag = reinterpret_cast<uint8_t *>(static_cast<char *>(workspace) +
+                                          orthros::attn_bwd_kflag_offset(B, T_out, T_kv, Hkv, Hq, d));
+    p.nkb = orthros::attn_bwd_key_blocks(T_kv);
     p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
                                            orthros::attn_bwd_workspace_bytes(B, T_out, T_kv, Hkv, Hq, d));
     p.q16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(p.part_ml) + orthros::attn_bwd_split_bytes(B, Hkv));
@@ -565,6 +596,9 @@ orthros_status orthros_attn_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k
     p.lse = reinterpret_cast<float *>(ws);
     p.Drow = p.lse + static_cast<size_t>(B) * T * Hq;
     p.k16 = reinterpret_cast<uint16_t *>(ws + orthros::attn_bwd_k16_offset(B, T, Hq));
+    p.kexp = reinterpret_cast<int8_t *>(ws + orthros::attn_bwd_kexp_offset(B, T, T, Hkv, Hq, d));
+    p.kflag = reinterpret_cast<uint8_t *>(ws + orthros::attn_bwd_kflag_offset(B, T, T, Hkv, Hq, d));
+    p.nkb = orthros::attn_bwd_key_blocks(T);
     p.q16 = reinterpret_cast<uint16_t *>(ws + orthros::attn_bwd_workspace_bytes(B, T, T, Hkv, Hq, d));
     p.dev_err = dev_err;
     p.B = B;

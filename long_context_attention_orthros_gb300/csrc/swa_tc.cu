@@ -14,8 +14,11 @@
 //
 // Arithmetic:
 //   S = q K^T in fp16 (q rounded once to fp16 after scale-offset, softmax scale
-//       and log2(e); K converted from bf16 to fp16 in shared memory, exact for
-//       |k| < 65520, otherwise ORTHROS_DEVERR_RANGE), fp32 accumulation;
+//       and log2(e); K converted from bf16 to fp16 in shared memory: a key row
+//       whose largest |k| reaches 65520 (beyond fp16) is first scaled by an exact
+//       power of two 2^-e_j into [2^14, 2^15), and the softmax multiplies that
+//       key's logits by 2^e_j, so every finite bf16 key is taken), fp32
+//       accumulation;
 //   P = exp2(S - rowmax) over the whole band at once (the band fits in tensor
 //       memory, so there is no online rescaling), stored as bf16 over S;
 //   O = P V in bf16 with fp32 accumulation; o = O / rowsum rounded to bf16.
@@ -59,10 +62,14 @@ struct TcCfg {
     static constexpr int Q_SLAB = ROWS * 128;
     static constexpr int Q_BYTES = SLABS * Q_SLAB;  // one of two query buffers
     static constexpr int BAR_OFF = Q_OFF + 2 * Q_BYTES;
-    static constexpr int NBARS = 3 * STAGES + 11;
-    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;      // tensor-memory base address
+    static constexpr int NBARS = 3 * STAGES + 13;
+    static constexpr int KEXP_OFF = BAR_OFF + NBARS * 8;      // int8 [STAGES][KB]: key row shift e_j
+    static constexpr int KFLAG_OFF = KEXP_OFF + STAGES * KB;  // uint8 [2 warps][8]: slot holds shifted rows
+    static constexpr int KBAND_OFF = KFLAG_OFF + 16;          // uint32 [2]: shifted blocks of a tile's band
+    static constexpr int HOLD_OFF = KBAND_OFF + 8;            // tensor-memory base address
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;         // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(STAGES <= 8, "one flag byte per slot in a 64-bit word");
     static constexpr uint32_t TM_SSTRIDE = 32 * NB;
     static constexpr uint32_t TM_O = 384;
     static constexpr uint32_t TM_COLS = 512;
@@ -110,6 +117,9 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *p_full = qfull + 6;            // [2] P written over S
     uint64_t *o_full = qfull + 8;            // [2] O = P V complete (by the parity of the tile)
     uint64_t *o_free = qfull + 10;           // O read out of tensor memory
+    uint64_t *kinfo = qfull + 11;            // [2] the band's shift word of S buffer u written
+    int8_t *kexp = reinterpret_cast<int8_t *>(smem + C::KEXP_OFF);
+    volatile uint32_t *kband = reinterpret_cast<volatile uint32_t *>(smem + C::KBAND_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,6 +129,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&kconv[s], 2);
             mbar_init(&empty[s], 1);
         }
+        reinterpret_cast<uint64_t *>(smem + C::KFLAG_OFF)[0] = 0;
+        reinterpret_cast<uint64_t *>(smem + C::KFLAG_OFF)[1] = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
             mbar_init(&qt_full[i], 4);
@@ -128,6 +140,8 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(&o_full[0], 1);
         mbar_init(&o_full[1], 1);
         mbar_init(o_free, 4);
+        mbar_init(&kinfo[0], 1);
+        mbar_init(&kinfo[1], 1);
         tmem_holder[1] = static_cast<uint32_t>(p.n_base);
         fence_barrier_init();
     }
@@ -289,6 +303,21 @@ __global__ void __launch_bounds__(512, 1)
                         umma_ss(tbase + buf * C::TM_SSTRIDE, qdesc + qoff, kdesc + koff, idesc, kk != 0);
                     }
                     umma_commit(&s_full[buf]);
+                    // which blocks of the band hold shifted key rows (the converters' flags, seen
+                    // through the kconv waits above), for the softmax of this tile
+                    const volatile uint64_t *kf = reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF);
+                    const uint64_t f0 = kf[0], f1 = kf[1];
+                    uint32_t smask = 0;  // bits 2 j, 2 j + 1: band block j holds shifted rows of converter warp 0, 1
+                    if ((f0 | f1) != 0) {
+#pragma unroll 1
+                        for (int j = 0; j < nb; ++j) {
+                            const int sh = 8 * ((idx0 + j) % C::STAGES);
+                            smask |= (((f0 >> sh) & 0xffu) ? 1u : 0u) << (2 * j);
+                            smask |= (((f1 >> sh) & 0xffu) ? 1u : 0u) << (2 * j + 1);
+                        }
+                    }
+                    kband[buf] = smask | (slot0 << 16);
+                    mbar_arrive(&kinfo[buf]);
                 }
                 // ---- O = P V for the previous tile: within a segment it keeps the blocks this tile
                 // still uses; at a segment change or after the last tile it releases its whole band
@@ -307,7 +336,12 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------------ K converters
-        const int ct = threadIdx.x - 64;  // 0..63
+        // 8 lanes per key row (the row's 16-byte chunk c8 in every slab), rows rsub + 4 NCW i
+        constexpr int NCW = 2;            // converter warps
+        const int ct = threadIdx.x - 64;  // 0 .. 63
+        const int c8 = ct & 7, rsub = ct >> 3;
+        constexpr int ROWS_T = C::KB / (4 * NCW);  // key rows per thread and block
+        uint8_t *kflag = smem + C::KFLAG_OFF + (warp - 2) * 8;
         bool ok = true, bad = false;
         long long idx = 0;
         for (long long gt = gt_begin; gt < gt_end && ok;) {
@@ -320,26 +354,54 @@ __global__ void __launch_bounds__(512, 1)
                     ok = false;
                     break;
                 }
-                const int copies = s < C::MIRROR ? 2 : 1;
+                // common case: every chunk below 65520 converts as is; when a chunk of the warp's
+                // rows reaches it, the warp shifts those rows instead (rare)
+                // common case: every chunk below 65520 converts as is, in passes of up to four rows
+                // per lane (loads of a pass in flight together); when a chunk of the warp's rows
+                // reaches 65520 the warp shifts its rows instead (rare)
+                constexpr int RP = ROWS_T < 4 ? ROWS_T : 4;
+                bool block_any = false;
+                int r_bad = 0;  // first row (of this lane's) of the pass that found a value beyond fp16
+#pragma unroll 1
+                for (int r0 = 0; r0 < ROWS_T && !block_any; r0 += RP) {
+                    uint4 u[RP][C::SLABS];
+                    uint32_t kept = 0;
 #pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl)
-                    for (int cp = 0; cp < copies; ++cp) {
-                        uint8_t *blk = smem + C::K_OFF + sl * C::K_SLAB + (s + cp * C::STAGES) * C::SLOT;
+                    for (int r = 0; r < RP; ++r)
 #pragma unroll
-                        for (int c = ct; c < C::SLOT / 16; c += 64) {
-                            uint4 *ptr = reinterpret_cast<uint4 *>(blk + c * 16);
-                            uint4 u = *ptr;
-                            uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_bf16x2(w[e]);
-                                bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
-                                __half2 hv = __floats2half2_rn(f.x, f.y);
-                                w[e] = *reinterpret_cast<uint32_t *>(&hv);
-                            }
-                            *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int sl = 0; sl < C::SLABS; ++sl) {
+                            u[r][sl] = *reinterpret_cast<const uint4 *>(smem + C::K_OFF + sl * C::K_SLAB + s * C::SLOT +
+                                                                        (rsub + 4 * NCW * (r0 + r)) * 128 + c8 * 16);
+                            kept |= (bf16x8_absmax(u[r][sl]) < 65520.f ? 0u : 1u) << (r * C::SLABS + sl);
                         }
+                    block_any = __any_sync(0xffffffffu, kept != 0);
+                    r_bad = r0;
+                    if (!block_any) {
+#pragma unroll
+                        for (int r = 0; r < RP; ++r)
+#pragma unroll
+                            for (int sl = 0; sl < C::SLABS; ++sl) {
+                                uint8_t *dst = smem + C::K_OFF + sl * C::K_SLAB + s * C::SLOT +
+                                               (rsub + 4 * NCW * (r0 + r)) * 128 + c8 * 16;
+                                const uint4 h = k_to_fp16(u[r][sl]);
+                                *reinterpret_cast<uint4 *>(dst) = h;
+                                if (s < C::MIRROR)
+                                    *reinterpret_cast<uint4 *>(dst + C::STAGES * C::SLOT) = h;
+                            }
                     }
+                }
+                if (block_any) {
+                    // rows of the passes before r_bad are converted and hold nothing beyond fp16;
+                    // the rest, still bf16, take the per-row shift
+                    if (c8 == 0)
+                        for (int r = 0; r < r_bad; ++r)
+                            kexp[s * C::KB + rsub + 4 * NCW * r] = 0;
+                    shift_key_rows<C::SLABS>(smem + C::K_OFF + s * C::SLOT, C::K_SLAB,
+                                             s < C::MIRROR ? C::STAGES * C::SLOT : 0, rsub + 4 * NCW * r_bad, 4 * NCW,
+                                             ROWS_T - r_bad, c8, kexp + s * C::KB, bad);
+                }
+                if (lane == 0)
+                    kflag[s] = block_any ? 1 : 0;
                 fence_proxy_async_smem();  // the MMA reads the converted block through the async proxy
                 __syncwarp();
                 if (lane == 0)
@@ -362,7 +424,7 @@ __global__ void __launch_bounds__(512, 1)
         const float NEG_INF = -__int_as_float(0x7f800000);
         // rows can be written as whole 32-byte sectors when the output is 32-byte aligned
         const bool o32 = ((reinterpret_cast<uintptr_t>(p.o) | static_cast<uintptr_t>(p.o_bstride * 2)) & 31u) == 0;
-        bool ok = true;
+        bool ok = true, range_bad = false;
         int it = 0;
         // this warpgroup's epilogue for its tile `eit`: O / l -> bf16 -> global memory
         auto epilogue = [&](int eit, int eb, int eg, int en, float inv_l) -> bool {
@@ -425,11 +487,16 @@ __global__ void __launch_bounds__(512, 1)
                 const int bs = klo * 32;
                 const int t = n * TOK + ti;
                 const int lo_key = max(0, t - p.window + 1), hi_key = min(t, p.T - 1);
-                if (!mbar_wait(&s_full[wg], static_cast<uint32_t>((it >> 1) & 1))) {
+                if (!mbar_wait(&s_full[wg], static_cast<uint32_t>((it >> 1) & 1)) ||
+                    !mbar_wait(&kinfo[wg], static_cast<uint32_t>((it >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // blocks of the band whose key rows were shifted into fp16 range (almost always none)
+                const uint32_t band = kband[wg];
+                const uint32_t smask = band & 0xffffu;
+                const int slot0 = static_cast<int>(band >> 16);
                 // keys of this row: lo_key .. hi_key; a key is valid iff 0 <= key - lo_key <= span
                 int lo = lo_key, span = hi_key - lo_key;
                 if (span < 0) {
@@ -437,7 +504,6 @@ __global__ void __launch_bounds__(512, 1)
                     span = 0;
                 }
                 const unsigned uspan = static_cast<unsigned>(span);
-                uint32_t va[32], vb[32];
                 // chunks whose keys are inside the window of every row of this warp need no mask
                 unsigned inner = 0;
                 for (int q = 0; q < nb; ++q) {
@@ -445,65 +511,79 @@ __global__ void __launch_bounds__(512, 1)
                     if (__all_sync(0xffffffffu, key0 >= lo_key && key0 + 31 <= hi_key))
                         inner |= 1u << q;
                 }
-                // row max of one 32-column chunk into m4; a chunk that needs the mask is
-                // masked here and written back, so the exponent pass needs no mask
-                auto chunk_max = [&](uint32_t (&v)[32], int q, float (&m4)[4]) {
-                    if (!(inner >> q & 1u)) {
-                        const int k0 = bs + 32 * q - lo;
+                // logits of shifted key rows times 2^e_j (rare): rewritten in tensor memory first
+#pragma unroll 1
+                for (int q = 0; q < nb && smask != 0; ++q) {
+                    const uint32_t wm = (smask >> (2 * q)) & 3u;
+                    if (wm != 0)
+                        unshift_chunk32(s_col + 32 * q, kexp + ((slot0 + q) % C::STAGES) * C::KB, 0, wm, 8, 4,
+                                        range_bad);
+                }
+                // The band is read in 16-column halves, the next half's load in flight while the
+                // current one is processed (tcgen05.wait::ld waits for every load of the thread).
+                // Row max of one half into m4; a half of a chunk that needs the mask is masked here
+                // and written back, so the exponent pass needs no mask
+                auto half_max = [&](uint32_t (&v)[16], int hq, float (&m4)[4]) {
+                    if (!(inner >> (hq >> 1) & 1u)) {
+                        const int k0 = bs + 16 * hq - lo;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
+                        for (int e = 0; e < 16; ++e)
                             if (static_cast<unsigned>(k0 + e) > uspan)
                                 v[e] = __float_as_uint(NEG_INF);
-                        tmem_st32(s_col + 32 * q, v);
+                        tmem_st16(s_col + 16 * hq, v);
                     }
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2)
+                    for (int e = 0; e < 16; e += 2)
                         m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
                 };
-                // P = exp2(S - mu) of one chunk as bf16 pairs; row sums into l2
-                auto chunk_exp = [&](const uint32_t (&v)[32], float2 nmu, float2 (&l2)[2], uint32_t (&pw)[16]) {
+                // P = exp2(S - mu) of one half as 8 bf16 pairs (written over S columns already read);
+                // row sums into l2
+                auto half_exp = [&](const uint32_t (&v)[16], float2 nmu, float2 (&l2)[2], int hq) {
+                    uint32_t pw[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
+                    for (int e = 0; e < 8; ++e) {
                         const float2 d = fadd2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), nmu);
                         const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
                         l2[e & 1] = fadd2(l2[e & 1], pp);
                         pw[e] = pack_bf16x2(pp.x, pp.y);
                     }
+                    tmem_st8(s_col + 8 * hq, pw);
                 };
-                // pass 1: row max over the band, two 32-column chunks per round
+                const int nh = 2 * nb;
+                uint32_t va[16], vb[16];
+                // pass 1: row max over the band
                 float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+                tmem_ld16(s_col, va);
+                tmem_wait_ld();
 #pragma unroll 1
-                for (int q = 0; q < nb; q += 2) {
-                    const bool two = q + 1 < nb;
-                    tmem_ld32(s_col + 32 * q, va);
-                    if (two)
-                        tmem_ld32(s_col + 32 * (q + 1), vb);
+                for (int hq = 0; hq < nh; hq += 2) {
+                    tmem_ld16(s_col + 16 * (hq + 1), vb);
+                    half_max(va, hq, m4);
                     tmem_wait_ld();
-                    chunk_max(va, q, m4);
-                    if (two)
-                        chunk_max(vb, q + 1, m4);
+                    if (hq + 2 < nh)
+                        tmem_ld16(s_col + 16 * (hq + 2), va);
+                    half_max(vb, hq + 1, m4);
+                    if (hq + 2 < nh)
+                        tmem_wait_ld();
                 }
                 tmem_wait_st();
                 const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float mu = (m == NEG_INF) ? 0.f : m;
                 const float2 nmu = make_float2(-mu, -mu);
-                // pass 2: P = exp2(S - max) as bf16 over S (P columns 16q.. overwrite S
-                // columns of chunks already read), row sum
+                // pass 2: P = exp2(S - max) as bf16 over S, row sum
                 float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                tmem_ld16(s_col, va);
+                tmem_wait_ld();
 #pragma unroll 1
-                for (int q = 0; q < nb; q += 2) {
-                    const bool two = q + 1 < nb;
-                    tmem_ld32(s_col + 32 * q, va);
-                    if (two)
-                        tmem_ld32(s_col + 32 * (q + 1), vb);
+                for (int hq = 0; hq < nh; hq += 2) {
+                    tmem_ld16(s_col + 16 * (hq + 1), vb);
+                    half_exp(va, nmu, l2, hq);
                     tmem_wait_ld();
-                    uint32_t pw[16];
-                    chunk_exp(va, nmu, l2, pw);
-                    tmem_st16(s_col + 16 * q, pw);
-                    if (two) {
-                        chunk_exp(vb, nmu, l2, pw);
-                        tmem_st16(s_col + 16 * (q + 1), pw);
-                    }
+                    if (hq + 2 < nh)
+                        tmem_ld16(s_col + 16 * (hq + 2), va);
+                    half_exp(vb, nmu, l2, hq + 1);
+                    if (hq + 2 < nh)
+                        tmem_wait_ld();
                 }
                 const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
                 const float l0 = l4[0] + l4[1], l1 = l4[2] + l4[3];
@@ -524,10 +604,12 @@ __global__ void __launch_bounds__(512, 1)
             }
             gt += n1 - n0;
         }
+        if (range_bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         if (!ok && lane == 0)
             record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
     } else {
-        // ------------------------------------------------------------------ query preparation + epilogue
+        // ------------------------------------------------------------------ query preparation
         const int tid = threadIdx.x - 384;  // 0..127
         const int cr = tid % C::CPR;        // this thread's 16-byte chunk within a query row
         const int row0 = tid / C::CPR;      // first row it prepares; then every RPP-th row

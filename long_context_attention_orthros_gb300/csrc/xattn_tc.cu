@@ -9,8 +9,9 @@
 // lands them (row = copy * G + head).  It streams the keys 0 .. max(pos) of its
 // rows in blocks of 64 through a four-stage ring, each block serving both tiles:
 //   S_t = q_t K^T   (fp16: q rounded once after scale-offset, softmax scale and
-//                    log2(e); K converted from bf16 in shared memory, exact for
-//                    |k| < 65520, otherwise ORTHROS_DEVERR_RANGE), fp32 in TMEM;
+//                    log2(e); K converted from bf16 in shared memory, a key row
+//                    whose largest |k| reaches 65520 scaled by an exact 2^-e_j
+//                    first and its logits multiplied back by 2^e_j), fp32 in TMEM;
 //   online softmax per row with the row's own causal limit (key <= pos), P as
 //   bf16 over S; the running max is raised only when it grows by more than 8 (in
 //   log2 units), so the rescale of O is rare and P stays <= 256 (exact scaling);
@@ -53,7 +54,9 @@ struct XtCfg {
     static constexpr int Q_BYTES = SLABS * Q_SLAB;
     static constexpr int POS_OFF = Q_OFF + 2 * Q_BYTES;   // int [256]: row limits
     static constexpr int RED_OFF = POS_OFF + 256 * 4;     // int [16]: per-warp maxima
-    static constexpr int BAR_OFF = RED_OFF + 16 * 4;
+    static constexpr int KEXP_OFF = RED_OFF + 16 * 4;     // int8 [STAGES][KB]: key row shift e_j
+    static constexpr int KFLAG_OFF = KEXP_OFF + STAGES * KB;  // uint8 [STAGES][8]: converter warp w shifted rows
+    static constexpr int BAR_OFF = KFLAG_OFF + STAGES * 8;
     static constexpr int NBARS = 3 * STAGES + 16;
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *o_final = qfull + 14;          // [tile] O += P V of the last block complete
     int *s_pos = reinterpret_cast<int *>(smem + C::POS_OFF);
     int *s_red = reinterpret_cast<int *>(smem + C::RED_OFF);
+    int8_t *kexp = reinterpret_cast<int8_t *>(smem + C::KEXP_OFF);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_init(&p_full[2 * t + u], 4);
             }
         }
+        for (int s = 0; s < C::STAGES; ++s)
+            reinterpret_cast<uint64_t *>(smem + C::KFLAG_OFF)[s] = 0;
         fence_barrier_init();
     }
     if (warp == 1)
@@ -270,26 +276,51 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive(&qt_full[t]);
             }
         }
+        // K conversion: 8 consecutive lanes per key row (its 16-byte chunk c8 in every slab), the
+        // (row, c8) pairs dealt out cid, cid + 192, cid + 384 (warp-uniform: 192 and 128 are
+        // multiples of 32)
         const int cid = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 384 + 64;  // 0..191
+        const int cw = cid >> 5;                                                // converter warp 0..5
+        constexpr int PAIRS = C::KB * 8;
+        static_assert(C::CONV_THREADS % 32 == 0 && (C::KB * 8) % 32 == 0 && C::CONV_THREADS / 8 == 24,
+                      "rows of a converter warp: (cid / 8) + 24 it");
         for (int j = 0; j < nkb && ok; ++j) {
             const int s = j % C::STAGES;
             if (!(ok = mbar_wait(&full[s], static_cast<uint32_t>((j / C::STAGES) & 1))))
                 break;
             uint8_t *blk = smem + C::K_OFF + s * C::SLABS * C::KSLOT;
-#pragma unroll 4
-            for (int c = cid; c < C::SLABS * C::KSLOT / 16; c += C::CONV_THREADS) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(blk + c * 16);
-                uint4 u = *ptr;
-                uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            // common case: every chunk below 65520 converts as is; when a chunk of the warp's rows
+            // reaches it, the warp shifts those rows instead (rare)
+            constexpr int ITS = (PAIRS + C::CONV_THREADS - 1) / C::CONV_THREADS;
+            const int nrows = cid + (ITS - 1) * C::CONV_THREADS < PAIRS ? ITS : ITS - 1;  // warp-uniform
+            uint4 u[ITS][C::SLABS];
+            uint32_t kept = 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack_bf16x2(w[e]);
-                    bad |= !(fmaxf(fabsf(f.x), fabsf(f.y)) < 65520.f);
-                    __half2 hv = __floats2half2_rn(f.x, f.y);
-                    w[e] = *reinterpret_cast<uint32_t *>(&hv);
+            for (int it = 0; it < ITS; ++it)
+                if (it < nrows) {
+#pragma unroll
+                    for (int sl = 0; sl < C::SLABS; ++sl) {
+                        u[it][sl] = *reinterpret_cast<const uint4 *>(blk + sl * C::KSLOT + ((cid >> 3) + 24 * it) * 128 +
+                                                                     (cid & 7) * 16);
+                        kept |= (bf16x8_absmax(u[it][sl]) < 65520.f ? 0u : 1u) << (it * C::SLABS + sl);
+                    }
                 }
-                *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+            const bool wany = __any_sync(0xffffffffu, kept != 0);
+            if (!wany) {
+#pragma unroll
+                for (int it = 0; it < ITS; ++it)
+                    if (it < nrows) {
+#pragma unroll
+                        for (int sl = 0; sl < C::SLABS; ++sl)
+                            *reinterpret_cast<uint4 *>(blk + sl * C::KSLOT + ((cid >> 3) + 24 * it) * 128 + (cid & 7) * 16) =
+                                k_to_fp16(u[it][sl]);
+                    }
+            } else {
+                shift_key_rows<C::SLABS>(blk, C::KSLOT, 0, cid >> 3, C::CONV_THREADS / 8, nrows, cid & 7,
+                                         kexp + s * C::KB, bad);
             }
+            if (lane == 0)
+                smem[C::KFLAG_OFF + s * 8 + cw] = wany ? 1 : 0;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
@@ -310,9 +341,10 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t o_col = tbase + (static_cast<uint32_t>(rw * 32) << 16) + C::TM_O + D * t;
         const float NEG_INF = -__int_as_float(0x7f800000);
         float m = NEG_INF, l = 0.f;
-        bool ok = true;
+        bool ok = true, range_bad = false;
         for (int j = 0; j < nkb && ok; ++j) {
             const int u = j & 1;
+            const int ks = j % C::STAGES;
             if (!(ok = mbar_wait(&s_full[2 * t + u], static_cast<uint32_t>((j >> 1) & 1))))
                 break;
             tc_fence_after();
@@ -323,7 +355,28 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t va[32], vb[32];
             tmem_ld32(s_col, va);
             tmem_ld32(s_col + 32, vb);
+            // the block's shift flags: its conversion barrier completed before its S was issued, so
+            // this non-blocking test succeeds and orders the flag read after the converters' writes
+            const uint32_t kph = static_cast<uint32_t>((j / C::STAGES) & 1);
+            const bool conv_seen = mbar_test_wait(&kconv[ks], kph);
+            const uint64_t kf = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
             tmem_wait_ld();
+            if (!conv_seen || kf != 0) {
+                if (!(ok = mbar_wait(&kconv[ks], kph)))
+                    break;
+                const uint64_t kf2 = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
+                uint32_t kw = 0;  // one bit per converter warp that shifted rows of this block
+#pragma unroll
+                for (int cw = 0; cw < C::CONV_THREADS / 32; ++cw)
+                    kw |= (((kf2 >> (8 * cw)) & 0xffu) ? 1u : 0u) << cw;
+                if (kw != 0) {  // logits of shifted key rows times 2^e_j (rare), in tensor memory
+                    unshift_chunk32(s_col, kexp + ks * C::KB, 0, kw, 24, 4, range_bad);
+                    unshift_chunk32(s_col + 32, kexp + ks * C::KB, 32, kw, 24, 4, range_bad);
+                    tmem_ld32(s_col, va);
+                    tmem_ld32(s_col + 32, vb);
+                    tmem_wait_ld();
+                }
+            }
             if (!whole) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -439,6 +492,8 @@ __global__ void __launch_bounds__(512, 1)
             for (int c = 0; c < D; c += 8)
                 *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (range_bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
         if (!ok && lane == 0)
             record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
     }

@@ -112,7 +112,11 @@ def test_decode_workspace_size_and_checks(L):
 def test_swa_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 128)
-    assert n == 2 * 4 * 2 * 1000 * 32 + 2 * 2 * 1000 * 8 * 128 + 2 * 2 * 1000 * 32 * 128  # lse, D; fp16 K, q
+    nkb = (1000 + 63) // 64  # 64-key blocks
+    # lse, D; fp16 K; each key row's shift (int8, whole blocks); each block's flag; fp16 q
+    # (every part here is already a multiple of 256 bytes)
+    assert n == (2 * 4 * 2 * 1000 * 32 + 2 * 2 * 1000 * 8 * 128 + 2 * 8 * nkb * 64 + 256 +
+                 2 * 2 * 1000 * 32 * 128)
     assert L.orthros_swa_bwd_workspace_size(2, 1000, 32, 8, 96) == 0
     assert L.orthros_swa_bwd_workspace_size(0, 1000, 32, 8, 128) == 0
 
@@ -128,8 +132,10 @@ def test_swa_bwd_workspace_size_and_checks(L):
 def test_xattn_bwd_workspace_size_and_checks(L):
     p, _keep = _aligned_dummy()
     n = L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 128)
-    # row lse and D, fp16 K, split partials, the copies' fp16 q
-    assert n == 2 * 4 * 4 * 2048 * 32 + 2 * 4 * 16384 * 8 * 128 + 4 * 8 * 64 * 128 * 8 + 2 * 4 * 2048 * 32 * 128
+    # row lse and D, fp16 K, key-row shifts and block flags (16384 keys: 256 blocks), split
+    # partials, the copies' fp16 q
+    assert n == (2 * 4 * 4 * 2048 * 32 + 2 * 4 * 16384 * 8 * 128 + 4 * 8 * 16384 + 4 * 8 * 256 +
+                 4 * 8 * 64 * 128 * 8 + 2 * 4 * 2048 * 32 * 128)
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 0, 32, 8, 128) == 0
     assert L.orthros_xattn_bwd_workspace_size(4, 2048, 16384, 32, 8, 96) == 0
 

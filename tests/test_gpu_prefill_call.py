@@ -60,6 +60,10 @@ def _positions(cfg, seed):
     (3, 5000, 8, 2, 128, 2),    # each stream spread over many CTAs
     (1, 5, 4, 1, 128, 2),       # fewer tiles than SMs
     (2, 1000, 32, 8, 128, 8),   # 32 copy rows per KV head
+    (1, 3000, 16, 2, 128, 1),   # G=8, one copy
+    (2, 4097, 8, 4, 128, 4),    # G=2, 8 copy rows, T off the tile grid
+    (1, 300, 16, 2, 64, 1),     # d=64, G=8
+    (4, 9000, 32, 8, 128, 2),   # 8 copy rows of 8B-class heads, streams over many CTAs
 ])
 def test_prefill_call_parity(B, T, Hq, Hkv, d, T_out):
     cfg = PrefillConfig("call", B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, T_out=T_out)
@@ -93,3 +97,25 @@ def test_prefill_call_bad_position():
                        inp.beta_c, cfg.scale)
     assert_parity(got[:, :1], ref, "valid copy next to bad ones")
     assert torch.equal(o.view(torch.int16), o_swa.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,Hq,Hkv", [(600, 8, 2), (5000, 16, 2)])
+def test_prefill_call_bad_and_early_positions(T, Hq, Hkv):
+    """An out-of-range position gets zeros and the position flag; copies at position 0 and in
+    the first window meet the oracle."""
+    cfg = PrefillConfig("call_bad1", B=2, T=T, Hq=Hq, Hkv=Hkv, d=128, T_out=8 // (Hq // Hkv))
+    inp = make_prefill(cfg, 46 + T)
+    inp.pos[:] = np.array([[0, -1], [T, 37]] if cfg.T_out == 2 else [[-5], [T - 1]], np.int32)
+    o, oc, o_swa, err = _run(inp)
+    assert err & orth.DEVERR_POSITION
+    assert torch.equal(o.view(torch.int16), o_swa.view(torch.int16))
+    got = val(oc)
+    valid = (inp.pos >= 0) & (inp.pos < T)
+    assert (got[~valid] == 0).all()
+    for b in range(cfg.B):
+        for i in range(cfg.T_out):
+            if valid[b, i]:
+                ref = oracle.xattn(np.ascontiguousarray(inp.qc_raw[b:b + 1, i:i + 1]),
+                                   np.ascontiguousarray(inp.pos[b:b + 1, i:i + 1]), inp.k[b:b + 1], inp.v[b:b + 1],
+                                   inp.alpha_c, inp.beta_c, cfg.scale)
+                assert_parity(got[b:b + 1, i:i + 1], ref, f"copy ({b}, {i})")
