@@ -66,7 +66,7 @@ typedef enum {
 #define ORTHROS_DEVERR_POSITION 1   /* a copy position outside [0, T_kv) */
 #define ORTHROS_DEVERR_CACHE_FULL 2 /* decode: cache_len[b] + 1 > L_max */
 #define ORTHROS_DEVERR_TIMEOUT 4    /* an internal pipeline wait gave up after ~2 s (a bug) */
-#define ORTHROS_DEVERR_RANGE 8      /* swa: a key or scaled query outside the fp16 range of QK^T */
+#define ORTHROS_DEVERR_RANGE 8      /* an infinite key, a scaled query (or gradient dS) beyond fp16, or a logit beyond fp32 */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *orthros_status_string(orthros_status s);
@@ -87,9 +87,12 @@ int orthros_version(void);
  * own sequence.  window >= T gives plain causal attention.  Accumulation and
  * softmax are fp32.  q . k is taken with at least 11 significant bits of the
  * scaled query: in fp16 on the tensor-memory path (q rounded once to fp16, K
- * converted exactly from bf16; |k| >= 65520 or a scaled |q| >= 65504 sets
- * ORTHROS_DEVERR_RANGE), or as a bf16 high part plus residual on the path used
- * for windows too wide for tensor memory.  The softmax weights enter P V as
+ * converted from bf16; a key row whose largest |k| reaches 65520 is converted as
+ * k * 2^-e with its largest element in [2^14, 2^15) and its logits multiplied back
+ * by 2^e in fp32, so every finite key is taken; an infinite key, a scaled |q| >=
+ * 65504 or a logit beyond fp32 sets ORTHROS_DEVERR_RANGE), or as a bf16 high part
+ * plus residual on the path used for windows too wide for tensor memory.  The
+ * softmax weights enter P V as
  * bf16; o is rounded to bf16 (nearest even).
  */
 orthros_status orthros_swa_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
@@ -305,9 +308,10 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  *   outputs, every element written (dalpha and dbeta are zeroed first)
  *   workspace: orthros_swa_bwd_workspace_size(...) bytes, 16-byte aligned.
  * Products take fp32 accumulation.  q . k on tensor memory is fp16: K converted
- * exactly from bf16 into the workspace and q rounded once to fp16, as the
- * forward's tensor-memory path (|k| >= 65520 or |q| >= 65504 sets
- * ORTHROS_DEVERR_RANGE); the dq kernel used without lse (warp MMAs) takes q as
+ * from bf16 into the workspace (key rows beyond fp16 shifted by a power of two, as
+ * on the forward's tensor-memory path, with the row shifts kept in the workspace)
+ * and q rounded once to fp16 (|q| >= 65504 sets ORTHROS_DEVERR_RANGE); the dq
+ * kernel used without lse (warp MMAs) takes q as
  * a bf16 high part plus residual.  P is rounded to bf16 before it multiplies
  * dO; dS is rounded to bf16 before it multiplies K (dq) and to fp16 before it
  * multiplies the fp16 q (dk; |dS| >= 65504 sets ORTHROS_DEVERR_RANGE).
