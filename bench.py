@@ -196,9 +196,9 @@ def launches_per_prefill_step(cfg) -> int:
 
 def bwd_launches_per_call(T_out) -> int:
     """Kernels one orthros_attn_bwd call launches with both forwards' log-sum-exp given (mirror of
-    attn_bwd.cuh): fp16 K; the base stream's fp16 q, D, persistent dq and dalpha / dbeta sums;
-    the copies' fp16 q, D and dq; one dk/dv launch for both streams."""
-    return 1 + 4 + (3 if T_out > 0 else 0) + 1
+    attn_bwd.cuh): fp16 K; the base stream's rows pass (fp16 q and D), persistent dq and
+    dalpha / dbeta sums; the copies' rows pass and dq; one dk/dv launch for both streams."""
+    return 1 + 3 + (2 if T_out > 0 else 0) + 1
 
 
 def _events(n):

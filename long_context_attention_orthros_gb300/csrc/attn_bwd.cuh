@@ -12,8 +12,8 @@
 // P - window + 1 .. P (window = T_kv for the copies: keys 0 .. P).
 // Launches (bf16 / fp16 operands, fp32 accumulation, fp32 outputs):
 //   attn_bwd_k16_kernel     an exact fp16 copy of K (for q . k on tensor memory);
-//   attn_bwd_q16_kernel     the scale-offset q of the stream's rows as fp16;
-//   attn_bwd_d_kernel       D = dO . o per row (and a given forward log-sum-exp in log2 units);
+//   attn_bwd_rows_kernel    the scale-offset q of the stream's rows as fp16, D = dO . o per row
+//                           (and a given forward log-sum-exp in log2 units), one pass;
 //   attn_bwd_dq_kernel      (base stream without the forward's log-sum-exp) warp MMAs, rows
 //                           on the MMA's M side: K/V stream through a two-stage shared-memory
 //                           ring of 64-key blocks (cp.async); pass 1 takes each row's
@@ -156,35 +156,6 @@ __device__ __forceinline__ uint4 scale_offset_fp16(uint4 u, const float *alpha, 
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(256) attn_bwd_q16_kernel(const orthros_bf16 *x, const float *alpha,
-                                                           const float *beta, uint16_t *q16, long long n8, int hd8,
-                                                           int32_t *dev_err)
-{
-    bool bad = false;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const int step = static_cast<int>(stride % hd8);
-    long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    int c = static_cast<int>(i % hd8);  // column chunk of chunk i
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
-    uint4 *q4 = reinterpret_cast<uint4 *>(q16);
-    for (; i < n8; i += 2 * stride) {
-        const long long i2 = i + stride;
-        int c2 = c + step;
-        c2 -= c2 >= hd8 ? hd8 : 0;
-        const uint4 u0 = __ldg(x4 + i);
-        uint4 u1 = make_uint4(0u, 0u, 0u, 0u);
-        if (i2 < n8)
-            u1 = __ldg(x4 + i2);
-        q4[i] = scale_offset_fp16(u0, alpha, beta, c * 8, bad);
-        if (i2 < n8)
-            q4[i2] = scale_offset_fp16(u1, alpha, beta, c2 * 8, bad);
-        c = c2 + step;
-        c -= c >= hd8 ? hd8 : 0;
-    }
-    if (bad)
-        record_error(dev_err, ORTHROS_DEVERR_RANGE);
-}
-
 // dalpha[c] += sum_rows x * dq, dbeta[c] += sum_rows dq over the columns c = h * D + d, with
 // dq = dq_raw / alpha (both sums are linear in the rows: one pass after the dq kernel).
 // Each thread owns 4 columns over a run of rows; one atomic per column and CTA.
@@ -224,25 +195,35 @@ __global__ void __launch_bounds__(256) attn_bwd_dab_kernel(const float *dq_raw, 
     atomicAdd(dbeta + c4 + 3, sb.w);
 }
 
-// ------------------------------------------------------------------ D = dO . o
+// ------------------------------------------------------------------ fp16 q and D = dO . o
 
-// D/8 lanes per row, 16-byte loads (two or four rows per warp in flight)
+// One pass over the stream's query rows: q = x alpha + beta as fp16 into the workspace (read by
+// the dK/dV kernel and the persistent dQ; |q| >= 65504 sets ORTHROS_DEVERR_RANGE), D = dO . o
+// per row, and a given forward log-sum-exp in log2 units.  D / 8 lanes per row, 16 bytes of
+// each of x, o and dO per lane, all three loads in flight.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, const orthros_bf16 *dO, float *Dout,
-                                                         const float *lse_in, float *lse_out, long long rows)
+__global__ void __launch_bounds__(256) attn_bwd_rows_kernel(const orthros_bf16 *x, const float *alpha,
+                                                            const float *beta, uint16_t *q16, const orthros_bf16 *o,
+                                                            const orthros_bf16 *dO, float *Dout, const float *lse_in,
+                                                            float *lse_out, long long rows, int Hq, int32_t *dev_err)
 {
     constexpr int LPR = D / 8;  // lanes per row
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / LPR;
     const int sub = threadIdx.x % LPR;
+    bool bad = false;
     float acc = 0.f;
     if (row < rows) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(o + row * D) + sub);
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + row * D) + sub);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        const long long off = row * D + sub * 8;
+        const uint4 xa = __ldg(reinterpret_cast<const uint4 *>(x + off));
+        const uint4 oa = __ldg(reinterpret_cast<const uint4 *>(o + off));
+        const uint4 ga = __ldg(reinterpret_cast<const uint4 *>(dO + off));
+        const int h = static_cast<int>(row % Hq);
+        *reinterpret_cast<uint4 *>(q16 + off) = scale_offset_fp16(xa, alpha + h * D, beta + h * D, sub * 8, bad);
+        const uint32_t aw[4] = {oa.x, oa.y, oa.z, oa.w}, bw[4] = {ga.x, ga.y, ga.z, ga.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 x = unpack_bf16x2(aw[e]), y = unpack_bf16x2(bw[e]);
-            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+            const float2 u = unpack_bf16x2(aw[e]), v = unpack_bf16x2(bw[e]);
+            acc = fmaf(u.x, v.x, fmaf(u.y, v.y, acc));
         }
     }
 #pragma unroll
@@ -253,6 +234,8 @@ __global__ void __launch_bounds__(256) attn_bwd_d_kernel(const orthros_bf16 *o, 
         if (lse_in != nullptr)  // the forward's log-sum-exp, to log2 units
             lse_out[row] = lse_in[row] * kLog2eF;
     }
+    if (bad)
+        record_error(dev_err, ORTHROS_DEVERR_RANGE);
 }
 
 // ------------------------------------------------------------------ dQ (rows on M)
@@ -385,7 +368,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
 #pragma unroll 1
     for (int pass = p.lse_in != nullptr ? 2 : 1; pass <= 2; ++pass) {
         if (pass == 2) {
-            if (p.lse_in != nullptr) {  // converted to log2 units by the D kernel
+            if (p.lse_in != nullptr) {  // converted to log2 units by the rows kernel
                 lseA = vA ? p.lse[rA] : 0.f;
                 lseB = vB ? p.lse[rB] : 0.f;
             } else {
@@ -517,7 +500,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const AttnBwdParams p)
 // shared memory (one TMA load each).  The query rows that can see them stream through
 // a four-stage ring in rounds of 64 (64/G units x G heads, in the order the 4-D TMA box
 // lands them): q as fp16 (the scale-offset applied and rounded once by
-// attn_bwd_q16_kernel, which also flags a query outside the fp16 range) and dO.  Per round
+// attn_bwd_rows_kernel, which also flags a query outside the fp16 range) and dO.  Per round
 //   S^T  = K q^T          (fp16: K from the call's exact fp16 copy)
 //   dP^T = V dO^T         (bf16) fp32 in tensor memory (two buffers each)
 //   P^T  = exp2(S^T c - lse_row) on the row's keys, dS^T = P^T (dP^T - D_row), written
@@ -1224,7 +1207,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         const float c2 = p.scale * kLog2eF;
         const float NEG_INF = -__int_as_float(0x7f800000);
         float m = NEG_INF, l = 0.f;
-        // known beforehand (log2 units): from the forward via the D kernel, or the split combine
+        // known beforehand (log2 units): from the forward via the rows kernel, or the split combine
         float lse = ((p.lse_in != nullptr || mode == 2) && P >= 0) ? p.lse[ri] : 0.f;
         bool kshift_bad = false;
         for (int n = 0; ok && n < nsteps; ++n) {
@@ -1410,7 +1393,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // as in the dq kernel above: S = q K16^T (fp16), dP = dO V^T, dS = P (dP - D) over dP as
 // bf16, dQ += dS K.
 // The query tile arrives as fp16 q = x alpha + beta, made for the whole tensor beforehand
-// (attn_bwd_q16_kernel), and dalpha / dbeta are summed afterwards from dq_raw
+// (attn_bwd_rows_kernel), and dalpha / dbeta are summed afterwards from dq_raw
 // (attn_bwd_dab_kernel): both were measured to pace this kernel when done per tile here
 // (q preparation 7.8 us and the per-head butterfly 14.6 us of a 21 us tile).
 // Roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory allocation and MMA issue;
@@ -1641,7 +1624,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             const bool live = uu < p.n_units;
             const int P = live ? uu : -1, lo = P - p.window + 1;
             const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
-            const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the D kernel converted it)
+            const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the rows kernel converted it)
             const float Drow = live ? p.Drow[ri] : 0.f;
             for (int j = 0; j < nb; ++j, ++n) {
                 const int u = static_cast<int>(n % C::NBUF);
@@ -1792,18 +1775,12 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    // the fp16 scale-offset q: read by the dK/dV kernel and the base stream's persistent dQ
+    // the fp16 scale-offset q (read by the dK/dV kernel and the base stream's persistent dQ),
+    // each row's D and the given log-sum-exp in log2 units: one pass
     const bool persistent = !COPY && p.lse_in != nullptr;  // base dq on tensor memory
     if (rows > 0) {
-        const long long n8 = rows * D / 8;
-        attn_bwd_q16_kernel<<<static_cast<unsigned>(min(n8 / 256 + 1, 152LL * 8)), 256, 0, stream>>>(
-            p.q, p.alpha, p.beta, p.q16, n8, p.Hq * D / 8, p.dev_err);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-    }
-    if (rows > 0) {
-        attn_bwd_d_kernel<D><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
-            p.o, p.dO, p.Drow, p.lse_in, p.lse, rows);
+        attn_bwd_rows_kernel<D><<<static_cast<unsigned>((rows * (D / 8) + 255) / 256), 256, 0, stream>>>(
+            p.q, p.alpha, p.beta, p.q16, p.o, p.dO, p.Drow, p.lse_in, p.lse, rows, p.Hq, p.dev_err);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
         // base rows see at most window + 128/G keys: a tensor-memory CTA (one per SM) spends
