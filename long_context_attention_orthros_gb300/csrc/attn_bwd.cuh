@@ -1724,6 +1724,532 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ base-stream dQ over the key band
+
+// Persistent like the kernel above, but a row tile's whole key band is one MMA wide.  Keys stream
+// through a ring of NSLOT 32-key slots (block kb in load order n sits in slot n % NSLOT); a tile's
+// band (at most NSLOT - 1 blocks, so that the next tile's first new block loads meanwhile) is a
+// run of consecutive loads.  S = q K16^T and dP = dO V^T each take one N = 32 * NSLOT product per
+// K step over the whole ring: columns of slots outside the band are never read.  dS (fp16) is
+// written over dP and dQ = dS K16 runs from tensor memory, 16 keys per K step, over the band's
+// slots only.  The fp16 copy of K holds k * 2^-e for the rare key rows beyond fp16: their logits
+// are scaled back by 2^e in tensor memory and their dS columns by 2^e before the fp16 rounding
+// (|dS 2^e| >= 65504 sets ORTHROS_DEVERR_RANGE).  With FOLD the epilogue also sums
+// dalpha = sum x * dq and dbeta = sum dq over the CTA's rows (lanes of one head reduce-scatter
+// each 32-column chunk, so each lane owns G columns of its head; global atomics when the KV
+// head changes and at the end).
+// Roles (384 threads): warp 0 TMA producer, warp 1 tensor-memory allocation and MMA issue,
+// warps 4-7 dS (lane = row), warps 8-11 the epilogue (the same lanes); warps 2-3 idle.
+// Tensor memory: S at 0, dP (then dS) at N, dQ at 2 N.
+template <int D>
+struct BbCfg {
+    static constexpr int ROWS = 128;
+    static constexpr int KB = 32;                      // keys per slot
+    static constexpr int NSLOT = 6;
+    static constexpr int N = KB * NSLOT;               // S / dP columns
+    static constexpr int SLABS = D / 64;
+    static constexpr int QSLAB = ROWS * 128;
+    static constexpr int SLOT = KB * 128;              // one slot of one 64-column slab
+    static constexpr int RSLAB = NSLOT * SLOT;         // one 64-column slab of a ring
+    static constexpr int QBUF = 2 * SLABS * QSLAB;     // one query buffer: fp16 q, dO
+    static constexpr int Q16_OFF = 0;
+    static constexpr int DO_OFF = SLABS * QSLAB;
+    static constexpr int K16_OFF = 2 * QBUF;           // ring of the fp16 K
+    static constexpr int V_OFF = K16_OFF + SLABS * RSLAB;
+    static constexpr int BAR_OFF = V_OFF + SLABS * RSLAB;
+    static constexpr int NBARS = 2 + 2 + 2 * NSLOT + 4;
+    static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = HOLD_OFF + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t TM_S = 0, TM_DP = N, TM_DQ = 2 * N;
+    static_assert(TM_DQ + D <= 512, "tensor memory budget");
+};
+
+// The band of a CTA's tiles in load order: tiles run in (batch, KV head, row tile) order, so
+// within one (batch, KV head) each tile loads the blocks past the previous tile's band; a new
+// (batch, KV head) loads its whole band.  Every role steps one of these through the same tiles.
+struct BandRun {
+    int bh = -1, hi = -1;
+    long long nh = -1;  // load index of the current band's last block
+    // step to a tile with band blocks lo..hi of sequence bh; returns the first block to load
+    __device__ __forceinline__ int step(int bh_t, int lo, int hi_t)
+    {
+        const int first = (bh_t == bh && hi >= lo) ? hi + 1 : lo;
+        nh += hi_t - first + 1;
+        bh = bh_t;
+        hi = hi_t;
+        return first;
+    }
+};
+
+template <int D, int G, bool FOLD>
+__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
+    attn_bwd_dq_band_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                            const __grid_constant__ CUtensorMap k16map, const __grid_constant__ CUtensorMap vmap,
+                            const AttnBwdParams p)
+{
+    using C = BbCfg<D>;
+    constexpr int UNITS = C::ROWS / G;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *q_full = bars;                     // [2] a tile's fp16 q and dO landed
+    uint64_t *q_free = bars + 2;                 // [2] a tile's S, dP done: the buffer may be reloaded
+    uint64_t *kv_full = bars + 4;                // [NSLOT] block landed
+    uint64_t *kv_empty = kv_full + C::NSLOT;     // [NSLOT] block no longer read
+    uint64_t *s_full = kv_empty + C::NSLOT;      // S, dP of a tile complete
+    uint64_t *p_full = s_full + 1;               // dS written (and S read)
+    uint64_t *dq_final = s_full + 2;             // dQ of a tile complete (dS read)
+    uint64_t *dq_free = s_full + 3;              // dQ read by the epilogue
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::HOLD_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_xt = (p.n_units + UNITS - 1) / UNITS;
+    const long long n_tiles = static_cast<long long>(p.B) * p.Hkv * n_xt;
+    const long long per = (n_tiles + gridDim.x - 1) / gridDim.x;
+    const long long t_begin = blockIdx.x * per, t_end = min(n_tiles, t_begin + per);
+    // tile tau: sequence bh = b * Hkv + g, first unit u0, band blocks lo .. hi
+    auto tile = [&](long long tau, int &bh, int &u0, int &lo, int &hi) {
+        bh = static_cast<int>(tau / n_xt);
+        u0 = static_cast<int>(tau % n_xt) * UNITS;
+        lo = max(0, u0 - p.window + 1) / C::KB;
+        hi = (min(p.n_units, u0 + UNITS) - 1) / C::KB;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(&q_full[qb], 1);
+            mbar_init(&q_free[qb], 1);
+        }
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 4);
+        mbar_init(dq_final, 1);
+        mbar_init(dq_free, 4);
+        fence_barrier_init();
+    }
+    if (warp == 1)
+        tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&omap);
+            tma_prefetch_desc(&k16map);
+            tma_prefetch_desc(&vmap);
+        }
+        BandRun run;
+        long long n = 0;  // blocks loaded so far
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int bh, u0, lo, hi;
+            tile(tau, bh, u0, lo, hi);
+            const int first = run.step(bh, lo, hi);
+            const int b = bh / p.Hkv, g = bh % p.Hkv, qb = static_cast<int>(i & 1);
+            // query buffer qb is free once tile i - 2's S, dP are done
+            if (i >= 2 && !(ok = warp_wait(&q_free[qb], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&q_full[qb], 2 * C::SLABS * C::QSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB, &qmap, &q_full[qb], sl * 64, g * G,
+                                u0, b);
+                    tma_load_4d(smem + qb * C::QBUF + C::DO_OFF + sl * C::QSLAB, &omap, &q_full[qb], sl * 64, g * G,
+                                u0, b);
+                }
+            }
+            for (int kb = first; kb <= hi; ++kb, ++n) {
+                const int slot = static_cast<int>(n % C::NSLOT);
+                // the slot's previous block (load n - NSLOT) is released after the dQ of its last tile
+                if (n >= C::NSLOT &&
+                    !(ok = warp_wait(&kv_empty[slot], static_cast<uint32_t>(((n / C::NSLOT) - 1) & 1))))
+                    break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&kv_full[slot], 2 * C::SLABS * C::SLOT);
+#pragma unroll
+                    for (int sl = 0; sl < C::SLABS; ++sl) {
+                        const int o = sl * C::RSLAB + slot * C::SLOT;
+                        tma_load_4d(smem + C::K16_OFF + o, &k16map, &kv_full[slot], sl * 64, g, kb * C::KB, b);
+                        tma_load_4d(smem + C::V_OFF + o, &vmap, &kv_full[slot], sl * 64, g, kb * C::KB, b);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC_S = umma_idesc(128, C::N, false, false);  // fp16
+        constexpr uint32_t IDESC_DP = umma_idesc(128, C::N, true, false);  // bf16
+        constexpr uint32_t IDESC_DQ = umma_idesc(128, D, false, true);     // fp16 dS, K16 MN-major
+        const uint64_t kdesc = umma_desc_sw128(sbase + C::K16_OFF, 16, 1024);
+        const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF, 16, 1024);
+        BandRun run, ahead;
+        long long n = 0, released = 0;  // blocks whose arrival was awaited; blocks released
+        bool have_next = false;
+        int nbh = 0, nu0 = 0, nlo = 0, nhi = 0;
+        if (t_begin < t_end) {
+            tile(t_begin, nbh, nu0, nlo, nhi);
+            have_next = true;
+        }
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            const int bh = nbh, lo = nlo, hi = nhi;
+            const int first = run.step(bh, lo, hi);
+            const long long nf = run.nh - (hi - lo);  // load index of block lo
+            have_next = tau + 1 < t_end;
+            if (have_next)
+                tile(tau + 1, nbh, nu0, nlo, nhi);
+            const int qb = static_cast<int>(i & 1);
+            if (!(ok = warp_wait(&q_full[qb], static_cast<uint32_t>((i >> 1) & 1))))
+                break;
+            for (int kb = first; ok && kb <= hi; ++kb, ++n)
+                ok = warp_wait(&kv_full[n % C::NSLOT], static_cast<uint32_t>((n / C::NSLOT) & 1));
+            if (!ok)
+                break;
+            const uint64_t qdesc = umma_desc_sw128(sbase + qb * C::QBUF + C::Q16_OFF, 16, 1024);
+            const uint64_t odesc = umma_desc_sw128(sbase + qb * C::QBUF + C::DO_OFF, 16, 1024);
+            if (lane == 0) {  // S over the whole ring (S was read by the dS of tile i - 1)
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::RSLAB + (kk & 3) * 32) >> 4;
+                    umma_ss(tbase + C::TM_S, qdesc + qo, kdesc + ko, IDESC_S, kk != 0);
+                }
+            }
+            __syncwarp();
+            // dP overwrites the columns where tile i - 1's dS was read by its dQ
+            if (i >= 1 && !(ok = warp_wait(dq_final, static_cast<uint32_t>((i - 1) & 1))))
+                break;
+            if (lane == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = static_cast<uint32_t>((kk >> 2) * C::QSLAB + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = static_cast<uint32_t>((kk >> 2) * C::RSLAB + (kk & 3) * 32) >> 4;
+                    umma_ss(tbase + C::TM_DP, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
+                }
+                umma_commit(s_full);
+                umma_commit(&q_free[qb]);
+            }
+            __syncwarp();
+            // dQ is free once the epilogue has read tile i - 1's; dS of this tile written
+            if ((i >= 1 && !(ok = warp_wait(dq_free, static_cast<uint32_t>((i - 1) & 1)))) ||
+                !(ok = warp_wait(p_full, static_cast<uint32_t>(i & 1))))
+                break;
+            if (lane == 0) {
+                tc_fence_after();
+                for (int kb = lo; kb <= hi; ++kb) {
+                    const int j = static_cast<int>((nf + (kb - lo)) % C::NSLOT);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t bdesc =
+                            umma_desc_sw128(sbase + C::K16_OFF + j * C::SLOT + h * 2048, C::RSLAB, 1024);
+                        umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + 16 * j + 8 * h, bdesc, IDESC_DQ,
+                                (kb > lo || h > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(dq_final);
+            }
+            __syncwarp();
+            // blocks the next tile's band does not hold are free once this dQ is done
+            if (have_next) {
+                ahead = run;
+                ahead.step(nbh, nlo, nhi);
+                const long long next_first = ahead.nh - (nhi - nlo);
+                if (lane == 0)
+                    for (long long m = released; m < next_first; ++m)
+                        umma_commit(&kv_empty[m % C::NSLOT]);
+                __syncwarp();
+                if (next_first > released)
+                    released = next_first;
+            }
+        }
+    } else if (warp < 4) {
+        // warps 2-3: no role
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------ dS (lane = row)
+        const int rw = warp - 4;
+        const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        const float c2 = p.scale * kLog2eF;
+        float ds_max = 0.f;  // dS goes to fp16
+        bool kshift_bad = false;
+        BandRun run;
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            int bh, u0, lo, hi;
+            tile(tau, bh, u0, lo, hi);
+            run.step(bh, lo, hi);
+            const int s0 = static_cast<int>((run.nh - (hi - lo)) % C::NSLOT);  // slot of block lo
+            const int b = bh / p.Hkv, g = bh % p.Hkv;
+            const int uu = u0 + r / G, h = g * G + r % G;
+            const bool live = uu < p.n_units;
+            const int P = live ? uu : -1, klo = P - p.window + 1;
+            const long long ri = (static_cast<long long>(b) * p.n_units + uu) * p.Hq + h;
+            const float lse = live ? p.lse[ri] : 0.f;  // log2 units (the rows kernel converted it)
+            const float Drow = live ? p.Drow[ri] : 0.f;
+            const int8_t *ke = p.kexp + static_cast<long long>(bh) * p.nkb * 64;
+            const uint8_t *kf = p.kflag + static_cast<long long>(bh) * p.nkb;
+            // band blocks holding key rows beyond fp16 (rare): one bit per slot
+            uint32_t shifted = 0;
+            for (int kb = lo; kb <= hi; ++kb)
+                if (kf[kb >> 1] != 0)
+                    shifted |= 1u << ((s0 + kb - lo) % C::NSLOT);
+            // the band's slots (slot s0 + d holds block lo + d); the others are stale or loading
+            uint32_t band = 0;
+            for (int d = 0; d <= hi - lo; ++d)
+                band |= 1u << ((s0 + d) % C::NSLOT);
+            if (!(ok = warp_wait(s_full, static_cast<uint32_t>(i & 1))))
+                break;
+            tc_fence_after();
+            for (uint32_t m = shifted; m != 0; m &= m - 1) {  // rare: logits of shifted key rows times 2^e
+                const int j = __ffs(m) - 1;
+                unshift_chunk32(tl + C::TM_S + 32 * j, ke, (lo + (j - s0 + C::NSLOT) % C::NSLOT) * C::KB, 1u, 1, 1,
+                                kshift_bad);
+            }
+            // the band's slots in slot order, the next slot's S and dP loads in flight while this
+            // one is computed (a tensor-memory load takes several hundred cycles to land); dS of
+            // slot j goes over dP columns 16 j .. 16 j + 15, below every column still to be read
+            int j = __ffs(band) - 1;
+            uint32_t sa[32], da[32];
+            tmem_ld32(tl + C::TM_S + 32 * j, sa);
+            tmem_ld32(tl + C::TM_DP + 32 * j, da);
+#pragma unroll 1
+            while (true) {
+                tmem_wait_ld();
+                uint32_t sv[32], dv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    sv[e] = sa[e];
+                    dv[e] = da[e];
+                }
+                const uint32_t rest = band & ~((2u << j) - 1u);
+                const int jn = rest != 0 ? __ffs(rest) - 1 : -1;
+                if (jn >= 0) {
+                    tmem_ld32(tl + C::TM_S + 32 * jn, sa);
+                    tmem_ld32(tl + C::TM_DP + 32 * jn, da);
+                }
+                const int key0 = (lo + (j - s0 + C::NSLOT) % C::NSLOT) * C::KB;
+                const bool fl = (shifted >> j) & 1u;
+                uint32_t dw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int key = key0 + 2 * e + q;
+                        const bool valid = key <= P && key >= klo;
+                        const float pr = fast_exp2(__uint_as_float(sv[2 * e + q]) * c2 - lse);
+                        ds[q] = valid ? pr * (__uint_as_float(dv[2 * e + q]) - Drow) : 0.f;
+                    }
+                    if (fl) {  // dQ takes K16 = k 2^-e: dS times 2^e
+                        ds[0] *= exp2i(ke[key0 + 2 * e]);
+                        ds[1] *= exp2i(ke[key0 + 2 * e + 1]);
+                    }
+                    ds_max = fmaxf(ds_max, fmaxf(fabsf(ds[0]), fabsf(ds[1])));
+                    __half2 hv = __floats2half2_rn(ds[0], ds[1]);
+                    dw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                tmem_st16(tl + C::TM_DP + 16 * j, dw);
+                if (jn < 0)
+                    break;
+                j = jn;
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(p_full);
+        }
+        if (!(ds_max < 65504.f) || kshift_bad)
+            record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
+    } else {
+        // ------------------------------------------------------------------ epilogue (warps 8-11)
+        // dq_raw = scale dQ alpha; with FOLD also dalpha += x dq, dbeta += dq (dq = scale dQ).
+        // x is read one 16-column piece ahead (G = 4; G = 8 has the registers for one piece only),
+        // and the next tile's rows are prefetched into L2 while this tile is stored.
+        const int rw = warp - 8;
+        const int r = rw * 32 + lane;
+        const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        constexpr int NCH = D / 32;
+        constexpr int OWN = FOLD ? G / 2 : 1;  // columns a lane owns per 16-column half after the reduce-scatter
+        constexpr bool AHEAD = G == 4;
+        float acc_a[FOLD ? NCH : 1][2][OWN], acc_b[FOLD ? NCH : 1][2][OWN];
+        int cur_g = -1;
+        // lane's columns: chunk c, half hh: 32 c + 16 hh + (lane / G) OWN + e; head lane % G
+        auto flush = [&](int gg) {
+            if (FOLD && gg >= 0) {
+                const int col0 = (gg * G + lane % G) * D + (lane / G) * OWN;
+#pragma unroll
+                for (int c = 0; c < (FOLD ? NCH : 1); ++c)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int e = 0; e < OWN; ++e) {
+                            atomicAdd(p.dalpha + col0 + 32 * c + 16 * hh + e, acc_a[c][hh][e]);
+                            atomicAdd(p.dbeta + col0 + 32 * c + 16 * hh + e, acc_b[c][hh][e]);
+                        }
+            }
+        };
+        auto row_off = [&](long long t, bool &lv, int &hd) {
+            int bh, u0, lo, hi;
+            tile(t, bh, u0, lo, hi);
+            const int uu = u0 + r / G;
+            hd = (bh % p.Hkv) * G + r % G;
+            lv = uu < p.n_units;
+            return ((static_cast<long long>(bh / p.Hkv) * p.n_units + uu) * p.Hq + hd) * D;
+        };
+        auto load_x = [&](long long off, bool lv, int c, uint4 (&xr)[2]) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                xr[e] = lv ? __ldg(reinterpret_cast<const uint4 *>(p.q + off + c) + e) : make_uint4(0u, 0u, 0u, 0u);
+        };
+        for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
+            const int g = static_cast<int>((tau / ((p.n_units + UNITS - 1) / UNITS)) % p.Hkv);
+            if (FOLD && g != cur_g) {
+                flush(cur_g);
+#pragma unroll
+                for (int c = 0; c < (FOLD ? NCH : 1); ++c)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int e = 0; e < OWN; ++e)
+                            acc_a[c][hh][e] = acc_b[c][hh][e] = 0.f;
+                cur_g = g;
+            }
+            bool live;
+            int h;
+            const long long off = row_off(tau, live, h);
+            uint4 xn[2];
+            if (FOLD && AHEAD)
+                load_x(off, live, 0, xn);
+            if (FOLD && tau + 1 < t_end) {  // the next tile's row of x into L2
+                bool lv;
+                int hd;
+                const long long on = row_off(tau + 1, lv, hd);
+                if (lv) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + on));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + on + 64));
+                }
+            }
+            if (!(ok = warp_wait(dq_final, static_cast<uint32_t>(i & 1))))
+                break;
+            tc_fence_after();
+            // 16-column pieces of dQ, the next piece's load in flight while this one is stored
+            uint32_t wa[16];
+            tmem_ld16(tl + C::TM_DQ, wa);
+            const float sc = p.scale;
+#pragma unroll
+            for (int pc = 0; pc < D / 16; ++pc) {
+                const int c = 16 * pc;
+                uint4 xr[2];
+                if (FOLD) {
+                    if (AHEAD) {
+                        xr[0] = xn[0];
+                        xr[1] = xn[1];
+                        if (c + 16 < D)
+                            load_x(off, live, c + 16, xn);
+                    } else {
+                        load_x(off, live, c, xr);
+                    }
+                }
+                tmem_wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = wa[e];
+                if (c + 16 < D)
+                    tmem_ld16(tl + C::TM_DQ + c + 16, wa);
+                if (live) {  // dq_raw = scale dQ alpha, whole 32-byte sectors per store
+#pragma unroll
+                    for (int e = 0; e < 16; e += 8) {
+                        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
+                        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e + 4));
+                        st_global_v8(p.dq + off + c + e,
+                                     make_uint4(__float_as_uint(__uint_as_float(w[e]) * sc * a0.x),
+                                                __float_as_uint(__uint_as_float(w[e + 1]) * sc * a0.y),
+                                                __float_as_uint(__uint_as_float(w[e + 2]) * sc * a0.z),
+                                                __float_as_uint(__uint_as_float(w[e + 3]) * sc * a0.w)),
+                                     make_uint4(__float_as_uint(__uint_as_float(w[e + 4]) * sc * a1.x),
+                                                __float_as_uint(__uint_as_float(w[e + 5]) * sc * a1.y),
+                                                __float_as_uint(__uint_as_float(w[e + 6]) * sc * a1.z),
+                                                __float_as_uint(__uint_as_float(w[e + 7]) * sc * a1.w)));
+                    }
+                }
+                if (FOLD) {
+                    float va[16], vb[16];
+                    const uint32_t xw[8] = {xr[0].x, xr[0].y, xr[0].z, xr[0].w, xr[1].x, xr[1].y, xr[1].z, xr[1].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 xv = unpack_bf16x2(xw[e]);
+                        const float d0 = live ? __uint_as_float(w[2 * e]) * sc : 0.f;
+                        const float d1 = live ? __uint_as_float(w[2 * e + 1]) * sc : 0.f;
+                        vb[2 * e] = d0;
+                        vb[2 * e + 1] = d1;
+                        va[2 * e] = xv.x * d0;
+                        va[2 * e + 1] = xv.y * d1;
+                    }
+                    // reduce-scatter over the 32 / G lanes of this head: halve the vector per step
+#pragma unroll
+                    for (int st = 0; (16 >> st) >= G; ++st) {
+                        const int m = 16 >> st, half = 8 >> st;
+                        const bool up = (lane & m) != 0;
+#pragma unroll
+                        for (int e = 0; e < half; ++e) {
+                            const float sa = up ? va[e] : va[e + half], ka = up ? va[e + half] : va[e];
+                            const float sb = up ? vb[e] : vb[e + half], kb2 = up ? vb[e + half] : vb[e];
+                            va[e] = ka + __shfl_xor_sync(0xffffffffu, sa, m);
+                            vb[e] = kb2 + __shfl_xor_sync(0xffffffffu, sb, m);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < OWN; ++e) {
+                        acc_a[FOLD ? pc / 2 : 0][pc % 2][e] += va[e];
+                        acc_b[FOLD ? pc / 2 : 0][pc % 2][e] += vb[e];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(dq_free);  // this warp's lanes of dQ are read
+        }
+        if (ok)
+            flush(cur_g);
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// the band kernel's limits: G >= 4 (a 128-row tile spans at most 32 units) and every tile's band
+// within NSLOT - 1 slots
+__host__ inline bool dq_band_fits(int G, int window)
+{
+    if (G < 4)
+        return false;
+    const int units = 128 / G, kb = BbCfg<128>::KB;
+    int most = 0;
+    for (int a = 0; a < kb; a += units) {  // tile starts u0 = a (mod 32), far from the sequence start
+        const int u0 = 1 << 20 | a;
+        most = max(most, (u0 + units - 1) / kb - (u0 - window + 1) / kb + 1);
+    }
+    return most <= BbCfg<128>::NSLOT - 1;
+}
+
 // ------------------------------------------------------------------ split log-sum-exp
 
 // rows of the single row tile of each (batch, KV head): merge the splits' (max, sum) into
@@ -1755,6 +2281,20 @@ __global__ void __launch_bounds__(128) attn_bwd_lse_combine_kernel(const AttnBwd
 static size_t dq_smem(int D, int G)
 {
     return static_cast<size_t>(4) * (D / 64) * BWD_KEYS * 128 + 2 * G * D * 4 + 16 + 1024;
+}
+
+// dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]: 4 columns per
+// thread, runs of token rows per CTA
+static cudaError_t launch_dab(const AttnBwdParams &p, int D, int sms, cudaStream_t stream)
+{
+    const long long trows = static_cast<long long>(p.B) * p.n_units;
+    const int cols = p.Hq * D;
+    const unsigned gx = static_cast<unsigned>((cols / 4 + 255) / 256);
+    const long long gy_t = (2LL * sms * 4 + gx - 1) / gx, gy = trows < gy_t ? trows : gy_t;
+    const int per = static_cast<int>((trows + gy - 1) / gy);
+    attn_bwd_dab_kernel<<<dim3(gx, static_cast<unsigned>((trows + per - 1) / per)), 256, 0, stream>>>(
+        p.dq, p.q, p.alpha, p.dalpha, p.dbeta, trows, cols, per);
+    return cudaGetLastError();
 }
 
 // One stream's launches before dK/dV: zeroed dalpha / dbeta, the fp16 copy of K (unless another
@@ -1828,6 +2368,30 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
             } else {
                 k1<<<g1, DKV_TC_THREADS, s1, stream>>>(maps[4], maps[5], maps[6], maps[7], maps[8], p);
             }
+        } else if (persistent && G >= 4 && dq_band_fits(G, p.window)) {
+            // base stream with the forward's log-sum-exp, each tile's key band one MMA wide; for
+            // G <= 8 the dalpha / dbeta sums come out of its epilogue
+            if constexpr (G >= 4) {
+                constexpr bool FOLD = G <= 8;
+                const size_t s1 = BbCfg<D>::SMEM;
+                auto k1 = attn_bwd_dq_band_kernel<D, G, FOLD>;
+                if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(s1))) != cudaSuccess)
+                    return e;
+                int dev = 0, sms = 0;
+                if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+                    (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                    return e;
+                constexpr int UNITS = BbCfg<D>::ROWS / G;
+                const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
+                k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
+                    maps[9], maps[5], maps[10], maps[11], p);
+                if (!FOLD) {
+                    if ((e = cudaGetLastError()) != cudaSuccess)
+                        return e;
+                    e = launch_dab(p, D, sms, stream);
+                }
+            }
         } else if (persistent) {
             // base stream with the forward's log-sum-exp: the persistent tensor-memory kernel
             const size_t s1 = BpCfg<D>::SMEM;
@@ -1845,15 +2409,7 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
                 maps[9], maps[5], maps[6], maps[7], maps[8], p);
             if ((e = cudaGetLastError()) != cudaSuccess)
                 return e;
-            // dalpha, dbeta from dq_raw and x, [B * n_units token rows] x [Hq * D columns]:
-            // 4 columns per thread, runs of token rows per CTA
-            const long long trows = static_cast<long long>(p.B) * p.n_units;
-            const int cols = p.Hq * D;
-            const unsigned gx = static_cast<unsigned>((cols / 4 + 255) / 256);
-            const long long gy_t = (2LL * sms * 4 + gx - 1) / gx, gy = trows < gy_t ? trows : gy_t;
-            const int per = static_cast<int>((trows + gy - 1) / gy);
-            attn_bwd_dab_kernel<<<dim3(gx, static_cast<unsigned>((trows + per - 1) / per)), 256, 0, stream>>>(
-                p.dq, p.q, p.alpha, p.dalpha, p.dbeta, trows, cols, per);
+            e = launch_dab(p, D, sms, stream);
         } else {
             const size_t s1 = dq_smem(D, G);
             auto k1 = attn_bwd_dq_kernel<D, G, COPY>;
@@ -1864,7 +2420,9 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
             dim3 g1((p.n_units + UNITS - 1) / UNITS, p.B * p.Hkv);
             k1<<<g1, 128, s1, stream>>>(p);
         }
-        if ((e = cudaGetLastError()) != cudaSuccess)
+        if (e == cudaSuccess)
+            e = cudaGetLastError();
+        if (e != cudaSuccess)
             return e;
     }
     return cudaSuccess;

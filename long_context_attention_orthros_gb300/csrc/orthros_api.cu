@@ -87,8 +87,8 @@ const float kLog2e = 1.4426950408889634f;
 
 // tensor maps of the gradient's kernels: for dK/dV, the fp16 q and dO in rounds of 64 rows
 // (64/G units x G heads), V and the fp16 K in blocks of 128 keys; for dQ, raw q and dO in
-// tiles of 128 rows, K, V and the fp16 K in blocks of 64 keys, and the fp16 q in tiles of 128
-// rows (the base stream's persistent dQ)
+// tiles of 128 rows, K, V and the fp16 K in blocks of 64 keys, the fp16 q in tiles of 128
+// rows (the base stream's persistent dQ), and the fp16 K and V in blocks of 32 keys (its band)
 bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16,
               const void *q16, int d, int Hq, int Hkv, int n_units, int T_kv, int B)
 {
@@ -100,7 +100,8 @@ bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, cons
            make_map(&m[4], q, d, Hq, n_units, B, qs, G, 128 / G) &&
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
            make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 64) &&
-           make_map(&m[9], q16, d, Hq, n_units, B, qs, G, 128 / G);
+           make_map(&m[9], q16, d, Hq, n_units, B, qs, G, 128 / G) &&
+           make_map(&m[10], k16, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32);
 }
 
 }  // namespace

@@ -54,6 +54,12 @@ def test_forward_lse_matches_oracle(B, T, Hq, Hkv, d, w):
     (1, 640, 8, 2, 128, 600),
     (2, 4000, 16, 4, 128, 128),  # 1000 row tiles: each persistent CTA walks several
     (1, 3000, 32, 8, 64, 128),   # d=64, 752 row tiles, ragged last tile
+    (1, 1000, 16, 1, 128, 128),  # G=16: band dq, dalpha / dbeta in their own pass
+    (1, 700, 8, 2, 128, 129),    # G=4, the widest window whose band fits the key ring
+    (1, 700, 8, 2, 128, 130),    # one key wider: 64-key blocks
+    (1, 600, 4, 2, 128, 128),    # G=2: 64-key blocks
+    (2, 333, 8, 1, 64, 50),      # G=8, d=64, narrow window
+    (3, 2000, 8, 2, 128, 97),    # three sequences per KV head group over the CTAs' tile runs
 ])
 def test_gradient_with_forward_lse(B, T, Hq, Hkv, d, w):
     q, k, v, a, b, dO = _inputs(3000 + T, B, T, Hq, Hkv, d)
