@@ -194,11 +194,16 @@ def launches_per_prefill_step(cfg) -> int:
     return 2 + (0 if splits * wk == 1 else 1)
 
 
-def bwd_launches_per_call(T_out) -> int:
+def bwd_launches_per_call(T_out, G, window) -> int:
     """Kernels one orthros_attn_bwd call launches with both forwards' log-sum-exp given (mirror of
-    attn_bwd.cuh): fp16 K; the base stream's rows pass (fp16 q and D), persistent dq and
-    dalpha / dbeta sums; the copies' rows pass and dq; one dk/dv launch for both streams."""
-    return 1 + 3 + (2 if T_out > 0 else 0) + 1
+    attn_bwd.cuh): fp16 K; the base stream's rows pass (fp16 q and D) and dq (the key-band kernel
+    sums dalpha / dbeta in its epilogue for G = 4, 8 when the band fits five 32-key slots, else a
+    separate pass sums them); the copies' rows pass and dq; one dk/dv launch for both streams."""
+    units = 128 // G if G >= 4 else 0
+    band = units > 0 and max(((1 << 20) + a + units - 1) // 32 - ((1 << 20) + a - window + 1) // 32 + 1
+                             for a in range(0, 32, units)) <= 5
+    base = 2 if band and G <= 8 else 3
+    return 1 + base + (2 if T_out > 0 else 0) + 1
 
 
 def _events(n):
@@ -502,7 +507,7 @@ def run_gradient(dev, world, g, o, oc, cfg, peaks, calls: int = 5):
     ms = allreduce_max(e0.elapsed_time(e1) / calls, world)
     assert all(bool(torch.isfinite(t).all()) for t in grads)
     del grads, dO, dOc, ws, lse, lsec, q
-    per_call = bwd_launches_per_call(T_out)
+    per_call = bwd_launches_per_call(T_out, Hq // Hkv, cfg.window)
     # algorithmic bytes: q_raw, o, dO (bf16) and each row's log-sum-exp read, K and V read, fp32
     # dq, dk, dv written, once each (both streams); dalpha / dbeta are [Hq, d]
     rows = B * (T + T_out) * Hq
