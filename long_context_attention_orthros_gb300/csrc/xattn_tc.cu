@@ -7,8 +7,10 @@
 // A CTA owns 256 copy rows of one (batch, KV head): tiles A and B of 128 rows =
 // 128 / G copies x the G query heads of the KV head, in the order a 4-D TMA box
 // lands them (row = copy * G + head).  It streams the keys 0 .. max(pos) of its
-// rows in blocks of 64 through a four-stage ring, each block serving both tiles:
-//   S_t = q_t K^T   (fp16: q rounded once after scale-offset, softmax scale and
+// rows in blocks of 64 through a four-stage ring (slab-major, so the two slots of
+// a pair are adjacent), each pair of blocks serving both tiles:
+//   S_t = q_t K^T   (one N = 128 product per K step over the pair's 128 keys;
+//                    fp16: q rounded once after scale-offset, softmax scale and
 //                    log2(e); K converted from bf16 in shared memory, a key row
 //                    whose largest |k| reaches 65520 scaled by an exact 2^-e_j
 //                    first and its logits multiplied back by 2^e_j), fp32 in TMEM;
@@ -16,10 +18,13 @@
 //   bf16 over S; the running max is raised only when it grows by more than 8 (in
 //   log2 units), so the rescale of O is rare and P stays <= 256 (exact scaling);
 //   O_t += P V      (bf16, fp32 accumulation in TMEM);
-// and finally o' = O / l rounded to bf16.  Each tile has two S buffers, so the
-// MMA issuer computes S of block j + 1 while the softmax works on block j, and
-// O += P V of block j runs while the softmax moves on to block j + 1.  Rows whose position is outside
-// [0, T_kv) get zeros and ORTHROS_DEVERR_POSITION.
+// and finally o' = O / l rounded to bf16.  Each tile has one 128-column S buffer;
+// the two tiles take turns on the tensor pipe (S_A, S_B, then per pair P V of A,
+// S_A of the next pair, P V of B, S_B of the next pair), so one tile's MMAs run
+// while the other's softmax works.  The softmax takes a pair as two 64-column
+// halves; when the second half raises the running max, the first half's P is
+// rescaled in place.  Rows whose position is outside [0, T_kv) get zeros and
+// ORTHROS_DEVERR_POSITION.
 //
 // Roles (512 threads, one CTA per SM):
 //   warp 0        TMA producer: the two raw query tiles, K/V blocks
@@ -28,7 +33,7 @@
 //   warps 4-7     softmax and epilogue of tile A (TMEM lanes = rows)
 //   warps 8-11    the same for tile B
 //   warps 12-15   query preparation of both tiles, then K conversion
-// Tensor memory: S of tile t, buffer u at 128 t + 64 u; O_A at 256, O_B at 256 + D.
+// Tensor memory: S of tile t at 128 t; O_A at 256, O_B at 256 + D.
 // Every mbarrier wait is bounded; a timeout records ORTHROS_DEVERR_TIMEOUT and
 // all roles drain to the common exit, where tensor memory is released.
 #include <cuda_fp16.h>
@@ -46,10 +51,10 @@ struct XtCfg {
     static constexpr int SLABS = D / 64;
     static constexpr int STAGES = 4;
     static constexpr int KSLOT = KB * 128;     // one 64-wide slab of one block
-    static constexpr int STAGE_SLABS = STAGES * SLABS;
+    static constexpr int SLAB_STRIDE = STAGES * KSLOT;  // slab-major ring: a slab holds every slot
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + STAGE_SLABS * KSLOT;
-    static constexpr int Q_OFF = V_OFF + STAGE_SLABS * KSLOT;
+    static constexpr int V_OFF = K_OFF + SLABS * SLAB_STRIDE;
+    static constexpr int Q_OFF = V_OFF + SLABS * SLAB_STRIDE;
     static constexpr int Q_SLAB = ROWS * 128;
     static constexpr int Q_BYTES = SLABS * Q_SLAB;
     static constexpr int POS_OFF = Q_OFF + 2 * Q_BYTES;   // int [256]: row limits
@@ -61,7 +66,7 @@ struct XtCfg {
     static constexpr int HOLD_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = HOLD_OFF + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t TM_S = 0;        // + 128 * tile + 64 * buffer
+    static constexpr uint32_t TM_S = 0;        // + 128 * tile
     static constexpr uint32_t TM_O = 256;      // + D * tile
     static constexpr int CPR = D / 8;          // 16-byte chunks per query row
     static constexpr int RPP = 128 / CPR;      // rows one pass of 128 threads covers
@@ -85,10 +90,10 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *empty = bars + 2 * C::STAGES;  // [STAGES] block released (MMA commit)
     uint64_t *qfull = bars + 3 * C::STAGES;  // [2] raw query tile landed
     uint64_t *qt_full = qfull + 2;           // [2] query tile prepared
-    uint64_t *s_full = qfull + 4;            // [tile][buffer] S of a block complete
-    uint64_t *p_full = qfull + 8;            // [tile][buffer] P written (and O rescaled if needed)
-    uint64_t *o_done = qfull + 12;           // [tile] O += P V of a block complete (one phase per block)
-    uint64_t *o_final = qfull + 14;          // [tile] O += P V of the last block complete
+    uint64_t *s_full = qfull + 4;            // [tile] S of a pair of blocks complete
+    uint64_t *p_full = qfull + 8;            // [tile] P written (and O rescaled if needed)
+    uint64_t *o_done = qfull + 12;           // [tile] O += P V of a pair complete (one phase per pair)
+    uint64_t *o_final = qfull + 14;          // [tile] O += P V of the last pair complete
     int *s_pos = reinterpret_cast<int *>(smem + C::POS_OFF);
     int *s_red = reinterpret_cast<int *>(smem + C::RED_OFF);
     int8_t *kexp = reinterpret_cast<int8_t *>(smem + C::KEXP_OFF);
@@ -127,10 +132,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&qt_full[t], 4);
             mbar_init(&o_done[t], 1);
             mbar_init(&o_final[t], 1);
-            for (int u = 0; u < 2; ++u) {
-                mbar_init(&s_full[2 * t + u], 1);
-                mbar_init(&p_full[2 * t + u], 4);
-            }
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 4);
         }
         for (int s = 0; s < C::STAGES; ++s)
             reinterpret_cast<uint64_t *>(smem + C::KFLAG_OFF)[s] = 0;
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int w = 0; w < 8; ++w)
         kmax = max(kmax, s_red[w]);
     const int nkb = kmax < 0 ? 0 : kmax / C::KB + 1;  // key blocks of this CTA
+    const int npair = (nkb + 1) / 2;                   // pairs of blocks: one S product each
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(512, 1)
                     tma_load_4d(smem + C::Q_OFF + t * C::Q_BYTES + sl * C::Q_SLAB, &qmap, &qfull[t], sl * 64, g * G,
                                 (row_base + t * 128) / G, b);
             }
-            for (int j = 0; j < nkb; ++j) {
+            for (int j = 0; j < 2 * npair; ++j) {
                 const int s = j % C::STAGES;
                 if (j >= C::STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>(((j / C::STAGES) - 1) & 1))) {
                     record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
@@ -170,61 +174,68 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive_expect_tx(&full[s], 2 * C::SLABS * C::KSLOT);
 #pragma unroll
                 for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + C::K_OFF + (s * C::SLABS + sl) * C::KSLOT, &kmap, &full[s], sl * 64, g,
+                    tma_load_4d(smem + C::K_OFF + sl * C::SLAB_STRIDE + s * C::KSLOT, &kmap, &full[s], sl * 64, g,
                                 j * C::KB, b);
-                    tma_load_4d(smem + C::V_OFF + (s * C::SLABS + sl) * C::KSLOT, &vmap, &full[s], sl * 64, g,
+                    tma_load_4d(smem + C::V_OFF + sl * C::SLAB_STRIDE + s * C::KSLOT, &vmap, &full[s], sl * 64, g,
                                 j * C::KB, b);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nkb > 0) {
-            constexpr uint32_t IDESC_QK = umma_idesc(128, C::KB, false, false);
+        // Pair pp = key blocks 2 pp, 2 pp + 1 (ring slots 2 pp mod 4 and the next one, adjacent in
+        // every slab): S_t = q_t K^T is one N = 128 product per K step into tile t's single S
+        // buffer, and O_t += P V eight K steps of 16 keys.  Order S_A(0) S_B(0), then per pair
+        // PV_A(pp) S_A(pp+1) PV_B(pp) S_B(pp+1): S_t(pp+1) overwrites the P that PV_t(pp) reads,
+        // so it waits for that PV to complete, while the other tile's work keeps the pipe busy.
+        if (lane == 0 && npair > 0) {
+            constexpr uint32_t IDESC_QK = umma_idesc(128, 2 * C::KB, false, false);
             constexpr uint32_t IDESC_PV = umma_idesc(128, D, true, true);
             bool ok = mbar_wait(&qt_full[0], 0) && mbar_wait(&qt_full[1], 0);
-            // pass j: S of block j (both tiles), then O += P V of block j - 1
-            for (int j = 0; j <= nkb && ok; ++j) {
-                if (j < nkb) {
-                    const int s = j % C::STAGES;
-                    const uint32_t ph = static_cast<uint32_t>((j / C::STAGES) & 1);
-                    if (!(ok = mbar_wait(&full[s], ph) && mbar_wait(&kconv[s], ph)))
-                        break;
-                    const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + s * C::SLABS * C::KSLOT, 16, 1024);
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        // S buffer j & 1 is free once O += P V of block j - 2 has read it
-                        if (j >= 2 && !(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 2) & 1))))
-                            break;
-                        tc_fence_after();
-                        const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
-                        const uint32_t s_tm = tbase + C::TM_S + 128 * t + 64 * (j & 1);
+            auto issue_s = [&](int t, int pp) -> bool {
+                const int s0 = (2 * pp) % C::STAGES;
+                const uint32_t ph = static_cast<uint32_t>(((2 * pp) / C::STAGES) & 1);
+                if (t == 0)  // the pair's blocks landed and converted
+                    for (int h = 0; h < 2; ++h)
+                        if (!(mbar_wait(&full[s0 + h], ph) && mbar_wait(&kconv[s0 + h], ph)))
+                            return false;
+                if (pp >= 1 && !mbar_wait(&o_done[t], static_cast<uint32_t>((pp - 1) & 1)))
+                    return false;
+                tc_fence_after();
+                const uint64_t kdesc = umma_desc_sw128(sbase + C::K_OFF + s0 * C::KSLOT, 16, 1024);
+                const uint64_t qdesc = umma_desc_sw128(sbase + C::Q_OFF + t * C::Q_BYTES, 16, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::KSLOT + (kk & 3) * 32) >> 4;
-                            const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
-                            umma_ss(s_tm, qdesc + qoff, kdesc + koff, IDESC_QK, kk != 0);
-                        }
-                        umma_commit(&s_full[2 * t + (j & 1)]);
-                    }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = static_cast<uint32_t>((kk >> 2) * C::SLAB_STRIDE + (kk & 3) * 32) >> 4;
+                    const uint32_t qoff = static_cast<uint32_t>((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+                    umma_ss(tbase + C::TM_S + 128 * t, qdesc + qoff, kdesc + koff, IDESC_QK, kk != 0);
                 }
-                if (j >= 1 && ok) {
-                    const int jp = j - 1, sp = jp % C::STAGES;
-                    const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + sp * C::SLABS * C::KSLOT, C::KSLOT, 1024);
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (!(ok = mbar_wait(&p_full[2 * t + (jp & 1)], static_cast<uint32_t>((jp >> 1) & 1))))
-                            break;
-                        tc_fence_after();
-                        const uint32_t p_tm = tbase + C::TM_S + 128 * t + 64 * (jp & 1);
+                umma_commit(&s_full[t]);
+                return true;
+            };
+            auto issue_pv = [&](int t, int pp) -> bool {
+                if (!mbar_wait(&p_full[t], static_cast<uint32_t>(pp & 1)))
+                    return false;
+                tc_fence_after();
+                const int s0 = (2 * pp) % C::STAGES;
+                const uint64_t vdesc = umma_desc_sw128(sbase + C::V_OFF + s0 * C::KSLOT, C::SLAB_STRIDE, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < C::KB / 16; ++kk)
-                            umma_ts(tbase + C::TM_O + D * t, p_tm + 8 * kk,
-                                    vdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_PV, (jp > 0 || kk > 0) ? 1u : 0u);
-                        umma_commit(&o_done[t]);
-                        if (jp == nkb - 1)
-                            umma_commit(&o_final[t]);  // the epilogue's own barrier (o_done may run ahead of it)
-                    }
-                    umma_commit(&empty[sp]);
-                }
+                for (int kk = 0; kk < 2 * C::KB / 16; ++kk)
+                    umma_ts(tbase + C::TM_O + D * t, tbase + C::TM_S + 128 * t + 8 * kk,
+                            vdesc + static_cast<uint64_t>(kk * (2048 >> 4)), IDESC_PV, (pp > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&o_done[t]);
+                if (pp == npair - 1)
+                    umma_commit(&o_final[t]);  // the epilogue's own barrier (o_done may run ahead of it)
+                return true;
+            };
+            ok = ok && issue_s(0, 0) && issue_s(1, 0);
+            for (int pp = 0; pp < npair && ok; ++pp) {
+                ok = issue_pv(0, pp) && (pp + 1 >= npair || issue_s(0, pp + 1)) && issue_pv(1, pp);
+                if (!ok)
+                    break;
+                umma_commit(&empty[(2 * pp) % C::STAGES]);  // both tiles' S and PV of the pair are done
+                umma_commit(&empty[(2 * pp) % C::STAGES + 1]);
+                ok = pp + 1 >= npair || issue_s(1, pp + 1);
             }
             if (!ok)
                 record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
@@ -284,11 +295,11 @@ __global__ void __launch_bounds__(512, 1)
         constexpr int PAIRS = C::KB * 8;
         static_assert(C::CONV_THREADS % 32 == 0 && (C::KB * 8) % 32 == 0 && C::CONV_THREADS / 8 == 24,
                       "rows of a converter warp: (cid / 8) + 24 it");
-        for (int j = 0; j < nkb && ok; ++j) {
+        for (int j = 0; j < 2 * npair && ok; ++j) {
             const int s = j % C::STAGES;
             if (!(ok = mbar_wait(&full[s], static_cast<uint32_t>((j / C::STAGES) & 1))))
                 break;
-            uint8_t *blk = smem + C::K_OFF + s * C::SLABS * C::KSLOT;
+            uint8_t *blk = smem + C::K_OFF + s * C::KSLOT;
             // common case: every chunk below 65520 converts as is; when a chunk of the warp's rows
             // reaches it, the warp shifts those rows instead (rare)
             constexpr int ITS = (PAIRS + C::CONV_THREADS - 1) / C::CONV_THREADS;
@@ -300,8 +311,8 @@ __global__ void __launch_bounds__(512, 1)
                 if (it < nrows) {
 #pragma unroll
                     for (int sl = 0; sl < C::SLABS; ++sl) {
-                        u[it][sl] = *reinterpret_cast<const uint4 *>(blk + sl * C::KSLOT + ((cid >> 3) + 24 * it) * 128 +
-                                                                     (cid & 7) * 16);
+                        u[it][sl] = *reinterpret_cast<const uint4 *>(blk + sl * C::SLAB_STRIDE +
+                                                                     ((cid >> 3) + 24 * it) * 128 + (cid & 7) * 16);
                         kept |= (bf16x8_absmax(u[it][sl]) < 65520.f ? 0u : 1u) << (it * C::SLABS + sl);
                     }
                 }
@@ -312,11 +323,11 @@ __global__ void __launch_bounds__(512, 1)
                     if (it < nrows) {
 #pragma unroll
                         for (int sl = 0; sl < C::SLABS; ++sl)
-                            *reinterpret_cast<uint4 *>(blk + sl * C::KSLOT + ((cid >> 3) + 24 * it) * 128 + (cid & 7) * 16) =
-                                k_to_fp16(u[it][sl]);
+                            *reinterpret_cast<uint4 *>(blk + sl * C::SLAB_STRIDE + ((cid >> 3) + 24 * it) * 128 +
+                                                       (cid & 7) * 16) = k_to_fp16(u[it][sl]);
                     }
             } else {
-                shift_key_rows<C::SLABS>(blk, C::KSLOT, 0, cid >> 3, C::CONV_THREADS / 8, nrows, cid & 7,
+                shift_key_rows<C::SLABS>(blk, C::SLAB_STRIDE, 0, cid >> 3, C::CONV_THREADS / 8, nrows, cid & 7,
                                          kexp + s * C::KB, bad);
             }
             if (lane == 0)
@@ -342,105 +353,129 @@ __global__ void __launch_bounds__(512, 1)
         const float NEG_INF = -__int_as_float(0x7f800000);
         float m = NEG_INF, l = 0.f;
         bool ok = true, range_bad = false;
-        for (int j = 0; j < nkb && ok; ++j) {
-            const int u = j & 1;
-            const int ks = j % C::STAGES;
-            if (!(ok = mbar_wait(&s_full[2 * t + u], static_cast<uint32_t>((j >> 1) & 1))))
+        // pair pp: the two 64-column halves of S_t in turn (half hh = key block 2 pp + hh), each with
+        // the lazily raised running max; P of half hh goes to columns 32 hh .. 32 hh + 31 as bf16
+        for (int pp = 0; pp < npair && ok; ++pp) {
+            if (!(ok = mbar_wait(&s_full[t], static_cast<uint32_t>(pp & 1))))
                 break;
             tc_fence_after();
-            const uint32_t s_col = s_lane + 64 * u;
-            const int k0 = j * C::KB;
-            const bool whole = __all_sync(0xffffffffu, k0 + C::KB - 1 <= pr);
-            const int nvalid = pr - k0;  // column c is a valid key iff c <= nvalid
-            uint32_t va[32], vb[32];
-            tmem_ld32(s_col, va);
-            tmem_ld32(s_col + 32, vb);
-            // the block's shift flags: its conversion barrier completed before its S was issued, so
-            // this non-blocking test succeeds and orders the flag read after the converters' writes
-            const uint32_t kph = static_cast<uint32_t>((j / C::STAGES) & 1);
-            const bool conv_seen = mbar_test_wait(&kconv[ks], kph);
-            const uint64_t kf = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
-            tmem_wait_ld();
-            if (!conv_seen || kf != 0) {
-                if (!(ok = mbar_wait(&kconv[ks], kph)))
-                    break;
-                const uint64_t kf2 = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
-                uint32_t kw = 0;  // one bit per converter warp that shifted rows of this block
-#pragma unroll
-                for (int cw = 0; cw < C::CONV_THREADS / 32; ++cw)
-                    kw |= (((kf2 >> (8 * cw)) & 0xffu) ? 1u : 0u) << cw;
-                if (kw != 0) {  // logits of shifted key rows times 2^e_j (rare), in tensor memory
-                    unshift_chunk32(s_col, kexp + ks * C::KB, 0, kw, 24, 4, range_bad);
-                    unshift_chunk32(s_col + 32, kexp + ks * C::KB, 32, kw, 24, 4, range_bad);
-                    tmem_ld32(s_col, va);
-                    tmem_ld32(s_col + 32, vb);
-                    tmem_wait_ld();
-                }
-            }
-            if (!whole) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if (e > nvalid)
-                        va[e] = __float_as_uint(NEG_INF);
-                    if (32 + e > nvalid)
-                        vb[e] = __float_as_uint(NEG_INF);
-                }
-            }
-            float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(va[e]), __uint_as_float(va[e + 1]));
-                m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(vb[e]), __uint_as_float(vb[e + 1]));
-            }
-            const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            // raise the running max only when it grows by more than 2^8 (P stays <= 256)
-            const bool raise = mb > m + 8.f;
-            if (__any_sync(0xffffffffu, raise)) {
-                const float f = raise ? fast_exp2(m - mb) : 1.f;  // m = -inf on the first block: f = 0
-                if (j > 0) {
-                    // O holds blocks up to j - 1 once their O += P V is complete
-                    if (!(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1))))
-                        break;
-                    tc_fence_after();
+            float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t w[32];
-                        tmem_ld32(o_col + c, w);
-                        tmem_wait_ld();
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+                const int j = 2 * pp + hh;
+                const int ks = j % C::STAGES;
+                const uint32_t s_col = s_lane + 64 * hh;
+                const int k0 = j * C::KB;
+                const bool whole = __all_sync(0xffffffffu, k0 + C::KB - 1 <= pr);
+                const int nvalid = pr - k0;  // column c is a valid key iff c <= nvalid
+                uint32_t va[32], vb[32];
+                tmem_ld32(s_col, va);
+                tmem_ld32(s_col + 32, vb);
+                // the block's shift flags: its conversion barrier completed before its S was issued,
+                // so this non-blocking test succeeds and orders the flag read after the converters'
+                // writes
+                const uint32_t kph = static_cast<uint32_t>((j / C::STAGES) & 1);
+                const bool conv_seen = mbar_test_wait(&kconv[ks], kph);
+                const uint64_t kf = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
+                tmem_wait_ld();
+                if (!conv_seen || kf != 0) {
+                    if (!(ok = mbar_wait(&kconv[ks], kph)))
+                        break;
+                    const uint64_t kf2 = *reinterpret_cast<const volatile uint64_t *>(smem + C::KFLAG_OFF + ks * 8);
+                    uint32_t kw = 0;  // one bit per converter warp that shifted rows of this block
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            w[e] = __float_as_uint(__uint_as_float(w[e]) * f);
-                        tmem_st32(o_col + c, w);
+                    for (int cw = 0; cw < C::CONV_THREADS / 32; ++cw)
+                        kw |= (((kf2 >> (8 * cw)) & 0xffu) ? 1u : 0u) << cw;
+                    if (kw != 0) {  // logits of shifted key rows times 2^e_j (rare), in tensor memory
+                        unshift_chunk32(s_col, kexp + ks * C::KB, 0, kw, 24, 4, range_bad);
+                        unshift_chunk32(s_col + 32, kexp + ks * C::KB, 32, kw, 24, 4, range_bad);
+                        tmem_ld32(s_col, va);
+                        tmem_ld32(s_col + 32, vb);
+                        tmem_wait_ld();
                     }
                 }
-                if (raise) {
-                    l *= f;
-                    m = mb;
+                if (!whole) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (e > nvalid)
+                            va[e] = __float_as_uint(NEG_INF);
+                        if (32 + e > nvalid)
+                            vb[e] = __float_as_uint(NEG_INF);
+                    }
+                }
+                float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(va[e]), __uint_as_float(va[e + 1]));
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(vb[e]), __uint_as_float(vb[e + 1]));
+                }
+                const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                // raise the running max only when it grows by more than 2^8 (P stays <= 256)
+                const bool raise = mb > m + 8.f;
+                if (__any_sync(0xffffffffu, raise)) {
+                    const float f = raise ? fast_exp2(m - mb) : 1.f;  // m = -inf before the first key: f = 0
+                    if (pp > 0) {
+                        // O holds the pairs before pp (S_t of this pair waited for their P V)
+                        if (!(ok = mbar_wait(&o_done[t], static_cast<uint32_t>((pp - 1) & 1))))
+                            break;
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t w[32];
+                            tmem_ld32(o_col + c, w);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                w[e] = __float_as_uint(__uint_as_float(w[e]) * f);
+                            tmem_st32(o_col + c, w);
+                        }
+                    }
+                    if (hh == 1) {  // P of the first half was taken against the old max: scale it too
+                        tmem_wait_st();
+                        uint32_t w[32];
+                        tmem_ld32(s_lane, w);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 pq = unpack_bf16x2(w[e]);
+                            w[e] = pack_bf16x2(pq.x * f, pq.y * f);
+                        }
+                        tmem_st32(s_lane, w);
+                        l2[0].x *= f;
+                        l2[0].y *= f;
+                        l2[1].x *= f;
+                        l2[1].y *= f;
+                    }
+                    if (raise) {
+                        l *= f;
+                        m = mb;
+                    }
+                }
+                const float uo = (m == NEG_INF) ? 0.f : m;
+                const float2 nu = make_float2(-uo, -uo);
+                // P = exp2(S - m) as bf16 over columns 32 hh .. 32 hh + 31 of the S buffer, row sum
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    const uint32_t *v = hq ? vb : va;
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 d = fadd2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), nu);
+                        const float2 pp2 = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+                        l2[e & 1] = fadd2(l2[e & 1], pp2);
+                        pw[e] = pack_bf16x2(pp2.x, pp2.y);
+                    }
+                    tmem_st16(s_lane + 32 * hh + 16 * hq, pw);
                 }
             }
-            const float uo = (m == NEG_INF) ? 0.f : m;
-            const float2 nu = make_float2(-uo, -uo);
-            // P = exp2(S - m) as bf16 over the first 32 columns of this S buffer, row sum
-            float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-                const uint32_t *v = hq ? vb : va;
-                uint32_t pw[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 d = fadd2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), nu);
-                    const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-                    l2[e & 1] = fadd2(l2[e & 1], pp);
-                    pw[e] = pack_bf16x2(pp.x, pp.y);
-                }
-                tmem_st16(s_col + 16 * hq, pw);
-            }
+            if (!ok)
+                break;
             l += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[2 * t + u]);
+                mbar_arrive(&p_full[t]);
         }
         // ---- epilogue: O / l -> bf16 -> the copy's output row (and its log-sum-exp)
         const bool store = row < R;

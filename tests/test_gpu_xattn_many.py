@@ -90,3 +90,24 @@ def test_many_copies_all_rejected():
     got, err = _xattn(inp, pos)
     assert err & orth.DEVERR_POSITION
     assert (got == 0).all()
+
+
+@pytest.mark.parametrize("boost_block", [1, 3])
+def test_running_max_raised_in_the_second_half_of_a_key_pair(boost_block):
+    """The tensor-memory kernel takes 128 keys per softmax step as two 64-key halves with a
+    lazily raised running max.  Key block `boost_block` (the second half of a pair) scaled by
+    4 (exact in bf16) makes its logits several times larger, so most rows raise their max there
+    and the first half's already written weights must be rescaled in place; without that they
+    would outweigh the second half by about 2^9."""
+    from synthetic import bf16_bits, bf16_to_f32
+    cfg = PrefillConfig("raise", B=1, T=600, Hq=8, Hkv=2, d=128, T_out=64)
+    inp = make_prefill(cfg, 4242 + boost_block)
+    k = bf16_to_f32(inp.k)
+    k[:, 64 * boost_block:64 * boost_block + 64] *= np.float32(4.0)
+    inp.k[...] = bf16_bits(k)
+    pos = np.full((cfg.B, cfg.T_out), cfg.T - 1, np.int32)
+    pos[:, :8] = [64 * boost_block + 63, 64 * boost_block, 64 * boost_block - 1, 64 * boost_block + 64, 599, 300,
+                  200, 127]
+    got, err = _xattn(inp, pos)
+    assert err == 0
+    assert_parity(got, _ref(inp, pos), "running max raised in a pair's second half")
