@@ -47,6 +47,8 @@ ALL_LEGS = ("prefill", "e2e", "decode", "decode_b8", "gradient", "sft", "prefill
 HBM_NAMEPLATE_GBS = 8000.0
 SWA_SOURCES = ("swa_fwd.cu", "swa_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh")
 DECODE_SOURCES = ("decode_step.cu", "xattn.cuh", "common.cuh", "kernels.cuh")
+BWD_SOURCES = ("attn_bwd.cuh", "attn_bwd.cu", "attn_bwd_d128.cu", "tc.cuh", "common.cuh", "kernels.cuh")
+XTC_SOURCES = ("xattn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh")
 L2_NOTE = "inputs larger than L2 (129 MB), no flush"
 
 
@@ -520,10 +522,12 @@ def run_gradient(dev, world, g, o, oc, cfg, peaks, calls: int = 5):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     gbs = nbytes / (ms / 1e3) / 1e9
     tfs = flops / (ms / 1e3) / 1e12
+    traffic, tsrc = profile_traffic(f"attn_bwd_{cfg.name}", BWD_SOURCES)
     roof = {"kernel": f"attn_bwd ({per_call} launches)", "bound": bound,
             "achieved": gbs if bound == "hbm" else tfs, "peak": peaks["hbm"] if bound == "hbm" else peaks["bf16"],
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": max(t_hbm, t_tc) / ms,
-            "traffic": None, "peak_kind": peaks["kind"], "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "traffic": traffic, "traffic_source": tsrc, "peak_kind": peaks["kind"], "algorithmic_bytes": nbytes,
+            "algorithmic_flops": flops,
             "roofline_ms": max(t_hbm, t_tc), "hbm_ms": t_hbm, "tensor_ms": t_tc, "tflops": tfs}
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms,
             "what": "attn_bwd: both streams' gradient in one call (dK/dV written once), each stream with its "
@@ -610,13 +614,16 @@ def run_sft(dev, world, peaks, steps, warmup):
     tfs = flops / (x_ms / 1e3) / 1e12
     t_tc = flops / (peaks["bf16_sustained"] * 1e12) * 1e3
     t_hbm = xb / (peaks["hbm"] * 1e9) * 1e3
+    traffic, tsrc = profile_traffic(f"xattn_tc_{cfg.name}", XTC_SOURCES)
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "copies_per_s": B * cfg.T_out * world / (ms / 1e3), "config": _config_line(cfg),
             "roofline": {"kernel": "xattn_tc", "bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": tfs,
                          "peak": peaks["bf16_sustained"], "unit": "TFLOP/s", "frac": max(t_tc, t_hbm) / x_ms,
-                         "frac_of_burst": tfs / peaks["bf16"], "traffic": None, "peak_kind": peaks["kind"] + " sustained",
+                         "frac_of_burst": tfs / peaks["bf16"], "traffic": traffic, "traffic_source": tsrc,
+                         "peak_kind": peaks["kind"] + " sustained",
                          "algorithmic_flops": flops, "algorithmic_bytes": xb, "ms_per_launch": x_ms},
-            "swa": hbm_roofline("swa_fwd", swa_bytes(B, T, Hq, Hkv, d), swa_ms, peaks),
+            "swa": hbm_roofline("swa_tc", swa_bytes(B, T, Hq, Hkv, d), swa_ms, peaks, f"swa_fwd_{cfg.name}",
+                                SWA_SOURCES),
             "gpu_launches": steps * launches_per_prefill_step(cfg)}
 
 
