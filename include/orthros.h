@@ -314,12 +314,16 @@ size_t orthros_swa_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
  * kernel used without lse (warp MMAs) takes q as
  * a bf16 high part plus residual.  P is rounded to bf16 before it multiplies
  * dO; dS is rounded to bf16 before it multiplies K (dq) and to fp16 before it
- * multiplies the fp16 q (dk; |dS| >= 65504 sets ORTHROS_DEVERR_RANGE).
- * Launches: the fp16 copies of K and of q, D_t (which also converts a given
- * lse), dq (rows on the MMA's M side: with lse a persistent tensor-memory
- * kernel followed by a column sum for dalpha, dbeta; else a two-pass warp-MMA
- * one that stores each row's log-sum-exp), then dk and dv (keys on the M side,
- * tensor memory, no atomics).  dq, dk, dv have one writer per element;
+ * multiplies the fp16 q (dk; |dS| >= 65504 sets ORTHROS_DEVERR_RANGE).  The
+ * key-band dq (below) takes dS in fp16 against the fp16 K, times 2^e for a key
+ * row shifted by 2^-e (|dS 2^e| >= 65504 sets ORTHROS_DEVERR_RANGE).
+ * Launches: the fp16 copy of K; one pass over the query rows for the fp16 q,
+ * D_t and a given lse in log2 units; dq (rows on the MMA's M side: with lse a
+ * persistent tensor-memory kernel, which for Hq / Hkv in {4, 8} and windows
+ * whose row tile sees at most five 32-key blocks takes each tile's key band
+ * in one product and sums dalpha, dbeta itself, else a column sum follows;
+ * without lse a two-pass warp-MMA kernel that stores each row's log-sum-exp),
+ * then dk and dv (keys on the M side, tensor memory, no atomics).  dq, dk, dv have one writer per element;
  * dalpha, dbeta are summed with atomics.  dev_err (optional) as elsewhere.
  * Supported: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}; any window >= 1.
  * Outputs must not alias inputs.
