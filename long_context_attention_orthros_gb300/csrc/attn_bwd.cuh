@@ -1738,8 +1738,11 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
 // dalpha = sum x * dq and dbeta = sum dq over the CTA's rows (lanes of one head reduce-scatter
 // each 32-column chunk, so each lane owns G columns of its head; global atomics when the KV
 // head changes and at the end).
-// Roles (384 threads): warp 0 TMA producer, warp 1 tensor-memory allocation and MMA issue,
-// warps 4-7 dS (lane = row), warps 8-11 the epilogue (the same lanes); warps 2-3 idle.
+// Roles (512 threads): warp 0 TMA producer, warp 1 tensor-memory allocation and MMA issue,
+// warps 4-7 and 8-11 dS (lane = row; the first group slots 0-2 of the ring, the second slots
+// 3-5, each writing its dS over its own slots' dP columns) and, once a tile's dQ is done, the
+// dalpha / dbeta sums over their half of the columns (FOLD); warps 12-15 store dq_raw (the same
+// lanes); warps 2-3 idle.
 // Tensor memory: S at 0, dP (then dS) at N, dQ at 2 N.
 template <int D>
 struct BbCfg {
@@ -1763,6 +1766,10 @@ struct BbCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
     static constexpr uint32_t TM_S = 0, TM_DP = N, TM_DQ = 2 * N;
     static_assert(TM_DQ + D <= 512, "tensor memory budget");
+    static constexpr int THREADS = 512;
+    // dS of slot j (16 packed fp16 pairs) over dP columns of its own dS group's slots:
+    // slots 0-2 at 16 j (dP slots 0-1), slots 3-5 at 48 + 16 j (dP slots 3-4)
+    static __device__ __forceinline__ uint32_t ds_col(int j) { return static_cast<uint32_t>(j < 3 ? 16 * j : 48 + 16 * j); }
 };
 
 // The band of a CTA's tiles in load order: tiles run in (batch, KV head, row tile) order, so
@@ -1783,7 +1790,7 @@ struct BandRun {
 };
 
 template <int D, int G, bool FOLD>
-__global__ void __launch_bounds__(DKV_TC_THREADS, 1)
+__global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
     attn_bwd_dq_band_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                             const __grid_constant__ CUtensorMap k16map, const __grid_constant__ CUtensorMap vmap,
                             const AttnBwdParams p)
@@ -1827,9 +1834,9 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             mbar_init(&kv_empty[s], 1);
         }
         mbar_init(s_full, 1);
-        mbar_init(p_full, 4);
+        mbar_init(p_full, 8);
         mbar_init(dq_final, 1);
-        mbar_init(dq_free, 4);
+        mbar_init(dq_free, FOLD ? 12 : 4);  // the store warps, and the dS warps once they have summed
         fence_barrier_init();
     }
     if (warp == 1)
@@ -1953,7 +1960,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     for (int h = 0; h < 2; ++h) {
                         const uint64_t bdesc =
                             umma_desc_sw128(sbase + C::K16_OFF + j * C::SLOT + h * 2048, C::RSLAB, 1024);
-                        umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + 16 * j + 8 * h, bdesc, IDESC_DQ,
+                        umma_ts(tbase + C::TM_DQ, tbase + C::TM_DP + C::ds_col(j) + 8 * h, bdesc, IDESC_DQ,
                                 (kb > lo || h > 0) ? 1u : 0u);
                     }
                 }
@@ -1975,14 +1982,36 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
         }
     } else if (warp < 4) {
         // warps 2-3: no role
-    } else if (warp < 8) {
-        // ------------------------------------------------------------------ dS (lane = row)
-        const int rw = warp - 4;
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ dS (lane = row), sums
+        const int rw = warp & 3;
+        const int grp = warp < 8 ? 0 : 1;
+        const uint32_t gmask = grp == 0 ? 0x07u : 0x38u;  // this group's ring slots
         const int r = rw * 32 + lane;  // row of the tile = tensor-memory lane
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
         const float c2 = p.scale * kLog2eF;
         float ds_max = 0.f;  // dS goes to fp16
         bool kshift_bad = false;
+        // FOLD: this group's half of the columns of dalpha += x dq, dbeta += dq (dq = scale dQ).
+        // The lanes of one head reduce-scatter each 16-column piece, after which a lane owns G / 2
+        // columns of its head (lane / G picks which); sums stay in registers across the CTA's
+        // tiles and go to global memory with atomics when the KV head changes and at the end.
+        constexpr int OWN = FOLD ? G / 2 : 1;
+        constexpr int NP = D / 32;  // 16-column pieces in half the columns
+        float acc_a[NP][OWN], acc_b[NP][OWN];
+        int cur_g = -1;
+        auto flush = [&](int gg) {
+            if (FOLD && gg >= 0) {
+                const int col0 = (gg * G + lane % G) * D + grp * (D / 2) + (lane / G) * OWN;
+#pragma unroll
+                for (int pc = 0; pc < NP; ++pc)
+#pragma unroll
+                    for (int e = 0; e < OWN; ++e) {
+                        atomicAdd(p.dalpha + col0 + 16 * pc + e, acc_a[pc][e]);
+                        atomicAdd(p.dbeta + col0 + 16 * pc + e, acc_b[pc][e]);
+                    }
+            }
+        };
         BandRun run;
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int bh, u0, lo, hi;
@@ -1998,45 +2027,34 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
             const float Drow = live ? p.Drow[ri] : 0.f;
             const int8_t *ke = p.kexp + static_cast<long long>(bh) * p.nkb * 64;
             const uint8_t *kf = p.kflag + static_cast<long long>(bh) * p.nkb;
-            // band blocks holding key rows beyond fp16 (rare): one bit per slot
-            uint32_t shifted = 0;
-            for (int kb = lo; kb <= hi; ++kb)
+            // this group's band slots (slot s0 + d holds block lo + d); the others are stale or
+            // loading, and those of shifted key rows (rare)
+            uint32_t band = 0, shifted = 0;
+            for (int kb = lo; kb <= hi; ++kb) {
+                const uint32_t bit = 1u << ((s0 + kb - lo) % C::NSLOT);
+                band |= bit;
                 if (kf[kb >> 1] != 0)
-                    shifted |= 1u << ((s0 + kb - lo) % C::NSLOT);
-            // the band's slots (slot s0 + d holds block lo + d); the others are stale or loading
-            uint32_t band = 0;
-            for (int d = 0; d <= hi - lo; ++d)
-                band |= 1u << ((s0 + d) % C::NSLOT);
+                    shifted |= bit;
+            }
+            band &= gmask;
+            shifted &= gmask;
             if (!(ok = warp_wait(s_full, static_cast<uint32_t>(i & 1))))
                 break;
             tc_fence_after();
-            for (uint32_t m = shifted; m != 0; m &= m - 1) {  // rare: logits of shifted key rows times 2^e
+            for (uint32_t m = shifted; m != 0; m &= m - 1) {  // logits of shifted key rows times 2^e
                 const int j = __ffs(m) - 1;
                 unshift_chunk32(tl + C::TM_S + 32 * j, ke, (lo + (j - s0 + C::NSLOT) % C::NSLOT) * C::KB, 1u, 1, 1,
                                 kshift_bad);
             }
-            // the band's slots in slot order, the next slot's S and dP loads in flight while this
-            // one is computed (a tensor-memory load takes several hundred cycles to land); dS of
-            // slot j goes over dP columns 16 j .. 16 j + 15, below every column still to be read
-            int j = __ffs(band) - 1;
-            uint32_t sa[32], da[32];
-            tmem_ld32(tl + C::TM_S + 32 * j, sa);
-            tmem_ld32(tl + C::TM_DP + 32 * j, da);
+            // the group's slots in slot order; dS of slot j goes over dP columns of the group's
+            // own slots, below every column it has still to read
 #pragma unroll 1
-            while (true) {
-                tmem_wait_ld();
+            for (uint32_t m = band; m != 0; m &= m - 1) {
+                const int j = __ffs(m) - 1;
                 uint32_t sv[32], dv[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    sv[e] = sa[e];
-                    dv[e] = da[e];
-                }
-                const uint32_t rest = band & ~((2u << j) - 1u);
-                const int jn = rest != 0 ? __ffs(rest) - 1 : -1;
-                if (jn >= 0) {
-                    tmem_ld32(tl + C::TM_S + 32 * jn, sa);
-                    tmem_ld32(tl + C::TM_DP + 32 * jn, da);
-                }
+                tmem_ld32(tl + C::TM_S + 32 * j, sv);
+                tmem_ld32(tl + C::TM_DP + 32 * j, dv);
+                tmem_wait_ld();
                 const int key0 = (lo + (j - s0 + C::NSLOT) % C::NSLOT) * C::KB;
                 const bool fl = (shifted >> j) & 1u;
                 uint32_t dw[16];
@@ -2054,113 +2072,117 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                         ds[0] *= exp2i(ke[key0 + 2 * e]);
                         ds[1] *= exp2i(ke[key0 + 2 * e + 1]);
                     }
-                    ds_max = fmaxf(ds_max, fmaxf(fabsf(ds[0]), fabsf(ds[1])));
+                    ds_max = fmax3(ds_max, fabsf(ds[0]), fabsf(ds[1]));
                     __half2 hv = __floats2half2_rn(ds[0], ds[1]);
                     dw[e] = *reinterpret_cast<uint32_t *>(&hv);
                 }
-                tmem_st16(tl + C::TM_DP + 16 * j, dw);
-                if (jn < 0)
-                    break;
-                j = jn;
+                tmem_st16(tl + C::TM_DP + C::ds_col(j), dw);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(p_full);
+            if constexpr (FOLD) {
+                // the sums of this tile, once its dQ is done (while the next tile's S, dP run)
+                if (g != cur_g) {
+                    flush(cur_g);
+#pragma unroll
+                    for (int pc = 0; pc < NP; ++pc)
+#pragma unroll
+                        for (int e = 0; e < OWN; ++e)
+                            acc_a[pc][e] = acc_b[pc][e] = 0.f;
+                    cur_g = g;
+                }
+                // x of the row's half: all loads in flight before the wait (G = 4); piece by piece
+                // for G = 8, whose wider per-lane sums leave no registers for them
+                constexpr bool XALL = G == 4;
+                const long long off = ri * D + grp * (D / 2);
+                uint4 xr[XALL ? 2 * NP : 2];
+                if (XALL) {
+#pragma unroll
+                    for (int e = 0; e < (XALL ? 2 * NP : 2); ++e)
+                        xr[e] = live ? __ldg(reinterpret_cast<const uint4 *>(p.q + off) + e) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (!(ok = warp_wait(dq_final, static_cast<uint32_t>(i & 1))))
+                    break;
+                tc_fence_after();
+                const float sc = p.scale;
+#pragma unroll
+                for (int pc = 0; pc < NP; ++pc) {
+                    const int xi = XALL ? 2 * pc : 0;
+                    if (!XALL) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            xr[e] = live ? __ldg(reinterpret_cast<const uint4 *>(p.q + off + 16 * pc) + e)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    uint32_t w[16];
+                    tmem_ld16(tl + C::TM_DQ + grp * (D / 2) + 16 * pc, w);
+                    tmem_wait_ld();
+                    float va[16], vb[16];
+                    const uint32_t xw[8] = {xr[xi].x,     xr[xi].y,     xr[xi].z,     xr[xi].w,
+                                            xr[xi + 1].x, xr[xi + 1].y, xr[xi + 1].z, xr[xi + 1].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 xv = unpack_bf16x2(xw[e]);
+                        const float d0 = live ? __uint_as_float(w[2 * e]) * sc : 0.f;
+                        const float d1 = live ? __uint_as_float(w[2 * e + 1]) * sc : 0.f;
+                        vb[2 * e] = d0;
+                        vb[2 * e + 1] = d1;
+                        va[2 * e] = xv.x * d0;
+                        va[2 * e + 1] = xv.y * d1;
+                    }
+                    // reduce-scatter over the 32 / G lanes of this head: halve the vector per step
+#pragma unroll
+                    for (int st = 0; (16 >> st) >= G; ++st) {
+                        const int mk = 16 >> st, half = 8 >> st;
+                        const bool up = (lane & mk) != 0;
+#pragma unroll
+                        for (int e = 0; e < half; ++e) {
+                            const float sa = up ? va[e] : va[e + half], ka = up ? va[e + half] : va[e];
+                            const float sb = up ? vb[e] : vb[e + half], kb2 = up ? vb[e + half] : vb[e];
+                            va[e] = ka + __shfl_xor_sync(0xffffffffu, sa, mk);
+                            vb[e] = kb2 + __shfl_xor_sync(0xffffffffu, sb, mk);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < OWN; ++e) {
+                        acc_a[pc][e] += va[e];
+                        acc_b[pc][e] += vb[e];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(dq_free);  // this warp's share of dQ is read
+            }
         }
+        if (FOLD && ok)
+            flush(cur_g);
         if (!(ds_max < 65504.f) || kshift_bad)
             record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
-        // ------------------------------------------------------------------ epilogue (warps 8-11)
-        // dq_raw = scale dQ alpha; with FOLD also dalpha += x dq, dbeta += dq (dq = scale dQ).
-        // x is read one 16-column piece ahead (G = 4; G = 8 has the registers for one piece only),
-        // and the next tile's rows are prefetched into L2 while this tile is stored.
-        const int rw = warp - 8;
+        // ------------------------------------------------------------------ dq_raw stores (warps 12-15)
+        // dq_raw = scale dQ alpha, in 16-column pieces with the next piece's load in flight
+        const int rw = warp - 12;
         const int r = rw * 32 + lane;
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
-        constexpr int NCH = D / 32;
-        constexpr int OWN = FOLD ? G / 2 : 1;  // columns a lane owns per 16-column half after the reduce-scatter
-        constexpr bool AHEAD = G == 4;
-        float acc_a[FOLD ? NCH : 1][2][OWN], acc_b[FOLD ? NCH : 1][2][OWN];
-        int cur_g = -1;
-        // lane's columns: chunk c, half hh: 32 c + 16 hh + (lane / G) OWN + e; head lane % G
-        auto flush = [&](int gg) {
-            if (FOLD && gg >= 0) {
-                const int col0 = (gg * G + lane % G) * D + (lane / G) * OWN;
-#pragma unroll
-                for (int c = 0; c < (FOLD ? NCH : 1); ++c)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                        for (int e = 0; e < OWN; ++e) {
-                            atomicAdd(p.dalpha + col0 + 32 * c + 16 * hh + e, acc_a[c][hh][e]);
-                            atomicAdd(p.dbeta + col0 + 32 * c + 16 * hh + e, acc_b[c][hh][e]);
-                        }
-            }
-        };
-        auto row_off = [&](long long t, bool &lv, int &hd) {
-            int bh, u0, lo, hi;
-            tile(t, bh, u0, lo, hi);
-            const int uu = u0 + r / G;
-            hd = (bh % p.Hkv) * G + r % G;
-            lv = uu < p.n_units;
-            return ((static_cast<long long>(bh / p.Hkv) * p.n_units + uu) * p.Hq + hd) * D;
-        };
-        auto load_x = [&](long long off, bool lv, int c, uint4 (&xr)[2]) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-                xr[e] = lv ? __ldg(reinterpret_cast<const uint4 *>(p.q + off + c) + e) : make_uint4(0u, 0u, 0u, 0u);
-        };
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
-            const int g = static_cast<int>((tau / ((p.n_units + UNITS - 1) / UNITS)) % p.Hkv);
-            if (FOLD && g != cur_g) {
-                flush(cur_g);
-#pragma unroll
-                for (int c = 0; c < (FOLD ? NCH : 1); ++c)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                        for (int e = 0; e < OWN; ++e)
-                            acc_a[c][hh][e] = acc_b[c][hh][e] = 0.f;
-                cur_g = g;
-            }
-            bool live;
-            int h;
-            const long long off = row_off(tau, live, h);
-            uint4 xn[2];
-            if (FOLD && AHEAD)
-                load_x(off, live, 0, xn);
-            if (FOLD && tau + 1 < t_end) {  // the next tile's row of x into L2
-                bool lv;
-                int hd;
-                const long long on = row_off(tau + 1, lv, hd);
-                if (lv) {
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + on));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + on + 64));
-                }
-            }
+            int bh, u0, lo, hi;
+            tile(tau, bh, u0, lo, hi);
+            const int b = bh / p.Hkv, g = bh % p.Hkv;
+            const int uu = u0 + r / G, h = g * G + r % G;
+            const bool live = uu < p.n_units;
+            const long long off = ((static_cast<long long>(b) * p.n_units + uu) * p.Hq + h) * D;
             if (!(ok = warp_wait(dq_final, static_cast<uint32_t>(i & 1))))
                 break;
             tc_fence_after();
-            // 16-column pieces of dQ, the next piece's load in flight while this one is stored
             uint32_t wa[16];
             tmem_ld16(tl + C::TM_DQ, wa);
             const float sc = p.scale;
 #pragma unroll
-            for (int pc = 0; pc < D / 16; ++pc) {
-                const int c = 16 * pc;
-                uint4 xr[2];
-                if (FOLD) {
-                    if (AHEAD) {
-                        xr[0] = xn[0];
-                        xr[1] = xn[1];
-                        if (c + 16 < D)
-                            load_x(off, live, c + 16, xn);
-                    } else {
-                        load_x(off, live, c, xr);
-                    }
-                }
+            for (int c = 0; c < D; c += 16) {
                 tmem_wait_ld();
                 uint32_t w[16];
 #pragma unroll
@@ -2168,7 +2190,7 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                     w[e] = wa[e];
                 if (c + 16 < D)
                     tmem_ld16(tl + C::TM_DQ + c + 16, wa);
-                if (live) {  // dq_raw = scale dQ alpha, whole 32-byte sectors per store
+                if (live) {  // whole 32-byte sectors per store
 #pragma unroll
                     for (int e = 0; e < 16; e += 8) {
                         const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
@@ -2184,46 +2206,12 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
                                                 __float_as_uint(__uint_as_float(w[e + 7]) * sc * a1.w)));
                     }
                 }
-                if (FOLD) {
-                    float va[16], vb[16];
-                    const uint32_t xw[8] = {xr[0].x, xr[0].y, xr[0].z, xr[0].w, xr[1].x, xr[1].y, xr[1].z, xr[1].w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 xv = unpack_bf16x2(xw[e]);
-                        const float d0 = live ? __uint_as_float(w[2 * e]) * sc : 0.f;
-                        const float d1 = live ? __uint_as_float(w[2 * e + 1]) * sc : 0.f;
-                        vb[2 * e] = d0;
-                        vb[2 * e + 1] = d1;
-                        va[2 * e] = xv.x * d0;
-                        va[2 * e + 1] = xv.y * d1;
-                    }
-                    // reduce-scatter over the 32 / G lanes of this head: halve the vector per step
-#pragma unroll
-                    for (int st = 0; (16 >> st) >= G; ++st) {
-                        const int m = 16 >> st, half = 8 >> st;
-                        const bool up = (lane & m) != 0;
-#pragma unroll
-                        for (int e = 0; e < half; ++e) {
-                            const float sa = up ? va[e] : va[e + half], ka = up ? va[e + half] : va[e];
-                            const float sb = up ? vb[e] : vb[e + half], kb2 = up ? vb[e + half] : vb[e];
-                            va[e] = ka + __shfl_xor_sync(0xffffffffu, sa, m);
-                            vb[e] = kb2 + __shfl_xor_sync(0xffffffffu, sb, m);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < OWN; ++e) {
-                        acc_a[FOLD ? pc / 2 : 0][pc % 2][e] += va[e];
-                        acc_b[FOLD ? pc / 2 : 0][pc % 2][e] += vb[e];
-                    }
-                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(dq_free);  // this warp's lanes of dQ are read
+                mbar_arrive(dq_free);  // this warp's lanes of dQ are stored
         }
-        if (ok)
-            flush(cur_g);
     }
     if (!ok && lane == 0)
         record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
@@ -2370,7 +2358,7 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
             }
         } else if (persistent && G >= 4 && dq_band_fits(G, p.window)) {
             // base stream with the forward's log-sum-exp, each tile's key band one MMA wide; for
-            // G <= 8 the dalpha / dbeta sums come out of its epilogue
+            // G <= 8 the dalpha / dbeta sums come out of its dS warps
             if constexpr (G >= 4) {
                 constexpr bool FOLD = G <= 8;
                 const size_t s1 = BbCfg<D>::SMEM;
@@ -2384,7 +2372,7 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
                     return e;
                 constexpr int UNITS = BbCfg<D>::ROWS / G;
                 const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
-                k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), DKV_TC_THREADS, s1, stream>>>(
+                k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), BbCfg<D>::THREADS, s1, stream>>>(
                     maps[9], maps[5], maps[10], maps[11], p);
                 if (!FOLD) {
                     if ((e = cudaGetLastError()) != cudaSuccess)
