@@ -49,6 +49,7 @@ SWA_SOURCES = ("swa_fwd.cu", "swa_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh")
 DECODE_SOURCES = ("decode_step.cu", "xattn.cuh", "common.cuh", "kernels.cuh")
 BWD_SOURCES = ("attn_bwd.cuh", "attn_bwd.cu", "attn_bwd_d128.cu", "tc.cuh", "common.cuh", "kernels.cuh")
 XTC_SOURCES = ("xattn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh")
+XATTN_SOURCES = ("xattn_fwd.cu", "xattn.cuh", "common.cuh", "kernels.cuh")
 L2_NOTE = "inputs larger than L2 (129 MB), no flush"
 
 
@@ -85,6 +86,22 @@ def profile_traffic(name, sources):
     if d.get("kernel_source_sha256_16") != kernel_hash(*sources):
         return None, None
     return d.get("dram_bytes_per_launch"), f"profiles/{name}.json"
+
+
+def step_roofline(swa_nbytes, step_nbytes, ms, peaks, name):
+    """The prefill step as one unit: with few copies its two kernels run at once (the copies'
+    split-KV pass on the SMs the SWA kernel leaves), so the step's algorithmic bytes over its
+    time.  traffic: the two kernels' one-pass DRAM captures, when both are current."""
+    gbs = step_nbytes / (ms / 1e3) / 1e9
+    t_swa, s_swa = profile_traffic(f"swa_fwd_{name}", SWA_SOURCES)
+    t_x, s_x = profile_traffic(f"xattn_fwd_{name}", XATTN_SOURCES)
+    both = t_swa is not None and t_x is not None
+    return {"kernel": "prefill step: swa_tc_kernel with the copies' split-KV pass beside it", "bound": "hbm",
+            "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+            "frac_nameplate": gbs / HBM_NAMEPLATE_GBS, "nameplate_peak": HBM_NAMEPLATE_GBS,
+            "traffic": t_swa + t_x if both else None, "traffic_source": f"{s_swa} + {s_x}" if both else None,
+            "peak_kind": peaks["kind"], "algorithmic_bytes": step_nbytes, "swa_algorithmic_bytes": swa_nbytes,
+            "ms_per_launch": ms, "concurrent": True}
 
 
 def hbm_roofline(kernel, nbytes, ms, peaks, traffic_name=None, sources=()):
@@ -334,8 +351,11 @@ def _upload_prefill(inp, dev):
 
 
 def time_prefill(g, cfg, dev, steps, warmup, world):
-    """Time `steps` prefill steps (SWA + copies) after `warmup` untimed ones, with CUDA events
-    around the whole region and around each kernel call on the launching stream."""
+    """Time `steps` prefill steps after `warmup` untimed ones: one orthros_prefill_fwd call per
+    step (for few copies it runs their split-KV pass on a second stream beside the SWA kernel),
+    with CUDA events around the whole region on the launching stream.  Then each kernel alone
+    (SWA on every SM, then the copies' pass), with events around each call, for the per-kernel
+    rooflines."""
     import torch
     import long_context_attention_orthros_gb300 as orth
     B, T, Hq, d, T_out = cfg.B, cfg.T, cfg.Hq, cfg.d, cfg.T_out
@@ -345,21 +365,10 @@ def time_prefill(g, cfg, dev, steps, warmup, world):
                      device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ev_s, ev_x = [], []
 
-    def step(timed=False):
-        if timed:
-            e = _events(3)
-            e[0].record(stream)
-        orth.swa_fwd(g["q"], g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale, out=o, dev_err=err)
-        if timed:
-            e[1].record(stream)
-        orth.xattn_fwd(g["qc"], g["pos"], g["k"], g["v"], g["ac"], g["bc"], scale=cfg.scale, out=oc, workspace=ws,
-                       dev_err=err)
-        if timed:
-            e[2].record(stream)
-            ev_s.append((e[0], e[1]))
-            ev_x.append((e[1], e[2]))
+    def step():
+        orth.prefill_fwd(g["q"], g["k"], g["v"], g["a"], g["b"], g["qc"], g["pos"], g["ac"], g["bc"],
+                         window=cfg.window, scale=cfg.scale, out=o, out_c=oc, workspace=ws, dev_err=err)
 
     for _ in range(warmup):
         step()
@@ -369,11 +378,23 @@ def time_prefill(g, cfg, dev, steps, warmup, world):
     t0, t1 = _events(2)
     t0.record(stream)
     for _ in range(steps):
-        step(timed=True)
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
     ms = allreduce_max(t0.elapsed_time(t1) / steps, world)
+    ev_s, ev_x = [], []
+    for _ in range(max(3, min(steps, 10))):
+        e = _events(3)
+        e[0].record(stream)
+        orth.swa_fwd(g["q"], g["k"], g["v"], g["a"], g["b"], window=cfg.window, scale=cfg.scale, out=o, dev_err=err)
+        e[1].record(stream)
+        orth.xattn_fwd(g["qc"], g["pos"], g["k"], g["v"], g["ac"], g["bc"], scale=cfg.scale, out=oc, workspace=ws,
+                       dev_err=err)
+        e[2].record(stream)
+        ev_s.append((e[0], e[1]))
+        ev_x.append((e[1], e[2]))
+    torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error word {int(err.item())}"
     return ms, _mean_ms(ev_s), _mean_ms(ev_x), o, oc, ws, err
 
@@ -639,9 +660,9 @@ def run_prefill_1m(dev, world, peaks, steps, warmup):
     nbytes = swa_bytes(B, T, Hq, Hkv, d)
     step_bytes = nbytes + xattn_bytes(pos, Hq, Hkv, d, T)
     return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "config": _config_line(cfg), "xattn_ms": x_ms,
-            "roofline": hbm_roofline("swa_tc", nbytes, swa_ms, peaks, f"swa_fwd_{cfg.name}", SWA_SOURCES),
-            "step_frac": step_bytes / (ms / 1e3) / 1e9 / peaks["hbm"], "step_algorithmic_bytes": step_bytes,
+            "config": _config_line(cfg), "xattn_alone_ms": x_ms,
+            "roofline": step_roofline(nbytes, step_bytes, ms, peaks, cfg.name),
+            "swa_alone": hbm_roofline("swa_tc", nbytes, swa_ms, peaks, f"swa_fwd_{cfg.name}", SWA_SOURCES),
             "gpu_launches": steps * launches_per_prefill_step(cfg)}
 
 
@@ -683,9 +704,10 @@ def run_gpu(args):
         "metric": METRIC, "value": tokens * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config_line(cfg),
-        "roofline": hbm_roofline("swa_tc", nbytes, swa_ms, peaks, f"swa_fwd_{cfg.name}", SWA_SOURCES),
+        "roofline": step_roofline(nbytes, step_bytes, ms, peaks, cfg.name),
+        "swa_alone": hbm_roofline("swa_tc", nbytes, swa_ms, peaks, f"swa_fwd_{cfg.name}", SWA_SOURCES),
         "step": {"algorithmic_bytes": step_bytes, "frac": step_bytes / (ms / 1e3) / 1e9 / peaks["hbm"],
-                 "swa_ms": swa_ms, "xattn_ms": x_ms},
+                 "swa_alone_ms": swa_ms, "xattn_alone_ms": x_ms},
         "gpu_launches": args.steps * launches_per_prefill_step(cfg),
         "clocks": clocks,
     }

@@ -191,13 +191,19 @@ size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, 
 
 /*
  * One prefill layer in one call (the paper has no counterpart; a convenience):
- * Eq. (4) for the base stream, then Eq. (5) for T_out output copies over the
- * base K/V up to their original positions (Sec. 3.2, prefill mode).  Exactly
- * orthros_swa_fwd followed by orthros_xattn_fwd with T_kv = T on the same
- * stream, with the same results and error behaviour (three kernel launches; the
- * copies' kernel reads K/V a second time).  A variant that attended the copies
- * inside the SWA pass, reading K/V once, measured no faster on GB300: the extra
- * work in the SWA kernel cost as much time as the second read saves.
+ * Eq. (4) for the base stream and Eq. (5) for T_out output copies over the base
+ * K/V up to their original positions (Sec. 3.2, prefill mode), with the results
+ * and error behaviour of orthros_swa_fwd and orthros_xattn_fwd with T_kv = T
+ * (bit for bit).  For few copies (the split-KV path of orthros_xattn_fwd) the
+ * copies' kernels run on a second stream of the library's own, forked from and
+ * joined back into `stream` with events, while the SWA kernel, which is bound by
+ * its MMA issue, holds fewer SMs: the copies' pass, bound by HBM, takes the rest
+ * and the spare bandwidth (three kernel launches; the copies' kernel reads K/V a
+ * second time).  Work queued on `stream` after the call runs after both.  For
+ * many copies the two run one after the other on `stream`.  Capturable in a CUDA
+ * graph.  A variant that attended the copies inside the SWA pass, reading K/V
+ * once, measured no faster on GB300: the extra work in the SWA kernel cost as
+ * much time as the second read saves.
  *
  *   q_raw, k, v, alpha, beta, o, window, q_bstride, kv_bstride, o_bstride:
  *          as orthros_swa_fwd

@@ -184,7 +184,8 @@ orthros_status swa_setup(const orthros_bf16 *q_raw, const orthros_bf16 *k, const
 orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
                             const float *alpha, const float *beta, orthros_bf16 *o, float *lse, int B, int T, int Hq,
                             int Hkv, int d, int window, float scale, int64_t q_bstride, int64_t kv_bstride,
-                            int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream)
+                            int64_t o_bstride, int row_begin, int row_end, int32_t *dev_err, void *stream,
+                            int sm_reserve = 0)
 {
     CUtensorMap maps[4];
     SwaParams p;
@@ -193,7 +194,7 @@ orthros_status swa_fwd_impl(const orthros_bf16 *q_raw, const orthros_bf16 *k, co
                                         kv_bstride, o_bstride, row_begin, row_end, dev_err, maps, p, &empty);
     if (st != ORTHROS_OK || empty)
         return st;
-    const int sms = num_sms();
+    const int sms = num_sms() - sm_reserve;  // the persistent kernel's CTAs
     if (sms <= 0)
         return ORTHROS_ERR_CUDA;
     const cudaError_t e =
@@ -339,6 +340,42 @@ size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, 
     return T_out == 0 ? 256 : orthros::xattn_workspace_bytes(B, T_out, T, Hq, Hkv, d);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The stream on which orthros_prefill_fwd runs the copies' pass beside the SWA kernel: one per
+// device, created on first use and kept for the life of the process.
+cudaStream_t copy_stream()
+{
+    static std::mutex mu;
+    static cudaStream_t streams[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (streams[dev] == nullptr && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+        streams[dev] = nullptr;
+    return streams[dev];
+}
+
+// SMs that the persistent SWA kernel leaves to the copies' split-KV pass so that the two, run at
+// once, end together: SMs shared in proportion to each pass's bytes over its per-SM rate.  On a
+// GB300 the SWA kernel (bound by its MMA issue) moves about 37 GB/s per SM and the split-KV pass
+// about 1.7 times that once the SWA kernel holds the other SMs.
+int copy_sm_reserve(int sms, int B, int T, int Hq, int Hkv, int d)
+{
+    const double swa_bytes = 2.0 * B * T * (2.0 * Hq + 2.0 * Hkv) * d;  // q, o, K, V
+    const double copy_bytes = 2.0 * B * T * 2.0 * Hkv * d;              // K, V up to the last position
+    const double c = (copy_bytes / 1.7) / swa_bytes;
+    const int x = static_cast<int>(std::lround(sms * c / (1.0 + c)));
+    return x < 2 ? 0 : (x > sms / 4 ? sms / 4 : x);
+}
+
+}  // namespace
+
+extern "C" {
+
 orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16 *k, const orthros_bf16 *v,
                                    const float *alpha, const float *beta, orthros_bf16 *o, const orthros_bf16 *qc_raw,
                                    const int32_t *pos, const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
@@ -351,12 +388,46 @@ orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16
         return ORTHROS_ERR_INVALID_ARG;
     if (T_out > 0 && (!workspace || ws_bytes < orthros_prefill_workspace_size(B, T, T_out, Hq, Hkv, d)))
         return ORTHROS_ERR_WORKSPACE;
-    const orthros_status st = orthros_swa_fwd(q_raw, k, v, alpha, beta, o, B, T, Hq, Hkv, d, window, scale,
-                                              q_bstride, kv_bstride, o_bstride, dev_err, stream);
-    if (st != ORTHROS_OK || T_out == 0)
-        return st;
-    return orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T, Hq, Hkv, d, scale, qc_bstride,
-                             kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, stream);
+    // Few copies (the split-KV pass, bound by HBM) run on a second stream while the SWA kernel,
+    // bound by its MMA issue and holding fewer SMs, runs on the caller's; the caller's stream
+    // waits for both.  Many copies (the tensor-memory kernel) run after the SWA kernel.
+    const int sms = num_sms();
+    const bool overlap = T_out > 0 && (d == 64 || d == 128) && heads_ok(Hq, Hkv) &&
+                         !orthros::xattn_tc_supported(d, Hq / Hkv, T_out) && sms > 0;
+    const int reserve = overlap ? copy_sm_reserve(sms, B, T, Hq, Hkv, d) : 0;
+    cudaStream_t cs = reserve > 0 ? copy_stream() : nullptr;
+    if (cs == nullptr) {
+        const orthros_status st = orthros_swa_fwd(q_raw, k, v, alpha, beta, o, B, T, Hq, Hkv, d, window, scale,
+                                                  q_bstride, kv_bstride, o_bstride, dev_err, stream);
+        if (st != ORTHROS_OK || T_out == 0)
+            return st;
+        return orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T, Hq, Hkv, d, scale, qc_bstride,
+                                 kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, stream);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+        if (fork)
+            cudaEventDestroy(fork);
+        return ORTHROS_ERR_CUDA;
+    }
+    orthros_status st = ORTHROS_ERR_CUDA;
+    if (cudaEventRecord(fork, s) == cudaSuccess && cudaStreamWaitEvent(cs, fork, 0) == cudaSuccess) {
+        // the SWA kernel is launched first so that its persistent CTAs take their SMs first
+        st = swa_fwd_impl(q_raw, k, v, alpha, beta, o, nullptr, B, T, Hq, Hkv, d, window, scale, q_bstride,
+                          kv_bstride, o_bstride, 0, T < 1 ? 0 : T, dev_err, stream, reserve);
+        if (st == ORTHROS_OK)
+            st = orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T, Hq, Hkv, d, scale,
+                                   qc_bstride, kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, cs);
+        // the caller's stream waits for whatever the copy stream was given
+        if ((cudaEventRecord(join, cs) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess) &&
+            st == ORTHROS_OK)
+            st = ORTHROS_ERR_CUDA;
+    }
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    return st;
 }
 
 size_t orthros_decode_workspace_size(int B, int L_max, int Hq, int Hkv, int d)

@@ -1,6 +1,8 @@
 """GPU parity of the one-call prefill layer (orthros_prefill_fwd) against the fp64
-oracle: the base stream (Eq. 4) and the output copies (Eq. 5) of one call.  The
-base output must also equal a separate orthros_swa_fwd bit for bit."""
+oracle: the base stream (Eq. 4) and the output copies (Eq. 5) of one call.  Both
+outputs must also equal separate orthros_swa_fwd / orthros_xattn_fwd calls bit for bit
+(for few copies the call runs the copies' pass on a second stream beside the SWA
+kernel, which holds fewer SMs; neither changes any result)."""
 import numpy as np
 import pytest
 import torch
@@ -23,7 +25,9 @@ def _run(inp, window=None):
     o, oc = orth.prefill_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), qc, i32(inp.pos), f32(inp.alpha_c),
                              f32(inp.beta_c), window=w, scale=cfg.scale, dev_err=err)
     o_swa = orth.swa_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), window=w, scale=cfg.scale, dev_err=err)
+    oc_x = orth.xattn_fwd(qc, i32(inp.pos), k, v, f32(inp.alpha_c), f32(inp.beta_c), scale=cfg.scale, dev_err=err)
     torch.cuda.synchronize()
+    assert torch.equal(oc.view(torch.int16), oc_x.view(torch.int16)), "copy output differs from xattn_fwd"
     return o, oc, o_swa, int(err.item())
 
 
@@ -119,3 +123,59 @@ def test_prefill_call_bad_and_early_positions(T, Hq, Hkv):
                                    np.ascontiguousarray(inp.pos[b:b + 1, i:i + 1]), inp.k[b:b + 1], inp.v[b:b + 1],
                                    inp.alpha_c, inp.beta_c, cfg.scale)
                 assert_parity(got[b:b + 1, i:i + 1], ref, f"copy ({b}, {i})")
+
+
+def test_prefill_call_stream_order():
+    """Back-to-back calls with K rewritten on the caller's stream between them: the copies'
+    pass (on the second stream) of each call sees the K of its own call."""
+    cfg = PrefillConfig("call_order", B=2, T=4096, Hq=32, Hkv=8, d=128, T_out=1)
+    inp = make_prefill(cfg, 47)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    q, k, v = bf(inp.q_raw), bf(inp.k), bf(inp.v)
+    qc, pos = bf(inp.qc_raw), i32(inp.pos)
+    a, b, ac, bc = f32(inp.alpha), f32(inp.beta), f32(inp.alpha_c), f32(inp.beta_c)
+    outs = []
+    for it in range(3):
+        o, oc = orth.prefill_fwd(q, k, v, a, b, qc, pos, ac, bc, window=cfg.window, scale=cfg.scale, dev_err=err)
+        outs.append((o, oc, k.clone()))
+        k.mul_(-1.0)  # on the caller's stream, right behind the call
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for o, oc, kk in outs:
+        o_ref = orth.swa_fwd(q, kk, v, a, b, window=cfg.window, scale=cfg.scale)
+        oc_ref = orth.xattn_fwd(qc, pos, kk, v, ac, bc, scale=cfg.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(oc.view(torch.int16), oc_ref.view(torch.int16))
+
+
+def test_prefill_call_cuda_graph():
+    """The call captured in a CUDA graph (its second stream joins the capture) and replayed
+    gives the eager call's bits."""
+    cfg = PrefillConfig("call_graph", B=2, T=4096, Hq=32, Hkv=8, d=128, T_out=1)
+    inp = make_prefill(cfg, 48)
+    q, k, v = bf(inp.q_raw), bf(inp.k), bf(inp.v)
+    qc, pos = bf(inp.qc_raw), i32(inp.pos)
+    a, b, ac, bc = f32(inp.alpha), f32(inp.beta), f32(inp.alpha_c), f32(inp.beta_c)
+    ws = torch.empty(max(orth.prefill_workspace_size(cfg.B, cfg.T, cfg.T_out, cfg.Hq, cfg.Hkv, cfg.d), 256),
+                     dtype=torch.uint8, device=dev())
+    o = torch.empty((cfg.B, cfg.T, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=dev())
+    oc = torch.empty((cfg.B, cfg.T_out, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=dev())
+    o_e, oc_e = orth.prefill_fwd(q, k, v, a, b, qc, pos, ac, bc, window=cfg.window, scale=cfg.scale)
+    s = torch.cuda.Stream(dev())
+    s.wait_stream(torch.cuda.current_stream(dev()))
+    with torch.cuda.stream(s):  # warm the call on the capture stream
+        orth.prefill_fwd(q, k, v, a, b, qc, pos, ac, bc, window=cfg.window, scale=cfg.scale, out=o, out_c=oc,
+                         workspace=ws)
+    torch.cuda.current_stream(dev()).wait_stream(s)
+    torch.cuda.synchronize()
+    o.zero_()
+    oc.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        orth.prefill_fwd(q, k, v, a, b, qc, pos, ac, bc, window=cfg.window, scale=cfg.scale, out=o, out_c=oc,
+                         workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o_e.view(torch.int16))
+    assert torch.equal(oc.view(torch.int16), oc_e.view(torch.int16))
