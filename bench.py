@@ -210,7 +210,8 @@ def launches_per_prefill_step(cfg) -> int:
     splits = min(max(1, math.ceil(304 / base)), math.ceil(cfg.T / 256))
     chunk = math.ceil(math.ceil(cfg.T / splits) / 64) * 64
     splits = math.ceil(cfg.T / chunk)
-    return 2 + (0 if splits * wk == 1 else 1)
+    n_part = splits if rows <= 8 else splits * wk  # at most 8 rows: one partial per CTA
+    return 2 + (0 if n_part == 1 else 1)
 
 
 def bwd_launches_per_call(T_out, G, window) -> int:

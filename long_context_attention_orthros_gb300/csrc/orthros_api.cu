@@ -362,12 +362,12 @@ cudaStream_t copy_stream()
 // SMs that the persistent SWA kernel leaves to the copies' split-KV pass so that the two, run at
 // once, end together: SMs shared in proportion to each pass's bytes over its per-SM rate.  On a
 // GB300 the SWA kernel (bound by its MMA issue) moves about 37 GB/s per SM and the split-KV pass
-// about 1.7 times that once the SWA kernel holds the other SMs.
+// about twice that once the SWA kernel holds the other SMs.
 int copy_sm_reserve(int sms, int B, int T, int Hq, int Hkv, int d)
 {
     const double swa_bytes = 2.0 * B * T * (2.0 * Hq + 2.0 * Hkv) * d;  // q, o, K, V
     const double copy_bytes = 2.0 * B * T * 2.0 * Hkv * d;              // K, V up to the last position
-    const double c = (copy_bytes / 1.7) / swa_bytes;
+    const double c = (copy_bytes / 2.0) / swa_bytes;
     const int x = static_cast<int>(std::lround(sms * c / (1.0 + c)));
     return x < 2 ? 0 : (x > sms / 4 ? sms / 4 : x);
 }

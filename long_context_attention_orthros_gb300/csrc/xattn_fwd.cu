@@ -14,12 +14,16 @@
 // 3-stage TMA ring (64-key blocks, 128-byte swizzle) filled by one producer
 // warp; kmax is the largest position among its rows.  Four consumer warps run
 // the online softmax with warp MMAs:
-//   * few rows (T_out * G <= 16): all four warps share the same 16 rows and
-//     take every fourth 16-key chunk of a block (4 partial results per CTA);
+//   * at most 8 rows (T_out * G <= 8, e.g. one copy of G = 4 heads): the rows on
+//     the MMA's N side and 16 keys on M (half the MMAs of a 16-row tile); each
+//     warp takes one 16-key chunk of every block and the four warps merge their
+//     results in shared memory (one partial per CTA);
+//   * up to 16 rows: all four warps share the same 16 rows and take every
+//     fourth 16-key chunk of a block (4 partial results per CTA);
 //   * many rows: each warp owns 16 rows and walks every chunk.
-// Each warp writes an unnormalised partial (max, sum, o[d]) per row; a second
-// kernel merges the partials of a row with a warp-shuffle log-sum-exp reduction.
-// When a row has a single partial the first kernel writes the output directly.
+// Partials are unnormalised (max, sum, o[d]) per row; a second kernel merges the
+// partials of a row with a warp-shuffle log-sum-exp reduction.  When a row has a
+// single partial the first kernel writes the output directly.
 #include "kernels.cuh"
 #include "xattn.cuh"
 
@@ -205,6 +209,195 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
     }
 }
 
+// At most 8 rows of one (batch, KV head): grid (split, 1, batch * KV head).  The rows sit on the
+// MMA's N side (WarpKeys16: S^T = K q^T, O^T += V^T P^T), warp w takes keys 16 w .. 16 w + 15 of
+// every 64-key block, and the four warps' (max, sum, o) are merged in shared memory (the ring is
+// free once every block has been consumed) into one partial per CTA, or the output when the CTA
+// is the row's only split.
+template <int D>
+__global__ void __launch_bounds__(XCfg<D>::THREADS)
+    xattn_partial_keys_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                              const XattnParams p)
+{
+    using C = XCfg<D>;
+    constexpr int RMAX = 8;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_s + pad;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    int *s_pos = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [RMAX], -1 = masked row
+
+    const int split = blockIdx.x, bh = blockIdx.z;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x < RMAX) {
+        const int r = threadIdx.x;
+        int ps = -1;
+        if (r < p.R) {
+            ps = p.pos[static_cast<long long>(b) * p.T_out + r / p.G];
+            if (ps < 0 || ps >= p.T_kv) {
+                if (split == 0 && r % p.G == 0)
+                    record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
+                ps = -1;
+            }
+        }
+        s_pos[r] = ps;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    int kmax = -1;
+    for (int i = 0; i < RMAX; ++i)
+        kmax = max(kmax, s_pos[i]);
+    const int js = split * p.chunk;
+    const int je = min(js + p.chunk, kmax + 1);
+    const int nblk = je > js ? (je - js + C::KB - 1) / C::KB : 0;
+
+    if (warp == C::CWARPS) {
+        if (lane != 0)
+            return;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        for (int i = 0; i < nblk; ++i) {
+            const int s = i % C::STAGES;
+            if (i >= C::STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / C::STAGES) - 1) & 1))) {
+                record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+                return;
+            }
+            uint8_t *dst = smem + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl) {
+                tma_load_4d(dst + sl * C::SLAB, &kmap, &full[s], sl * 64, g, js + i * C::KB, b);
+                tma_load_4d(dst + C::KV_BYTES + sl * C::SLAB, &vmap, &full[s], sl * 64, g,
+                            js + i * C::KB, b);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // q^T fragments hold row lane / 4; the lane keeps rows 2 (lane % 4) + {0, 1}.  Padding rows
+    // (beyond R) borrow kmax so they never force the masked path; their results are never
+    // written.  Rows with a bad position keep -1 (every key masked).
+    WarpKeys16<D, 1, false> st;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int row = lane >> 2;
+            const int dcol = kt * 16 + 2 * (lane & 3) + 8 * hf;
+            uint32_t hi = 0, lo = 0;
+            if (row < p.R && s_pos[row] >= 0) {
+                const int h = g * p.G + row % p.G;
+                const orthros_bf16 *qrow = p.qc + b * p.qc_bstride + (static_cast<long long>(row / p.G) * p.Hq + h) * D;
+                load_q_pair(qrow, p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale, hi, lo);
+            }
+            st.qb[0][kt][hf] = hi;
+            st.ql[0][kt][hf] = lo;
+        }
+    st.reset();
+    auto lim_of = [&](int r) { return r < p.R ? s_pos[r] : kmax; };
+    int lim[1][2];
+    lim[0][0] = lim_of(2 * (lane & 3));
+    lim[0][1] = lim_of(2 * (lane & 3) + 1);
+    int pmin = 0x7fffffff, pmax = -1;
+    for (int i = 0; i < RMAX; ++i) {
+        pmin = min(pmin, lim_of(i));
+        pmax = max(pmax, lim_of(i));
+    }
+
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+        const int s = i % C::STAGES;
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((i / C::STAGES) & 1))) {
+            ok = false;
+            break;
+        }
+        const uint32_t kbase = sbase + s * C::STAGE_BYTES;
+        const int j0 = js + i * C::KB + warp * 16;
+        if (j0 <= pmax)
+            st.step(kbase, C::SLAB, kbase + C::KV_BYTES, C::SLAB, warp * 16, j0, lim, j0 + 15 <= pmin);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+    st.finish_sums();
+
+    // the four warps' results, each scaled to the CTA's max, summed through shared memory
+    constexpr int CT = C::CWARPS * 32;
+    float *ms = reinterpret_cast<float *>(smem);  // [CWARPS][RMAX] max
+    float *ls = ms + C::CWARPS * RMAX;            // [CWARPS][RMAX] sum
+    float *os = ls + C::CWARPS * RMAX;            // [CWARPS][RMAX][D] output
+    named_barrier(3, CT);  // every warp is past its last block: the ring may be overwritten
+#pragma unroll
+    for (int r2 = 0; r2 < 2; ++r2)
+        if ((lane >> 2) == 0) {
+            ms[warp * RMAX + 2 * lane + r2] = st.m[0][r2];
+            ls[warp * RMAX + 2 * lane + r2] = st.l[0][r2];
+        }
+    named_barrier(3, CT);
+    const float NEG_INF = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int r2 = 0; r2 < 2; ++r2) {
+        const int row = 2 * (lane & 3) + r2;
+        float M = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < C::CWARPS; ++w)
+            M = fmaxf(M, ms[w * RMAX + row]);
+        const float f = (M == NEG_INF || st.m[0][r2] == NEG_INF) ? 0.f : fast_exp2(st.m[0][r2] - M);
+        float *po = os + (warp * RMAX + row) * D + (lane >> 2);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            po[16 * mt] = st.o[0][mt][r2] * f;
+            po[16 * mt + 8] = st.o[0][mt][2 + r2] * f;
+        }
+    }
+    named_barrier(3, CT);
+    const int BH = p.B * p.Hkv;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < p.R * (D / 2); i += CT) {  // two columns per thread and step
+        const int row = i / (D / 2), c = 2 * (i % (D / 2));
+        float M = NEG_INF, L = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::CWARPS; ++w)
+            M = fmaxf(M, ms[w * RMAX + row]);
+#pragma unroll
+        for (int w = 0; w < C::CWARPS; ++w) {
+            if (ms[w * RMAX + row] != NEG_INF)
+                L += ls[w * RMAX + row] * fast_exp2(ms[w * RMAX + row] - M);
+            a0 += os[(w * RMAX + row) * D + c];
+            a1 += os[(w * RMAX + row) * D + c + 1];
+        }
+        const int h = g * p.G + row % p.G, copy = row / p.G;
+        if (p.direct) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            *reinterpret_cast<uint32_t *>(p.oc + b * p.oc_bstride + (static_cast<long long>(copy) * p.Hq + h) * D + c) =
+                pack_bf16x2(a0 * inv, a1 * inv);
+            if (c == 0 && p.lse != nullptr)
+                p.lse[(static_cast<long long>(b) * p.T_out + copy) * p.Hq + h] =
+                    L > 0.f ? (M + __log2f(L)) * kLn2F : NEG_INF;
+        } else {
+            const long long slot = (static_cast<long long>(split) * BH + bh) * p.R + row;
+            *reinterpret_cast<float2 *>(p.part_o + slot * D + c) = make_float2(a0, a1);
+            if (c == 0)
+                p.part_ml[slot] = make_float2(M, L);
+        }
+    }
+}
+
 // One warp per output row: merge the row's partial (max, sum, o) triples.
 template <int D>
 __global__ void __launch_bounds__(128) xattn_combine_kernel(const XattnParams p)
@@ -304,7 +497,7 @@ __global__ void __launch_bounds__(128) xattn_combine_kernel(const XattnParams p)
 // ------------------------------------------------------------------ host side
 
 struct XattnPlan {
-    int WK, RPC, row_tiles, splits, chunk, n_part, direct;
+    int WK, RPC, row_tiles, splits, chunk, n_part, direct, keys;
 };
 
 // Deterministic split plan (also used by the workspace-size query): aim for about
@@ -330,7 +523,8 @@ XattnPlan xattn_plan(int B, int T_out, int T_kv, int Hq, int Hkv)
     splits = (T_kv + chunk - 1) / chunk;
     pl.splits = static_cast<int>(splits);
     pl.chunk = static_cast<int>(chunk);
-    pl.n_part = pl.splits * pl.WK;
+    pl.keys = R <= 8 ? 1 : 0;  // rows on the MMA's N side, one partial per CTA
+    pl.n_part = pl.keys ? pl.splits : pl.splits * pl.WK;
     pl.direct = pl.n_part == 1 ? 1 : 0;
     return pl;
 }
@@ -361,6 +555,19 @@ static cudaError_t launch_partial(const CUtensorMap &k, const CUtensorMap &v, co
     return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_partial_keys(const CUtensorMap &k, const CUtensorMap &v, const XattnParams &p,
+                                       cudaStream_t stream)
+{
+    auto kern = xattn_partial_keys_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<D>::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid(p.splits, 1, p.B * p.Hkv);
+    kern<<<grid, XCfg<D>::THREADS, XCfg<D>::SMEM, stream>>>(k, v, p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p,
                          void *workspace, cudaStream_t stream)
 {
@@ -379,7 +586,9 @@ cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, Xatt
         p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
     }
     cudaError_t e;
-    if (D == 128)
+    if (pl.keys)
+        e = D == 128 ? launch_partial_keys<128>(k, v, p, stream) : launch_partial_keys<64>(k, v, p, stream);
+    else if (D == 128)
         e = pl.WK == 4 ? launch_partial<128, 4>(k, v, p, stream) : launch_partial<128, 1>(k, v, p, stream);
     else
         e = pl.WK == 4 ? launch_partial<64, 4>(k, v, p, stream) : launch_partial<64, 1>(k, v, p, stream);
