@@ -374,7 +374,11 @@ size_t orthros_xattn_bwd_workspace_size(int B, int T_out, int T_kv, int Hq, int 
  * memory in two passes (the first finds each copy row's log-sum-exp; skipped
  * when lse is given); when one 128-row tile per (batch, KV head) holds every
  * copy, its key range is split over many CTAs (without lse: per-split maxima
- * and sums and a combine first; then per-split dq added up).
+ * and sums and a combine first; then per-split dq added up).  With lse and at
+ * most 8 copy rows per KV head (T_out * Hq / Hkv <= 8) the dq runs on warp MMAs
+ * instead, q . k with q as a bf16 high part plus residual against the bf16 K
+ * (no fp16 K, no key shifts), dS rounded to bf16, the keys split over CTAs and
+ * each split's dq, dalpha_c, dbeta_c added with atomics.
  * T_out == 0 leaves dk, dv as they are (accumulate) or zero.  Outputs must not
  * alias inputs.
  */

@@ -23,8 +23,12 @@
 //                           atomics;
 //   attn_bwd_dq_tc_base_kernel + attn_bwd_dab_kernel  (base stream with it) the same on
 //                           tcgen05, persistent, then the dalpha / dbeta column sums;
+//   attn_bwd_dq_band_kernel (base stream with it, G >= 4, narrow windows) tcgen05, each row
+//                           tile's whole key band per MMA, dalpha / dbeta folded in (below);
 //   attn_bwd_dq_tc_kernel   (copies) the same on tcgen05, one or two passes, optionally
 //                           split over the keys (below);
+//   attn_bwd_dq_copies_keys_kernel  (copies with it, at most 8 rows per KV head) warp MMAs
+//                           with the rows on N, keys split over CTAs (below);
 //   attn_bwd_dkv_tc_kernel  keys on tcgen05's M side, dK and dV in tensor memory (below),
 //                           for one stream or for both of a layer.
 // P enters dV as bf16; dS enters dQ as bf16 and dK as fp16 (beside the fp16 q).
@@ -1724,6 +1728,229 @@ __global__ void __launch_bounds__(DKV_TC_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ copies' dQ, few rows
+
+// At most 8 copy rows of one (batch, KV head) (one copy of G = 4 heads, say) with the forward's
+// log-sum-exp known: a tensor-memory tile would carry 120 empty rows of its 128.  Here the rows
+// sit on the warp MMA's N side and 16 keys on M, as in the forward's split-KV kernel:
+//   S^T = K q^T (q = (x alpha + beta) scale log2(e) as bf16 high part + residual, so S is in
+//   log2 units), dP^T = V dO^T, P^T = exp2(S^T - lse2), dS^T = P^T (dP^T - D) (rounded to bf16),
+//   dQ^T += K^T dS^T,
+// with K and V read as bf16 straight from the inputs.  Grid (split, 1, batch * KV head); the keys
+// 0 .. max(pos) of the CTA's rows are split into chunks of 64-key blocks, which stream through a
+// 3-stage TMA ring; warp w takes keys 16 w .. 16 w + 15 of every block, and the four warps' dQ
+// are summed through shared memory.  The CTA then adds its share: dq_raw += scale dQ alpha,
+// dalpha += x scale dQ, dbeta += scale dQ (all linear in dQ; dq_raw zeroed first unless there is
+// one split, which stores it, zeros included for rows without a valid position).
+template <int D>
+struct BkCfg {
+    static constexpr int KB = 64;
+    static constexpr int SLAB = KB * 128;
+    static constexpr int KV_BYTES = KB * D * 2;
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+    static constexpr int STAGES = 3;
+    static constexpr int CWARPS = 4;
+    static constexpr int THREADS = (CWARPS + 1) * 32;
+    static constexpr int RMAX = 8;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int MISC_OFF = BAR_OFF + 2 * STAGES * 8;  // int [RMAX] positions
+    static constexpr int SMEM = MISC_OFF + RMAX * 4 + 1024;
+    static_assert(CWARPS * RMAX * D * 4 <= BAR_OFF, "the dQ merge fits in the ring");
+};
+
+template <int D>
+__global__ void __launch_bounds__(BkCfg<D>::THREADS)
+    attn_bwd_dq_copies_keys_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                                   const AttnBwdParams p)
+{
+    using C = BkCfg<D>;
+    constexpr int RMAX = C::RMAX;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    int *s_pos = reinterpret_cast<int *>(smem + C::MISC_OFF);
+
+    const int G = p.Hq / p.Hkv, R = p.n_units * G;
+    const int split = blockIdx.x, bh = blockIdx.z;
+    const int b = bh / p.Hkv, g = bh % p.Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x < RMAX) {
+        const int r = threadIdx.x;
+        const int P = r < R ? unit_pos<true>(p, b, r / G) : -1;
+        if (r < R && P < 0 && r % G == 0 && split == 0)
+            record_error(p.dev_err, ORTHROS_DEVERR_POSITION);
+        s_pos[r] = P;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    int kmax = -1;
+    for (int i = 0; i < RMAX; ++i)
+        kmax = max(kmax, s_pos[i]);
+    const int nbk = (kmax + C::KB) / C::KB;  // blocks of keys 0 .. kmax
+    const int per = (nbk + p.splits - 1) / p.splits;
+    const int blk0 = split * per, nblk = max(0, min(per, nbk - blk0));
+
+    if (warp == C::CWARPS) {
+        // ------------------------------------------------------------------ producer
+        if (lane != 0)
+            return;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        for (int i = 0; i < nblk; ++i) {
+            const int s = i % C::STAGES;
+            if (i >= C::STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / C::STAGES) - 1) & 1))) {
+                record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+                return;
+            }
+            uint8_t *dst = smem + s * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl) {
+                tma_load_4d(dst + sl * C::SLAB, &kmap, &full[s], sl * 64, g, (blk0 + i) * C::KB, b);
+                tma_load_4d(dst + C::KV_BYTES + sl * C::SLAB, &vmap, &full[s], sl * 64, g, (blk0 + i) * C::KB, b);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // B fragments hold row lane / 4 (q^T high / residual, dO^T); the lane's accumulators hold rows
+    // 2 (lane % 4) + {0, 1} and, for dQ^T, d = 16 mt + lane / 4 (+ 8)
+    const float c2 = p.scale * kLog2eF;
+    uint32_t qb[D / 16][2], ql[D / 16][2], ob[D / 16][2];
+    {
+        const int row = lane >> 2;
+        const bool valid = row < R && s_pos[row] >= 0;
+        const int h = g * G + row % G;
+        const long long ri = (static_cast<long long>(b) * p.n_units + row / G) * p.Hq + h;
+#pragma unroll
+        for (int kt = 0; kt < D / 16; ++kt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int dcol = kt * 16 + 2 * (lane & 3) + 8 * hf;
+                uint32_t hi = 0, lo = 0, ow = 0;
+                if (valid) {
+                    load_q_pair(p.q + ri * D, p.alpha + h * D, p.beta + h * D, dcol, c2, hi, lo);
+                    ow = __ldg(reinterpret_cast<const unsigned int *>(p.dO + ri * D + dcol));
+                }
+                qb[kt][hf] = hi;
+                ql[kt][hf] = lo;
+                ob[kt][hf] = ow;
+            }
+    }
+    int lim[2];
+    float lse2[2], Dr[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int row = 2 * (lane & 3) + i;
+        const int P = row < R ? s_pos[row] : -1;
+        lim[i] = P;
+        const long long ri = (static_cast<long long>(b) * p.n_units + row / G) * p.Hq + g * G + row % G;
+        lse2[i] = P >= 0 ? p.lse[ri] : 0.f;
+        Dr[i] = P >= 0 ? p.Drow[ri] : 0.f;
+    }
+    float dq[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+        dq[mt][0] = dq[mt][1] = dq[mt][2] = dq[mt][3] = 0.f;
+    // ldmatrix rows: A of K and of V (16 keys x 16 d, row-major), A of K^T (16 d x 16 keys)
+    const int ka_row = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), ka_hi = lane >> 4;
+    const int ta_row = warp * 16 + (lane & 7) + ((lane >> 4) << 3), ta_hi = (lane >> 3) & 1;
+
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+        const int s = i % C::STAGES;
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((i / C::STAGES) & 1))) {
+            ok = false;
+            break;
+        }
+        const uint32_t kbase = sbase + s * C::STAGE_BYTES, vbase = kbase + C::KV_BYTES;
+        const int j0 = (blk0 + i) * C::KB + warp * 16;
+        if (j0 <= kmax) {
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kt = 0; kt < D / 16; ++kt) {
+                uint32_t a[4], v[4];
+                const uint32_t off = (kt * 16 / 64) * C::SLAB + sw128_offset(ka_row, ((kt * 16) % 64) / 8 + ka_hi);
+                ldsm_x4(kbase + off, a[0], a[1], a[2], a[3]);
+                ldsm_x4(vbase + off, v[0], v[1], v[2], v[3]);
+                float *s1 = (kt & 1) ? sb : sa, *d1 = (kt & 1) ? db : da;
+                mma_16816(s1, a, qb[kt][0], qb[kt][1]);
+                mma_16816(s1, a, ql[kt][0], ql[kt][1]);
+                mma_16816(d1, v, ob[kt][0], ob[kt][1]);
+            }
+            // element e: key j0 + lane / 4 + 8 (e >> 1), row 2 (lane % 4) + (e & 1)
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = j0 + (lane >> 2) + ((e >> 1) << 3), ri = e & 1;
+                const float pr = key <= lim[ri] ? fast_exp2(sa[e] + sb[e] - lse2[ri]) : 0.f;
+                ds[e] = pr * (da[e] + db[e] - Dr[ri]);
+            }
+            const uint32_t b0 = movmatrix_trans(pack_bf16x2(ds[0], ds[1]));
+            const uint32_t b1 = movmatrix_trans(pack_bf16x2(ds[2], ds[3]));
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_trans(kbase + (mt * 16 / 64) * C::SLAB + sw128_offset(ta_row, ((mt * 16) % 64) / 8 + ta_hi),
+                              a[0], a[1], a[2], a[3]);
+                mma_16816(dq[mt], a, b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);
+    }
+    if (!ok && lane == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+
+    // the four warps' dQ^T summed through shared memory (the ring is free once every warp is past
+    // its last block), then this CTA's share added to the outputs
+    constexpr int CT = C::CWARPS * 32;
+    float *os = reinterpret_cast<float *>(smem);  // [CWARPS][RMAX][D]
+    named_barrier(2, CT);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float *po = os + (warp * RMAX + 2 * (lane & 3) + i) * D + (lane >> 2);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            po[16 * mt] = dq[mt][i];
+            po[16 * mt + 8] = dq[mt][2 + i];
+        }
+    }
+    named_barrier(2, CT);
+    for (int i = threadIdx.x; i < R * D; i += CT) {
+        const int row = i / D, c = i % D;
+        const int h = g * G + row % G;
+        const long long ri = (static_cast<long long>(b) * p.n_units + row / G) * p.Hq + h;
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::CWARPS; ++w)
+            a += os[(w * RMAX + row) * D + c];
+        const float dqv = s_pos[row] >= 0 ? a * p.scale : 0.f;
+        if (p.splits == 1) {
+            p.dq[ri * D + c] = dqv * p.alpha[h * D + c];
+        } else if (s_pos[row] >= 0) {
+            atomicAdd(p.dq + ri * D + c, dqv * p.alpha[h * D + c]);
+        }
+        if (s_pos[row] >= 0) {
+            const float x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(p.q)[ri * D + c]) << 16);
+            atomicAdd(p.dalpha + h * D + c, x * dqv);
+            atomicAdd(p.dbeta + h * D + c, dqv);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ base-stream dQ over the key band
 
 // Persistent like the kernel above, but a row tile's whole key band is one MMA wide.  Keys stream
@@ -2316,7 +2543,24 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
         // faster there (whole base gradient of a 2 x 128K-token, 32/8-head, w = 128 layer:
         // 21.6 vs 23.5 ms with the forward's log-sum-exp, 23.4 vs 24.5 ms without); copies
         // see long key ranges (2.54 vs 4.87 ms for 2048 copies of a 16K layer)
-        if (COPY) {
+        if (COPY && p.lse_in != nullptr && p.n_units * G <= BkCfg<D>::RMAX) {
+            // a few copy rows with the forward's log-sum-exp: rows on the warp MMA's N side, the
+            // keys split so that the grid fills the GPU (two CTAs' worth per SM)
+            int dev = 0, sms = 0;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                return e;
+            const int nbk = (p.T_kv + BkCfg<D>::KB - 1) / BkCfg<D>::KB;
+            AttnBwdParams ps = p;
+            ps.splits = max(1, min(min(ATTN_BWD_MAX_SPLITS, 2 * sms / (p.B * p.Hkv)), nbk / 4));
+            if (ps.splits >= 2 && (e = cudaMemsetAsync(p.dq, 0, sizeof(float) * rows * D, stream)) != cudaSuccess)
+                return e;
+            auto k1 = attn_bwd_dq_copies_keys_kernel<D>;
+            if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, BkCfg<D>::SMEM)) !=
+                cudaSuccess)
+                return e;
+            k1<<<dim3(ps.splits, 1, p.B * p.Hkv), BkCfg<D>::THREADS, BkCfg<D>::SMEM, stream>>>(maps[6], maps[7], ps);
+        } else if (COPY) {
             const size_t s1 = BqCfg<D>::SMEM;
             auto k1 = attn_bwd_dq_tc_kernel<D, G, COPY>;
             if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1))) !=

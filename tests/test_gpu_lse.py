@@ -173,6 +173,12 @@ def test_copy_forward_lse_of_a_bad_position_is_minus_infinity():
 
 @pytest.mark.parametrize("B,T_kv,T_out,Hq,Hkv,d,positions", XATTN_LSE_CASES + [
     (1, 16384, 3, 32, 8, 128, "random"),  # few copies over long keys: the split dq, second pass only
+    # at most 8 copy rows per KV head: the warp-MMA dq with the rows on N
+    (1, 100, 1, 32, 8, 128, "tail_shuffled"),  # one split: dq stored, not added
+    (2, 16384, 2, 8, 4, 128, "random"),        # G=2, positions anywhere (0 included)
+    (1, 3000, 1, 16, 2, 64, "random"),         # G=8, d=64
+    (1, 5000, 8, 4, 4, 128, "random"),         # G=1, 8 copies
+    (3, 20000, 2, 32, 8, 128, "tail_shuffled"),  # 8 rows, 3 sequences, keys off the block grid
 ])
 def test_copy_gradient_with_forward_lse(B, T_kv, T_out, Hq, Hkv, d, positions):
     from tests.gpu_util import i32
@@ -187,3 +193,30 @@ def test_copy_gradient_with_forward_lse(B, T_kv, T_out, Hq, Hkv, d, positions):
     ref = oracle.xattn_bwd(qc, pos, k, v, ac, bc, dOc, scale)
     for name, g, r in zip(NAMES, got, ref):
         _assert_grad(g.cpu().numpy().astype(np.float64), r, name)
+
+
+def test_copy_gradient_with_forward_lse_bad_positions_few_rows():
+    """The warp-MMA copies' dq (at most 8 rows per KV head): a copy with a position outside the
+    keys gets a zero dq row, adds nothing to dalpha / dbeta, and sets the position bit."""
+    from tests.gpu_util import i32
+    B, T_kv, T_out, Hq, Hkv, d = 2, 9000, 2, 32, 8, 128
+    qc, pos, k, v, ac, bc, dOc = _copy_inputs(7400, B, T_kv, T_out, Hq, Hkv, d, "random")
+    bad = pos.copy()
+    bad[0, 1] = T_kv
+    bad[1, 0] = -3
+    scale = 1.0 / math.sqrt(d)
+    args = (bf(qc), i32(bad), bf(k), bf(v), f32(ac), f32(bc))
+    oc, lse = orth.xattn_fwd(*args, scale=scale, lse=True)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = orth.xattn_bwd(*args, oc, bf(dOc), scale=scale, lse=lse, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & orth.DEVERR_POSITION
+    dq = got[0].cpu().numpy().astype(np.float64)
+    assert (dq[0, 1] == 0).all() and (dq[1, 0] == 0).all()
+    # the valid copies alone, one sequence at a time, against the oracle
+    ref0 = oracle.xattn_bwd(qc[:1, :1], pos[:1, :1], k[:1], v[:1], ac, bc, dOc[:1, :1], scale)
+    ref1 = oracle.xattn_bwd(qc[1:, 1:], pos[1:, 1:], k[1:], v[1:], ac, bc, dOc[1:, 1:], scale)
+    _assert_grad(dq[:1, :1], ref0[0], "dq of the valid copy, sequence 0")
+    _assert_grad(dq[1:, 1:], ref1[0], "dq of the valid copy, sequence 1")
+    for i, name in ((3, "dalpha"), (4, "dbeta")):
+        _assert_grad(got[i].cpu().numpy().astype(np.float64), ref0[i] + ref1[i], name)
