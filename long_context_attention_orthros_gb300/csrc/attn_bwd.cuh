@@ -1981,9 +1981,12 @@ struct BbCfg {
     static constexpr int QSLAB = ROWS * 128;
     static constexpr int SLOT = KB * 128;              // one slot of one 64-column slab
     static constexpr int RSLAB = NSLOT * SLOT;         // one 64-column slab of a ring
-    static constexpr int QBUF = 2 * SLABS * QSLAB;     // one query buffer: fp16 q, dO
+    static constexpr int QBUF = 2 * SLABS * QSLAB;     // the query buffer: fp16 q, dO
     static constexpr int Q16_OFF = 0;
     static constexpr int DO_OFF = SLABS * QSLAB;
+    static constexpr int DQS_OFF = QBUF;               // dq_raw staging: D / 32 tiles of ROWS x 128 B
+    static constexpr int DQS_TILE = ROWS * 128;
+    static_assert((D / 32) * DQS_TILE == QBUF, "the staging tiles fill the second buffer");
     static constexpr int K16_OFF = 2 * QBUF;           // ring of the fp16 K
     static constexpr int V_OFF = K16_OFF + SLABS * RSLAB;
     static constexpr int BAR_OFF = V_OFF + SLABS * RSLAB;
@@ -2020,7 +2023,7 @@ template <int D, int G, bool FOLD>
 __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
     attn_bwd_dq_band_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                             const __grid_constant__ CUtensorMap k16map, const __grid_constant__ CUtensorMap vmap,
-                            const AttnBwdParams p)
+                            const __grid_constant__ CUtensorMap dqmap, const AttnBwdParams p)
 {
     using C = BbCfg<D>;
     constexpr int UNITS = C::ROWS / G;
@@ -2028,8 +2031,8 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *q_full = bars;                     // [2] a tile's fp16 q and dO landed
-    uint64_t *q_free = bars + 2;                 // [2] a tile's S, dP done: the buffer may be reloaded
+    uint64_t *q_full = bars;                     // a tile's fp16 q and dO landed (one phase per tile)
+    uint64_t *q_free = bars + 2;                 // a tile's S, dP done: the buffer may be reloaded
     uint64_t *kv_full = bars + 4;                // [NSLOT] block landed
     uint64_t *kv_empty = kv_full + C::NSLOT;     // [NSLOT] block no longer read
     uint64_t *s_full = kv_empty + C::NSLOT;      // S, dP of a tile complete
@@ -2088,20 +2091,7 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
             int bh, u0, lo, hi;
             tile(tau, bh, u0, lo, hi);
             const int first = run.step(bh, lo, hi);
-            const int b = bh / p.Hkv, g = bh % p.Hkv, qb = static_cast<int>(i & 1);
-            // query buffer qb is free once tile i - 2's S, dP are done
-            if (i >= 2 && !(ok = warp_wait(&q_free[qb], static_cast<uint32_t>(((i - 2) >> 1) & 1))))
-                break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&q_full[qb], 2 * C::SLABS * C::QSLAB);
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + qb * C::QBUF + C::Q16_OFF + sl * C::QSLAB, &qmap, &q_full[qb], sl * 64, g * G,
-                                u0, b);
-                    tma_load_4d(smem + qb * C::QBUF + C::DO_OFF + sl * C::QSLAB, &omap, &q_full[qb], sl * 64, g * G,
-                                u0, b);
-                }
-            }
+            const int b = bh / p.Hkv, g = bh % p.Hkv;
             for (int kb = first; kb <= hi; ++kb, ++n) {
                 const int slot = static_cast<int>(n % C::NSLOT);
                 // the slot's previous block (load n - NSLOT) is released after the dQ of its last tile
@@ -2116,6 +2106,18 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
                         tma_load_4d(smem + C::K16_OFF + o, &k16map, &kv_full[slot], sl * 64, g, kb * C::KB, b);
                         tma_load_4d(smem + C::V_OFF + o, &vmap, &kv_full[slot], sl * 64, g, kb * C::KB, b);
                     }
+                }
+            }
+            // the single query buffer is free once tile i - 1's S, dP are done (the tile's new key
+            // block above loads first: its slot was freed long before)
+            if (!ok || (i >= 1 && !(ok = warp_wait(q_free, static_cast<uint32_t>((i - 1) & 1)))))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
+                    tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
                 }
             }
         }
@@ -2141,15 +2143,14 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
             have_next = tau + 1 < t_end;
             if (have_next)
                 tile(tau + 1, nbh, nu0, nlo, nhi);
-            const int qb = static_cast<int>(i & 1);
-            if (!(ok = warp_wait(&q_full[qb], static_cast<uint32_t>((i >> 1) & 1))))
+            if (!(ok = warp_wait(q_full, static_cast<uint32_t>(i & 1))))
                 break;
             for (int kb = first; ok && kb <= hi; ++kb, ++n)
                 ok = warp_wait(&kv_full[n % C::NSLOT], static_cast<uint32_t>((n / C::NSLOT) & 1));
             if (!ok)
                 break;
-            const uint64_t qdesc = umma_desc_sw128(sbase + qb * C::QBUF + C::Q16_OFF, 16, 1024);
-            const uint64_t odesc = umma_desc_sw128(sbase + qb * C::QBUF + C::DO_OFF, 16, 1024);
+            const uint64_t qdesc = umma_desc_sw128(sbase + C::Q16_OFF, 16, 1024);
+            const uint64_t odesc = umma_desc_sw128(sbase + C::DO_OFF, 16, 1024);
             if (lane == 0) {  // S over the whole ring (S was read by the dS of tile i - 1)
                 tc_fence_after();
 #pragma unroll
@@ -2172,7 +2173,7 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
                     umma_ss(tbase + C::TM_DP, odesc + qo, vdesc + ko, IDESC_DP, kk != 0);
                 }
                 umma_commit(s_full);
-                umma_commit(&q_free[qb]);
+                umma_commit(q_free);
             }
             __syncwarp();
             // dQ is free once the epilogue has read tile i - 1's; dS of this tile written
@@ -2391,54 +2392,63 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
             record_error(p.dev_err, ORTHROS_DEVERR_RANGE);
     } else {
         // ------------------------------------------------------------------ dq_raw stores (warps 12-15)
-        // dq_raw = scale dQ alpha, in 16-column pieces with the next piece's load in flight
+        // dq_raw = scale dQ alpha: 32 columns at a time from tensor memory (the next load in flight)
+        // into D / 32 staging tiles laid out as the dq map's 128-byte swizzled boxes, which one
+        // thread stores by TMA (rows past the stream are clipped).  The four warps meet at a
+        // barrier that also ANDs their wait results, so a timeout in one stops all four.
         const int rw = warp - 12;
         const int r = rw * 32 + lane;
         const uint32_t tl = tbase + (static_cast<uint32_t>(rw * 32) << 16);
+        const bool issuer = warp == 12 && lane == 0;
+        const float sc = p.scale;
         for (long long tau = t_begin, i = 0; ok && tau < t_end; ++tau, ++i) {
             int bh, u0, lo, hi;
             tile(tau, bh, u0, lo, hi);
             const int b = bh / p.Hkv, g = bh % p.Hkv;
-            const int uu = u0 + r / G, h = g * G + r % G;
-            const bool live = uu < p.n_units;
-            const long long off = ((static_cast<long long>(b) * p.n_units + uu) * p.Hq + h) * D;
-            if (!(ok = warp_wait(dq_final, static_cast<uint32_t>(i & 1))))
+            const int h = g * G + r % G;
+            if (issuer)
+                bulk_wait_read_all();  // the previous tile's stores have read the staging tiles
+            const bool got = warp_wait(dq_final, static_cast<uint32_t>(i & 1));
+            if (!(ok = bar_red_and(1, 128, got)))
                 break;
             tc_fence_after();
-            uint32_t wa[16];
-            tmem_ld16(tl + C::TM_DQ, wa);
-            const float sc = p.scale;
-#pragma unroll
-            for (int c = 0; c < D; c += 16) {
+            uint32_t wa[32];
+            tmem_ld32(tl + C::TM_DQ, wa);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
                 tmem_wait_ld();
-                uint32_t w[16];
+                uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+                for (int e = 0; e < 32; ++e)
                     w[e] = wa[e];
-                if (c + 16 < D)
-                    tmem_ld16(tl + C::TM_DQ + c + 16, wa);
-                if (live) {  // whole 32-byte sectors per store
+                if (c + 1 < D / 32) {
+                    tmem_ld32(tl + C::TM_DQ + 32 * (c + 1), wa);
+                } else {  // every column of dQ is read: the accumulator is free
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(dq_free);
+                }
+                uint8_t *tile_c = smem + C::DQS_OFF + c * C::DQS_TILE;
 #pragma unroll
-                    for (int e = 0; e < 16; e += 8) {
-                        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e));
-                        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + c + e + 4));
-                        st_global_v8(p.dq + off + c + e,
-                                     make_uint4(__float_as_uint(__uint_as_float(w[e]) * sc * a0.x),
-                                                __float_as_uint(__uint_as_float(w[e + 1]) * sc * a0.y),
-                                                __float_as_uint(__uint_as_float(w[e + 2]) * sc * a0.z),
-                                                __float_as_uint(__uint_as_float(w[e + 3]) * sc * a0.w)),
-                                     make_uint4(__float_as_uint(__uint_as_float(w[e + 4]) * sc * a1.x),
-                                                __float_as_uint(__uint_as_float(w[e + 5]) * sc * a1.y),
-                                                __float_as_uint(__uint_as_float(w[e + 6]) * sc * a1.z),
-                                                __float_as_uint(__uint_as_float(w[e + 7]) * sc * a1.w)));
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(p.alpha + h * D + 32 * c + 4 * j));
+                    *reinterpret_cast<float4 *>(tile_c + sw128_offset(r, j)) =
+                        make_float4(__uint_as_float(w[4 * j]) * sc * a.x, __uint_as_float(w[4 * j + 1]) * sc * a.y,
+                                    __uint_as_float(w[4 * j + 2]) * sc * a.z, __uint_as_float(w[4 * j + 3]) * sc * a.w);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(dq_free);  // this warp's lanes of dQ are stored
+            fence_proxy_async_smem();
+            named_barrier(1, 128);  // every store warp's rows are in the staging tiles
+            if (issuer) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    tma_store_4d(&dqmap, smem + C::DQS_OFF + c * C::DQS_TILE, 32 * c, g * G, u0, b);
+                bulk_commit();
+            }
         }
+        if (issuer)
+            bulk_wait_all();  // the last stores are complete before the kernel ends
     }
     if (!ok && lane == 0)
         record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
@@ -2617,7 +2627,7 @@ static cudaError_t launch_rows_t(const AttnBwdParams &p, const CUtensorMap *maps
                 constexpr int UNITS = BbCfg<D>::ROWS / G;
                 const long long tiles = static_cast<long long>(p.B) * p.Hkv * ((p.n_units + UNITS - 1) / UNITS);
                 k1<<<static_cast<unsigned>(tiles < sms ? tiles : sms), BbCfg<D>::THREADS, s1, stream>>>(
-                    maps[9], maps[5], maps[10], maps[11], p);
+                    maps[9], maps[5], maps[10], maps[11], maps[12], p);
                 if (!FOLD) {
                     if ((e = cudaGetLastError()) != cudaSuccess)
                         return e;

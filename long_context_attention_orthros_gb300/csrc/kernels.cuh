@@ -103,7 +103,7 @@ size_t attn_bwd_split_bytes(int B, int Hkv);
 // 64 x 1 x 128 keys (dK/dV); [4], [5] q raw and dO with boxes of 64 x G x 128/G, [6..8] K, V
 // and the fp16 K with boxes of 64 x 1 x 64 (dQ); [9] the fp16 q with boxes of 64 x G x 128/G;
 // [10], [11] the fp16 K and V with boxes of 64 x 1 x 32 (the base stream's band dQ)
-constexpr int ATTN_BWD_MAPS = 12;
+constexpr int ATTN_BWD_MAPS = 13;
 cudaError_t launch_attn_bwd(int D, int G, const AttnBwdParams &p, const CUtensorMap *maps, cudaStream_t stream);
 // a layer's gradient, both streams: p the base stream, pc the copies (pc.k16 = p.k16; maps and
 // mapsc as above for each stream, mapsc's fp16-K maps over p.k16); dK / dV written once

@@ -89,8 +89,28 @@ const float kLog2e = 1.4426950408889634f;
 // (64/G units x G heads), V and the fp16 K in blocks of 128 keys; for dQ, raw q and dO in
 // tiles of 128 rows, K, V and the fp16 K in blocks of 64 keys, the fp16 q in tiles of 128
 // rows (the base stream's persistent dQ), and the fp16 K and V in blocks of 32 keys (its band)
+// 4-D fp32 view {d, H, T, B} of a dense token-major tensor, 128-byte swizzled boxes of
+// {32, box_h, box_t, 1} (stores clip at the tensor's edges).
+bool make_map_f32(CUtensorMap *m, const void *base, int d, int H, long long T, int B, int box_h, int box_t)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4,
+                             static_cast<cuuint64_t>(T) * H * d * 4};
+    cuuint32_t box[4] = {32u, static_cast<cuuint32_t>(box_h), static_cast<cuuint32_t>(box_t), 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// m[12]: the fp32 dq_raw output of the stream (the band dq kernel stores it by TMA); a copy of
+// m[9] when dq is null (never used then)
 bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, const void *v, const void *k16,
-              const void *q16, int d, int Hq, int Hkv, int n_units, int T_kv, int B)
+              const void *q16, int d, int Hq, int Hkv, int n_units, int T_kv, int B, const void *dq)
 {
     const int G = Hq / Hkv;
     const long long qs = static_cast<long long>(n_units) * Hq * d, ks = static_cast<long long>(T_kv) * Hkv * d;
@@ -101,7 +121,9 @@ bool bwd_maps(CUtensorMap *m, const void *q, const void *dO, const void *k, cons
            make_map(&m[5], dO, d, Hq, n_units, B, qs, G, 128 / G) && make_map(&m[6], k, d, Hkv, T_kv, B, ks, 1, 64) &&
            make_map(&m[7], v, d, Hkv, T_kv, B, ks, 1, 64) && make_map(&m[8], k16, d, Hkv, T_kv, B, ks, 1, 64) &&
            make_map(&m[9], q16, d, Hq, n_units, B, qs, G, 128 / G) &&
-           make_map(&m[10], k16, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32);
+           make_map(&m[10], k16, d, Hkv, T_kv, B, ks, 1, 32) && make_map(&m[11], v, d, Hkv, T_kv, B, ks, 1, 32) &&
+           (dq != nullptr && n_units > 0 ? make_map_f32(&m[12], dq, d, Hq, n_units, B, G, 128 / G)
+                                         : (m[12] = m[9], true));
 }
 
 }  // namespace
@@ -540,7 +562,7 @@ orthros_status orthros_swa_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k,
     p.accumulate = 0;
     p.scale = scale;
     CUtensorMap maps[orthros::ATTN_BWD_MAPS];
-    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B))
+    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B, dq_raw))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
@@ -610,7 +632,7 @@ orthros_status orthros_xattn_bwd(const orthros_bf16 *qc_raw, const int32_t *pos,
     p.scale = scale;
     CUtensorMap maps[orthros::ATTN_BWD_MAPS];
     if (!bwd_maps(maps, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, T_out > 0 ? p.q16 : p.k16, d, Hq, Hkv,
-                  T_out > 0 ? T_out : 1, T_kv, B))
+                  T_out > 0 ? T_out : 1, T_kv, B, nullptr))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e = orthros::launch_attn_bwd(d, Hq / Hkv, p, maps, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
@@ -701,9 +723,9 @@ orthros_status orthros_attn_bwd(const orthros_bf16 *q_raw, const orthros_bf16 *k
     pc.n_units = T_out;
     pc.window = T;  // a copy at position P sees keys 0..P
     CUtensorMap maps[orthros::ATTN_BWD_MAPS], mapsc[orthros::ATTN_BWD_MAPS];
-    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B) ||
+    if (!bwd_maps(maps, q_raw, dO, k, v, p.k16, p.q16, d, Hq, Hkv, T, T, B, dq_raw) ||
         !bwd_maps(mapsc, T_out > 0 ? qc_raw : k, T_out > 0 ? dOc : k, k, v, p.k16, T_out > 0 ? pc.q16 : p.k16, d, Hq,
-                  Hkv, T_out > 0 ? T_out : 1, T, B))
+                  Hkv, T_out > 0 ? T_out : 1, T, B, nullptr))
         return ORTHROS_ERR_CUDA;
     const cudaError_t e =
         orthros::launch_attn_bwd_layer(d, Hq / Hkv, p, pc, maps, mapsc, static_cast<cudaStream_t>(stream));
