@@ -2092,6 +2092,18 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
             tile(tau, bh, u0, lo, hi);
             const int first = run.step(bh, lo, hi);
             const int b = bh / p.Hkv, g = bh % p.Hkv;
+            // the single query buffer is free once tile i - 1's S, dP are done, well before the
+            // slot of this tile's new key block (freed by tile i - 1's dQ): q goes first
+            if (i >= 1 && !(ok = warp_wait(q_free, static_cast<uint32_t>((i - 1) & 1))))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
+                    tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
+                }
+            }
             for (int kb = first; kb <= hi; ++kb, ++n) {
                 const int slot = static_cast<int>(n % C::NSLOT);
                 // the slot's previous block (load n - NSLOT) is released after the dQ of its last tile
@@ -2106,18 +2118,6 @@ __global__ void __launch_bounds__(BbCfg<D>::THREADS, 1)
                         tma_load_4d(smem + C::K16_OFF + o, &k16map, &kv_full[slot], sl * 64, g, kb * C::KB, b);
                         tma_load_4d(smem + C::V_OFF + o, &vmap, &kv_full[slot], sl * 64, g, kb * C::KB, b);
                     }
-                }
-            }
-            // the single query buffer is free once tile i - 1's S, dP are done (the tile's new key
-            // block above loads first: its slot was freed long before)
-            if (!ok || (i >= 1 && !(ok = warp_wait(q_free, static_cast<uint32_t>((i - 1) & 1)))))
-                break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, 2 * C::SLABS * C::QSLAB);
-#pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_4d(smem + C::Q16_OFF + sl * C::QSLAB, &qmap, q_full, sl * 64, g * G, u0, b);
-                    tma_load_4d(smem + C::DO_OFF + sl * C::QSLAB, &omap, q_full, sl * 64, g * G, u0, b);
                 }
             }
         }
