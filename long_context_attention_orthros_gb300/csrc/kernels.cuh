@@ -117,8 +117,9 @@ cudaError_t launch_swa_tc(int D, int G, const CUtensorMap &q, const CUtensorMap 
                           const CUtensorMap &o, const SwaParams &p, int num_sms, cudaStream_t stream);
 
 size_t xattn_workspace_bytes(int B, int T_out, int T_kv, int Hq, int Hkv, int D);
+// ctas > 0: at most 8 copy rows per (batch, KV head) run on exactly `ctas` CTAs of one SM each
 cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p, void *workspace,
-                         cudaStream_t stream);
+                         cudaStream_t stream, int ctas = 0);
 // merge split partials [n_part][B*Hkv][R][D] into the copy outputs
 cudaError_t launch_xattn_combine(int D, const XattnParams &p, cudaStream_t stream);
 // many copies per (batch, KV head) (T_out * G >= 256): tcgen05 flash kernel over key blocks of

@@ -274,7 +274,7 @@ orthros_status xattn_fwd_impl(const orthros_bf16 *qc_raw, const int32_t *pos, co
                               const orthros_bf16 *v, const float *alpha_c, const float *beta_c, orthros_bf16 *oc,
                               float *lse, int B, int T_out, int T_kv, int Hq, int Hkv, int d, float scale,
                               int64_t qc_bstride, int64_t kv_bstride, int64_t oc_bstride, void *workspace,
-                              size_t ws_bytes, int32_t *dev_err, void *stream)
+                              size_t ws_bytes, int32_t *dev_err, void *stream, int ctas = 0)
 {
     if (B < 1 || T_out < 0 || T_kv < 1 || !std::isfinite(scale))
         return ORTHROS_ERR_INVALID_ARG;
@@ -324,7 +324,7 @@ orthros_status xattn_fwd_impl(const orthros_bf16 *qc_raw, const int32_t *pos, co
     } else {
         if (!make_map(&mk, k, d, Hkv, T_kv, B, ks, 1, 64) || !make_map(&mv, v, d, Hkv, T_kv, B, ks, 1, 64))
             return ORTHROS_ERR_CUDA;
-        e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream));
+        e = orthros::launch_xattn(d, mk, mv, p, workspace, static_cast<cudaStream_t>(stream), ctas);
     }
     return e == cudaSuccess ? ORTHROS_OK : ORTHROS_ERR_CUDA;
 }
@@ -410,12 +410,15 @@ orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16
         return ORTHROS_ERR_INVALID_ARG;
     if (T_out > 0 && (!workspace || ws_bytes < orthros_prefill_workspace_size(B, T, T_out, Hq, Hkv, d)))
         return ORTHROS_ERR_WORKSPACE;
-    // Few copies (the split-KV pass, bound by HBM) run on a second stream while the SWA kernel,
-    // bound by its MMA issue and holding fewer SMs, runs on the caller's; the caller's stream
-    // waits for both.  Many copies (the tensor-memory kernel) run after the SWA kernel.
+    // At most 8 copy rows per KV head (the split-KV pass with the rows on the MMA's N side, bound
+    // by HBM) run on a second stream while the SWA kernel, bound by its MMA issue and holding
+    // fewer SMs, runs on the caller's; the caller's stream waits for both.  The copies' kernel
+    // then has exactly as many CTAs as SMs left to it, each too large to share an SM, so it
+    // cannot take SWA's SMs whichever grid is dispatched first.  Otherwise the two run one
+    // after the other on the caller's stream.
     const int sms = num_sms();
     const bool overlap = T_out > 0 && (d == 64 || d == 128) && heads_ok(Hq, Hkv) &&
-                         !orthros::xattn_tc_supported(d, Hq / Hkv, T_out) && sms > 0;
+                         static_cast<long long>(T_out) * (Hq / Hkv) <= 8 && sms > 0;
     const int reserve = overlap ? copy_sm_reserve(sms, B, T, Hq, Hkv, d) : 0;
     cudaStream_t cs = reserve > 0 ? copy_stream() : nullptr;
     if (cs == nullptr) {
@@ -440,8 +443,8 @@ orthros_status orthros_prefill_fwd(const orthros_bf16 *q_raw, const orthros_bf16
         st = swa_fwd_impl(q_raw, k, v, alpha, beta, o, nullptr, B, T, Hq, Hkv, d, window, scale, q_bstride,
                           kv_bstride, o_bstride, 0, T < 1 ? 0 : T, dev_err, stream, reserve);
         if (st == ORTHROS_OK)
-            st = orthros_xattn_fwd(qc_raw, pos, k, v, alpha_c, beta_c, oc, B, T_out, T, Hq, Hkv, d, scale,
-                                   qc_bstride, kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, cs);
+            st = xattn_fwd_impl(qc_raw, pos, k, v, alpha_c, beta_c, oc, nullptr, B, T_out, T, Hq, Hkv, d, scale,
+                                qc_bstride, kv_bstride, oc_bstride, workspace, ws_bytes, dev_err, cs, reserve);
         // the caller's stream waits for whatever the copy stream was given
         if ((cudaEventRecord(join, cs) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess) &&
             st == ORTHROS_OK)

@@ -398,6 +398,219 @@ __global__ void __launch_bounds__(XCfg<D>::THREADS)
     }
 }
 
+// The same work as xattn_partial_keys_kernel on a fixed number of CTAs that walk the (split,
+// batch * KV head) items, for a copies' pass that runs beside the persistent SWA kernel on the
+// SMs it leaves: a CTA takes more than half of an SM's shared memory, so however the two grids
+// are dispatched the pass holds at most gridDim.x SMs.  Each CTA runs two independent lanes of
+// one producer warp and four consumer warps, each lane with its own ring and its own scratch
+// for the warps' merge (so the next item's blocks load while an item is merged).
+template <int D>
+struct XpCfg {
+    using X = XCfg<D>;
+    static constexpr int RMAX = 8;
+    static constexpr int LANE_THREADS = X::THREADS;                     // 4 consumer warps + producer
+    static constexpr int THREADS = 2 * LANE_THREADS;
+    static constexpr int SCR_OFF = X::STAGES * X::STAGE_BYTES;         // [CWARPS][RMAX] max, sum; [CWARPS][RMAX][D] o
+    static constexpr int SCR_BYTES = X::CWARPS * RMAX * (2 + D) * 4;
+    static constexpr int BAR_OFF = SCR_OFF + SCR_BYTES;
+    static constexpr int LANE_BYTES = (BAR_OFF + 2 * X::STAGES * 8 + 1023) / 1024 * 1024;
+    static constexpr int SMEM_USED = 2 * LANE_BYTES + 1024;
+    static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(XpCfg<D>::THREADS, 1)
+    xattn_partial_keys_persist_kernel(const __grid_constant__ CUtensorMap kmap,
+                                      const __grid_constant__ CUtensorMap vmap, const XattnParams p)
+{
+    using C = XCfg<D>;
+    using P = XpCfg<D>;
+    constexpr int RMAX = P::RMAX;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
+    const int L = threadIdx.x / P::LANE_THREADS, lt = threadIdx.x % P::LANE_THREADS;
+    const int lw = lt >> 5, lane = lt & 31;
+    uint8_t *smem = smem_raw + pad + L * P::LANE_BYTES;
+    const uint32_t sbase = raw_s + pad + L * P::LANE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    if (lt == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int BH = p.B * p.Hkv;
+    const long long n_items = static_cast<long long>(p.splits) * BH;
+    const long long w_step = 2LL * gridDim.x;
+    // an item's key blocks: keys split * chunk .. up to the largest valid position of its rows
+    auto item_keys = [&](long long w, int &split, int &b, int &g, int &kmax, int &js, int &nblk) {
+        split = static_cast<int>(w % p.splits);
+        const int bh = static_cast<int>(w / p.splits);
+        b = bh / p.Hkv;
+        g = bh % p.Hkv;
+        kmax = -1;
+        for (int r = 0; r < p.R; ++r) {
+            const int ps = __ldg(p.pos + static_cast<long long>(b) * p.T_out + r / p.G);
+            if (ps >= 0 && ps < p.T_kv)
+                kmax = max(kmax, ps);
+        }
+        js = split * p.chunk;
+        const int je = min(js + p.chunk, kmax + 1);
+        nblk = je > js ? (je - js + C::KB - 1) / C::KB : 0;
+    };
+
+    if (lw == C::CWARPS) {
+        // ------------------------------------------------------------------ producer of lane L
+        if (lane != 0)
+            return;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        long long i = 0;  // blocks loaded by this lane over all its items
+        for (long long w = 2LL * blockIdx.x + L; w < n_items; w += w_step) {
+            int split, b, g, kmax, js, nblk;
+            item_keys(w, split, b, g, kmax, js, nblk);
+            for (int j = 0; j < nblk; ++j, ++i) {
+                const int s = static_cast<int>(i % C::STAGES);
+                if (i >= C::STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / C::STAGES) - 1) & 1))) {
+                    record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+                    return;
+                }
+                uint8_t *dst = smem + s * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+#pragma unroll
+                for (int sl = 0; sl < D / 64; ++sl) {
+                    tma_load_4d(dst + sl * C::SLAB, &kmap, &full[s], sl * 64, g, js + j * C::KB, b);
+                    tma_load_4d(dst + C::KV_BYTES + sl * C::SLAB, &vmap, &full[s], sl * 64, g, js + j * C::KB, b);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers of lane L
+    // every consumer warp passes the same named barriers for every item, whatever happens to
+    // its waits (a timed-out wait only stops its work), so none is left waiting at a barrier
+    constexpr int CT = C::CWARPS * 32;
+    const int bar_id = 3 + L;
+    float *ms = reinterpret_cast<float *>(smem + P::SCR_OFF);  // [CWARPS][RMAX] max
+    float *ls = ms + C::CWARPS * RMAX;                           // [CWARPS][RMAX] sum
+    float *os = ls + C::CWARPS * RMAX;                           // [CWARPS][RMAX][D] output
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    bool ok = true;
+    long long i = 0;
+    for (long long w = 2LL * blockIdx.x + L; w < n_items; w += w_step) {
+        int split, b, g, kmax, js, nblk;
+        item_keys(w, split, b, g, kmax, js, nblk);
+        const int bh = b * p.Hkv + g;
+        // row r's last key (-1: a bad position, every key masked); padding rows borrow kmax
+        auto lim_of = [&](int r) {
+            if (r >= p.R)
+                return kmax;
+            const int ps = __ldg(p.pos + static_cast<long long>(b) * p.T_out + r / p.G);
+            return (ps >= 0 && ps < p.T_kv) ? ps : -1;
+        };
+        WarpKeys16<D, 1, false> st;
+#pragma unroll
+        for (int kt = 0; kt < D / 16; ++kt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int row = lane >> 2;
+                const int dcol = kt * 16 + 2 * (lane & 3) + 8 * hf;
+                uint32_t hi = 0, lo = 0;
+                if (row < p.R && lim_of(row) >= 0) {
+                    const int h = g * p.G + row % p.G;
+                    const orthros_bf16 *qrow =
+                        p.qc + b * p.qc_bstride + (static_cast<long long>(row / p.G) * p.Hq + h) * D;
+                    load_q_pair(qrow, p.alpha_c + h * D, p.beta_c + h * D, dcol, p.qscale, hi, lo);
+                }
+                st.qb[0][kt][hf] = hi;
+                st.ql[0][kt][hf] = lo;
+            }
+        st.reset();
+        int lim[1][2];
+        lim[0][0] = lim_of(2 * (lane & 3));
+        lim[0][1] = lim_of(2 * (lane & 3) + 1);
+        int pmin = 0x7fffffff, pmax = -1;
+        for (int r = 0; r < RMAX; ++r) {
+            pmin = min(pmin, lim_of(r));
+            pmax = max(pmax, lim_of(r));
+        }
+        for (int j = 0; j < nblk; ++j, ++i) {
+            const int s = static_cast<int>(i % C::STAGES);
+            if (ok && !mbar_wait(&full[s], static_cast<uint32_t>((i / C::STAGES) & 1)))
+                ok = false;
+            const uint32_t kbase = sbase + s * C::STAGE_BYTES;
+            const int j0 = js + j * C::KB + lw * 16;
+            if (ok && j0 <= pmax)
+                st.step(kbase, C::SLAB, kbase + C::KV_BYTES, C::SLAB, lw * 16, j0, lim, j0 + 15 <= pmin);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[s]);
+        }
+        st.finish_sums();
+        named_barrier(bar_id, CT);  // the previous item's merge has been read: the scratch is free
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2)
+            if ((lane >> 2) == 0) {
+                ms[lw * RMAX + 2 * lane + r2] = st.m[0][r2];
+                ls[lw * RMAX + 2 * lane + r2] = st.l[0][r2];
+            }
+        named_barrier(bar_id, CT);
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+            const int row = 2 * (lane & 3) + r2;
+            float M = NEG_INF;
+#pragma unroll
+            for (int q = 0; q < C::CWARPS; ++q)
+                M = fmaxf(M, ms[q * RMAX + row]);
+            const float f = (M == NEG_INF || st.m[0][r2] == NEG_INF) ? 0.f : fast_exp2(st.m[0][r2] - M);
+            float *po = os + (lw * RMAX + row) * D + (lane >> 2);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                po[16 * mt] = st.o[0][mt][r2] * f;
+                po[16 * mt + 8] = st.o[0][mt][2 + r2] * f;
+            }
+        }
+        named_barrier(bar_id, CT);
+        for (int x = lt; x < p.R * (D / 2); x += CT) {  // two columns per thread and step
+            const int row = x / (D / 2), c = 2 * (x % (D / 2));
+            float M = NEG_INF, Ls = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < C::CWARPS; ++q)
+                M = fmaxf(M, ms[q * RMAX + row]);
+#pragma unroll
+            for (int q = 0; q < C::CWARPS; ++q) {
+                if (ms[q * RMAX + row] != NEG_INF)
+                    Ls += ls[q * RMAX + row] * fast_exp2(ms[q * RMAX + row] - M);
+                a0 += os[(q * RMAX + row) * D + c];
+                a1 += os[(q * RMAX + row) * D + c + 1];
+            }
+            const int h = g * p.G + row % p.G, copy = row / p.G;
+            if (p.direct) {
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                *reinterpret_cast<uint32_t *>(p.oc + b * p.oc_bstride + (static_cast<long long>(copy) * p.Hq + h) * D +
+                                              c) = pack_bf16x2(a0 * inv, a1 * inv);
+                if (c == 0 && p.lse != nullptr)
+                    p.lse[(static_cast<long long>(b) * p.T_out + copy) * p.Hq + h] =
+                        Ls > 0.f ? (M + __log2f(Ls)) * kLn2F : NEG_INF;
+            } else {
+                const long long slot = (static_cast<long long>(split) * BH + bh) * p.R + row;
+                *reinterpret_cast<float2 *>(p.part_o + slot * D + c) = make_float2(a0, a1);
+                if (c == 0)
+                    p.part_ml[slot] = make_float2(M, Ls);
+            }
+        }
+    }
+    if (!ok && lt == 0)
+        record_error(p.dev_err, ORTHROS_DEVERR_TIMEOUT);
+}
+
 // One warp per output row: merge the row's partial (max, sum, o) triples.
 template <int D>
 __global__ void __launch_bounds__(128) xattn_combine_kernel(const XattnParams p)
@@ -556,6 +769,18 @@ static cudaError_t launch_partial(const CUtensorMap &k, const CUtensorMap &v, co
 }
 
 template <int D>
+static cudaError_t launch_partial_keys_persist(const CUtensorMap &k, const CUtensorMap &v, const XattnParams &p,
+                                               int ctas, cudaStream_t stream)
+{
+    auto kern = xattn_partial_keys_persist_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, XpCfg<D>::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<static_cast<unsigned>(ctas), XpCfg<D>::THREADS, XpCfg<D>::SMEM, stream>>>(k, v, p);
+    return cudaGetLastError();
+}
+
+template <int D>
 static cudaError_t launch_partial_keys(const CUtensorMap &k, const CUtensorMap &v, const XattnParams &p,
                                        cudaStream_t stream)
 {
@@ -569,7 +794,7 @@ static cudaError_t launch_partial_keys(const CUtensorMap &k, const CUtensorMap &
 }
 
 cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, XattnParams p,
-                         void *workspace, cudaStream_t stream)
+                         void *workspace, cudaStream_t stream, int ctas)
 {
     const XattnPlan pl = xattn_plan(p.B, p.T_out, p.T_kv, p.Hq, p.Hkv);
     p.G = p.Hq / p.Hkv;
@@ -586,7 +811,10 @@ cudaError_t launch_xattn(int D, const CUtensorMap &k, const CUtensorMap &v, Xatt
         p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
     }
     cudaError_t e;
-    if (pl.keys)
+    if (pl.keys && ctas > 0)  // on at most `ctas` SMs, beside the SWA kernel
+        e = D == 128 ? launch_partial_keys_persist<128>(k, v, p, ctas, stream)
+                     : launch_partial_keys_persist<64>(k, v, p, ctas, stream);
+    else if (pl.keys)
         e = D == 128 ? launch_partial_keys<128>(k, v, p, stream) : launch_partial_keys<64>(k, v, p, stream);
     else if (D == 128)
         e = pl.WK == 4 ? launch_partial<128, 4>(k, v, p, stream) : launch_partial<128, 1>(k, v, p, stream);
