@@ -152,6 +152,12 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
     uint64_t *empty = full + C::STAGES;
     int *s_flag = reinterpret_cast<int *>(smem + C::BAR_OFF + 2 * C::STAGES * 8);
 
+    // Launched as a programmatic dependent of the previous kernel on the stream (the previous
+    // step, say): the next step's grid may be launched as soon as every CTA of this one has
+    // started, and this grid touches nothing the previous one wrote (cache_len, the cache, the
+    // partials' workspace) before that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int x = blockIdx.x, bh = blockIdx.y;
     const int b = bh / p.Hkv, g = bh % p.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -479,9 +485,20 @@ static cudaError_t launch_decode_t(const CUtensorMap &k, const CUtensorMap &v, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
     if (e != cudaSuccess)
         return e;
-    dim3 grid(p.nsplit + 1, p.B * p.Hkv);
-    kern<<<grid, DCfg<D>::THREADS, DCfg<D>::SMEM, stream>>>(k, v, p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the grid is set up while the previous kernel on the stream
+    // finishes (its CTAs wait for it before their first access; see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nsplit + 1, p.B * p.Hkv);
+    cfg.blockDim = dim3(DCfg<D>::THREADS);
+    cfg.dynamicSmemBytes = DCfg<D>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, k, v, p);
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_decode(int D, const CUtensorMap &k, const CUtensorMap &v, DecodeParams p,
