@@ -194,13 +194,14 @@ size_t orthros_prefill_workspace_size(int B, int T, int T_out, int Hq, int Hkv, 
  * Eq. (4) for the base stream and Eq. (5) for T_out output copies over the base
  * K/V up to their original positions (Sec. 3.2, prefill mode), with the results
  * and error behaviour of orthros_swa_fwd and orthros_xattn_fwd with T_kv = T
- * (bit for bit).  For few copies (the split-KV path of orthros_xattn_fwd) the
- * copies' kernels run on a second stream of the library's own, forked from and
- * joined back into `stream` with events, while the SWA kernel, which is bound by
- * its MMA issue, holds fewer SMs: the copies' pass, bound by HBM, takes the rest
- * and the spare bandwidth (three kernel launches; the copies' kernel reads K/V a
- * second time).  Work queued on `stream` after the call runs after both.  For
- * many copies the two run one after the other on `stream`.  Capturable in a CUDA
+ * (bit for bit).  For at most 8 copy rows per KV head (T_out * Hq / Hkv <= 8,
+ * e.g. one copy per sequence) the copies' kernels run on a second stream of the
+ * library's own, forked from and joined back into `stream` with events, while
+ * the SWA kernel, which is bound by its MMA issue, holds fewer SMs: the copies'
+ * pass, bound by HBM, runs on exactly the SMs left to it (one CTA per SM) and
+ * uses the spare bandwidth (three kernel launches; the copies' kernel reads K/V
+ * a second time).  Work queued on `stream` after the call runs after both.  For
+ * more copies the two run one after the other on `stream`.  Capturable in a CUDA
  * graph.  A variant that attended the copies inside the SWA pass, reading K/V
  * once, measured no faster on GB300: the extra work in the SWA kernel cost as
  * much time as the second read saves.
