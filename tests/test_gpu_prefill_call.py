@@ -68,6 +68,8 @@ def _positions(cfg, seed):
     (2, 4097, 8, 4, 128, 4),    # G=2, 8 copy rows, T off the tile grid
     (1, 300, 16, 2, 64, 1),     # d=64, G=8
     (4, 9000, 32, 8, 128, 2),   # 8 copy rows of 8B-class heads, streams over many CTAs
+    (2, 3000, 8, 8, 128, 3),    # G=1: the copies' pass beside SWA on more SMs (its share of bytes is larger)
+    (1, 6000, 8, 4, 64, 4),     # G=2, d=64, 8 copy rows
 ])
 def test_prefill_call_parity(B, T, Hq, Hkv, d, T_out):
     cfg = PrefillConfig("call", B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, T_out=T_out)
