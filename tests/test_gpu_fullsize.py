@@ -1,5 +1,5 @@
 """GPU parity at the workloads' full sizes, in the launch configuration bench.py
-times, against the fp64 oracle:
+times (one orthros_prefill_fwd call per prefill), against the fp64 oracle:
 
 * the 8B-class 128K prefill (B=2): every base output row and both copies;
 * the 1M-token prefill with scaled key rows: 16384 seeded random base rows, the
@@ -24,17 +24,24 @@ CHUNK_ROWS = 8192  # oracle rows per call when every row is compared
 
 
 def _run_prefill(cfg, inp):
+    """One orthros_prefill_fwd call, as bench.py times it (for few copies the copies' pass runs
+    beside the SWA kernel on a second stream); its outputs must also have orthros_swa_fwd's and
+    orthros_xattn_fwd's bits."""
     err = torch.zeros(1, dtype=torch.int32, device=dev())
     q_all = bf(inp.q_raw)
     k, v = bf(inp.k), bf(inp.v)
-    o = orth.swa_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), window=cfg.window, scale=cfg.scale,
-                     dev_err=err)
     qc = q_all[:, cfg.T:] if cfg.appended else bf(inp.qc_raw)
-    oc = orth.xattn_fwd(qc, i32(inp.pos), k, v, f32(inp.alpha_c), f32(inp.beta_c), scale=cfg.scale,
-                        dev_err=err)
+    o, oc = orth.prefill_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), qc, i32(inp.pos), f32(inp.alpha_c),
+                             f32(inp.beta_c), window=cfg.window, scale=cfg.scale, dev_err=err)
+    o_swa = orth.swa_fwd(q_all, k, v, f32(inp.alpha), f32(inp.beta), window=cfg.window, scale=cfg.scale,
+                         dev_err=err)
+    oc_x = orth.xattn_fwd(qc, i32(inp.pos), k, v, f32(inp.alpha_c), f32(inp.beta_c), scale=cfg.scale,
+                          dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    del q_all, k, v, qc
+    assert torch.equal(o.view(torch.int16), o_swa.view(torch.int16)), "prefill_fwd base output"
+    assert torch.equal(oc.view(torch.int16), oc_x.view(torch.int16)), "prefill_fwd copy output"
+    del q_all, k, v, qc, o_swa, oc_x
     return o, oc
 
 

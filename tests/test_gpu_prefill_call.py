@@ -57,6 +57,7 @@ def _positions(cfg, seed):
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,d,T_out", [
     (2, 1000, 32, 8, 128, 1),   # 8B-class heads, one copy (the prefill workload's shape)
+    (1, 20000, 32, 8, 128, 1),  # one sequence (the 1M workload's layout), copies beside SWA
     (2, 1000, 32, 8, 128, 4),   # 16 copy rows per KV head
     (1, 777, 8, 4, 64, 3),      # G=2, d=64
     (1, 257, 16, 2, 128, 2),    # G=8
